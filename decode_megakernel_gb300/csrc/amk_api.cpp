@@ -1,0 +1,603 @@
+// Host side of the C ABI declared in include/amk.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/amk.h"
+#include "device_model.hpp"
+#include "schedule.hpp"
+
+using namespace amk;
+
+struct amk_ctx {
+  amk_config cfg{};
+  ModelGeom geom;
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  void* kv = nullptr;
+  DevModel dm{};
+  const void* kernel = nullptr;
+  int smem = 0;
+  uint32_t epoch = 0;
+  int32_t kv_len = 0;
+  float* logits_stage = nullptr;
+  uint64_t timeout_ns = 0;
+  amk_status poisoned = AMK_OK;
+  std::string err;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+amk_status fail(amk_ctx* ctx, amk_status st, const std::string& msg) {
+  if (ctx) ctx->err = msg;
+  g_last_error = msg;
+  return st;
+}
+
+amk_status cuda_fail(amk_ctx* ctx, cudaError_t e, const char* what) {
+  return fail(ctx, AMK_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define AMK_CUDA(ctx, call)                                      \
+  do {                                                           \
+    cudaError_t e_ = (call);                                     \
+    if (e_ != cudaSuccess) return cuda_fail((ctx), e_, #call);   \
+  } while (0)
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Workspace layout: every region 256-byte aligned.
+struct Layout {
+  size_t w[M_NUM] = {};
+  size_t scales[M_NUM] = {};
+  size_t mats = 0, embed = 0, attn_norm = 0, ffn_norm = 0, final_norm = 0, rope = 0;
+  size_t x = 0, q = 0, o = 0, a = 0, part = 0, logits = 0, counters = 0, status = 0;
+  size_t tasks = 0, queue_off = 0, queue_body = 0, total = 0;
+};
+
+Layout make_layout(const ModelGeom& g, const Schedule& s) {
+  const amk_config& c = g.cfg;
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  for (int k = 0; k < M_NUM; ++k) {
+    const int layers = k == M_LM ? 1 : c.n_layers;
+    L.w[k] = take((size_t)g.mat[k].bytes * layers);
+  }
+  for (int k = 0; k < M_NUM; ++k) {
+    const int layers = k == M_LM ? 1 : c.n_layers;
+    L.scales[k] = g.mat[k].fmt == AMK_FORMAT_INT8 ? take((size_t)g.mat[k].rows_padded * 2 * layers) : 0;
+  }
+  L.mats = take(sizeof(DevMat) * M_NUM);
+  L.embed = take((size_t)c.vocab * c.hidden * 2);
+  L.attn_norm = take((size_t)c.n_layers * c.hidden * 2);
+  L.ffn_norm = take((size_t)c.n_layers * c.hidden * 2);
+  L.final_norm = take((size_t)c.hidden * 2);
+  L.rope = take((size_t)c.max_seq * (c.head_dim / 2) * sizeof(float) * 2);
+  const size_t qd = (size_t)c.n_heads * c.head_dim;
+  L.x = take((size_t)c.hidden * 4);
+  L.q = take(qd * 4);
+  L.o = take(qd * 4);
+  L.a = take((size_t)c.ffn * 4);
+  L.part = take((size_t)c.n_kv_heads * g.splits * g.part_stride * 4);
+  L.logits = take((size_t)c.vocab * 4);
+  L.counters = take(s.counters.size() * 4);
+  L.status = take(64);
+  size_t n_queued = 0;
+  for (const auto& q : s.queues) n_queued += q.size();
+  L.tasks = take(n_queued * sizeof(DevTask));
+  L.queue_off = take((s.queues.size() + 1) * 4);
+  L.queue_body = take(s.queues.size() * 4);
+  L.total = off;
+  return L;
+}
+
+amk_status resolve_ctas(const amk_schedule_config* sched, BuildOptions* opt, std::string* why) {
+  *opt = BuildOptions{};
+  if (sched) {
+    opt->num_ctas = sched->num_ctas;
+    opt->attn_splits = sched->attn_splits;
+    opt->max_rows_per_task = sched->max_rows_per_task;
+    if (sched->num_ctas < 0 || sched->attn_splits < 0 || sched->max_rows_per_task < 0 ||
+        sched->watchdog_ms < 0) {
+      *why = "negative schedule knob";
+      return AMK_ERR_INVALID_ARG;
+    }
+  }
+  if (opt->num_ctas == 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      *why = std::string("no CUDA device to size the schedule: ") + cudaGetErrorString(e);
+      return AMK_ERR_CUDA;
+    }
+    opt->num_ctas = sms;
+  }
+  return AMK_OK;
+}
+
+int lm_format(const amk_config& c) { return c.tied_embeddings ? AMK_FORMAT_BF16 : c.lm_head_format; }
+
+amk_status plan(const amk_config* cfg, const amk_schedule_config* sched, ModelGeom* g,
+                Schedule* s, std::string* why) {
+  if (!cfg) {
+    *why = "config is NULL";
+    return AMK_ERR_INVALID_ARG;
+  }
+  BuildOptions opt;
+  amk_status st = resolve_ctas(sched, &opt, why);
+  if (st != AMK_OK) return st;
+  st = plan_geometry(*cfg, opt, g, why);
+  if (st != AMK_OK) return st;
+  if (!decode_kernel_for(cfg->weight_format, lm_format(*cfg))) {
+    *why = "no kernel for this weight / LM-head format pair";
+    return AMK_ERR_UNSUPPORTED;
+  }
+  if (s) *s = build_schedule(*g);
+  return AMK_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// present and aligned for the kernel's vector loads (bf16 rows are read 16
+// bytes, int8 rows 8 bytes, int4 rows 4 bytes, fp16 scales 2 bytes at a time)
+bool linear_ok(const amk_linear& l, int fmt) {
+  if (!l.w) return false;
+  if (fmt == AMK_FORMAT_BF16) return aligned(l.w, 16);
+  if (fmt == AMK_FORMAT_INT8) return aligned(l.w, 8) && l.scales && aligned(l.scales, 2);
+  return aligned(l.w, 4) && l.scales && aligned(l.scales, 2) && l.zeros;
+}
+
+amk_status launch_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits, int skip_lm) {
+  StepParams p;
+  p.m = ctx->dm;
+  p.logits = logits;
+  p.token = token;
+  p.pos = pos;
+  p.epoch = ++ctx->epoch;
+  p.skip_lm = skip_lm;
+  p.timeout_ns = ctx->timeout_ns;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchCooperativeKernel(ctx->kernel, dim3(ctx->geom.num_ctas),
+                                              dim3(kThreads), args, (size_t)ctx->smem, ctx->stream);
+  if (e != cudaSuccess) {
+    ctx->poisoned = AMK_ERR_CUDA;
+    return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel");
+  }
+  return AMK_OK;
+}
+
+amk_status step_checks(amk_ctx* ctx, int32_t token, int32_t pos) {
+  if (!ctx) return fail(nullptr, AMK_ERR_INVALID_ARG, "context is NULL");
+  if (ctx->poisoned != AMK_OK) return fail(ctx, ctx->poisoned, "context is poisoned: " + ctx->err);
+  if (token < 0 || token >= ctx->cfg.vocab) return fail(ctx, AMK_ERR_INVALID_ARG, "token out of range");
+  if (pos < 0 || pos >= ctx->cfg.max_seq) return fail(ctx, AMK_ERR_INVALID_ARG, "pos out of range");
+  if (pos > ctx->kv_len)
+    return fail(ctx, AMK_ERR_INVALID_ARG, "pos is beyond the valid KV length (positions must be sequential)");
+  return AMK_OK;
+}
+
+amk_status read_status(amk_ctx* ctx) {
+  uint32_t st[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaMemcpyAsync(st, ctx->dm.status, sizeof st, cudaMemcpyDeviceToHost, ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) {
+    ctx->poisoned = AMK_ERR_CUDA;
+    return cuda_fail(ctx, e, "reading the device status");
+  }
+  if (st[0] == ST_OK) return AMK_OK;
+  char buf[160];
+  snprintf(buf, sizeof buf, "device %s at CTA %u, task %u, site %u",
+           st[0] == ST_TIMEOUT ? "watchdog timeout" : "check failure", st[1], st[2], st[3]);
+  ctx->poisoned = st[0] == ST_TIMEOUT ? AMK_ERR_TIMEOUT : AMK_ERR_DEVICE_CHECK;
+  return fail(ctx, ctx->poisoned, buf);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* amk_status_string(amk_status s) {
+  switch (s) {
+    case AMK_OK: return "ok";
+    case AMK_ERR_INVALID_ARG: return "invalid argument";
+    case AMK_ERR_UNSUPPORTED: return "unsupported model variant";
+    case AMK_ERR_SCHEDULE_INVALID: return "schedule rejected by the validator";
+    case AMK_ERR_CUDA: return "CUDA error";
+    case AMK_ERR_OOM: return "workspace too small";
+    case AMK_ERR_TIMEOUT: return "device watchdog timeout";
+    case AMK_ERR_DEVICE_CHECK: return "device check failed";
+  }
+  return "unknown status";
+}
+
+const char* amk_last_error(const amk_ctx* ctx) {
+  return ctx ? ctx->err.c_str() : g_last_error.c_str();
+}
+
+amk_status amk_check_config(const amk_config* cfg) {
+  if (!cfg) return fail(nullptr, AMK_ERR_INVALID_ARG, "config is NULL");
+  ModelGeom g;
+  BuildOptions opt;
+  opt.num_ctas = 1;
+  std::string why;
+  amk_status st = plan_geometry(*cfg, opt, &g, &why);
+  if (st != AMK_OK) return fail(nullptr, st, why);
+  if (!decode_kernel_for(cfg->weight_format, lm_format(*cfg)))
+    return fail(nullptr, AMK_ERR_UNSUPPORTED, "no kernel for this weight / LM-head format pair");
+  return AMK_OK;
+}
+
+size_t amk_kv_cache_bytes(const amk_config* cfg) {
+  if (!cfg || cfg->n_layers <= 0 || cfg->n_kv_heads <= 0 || cfg->max_seq <= 0 || cfg->head_dim <= 0)
+    return 0;
+  return (size_t)cfg->n_layers * 2 * cfg->n_kv_heads * cfg->max_seq * cfg->head_dim * 2;
+}
+
+size_t amk_workspace_bytes(const amk_config* cfg, const amk_schedule_config* sched) {
+  ModelGeom g;
+  Schedule s;
+  std::string why;
+  if (plan(cfg, sched, &g, &s, &why) != AMK_OK) {
+    g_last_error = why;
+    return 0;
+  }
+  return make_layout(g, s).total;
+}
+
+amk_status amk_build_schedule(const amk_config* cfg, const amk_schedule_config* sched, void* buf,
+                              size_t cap, size_t* needed) {
+  ModelGeom g;
+  Schedule s;
+  std::string why;
+  amk_status st = plan(cfg, sched, &g, &s, &why);
+  if (st != AMK_OK) return fail(nullptr, st, why);
+  std::vector<int64_t> words = serialize(s);
+  const size_t bytes = words.size() * sizeof(int64_t);
+  if (needed) *needed = bytes;
+  if (!buf) return AMK_OK;
+  if (cap < bytes) return fail(nullptr, AMK_ERR_INVALID_ARG, "buffer too small for the schedule");
+  std::memcpy(buf, words.data(), bytes);
+  return AMK_OK;
+}
+
+amk_status amk_validate_serialized(const void* buf, size_t bytes, char* report, size_t cap) {
+  auto put = [&](const std::string& m) {
+    if (report && cap) {
+      size_t n = m.size() < cap - 1 ? m.size() : cap - 1;
+      std::memcpy(report, m.data(), n);
+      report[n] = 0;
+    }
+  };
+  if (!buf || bytes % sizeof(int64_t)) {
+    put("buffer is NULL or not whole int64 words");
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "bad serialised schedule buffer");
+  }
+  Schedule s;
+  std::string why;
+  if (!deserialize(static_cast<const int64_t*>(buf), bytes / sizeof(int64_t), &s, &why)) {
+    put("malformed: " + why);
+    return fail(nullptr, AMK_ERR_SCHEDULE_INVALID, why);
+  }
+  Report r = validate(s);
+  put(r.msg);
+  if (!r.ok) return fail(nullptr, AMK_ERR_SCHEDULE_INVALID, r.msg);
+  return AMK_OK;
+}
+
+amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, void* workspace_dev,
+                            size_t workspace_bytes, void* kv_cache_dev, void* stream,
+                            const amk_schedule_config* sched, amk_ctx** out) {
+  if (!out) return fail(nullptr, AMK_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg || !weights || !workspace_dev || !kv_cache_dev)
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "NULL config, weights, workspace or KV cache");
+  if (((uintptr_t)workspace_dev & 255) || ((uintptr_t)kv_cache_dev & 15))
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "workspace must be 256-byte and KV cache 16-byte aligned");
+
+  amk_ctx* ctx = new (std::nothrow) amk_ctx;
+  if (!ctx) return fail(nullptr, AMK_ERR_OOM, "host allocation failed");
+  auto bail = [&](amk_status st) {
+    g_last_error = ctx->err;
+    delete ctx;
+    return st;
+  };
+
+  Schedule s;
+  std::string why;
+  amk_status st = plan(cfg, sched, &ctx->geom, &s, &why);
+  if (st != AMK_OK) return bail(fail(ctx, st, why));
+  const amk_config& c = *cfg;
+  const ModelGeom& g = ctx->geom;
+
+  // the safety gate: nothing is launched for a schedule that fails it
+  Report rep = validate(s);
+  if (!rep.ok) return bail(fail(ctx, AMK_ERR_SCHEDULE_INVALID, "schedule rejected: " + rep.msg));
+
+  // weights present for every matrix
+  const int lmf = lm_format(c);
+  if (!weights->embed || !weights->final_norm || !weights->layers || !aligned(weights->embed, 16) ||
+      !aligned(weights->final_norm, 2))
+    return bail(fail(ctx, AMK_ERR_INVALID_ARG, "missing or misaligned embedding, final norm or layer table"));
+  if (!c.tied_embeddings && !linear_ok(weights->lm_head, lmf))
+    return bail(fail(ctx, AMK_ERR_INVALID_ARG, "missing LM-head weights"));
+  for (int l = 0; l < c.n_layers; ++l) {
+    const amk_layer_weights& lw = weights->layers[l];
+    if (!lw.attn_norm || !lw.ffn_norm || !aligned(lw.attn_norm, 2) || !aligned(lw.ffn_norm, 2))
+      return bail(fail(ctx, AMK_ERR_INVALID_ARG, "missing or misaligned norm weights"));
+    for (const amk_linear* lin : {&lw.wq, &lw.wk, &lw.wv, &lw.wo, &lw.wg, &lw.wu, &lw.wd})
+      if (!linear_ok(*lin, c.weight_format))
+        return bail(fail(ctx, AMK_ERR_INVALID_ARG, "missing or misaligned linear weights / scales / zeros"));
+  }
+
+  Layout L = make_layout(g, s);
+  if (workspace_bytes < L.total) {
+    char buf[128];
+    snprintf(buf, sizeof buf, "workspace has %zu bytes, needs %zu", workspace_bytes, L.total);
+    return bail(fail(ctx, AMK_ERR_OOM, buf));
+  }
+
+  ctx->cfg = c;
+  ctx->stream = (cudaStream_t)stream;
+  ctx->ws = (uint8_t*)workspace_dev;
+  ctx->ws_bytes = workspace_bytes;
+  ctx->kv = kv_cache_dev;
+  ctx->timeout_ns = (uint64_t)(sched && sched->watchdog_ms > 0 ? sched->watchdog_ms : 2000) * 1000000ull;
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) return bail(fail(ctx, AMK_ERR_CUDA, "cudaGetDevice failed"));
+
+  // kernel and co-residency of one CTA per SM
+  ctx->kernel = decode_kernel_for(c.weight_format, lmf);
+  ctx->smem = decode_smem_bytes();
+  {
+    cudaError_t e = cudaFuncSetAttribute(ctx->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ctx->smem);
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "cudaFuncSetAttribute"));
+    int per_sm = 0, sms = 0, coop = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ctx->kernel, kThreads, ctx->smem);
+    if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "occupancy query"));
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device);
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, ctx->device);
+    if (!coop) return bail(fail(ctx, AMK_ERR_UNSUPPORTED, "device lacks cooperative launch"));
+    if (per_sm < 1 || g.num_ctas > per_sm * sms)
+      return bail(fail(ctx, AMK_ERR_UNSUPPORTED, "num_ctas exceeds co-resident CTAs"));
+  }
+
+  // device model
+  uint8_t* ws = ctx->ws;
+  DevMat mats[M_NUM];
+  for (int k = 0; k < M_NUM; ++k) {
+    const MatGeom& m = g.mat[k];
+    DevMat& d = mats[k];
+    d.base = ws + L.w[k];
+    d.scales = L.scales[k] ? (const uint16_t*)(ws + L.scales[k]) : nullptr;
+    d.layer_bytes = m.bytes;
+    d.rb_bytes = m.rb_bytes;
+    d.stage_bytes = (int32_t)(m.tile_bytes + m.side_bytes);
+    d.fmt = m.fmt;
+    d.rows = m.rows;
+    d.rows_padded = m.rows_padded;
+    d.K = m.K;
+    d.Kp = m.Kp;
+    d.Kt = m.Kt;
+    d.nkt = m.nkt;
+    d.Rt = m.Rt;
+    d.cpr_shift = m.cpr_shift;
+  }
+  DevModel& dm = ctx->dm;
+  dm.mat = (const DevMat*)(ws + L.mats);
+  dm.n_layers = c.n_layers;
+  dm.hidden = c.hidden;
+  dm.n_heads = c.n_heads;
+  dm.n_kv_heads = c.n_kv_heads;
+  dm.head_dim = c.head_dim;
+  dm.ffn = c.ffn;
+  dm.vocab = c.vocab;
+  dm.max_seq = c.max_seq;
+  dm.group = g.group;
+  dm.splits = g.splits;
+  dm.part_stride = g.part_stride;
+  dm.num_ctas = g.num_ctas;
+  dm.rms_eps = c.rms_eps;
+  dm.embed = (const uint16_t*)(ws + L.embed);
+  dm.final_norm = (const uint16_t*)(ws + L.final_norm);
+  dm.attn_norm = (const uint16_t*)(ws + L.attn_norm);
+  dm.ffn_norm = (const uint16_t*)(ws + L.ffn_norm);
+  dm.rope = (const float2*)(ws + L.rope);
+  dm.kv = (uint16_t*)kv_cache_dev;
+  dm.x = (float*)(ws + L.x);
+  dm.q = (float*)(ws + L.q);
+  dm.o = (float*)(ws + L.o);
+  dm.a = (float*)(ws + L.a);
+  dm.part = (float*)(ws + L.part);
+  dm.counters = (uint32_t*)(ws + L.counters);
+  dm.status = (uint32_t*)(ws + L.status);
+  dm.tasks = (const DevTask*)(ws + L.tasks);
+  dm.queue_off = (const int32_t*)(ws + L.queue_off);
+  dm.queue_body = (const int32_t*)(ws + L.queue_body);
+  ctx->logits_stage = (float*)(ws + L.logits);
+
+  // task table, queue order per CTA
+  std::vector<DevTask> tasks;
+  std::vector<int32_t> qoff(s.queues.size() + 1, 0), qbody(s.queues.size(), 0);
+  for (size_t q = 0; q < s.queues.size(); ++q) {
+    qoff[q] = (int32_t)tasks.size();
+    qbody[q] = s.body_len[q];
+    for (int32_t id : s.queues[q]) {
+      const Task& t = s.tasks[id];
+      DevTask d{};
+      d.type = (int16_t)t.type;
+      d.layer = (int16_t)t.layer;
+      d.wait_counter = t.waits.empty() ? -1 : t.waits[0].counter;
+      d.wait_count = t.waits.empty() ? 0u : (uint32_t)t.waits[0].threshold;
+      d.signal = t.signal;
+      d.a0 = (int32_t)t.a[0];
+      d.a1 = (int32_t)t.a[1];
+      d.a2 = (int32_t)t.a[2];
+      d.a3 = (int32_t)t.a[3];
+      if (t.waits.size() > 1) return bail(fail(ctx, AMK_ERR_SCHEDULE_INVALID, "kernel supports one wait per task"));
+      tasks.push_back(d);
+    }
+  }
+  qoff[s.queues.size()] = (int32_t)tasks.size();
+
+  // rotate-half RoPE table, computed in double and rounded to float
+  const int half = c.head_dim / 2;
+  std::vector<float> rope((size_t)c.max_seq * half * 2);
+  for (int pos = 0; pos < c.max_seq; ++pos)
+    for (int i = 0; i < half; ++i) {
+      const double ang = (double)pos * std::pow((double)c.rope_theta, -2.0 * i / c.head_dim);
+      rope[((size_t)pos * half + i) * 2 + 0] = (float)std::cos(ang);
+      rope[((size_t)pos * half + i) * 2 + 1] = (float)std::sin(ang);
+    }
+
+  cudaStream_t st_ = ctx->stream;
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.mats, mats, sizeof mats, cudaMemcpyHostToDevice, st_));
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.tasks, tasks.data(), tasks.size() * sizeof(DevTask),
+                                cudaMemcpyHostToDevice, st_));
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.queue_off, qoff.data(), qoff.size() * 4, cudaMemcpyHostToDevice, st_));
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.queue_body, qbody.data(), qbody.size() * 4, cudaMemcpyHostToDevice, st_));
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice, st_));
+  AMK_CUDA(ctx, cudaMemsetAsync(ws + L.counters, 0, s.counters.size() * 4, st_));
+  AMK_CUDA(ctx, cudaMemsetAsync(ws + L.status, 0, 64, st_));
+  AMK_CUDA(ctx, cudaMemsetAsync(ws + L.x, 0, L.counters - L.x, st_));
+
+  // weights: embedding (row major copy), norms, tiled matrices
+  const size_t H2 = (size_t)c.hidden * 2;
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.embed, weights->embed, (size_t)c.vocab * H2, cudaMemcpyDeviceToDevice, st_));
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.final_norm, weights->final_norm, H2, cudaMemcpyDeviceToDevice, st_));
+  for (int l = 0; l < c.n_layers; ++l) {
+    const amk_layer_weights& lw = weights->layers[l];
+    AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.attn_norm + l * H2, lw.attn_norm, H2, cudaMemcpyDeviceToDevice, st_));
+    AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.ffn_norm + l * H2, lw.ffn_norm, H2, cudaMemcpyDeviceToDevice, st_));
+    launch_pack_matrix(M_QKV, c.weight_format, mats[M_QKV], l, lw.wq.w, lw.wq.scales, lw.wq.zeros,
+                       lw.wk.w, lw.wk.scales, lw.wk.zeros, lw.wv.w, lw.wv.scales, lw.wv.zeros,
+                       c.n_heads, c.n_kv_heads, c.head_dim, st_);
+    launch_pack_matrix(M_O, c.weight_format, mats[M_O], l, lw.wo.w, lw.wo.scales, lw.wo.zeros,
+                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c.n_heads,
+                       c.n_kv_heads, c.head_dim, st_);
+    launch_pack_matrix(M_GU, c.weight_format, mats[M_GU], l, lw.wg.w, lw.wg.scales, lw.wg.zeros,
+                       lw.wu.w, lw.wu.scales, lw.wu.zeros, nullptr, nullptr, nullptr, c.n_heads,
+                       c.n_kv_heads, c.head_dim, st_);
+    launch_pack_matrix(M_DOWN, c.weight_format, mats[M_DOWN], l, lw.wd.w, lw.wd.scales, lw.wd.zeros,
+                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c.n_heads,
+                       c.n_kv_heads, c.head_dim, st_);
+    AMK_CUDA(ctx, cudaGetLastError());
+  }
+  if (c.tied_embeddings)
+    launch_pack_matrix(M_LM, AMK_FORMAT_BF16, mats[M_LM], 0, weights->embed, nullptr, nullptr,
+                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c.n_heads,
+                       c.n_kv_heads, c.head_dim, st_);
+  else
+    launch_pack_matrix(M_LM, lmf, mats[M_LM], 0, weights->lm_head.w, weights->lm_head.scales,
+                       weights->lm_head.zeros, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                       c.n_heads, c.n_kv_heads, c.head_dim, st_);
+  AMK_CUDA(ctx, cudaGetLastError());
+  AMK_CUDA(ctx, cudaStreamSynchronize(st_));
+  ctx->kv_len = 0;
+  *out = ctx;
+  return AMK_OK;
+}
+
+amk_status amk_prefill(amk_ctx* ctx, const int32_t* host_tokens, int32_t n, int32_t start_pos) {
+  if (!ctx) return fail(nullptr, AMK_ERR_INVALID_ARG, "context is NULL");
+  if (n < 0 || (n > 0 && !host_tokens)) return fail(ctx, AMK_ERR_INVALID_ARG, "bad token array");
+  if (start_pos < 0 || (int64_t)start_pos + n > ctx->cfg.max_seq)
+    return fail(ctx, AMK_ERR_INVALID_ARG, "prefill runs past max_seq");
+  for (int32_t i = 0; i < n; ++i) {
+    amk_status st = step_checks(ctx, host_tokens[i], start_pos + i);
+    if (st != AMK_OK) return st;
+    st = launch_step(ctx, host_tokens[i], start_pos + i, nullptr, 1);
+    if (st != AMK_OK) return st;
+    ctx->kv_len = start_pos + i + 1;
+  }
+  return AMK_OK;
+}
+
+amk_status amk_decode_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_dev) {
+  amk_status st = step_checks(ctx, token, pos);
+  if (st != AMK_OK) return st;
+  if (!logits_dev) return fail(ctx, AMK_ERR_INVALID_ARG, "logits pointer is NULL");
+  st = launch_step(ctx, token, pos, logits_dev, 0);
+  if (st == AMK_OK) ctx->kv_len = pos + 1;
+  return st;
+}
+
+amk_status amk_decode_step_host(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_host) {
+  amk_status st = step_checks(ctx, token, pos);
+  if (st != AMK_OK) return st;
+  if (!logits_host) return fail(ctx, AMK_ERR_INVALID_ARG, "logits pointer is NULL");
+  st = launch_step(ctx, token, pos, ctx->logits_stage, 0);
+  if (st != AMK_OK) return st;
+  ctx->kv_len = pos + 1;
+  cudaError_t e = cudaMemcpyAsync(logits_host, ctx->logits_stage, (size_t)ctx->cfg.vocab * 4,
+                                  cudaMemcpyDeviceToHost, ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "logits copy");
+  return amk_sync(ctx);
+}
+
+amk_status amk_set_kv_length(amk_ctx* ctx, int32_t n) {
+  if (!ctx) return fail(nullptr, AMK_ERR_INVALID_ARG, "context is NULL");
+  if (n < 0 || n > ctx->cfg.max_seq) return fail(ctx, AMK_ERR_INVALID_ARG, "KV length out of range");
+  ctx->kv_len = n;
+  return AMK_OK;
+}
+
+int32_t amk_kv_length(const amk_ctx* ctx) { return ctx ? ctx->kv_len : -1; }
+
+amk_status amk_sync(amk_ctx* ctx) {
+  if (!ctx) return fail(nullptr, AMK_ERR_INVALID_ARG, "context is NULL");
+  if (ctx->poisoned != AMK_OK) return fail(ctx, ctx->poisoned, ctx->err);
+  cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) {
+    ctx->poisoned = AMK_ERR_CUDA;
+    return cuda_fail(ctx, e, "cudaStreamSynchronize");
+  }
+  return read_status(ctx);
+}
+
+void amk_free(amk_ctx* ctx) { delete ctx; }
+
+amk_status amk_debug_watchdog_probe(void* scratch_dev, void* stream, int32_t limit_us,
+                                    int32_t* device_status) {
+  if (!scratch_dev || !device_status || limit_us <= 0 || limit_us > 10000000)
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "bad watchdog probe arguments");
+  cudaStream_t s = (cudaStream_t)stream;
+  AMK_CUDA(nullptr, cudaMemsetAsync(scratch_dev, 0, 256, s));
+  launch_watchdog_probe((uint32_t*)scratch_dev, (uint64_t)limit_us * 1000ull, stream);
+  AMK_CUDA(nullptr, cudaGetLastError());
+  uint32_t st[4];
+  AMK_CUDA(nullptr, cudaMemcpyAsync(st, (uint32_t*)scratch_dev + 16, sizeof st, cudaMemcpyDeviceToHost, s));
+  AMK_CUDA(nullptr, cudaStreamSynchronize(s));
+  *device_status = st[0] == ST_OK ? AMK_OK : st[0] == ST_TIMEOUT ? AMK_ERR_TIMEOUT : AMK_ERR_DEVICE_CHECK;
+  return AMK_OK;
+}
+
+amk_status amk_debug_dequant(int32_t format, const amk_linear* lin, int32_t out_features,
+                             int32_t in_features, float* out_dev, void* stream) {
+  if (!lin || !out_dev || out_features <= 0 || in_features <= 0 || in_features % 8 ||
+      !aligned(out_dev, 4))
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "bad dequant arguments");
+  if (format < AMK_FORMAT_BF16 || format > AMK_FORMAT_INT4 || !linear_ok(*lin, format))
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "bad format or missing scales / zeros");
+  if (format == AMK_FORMAT_INT4 && in_features % 128)
+    return fail(nullptr, AMK_ERR_UNSUPPORTED, "int4 needs in_features % 128 == 0");
+  launch_debug_dequant(format, lin->w, lin->scales, lin->zeros, out_features, in_features, out_dev, stream);
+  AMK_CUDA(nullptr, cudaGetLastError());
+  AMK_CUDA(nullptr, cudaStreamSynchronize((cudaStream_t)stream));
+  return AMK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,992 @@
+// Persistent batch-1 decode kernel for sm_103a.
+//
+// One cooperative CTA per SM walks its static task queue (wait -> dispatch
+// -> signal on monotonic counters, the execution model of the
+// AutoMegaKernel "Layer 0" VM).  Unlike the pages' design, a CTA is split
+// into a producer warp and eight consumer warps:
+//   * the producer streams every weight tile (and the KV-cache history) of
+//     the CTA's whole queue through a 12-slot shared-memory ring with 1-D
+//     TMA bulk copies completing on mbarriers.  Weights never depend on
+//     activations, so the producer runs ahead across the counter waits;
+//     this hides the per-tile cross-SM synchronisation cost the pages name
+//     as the bottleneck on high-bandwidth GPUs (AMK "Experimental results":
+//     training-class GPUs).
+//   * the consumers wait on counters, keep the activation vector in
+//     registers, reduce with warp shuffles, apply the fused epilogues
+//     (RoPE + KV append, residual adds, SwiGLU, logits) and signal.
+// Every wait is bounded by %globaltimer: on expiry the kernel records a
+// status word, lets its own copies land and returns.
+#include <algorithm>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "device_model.hpp"
+
+namespace amk {
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(tx)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// named barrier 1: the 256 consumer threads only (the producer warp never joins)
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// consumer barrier that also ORs a predicate over all consumer threads
+__device__ __forceinline__ bool consumer_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(kConsumerThreads)
+      : "memory");
+  return r != 0;
+}
+
+// ------------------------------------------------------------ shared memory
+
+struct Smem {
+  uint8_t ring[kStages][kSlotBytes];
+  float scratch[kScratchFloats];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  float misc[32];
+  int32_t abort_flag;
+  int32_t flag;
+};
+static_assert(sizeof(Smem) <= kSmemBytes, "shared memory layout");
+
+// ------------------------------------------------------------- status
+
+__device__ void set_status(uint32_t* status, uint32_t code, uint32_t task, uint32_t site) {
+  if (atomicCAS(&status[0], 0u, code) == 0u) {
+    status[1] = blockIdx.x;
+    status[2] = task;
+    status[3] = site;
+    __threadfence();
+  }
+}
+
+// Bounded wait on a counter: true once counter >= target (wrap-safe).
+__device__ bool wait_counter(const uint32_t* ctr, uint32_t target, uint32_t* status,
+                             volatile int32_t* abort_flag, uint64_t timeout_ns, uint32_t task) {
+  const uint64_t t0 = global_timer();
+  for (uint32_t spin = 1;; ++spin) {
+    if ((int32_t)(ld_acquire(ctr) - target) >= 0) return true;
+    if ((spin & 31u) == 0u) {
+      if (*abort_flag || ld_relaxed(status) != 0u) return false;
+      if (global_timer() - t0 > timeout_ns) {
+        set_status(status, ST_TIMEOUT, task, SITE_COUNTER);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait for an mbarrier phase.  Gives up when the CTA is aborting.
+__device__ bool wait_phase(uint64_t* bar, uint32_t parity, uint32_t* status,
+                           volatile int32_t* abort_flag, uint64_t timeout_ns, uint32_t task,
+                           uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((spin & 15u) == 0u && global_timer() - t0 > timeout_ns) {
+      set_status(status, ST_TIMEOUT, task, site);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------ task helpers
+
+__device__ __forceinline__ int mat_kind(int type) {
+  switch (type) {
+    case T_QKV: return M_QKV;
+    case T_OPROJ: return M_O;
+    case T_GATEUP: return M_GU;
+    case T_DOWN: return M_DOWN;
+    default: return M_LM;
+  }
+}
+
+// context split j of a KV head: cached positions [t0, t1) read from the
+// cache history; the current position is handled by the last split
+__device__ __forceinline__ void attn_range(int pos, int splits, int j, int* t0, int* t1) {
+  const int len = (pos + splits - 1) / splits;
+  int a = j * len;
+  if (a > pos) a = pos;
+  int b = a + len;
+  if (b > pos) b = pos;
+  *t0 = a;
+  *t1 = b;
+}
+
+__device__ __forceinline__ int attn_positions_per_stage(int head_dim) {
+  return (kStageBytes / 2) / (head_dim * 2);
+}
+
+__device__ __forceinline__ const uint16_t* kv_row(const DevModel& m, int layer, int kvsel, int g,
+                                                  int t) {
+  return m.kv + ((((int64_t)layer * 2 + kvsel) * m.n_kv_heads + g) * m.max_seq + t) *
+                    (int64_t)m.head_dim;
+}
+
+// -------------------------------------------------------------- producer
+
+__device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
+  const DevModel& m = p.m;
+  const uint64_t pol_w = policy_evict_first();
+  const uint64_t pol_kv = policy_evict_normal();
+  volatile int32_t* abort_flag = &sm.abort_flag;
+  uint32_t slot = 0, phase = 0;
+  uint32_t issued = 0;     // slots that have held a copy
+  uint32_t parity = 0;     // parity of each slot's last issued phase
+  bool ok = true;
+  for (int i = 0; i < n && ok; ++i) {
+    const DevTask t = q[i];
+    if (t.type == T_ATTN) {
+      int t0, t1;
+      attn_range(p.pos, m.splits, t.a1, &t0, &t1);
+      const int pps = attn_positions_per_stage(m.head_dim);
+      const uint16_t* kb = kv_row(m, t.layer, 0, t.a0, 0);
+      const uint16_t* vb = kv_row(m, t.layer, 1, t.a0, 0);
+      for (int s0 = t0; s0 < t1 && ok; s0 += pps) {
+        const int np = min(pps, t1 - s0);
+        const uint32_t bytes = (uint32_t)np * m.head_dim * 2;
+        ok = wait_phase(&sm.empty[slot], phase ^ 1u, m.status, abort_flag, p.timeout_ns, i,
+                        SITE_EMPTY) && !*abort_flag;
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sm.full[slot], 2 * bytes);
+        bulk_copy_g2s(sm.ring[slot], kb + (int64_t)s0 * m.head_dim, bytes, &sm.full[slot], pol_kv);
+        bulk_copy_g2s(sm.ring[slot] + kStageBytes / 2, vb + (int64_t)s0 * m.head_dim, bytes,
+                      &sm.full[slot], pol_kv);
+        issued |= 1u << slot;
+        parity = (parity & ~(1u << slot)) | (phase << slot);
+        if (++slot == kStages) { slot = 0; phase ^= 1u; }
+      }
+    } else {
+      const int kind = mat_kind(t.type);
+      const DevMat M = m.mat[kind];
+      const uint8_t* src = M.base + (kind == M_LM ? 0 : (int64_t)t.layer * M.layer_bytes) +
+                           (int64_t)t.a0 * M.rb_bytes;
+      const int nst = (t.a1 - t.a0) * M.nkt;
+      for (int s = 0; s < nst && ok; ++s) {
+        ok = wait_phase(&sm.empty[slot], phase ^ 1u, m.status, abort_flag, p.timeout_ns, i,
+                        SITE_EMPTY) && !*abort_flag;
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)M.stage_bytes);
+        bulk_copy_g2s(sm.ring[slot], src + (int64_t)s * M.stage_bytes, (uint32_t)M.stage_bytes,
+                      &sm.full[slot], pol_w);
+        issued |= 1u << slot;
+        parity = (parity & ~(1u << slot)) | (phase << slot);
+        if (++slot == kStages) { slot = 0; phase ^= 1u; }
+      }
+    }
+  }
+  // Every copy this CTA issued must land before its shared memory goes away.
+  // Consumers normally wait for all of them already; when they stop early
+  // (a failed wait anywhere) this is what keeps the CTA from exiting with
+  // a copy in flight.
+  for (int s = 0; s < kStages; ++s) {
+    if (!(issued & (1u << s))) continue;
+    const uint32_t par = (parity >> s) & 1u;
+    const uint64_t t0 = global_timer();
+    while (!mbar_try_wait(&sm.full[s], par)) {
+      if (global_timer() - t0 > p.timeout_ns) {
+        set_status(m.status, ST_TIMEOUT, 0xFFFFFFFFu, SITE_DRAIN);
+        break;
+      }
+    }
+  }
+  (void)ok;
+}
+
+// -------------------------------------------------------------- consumers
+
+struct Ring {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void advance() {
+    if (++slot == kStages) { slot = 0; phase ^= 1u; }
+  }
+};
+
+// weight decoding of one 8-element chunk (shared with the dequant check)
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// int8 byte i of w as float: (q + 128) placed under exponent 2^23, minus 2^23 + 128
+__device__ __forceinline__ float i8_at(uint32_t w_xor80, int i) {
+  const uint32_t sel = 0x7440u | (uint32_t)i;
+  return __uint_as_float(__byte_perm(w_xor80, 0x4B000000u, sel)) - 8388736.0f;
+}
+
+// int4 nibble i of w as float (exact)
+__device__ __forceinline__ float u4_at(uint32_t w, int i) {
+  return __uint_as_float(0x4B000000u | ((w >> (4 * i)) & 0xFu)) - 8388608.0f;
+}
+
+__device__ __forceinline__ float fp16_bits_to_float(uint16_t b) {
+  return __half2float(__ushort_as_half(b));
+}
+
+template <int FMT>
+struct Fmt;
+template <>
+struct Fmt<AMK_FORMAT_BF16> { static constexpr int kPasses = 4; };
+template <>
+struct Fmt<AMK_FORMAT_INT8> { static constexpr int kPasses = 8; };
+template <>
+struct Fmt<AMK_FORMAT_INT4> { static constexpr int kPasses = 16; };
+
+// Sum P per-lane values over the warp.  Lanes whose low (5 - log2 P) bits
+// are zero return the total of value index (lane >> (5 - log2 P)).
+template <int P>
+__device__ __forceinline__ float transpose_reduce(float (&v)[P], int lane) {
+#pragma unroll
+  for (int n = P, msk = 16; n > 1; n >>= 1, msk >>= 1) {
+    const bool up = (lane & msk) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float keep = up ? v[i + n / 2] : v[i];
+      const float send = up ? v[i] : v[i + n / 2];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, msk);
+    }
+  }
+#pragma unroll
+  for (int msk = 16 / P; msk >= 1; msk >>= 1) v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], msk);
+  return v[0];
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int msk = 16; msk >= 1; msk >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, msk);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int msk = 16; msk >= 1; msk >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, msk));
+  return v;
+}
+
+__device__ __forceinline__ void load8_f32(const float* src, float* d) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+  const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 1);
+  d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
+  d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
+}
+
+__device__ __forceinline__ void load8_bf16(const uint16_t* src, float* d) {
+  const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+  d[0] = bf16_lo(w.x); d[1] = bf16_hi(w.x); d[2] = bf16_lo(w.y); d[3] = bf16_hi(w.y);
+  d[4] = bf16_lo(w.z); d[5] = bf16_hi(w.z); d[6] = bf16_lo(w.w); d[7] = bf16_hi(w.w);
+}
+
+// Activation chunk owned by a consumer thread: h[kt][i] = act[kt*Kt + chunk*8 + i].
+// QKV, gate/up and LM head take rmsnorm(x) * w_norm; O takes o; down takes a.
+__device__ void load_activation(const StepParams& p, Smem& sm, const DevTask& t, const DevMat& M,
+                                int chunk, float (&h)[8][8]) {
+  const DevModel& m = p.m;
+  const int tid = threadIdx.x;
+  const bool norm = t.type == T_QKV || t.type == T_GATEUP || t.type == T_LMHEAD;
+  const bool from_embed = t.type == T_QKV && t.layer == 0;
+  const float* src = t.type == T_OPROJ ? m.o : t.type == T_DOWN ? m.a : m.x;
+  const uint16_t* emb = m.embed + (int64_t)p.token * m.hidden;
+  float ss = 0.f;
+#pragma unroll
+  for (int kt = 0; kt < 8; ++kt) {
+    if (kt < M.nkt) {
+      const int k = kt * M.Kt + chunk * 8;
+      if (k < M.K) {  // K is a multiple of 8
+        if (from_embed) load8_bf16(emb + k, h[kt]);
+        else load8_f32(src + k, h[kt]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[kt][i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(h[kt][i], h[kt][i], ss);
+    }
+  }
+  if (!norm) return;
+  // threads tid < Kt/8 hold every chunk once: their squares sum to sum(x^2)
+  const int cpr = 1 << M.cpr_shift;
+  ss = warp_sum(tid < cpr ? ss : 0.f);
+  if ((tid & 31) == 0) sm.misc[tid >> 5] = ss;
+  consumer_sync();
+  float tot = 0.f;
+  for (int w = 0; w < (cpr >> 5); ++w) tot += sm.misc[w];
+  const float r = rsqrtf(tot / (float)m.hidden + m.rms_eps);
+  const uint16_t* nw = t.type == T_QKV ? m.attn_norm + (int64_t)t.layer * m.hidden
+                       : t.type == T_GATEUP ? m.ffn_norm + (int64_t)t.layer * m.hidden
+                                            : m.final_norm;
+#pragma unroll
+  for (int kt = 0; kt < 8; ++kt) {
+    if (kt < M.nkt) {
+      const int k = kt * M.Kt + chunk * 8;
+      if (k < M.K) {
+        float w8[8];
+        load8_bf16(nw + k, w8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[kt][i] = h[kt][i] * r * w8[i];
+      }
+    }
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ float chunk_dot(const uint8_t* tile, const DevMat& M, int row,
+                                           int chunk, const float (&h)[8], float acc) {
+  if constexpr (FMT == AMK_FORMAT_BF16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + (((row << M.cpr_shift) + chunk) << 4));
+    acc = fmaf(bf16_lo(w.x), h[0], acc);
+    acc = fmaf(bf16_hi(w.x), h[1], acc);
+    acc = fmaf(bf16_lo(w.y), h[2], acc);
+    acc = fmaf(bf16_hi(w.y), h[3], acc);
+    acc = fmaf(bf16_lo(w.z), h[4], acc);
+    acc = fmaf(bf16_hi(w.z), h[5], acc);
+    acc = fmaf(bf16_lo(w.w), h[6], acc);
+    acc = fmaf(bf16_hi(w.w), h[7], acc);
+    return acc;
+  } else if constexpr (FMT == AMK_FORMAT_INT8) {
+    const uint2 w = *reinterpret_cast<const uint2*>(tile + (((row << M.cpr_shift) + chunk) << 3));
+    const uint32_t a = w.x ^ 0x80808080u, b = w.y ^ 0x80808080u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc = fmaf(i8_at(a, i), h[i], acc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc = fmaf(i8_at(b, i), h[4 + i], acc);
+    return acc;
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + (((row << M.cpr_shift) + chunk) << 2));
+    // side data after the codes: fp16 scales [Rt][Kt/128], then u8 zeros [Rt][Kt/128]
+    const int ngt = M.Kt >> 7;
+    const int gi = row * ngt + (chunk >> 4);
+    const uint8_t* side = tile + kStageBytes;
+    const float s = fp16_bits_to_float(reinterpret_cast<const uint16_t*>(side)[gi]);
+    const float z = (float)side[M.Rt * ngt * 2 + gi];
+    float d = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d = fmaf(u4_at(w, i) - z, h[i], d);
+    return fmaf(s, d, acc);
+  }
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// GEMV task: rows [a0*Rt, a1*Rt) of one tiled matrix against the activation
+template <int FMT>
+__device__ __noinline__ bool gemv_task(const StepParams& p, Smem& sm, const DevTask& t, Ring& ring,
+                          bool failed, uint32_t task_idx) {
+  constexpr int P = Fmt<FMT>::kPasses;
+  const DevModel& m = p.m;
+  const int kind = mat_kind(t.type);
+  const DevMat M = m.mat[kind];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cs = M.cpr_shift;
+  const int chunk = tid & ((1 << cs) - 1);
+  const int rsub = tid >> cs;
+  const int rpp = kConsumerThreads >> cs;
+  const int wpg_shift = cs - 5;  // log2 warps per row group
+  const int wg = warp & ((1 << wpg_shift) - 1);
+  volatile int32_t* abort_flag = &sm.abort_flag;
+
+  float h[8][8];
+  load_activation(p, sm, t, M, chunk, h);
+
+  // layer-0 QKV tasks also initialise their slice of the residual stream
+  if (t.type == T_QKV && t.layer == 0) {
+    const uint16_t* emb = m.embed + (int64_t)p.token * m.hidden;
+    for (int e = t.a2 + tid; e < t.a3; e += kConsumerThreads)
+      m.x[e] = __uint_as_float((uint32_t)emb[e] << 16);
+  }
+
+  float* red = sm.scratch;
+  const int nrb = t.a1 - t.a0;
+  for (int rb = 0; rb < nrb; ++rb) {
+    float acc[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int kt = 0; kt < 8; ++kt) {
+      if (kt < M.nkt) {
+        if (!failed)
+          failed = !wait_phase(&sm.full[ring.slot], ring.phase, m.status, abort_flag,
+                               p.timeout_ns, task_idx, SITE_FULL);
+        if (!failed) {
+          const uint8_t* tile = sm.ring[ring.slot];
+#pragma unroll
+          for (int ps = 0; ps < P; ++ps)
+            acc[ps] = chunk_dot<FMT>(tile, M, ps * rpp + rsub, chunk, h[kt], acc[ps]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[ring.slot]);
+        ring.advance();
+      }
+    }
+    const float v = transpose_reduce<P>(acc, lane);
+    constexpr int kLaneStride = 32 / P;
+    if ((lane & (kLaneStride - 1)) == 0) {
+      const int ps = lane / kLaneStride;
+      const int row = rb * M.Rt + ps * rpp + rsub;
+      red[row * 8 + wg] = v;
+    }
+  }
+
+  if (consumer_sync_or(failed)) return false;
+
+  // epilogue: one row (or one row pair) per thread
+  const int nrows = nrb * M.Rt;
+  const int row0 = t.a0 * M.Rt;
+  const int nwg = 1 << wpg_shift;
+  auto row_sum = [&](int r) {
+    float y = 0.f;
+    for (int w = 0; w < nwg; ++w) y += red[r * 8 + w];
+    return y;
+  };
+  if (t.type == T_QKV || t.type == T_GATEUP) {
+    for (int pr = tid; pr < nrows / 2; pr += kConsumerThreads) {
+      const int R = row0 + 2 * pr;
+      if (R >= M.rows) continue;
+      float y0 = row_sum(2 * pr), y1 = row_sum(2 * pr + 1);
+      if (FMT == AMK_FORMAT_INT8) {
+        const uint16_t* sc = M.scales + (int64_t)t.layer * M.rows_padded;
+        y0 *= fp16_bits_to_float(sc[R]);
+        y1 *= fp16_bits_to_float(sc[R + 1]);
+      }
+      if (t.type == T_GATEUP) {
+        m.a[R >> 1] = silu(y0) * y1;
+        continue;
+      }
+      const int hd = m.head_dim, half = hd >> 1;
+      const int qd = m.n_heads * hd, kvd = m.n_kv_heads * hd;
+      if (R < qd + kvd) {
+        // rotate-half RoPE pair (i, i + hd/2) at position pos
+        const bool is_q = R < qd;
+        const int rr = is_q ? R : R - qd;
+        const int head = rr / hd, i = (rr % hd) >> 1;
+        const float2 cs2 = m.rope[(int64_t)p.pos * half + i];
+        const float a = y0 * cs2.x - y1 * cs2.y;
+        const float b = y1 * cs2.x + y0 * cs2.y;
+        if (is_q) {
+          m.q[head * hd + i] = a;
+          m.q[head * hd + half + i] = b;
+        } else {
+          uint16_t* kr = const_cast<uint16_t*>(kv_row(m, t.layer, 0, head, p.pos));
+          kr[i] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+          kr[half + i] = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+        }
+      } else {
+        const int vr = R - qd - kvd;
+        uint16_t* vrow = const_cast<uint16_t*>(kv_row(m, t.layer, 1, vr / hd, p.pos));
+        vrow[vr % hd] = __bfloat16_as_ushort(__float2bfloat16_rn(y0));
+        vrow[vr % hd + 1] = __bfloat16_as_ushort(__float2bfloat16_rn(y1));
+      }
+    }
+  } else {
+    for (int r = tid; r < nrows; r += kConsumerThreads) {
+      const int R = row0 + r;
+      if (R >= M.rows) continue;
+      float y = row_sum(r);
+      if (FMT == AMK_FORMAT_INT8) {
+        const uint16_t* sc = M.scales + (kind == M_LM ? 0 : (int64_t)t.layer * M.rows_padded);
+        y *= fp16_bits_to_float(sc[R]);
+      }
+      if (t.type == T_LMHEAD) {
+        p.logits[R] = y;
+      } else {  // O projection / down projection: residual add on owned rows
+        m.x[R] = __ldcg(m.x + R) + y;
+      }
+    }
+  }
+  return true;
+}
+
+// Split-K GQA attention of one KV head over one context split; the last
+// split to finish merges all splits of the head (LSE combine) into o.
+// HD: head_dim; a lane owns DPL = HD/32 dims of every head of the group.
+template <int HD>
+__device__ __noinline__ bool attn_task(const StepParams& p, Smem& sm, const DevTask& t, Ring& ring,
+                          bool failed, uint32_t task_idx) {
+  constexpr int DPL = HD / 32;
+  constexpr int GMAX = kMaxGroupDim / HD;
+  const DevModel& m = p.m;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int hd = HD, G = m.group, g = t.a0, j = t.a1;
+  volatile int32_t* abort_flag = &sm.abort_flag;
+
+  // queries of the group, pre-scaled so that scores are in log2 units
+  const float qscale = 1.4426950408889634f * rsqrtf((float)hd);
+  float qr[GMAX][DPL];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d)
+      qr[h][d] = h < G ? __ldcg(m.q + (int64_t)(g * G + h) * hd + lane * DPL + d) * qscale : 0.f;
+  float mx[GMAX], l[GMAX], acc[GMAX][DPL];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    mx[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[h][d] = 0.f;
+  }
+
+  auto update = [&](const float* kf, const float* vf) {
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      if (h < G) {
+        float s = 0.f;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) s = fmaf(qr[h][d], kf[d], s);
+        s = warp_sum(s);
+        const float mn = fmaxf(mx[h], s);
+        const float alpha = exp2f(mx[h] - mn);
+        const float pe = exp2f(s - mn);
+        l[h] = l[h] * alpha + pe;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(acc[h][d], alpha, pe * vf[d]);
+        mx[h] = mn;
+      }
+    }
+  };
+  auto load_kv = [&](const uint16_t* src, float* f, bool global) {
+    if constexpr (DPL == 4) {
+      uint2 w;
+      if (global) w = __ldcg(reinterpret_cast<const uint2*>(src + lane * 4));
+      else w = *reinterpret_cast<const uint2*>(src + lane * 4);
+      f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+    } else {
+      uint32_t w;
+      if (global) w = __ldcg(reinterpret_cast<const unsigned int*>(src + lane * 2));
+      else w = *reinterpret_cast<const uint32_t*>(src + lane * 2);
+      f[0] = bf16_lo(w); f[1] = bf16_hi(w);
+    }
+  };
+
+  int t0, t1;
+  attn_range(p.pos, m.splits, j, &t0, &t1);
+  const int pps = attn_positions_per_stage(hd);
+  for (int s0 = t0; s0 < t1; s0 += pps) {
+    const int np = min(pps, t1 - s0);
+    if (!failed)
+      failed = !wait_phase(&sm.full[ring.slot], ring.phase, m.status, abort_flag, p.timeout_ns,
+                           task_idx, SITE_FULL);
+    if (!failed) {
+      const uint16_t* kt = reinterpret_cast<const uint16_t*>(sm.ring[ring.slot]);
+      const uint16_t* vt = reinterpret_cast<const uint16_t*>(sm.ring[ring.slot] + kStageBytes / 2);
+      for (int pi = warp; pi < np; pi += kConsumerWarps) {
+        float kf[DPL], vf[DPL];
+        load_kv(kt + pi * hd, kf, false);
+        load_kv(vt + pi * hd, vf, false);
+        update(kf, vf);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[ring.slot]);
+    ring.advance();
+  }
+  // the current position, written this step by the QKV tasks
+  if (!failed && j == m.splits - 1 && warp == 0) {
+    float kf[DPL], vf[DPL];
+    load_kv(kv_row(m, t.layer, 0, g, p.pos), kf, true);
+    load_kv(kv_row(m, t.layer, 1, g, p.pos), vf, true);
+    update(kf, vf);
+  }
+
+  // merge the eight warps' partial softmax states
+  float* mg = sm.scratch;  // [warp][G][hd + 2]
+  const int ws = G * (hd + 2);
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    if (h < G) {
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) mg[warp * ws + h * (hd + 2) + lane * DPL + d] = acc[h][d];
+      if (lane == 0) {
+        mg[warp * ws + h * (hd + 2) + hd] = mx[h];
+        mg[warp * ws + h * (hd + 2) + hd + 1] = l[h];
+      }
+    }
+  }
+  if (consumer_sync_or(failed)) return false;
+  float* part = m.part + (int64_t)(g * m.splits + j) * m.part_stride;
+  for (int idx = tid; idx < G * hd; idx += kConsumerThreads) {
+    const int h = idx / hd, d = idx % hd;
+    float M = -INFINITY;
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg[w * ws + h * (hd + 2) + hd]);
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = mg[w * ws + h * (hd + 2) + hd];
+        if (mw == -INFINITY) continue;
+        const float sc = exp2f(mw - M);
+        L = fmaf(mg[w * ws + h * (hd + 2) + hd + 1], sc, L);
+        A = fmaf(mg[w * ws + h * (hd + 2) + d], sc, A);
+      }
+    }
+    part[h * (hd + 2) + d] = A;
+    if (d == 0) {
+      part[h * (hd + 2) + hd] = M;
+      part[h * (hd + 2) + hd + 1] = L;
+    }
+  }
+  consumer_sync();
+
+  // ticket: the last split of this KV head to arrive merges all splits
+  if (tid == 0) {
+    const uint32_t old = atom_add_acq_rel(m.counters + t.signal, 1u);
+    sm.flag = (old + 1u == p.epoch * (uint32_t)m.splits) ? 1 : 0;
+  }
+  consumer_sync();
+  if (!sm.flag) return true;
+
+  const float* pg = m.part + (int64_t)g * m.splits * m.part_stride;
+  for (int idx = tid; idx < G * hd; idx += kConsumerThreads) {
+    const int h = idx / hd, d = idx % hd;
+    float M = -INFINITY;
+    for (int s = 0; s < m.splits; ++s) M = fmaxf(M, __ldcg(pg + (int64_t)s * m.part_stride + h * (hd + 2) + hd));
+    float L = 0.f, A = 0.f;
+    for (int s = 0; s < m.splits; ++s) {
+      const float* ps = pg + (int64_t)s * m.part_stride + h * (hd + 2);
+      const float ms = __ldcg(ps + hd);
+      if (ms == -INFINITY) continue;
+      const float sc = exp2f(ms - M);
+      L = fmaf(__ldcg(ps + hd + 1), sc, L);
+      A = fmaf(__ldcg(ps + d), sc, A);
+    }
+    m.o[(int64_t)(g * G + h) * hd + d] = A / L;
+  }
+  consumer_sync();
+  if (tid == 0) red_release_add(m.counters + t.a2, 1u);
+  return true;
+}
+
+template <int QKV_FMT, int LM_FMT>
+__device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
+  const DevModel& m = p.m;
+  const int tid = threadIdx.x;
+  Ring ring;
+  volatile int32_t* abort_flag = &sm.abort_flag;
+  for (int i = 0; i < n; ++i) {
+    const DevTask t = q[i];
+    bool failed = false;
+    if (t.wait_counter >= 0 && tid == 0)
+      failed = !wait_counter(m.counters + t.wait_counter, p.epoch * t.wait_count, m.status,
+                             abort_flag, p.timeout_ns, (uint32_t)i);
+    if (consumer_sync_or(failed)) {
+      *abort_flag = 1;
+      return;
+    }
+    bool ok;
+    if (t.type == T_ATTN)
+      ok = m.head_dim == 128 ? attn_task<128>(p, sm, t, ring, false, (uint32_t)i)
+                             : attn_task<64>(p, sm, t, ring, false, (uint32_t)i);
+    else if (t.type == T_LMHEAD) ok = gemv_task<LM_FMT>(p, sm, t, ring, false, (uint32_t)i);
+    else ok = gemv_task<QKV_FMT>(p, sm, t, ring, false, (uint32_t)i);
+    if (!ok) {
+      *abort_flag = 1;
+      return;
+    }
+    if (t.type != T_ATTN) {
+      consumer_sync();  // epilogue stores done; scratch free for the next task
+      if (tid == 0 && t.signal >= 0) red_release_add(m.counters + t.signal, 1u);
+    }
+  }
+}
+
+template <int FMT, int LM_FMT>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ StepParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kConsumerWarps);
+    }
+    sm.abort_flag = 0;
+    sm.flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  const int c = blockIdx.x;
+  const int q0 = p.m.queue_off[c];
+  const int n = p.skip_lm ? p.m.queue_body[c] : p.m.queue_off[c + 1] - q0;
+  const DevTask* q = p.m.tasks + q0;
+  if (tid >= kConsumerThreads) {
+    if (tid == kConsumerThreads) producer_loop(p, sm, q, n);
+  } else {
+    consumer_loop<FMT, LM_FMT>(p, sm, q, n);
+  }
+}
+
+// ------------------------------------------------------------- dispatch
+
+using KernelFn = void (*)(StepParams);
+
+static KernelFn pick_kernel(int fmt, int lm_fmt) {
+#define AMK_K(a, b) \
+  if (fmt == a && lm_fmt == b) return decode_kernel<a, b>;
+  AMK_K(AMK_FORMAT_BF16, AMK_FORMAT_BF16)
+  AMK_K(AMK_FORMAT_INT8, AMK_FORMAT_INT8)
+  AMK_K(AMK_FORMAT_INT8, AMK_FORMAT_BF16)
+  AMK_K(AMK_FORMAT_INT4, AMK_FORMAT_INT4)
+  AMK_K(AMK_FORMAT_INT4, AMK_FORMAT_BF16)
+#undef AMK_K
+  return nullptr;
+}
+
+const void* decode_kernel_for(int fmt, int lm_fmt) {
+  return reinterpret_cast<const void*>(pick_kernel(fmt, lm_fmt));
+}
+
+int decode_smem_bytes() { return (int)sizeof(Smem); }
+
+// --------------------------------------------------------- weight packing
+
+struct PackArgs {
+  DevMat dst;                 // base already at the layer
+  uint16_t* scales_dst;       // int8 row scales of the layer, or null
+  const void* w[3];
+  const void* s[3];
+  const void* z[3];
+  int kind, fmt, n_heads, n_kv_heads, head_dim;
+};
+
+// packed row -> (source index, source row) or -1
+__device__ int pack_source(const PackArgs& a, int pr, int* row) {
+  const DevMat& M = a.dst;
+  if (pr >= M.rows) return -1;
+  if (a.kind == M_QKV) {
+    const int hd = a.head_dim, qd = a.n_heads * hd, kvd = a.n_kv_heads * hd;
+    if (pr < qd + kvd) {
+      const int rr = pr < qd ? pr : pr - qd;
+      const int i = rr % hd;
+      *row = rr / hd * hd + (i >> 1) + (i & 1) * (hd / 2);
+      return pr < qd ? 0 : 1;
+    }
+    *row = pr - qd - kvd;
+    return 2;
+  }
+  if (a.kind == M_GU) {
+    *row = pr >> 1;
+    return pr & 1;
+  }
+  *row = pr;
+  return 0;
+}
+
+__global__ void pack_kernel(const PackArgs a) {
+  const DevMat& M = a.dst;
+  const int chunks = M.Kp / 8;
+  const int64_t total = (int64_t)M.rows_padded * chunks;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int pr = (int)(idx / chunks);
+    const int c = (int)(idx % chunks);
+    const int k = c * 8;
+    int row = 0;
+    const int src = pack_source(a, pr, &row);
+    const int rb = pr / M.Rt, r = pr % M.Rt, kt = k / M.Kt, kk = k % M.Kt;
+    uint8_t* tile = const_cast<uint8_t*>(M.base) + ((int64_t)rb * M.nkt + kt) * M.stage_bytes;
+    const bool live = src >= 0 && k < M.K;
+    if (a.fmt == AMK_FORMAT_BF16) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (live) v = *reinterpret_cast<const uint4*>(
+                    static_cast<const uint16_t*>(a.w[src]) + (int64_t)row * M.K + k);
+      *reinterpret_cast<uint4*>(tile + ((int64_t)r * M.Kt + kk) * 2) = v;
+    } else if (a.fmt == AMK_FORMAT_INT8) {
+      uint2 v = make_uint2(0, 0);
+      if (live) v = *reinterpret_cast<const uint2*>(
+                    static_cast<const int8_t*>(a.w[src]) + (int64_t)row * M.K + k);
+      *reinterpret_cast<uint2*>(tile + (int64_t)r * M.Kt + kk) = v;
+      if (c == 0)
+        a.scales_dst[pr] = src >= 0 ? static_cast<const uint16_t*>(a.s[src])[row] : (uint16_t)0;
+    } else {
+      uint32_t v = 0;
+      if (live) v = *reinterpret_cast<const uint32_t*>(
+                    static_cast<const uint8_t*>(a.w[src]) + (int64_t)row * (M.K / 2) + k / 2);
+      *reinterpret_cast<uint32_t*>(tile + ((int64_t)r * M.Kt + kk) / 2) = v;
+      if ((kk & 127) == 0) {
+        const int ngt = M.Kt >> 7, gl = kk >> 7, gg = k >> 7;
+        uint16_t sc = 0;
+        uint8_t zz = 0;
+        if (live) {
+          const int ng = M.K / 128, zb = (ng + 1) / 2;
+          sc = static_cast<const uint16_t*>(a.s[src])[(int64_t)row * ng + gg];
+          const uint8_t zbyte = static_cast<const uint8_t*>(a.z[src])[(int64_t)row * zb + gg / 2];
+          zz = (gg & 1) ? (zbyte >> 4) : (zbyte & 15);
+        }
+        uint8_t* side = tile + kStageBytes;
+        reinterpret_cast<uint16_t*>(side)[r * ngt + gl] = sc;
+        side[M.Rt * ngt * 2 + r * ngt + gl] = zz;
+      }
+    }
+  }
+}
+
+void launch_pack_matrix(int kind, int fmt, const DevMat& dst, int layer, const void* w0,
+                        const void* s0, const void* z0, const void* w1, const void* s1,
+                        const void* z1, const void* w2, const void* s2, const void* z2,
+                        int n_heads, int n_kv_heads, int head_dim, void* stream) {
+  PackArgs a;
+  a.dst = dst;
+  a.dst.base = dst.base + (kind == M_LM ? 0 : (int64_t)layer * dst.layer_bytes);
+  a.scales_dst = dst.scales ? const_cast<uint16_t*>(dst.scales) +
+                                  (kind == M_LM ? 0 : (int64_t)layer * dst.rows_padded)
+                            : nullptr;
+  a.w[0] = w0; a.w[1] = w1; a.w[2] = w2;
+  a.s[0] = s0; a.s[1] = s1; a.s[2] = s2;
+  a.z[0] = z0; a.z[1] = z1; a.z[2] = z2;
+  a.kind = kind;
+  a.fmt = fmt;
+  a.n_heads = n_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  const int64_t total = (int64_t)dst.rows_padded * (dst.Kp / 8);
+  int blocks = (int)std::min<int64_t>((total + 255) / 256, 65536);
+  pack_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(a);
+}
+
+// ---------------------------------------------------------- test aids
+
+// A wait on a counter nothing signals: must end with ST_TIMEOUT, not hang.
+__global__ void watchdog_probe_kernel(uint32_t* scratch, uint64_t timeout_ns) {
+  __shared__ int32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    // scratch[0] counter (stays 0), scratch[16..20) status words
+    wait_counter(scratch, 1u, scratch + 16, &abort_flag, timeout_ns, blockIdx.x);
+  }
+}
+
+void launch_watchdog_probe(uint32_t* scratch, uint64_t timeout_ns, void* stream) {
+  watchdog_probe_kernel<<<4, 32, 0, (cudaStream_t)stream>>>(scratch, timeout_ns);
+}
+
+// element (r, k) of a HF-layout matrix through the kernel's chunk decoders
+__global__ void dequant_kernel(int fmt, const void* w, const void* scales, const void* zeros,
+                               int rows, int K, float* out) {
+  const int64_t total = (int64_t)rows * (K / 8);
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(idx / (K / 8)), k = (int)(idx % (K / 8)) * 8;
+    float* o = out + (int64_t)r * K + k;
+    if (fmt == AMK_FORMAT_BF16) {
+      const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(w) + (int64_t)r * K + k);
+      o[0] = bf16_lo(v.x); o[1] = bf16_hi(v.x); o[2] = bf16_lo(v.y); o[3] = bf16_hi(v.y);
+      o[4] = bf16_lo(v.z); o[5] = bf16_hi(v.z); o[6] = bf16_lo(v.w); o[7] = bf16_hi(v.w);
+    } else if (fmt == AMK_FORMAT_INT8) {
+      const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const int8_t*>(w) + (int64_t)r * K + k);
+      const float s = fp16_bits_to_float(static_cast<const uint16_t*>(scales)[r]);
+      const uint32_t a = v.x ^ 0x80808080u, b = v.y ^ 0x80808080u;
+      for (int i = 0; i < 4; ++i) o[i] = i8_at(a, i) * s;
+      for (int i = 0; i < 4; ++i) o[4 + i] = i8_at(b, i) * s;
+    } else {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(w) + (int64_t)r * (K / 2) + k / 2);
+      const int ng = K / 128, zb = (ng + 1) / 2, g = k / 128;
+      const float s = fp16_bits_to_float(static_cast<const uint16_t*>(scales)[(int64_t)r * ng + g]);
+      const uint8_t zbyte = static_cast<const uint8_t*>(zeros)[(int64_t)r * zb + g / 2];
+      const float z = (float)((g & 1) ? (zbyte >> 4) : (zbyte & 15));
+      for (int i = 0; i < 8; ++i) o[i] = (u4_at(v, i) - z) * s;
+    }
+  }
+}
+
+void launch_debug_dequant(int fmt, const void* w, const void* scales, const void* zeros,
+                          int rows, int K, float* out, void* stream) {
+  const int64_t total = (int64_t)rows * (K / 8);
+  int blocks = (int)std::min<int64_t>((total + 255) / 256, 65536);
+  if (blocks < 1) blocks = 1;
+  dequant_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(fmt, w, scales, zeros, rows, K, out);
+}
+
+}  // namespace amk

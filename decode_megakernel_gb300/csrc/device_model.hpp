@@ -1,0 +1,95 @@
+// Structures shared by the host library and the persistent decode kernel.
+#pragma once
+
+#include <cstdint>
+
+#include "schedule.hpp"
+
+namespace amk {
+
+// One task of a CTA's queue as the kernel reads it (32 bytes).
+struct alignas(16) DevTask {
+  int16_t type;
+  int16_t layer;
+  int32_t wait_counter;   // -1: no wait
+  uint32_t wait_count;    // producers of wait_counter per step
+  int32_t signal;         // -1: no signal
+  int32_t a0, a1, a2, a3; // GEMV: row blocks [a0, a1), layer-0 QKV x slice [a2, a3)
+                          // ATTN: kv head a0, split a1, completion counter a2
+};
+static_assert(sizeof(DevTask) == 32, "DevTask layout");
+
+// Tiled weight matrix (see MatGeom).  Layer l of a per-layer matrix starts
+// at base + l * layer_bytes; int8 row scales (fp16) of layer l start at
+// scales + l * rows_padded.
+struct DevMat {
+  const uint8_t* base;
+  const uint16_t* scales;
+  int64_t layer_bytes;
+  int64_t rb_bytes;
+  int32_t stage_bytes;    // tile + side bytes copied per stage
+  int32_t fmt, rows, rows_padded, K, Kp, Kt, nkt, Rt, cpr_shift;
+};
+
+struct DevModel {
+  const DevMat* mat;           // [M_NUM] in device memory (indexed by task kind)
+  int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, max_seq;
+  int32_t group, splits, part_stride, num_ctas;
+  float rms_eps;
+  int32_t pad0;
+  const uint16_t* embed;       // bf16 [vocab][hidden], row major
+  const uint16_t* final_norm;  // bf16 [hidden]
+  const uint16_t* attn_norm;   // bf16 [n_layers][hidden]
+  const uint16_t* ffn_norm;    // bf16 [n_layers][hidden]
+  const float2* rope;          // (cos, sin) [max_seq][head_dim / 2]
+  uint16_t* kv;                // bf16 [n_layers][2][n_kv_heads][max_seq][head_dim]
+  float* x;                    // residual stream [hidden]
+  float* q;                    // rotated queries [n_heads * head_dim]
+  float* o;                    // attention output [n_heads * head_dim]
+  float* a;                    // SwiGLU activations [ffn]
+  float* part;                 // attention partials [n_kv_heads][splits][group][head_dim + 2]
+  uint32_t* counters;
+  uint32_t* status;            // [0] code, [1] cta, [2] task, [3] site
+  const DevTask* tasks;        // queue of CTA c: tasks[queue_off[c] .. queue_off[c + 1])
+  const int32_t* queue_off;    // [num_ctas + 1]
+  const int32_t* queue_body;   // [num_ctas]: tasks run when the LM head is skipped
+};
+
+struct StepParams {
+  DevModel m;
+  float* logits;               // [vocab] fp32 output (unused when skip_lm)
+  int32_t token;
+  int32_t pos;
+  uint32_t epoch;              // 1-based launch index: counter targets are epoch * producers
+  int32_t skip_lm;
+  uint64_t timeout_ns;
+};
+
+enum DevStatus : uint32_t {
+  ST_OK = 0, ST_TIMEOUT = 1, ST_CHECK = 2
+};
+enum WaitSite : uint32_t {
+  SITE_COUNTER = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5
+};
+
+// kernel geometry
+constexpr int kConsumerWarps = kConsumerThreads / 32;  // 8
+constexpr int kThreads = kConsumerThreads + 32;        // + one producer warp
+constexpr int kStages = 12;
+constexpr int kSlotBytes = kStageBytes + kSideBytes;   // 17408
+constexpr int kScratchFloats = 4352;                   // GEMV row partials / attention merge
+constexpr int kSmemBytes = kStages * kSlotBytes + kScratchFloats * 4 + 2 * kStages * 8 + 256;
+
+// launch wrappers (decode_kernel.cu)
+int decode_smem_bytes();
+// persistent kernel instance for (layer weight format, LM-head format); null if none
+const void* decode_kernel_for(int fmt, int lm_fmt);
+void launch_pack_matrix(int kind, int fmt, const DevMat& dst, int layer, const void* w0,
+                        const void* s0, const void* z0, const void* w1, const void* s1,
+                        const void* z1, const void* w2, const void* s2, const void* z2,
+                        int n_heads, int n_kv_heads, int head_dim, void* stream);
+void launch_watchdog_probe(uint32_t* scratch, uint64_t timeout_ns, void* stream);
+void launch_debug_dequant(int fmt, const void* w, const void* scales, const void* zeros,
+                          int rows, int K, float* out, void* stream);
+
+}  // namespace amk

@@ -1,0 +1,129 @@
+// Schedule IR of the persistent decode kernel: geometry, builder, validator.
+//
+// The AutoMegaKernel pages describe the schedule as a typed task DAG
+// synchronised by monotonic counters, walked by one threadblock per SM
+// that runs wait -> dispatch -> signal over a local queue (AMK "Layer 0"
+// and "Layer 2"), and a safety gate that rejects a schedule before launch
+// unless the producer/consumer DAG is acyclic, every wait threshold t
+// satisfies 1 <= t <= #producers, the per-SM queue orders are valid,
+// multi-producer counters are joined before a consumer reads their data,
+// memory accesses respect happens-before, and outputs are reachable with
+// referential integrity (AMK "The safety gate").  This file is the
+// host-side half of that design for this kernel.
+//
+// Serialised form (int64 little-endian words), used by amk_build_schedule /
+// amk_validate_serialized and by the tests that build adversarial schedules:
+//   header  [0x414D4B53, version=1, n_tasks, n_counters, n_queues, n_buffers,
+//            n_waits, n_access, n_queue_items]
+//   buffers n_buffers x [size, kind]             kind: 0 scratch, 1 output, 2 state
+//   counters n_counters x [producers_per_step, completion_task or -1]
+//   tasks   n_tasks x [type, layer, queue, wait_begin, wait_count, signal,
+//                      access_begin, access_count, a0, a1, a2, a3]
+//   waits   n_waits x [counter, threshold]
+//   access  n_access x [buffer, lo, hi, write]
+//   queues  n_queues x [item_begin, item_count, body_count]
+//   items   n_queue_items x [task]
+// A task with queue -1 is a completion task: it runs once, on whichever CTA
+// delivers the last signal of the counter naming it as its completion.
+// body_count is the queue prefix that runs when the LM head is skipped
+// (prefill); the remaining items of a queue must be skippable.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/amk.h"
+
+namespace amk {
+
+enum TaskType : int32_t {
+  T_QKV = 0,      // rmsnorm + QKV GEMV + RoPE + KV append
+  T_ATTN = 1,     // split-K GQA attention over one context split of one KV head
+  T_OPROJ = 2,    // O GEMV + residual
+  T_GATEUP = 3,   // rmsnorm + gate/up GEMV + SwiGLU
+  T_DOWN = 4,     // down GEMV + residual
+  T_LMHEAD = 5,   // final rmsnorm + LM-head GEMV
+  T_COMBINE = 6,  // LSE merge of one KV head's attention splits (completion task)
+  T_NUM_TYPES = 7
+};
+
+enum BufKind : int32_t { BUF_SCRATCH = 0, BUF_OUTPUT = 1, BUF_STATE = 2 };
+
+// matrix kinds of the GEMV tasks
+enum MatKind : int32_t { M_QKV = 0, M_O = 1, M_GU = 2, M_DOWN = 3, M_LM = 4, M_NUM = 5 };
+
+struct Wait { int32_t counter; int32_t threshold; };
+struct Access { int32_t buffer; int64_t lo, hi; int32_t write; };
+
+struct Task {
+  int32_t type = 0, layer = 0, queue = -1;
+  std::vector<Wait> waits;
+  int32_t signal = -1;
+  std::vector<Access> acc;
+  int64_t a[4] = {0, 0, 0, 0};
+};
+
+struct Counter { int32_t producers = 0; int32_t completion = -1; };
+struct Buffer { int64_t size = 0; int32_t kind = BUF_SCRATCH; };
+
+struct Schedule {
+  std::vector<Task> tasks;
+  std::vector<Counter> counters;
+  std::vector<std::vector<int32_t>> queues;
+  std::vector<int32_t> body_len;   // per queue
+  std::vector<Buffer> buffers;
+};
+
+// Tiled layout of one weight matrix in the workspace.  Rows are grouped in
+// row blocks of Rt rows; a row block is nkt tiles of [Rt x Kt] elements,
+// each tile one 16 KB TMA stage; in_features is zero-padded to Kp = nkt*Kt.
+struct MatGeom {
+  int32_t fmt = 0;
+  int32_t rows = 0, rows_padded = 0;  // real rows, rows padded to Rt
+  int32_t K = 0, Kp = 0, Kt = 0, nkt = 0, Rt = 0;
+  int32_t cpr_shift = 0;              // log2(Kt / 8): threads sharing one row
+  int64_t tile_bytes = 0;             // code bytes of one tile (16384)
+  int64_t side_bytes = 0;             // per-tile scale/zero bytes (int4)
+  int64_t rb_bytes = 0;               // one row block: nkt * (tile + side)
+  int64_t bytes = 0;                  // whole matrix
+  int32_t n_rb() const { return rows_padded / Rt; }
+};
+
+constexpr int kStageBytes = 16384;
+constexpr int kSideBytes = 1024;
+constexpr int kConsumerThreads = 256;
+constexpr int kRowsMax = 256;
+constexpr int kMaxHReg = 64;        // activation floats a consumer thread keeps in registers
+constexpr int kMaxGroupDim = 512;   // (n_heads / n_kv_heads) * head_dim
+
+struct ModelGeom {
+  amk_config cfg{};
+  MatGeom mat[M_NUM];
+  int32_t num_ctas = 0, splits = 0, group = 0, rows_max = 0;
+  int32_t part_stride = 0;   // floats of one attention partial: group * (head_dim + 2)
+};
+
+struct BuildOptions {
+  int32_t num_ctas = 0;
+  int32_t attn_splits = 0;
+  int32_t max_rows_per_task = 0;
+};
+
+// Shape checks and tile geometry.  Returns AMK_OK or the reason in *why.
+amk_status plan_geometry(const amk_config& cfg, const BuildOptions& opt, ModelGeom* g,
+                         std::string* why);
+
+// Buffers of the per-step scratch the validator reasons about.
+enum BufId : int32_t { B_X = 0, B_Q, B_KVCUR, B_PART, B_O, B_A, B_LOGITS, B_NUM };
+
+// Lower a model to the task DAG (tasks, counters, per-CTA queues, accesses).
+Schedule build_schedule(const ModelGeom& g);
+
+struct Report { bool ok = true; std::string msg; };
+Report validate(const Schedule& s);
+
+std::vector<int64_t> serialize(const Schedule& s);
+bool deserialize(const int64_t* w, size_t n_words, Schedule* out, std::string* why);
+
+}  // namespace amk

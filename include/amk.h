@@ -1,0 +1,212 @@
+/*
+ * amk.h: C ABI of the GB300 batch-1 decode megakernel library (libamk.so).
+ *
+ * The library runs one autoregressive decode step of a Llama-family decoder
+ * at batch 1 (RMSNorm, QKV / O / gate-up / down / LM-head matrix-vector
+ * products, RoPE, GQA attention over a bf16 KV cache, SwiGLU) as ONE
+ * persistent CUDA kernel launch per token on an sm_103a GPU.  This is the
+ * path the AutoMegaKernel pages target ("Problem statement": single-stream
+ * batch-1 decode is bandwidth bound with floor t_min = weight_bytes / HBM
+ * bandwidth; launching one kernel per operator and round-tripping
+ * activations through HBM misses that floor).
+ *
+ * Conventions for every entry point:
+ *   - Device memory is allocated by the caller (for example through
+ *     PyTorch) and only borrowed by the library; the library allocates no
+ *     device memory of its own.  Host memory it owns is freed by amk_free.
+ *   - Pointers named *_dev are device pointers, *_host host pointers.
+ *   - Functions return an amk_status and never abort the process.  Device
+ *     work is stream ordered and asynchronous: failures that happen on the
+ *     device (watchdog timeout, device-side check) are reported by the next
+ *     amk_sync().  After AMK_ERR_TIMEOUT or AMK_ERR_DEVICE_CHECK the context
+ *     is poisoned: every later call returns the same status and the caller
+ *     must amk_free it (and may load a fresh context).
+ *   - Calls on one context must not overlap from several host threads.
+ */
+#ifndef AMK_H
+#define AMK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    AMK_OK = 0,
+    AMK_ERR_INVALID_ARG = 1,       /* a NULL pointer, a size or an index out of range */
+    AMK_ERR_UNSUPPORTED = 2,       /* a model variant the kernel does not implement */
+    AMK_ERR_SCHEDULE_INVALID = 3,  /* the task schedule failed validation: nothing launched */
+    AMK_ERR_CUDA = 4,              /* a CUDA runtime call failed (see amk_last_error) */
+    AMK_ERR_OOM = 5,               /* the caller's workspace is smaller than required */
+    AMK_ERR_TIMEOUT = 6,           /* a device-side wait hit the watchdog; context poisoned */
+    AMK_ERR_DEVICE_CHECK = 7       /* a device-side consistency check failed; context poisoned */
+} amk_status;
+
+enum { AMK_FORMAT_BF16 = 0, AMK_FORMAT_INT8 = 1, AMK_FORMAT_INT4 = 2 };
+
+/*
+ * Model shape (HuggingFace Llama conventions).
+ * Supported (else AMK_ERR_UNSUPPORTED, the analogue of the pages' rejection
+ * of unsupported variants such as biased projections, AMK "Key
+ * contributions" 2): no biases; head_dim 64 or 128; n_heads a multiple of
+ * n_kv_heads with (n_heads / n_kv_heads) * head_dim <= 512; in_features of
+ * every matrix <= 16384 (after padding to the kernel's tile); int4 needs
+ * hidden, n_heads*head_dim and ffn to be multiples of 128.
+ */
+typedef struct {
+    int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+    int32_t max_seq;          /* KV cache capacity in positions */
+    float rms_eps;
+    float rope_theta;         /* rotate-half RoPE base; no frequency scaling */
+    int32_t tied_embeddings;  /* 1: the LM head is the embedding matrix */
+    int32_t weight_format;    /* AMK_FORMAT_* of the 7 per-layer matrices */
+    int32_t lm_head_format;   /* AMK_FORMAT_* of an untied LM head (ignored when tied) */
+} amk_config;
+
+/*
+ * One weight matrix W [out_features][in_features] (nn.Linear layout), device
+ * pointers, in one of three formats:
+ *   BF16: w = bf16 [out][in]; scales = zeros = NULL.
+ *   INT8: w = int8 [out][in]; scales = fp16 [out]; W = q * s_row.
+ *   INT4: w = uint8 [out][in/2], two codes per byte, low nibble = even k;
+ *         scales = fp16 [out][in/128];
+ *         zeros = uint8 [out][ceil(in/256)], two 4-bit zero points per byte,
+ *         low nibble = even group; W = (q - z_group) * s_group.
+ * (int8 / int4 weight-only formats: AMK "Key contributions" 4.)
+ */
+typedef struct {
+    const void* w;
+    const void* scales;
+    const void* zeros;
+} amk_linear;
+
+typedef struct {
+    const void* attn_norm;    /* bf16 [hidden] */
+    const void* ffn_norm;     /* bf16 [hidden] */
+    amk_linear wq, wk, wv, wo, wg, wu, wd;
+} amk_layer_weights;
+
+typedef struct {
+    const void* embed;                 /* bf16 [vocab][hidden] */
+    const void* final_norm;            /* bf16 [hidden] */
+    amk_linear lm_head;                /* ignored when tied_embeddings */
+    const amk_layer_weights* layers;   /* HOST array [n_layers] of device pointers */
+} amk_weights;
+
+/*
+ * Schedule knobs (the pages' ScheduleConfig, AMK "Layer 2": tiling, SM
+ * assignment).  Zero selects the default for every field.
+ */
+typedef struct {
+    int32_t num_ctas;           /* persistent CTAs (default: one per SM) */
+    int32_t attn_splits;        /* context splits per KV head (default: num_ctas / n_kv_heads) */
+    int32_t max_rows_per_task;  /* rows of one GEMV task (default and maximum 256) */
+    int32_t watchdog_ms;        /* device wait limit before AMK_ERR_TIMEOUT (default 2000) */
+    int32_t reserved[4];
+} amk_schedule_config;
+
+typedef struct amk_ctx amk_ctx;
+
+/*
+ * Bytes of device workspace amk_load_weights needs for this model (repacked
+ * weights, activations, task table, counters).  Host only when
+ * sched->num_ctas > 0; otherwise it reads the SM count of the current
+ * device.  Returns 0 for an unsupported or invalid configuration.
+ */
+size_t amk_workspace_bytes(const amk_config* cfg, const amk_schedule_config* sched);
+
+/* Shape check alone (host only): AMK_OK, AMK_ERR_INVALID_ARG or AMK_ERR_UNSUPPORTED. */
+amk_status amk_check_config(const amk_config* cfg);
+
+/* Bytes of the KV cache the caller allocates: bf16 [n_layers][2 (K,V)][n_kv_heads][max_seq][head_dim]. */
+size_t amk_kv_cache_bytes(const amk_config* cfg);
+
+/*
+ * Build, validate and upload the task schedule, then repack the weights into
+ * the workspace (tile-major, RoPE pairs and gate/up rows interleaved).
+ *   workspace_dev  caller-owned, >= amk_workspace_bytes, 256-byte aligned;
+ *   kv_cache_dev   caller-owned, amk_kv_cache_bytes, 16-byte aligned; its
+ *                  content is kept: positions [0, n) become valid through
+ *                  amk_prefill, amk_decode_step or amk_set_kv_length;
+ *   stream         cudaStream_t (NULL = legacy default stream) that every
+ *                  launch of this context is ordered on.
+ * The schedule is checked (acyclic, every wait threshold t with
+ * 1 <= t <= #producers, races, output coverage; AMK "The safety gate")
+ * before anything is launched: a failure returns AMK_ERR_SCHEDULE_INVALID.
+ * Synchronous: on return the caller's weight buffers are no longer needed.
+ */
+amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights,
+                            void* workspace_dev, size_t workspace_bytes, void* kv_cache_dev,
+                            void* stream, const amk_schedule_config* sched, amk_ctx** out);
+
+/*
+ * n decode steps of host_tokens at positions start_pos.. with the LM head
+ * skipped: fills the KV cache.  start_pos must be <= the valid KV length and
+ * start_pos + n <= max_seq.  Asynchronous (one launch per token).
+ */
+amk_status amk_prefill(amk_ctx* ctx, const int32_t* host_tokens, int32_t n, int32_t start_pos);
+
+/*
+ * One decode step: token at position pos (0 <= pos <= valid KV length,
+ * pos < max_seq; a smaller pos rolls the context back) writes K,V of pos
+ * into the cache and fp32 logits [vocab] into logits_dev.  One persistent
+ * kernel launch; asynchronous.
+ */
+amk_status amk_decode_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_dev);
+
+/* The same step with the logits copied to host memory (pinned memory is
+ * fastest); waits for the step to finish and reports device failures. */
+amk_status amk_decode_step_host(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_host);
+
+/* Declare KV positions [0, n) valid (a cache filled by the caller). */
+amk_status amk_set_kv_length(amk_ctx* ctx, int32_t n);
+int32_t amk_kv_length(const amk_ctx* ctx);
+
+/* Wait for the context's stream and report device-side failures. */
+amk_status amk_sync(amk_ctx* ctx);
+
+/* Release host state.  Does not free caller memory.  NULL is accepted. */
+void amk_free(amk_ctx* ctx);
+
+const char* amk_status_string(amk_status s);
+/* Last error message of a context, or of the most recent failing call on this thread when ctx is NULL. */
+const char* amk_last_error(const amk_ctx* ctx);
+
+/*
+ * Schedule introspection (host only).  amk_build_schedule lowers a config
+ * to the task DAG the kernel would run (AMK "Layer 2": a typed Schedule IR
+ * synchronised by monotonic counters) and serialises it as int64 words
+ * into buf (cap bytes); *needed receives the size.  The format is
+ * documented in decode_megakernel_gb300/csrc/schedule.hpp.
+ * amk_validate_serialized runs the safety gate on such a buffer (which may
+ * come from anywhere) and writes a one-line report; AMK_OK means accepted.
+ */
+amk_status amk_build_schedule(const amk_config* cfg, const amk_schedule_config* sched,
+                              void* buf, size_t cap, size_t* needed);
+amk_status amk_validate_serialized(const void* buf, size_t bytes, char* report, size_t cap);
+
+/*
+ * Watchdog probe (test aid): launches a small grid of the decode kernel's
+ * bounded wait on a counter that nothing ever signals, with the given
+ * limit, and returns the status the device reported (expected
+ * AMK_ERR_TIMEOUT) in *device_status.  scratch_dev: >= 256 bytes of
+ * caller device memory.  Nothing hangs: every wait is time bounded.
+ */
+amk_status amk_debug_watchdog_probe(void* scratch_dev, void* stream, int32_t limit_us,
+                                    int32_t* device_status);
+
+/*
+ * Dequantisation check (test aid): writes the fp32 values the kernel's
+ * weight decoder produces for matrix `lin` of the given format and shape
+ * into out_dev [out_features][in_features].  Used to check that int8 / int4
+ * decoding is bit exact.
+ */
+amk_status amk_debug_dequant(int32_t format, const amk_linear* lin, int32_t out_features,
+                             int32_t in_features, float* out_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -66,6 +66,12 @@ def lib():
         L.orc_decode_step.restype = C.c_int
         L.orc_decode_step.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights), C.c_void_p,
                                       C.c_int32, C.c_int64, dp]
+        L.orc_decode_layers.restype = C.c_int
+        L.orc_decode_layers.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights), C.c_void_p,
+                                        dp, C.c_int64, C.c_int32, C.c_int32]
+        L.orc_logits_rows.restype = C.c_int
+        L.orc_logits_rows.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights), dp, dp,
+                                      C.c_int64, C.c_int64]
         L.orc_prefill.restype = C.c_int
         L.orc_prefill.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights), C.c_void_p,
                                   C.POINTER(C.c_int32), C.c_int64, C.c_int64]
@@ -205,6 +211,27 @@ class OracleModel:
                                    _dp(out) if logits else None)
         if rc != 0:
             raise ValueError("oracle decode step rejected its arguments")
+        return out
+
+    def embed(self, token: int) -> np.ndarray:
+        return self._w.embed[int(token)].double().numpy().copy()
+
+    def decode_layers(self, kv: torch.Tensor, x: np.ndarray, pos: int, l0: int, l1: int):
+        """Layers [l0, l1) of a decode step, in place on the residual x."""
+        self._check_kv(kv)
+        assert x.dtype == np.float64 and x.flags["C_CONTIGUOUS"] and x.size == self.cfg.hidden
+        rc = lib().orc_decode_layers(C.byref(self._cfg), C.byref(self._weights),
+                                     C.c_void_p(kv.data_ptr()), _dp(x), int(pos), int(l0), int(l1))
+        if rc != 0:
+            raise ValueError("oracle decode_layers rejected its arguments")
+
+    def logits_rows(self, x: np.ndarray, r0: int, r1: int, out: np.ndarray | None = None):
+        """Final norm + LM-head rows [r0, r1) (written into out[r0:r1])."""
+        out = np.zeros(self.cfg.vocab, dtype=np.float64) if out is None else out
+        rc = lib().orc_logits_rows(C.byref(self._cfg), C.byref(self._weights), _dp(x), _dp(out),
+                                   int(r0), int(r1))
+        if rc != 0:
+            raise ValueError("oracle logits_rows rejected its arguments")
         return out
 
     def prefill(self, kv: torch.Tensor, tokens, start_pos: int = 0):

@@ -214,17 +214,16 @@ static int check_config(const orc_config* c) {
     return 0;
 }
 
-int orc_decode_step(const orc_config* c, const orc_weights* w, uint16_t* kv,
-                    int32_t token, int64_t pos, double* logits) {
-    if (check_config(c) || !w || !kv) return -1;
-    if (token < 0 || token >= c->vocab || pos < 0 || pos >= c->max_seq) return -1;
+int orc_decode_layers(const orc_config* c, const orc_weights* w, uint16_t* kv, double* x,
+                      int64_t pos, int32_t l0, int32_t l1) {
+    if (check_config(c) || !w || !kv || !x) return -1;
+    if (pos < 0 || pos >= c->max_seq || l0 < 0 || l1 > c->n_layers || l0 > l1) return -1;
 
     const int64_t H = c->hidden, F = c->ffn, hd = c->head_dim;
     const int64_t qd = (int64_t)c->n_heads * hd, kvd = (int64_t)c->n_kv_heads * hd;
     const int64_t layer_stride = 2 * kvd * c->max_seq;     /* bf16 elements per layer */
     const int64_t kv_half = kvd * c->max_seq;              /* K block, then V block */
 
-    double* x = (double*)malloc(sizeof(double) * H);
     double* hn = (double*)malloc(sizeof(double) * H);
     double* q = (double*)malloc(sizeof(double) * qd);
     double* kk = (double*)malloc(sizeof(double) * kvd);
@@ -234,10 +233,7 @@ int orc_decode_step(const orc_config* c, const orc_weights* w, uint16_t* kv,
     double* g = (double*)malloc(sizeof(double) * F);
     double* u = (double*)malloc(sizeof(double) * F);
 
-    /* x = embedding row of the token */
-    for (int64_t i = 0; i < H; ++i) x[i] = orc_bf16_to_double(w->embed[(int64_t)token * H + i]);
-
-    for (int32_t l = 0; l < c->n_layers; ++l) {
+    for (int32_t l = l0; l < l1; ++l) {
         const orc_layer* L = &w->layers[l];
         uint16_t* kc = kv + l * layer_stride;
         uint16_t* vc = kc + kv_half;
@@ -266,14 +262,45 @@ int orc_decode_step(const orc_config* c, const orc_weights* w, uint16_t* kv,
         orc_linear_apply(&L->wd, H, F, g, y);
         for (int64_t i = 0; i < H; ++i) x[i] += y[i];
     }
-
-    if (logits) {
-        orc_rmsnorm(x, w->final_norm, H, c->rms_eps, hn);
-        orc_linear_apply(&w->lm_head, c->vocab, H, hn, logits);
-    }
-
-    free(x); free(hn); free(q); free(kk); free(vv); free(o); free(y); free(g); free(u);
+    free(hn); free(q); free(kk); free(vv); free(o); free(y); free(g); free(u);
     return 0;
+}
+
+int orc_logits_rows(const orc_config* c, const orc_weights* w, const double* x, double* logits,
+                    int64_t r0, int64_t r1) {
+    if (check_config(c) || !w || !x || !logits || r0 < 0 || r1 > c->vocab || r0 > r1) return -1;
+    const int64_t H = c->hidden;
+    double* hn = (double*)malloc(sizeof(double) * H);
+    orc_rmsnorm(x, w->final_norm, H, c->rms_eps, hn);
+    /* rows r0.. of the LM head are the linear map whose row 0 is row r0 */
+    orc_linear lm = w->lm_head;
+    if (lm.format == ORC_BF16) {
+        lm.w = (const uint16_t*)lm.w + r0 * H;
+    } else if (lm.format == ORC_INT8) {
+        lm.w = (const int8_t*)lm.w + r0 * H;
+        lm.scales += r0;
+    } else {
+        lm.w = (const uint8_t*)lm.w + r0 * (H / 2);
+        lm.scales += r0 * (H / 128);
+        lm.zeros += r0 * ((H / 128 + 1) / 2);
+    }
+    orc_linear_apply(&lm, r1 - r0, H, hn, logits + r0);
+    free(hn);
+    return 0;
+}
+
+int orc_decode_step(const orc_config* c, const orc_weights* w, uint16_t* kv,
+                    int32_t token, int64_t pos, double* logits) {
+    if (check_config(c) || !w || !kv) return -1;
+    if (token < 0 || token >= c->vocab || pos < 0 || pos >= c->max_seq) return -1;
+    const int64_t H = c->hidden;
+    double* x = (double*)malloc(sizeof(double) * H);
+    /* x = embedding row of the token */
+    for (int64_t i = 0; i < H; ++i) x[i] = orc_bf16_to_double(w->embed[(int64_t)token * H + i]);
+    int rc = orc_decode_layers(c, w, kv, x, pos, 0, c->n_layers);
+    if (rc == 0 && logits) rc = orc_logits_rows(c, w, x, logits, 0, c->vocab);
+    free(x);
+    return rc;
 }
 
 int orc_prefill(const orc_config* c, const orc_weights* w, uint16_t* kv,

@@ -103,6 +103,16 @@ void orc_attention(const double* q, const uint16_t* k, const uint16_t* v,
 int orc_decode_step(const orc_config* cfg, const orc_weights* w, uint16_t* kv,
                     int32_t token, int64_t pos, double* logits);
 
+/* The two halves of a decode step, for bounded timing samples:
+ * layers [l0, l1) applied in place to the residual x [hidden] at position
+ * pos (writing their K,V of pos), and the final norm + LM-head rows
+ * [r0, r1) of the vocabulary from the residual.  orc_decode_step is
+ * embedding -> orc_decode_layers(0, n_layers) -> orc_logits_rows(0, vocab). */
+int orc_decode_layers(const orc_config* cfg, const orc_weights* w, uint16_t* kv, double* x,
+                      int64_t pos, int32_t l0, int32_t l1);
+int orc_logits_rows(const orc_config* cfg, const orc_weights* w, const double* x,
+                    double* logits, int64_t r0, int64_t r1);
+
 /* n decode steps at positions start_pos.. without logits (fills the cache) */
 int orc_prefill(const orc_config* cfg, const orc_weights* w, uint16_t* kv,
                 const int32_t* tokens, int64_t n, int64_t start_pos);

@@ -1,0 +1,104 @@
+"""The C ABI: the library loads, exports every declared entry point, and its
+host-side argument checks answer without touching a GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from workload import configs as wc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def amk():
+    from decode_megakernel_gb300 import build
+    build.build()
+    from decode_megakernel_gb300 import amk as m
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "amk.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = set(re.findall(r"\b(amk_[a-z_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(amk):
+    names = declared_functions()
+    assert len(names) >= 17
+    lib = C.CDLL(amk.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(amk):
+    for s in range(8):
+        assert amk.status_string(s) and amk.status_string(s) != "unknown status"
+    assert amk.status_string(99) == "unknown status"
+
+
+def cfg_of(amk, **over):
+    base = dict(wc.TINY.__dict__)
+    base.update(over)
+    return amk.make_config(wc.ModelConfig(**base), 64)
+
+
+@pytest.mark.parametrize("over,expect", [
+    ({}, 0),
+    (dict(head_dim=96, hidden=384), 2),
+    (dict(n_kv_heads=3), 2),
+    (dict(n_heads=16, n_kv_heads=1), 2),     # group * head_dim = 1024 > 512
+    (dict(weight_format="int4"), 2),         # ffn 688 is not a multiple of 128
+    (dict(weight_format="int4", ffn=768), 0),
+    (dict(weight_format="int8"), 0),
+    (dict(ffn=30000), 2),                    # in_features beyond register-resident tiles
+])
+def test_check_config(amk, over, expect):
+    assert amk.amk_check_config(cfg_of(amk, **over)) == expect
+
+
+def test_check_config_invalid(amk):
+    c = cfg_of(amk)
+    c.n_layers = 0
+    assert amk.amk_check_config(c) == amk.AMK_ERR_INVALID_ARG
+    c = cfg_of(amk)
+    c.weight_format = 7
+    assert amk.amk_check_config(c) == amk.AMK_ERR_INVALID_ARG
+
+
+def test_sizes(amk):
+    c = amk.make_config(wc.LLAMA_8B_BF16, 2176)
+    assert amk.amk_kv_cache_bytes(c) == 32 * 2 * 8 * 2176 * 128 * 2
+    sc = amk.make_schedule_config(num_ctas=152)
+    ws = amk.amk_workspace_bytes(c, sc)
+    # the tiled weights dominate: at least the model's bytes
+    assert ws >= wc.weight_bytes_per_token(wc.LLAMA_8B_BF16)
+    assert ws < 1.1 * wc.weight_bytes_per_token(wc.LLAMA_8B_BF16) + c.vocab * c.hidden * 2
+    bad = cfg_of(amk, head_dim=96, hidden=384)
+    assert amk.amk_workspace_bytes(bad, sc) == 0
+
+
+def test_host_argument_checks_need_no_gpu(amk):
+    c = cfg_of(amk)
+    st, ctx = amk.amk_load_weights(c, amk.amk_weights(), 0, 0, 0, 0)
+    assert st == amk.AMK_ERR_INVALID_ARG and not ctx.value
+    assert amk.lib.amk_decode_step(None, 0, 0, None) == amk.AMK_ERR_INVALID_ARG
+    assert amk.lib.amk_prefill(None, None, 0, 0) == amk.AMK_ERR_INVALID_ARG
+    assert amk.lib.amk_sync(None) == amk.AMK_ERR_INVALID_ARG
+    assert amk.lib.amk_set_kv_length(None, 0) == amk.AMK_ERR_INVALID_ARG
+    assert amk.lib.amk_kv_length(None) == -1
+    amk.amk_free(None)
+    st, _ = amk.amk_debug_watchdog_probe(0, 0, 100)
+    assert st == amk.AMK_ERR_INVALID_ARG
+    assert amk.amk_debug_dequant(9, 1, 1, 1, 4, 8, 1, 0) == amk.AMK_ERR_INVALID_ARG
+    assert "NULL" in amk.last_error() or amk.last_error()
+
+
+def test_validate_rejects_garbage(amk):
+    st, rep = amk.amk_validate_serialized(b"\x00" * 80)
+    assert st == amk.AMK_ERR_SCHEDULE_INVALID and "malformed" in rep
+    st, rep = amk.amk_validate_serialized(b"\x01" * 7)
+    assert st == amk.AMK_ERR_INVALID_ARG

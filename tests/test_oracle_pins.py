@@ -446,3 +446,21 @@ def test_prefill_equals_sequential_steps_and_leaves_tail(oracle):
         m.decode_step(kv2, t, p, logits=False)
     assert np.array_equal(bf16_bits(kv1), bf16_bits(kv2))
     assert not kv1[:, :, :, len(toks):].float().abs().sum().item()
+
+
+def test_decode_step_is_layers_then_logits(oracle):
+    """The sampled halves compose to the full step exactly (same arithmetic)."""
+    for cfg in (wc.TINY, wc.ModelConfig(**{**wc.TINY.__dict__, "weight_format": "int4", "ffn": 768}),
+                wc.ModelConfig(**{**wc.TINY.__dict__, "weight_format": "int8"})):
+        w = synth.model_weights(cfg, seed=8)
+        m = oracle.OracleModel(w, 6)
+        kv1, kv2 = synth.empty_kv_cache(cfg, 6), synth.empty_kv_cache(cfg, 6)
+        for pos, tok in enumerate([11, 500, 7]):
+            full = m.decode_step(kv1, tok, pos)
+            x = m.embed(tok)
+            m.decode_layers(kv2, x, pos, 0, 1)
+            m.decode_layers(kv2, x, pos, 1, cfg.n_layers)
+            part = m.logits_rows(x, 0, 300)
+            m.logits_rows(x, 300, cfg.vocab, part)
+            assert np.array_equal(full, part)
+        assert np.array_equal(bf16_bits(kv1), bf16_bits(kv2))
