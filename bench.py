@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Batch-1 decode benchmark: tok/s and fraction of the weight+KV-bytes
+HBM roofline, on one of the five synthetic workloads.
+
+A step is one decode step of the whole model (every layer, attention over
+the KV cache, LM head) for one token: one persistent kernel launch through
+the C ABI.  Default workload: the Llama-3.1-8B-shaped bf16 model with the
+KV cache prefilled to 2048 random tokens; the timed steps cycle over the
+128 positions 2048..2175 with teacher-forced random tokens.
+
+Legs:
+  value         device time (CUDA events on the decode stream), inputs
+                resident in HBM; the 15 GB of weights per step exceed L2,
+                so no flush is needed between steps.
+  e2e           the same steps through amk_decode_step_host: token and
+                position go host->device as launch parameters, logits
+                come back into pinned host memory, timed on the host.
+  roofline      algorithmic bytes of each step (weights + KV read at
+                context pos+1) over the measured launch duration, against
+                the measured HBM copy bandwidth.
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same step
+                (one layer plus 1/L of the LM-head rows per sample).
+--impl reference times the oracle alone (the only other implementation).
+Multi-GPU: independent replicas, one per rank (the path does not shard).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tok/s (Llama-8B-shape bf16); % of weight+KV bytes/HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ["decode_kernel.cu", "device_model.hpp", "schedule.cpp", "schedule.hpp"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b-bf16")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="default: --steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--num-ctas", type=int, default=0)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "decode_megakernel_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(PROFILE_DIR, f"decode_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_sources_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(float(fields["traffic_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(dev) -> str:
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(dev).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return str(dev.index or 0)
+
+
+def reduce_over_ranks(local_ms: float, local_units: float, group=None):
+    """(max time, summed units) over ranks; identity when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return local_ms, local_units
+    backend = dist.get_backend(group)
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------ cpu oracle leg
+
+def oracle_sample(weights_cpu, kv_cpu, pos: int, token: int, n_samples: int | None,
+                  seconds: float | None, warmup: int = 0):
+    """Time the oracle on samples of one decode step: sample i runs layer
+    i mod L and LM-head rows of slice i mod L (1/L of the vocabulary).
+    Returns (samples timed, seconds, cores)."""
+    from oracle import binding as orc
+    cfg = weights_cpu.cfg
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    orc.set_threads(cores)
+    om = orc.OracleModel(weights_cpu, kv_cpu.shape[3])
+    L, V = cfg.n_layers, cfg.vocab
+    x = om.embed(token)
+    logits = None
+
+    def one(i):
+        nonlocal logits
+        layer = i % L
+        om.decode_layers(kv_cpu, x, pos, layer, layer + 1)
+        r0, r1 = layer * V // L, (layer + 1) * V // L
+        logits = om.logits_rows(x, r0, r1, logits)
+
+    for i in range(warmup):
+        one(i)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        one(warmup + n)
+        n += 1
+        el = time.perf_counter() - t0
+        if n_samples is not None and n >= n_samples:
+            break
+        if seconds is not None and el >= seconds and n >= 1:
+            break
+    return n, time.perf_counter() - t0, cores
+
+
+def host_weights_and_kv(wl, dev):
+    import torch
+    from workload import synth
+    cfg = wl.model
+    gen_dev = dev if dev is not None else torch.device("cpu")
+    w = synth.model_weights(cfg, seed=synth.WEIGHT_SEED, device=gen_dev)
+    w_cpu = w.to("cpu") if gen_dev.type != "cpu" else w
+    del w
+    kv = synth.synthetic_kv_cache(cfg, wl.prompt_len, wl.prompt_len + 1, device="cpu")
+    return w_cpu, kv
+
+
+def cpu_sample_desc(wl, n):
+    return (f"{n} oracle samples of the {wl.name} decode step at position {wl.prompt_len} "
+            f"(each: one transformer layer + 1/{wl.model.n_layers} of the LM-head rows, fp64, "
+            f"synthetic KV history of {wl.prompt_len} positions) = {n / wl.model.n_layers:.3f} tokens")
+
+
+# ----------------------------------------------------------------- arms
+
+def config_block(wl, args, num_ctas):
+    return {
+        "workload": wl.name,
+        "model": wl.description,
+        "weights_dtype": wl.model.weight_format,
+        "global_batch": 1,
+        "seq_len": wl.prompt_len,
+        "kv_positions_timed": f"{wl.prompt_len}..{wl.prompt_len + wl.decode_steps - 1} (cyclic)",
+        "parallelism": "replicas" if args.gpus > 1 else "single",
+        "persistent_ctas": num_ctas,
+        "l2": "no flush: every step streams the weights (> L2 capacity)",
+    }
+
+
+def run_reference(args, wl, rank, world):
+    import torch
+    if rank != 0:
+        return None
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    from workload import synth
+    w_cpu, kv = host_weights_and_kv(wl, dev)
+    tok = int(synth.decode_tokens(wl.model, 1)[0])
+    n, secs, cores = oracle_sample(w_cpu, kv, wl.prompt_len, tok, n_samples=args.steps, seconds=None,
+                                   warmup=args.warmup)
+    tokens = n / wl.model.n_layers
+    value = tokens / secs
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs * 1e3 / n, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(wl, args, 0),
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": cpu_sample_desc(wl, n)},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    from workload import configs as wc
+    from workload import synth
+
+    __graft_entry__.build()
+    from decode_megakernel_gb300 import amk
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = wl.model
+    P, D = wl.prompt_len, wl.decode_steps
+    max_seq = wl.max_seq
+    stream = torch.cuda.Stream(device=dev)
+    sched = amk.make_schedule_config(num_ctas=args.num_ctas)
+
+    weights = synth.model_weights(cfg, seed=synth.WEIGHT_SEED, device=dev)
+    dec = amk.Decoder(weights, max_seq, stream=stream, sched=sched)
+    num_ctas = args.num_ctas or torch.cuda.get_device_properties(dev).multi_processor_count
+    del weights
+    torch.cuda.empty_cache()
+    prompt = synth.prompt_tokens(cfg, P).tolist()
+    toks = synth.decode_tokens(cfg, D).tolist()
+    dec.prefill(prompt, 0)
+    dec.sync()
+
+    logits = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+    pos_of = lambda i: P + (i % D)  # noqa: E731
+    sampler = ClockSampler(gpu_id_for(dev))
+    for i in range(args.warmup):
+        dec.decode_step(toks[i % D], pos_of(i), logits)
+    dec.sync()
+
+    K = args.steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(K):
+            j = args.warmup + i
+            dec.decode_step(toks[j % D], pos_of(j), logits)
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    dec.sync()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
+    total_ms = evs[0].elapsed_time(evs[K])
+    max_ms, units = reduce_over_ranks(total_ms, float(K))
+    value = units / (max_ms / 1e3)
+
+    # roofline of the decode kernel (the whole step is this one kernel)
+    positions = [pos_of(args.warmup + i) for i in range(K)]
+    mean_bytes = sum(wc.step_bytes(cfg, p) for p in positions) / K
+    mean_launch_s = (sum(per) / K) / 1e3
+    achieved = mean_bytes / mean_launch_s / 1e9
+    peak, peak_src = measured_peak_gbs()
+
+    # end to end through the host-buffer entry point
+    n_e2e = args.e2e_steps or K
+    host_logits = torch.empty(cfg.vocab, dtype=torch.float32, pin_memory=True)
+    for i in range(min(3, n_e2e)):
+        dec.decode_step_host(toks[i % D], pos_of(i), host_logits)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        dec.decode_step_host(toks[i % D], pos_of(i), host_logits)
+    e2e_s = time.perf_counter() - t0
+    e2e_max_ms, e2e_units = reduce_over_ranks(e2e_s * 1e3, float(n_e2e))
+    e2e_value = e2e_units / (e2e_max_ms / 1e3)
+    assert np.isfinite(host_logits.numpy()).all()
+    dec.close()
+    del dec
+    torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(wl, args, num_ctas),
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
+                     "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "algorithmic_bytes_per_launch": mean_bytes,
+                     "mean_launch_ms": mean_launch_s * 1e3,
+                     "launch_ms_p10_p50_p90": [float(np.percentile(per, q)) for q in (10, 50, 90)]},
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 8,
+                "d2h_bytes_per_step": cfg.vocab * 4},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w_cpu, kv = host_weights_and_kv(wl, dev)
+        n, secs, cores = oracle_sample(w_cpu, kv, P, toks[0], n_samples=None, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": (n / cfg.n_layers) / secs, "unit": "tok/s", "cores": cores,
+                                "kind": "oracle", "sample": cpu_sample_desc(wl, n)}
+    return line if rank == 0 else None
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from workload import configs as wc
+    wl = wc.workload(args.workload)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+            world_eff = 1
+        else:
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+            world_eff = world
+    else:
+        world_eff = 1
+    if args.impl == "reference":
+        line = run_reference(args, wl, rank, world_eff)
+    else:
+        line = run_ours(args, wl, rank, world_eff, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
