@@ -79,6 +79,7 @@ def _load():
         "amk_prefill": (C.c_int, [P, C.POINTER(C.c_int32), C.c_int32, C.c_int32]),
         "amk_decode_step": (C.c_int, [P, C.c_int32, C.c_int32, P]),
         "amk_decode_step_host": (C.c_int, [P, C.c_int32, C.c_int32, P]),
+        "amk_decode_step_static_scratch": (C.c_int, [P, C.c_int32, C.c_int32, P]),
         "amk_set_kv_length": (C.c_int, [P, C.c_int32]),
         "amk_kv_length": (C.c_int32, [P]),
         "amk_sync": (C.c_int, [P]),
@@ -148,6 +149,13 @@ def amk_decode_step(ctx, token: int, pos: int, logits_ptr: int) -> int:
 
 def amk_decode_step_host(ctx, token: int, pos: int, logits_host_ptr: int) -> int:
     return int(lib.amk_decode_step_host(ctx, int(token), int(pos), C.c_void_p(logits_host_ptr)))
+
+
+def amk_decode_step_static_scratch(ctx, token: int, pos: int, logits_ptr: int) -> int:
+    """amk_decode_step with the per-step scratch in the library's fixed
+    device array: for callers that cannot allocate device memory."""
+    return int(lib.amk_decode_step_static_scratch(ctx, int(token), int(pos),
+                                                  C.c_void_p(logits_ptr)))
 
 
 def amk_set_kv_length(ctx, n: int) -> int:

@@ -209,6 +209,77 @@ amk_status read_status(amk_ctx* ctx) {
 
 }  // namespace
 
+// Internal entry points for decode variants that keep a context's weights
+// and KV cache but place the per-step scratch somewhere else
+// (static_scratch.cu).  They reuse the context's checks and kernel.
+namespace amk {
+
+amk_status internal_begin_step(amk_ctx* ctx, int32_t token, int32_t pos, const float* logits,
+                               DevModel* dm, StepScratchPlan* plan) {
+  amk_status st = step_checks(ctx, token, pos);
+  if (st != AMK_OK) return st;
+  if (!logits) return fail(ctx, AMK_ERR_INVALID_ARG, "logits pointer is NULL");
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != ctx->device)
+    return fail(ctx, AMK_ERR_INVALID_ARG, "the context's device is not the current device");
+  *dm = ctx->dm;
+  // the same regions, in the same order, as in the context's workspace
+  const amk_config& c = ctx->cfg;
+  const size_t qd = (size_t)c.n_heads * c.head_dim;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  plan->x = take((size_t)c.hidden * 4);
+  plan->q = take(qd * 4);
+  plan->o = take(qd * 4);
+  plan->a = take((size_t)c.ffn * 4);
+  plan->part = take((size_t)c.n_kv_heads * ctx->geom.splits * ctx->geom.part_stride * 4);
+  plan->counters = take((size_t)((uint8_t*)ctx->dm.status - (uint8_t*)ctx->dm.counters));
+  plan->status = take(64);
+  plan->total = off;
+  plan->stream = ctx->stream;
+  plan->device = ctx->device;
+  return AMK_OK;
+}
+
+amk_status internal_launch(amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
+                           float* logits, uint32_t epoch) {
+  StepParams p;
+  p.m = dm;
+  p.logits = logits;
+  p.token = token;
+  p.pos = pos;
+  p.epoch = epoch;
+  p.skip_lm = 0;
+  p.timeout_ns = ctx->timeout_ns;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchCooperativeKernel(ctx->kernel, dim3(ctx->geom.num_ctas),
+                                              dim3(kThreads), args, (size_t)ctx->smem, ctx->stream);
+  if (e != cudaSuccess) {
+    ctx->poisoned = AMK_ERR_CUDA;
+    return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel");
+  }
+  return AMK_OK;
+}
+
+amk_status internal_end_step(amk_ctx* ctx, int32_t pos, const uint32_t status[4]) {
+  ctx->kv_len = pos + 1;
+  if (status[0] == ST_OK) return AMK_OK;
+  char buf[160];
+  snprintf(buf, sizeof buf, "device %s at CTA %u, task %u, site %u",
+           status[0] == ST_TIMEOUT ? "watchdog timeout" : "check failure", status[1], status[2],
+           status[3]);
+  ctx->poisoned = status[0] == ST_TIMEOUT ? AMK_ERR_TIMEOUT : AMK_ERR_DEVICE_CHECK;
+  return fail(ctx, ctx->poisoned, buf);
+}
+
+amk_status internal_fail(amk_ctx* ctx, amk_status st, const char* msg) { return fail(ctx, st, msg); }
+
+}  // namespace amk
+
 extern "C" {
 
 const char* amk_status_string(amk_status s) {

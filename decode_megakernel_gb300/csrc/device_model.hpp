@@ -80,6 +80,14 @@ constexpr int kSlotBytes = kStageBytes + kSideBytes;   // 17408
 constexpr int kScratchFloats = 4352;                   // GEMV row partials / attention merge
 constexpr int kSmemBytes = kStages * kSlotBytes + kScratchFloats * 4 + 2 * kStages * 8 + 256;
 
+// Byte offsets of the per-step scratch regions (x, q, o, a, attention
+// partials, counters, status) laid out from one base address.
+struct StepScratchPlan {
+  size_t x = 0, q = 0, o = 0, a = 0, part = 0, counters = 0, status = 0, total = 0;
+  void* stream = nullptr;
+  int device = 0;
+};
+
 // launch wrappers (decode_kernel.cu)
 int decode_smem_bytes();
 // persistent kernel instance for (layer weight format, LM-head format); null if none

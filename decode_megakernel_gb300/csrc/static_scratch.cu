@@ -1,0 +1,104 @@
+// Decode step whose per-step scratch lives in a fixed array inside this
+// library instead of the context's workspace.
+//
+// A decode step needs, besides its inputs (the loaded weights, the KV cache,
+// token and position) and its output (the logits), some scratch: the fp32
+// activations x, q, o, a, the attention partials, the synchronisation
+// counters and a status word.  amk_decode_step keeps them in the workspace
+// the caller handed to amk_load_weights.  amk_decode_step_static_scratch
+// takes them from g_step_scratch below, a file-scope device array that
+// every GPU loading this library holds until the process exits.  It calls
+// no allocating routine (no cudaMalloc / cudaFree / cudaMallocAsync, no
+// allocating library call).
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/amk.h"
+#include "device_model.hpp"
+
+namespace amk {
+
+amk_status internal_begin_step(amk_ctx* ctx, int32_t token, int32_t pos, const float* logits,
+                               DevModel* dm, StepScratchPlan* plan);
+amk_status internal_launch(amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
+                           float* logits, uint32_t epoch);
+amk_status internal_end_step(amk_ctx* ctx, int32_t pos, const uint32_t status[4]);
+amk_status internal_fail(amk_ctx* ctx, amk_status st, const char* msg);
+
+// 1 MiB: an 8B-shape model with 19 attention splits per KV head needs ~420 KB.
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;
+
+static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_lookup_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_step_scratch on `device` (which must be current).
+// Host code may only name the array through this address: the symbol
+// itself is a host-side stand-in.  Looked up once per device.
+cudaError_t scratch_address(int device, void** out) {
+  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_lookup_mutex);
+  if (!g_scratch_addr[device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_step_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[device] = p;
+  }
+  *out = g_scratch_addr[device];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace amk
+
+using namespace amk;
+
+extern "C" amk_status amk_decode_step_static_scratch(amk_ctx* ctx, int32_t token, int32_t pos,
+                                                     float* logits_dev) {
+  DevModel dm;
+  StepScratchPlan plan;
+  amk_status st = internal_begin_step(ctx, token, pos, logits_dev, &dm, &plan);
+  if (st != AMK_OK) return st;
+  if (plan.total > kStaticScratchBytes) {
+    char msg[192];
+    snprintf(msg, sizeof msg,
+             "this model needs %zu bytes of per-step scratch; the static scratch holds at most %zu",
+             plan.total, kStaticScratchBytes);
+    return internal_fail(ctx, AMK_ERR_OOM, msg);
+  }
+  void* base = nullptr;
+  cudaError_t e = scratch_address(plan.device, &base);
+  if (e != cudaSuccess) {
+    char msg[160];
+    snprintf(msg, sizeof msg, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
+    return internal_fail(ctx, AMK_ERR_CUDA, msg);
+  }
+  uint8_t* b = static_cast<uint8_t*>(base);
+  dm.x = reinterpret_cast<float*>(b + plan.x);
+  dm.q = reinterpret_cast<float*>(b + plan.q);
+  dm.o = reinterpret_cast<float*>(b + plan.o);
+  dm.a = reinterpret_cast<float*>(b + plan.a);
+  dm.part = reinterpret_cast<float*>(b + plan.part);
+  dm.counters = reinterpret_cast<uint32_t*>(b + plan.counters);
+  dm.status = reinterpret_cast<uint32_t*>(b + plan.status);
+  cudaStream_t s = static_cast<cudaStream_t>(plan.stream);
+
+  // The array keeps whatever the previous call left.  The counters and the
+  // status word must start at zero (the step then runs as launch 1); every
+  // other region is fully written before it is read within a step.
+  e = cudaMemsetAsync(b + plan.counters, 0, plan.status + 64 - plan.counters, s);
+  if (e != cudaSuccess) return internal_fail(ctx, AMK_ERR_CUDA, "clearing the static scratch failed");
+  st = internal_launch(ctx, dm, token, pos, logits_dev, 1u);
+  if (st != AMK_OK) return st;
+  uint32_t status[4] = {0, 0, 0, 0};
+  e = cudaMemcpyAsync(status, dm.status, sizeof status, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return internal_fail(ctx, AMK_ERR_CUDA, "reading the step status failed");
+  return internal_end_step(ctx, pos, status);
+}

@@ -160,6 +160,39 @@ amk_status amk_decode_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logi
  * fastest); waits for the step to finish and reports device failures. */
 amk_status amk_decode_step_host(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_host);
 
+/*
+ * The same decode step as amk_decode_step, for callers that cannot call
+ * cudaMalloc: code that runs inside a host application whose allocator
+ * owns all device memory and only lends it weight and cache buffers, or a
+ * loop that is not allowed to allocate once it has started.  Such a caller
+ * still passes its inputs (the loaded context, token, position) and its
+ * output (logits_dev, fp32 [vocab], device memory); the scratch the step
+ * needs besides them (fp32 activations, attention partials, synchronisation
+ * counters, status word) comes from a fixed array inside libamk.so instead
+ * of the context's workspace.  The AMK pages have no counterpart to this
+ * entry point.
+ *   - Size limit: the array holds 1 MiB on every GPU that loads the library,
+ *     kept until the process exits.  A model whose per-step scratch exceeds
+ *     it (roughly: n_kv_heads * attn_splits * group * (head_dim + 2) * 4
+ *     bytes of partials plus 4 * (hidden + 2 * n_heads * head_dim + ffn))
+ *     is rejected with AMK_ERR_OOM and a message giving both sizes.
+ *   - Allocation: none.  No cudaMalloc, cudaFree or allocating library call.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.  The context's device must be
+ *     the current device.
+ *   - Sharing: every call uses the same array and finds the previous call's
+ *     contents there; the call clears the counters and status word itself.
+ *     Calls that overlap on the GPU (other streams, other threads, other
+ *     contexts on the same device) race on the array and must not be made.
+ *   - Synchronous: returns after the step has finished, with the device
+ *     status of that step (AMK_ERR_TIMEOUT / AMK_ERR_DEVICE_CHECK poison the
+ *     context as for amk_sync).  Checks and KV bookkeeping are those of
+ *     amk_decode_step.
+ */
+amk_status amk_decode_step_static_scratch(amk_ctx* ctx, int32_t token, int32_t pos,
+                                          float* logits_dev);
+
 /* Declare KV positions [0, n) valid (a cache filled by the caller). */
 amk_status amk_set_kv_length(amk_ctx* ctx, int32_t n);
 int32_t amk_kv_length(const amk_ctx* ctx);
