@@ -89,6 +89,8 @@ def _load():
         "amk_build_schedule": (C.c_int, [cfgp, schp, P, C.c_size_t, C.POINTER(C.c_size_t)]),
         "amk_validate_serialized": (C.c_int, [P, C.c_size_t, C.c_char_p, C.c_size_t]),
         "amk_debug_watchdog_probe": (C.c_int, [P, P, C.c_int32, C.POINTER(C.c_int32)]),
+        "amk_debug_trace_bytes": (C.c_size_t, [P, C.POINTER(C.c_int32)]),
+        "amk_debug_trace_step": (C.c_int, [P, C.c_int32, C.c_int32, P, P, C.c_size_t]),
         "amk_debug_dequant": (C.c_int, [C.c_int32, C.POINTER(amk_linear), C.c_int32, C.c_int32,
                                         P, P]),
     }
@@ -194,6 +196,18 @@ def amk_debug_watchdog_probe(scratch_ptr: int, stream_ptr: int, limit_us: int):
     st = lib.amk_debug_watchdog_probe(C.c_void_p(scratch_ptr), C.c_void_p(stream_ptr),
                                       int(limit_us), C.byref(dst))
     return int(st), int(dst.value)
+
+
+def amk_debug_trace_bytes(ctx):
+    stride = C.c_int32(0)
+    n = int(lib.amk_debug_trace_bytes(ctx, C.byref(stride)))
+    return n, int(stride.value)
+
+
+def amk_debug_trace_step(ctx, token: int, pos: int, logits_ptr: int, trace_ptr: int,
+                         trace_bytes: int) -> int:
+    return int(lib.amk_debug_trace_step(ctx, int(token), int(pos), C.c_void_p(logits_ptr),
+                                        C.c_void_p(trace_ptr), int(trace_bytes)))
 
 
 def amk_debug_dequant(fmt: int, w_ptr, s_ptr, z_ptr, out_features, in_features, out_ptr,

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/amk.h.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -30,6 +31,7 @@ struct amk_ctx {
   float* logits_stage = nullptr;
   uint64_t timeout_ns = 0;
   amk_status poisoned = AMK_OK;
+  int32_t max_queue = 0;  // longest per-CTA task queue (trace sizing)
   std::string err;
 };
 
@@ -171,6 +173,9 @@ amk_status launch_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits, 
   p.epoch = ++ctx->epoch;
   p.skip_lm = skip_lm;
   p.timeout_ns = ctx->timeout_ns;
+  p.trace = nullptr;
+  p.trace_stride = 0;
+  p.pad1 = 0;
   void* args[] = {&p};
   cudaError_t e = cudaLaunchCooperativeKernel(ctx->kernel, dim3(ctx->geom.num_ctas),
                                               dim3(kThreads), args, (size_t)ctx->smem, ctx->stream);
@@ -255,6 +260,9 @@ amk_status internal_launch(amk_ctx* ctx, const DevModel& dm, int32_t token, int3
   p.epoch = epoch;
   p.skip_lm = 0;
   p.timeout_ns = ctx->timeout_ns;
+  p.trace = nullptr;
+  p.trace_stride = 0;
+  p.pad1 = 0;
   void* args[] = {&p};
   cudaError_t e = cudaLaunchCooperativeKernel(ctx->kernel, dim3(ctx->geom.num_ctas),
                                               dim3(kThreads), args, (size_t)ctx->smem, ctx->stream);
@@ -523,6 +531,7 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
     }
   }
   qoff[s.queues.size()] = (int32_t)tasks.size();
+  for (const auto& q : s.queues) ctx->max_queue = std::max<int32_t>(ctx->max_queue, (int32_t)q.size());
 
   // rotate-half RoPE table, computed in double and rounded to float
   const int half = c.head_dim / 2;
@@ -640,6 +649,42 @@ amk_status amk_sync(amk_ctx* ctx) {
 }
 
 void amk_free(amk_ctx* ctx) { delete ctx; }
+
+size_t amk_debug_trace_bytes(const amk_ctx* ctx, int32_t* stride) {
+  if (!ctx) return 0;
+  if (stride) *stride = ctx->max_queue;
+  return (size_t)ctx->geom.num_ctas * (1 + (size_t)ctx->max_queue) * 8 * sizeof(int64_t);
+}
+
+amk_status amk_debug_trace_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_dev,
+                                int64_t* trace_dev, size_t trace_bytes) {
+  amk_status st = step_checks(ctx, token, pos);
+  if (st != AMK_OK) return st;
+  if (!logits_dev || !trace_dev || ((uintptr_t)trace_dev & 7) ||
+      trace_bytes < amk_debug_trace_bytes(ctx, nullptr))
+    return fail(ctx, AMK_ERR_INVALID_ARG, "bad logits or trace buffer (see amk_debug_trace_bytes)");
+  AMK_CUDA(ctx, cudaMemsetAsync(trace_dev, 0, amk_debug_trace_bytes(ctx, nullptr), ctx->stream));
+  StepParams p;
+  p.m = ctx->dm;
+  p.logits = logits_dev;
+  p.token = token;
+  p.pos = pos;
+  p.epoch = ++ctx->epoch;
+  p.skip_lm = 0;
+  p.timeout_ns = ctx->timeout_ns;
+  p.trace = trace_dev;
+  p.trace_stride = ctx->max_queue;
+  p.pad1 = 0;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchCooperativeKernel(ctx->kernel, dim3(ctx->geom.num_ctas),
+                                              dim3(kThreads), args, (size_t)ctx->smem, ctx->stream);
+  if (e != cudaSuccess) {
+    ctx->poisoned = AMK_ERR_CUDA;
+    return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel");
+  }
+  ctx->kv_len = pos + 1;
+  return amk_sync(ctx);
+}
 
 amk_status amk_debug_watchdog_probe(void* scratch_dev, void* stream, int32_t limit_us,
                                     int32_t* device_status) {

@@ -221,6 +221,10 @@ __device__ __forceinline__ const uint16_t* kv_row(const DevModel& m, int layer, 
 
 // -------------------------------------------------------------- producer
 
+__device__ __forceinline__ int64_t* trace_row(const StepParams& p, int i) {
+  return p.trace + ((int64_t)blockIdx.x * (1 + p.trace_stride) + 1 + i) * 8;
+}
+
 __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
   const uint64_t pol_w = policy_evict_first();
@@ -232,6 +236,8 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
   bool ok = true;
   for (int i = 0; i < n && ok; ++i) {
     const DevTask t = q[i];
+    int64_t blocked = 0;
+    if (p.trace) trace_row(p, i)[TR_P_FIRST] = (int64_t)global_timer();
     if (t.type == T_ATTN) {
       int t0, t1;
       attn_range(p.pos, m.splits, t.a1, &t0, &t1);
@@ -241,8 +247,10 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       for (int s0 = t0; s0 < t1 && ok; s0 += pps) {
         const int np = min(pps, t1 - s0);
         const uint32_t bytes = (uint32_t)np * m.head_dim * 2;
+        const int64_t c0 = p.trace ? clock64() : 0;
         ok = wait_phase(&sm.empty[slot], phase ^ 1u, m.status, abort_flag, p.timeout_ns, i,
                         SITE_EMPTY) && !*abort_flag;
+        if (p.trace) blocked += clock64() - c0;
         if (!ok) break;
         mbar_arrive_expect_tx(&sm.full[slot], 2 * bytes);
         bulk_copy_g2s(sm.ring[slot], kb + (int64_t)s0 * m.head_dim, bytes, &sm.full[slot], pol_kv);
@@ -259,8 +267,10 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
                            (int64_t)t.a0 * M.rb_bytes;
       const int nst = (t.a1 - t.a0) * M.nkt;
       for (int s = 0; s < nst && ok; ++s) {
+        const int64_t c0 = p.trace ? clock64() : 0;
         ok = wait_phase(&sm.empty[slot], phase ^ 1u, m.status, abort_flag, p.timeout_ns, i,
                         SITE_EMPTY) && !*abort_flag;
+        if (p.trace) blocked += clock64() - c0;
         if (!ok) break;
         mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)M.stage_bytes);
         bulk_copy_g2s(sm.ring[slot], src + (int64_t)s * M.stage_bytes, (uint32_t)M.stage_bytes,
@@ -269,6 +279,11 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
         parity = (parity & ~(1u << slot)) | (phase << slot);
         if (++slot == kStages) { slot = 0; phase ^= 1u; }
       }
+    }
+    if (p.trace) {
+      int64_t* tr = trace_row(p, i);
+      tr[TR_P_LAST] = (int64_t)global_timer();
+      tr[TR_P_BLOCKED] = blocked;
     }
   }
   // Every copy this CTA issued must land before its shared memory goes away.
@@ -291,21 +306,17 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
 
 // -------------------------------------------------------------- consumers
 
-struct Ring {
-  uint32_t slot = 0, phase = 0;
-  __device__ __forceinline__ void advance() {
-    if (++slot == kStages) { slot = 0; phase ^= 1u; }
-  }
-};
-
 // weight decoding of one 8-element chunk (shared with the dequant check)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float2 bf16x2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 
-// int8 byte i of w as float: (q + 128) placed under exponent 2^23, minus 2^23 + 128
+// int8 byte i of (w ^ 0x80808080) placed under the exponent of 2^23: 2^23 + q + 128
+__device__ __forceinline__ float i8_biased(uint32_t w_xor80, int i) {
+  return __uint_as_float(__byte_perm(w_xor80, 0x4B000000u, 0x7440u | (uint32_t)i));
+}
 __device__ __forceinline__ float i8_at(uint32_t w_xor80, int i) {
-  const uint32_t sel = 0x7440u | (uint32_t)i;
-  return __uint_as_float(__byte_perm(w_xor80, 0x4B000000u, sel)) - 8388736.0f;
+  return i8_biased(w_xor80, i) - 8388736.0f;
 }
 
 // int4 nibble i of w as float (exact)
@@ -313,21 +324,88 @@ __device__ __forceinline__ float u4_at(uint32_t w, int i) {
   return __uint_as_float(0x4B000000u | ((w >> (4 * i)) & 0xFu)) - 8388608.0f;
 }
 
+// int4 nibble i of w, left where it sits, under the exponent of 2^23:
+// 2^23 + q * 2^s with s = u4_shift(i); (value - 2^23) is exact.
+__device__ __forceinline__ constexpr int u4_shift(int i) { return i < 5 ? 4 * i : 4 * i - 12; }
+__device__ __forceinline__ float u4_biased(uint32_t w, uint32_t w_hi, int i) {
+  return i < 5 ? __uint_as_float(0x4B000000u | (w & (0xFu << (4 * i))))
+               : __uint_as_float(0x4B000000u | (w_hi & (0xFu << (4 * i - 12))));
+}
+
 __device__ __forceinline__ float fp16_bits_to_float(uint16_t b) {
   return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ void mbar_arrive32(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait32(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for a ring slot's data (consumer side).
+__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, const StepParams& p,
+                                          volatile int32_t* abort_flag, uint32_t task) {
+  if (mbar_try_wait32(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait32(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((spin & 15u) == 0u && global_timer() - t0 > p.timeout_ns) {
+      set_status(p.m.status, ST_TIMEOUT, task, SITE_FULL);
+      *abort_flag = 1;
+      return false;
+    }
+  }
 }
 
 template <int FMT>
 struct Fmt;
 template <>
-struct Fmt<AMK_FORMAT_BF16> { static constexpr int kPasses = 4; };
+struct Fmt<AMK_FORMAT_BF16> { static constexpr int kPasses = 4, kChunkBytes = 16; };
 template <>
-struct Fmt<AMK_FORMAT_INT8> { static constexpr int kPasses = 8; };
+struct Fmt<AMK_FORMAT_INT8> { static constexpr int kPasses = 8, kChunkBytes = 8; };
 template <>
-struct Fmt<AMK_FORMAT_INT4> { static constexpr int kPasses = 16; };
+struct Fmt<AMK_FORMAT_INT4> { static constexpr int kPasses = 16, kChunkBytes = 4; };
 
 // Sum P per-lane values over the warp.  Lanes whose low (5 - log2 P) bits
-// are zero return the total of value index (lane >> (5 - log2 P)).
+// are zero return the total of value index (lane >> (5 - log2 P)); the other
+// lanes of that group hold the same total.
 template <int P>
 __device__ __forceinline__ float transpose_reduce(float (&v)[P], int lane) {
 #pragma unroll
@@ -351,29 +429,28 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int msk = 16; msk >= 1; msk >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, msk));
-  return v;
-}
-
-__device__ __forceinline__ void load8_f32(const float* src, float* d) {
+__device__ __forceinline__ void load8_f32(const float* src, float2* d) {
   const float4 a = __ldcg(reinterpret_cast<const float4*>(src));
   const float4 b = __ldcg(reinterpret_cast<const float4*>(src) + 1);
-  d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
-  d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
+  d[0] = make_float2(a.x, a.y);
+  d[1] = make_float2(a.z, a.w);
+  d[2] = make_float2(b.x, b.y);
+  d[3] = make_float2(b.z, b.w);
 }
 
-__device__ __forceinline__ void load8_bf16(const uint16_t* src, float* d) {
+__device__ __forceinline__ void load8_bf16(const uint16_t* src, float2* d) {
   const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
-  d[0] = bf16_lo(w.x); d[1] = bf16_hi(w.x); d[2] = bf16_lo(w.y); d[3] = bf16_hi(w.y);
-  d[4] = bf16_lo(w.z); d[5] = bf16_hi(w.z); d[6] = bf16_lo(w.w); d[7] = bf16_hi(w.w);
+  d[0] = bf16x2(w.x);
+  d[1] = bf16x2(w.y);
+  d[2] = bf16x2(w.z);
+  d[3] = bf16x2(w.w);
 }
 
-// Activation chunk owned by a consumer thread: h[kt][i] = act[kt*Kt + chunk*8 + i].
-// QKV, gate/up and LM head take rmsnorm(x) * w_norm; O takes o; down takes a.
-__device__ void load_activation(const StepParams& p, Smem& sm, const DevTask& t, const DevMat& M,
-                                int chunk, float (&h)[8][8]) {
+// Activation chunk owned by a consumer thread: h[kt] holds act[kt*Kt + chunk*8 + 0..7]
+// as four pairs.  QKV, gate/up and LM head take rmsnorm(x) * w_norm; O takes
+// o; down takes a.
+__device__ __forceinline__ void load_activation(const StepParams& p, Smem& sm, const DevTask& t,
+                                                const DevMat& M, int chunk, float2 (&h)[8][4]) {
   const DevModel& m = p.m;
   const int tid = threadIdx.x;
   const bool norm = t.type == T_QKV || t.type == T_GATEUP || t.type == T_LMHEAD;
@@ -390,10 +467,10 @@ __device__ void load_activation(const StepParams& p, Smem& sm, const DevTask& t,
         else load8_f32(src + k, h[kt]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h[kt][i] = 0.f;
+        for (int i = 0; i < 4; ++i) h[kt][i] = make_float2(0.f, 0.f);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(h[kt][i], h[kt][i], ss);
+      for (int i = 0; i < 4; ++i) ss = fmaf(h[kt][i].x, h[kt][i].x, fmaf(h[kt][i].y, h[kt][i].y, ss));
     }
   }
   if (!norm) return;
@@ -413,59 +490,67 @@ __device__ void load_activation(const StepParams& p, Smem& sm, const DevTask& t,
     if (kt < M.nkt) {
       const int k = kt * M.Kt + chunk * 8;
       if (k < M.K) {
-        float w8[8];
+        float2 w8[4];
         load8_bf16(nw + k, w8);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h[kt][i] = h[kt][i] * r * w8[i];
+        for (int i = 0; i < 4; ++i)
+          h[kt][i] = make_float2(h[kt][i].x * r * w8[i].x, h[kt][i].y * r * w8[i].y);
       }
     }
   }
 }
 
+// One chunk of one row against the thread's activations, accumulated as a
+// pair of partial sums (packed FMA).  `a` is the chunk's shared address.
 template <int FMT>
-__device__ __forceinline__ float chunk_dot(const uint8_t* tile, const DevMat& M, int row,
-                                           int chunk, const float (&h)[8], float acc) {
+__device__ __forceinline__ float2 chunk_dot(uint32_t a, const float2 (&h)[4], float2 acc) {
   if constexpr (FMT == AMK_FORMAT_BF16) {
-    const uint4 w = *reinterpret_cast<const uint4*>(tile + (((row << M.cpr_shift) + chunk) << 4));
-    acc = fmaf(bf16_lo(w.x), h[0], acc);
-    acc = fmaf(bf16_hi(w.x), h[1], acc);
-    acc = fmaf(bf16_lo(w.y), h[2], acc);
-    acc = fmaf(bf16_hi(w.y), h[3], acc);
-    acc = fmaf(bf16_lo(w.z), h[4], acc);
-    acc = fmaf(bf16_hi(w.z), h[5], acc);
-    acc = fmaf(bf16_lo(w.w), h[6], acc);
-    acc = fmaf(bf16_hi(w.w), h[7], acc);
-    return acc;
-  } else if constexpr (FMT == AMK_FORMAT_INT8) {
-    const uint2 w = *reinterpret_cast<const uint2*>(tile + (((row << M.cpr_shift) + chunk) << 3));
-    const uint32_t a = w.x ^ 0x80808080u, b = w.y ^ 0x80808080u;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc = fmaf(i8_at(a, i), h[i], acc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc = fmaf(i8_at(b, i), h[4 + i], acc);
+    const uint4 w = lds128(a);
+    acc = __ffma2_rn(bf16x2(w.x), h[0], acc);
+    acc = __ffma2_rn(bf16x2(w.y), h[1], acc);
+    acc = __ffma2_rn(bf16x2(w.z), h[2], acc);
+    acc = __ffma2_rn(bf16x2(w.w), h[3], acc);
     return acc;
   } else {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + (((row << M.cpr_shift) + chunk) << 2));
-    // side data after the codes: fp16 scales [Rt][Kt/128], then u8 zeros [Rt][Kt/128]
-    const int ngt = M.Kt >> 7;
-    const int gi = row * ngt + (chunk >> 4);
-    const uint8_t* side = tile + kStageBytes;
-    const float s = fp16_bits_to_float(reinterpret_cast<const uint16_t*>(side)[gi]);
-    const float z = (float)side[M.Rt * ngt * 2 + gi];
-    float d = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d = fmaf(u4_at(w, i) - z, h[i], d);
-    return fmaf(s, d, acc);
+    const uint2 w = lds64(a);
+    const uint32_t x = w.x ^ 0x80808080u, y = w.y ^ 0x80808080u;
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+    acc = __ffma2_rn(__fadd2_rn(make_float2(i8_biased(x, 0), i8_biased(x, 1)), bias), h[0], acc);
+    acc = __ffma2_rn(__fadd2_rn(make_float2(i8_biased(x, 2), i8_biased(x, 3)), bias), h[1], acc);
+    acc = __ffma2_rn(__fadd2_rn(make_float2(i8_biased(y, 0), i8_biased(y, 1)), bias), h[2], acc);
+    acc = __ffma2_rn(__fadd2_rn(make_float2(i8_biased(y, 2), i8_biased(y, 3)), bias), h[3], acc);
+    return acc;
   }
+}
+
+// int4 chunk: h holds act * 2^-s per element position (see u4_shift), hs the
+// chunk's plain sum; returns acc + s_g * (sum(q * act) - z_g * sum(act)).
+__device__ __forceinline__ float chunk_dot_u4(uint32_t a, uint32_t side_s, uint32_t side_z,
+                                              const float2 (&h)[4], float hs, float acc) {
+  const uint32_t w = lds32(a);
+  const float s = fp16_bits_to_float((uint16_t)lds16(side_s));
+  const float z = (float)lds8(side_z);
+  const uint32_t w_hi = w >> 12;
+  const float2 bias = make_float2(-8388608.0f, -8388608.0f);
+  float2 d = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 q = __fadd2_rn(make_float2(u4_biased(w, w_hi, 2 * i), u4_biased(w, w_hi, 2 * i + 1)), bias);
+    d = __ffma2_rn(q, h[i], d);
+  }
+  return fmaf(s, fmaf(-z, hs, d.x + d.y), acc);
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
-// GEMV task: rows [a0*Rt, a1*Rt) of one tiled matrix against the activation
+// GEMV task: rows [a0*Rt, a1*Rt) of one tiled matrix against the activation.
+// `stage` counts the ring stages this CTA has consumed so far; returns the
+// count after this task, or -1 when the CTA is aborting.
 template <int FMT>
-__device__ __noinline__ bool gemv_task(const StepParams& p, Smem& sm, const DevTask& t, Ring& ring,
-                          bool failed, uint32_t task_idx) {
+__device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTask t, int stage,
+                                      uint32_t task_idx) {
   constexpr int P = Fmt<FMT>::kPasses;
+  constexpr int EB = Fmt<FMT>::kChunkBytes;
   const DevModel& m = p.m;
   const int kind = mat_kind(t.type);
   const DevMat M = m.mat[kind];
@@ -478,8 +563,21 @@ __device__ __noinline__ bool gemv_task(const StepParams& p, Smem& sm, const DevT
   const int wg = warp & ((1 << wpg_shift) - 1);
   volatile int32_t* abort_flag = &sm.abort_flag;
 
-  float h[8][8];
+  float2 h[8][4];
   load_activation(p, sm, t, M, chunk, h);
+  float hs[8];  // int4: per-chunk activation sums, then activations pre-scaled by 2^-s
+  if constexpr (FMT == AMK_FORMAT_INT4) {
+#pragma unroll
+    for (int kt = 0; kt < 8; ++kt) {
+      hs[kt] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        hs[kt] += h[kt][i].x + h[kt][i].y;
+        h[kt][i].x *= 1.0f / (float)(1 << u4_shift(2 * i));        // exact: power of two
+        h[kt][i].y *= 1.0f / (float)(1 << u4_shift(2 * i + 1));
+      }
+    }
+  }
 
   // layer-0 QKV tasks also initialise their slice of the residual stream
   if (t.type == T_QKV && t.layer == 0) {
@@ -488,39 +586,64 @@ __device__ __noinline__ bool gemv_task(const StepParams& p, Smem& sm, const DevT
       m.x[e] = __uint_as_float((uint32_t)emb[e] << 16);
   }
 
+  const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
+  const uint32_t full0 = smem_addr(&sm.full[0]);
+  const uint32_t empty0 = smem_addr(&sm.empty[0]);
+  const uint32_t off0 = (uint32_t)(((rsub << cs) + chunk) * EB);   // pass 0 chunk
+  const uint32_t pass_stride = (uint32_t)((rpp << cs) * EB);       // rows between passes
+  // int4 side data: fp16 scales [Rt][Kt/128] then u8 zeros [Rt][Kt/128]
+  const int ngt = M.Kt >> 7;
+  const uint32_t side_s0 = kStageBytes + (uint32_t)((rsub * ngt + (chunk >> 4)) * 2);
+  const uint32_t side_z0 = kStageBytes + (uint32_t)(M.Rt * ngt * 2 + rsub * ngt + (chunk >> 4));
+  uint32_t slot = (uint32_t)(stage % kStages), phase = (uint32_t)((stage / kStages) & 1);
+  bool failed = false;
+
   float* red = sm.scratch;
   const int nrb = t.a1 - t.a0;
   for (int rb = 0; rb < nrb; ++rb) {
-    float acc[P];
+    float2 acc2[FMT == AMK_FORMAT_INT4 ? 1 : P];
+    float acc1[FMT == AMK_FORMAT_INT4 ? P : 1];
 #pragma unroll
-    for (int i = 0; i < P; ++i) acc[i] = 0.f;
+    for (int i = 0; i < (FMT == AMK_FORMAT_INT4 ? 1 : P); ++i) acc2[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < (FMT == AMK_FORMAT_INT4 ? P : 1); ++i) acc1[i] = 0.f;
 #pragma unroll
     for (int kt = 0; kt < 8; ++kt) {
       if (kt < M.nkt) {
-        if (!failed)
-          failed = !wait_phase(&sm.full[ring.slot], ring.phase, m.status, abort_flag,
-                               p.timeout_ns, task_idx, SITE_FULL);
+        if (!failed) failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx);
         if (!failed) {
-          const uint8_t* tile = sm.ring[ring.slot];
+          const uint32_t tile = ring0 + slot * kSlotBytes;
 #pragma unroll
-          for (int ps = 0; ps < P; ++ps)
-            acc[ps] = chunk_dot<FMT>(tile, M, ps * rpp + rsub, chunk, h[kt], acc[ps]);
+          for (int ps = 0; ps < P; ++ps) {
+            if constexpr (FMT == AMK_FORMAT_INT4)
+              acc1[ps] = chunk_dot_u4(tile + off0 + ps * pass_stride,
+                                      tile + side_s0 + (uint32_t)(ps * rpp * ngt * 2),
+                                      tile + side_z0 + (uint32_t)(ps * rpp * ngt), h[kt], hs[kt],
+                                      acc1[ps]);
+            else
+              acc2[ps] = chunk_dot<FMT>(tile + off0 + ps * pass_stride, h[kt], acc2[ps]);
+          }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[ring.slot]);
-        ring.advance();
+        if (lane == 0) mbar_arrive32(empty0 + slot * 8);
+        if (++slot == kStages) { slot = 0; phase ^= 1u; }
       }
     }
-    const float v = transpose_reduce<P>(acc, lane);
+    float v[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+      if constexpr (FMT == AMK_FORMAT_INT4) v[i] = acc1[i];
+      else v[i] = acc2[i].x + acc2[i].y;
+    }
+    const float tot = transpose_reduce<P>(v, lane);
     constexpr int kLaneStride = 32 / P;
     if ((lane & (kLaneStride - 1)) == 0) {
       const int ps = lane / kLaneStride;
-      const int row = rb * M.Rt + ps * rpp + rsub;
-      red[row * 8 + wg] = v;
+      red[(rb * M.Rt + ps * rpp + rsub) * 8 + wg] = tot;
     }
   }
 
-  if (consumer_sync_or(failed)) return false;
+  if (consumer_sync_or(failed)) return -1;
 
   // epilogue: one row (or one row pair) per thread
   const int nrows = nrb * M.Rt;
@@ -586,135 +709,203 @@ __device__ __noinline__ bool gemv_task(const StepParams& p, Smem& sm, const DevT
       }
     }
   }
-  return true;
+  return stage + nrb * M.nkt;
 }
 
-// Split-K GQA attention of one KV head over one context split; the last
-// split to finish merges all splits of the head (LSE combine) into o.
-// HD: head_dim; a lane owns DPL = HD/32 dims of every head of the group.
-template <int HD>
-__device__ __noinline__ bool attn_task(const StepParams& p, Smem& sm, const DevTask& t, Ring& ring,
-                          bool failed, uint32_t task_idx) {
+// Split-K GQA attention of one KV head over one context split.  Per ring
+// stage a warp takes NPW cached positions; scores for R positions x G heads
+// are reduced in one transposed warp reduction, then the warp's running
+// softmax state is rescaled once per block of R positions.  The last split
+// of a KV head to finish merges all splits (LSE combine) into o.
+// HD: head_dim (a lane owns HD/32 dims of every head), G: query heads per KV head.
+template <int HD, int G>
+__device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTask t, int stage,
+                                      uint32_t task_idx) {
   constexpr int DPL = HD / 32;
-  constexpr int GMAX = kMaxGroupDim / HD;
+  constexpr int PPS = (kStageBytes / 2) / (HD * 2);   // positions per stage
+  constexpr int NPW = PPS / kConsumerWarps;           // positions per warp per stage
+  constexpr int R = (16 / G) < NPW ? (16 / G) : NPW;  // positions per block
+  constexpr int V = R * G;                            // scores per block
+  constexpr int LS = 32 / V;                          // lanes per score after the reduction
   const DevModel& m = p.m;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int hd = HD, G = m.group, g = t.a0, j = t.a1;
+  const int g = t.a0, j = t.a1;
   volatile int32_t* abort_flag = &sm.abort_flag;
 
   // queries of the group, pre-scaled so that scores are in log2 units
-  const float qscale = 1.4426950408889634f * rsqrtf((float)hd);
-  float qr[GMAX][DPL];
+  const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
+  float qr[G][DPL];
 #pragma unroll
-  for (int h = 0; h < GMAX; ++h)
+  for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int d = 0; d < DPL; ++d)
-      qr[h][d] = h < G ? __ldcg(m.q + (int64_t)(g * G + h) * hd + lane * DPL + d) * qscale : 0.f;
-  float mx[GMAX], l[GMAX], acc[GMAX][DPL];
+      qr[h][d] = __ldcg(m.q + (int64_t)(g * G + h) * HD + lane * DPL + d) * qscale;
+  float mx[G], l[G], acc[G][DPL];
 #pragma unroll
-  for (int h = 0; h < GMAX; ++h) {
+  for (int h = 0; h < G; ++h) {
     mx[h] = -INFINITY;
     l[h] = 0.f;
 #pragma unroll
     for (int d = 0; d < DPL; ++d) acc[h][d] = 0.f;
   }
 
-  auto update = [&](const float* kf, const float* vf) {
+  // one block of `np` (<= R) positions whose K and V rows this lane holds
+  auto block = [&](const float (&kf)[R][DPL], const float (&vf)[R][DPL], int np) {
+    float sc[V];
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-      if (h < G) {
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
         float s = 0.f;
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) s = fmaf(qr[h][d], kf[d], s);
-        s = warp_sum(s);
-        const float mn = fmaxf(mx[h], s);
-        const float alpha = exp2f(mx[h] - mn);
-        const float pe = exp2f(s - mn);
-        l[h] = l[h] * alpha + pe;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(acc[h][d], alpha, pe * vf[d]);
-        mx[h] = mn;
+        for (int d = 0; d < DPL; ++d) s = fmaf(qr[h][d], kf[r][d], s);
+        sc[r * G + h] = s;
       }
+    float s = transpose_reduce<V>(sc, lane);   // score of (r, h) = lane / LS
+    const int idx = lane / LS;
+    const int my_r = idx / G, my_h = idx % G;
+    if (my_r >= np) s = -INFINITY;               // positions past the end of the split
+    // block maximum per head: reduce over the lanes holding other positions
+    float bm = s;
+#pragma unroll
+    for (int msk = LS * G; msk < 32; msk <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, msk));
+    float alpha[G], mnew[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float b = __shfl_sync(0xFFFFFFFFu, bm, h * LS);
+      mnew[h] = fmaxf(mx[h], b);
+      alpha[h] = exp2f(mx[h] - mnew[h]);
     }
+    float mine = mnew[0];
+#pragma unroll
+    for (int h = 1; h < G; ++h) mine = my_h == h ? mnew[h] : mine;
+    const float pe = exp2f(s - mine);            // 0 for the padding positions
+    float bs = pe;
+#pragma unroll
+    for (int msk = LS * G; msk < 32; msk <<= 1) bs += __shfl_xor_sync(0xFFFFFFFFu, bs, msk);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      l[h] = fmaf(l[h], alpha[h], __shfl_sync(0xFFFFFFFFu, bs, h * LS));
+      mx[h] = mnew[h];
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) acc[h][d] *= alpha[h];
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pr = __shfl_sync(0xFFFFFFFFu, pe, (r * G + h) * LS);
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(pr, vf[r][d], acc[h][d]);
+      }
   };
-  auto load_kv = [&](const uint16_t* src, float* f, bool global) {
+  auto unpack = [&](uint32_t lo, uint32_t hi, float* f) {
     if constexpr (DPL == 4) {
-      uint2 w;
-      if (global) w = __ldcg(reinterpret_cast<const uint2*>(src + lane * 4));
-      else w = *reinterpret_cast<const uint2*>(src + lane * 4);
-      f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
+      f[0] = bf16_lo(lo); f[1] = bf16_hi(lo); f[2] = bf16_lo(hi); f[3] = bf16_hi(hi);
     } else {
-      uint32_t w;
-      if (global) w = __ldcg(reinterpret_cast<const unsigned int*>(src + lane * 2));
-      else w = *reinterpret_cast<const uint32_t*>(src + lane * 2);
-      f[0] = bf16_lo(w); f[1] = bf16_hi(w);
+      f[0] = bf16_lo(lo); f[1] = bf16_hi(lo);
     }
   };
 
+  const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
+  const uint32_t full0 = smem_addr(&sm.full[0]);
+  const uint32_t empty0 = smem_addr(&sm.empty[0]);
+  uint32_t slot = (uint32_t)(stage % kStages), phase = (uint32_t)((stage / kStages) & 1);
+  bool failed = false;
   int t0, t1;
   attn_range(p.pos, m.splits, j, &t0, &t1);
-  const int pps = attn_positions_per_stage(hd);
-  for (int s0 = t0; s0 < t1; s0 += pps) {
-    const int np = min(pps, t1 - s0);
-    if (!failed)
-      failed = !wait_phase(&sm.full[ring.slot], ring.phase, m.status, abort_flag, p.timeout_ns,
-                           task_idx, SITE_FULL);
+  int nst = 0;
+  for (int s0 = t0; s0 < t1; s0 += PPS) {
+    const int np = min(PPS, t1 - s0);
+    ++nst;
+    if (!failed) failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx);
     if (!failed) {
-      const uint16_t* kt = reinterpret_cast<const uint16_t*>(sm.ring[ring.slot]);
-      const uint16_t* vt = reinterpret_cast<const uint16_t*>(sm.ring[ring.slot] + kStageBytes / 2);
-      for (int pi = warp; pi < np; pi += kConsumerWarps) {
-        float kf[DPL], vf[DPL];
-        load_kv(kt + pi * hd, kf, false);
-        load_kv(vt + pi * hd, vf, false);
-        update(kf, vf);
+      const uint32_t kt = ring0 + slot * kSlotBytes;
+      const uint32_t vt = kt + kStageBytes / 2;
+      // warp w takes positions [w*NPW, (w+1)*NPW) of the stage
+#pragma unroll
+      for (int b0 = 0; b0 < NPW; b0 += R) {
+        const int first = warp * NPW + b0;
+        const int nb = min(R, np - first);
+        if (nb > 0) {
+          float kf[R][DPL], vf[R][DPL];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int pi = min(first + r, np - 1);
+            const uint32_t ko = kt + (uint32_t)((pi * HD + lane * DPL) * 2);
+            const uint32_t vo = vt + (uint32_t)((pi * HD + lane * DPL) * 2);
+            if constexpr (DPL == 4) {
+              const uint2 kw = lds64(ko), vw = lds64(vo);
+              unpack(kw.x, kw.y, kf[r]);
+              unpack(vw.x, vw.y, vf[r]);
+            } else {
+              unpack(lds32(ko), 0u, kf[r]);
+              unpack(lds32(vo), 0u, vf[r]);
+            }
+          }
+          block(kf, vf, nb);
+        }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[ring.slot]);
-    ring.advance();
+    if (lane == 0) mbar_arrive32(empty0 + slot * 8);
+    if (++slot == kStages) { slot = 0; phase ^= 1u; }
   }
   // the current position, written this step by the QKV tasks
   if (!failed && j == m.splits - 1 && warp == 0) {
-    float kf[DPL], vf[DPL];
-    load_kv(kv_row(m, t.layer, 0, g, p.pos), kf, true);
-    load_kv(kv_row(m, t.layer, 1, g, p.pos), vf, true);
-    update(kf, vf);
+    float kf[R][DPL], vf[R][DPL];
+    const uint16_t* kr = kv_row(m, t.layer, 0, g, p.pos) + lane * DPL;
+    const uint16_t* vr = kv_row(m, t.layer, 1, g, p.pos) + lane * DPL;
+    if constexpr (DPL == 4) {
+      const uint2 kw = __ldcg(reinterpret_cast<const uint2*>(kr));
+      const uint2 vw = __ldcg(reinterpret_cast<const uint2*>(vr));
+      unpack(kw.x, kw.y, kf[0]);
+      unpack(vw.x, vw.y, vf[0]);
+    } else {
+      unpack(__ldcg(reinterpret_cast<const unsigned int*>(kr)), 0u, kf[0]);
+      unpack(__ldcg(reinterpret_cast<const unsigned int*>(vr)), 0u, vf[0]);
+    }
+#pragma unroll
+    for (int r = 1; r < R; ++r)
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) { kf[r][d] = kf[0][d]; vf[r][d] = vf[0][d]; }
+    block(kf, vf, 1);
   }
 
   // merge the eight warps' partial softmax states
-  float* mg = sm.scratch;  // [warp][G][hd + 2]
-  const int ws = G * (hd + 2);
+  float* mg = sm.scratch;  // [warp][G][HD + 2]
+  constexpr int WS = G * (HD + 2);
+  static_assert(kConsumerWarps * WS <= kScratchFloats, "warp merge exceeds the scratch");
 #pragma unroll
-  for (int h = 0; h < GMAX; ++h) {
-    if (h < G) {
+  for (int h = 0; h < G; ++h) {
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) mg[warp * ws + h * (hd + 2) + lane * DPL + d] = acc[h][d];
-      if (lane == 0) {
-        mg[warp * ws + h * (hd + 2) + hd] = mx[h];
-        mg[warp * ws + h * (hd + 2) + hd + 1] = l[h];
-      }
+    for (int d = 0; d < DPL; ++d) mg[warp * WS + h * (HD + 2) + lane * DPL + d] = acc[h][d];
+    if (lane == 0) {
+      mg[warp * WS + h * (HD + 2) + HD] = mx[h];
+      mg[warp * WS + h * (HD + 2) + HD + 1] = l[h];
     }
   }
-  if (consumer_sync_or(failed)) return false;
+  if (consumer_sync_or(failed)) return -1;
   float* part = m.part + (int64_t)(g * m.splits + j) * m.part_stride;
-  for (int idx = tid; idx < G * hd; idx += kConsumerThreads) {
-    const int h = idx / hd, d = idx % hd;
+  for (int idx = tid; idx < G * HD; idx += kConsumerThreads) {
+    const int h = idx / HD, d = idx % HD;
     float M = -INFINITY;
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg[w * ws + h * (hd + 2) + hd]);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg[w * WS + h * (HD + 2) + HD]);
     float L = 0.f, A = 0.f;
     if (M != -INFINITY) {
+#pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = mg[w * ws + h * (hd + 2) + hd];
-        if (mw == -INFINITY) continue;
-        const float sc = exp2f(mw - M);
-        L = fmaf(mg[w * ws + h * (hd + 2) + hd + 1], sc, L);
-        A = fmaf(mg[w * ws + h * (hd + 2) + d], sc, A);
+        const float mw = mg[w * WS + h * (HD + 2) + HD];
+        const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        L = fmaf(mg[w * WS + h * (HD + 2) + HD + 1], sc, L);
+        A = fmaf(mg[w * WS + h * (HD + 2) + d], sc, A);
       }
     }
-    part[h * (hd + 2) + d] = A;
+    part[h * (HD + 2) + d] = A;
     if (d == 0) {
-      part[h * (hd + 2) + hd] = M;
-      part[h * (hd + 2) + hd + 1] = L;
+      part[h * (HD + 2) + HD] = M;
+      part[h * (HD + 2) + HD + 1] = L;
     }
   }
   consumer_sync();
@@ -725,38 +916,89 @@ __device__ __noinline__ bool attn_task(const StepParams& p, Smem& sm, const DevT
     sm.flag = (old + 1u == p.epoch * (uint32_t)m.splits) ? 1 : 0;
   }
   consumer_sync();
-  if (!sm.flag) return true;
-
-  const float* pg = m.part + (int64_t)g * m.splits * m.part_stride;
-  for (int idx = tid; idx < G * hd; idx += kConsumerThreads) {
-    const int h = idx / hd, d = idx % hd;
-    float M = -INFINITY;
-    for (int s = 0; s < m.splits; ++s) M = fmaxf(M, __ldcg(pg + (int64_t)s * m.part_stride + h * (hd + 2) + hd));
-    float L = 0.f, A = 0.f;
-    for (int s = 0; s < m.splits; ++s) {
-      const float* ps = pg + (int64_t)s * m.part_stride + h * (hd + 2);
-      const float ms = __ldcg(ps + hd);
-      if (ms == -INFINITY) continue;
-      const float sc = exp2f(ms - M);
-      L = fmaf(__ldcg(ps + hd + 1), sc, L);
-      A = fmaf(__ldcg(ps + d), sc, A);
+  if (sm.flag) {
+    // LSE merge of the S splits of this KV head.  Shared memory use is
+    // O(G) for any S: per-head maximum and normaliser by strided partial
+    // reductions, then every output element sums its S partials.
+    const int S = m.splits;
+    const float* pg = m.part + (int64_t)g * S * m.part_stride;
+    float* red = sm.scratch;                 // [8][G] partials, [G] max, [G] 1/L
+    auto m_of = [&](int s, int h) { return __ldcg(pg + (int64_t)s * m.part_stride + h * (HD + 2) + HD); };
+    auto l_of = [&](int s, int h) { return __ldcg(pg + (int64_t)s * m.part_stride + h * (HD + 2) + HD + 1); };
+    const int hh = tid % G;                  // every index tid + k*256 has head tid % G
+    float lm = -INFINITY;
+    for (int idx = tid; idx < S * G; idx += kConsumerThreads) lm = fmaxf(lm, m_of(idx / G, hh));
+#pragma unroll
+    for (int msk = G; msk < 32; msk <<= 1) lm = fmaxf(lm, __shfl_xor_sync(0xFFFFFFFFu, lm, msk));
+    if (lane < G) red[warp * G + lane] = lm;
+    consumer_sync();
+    if (tid < G) {
+      float M = -INFINITY;
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red[w * G + tid]);
+      red[8 * G + tid] = M;
     }
-    m.o[(int64_t)(g * G + h) * hd + d] = A / L;
+    consumer_sync();
+    const float Mh = red[8 * G + hh];
+    float ll = 0.f;
+    for (int idx = tid; idx < S * G; idx += kConsumerThreads) {
+      const float ms = m_of(idx / G, hh);
+      if (ms != -INFINITY) ll = fmaf(l_of(idx / G, hh), exp2f(ms - Mh), ll);
+    }
+#pragma unroll
+    for (int msk = G; msk < 32; msk <<= 1) ll += __shfl_xor_sync(0xFFFFFFFFu, ll, msk);
+    consumer_sync();                         // everyone has read the maxima's slot area
+    if (lane < G) red[warp * G + lane] = ll;
+    consumer_sync();
+    if (tid < G) {
+      float L = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) L += red[w * G + tid];
+      red[9 * G + tid] = 1.0f / L;
+    }
+    consumer_sync();
+    for (int idx = tid; idx < G * HD; idx += kConsumerThreads) {
+      const int h = idx / HD, d = idx % HD;
+      const float M = red[8 * G + h];
+      float A = 0.f;
+      for (int s = 0; s < S; ++s) {
+        const float* ps = pg + (int64_t)s * m.part_stride + h * (HD + 2);
+        const float ms = __ldcg(ps + HD);
+        if (ms != -INFINITY) A = fmaf(__ldcg(ps + d), exp2f(ms - M), A);
+      }
+      m.o[(int64_t)(g * G + h) * HD + d] = A * red[9 * G + h];
+    }
+    consumer_sync();
+    if (tid == 0) red_release_add(m.counters + t.a2, 1u);
   }
-  consumer_sync();
-  if (tid == 0) red_release_add(m.counters + t.a2, 1u);
-  return true;
+  return stage + nst;
+}
+
+template <int HD>
+__device__ __forceinline__ int attn_dispatch(const StepParams& p, Smem& sm, const DevTask& t,
+                                             int stage, uint32_t i) {
+  switch (p.m.group) {
+    case 1: return attn_task<HD, 1>(p, sm, t, stage, i);
+    case 2: return attn_task<HD, 2>(p, sm, t, stage, i);
+    case 4: return attn_task<HD, 4>(p, sm, t, stage, i);
+    default:
+      if constexpr (HD == 64) return attn_task<HD, 8>(p, sm, t, stage, i);
+      return -1;
+  }
 }
 
 template <int QKV_FMT, int LM_FMT>
 __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
   const int tid = threadIdx.x;
-  Ring ring;
+  int stage = 0;
   volatile int32_t* abort_flag = &sm.abort_flag;
   for (int i = 0; i < n; ++i) {
     const DevTask t = q[i];
     bool failed = false;
+    int64_t* tr = p.trace ? trace_row(p, i) : nullptr;
+    if (tr && tid == 0) {
+      tr[TR_C_BEGIN] = (int64_t)global_timer();
+      tr[TR_TAG] = t.type | (t.layer << 8);
+    }
     if (t.wait_counter >= 0 && tid == 0)
       failed = !wait_counter(m.counters + t.wait_counter, p.epoch * t.wait_count, m.status,
                              abort_flag, p.timeout_ns, (uint32_t)i);
@@ -764,20 +1006,22 @@ __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       *abort_flag = 1;
       return;
     }
-    bool ok;
+    if (tr && tid == 0) tr[TR_C_WAITED] = (int64_t)global_timer();
     if (t.type == T_ATTN)
-      ok = m.head_dim == 128 ? attn_task<128>(p, sm, t, ring, false, (uint32_t)i)
-                             : attn_task<64>(p, sm, t, ring, false, (uint32_t)i);
-    else if (t.type == T_LMHEAD) ok = gemv_task<LM_FMT>(p, sm, t, ring, false, (uint32_t)i);
-    else ok = gemv_task<QKV_FMT>(p, sm, t, ring, false, (uint32_t)i);
-    if (!ok) {
+      stage = m.head_dim == 128 ? attn_dispatch<128>(p, sm, t, stage, (uint32_t)i)
+                                : attn_dispatch<64>(p, sm, t, stage, (uint32_t)i);
+    else if (t.type == T_LMHEAD) stage = gemv_task<LM_FMT>(p, sm, t, stage, (uint32_t)i);
+    else stage = gemv_task<QKV_FMT>(p, sm, t, stage, (uint32_t)i);
+    if (stage < 0) {
       *abort_flag = 1;
       return;
     }
+    if (tr && tid == 0) tr[TR_C_DONE] = (int64_t)global_timer();
     if (t.type != T_ATTN) {
       consumer_sync();  // epilogue stores done; scratch free for the next task
       if (tid == 0 && t.signal >= 0) red_release_add(m.counters + t.signal, 1u);
     }
+    if (tr && tid == 0) tr[TR_C_SIGNALLED] = (int64_t)global_timer();
   }
 }
 
@@ -801,10 +1045,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int q0 = p.m.queue_off[c];
   const int n = p.skip_lm ? p.m.queue_body[c] : p.m.queue_off[c + 1] - q0;
   const DevTask* q = p.m.tasks + q0;
+  int64_t* hdr = p.trace ? p.trace + (int64_t)c * (1 + p.trace_stride) * 8 : nullptr;
+  if (hdr && tid == 0) {
+    hdr[0] = (int64_t)global_timer();
+    hdr[1] = clock64();
+    hdr[4] = n;
+  }
   if (tid >= kConsumerThreads) {
     if (tid == kConsumerThreads) producer_loop(p, sm, q, n);
   } else {
     consumer_loop<FMT, LM_FMT>(p, sm, q, n);
+  }
+  if (hdr && tid == 0) {
+    hdr[2] = (int64_t)global_timer();
+    hdr[3] = clock64();
   }
 }
 

@@ -63,6 +63,20 @@ struct StepParams {
   uint32_t epoch;              // 1-based launch index: counter targets are epoch * producers
   int32_t skip_lm;
   uint64_t timeout_ns;
+  // optional per-task timestamps (tuning aid): null, or
+  // int64 [num_ctas][1 + trace_stride][8], see kTrace* below
+  int64_t* trace;
+  int32_t trace_stride;
+  int32_t pad1;
+};
+
+// Trace record words.  Row 0 of a CTA: start / end %globaltimer and clock64.
+// Row 1 + i for task i: consumer begin (before its wait), wait satisfied,
+// main loop done, signalled; producer first / last issue, cycles blocked on
+// a full ring; task type | layer << 8.
+enum TraceWord : int {
+  TR_C_BEGIN = 0, TR_C_WAITED = 1, TR_C_DONE = 2, TR_C_SIGNALLED = 3,
+  TR_P_FIRST = 4, TR_P_LAST = 5, TR_P_BLOCKED = 6, TR_TAG = 7
 };
 
 enum DevStatus : uint32_t {

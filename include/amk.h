@@ -231,6 +231,22 @@ amk_status amk_debug_watchdog_probe(void* scratch_dev, void* stream, int32_t lim
                                     int32_t* device_status);
 
 /*
+ * Per-task timestamps of one decode step (tuning aid, in the spirit of the
+ * region timing of the Argus page, "Case 3").  amk_debug_trace_bytes gives
+ * the int64 buffer size and, in *stride, the longest task queue S.  The
+ * buffer is [num_ctas][1 + S][8]: row 0 of a CTA holds its start and end
+ * %globaltimer (ns) and clock64, and its task count; row 1 + i holds, for
+ * its i-th task: consumer begin (before the counter wait), wait satisfied,
+ * work done, signalled (%globaltimer ns); producer first and last copy
+ * issued (ns) and clock64 cycles blocked on a full ring; task type | layer
+ * << 8.  amk_debug_trace_step runs amk_decode_step with the recording on
+ * and waits for it.  trace_dev: caller device memory, 8-byte aligned.
+ */
+size_t amk_debug_trace_bytes(const amk_ctx* ctx, int32_t* stride);
+amk_status amk_debug_trace_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_dev,
+                                int64_t* trace_dev, size_t trace_bytes);
+
+/*
  * Dequantisation check (test aid): writes the fp32 values the kernel's
  * weight decoder produces for matrix `lin` of the given format and shape
  * into out_dev [out_features][in_features].  Used to check that int8 / int4
