@@ -653,7 +653,7 @@ void amk_free(amk_ctx* ctx) { delete ctx; }
 size_t amk_debug_trace_bytes(const amk_ctx* ctx, int32_t* stride) {
   if (!ctx) return 0;
   if (stride) *stride = ctx->max_queue;
-  return (size_t)ctx->geom.num_ctas * (1 + (size_t)ctx->max_queue) * 8 * sizeof(int64_t);
+  return (size_t)ctx->geom.num_ctas * (1 + (size_t)ctx->max_queue) * kTraceWords * sizeof(int64_t);
 }
 
 amk_status amk_debug_trace_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_dev,

@@ -222,7 +222,7 @@ __device__ __forceinline__ const uint16_t* kv_row(const DevModel& m, int layer, 
 // -------------------------------------------------------------- producer
 
 __device__ __forceinline__ int64_t* trace_row(const StepParams& p, int i) {
-  return p.trace + ((int64_t)blockIdx.x * (1 + p.trace_stride) + 1 + i) * 8;
+  return p.trace + ((int64_t)blockIdx.x * (1 + p.trace_stride) + 1 + i) * kTraceWords;
 }
 
 __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
@@ -380,11 +380,16 @@ __device__ __forceinline__ bool mbar_try_wait32(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for a ring slot's data (consumer side).
 __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, const StepParams& p,
-                                          volatile int32_t* abort_flag, uint32_t task) {
+                                          volatile int32_t* abort_flag, uint32_t task,
+                                          int64_t* starved = nullptr) {
   if (mbar_try_wait32(bar, parity)) return true;
   const uint64_t t0 = global_timer();
+  const int64_t c0 = starved ? clock64() : 0;
   for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait32(bar, parity)) return true;
+    if (mbar_try_wait32(bar, parity)) {
+      if (starved) *starved += clock64() - c0;
+      return true;
+    }
     if (*abort_flag) return false;
     if ((spin & 15u) == 0u && global_timer() - t0 > p.timeout_ns) {
       set_status(p.m.status, ST_TIMEOUT, task, SITE_FULL);
@@ -449,8 +454,9 @@ __device__ __forceinline__ void load8_bf16(const uint16_t* src, float2* d) {
 // Activation chunk owned by a consumer thread: h[kt] holds act[kt*Kt + chunk*8 + 0..7]
 // as four pairs.  QKV, gate/up and LM head take rmsnorm(x) * w_norm; O takes
 // o; down takes a.
+template <int NKT>
 __device__ __forceinline__ void load_activation(const StepParams& p, Smem& sm, const DevTask& t,
-                                                const DevMat& M, int chunk, float2 (&h)[8][4]) {
+                                                const DevMat& M, int chunk, float2 (&h)[NKT][4]) {
   const DevModel& m = p.m;
   const int tid = threadIdx.x;
   const bool norm = t.type == T_QKV || t.type == T_GATEUP || t.type == T_LMHEAD;
@@ -459,19 +465,17 @@ __device__ __forceinline__ void load_activation(const StepParams& p, Smem& sm, c
   const uint16_t* emb = m.embed + (int64_t)p.token * m.hidden;
   float ss = 0.f;
 #pragma unroll
-  for (int kt = 0; kt < 8; ++kt) {
-    if (kt < M.nkt) {
-      const int k = kt * M.Kt + chunk * 8;
-      if (k < M.K) {  // K is a multiple of 8
-        if (from_embed) load8_bf16(emb + k, h[kt]);
-        else load8_f32(src + k, h[kt]);
-      } else {
+  for (int kt = 0; kt < NKT; ++kt) {
+    const int k = kt * M.Kt + chunk * 8;
+    if (k < M.K) {  // K is a multiple of 8
+      if (from_embed) load8_bf16(emb + k, h[kt]);
+      else load8_f32(src + k, h[kt]);
+    } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) h[kt][i] = make_float2(0.f, 0.f);
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ss = fmaf(h[kt][i].x, h[kt][i].x, fmaf(h[kt][i].y, h[kt][i].y, ss));
+      for (int i = 0; i < 4; ++i) h[kt][i] = make_float2(0.f, 0.f);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ss = fmaf(h[kt][i].x, h[kt][i].x, fmaf(h[kt][i].y, h[kt][i].y, ss));
   }
   if (!norm) return;
   // threads tid < Kt/8 hold every chunk once: their squares sum to sum(x^2)
@@ -486,16 +490,14 @@ __device__ __forceinline__ void load_activation(const StepParams& p, Smem& sm, c
                        : t.type == T_GATEUP ? m.ffn_norm + (int64_t)t.layer * m.hidden
                                             : m.final_norm;
 #pragma unroll
-  for (int kt = 0; kt < 8; ++kt) {
-    if (kt < M.nkt) {
-      const int k = kt * M.Kt + chunk * 8;
-      if (k < M.K) {
-        float2 w8[4];
-        load8_bf16(nw + k, w8);
+  for (int kt = 0; kt < NKT; ++kt) {
+    const int k = kt * M.Kt + chunk * 8;
+    if (k < M.K) {
+      float2 w8[4];
+      load8_bf16(nw + k, w8);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          h[kt][i] = make_float2(h[kt][i].x * r * w8[i].x, h[kt][i].y * r * w8[i].y);
-      }
+      for (int i = 0; i < 4; ++i)
+        h[kt][i] = make_float2(h[kt][i].x * r * w8[i].x, h[kt][i].y * r * w8[i].y);
     }
   }
 }
@@ -546,9 +548,9 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 // GEMV task: rows [a0*Rt, a1*Rt) of one tiled matrix against the activation.
 // `stage` counts the ring stages this CTA has consumed so far; returns the
 // count after this task, or -1 when the CTA is aborting.
-template <int FMT>
+template <int FMT, int NKT>
 __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTask t, int stage,
-                                      uint32_t task_idx) {
+                                      uint32_t task_idx, int64_t* tr) {
   constexpr int P = Fmt<FMT>::kPasses;
   constexpr int EB = Fmt<FMT>::kChunkBytes;
   const DevModel& m = p.m;
@@ -563,12 +565,12 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   const int wg = warp & ((1 << wpg_shift) - 1);
   volatile int32_t* abort_flag = &sm.abort_flag;
 
-  float2 h[8][4];
-  load_activation(p, sm, t, M, chunk, h);
-  float hs[8];  // int4: per-chunk activation sums, then activations pre-scaled by 2^-s
+  float2 h[NKT][4];
+  load_activation<NKT>(p, sm, t, M, chunk, h);
+  float hs[NKT];  // int4: per-chunk activation sums, then activations pre-scaled by 2^-s
   if constexpr (FMT == AMK_FORMAT_INT4) {
 #pragma unroll
-    for (int kt = 0; kt < 8; ++kt) {
+    for (int kt = 0; kt < NKT; ++kt) {
       hs[kt] = 0.f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -597,6 +599,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   const uint32_t side_z0 = kStageBytes + (uint32_t)(M.Rt * ngt * 2 + rsub * ngt + (chunk >> 4));
   uint32_t slot = (uint32_t)(stage % kStages), phase = (uint32_t)((stage / kStages) & 1);
   bool failed = false;
+  int64_t starved = 0;
 
   float* red = sm.scratch;
   const int nrb = t.a1 - t.a0;
@@ -608,26 +611,25 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
 #pragma unroll
     for (int i = 0; i < (FMT == AMK_FORMAT_INT4 ? P : 1); ++i) acc1[i] = 0.f;
 #pragma unroll
-    for (int kt = 0; kt < 8; ++kt) {
-      if (kt < M.nkt) {
-        if (!failed) failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx);
-        if (!failed) {
-          const uint32_t tile = ring0 + slot * kSlotBytes;
+    for (int kt = 0; kt < NKT; ++kt) {
+      if (!failed)
+        failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
+      if (!failed) {
+        const uint32_t tile = ring0 + slot * kSlotBytes;
 #pragma unroll
-          for (int ps = 0; ps < P; ++ps) {
-            if constexpr (FMT == AMK_FORMAT_INT4)
-              acc1[ps] = chunk_dot_u4(tile + off0 + ps * pass_stride,
-                                      tile + side_s0 + (uint32_t)(ps * rpp * ngt * 2),
-                                      tile + side_z0 + (uint32_t)(ps * rpp * ngt), h[kt], hs[kt],
-                                      acc1[ps]);
-            else
-              acc2[ps] = chunk_dot<FMT>(tile + off0 + ps * pass_stride, h[kt], acc2[ps]);
-          }
+        for (int ps = 0; ps < P; ++ps) {
+          if constexpr (FMT == AMK_FORMAT_INT4)
+            acc1[ps] = chunk_dot_u4(tile + off0 + ps * pass_stride,
+                                    tile + side_s0 + (uint32_t)(ps * rpp * ngt * 2),
+                                    tile + side_z0 + (uint32_t)(ps * rpp * ngt), h[kt], hs[kt],
+                                    acc1[ps]);
+          else
+            acc2[ps] = chunk_dot<FMT>(tile + off0 + ps * pass_stride, h[kt], acc2[ps]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive32(empty0 + slot * 8);
-        if (++slot == kStages) { slot = 0; phase ^= 1u; }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive32(empty0 + slot * 8);
+      if (++slot == kStages) { slot = 0; phase ^= 1u; }
     }
     float v[P];
 #pragma unroll
@@ -643,6 +645,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
     }
   }
 
+  if (tr) tr[TR_C_STARVED] = starved;
   if (consumer_sync_or(failed)) return -1;
 
   // epilogue: one row (or one row pair) per thread
@@ -709,7 +712,22 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
       }
     }
   }
-  return stage + nrb * M.nkt;
+  return stage + nrb * NKT;
+}
+
+template <int FMT>
+__device__ __forceinline__ int gemv_dispatch(const StepParams& p, Smem& sm, const DevTask& t,
+                                             int stage, uint32_t i, int64_t* tr) {
+  switch (p.m.mat[mat_kind(t.type)].nkt) {
+    case 1: return gemv_task<FMT, 1>(p, sm, t, stage, i, tr);
+    case 2: return gemv_task<FMT, 2>(p, sm, t, stage, i, tr);
+    case 3: return gemv_task<FMT, 3>(p, sm, t, stage, i, tr);
+    case 4: return gemv_task<FMT, 4>(p, sm, t, stage, i, tr);
+    case 5: return gemv_task<FMT, 5>(p, sm, t, stage, i, tr);
+    case 6: return gemv_task<FMT, 6>(p, sm, t, stage, i, tr);
+    case 7: return gemv_task<FMT, 7>(p, sm, t, stage, i, tr);
+    default: return gemv_task<FMT, 8>(p, sm, t, stage, i, tr);
+  }
 }
 
 // Split-K GQA attention of one KV head over one context split.  Per ring
@@ -720,7 +738,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
 // HD: head_dim (a lane owns HD/32 dims of every head), G: query heads per KV head.
 template <int HD, int G>
 __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTask t, int stage,
-                                      uint32_t task_idx) {
+                                      uint32_t task_idx, int64_t* tr) {
   constexpr int DPL = HD / 32;
   constexpr int PPS = (kStageBytes / 2) / (HD * 2);   // positions per stage
   constexpr int NPW = PPS / kConsumerWarps;           // positions per warp per stage
@@ -812,13 +830,15 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   const uint32_t empty0 = smem_addr(&sm.empty[0]);
   uint32_t slot = (uint32_t)(stage % kStages), phase = (uint32_t)((stage / kStages) & 1);
   bool failed = false;
+  int64_t starved = 0;
   int t0, t1;
   attn_range(p.pos, m.splits, j, &t0, &t1);
   int nst = 0;
   for (int s0 = t0; s0 < t1; s0 += PPS) {
     const int np = min(PPS, t1 - s0);
     ++nst;
-    if (!failed) failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx);
+    if (!failed)
+      failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
     if (!failed) {
       const uint32_t kt = ring0 + slot * kSlotBytes;
       const uint32_t vt = kt + kStageBytes / 2;
@@ -872,6 +892,10 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     block(kf, vf, 1);
   }
 
+  if (tr) {
+    tr[TR_C_STARVED] = starved;
+    tr[TR_A_STAGES] = (int64_t)global_timer();
+  }
   // merge the eight warps' partial softmax states
   float* mg = sm.scratch;  // [warp][G][HD + 2]
   constexpr int WS = G * (HD + 2);
@@ -909,6 +933,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     }
   }
   consumer_sync();
+  if (tr) tr[TR_A_MERGED] = (int64_t)global_timer();
 
   // ticket: the last split of this KV head to arrive merges all splits
   if (tid == 0) {
@@ -916,71 +941,91 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     sm.flag = (old + 1u == p.epoch * (uint32_t)m.splits) ? 1 : 0;
   }
   consumer_sync();
+  if (tr) tr[TR_A_TICKET] = (int64_t)global_timer();
   if (sm.flag) {
     // LSE merge of the S splits of this KV head.  Shared memory use is
-    // O(G) for any S: per-head maximum and normaliser by strided partial
-    // reductions, then every output element sums its S partials.
+    // O(G) for any S.  One pass gives each head's maximum M and normaliser
+    // L = sum_s l_s 2^(m_s - M) (running maximum, rescaled sums); then every
+    // output element sums its S partials with independent loads.
     const int S = m.splits;
     const float* pg = m.part + (int64_t)g * S * m.part_stride;
-    float* red = sm.scratch;                 // [8][G] partials, [G] max, [G] 1/L
-    auto m_of = [&](int s, int h) { return __ldcg(pg + (int64_t)s * m.part_stride + h * (HD + 2) + HD); };
-    auto l_of = [&](int s, int h) { return __ldcg(pg + (int64_t)s * m.part_stride + h * (HD + 2) + HD + 1); };
-    const int hh = tid % G;                  // every index tid + k*256 has head tid % G
-    float lm = -INFINITY;
-    for (int idx = tid; idx < S * G; idx += kConsumerThreads) lm = fmaxf(lm, m_of(idx / G, hh));
+    float* red = sm.scratch;  // [8][G] maxima, [8][G] sums, [G] M, [G] 1/L
+    const int hh = tid % G;   // every index tid + k*256 has head tid % G
+    float lm = -INFINITY, ll = 0.f;
+    for (int idx = tid; idx < S * G; idx += kConsumerThreads) {
+      const float* ps = pg + (int64_t)(idx / G) * m.part_stride + hh * (HD + 2) + HD;
+      const float ms = __ldcg(ps), ls = __ldcg(ps + 1);
+      if (ms == -INFINITY) continue;
+      const float mn = fmaxf(lm, ms);
+      ll = (lm == -INFINITY ? 0.f : ll * exp2f(lm - mn)) + ls * exp2f(ms - mn);
+      lm = mn;
+    }
 #pragma unroll
-    for (int msk = G; msk < 32; msk <<= 1) lm = fmaxf(lm, __shfl_xor_sync(0xFFFFFFFFu, lm, msk));
-    if (lane < G) red[warp * G + lane] = lm;
+    for (int msk = G; msk < 32; msk <<= 1) {
+      const float om = __shfl_xor_sync(0xFFFFFFFFu, lm, msk);
+      const float ol = __shfl_xor_sync(0xFFFFFFFFu, ll, msk);
+      const float mn = fmaxf(lm, om);
+      if (mn != -INFINITY) {
+        ll = (lm == -INFINITY ? 0.f : ll * exp2f(lm - mn)) + (om == -INFINITY ? 0.f : ol * exp2f(om - mn));
+        lm = mn;
+      }
+    }
+    if (lane < G) {
+      red[warp * G + lane] = lm;
+      red[8 * G + warp * G + lane] = ll;
+    }
     consumer_sync();
     if (tid < G) {
       float M = -INFINITY;
       for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red[w * G + tid]);
-      red[8 * G + tid] = M;
-    }
-    consumer_sync();
-    const float Mh = red[8 * G + hh];
-    float ll = 0.f;
-    for (int idx = tid; idx < S * G; idx += kConsumerThreads) {
-      const float ms = m_of(idx / G, hh);
-      if (ms != -INFINITY) ll = fmaf(l_of(idx / G, hh), exp2f(ms - Mh), ll);
-    }
-#pragma unroll
-    for (int msk = G; msk < 32; msk <<= 1) ll += __shfl_xor_sync(0xFFFFFFFFu, ll, msk);
-    consumer_sync();                         // everyone has read the maxima's slot area
-    if (lane < G) red[warp * G + lane] = ll;
-    consumer_sync();
-    if (tid < G) {
       float L = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) L += red[w * G + tid];
-      red[9 * G + tid] = 1.0f / L;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float mw = red[w * G + tid];
+        if (mw != -INFINITY) L = fmaf(red[8 * G + w * G + tid], exp2f(mw - M), L);
+      }
+      red[16 * G + tid] = M;
+      red[17 * G + tid] = 1.0f / L;
     }
     consumer_sync();
     for (int idx = tid; idx < G * HD; idx += kConsumerThreads) {
       const int h = idx / HD, d = idx % HD;
-      const float M = red[8 * G + h];
+      const float M = red[16 * G + h];
+      const float* ph = pg + h * (HD + 2);
       float A = 0.f;
-      for (int s = 0; s < S; ++s) {
-        const float* ps = pg + (int64_t)s * m.part_stride + h * (HD + 2);
-        const float ms = __ldcg(ps + HD);
-        if (ms != -INFINITY) A = fmaf(__ldcg(ps + d), exp2f(ms - M), A);
+      int s = 0;
+      for (; s + 8 <= S; s += 8) {
+        float ms[8], av[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          ms[u] = __ldcg(ph + (int64_t)(s + u) * m.part_stride + HD);
+          av[u] = __ldcg(ph + (int64_t)(s + u) * m.part_stride + d);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (ms[u] != -INFINITY) A = fmaf(av[u], exp2f(ms[u] - M), A);
       }
-      m.o[(int64_t)(g * G + h) * HD + d] = A * red[9 * G + h];
+      for (; s < S; ++s) {
+        const float ms = __ldcg(ph + (int64_t)s * m.part_stride + HD);
+        if (ms != -INFINITY) A = fmaf(__ldcg(ph + (int64_t)s * m.part_stride + d), exp2f(ms - M), A);
+      }
+      m.o[(int64_t)(g * G + h) * HD + d] = A * red[17 * G + h];
     }
     consumer_sync();
     if (tid == 0) red_release_add(m.counters + t.a2, 1u);
+    if (tr) tr[TR_A_COMBINED] = (int64_t)global_timer();
   }
   return stage + nst;
 }
 
 template <int HD>
 __device__ __forceinline__ int attn_dispatch(const StepParams& p, Smem& sm, const DevTask& t,
-                                             int stage, uint32_t i) {
+                                             int stage, uint32_t i, int64_t* tr) {
   switch (p.m.group) {
-    case 1: return attn_task<HD, 1>(p, sm, t, stage, i);
-    case 2: return attn_task<HD, 2>(p, sm, t, stage, i);
-    case 4: return attn_task<HD, 4>(p, sm, t, stage, i);
+    case 1: return attn_task<HD, 1>(p, sm, t, stage, i, tr);
+    case 2: return attn_task<HD, 2>(p, sm, t, stage, i, tr);
+    case 4: return attn_task<HD, 4>(p, sm, t, stage, i, tr);
     default:
-      if constexpr (HD == 64) return attn_task<HD, 8>(p, sm, t, stage, i);
+      if constexpr (HD == 64) return attn_task<HD, 8>(p, sm, t, stage, i, tr);
       return -1;
   }
 }
@@ -1007,11 +1052,12 @@ __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       return;
     }
     if (tr && tid == 0) tr[TR_C_WAITED] = (int64_t)global_timer();
+    int64_t* tr0 = tid == 0 ? tr : nullptr;
     if (t.type == T_ATTN)
-      stage = m.head_dim == 128 ? attn_dispatch<128>(p, sm, t, stage, (uint32_t)i)
-                                : attn_dispatch<64>(p, sm, t, stage, (uint32_t)i);
-    else if (t.type == T_LMHEAD) stage = gemv_task<LM_FMT>(p, sm, t, stage, (uint32_t)i);
-    else stage = gemv_task<QKV_FMT>(p, sm, t, stage, (uint32_t)i);
+      stage = m.head_dim == 128 ? attn_dispatch<128>(p, sm, t, stage, (uint32_t)i, tr0)
+                                : attn_dispatch<64>(p, sm, t, stage, (uint32_t)i, tr0);
+    else if (t.type == T_LMHEAD) stage = gemv_dispatch<LM_FMT>(p, sm, t, stage, (uint32_t)i, tr0);
+    else stage = gemv_dispatch<QKV_FMT>(p, sm, t, stage, (uint32_t)i, tr0);
     if (stage < 0) {
       *abort_flag = 1;
       return;
@@ -1045,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int q0 = p.m.queue_off[c];
   const int n = p.skip_lm ? p.m.queue_body[c] : p.m.queue_off[c + 1] - q0;
   const DevTask* q = p.m.tasks + q0;
-  int64_t* hdr = p.trace ? p.trace + (int64_t)c * (1 + p.trace_stride) * 8 : nullptr;
+  int64_t* hdr = p.trace ? p.trace + (int64_t)c * (1 + p.trace_stride) * kTraceWords : nullptr;
   if (hdr && tid == 0) {
     hdr[0] = (int64_t)global_timer();
     hdr[1] = clock64();

@@ -64,19 +64,23 @@ struct StepParams {
   int32_t skip_lm;
   uint64_t timeout_ns;
   // optional per-task timestamps (tuning aid): null, or
-  // int64 [num_ctas][1 + trace_stride][8], see kTrace* below
+  // int64 [num_ctas][1 + trace_stride][kTraceWords], see TraceWord below
   int64_t* trace;
   int32_t trace_stride;
   int32_t pad1;
 };
 
-// Trace record words.  Row 0 of a CTA: start / end %globaltimer and clock64.
-// Row 1 + i for task i: consumer begin (before its wait), wait satisfied,
-// main loop done, signalled; producer first / last issue, cycles blocked on
-// a full ring; task type | layer << 8.
+// Trace record words.  Row 0 of a CTA: start / end %globaltimer and clock64,
+// task count.  Row 1 + i for task i: consumer begin (before its wait), wait
+// satisfied, main loop done, signalled; producer first / last issue, cycles
+// blocked on a full ring; task type | layer << 8; consumer cycles spent
+// waiting for ring data; attention only: stage loop done, warp merge and
+// partial stored, ticket taken, split merge done (last split only).
+constexpr int kTraceWords = 16;
 enum TraceWord : int {
   TR_C_BEGIN = 0, TR_C_WAITED = 1, TR_C_DONE = 2, TR_C_SIGNALLED = 3,
-  TR_P_FIRST = 4, TR_P_LAST = 5, TR_P_BLOCKED = 6, TR_TAG = 7
+  TR_P_FIRST = 4, TR_P_LAST = 5, TR_P_BLOCKED = 6, TR_TAG = 7,
+  TR_C_STARVED = 8, TR_A_STAGES = 9, TR_A_MERGED = 10, TR_A_TICKET = 11, TR_A_COMBINED = 12
 };
 
 enum DevStatus : uint32_t {

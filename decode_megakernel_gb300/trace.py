@@ -18,10 +18,11 @@ import sys
 import numpy as np
 
 TYPE_NAMES = {0: "qkv", 1: "attn", 2: "o_proj", 3: "gate_up", 4: "down", 5: "lm_head"}
+WORDS = 16  # int64 words per trace row
 
 
 def trace_step(dec, token: int, pos: int, logits):
-    """Run one traced decode step; returns int64 [num_ctas, 1 + S, 8]."""
+    """Run one traced decode step; returns int64 [num_ctas, 1 + S, 16]."""
     import torch
 
     from . import amk
@@ -29,7 +30,7 @@ def trace_step(dec, token: int, pos: int, logits):
     buf = torch.zeros(nbytes // 8, dtype=torch.int64, device=logits.device)
     amk.check(amk.amk_debug_trace_step(dec.ctx, token, pos, logits.data_ptr(), buf.data_ptr(),
                                        nbytes), dec.ctx)
-    return buf.cpu().numpy().reshape(-1, 1 + stride, 8)
+    return buf.cpu().numpy().reshape(-1, 1 + stride, WORDS)
 
 
 def summarize(tr: np.ndarray, n_layers: int) -> str:
@@ -44,10 +45,12 @@ def summarize(tr: np.ndarray, n_layers: int) -> str:
             rows.append((c, int(r[7]) & 0xFF, int(r[7]) >> 8, r))
     out = [f"step {step_us:.1f} us on {tr.shape[0]} CTAs; SM clock ~{clk_ghz:.2f} GHz"]
     out.append(f"{'task':8s} {'wait':>8s} {'work':>8s} {'work max':>9s} {'signal':>7s} "
-               f"{'span':>8s} {'blocked':>8s}   (us, mean over layers; wait/work/signal mean over CTAs)")
+               f"{'span':>8s} {'blocked':>8s} {'starved':>8s}   (us, mean over layers; "
+               f"wait/work/signal/blocked/starved mean over CTAs)")
     # phase order along the critical path
     order = [0, 1, 2, 3, 4]
     prev_end = {}
+    att = []
     spans = {k: [] for k in order + [5]}
     stats = {k: [] for k in order + [5]}
     for layer in range(n_layers):
@@ -60,11 +63,17 @@ def summarize(tr: np.ndarray, n_layers: int) -> str:
             work = (a[:, 2] - a[:, 1]) / 1e3
             sig = (a[:, 3] - a[:, 2]) / 1e3
             blocked = a[:, 6] / clk_ghz / 1e3
+            starved = a[:, 8] / clk_ghz / 1e3
+            if ty == 1:
+                att.append(((a[:, 9] - a[:, 1]).mean() / 1e3, (a[:, 10] - a[:, 9]).mean() / 1e3,
+                            (a[:, 11] - a[:, 10]).mean() / 1e3,
+                            ((a[:, 12] - a[:, 11])[a[:, 12] > 0]).mean() / 1e3))
             end = a[:, 3].max()
             start_ref = prev_end.get("last", a[:, 0].min())
             spans[ty].append((end - start_ref) / 1e3)
             prev_end["last"] = end
-            stats[ty].append((wait.mean(), work.mean(), work.max(), sig.mean(), blocked.mean()))
+            stats[ty].append((wait.mean(), work.mean(), work.max(), sig.mean(), blocked.mean(),
+                              starved.mean()))
     total_span = 0.0
     for ty in order + [5]:
         if not stats[ty]:
@@ -73,8 +82,12 @@ def summarize(tr: np.ndarray, n_layers: int) -> str:
         sp = float(np.mean(spans[ty]))
         total_span += sp * len(spans[ty])
         out.append(f"{TYPE_NAMES[ty]:8s} {s[0]:8.2f} {s[1]:8.2f} {s[2]:9.2f} {s[3]:7.2f} "
-                   f"{sp:8.2f} {s[4]:8.2f}")
+                   f"{sp:8.2f} {s[4]:8.2f} {s[5]:8.2f}")
     out.append(f"sum of spans {total_span:.1f} us")
+    if att:
+        a = np.array(att).mean(0)
+        out.append(f"attention: stage loop {a[0]:.2f}, warp merge + partial store {a[1]:.2f}, "
+                   f"ticket {a[2]:.2f}, split merge (last split) {a[3]:.2f} us")
     return "\n".join(out)
 
 

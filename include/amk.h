@@ -234,13 +234,16 @@ amk_status amk_debug_watchdog_probe(void* scratch_dev, void* stream, int32_t lim
  * Per-task timestamps of one decode step (tuning aid, in the spirit of the
  * region timing of the Argus page, "Case 3").  amk_debug_trace_bytes gives
  * the int64 buffer size and, in *stride, the longest task queue S.  The
- * buffer is [num_ctas][1 + S][8]: row 0 of a CTA holds its start and end
+ * buffer is [num_ctas][1 + S][16]: row 0 of a CTA holds its start and end
  * %globaltimer (ns) and clock64, and its task count; row 1 + i holds, for
  * its i-th task: consumer begin (before the counter wait), wait satisfied,
  * work done, signalled (%globaltimer ns); producer first and last copy
  * issued (ns) and clock64 cycles blocked on a full ring; task type | layer
- * << 8.  amk_debug_trace_step runs amk_decode_step with the recording on
- * and waits for it.  trace_dev: caller device memory, 8-byte aligned.
+ * << 8; consumer clock64 cycles spent waiting for ring data; for attention
+ * tasks, the ends of the stage loop, of the warp merge, of the ticket and
+ * (last split only) of the split merge (ns).  amk_debug_trace_step runs
+ * amk_decode_step with the recording on and waits for it.  trace_dev:
+ * caller device memory, 8-byte aligned.
  */
 size_t amk_debug_trace_bytes(const amk_ctx* ctx, int32_t* stride);
 amk_status amk_debug_trace_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits_dev,
