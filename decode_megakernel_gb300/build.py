@@ -47,8 +47,9 @@ def _run(cmd):
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link libamk.so; returns its path."""
-    if not force and not stale():
+    """Compile and link libamk.so; returns its path.  extra_flags (e.g.
+    -DAMK_STAGE_BYTES=16384 to build 16 KB tiles) force a rebuild."""
+    if not force and not extra_flags and not stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     flags = FLAGS + list(extra_flags or [])

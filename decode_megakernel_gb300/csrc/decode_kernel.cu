@@ -5,8 +5,9 @@
 // AutoMegaKernel "Layer 0" VM).  Unlike the pages' design, a CTA is split
 // into a producer warp and eight consumer warps:
 //   * the producer streams every weight tile (and the KV-cache history) of
-//     the CTA's whole queue through a 12-slot shared-memory ring with 1-D
-//     TMA bulk copies completing on mbarriers.  Weights never depend on
+//     the CTA's whole queue through a shared-memory ring of kStageBytes
+//     stages (128 KB in flight by default) with 1-D TMA bulk copies
+//     completing on mbarriers.  Weights never depend on
 //     activations, so the producer runs ahead across the counter waits;
 //     this hides the per-tile cross-SM synchronisation cost the pages name
 //     as the bottleneck on high-bandwidth GPUs (AMK "Experimental results":
@@ -225,66 +226,156 @@ __device__ __forceinline__ int64_t* trace_row(const StepParams& p, int i) {
   return p.trace + ((int64_t)blockIdx.x * (1 + p.trace_stride) + 1 + i) * kTraceWords;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// The tiles one task streams through the ring, in order.  A weight task's
+// tiles are consecutive stage_bytes chunks of one contiguous range; an
+// attention task's tile s holds K then V of up to pps cached positions.
+struct TaskTiles {
+  const uint8_t* k = nullptr;
+  const uint8_t* v = nullptr;
+  int64_t stride = 0;   // weights: bytes between tiles
+  uint32_t bytes = 0;   // weights: bytes per tile
+  int nst = 0;          // number of tiles
+  int t0 = 0, t1 = 0, pps = 0, row = 0;  // attention: positions, per stage, bytes per position
+  bool attn = false;
+};
+
+__device__ __forceinline__ TaskTiles task_tiles(const StepParams& p, const DevTask& t) {
+  const DevModel& m = p.m;
+  TaskTiles tt;
+  if (t.type == T_ATTN) {
+    attn_range(p.pos, m.splits, t.a1, &tt.t0, &tt.t1);
+    tt.pps = attn_positions_per_stage(m.head_dim);
+    tt.row = m.head_dim * 2;
+    tt.k = reinterpret_cast<const uint8_t*>(kv_row(m, t.layer, 0, t.a0, 0));
+    tt.v = reinterpret_cast<const uint8_t*>(kv_row(m, t.layer, 1, t.a0, 0));
+    tt.nst = (tt.t1 - tt.t0 + tt.pps - 1) / tt.pps;
+    tt.attn = true;
+  } else {
+    const int kind = mat_kind(t.type);
+    const DevMat M = m.mat[kind];
+    tt.k = M.base + (kind == M_LM ? 0 : (int64_t)t.layer * M.layer_bytes) + (int64_t)t.a0 * M.rb_bytes;
+    tt.stride = M.stage_bytes;
+    tt.bytes = (uint32_t)M.stage_bytes;
+    tt.nst = (t.a1 - t.a0) * M.nkt;
+  }
+  return tt;
+}
+
+// Producer: one thread streams every tile of the CTA's queue into the ring.
+// Whenever no slot is free it prefetches later tiles into L2 (up to
+// m.prefetch_tiles ahead of the last copy), so HBM keeps streaming while the
+// consumers wait on a counter; the ring copies then hit L2.
 __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_kv = policy_evict_normal();
   volatile int32_t* abort_flag = &sm.abort_flag;
+  const uint32_t nslots = (uint32_t)m.ring_slots;
   uint32_t slot = 0, phase = 0;
   uint32_t issued = 0;     // slots that have held a copy
   uint32_t parity = 0;     // parity of each slot's last issued phase
   bool ok = true;
-  for (int i = 0; i < n && ok; ++i) {
-    const DevTask t = q[i];
-    int64_t blocked = 0;
-    if (p.trace) trace_row(p, i)[TR_P_FIRST] = (int64_t)global_timer();
-    if (t.type == T_ATTN) {
-      int t0, t1;
-      attn_range(p.pos, m.splits, t.a1, &t0, &t1);
-      const int pps = attn_positions_per_stage(m.head_dim);
-      const uint16_t* kb = kv_row(m, t.layer, 0, t.a0, 0);
-      const uint16_t* vb = kv_row(m, t.layer, 1, t.a0, 0);
-      for (int s0 = t0; s0 < t1 && ok; s0 += pps) {
-        const int np = min(pps, t1 - s0);
-        const uint32_t bytes = (uint32_t)np * m.head_dim * 2;
-        const int64_t c0 = p.trace ? clock64() : 0;
-        ok = wait_phase(&sm.empty[slot], phase ^ 1u, m.status, abort_flag, p.timeout_ns, i,
-                        SITE_EMPTY) && !*abort_flag;
-        if (p.trace) blocked += clock64() - c0;
-        if (!ok) break;
+  const int64_t ahead = m.prefetch_tiles;
+
+  int ct = 0, cs = 0;                // copy cursor: task, tile
+  TaskTiles ctt;
+  bool cvalid = false;
+  int pt = 0, ps = 0;                // prefetch cursor
+  TaskTiles ptt;
+  bool pvalid = false;
+  int64_t copied = 0, prefetched = 0;
+  int64_t blocked = 0;
+
+  while (ct < n && ok) {
+    if (!cvalid) {
+      ctt = task_tiles(p, q[ct]);
+      cs = 0;
+      cvalid = true;
+      blocked = 0;
+      if (p.trace) trace_row(p, ct)[TR_P_FIRST] = (int64_t)global_timer();
+    }
+    if (cs == ctt.nst) {
+      if (p.trace) {
+        int64_t* tr = trace_row(p, ct);
+        tr[TR_P_LAST] = (int64_t)global_timer();
+        tr[TR_P_BLOCKED] = blocked;
+      }
+      ++ct;
+      cvalid = false;
+      continue;
+    }
+    if (mbar_test_wait(&sm.empty[slot], phase ^ 1u)) {
+      if (*abort_flag) { ok = false; break; }
+      if (ctt.attn) {
+        const int p0 = ctt.t0 + cs * ctt.pps;
+        const uint32_t bytes = (uint32_t)(min(ctt.pps, ctt.t1 - p0) * ctt.row);
         mbar_arrive_expect_tx(&sm.full[slot], 2 * bytes);
-        bulk_copy_g2s(sm.ring[slot], kb + (int64_t)s0 * m.head_dim, bytes, &sm.full[slot], pol_kv);
-        bulk_copy_g2s(sm.ring[slot] + kStageBytes / 2, vb + (int64_t)s0 * m.head_dim, bytes,
+        bulk_copy_g2s(sm.ring[slot], ctt.k + (int64_t)p0 * ctt.row, bytes, &sm.full[slot], pol_kv);
+        bulk_copy_g2s(sm.ring[slot] + kStageBytes / 2, ctt.v + (int64_t)p0 * ctt.row, bytes,
                       &sm.full[slot], pol_kv);
-        issued |= 1u << slot;
-        parity = (parity & ~(1u << slot)) | (phase << slot);
-        if (++slot == kStages) { slot = 0; phase ^= 1u; }
+      } else {
+        mbar_arrive_expect_tx(&sm.full[slot], ctt.bytes);
+        bulk_copy_g2s(sm.ring[slot], ctt.k + (int64_t)cs * ctt.stride, ctt.bytes, &sm.full[slot], pol_w);
       }
-    } else {
-      const int kind = mat_kind(t.type);
-      const DevMat M = m.mat[kind];
-      const uint8_t* src = M.base + (kind == M_LM ? 0 : (int64_t)t.layer * M.layer_bytes) +
-                           (int64_t)t.a0 * M.rb_bytes;
-      const int nst = (t.a1 - t.a0) * M.nkt;
-      for (int s = 0; s < nst && ok; ++s) {
-        const int64_t c0 = p.trace ? clock64() : 0;
-        ok = wait_phase(&sm.empty[slot], phase ^ 1u, m.status, abort_flag, p.timeout_ns, i,
-                        SITE_EMPTY) && !*abort_flag;
-        if (p.trace) blocked += clock64() - c0;
-        if (!ok) break;
-        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)M.stage_bytes);
-        bulk_copy_g2s(sm.ring[slot], src + (int64_t)s * M.stage_bytes, (uint32_t)M.stage_bytes,
-                      &sm.full[slot], pol_w);
-        issued |= 1u << slot;
-        parity = (parity & ~(1u << slot)) | (phase << slot);
-        if (++slot == kStages) { slot = 0; phase ^= 1u; }
+      issued |= 1u << slot;
+      parity = (parity & ~(1u << slot)) | (phase << slot);
+      if (++slot == nslots) { slot = 0; phase ^= 1u; }
+      ++cs;
+      ++copied;
+      continue;
+    }
+    // no free slot: prefetch a later tile into L2 while there is one in reach
+    if (prefetched < copied) {  // the copies overtook the prefetches
+      pt = ct;
+      ps = cs;
+      ptt = ctt;
+      pvalid = true;
+      prefetched = copied;
+    }
+    if (pt < n && prefetched < copied + ahead) {
+      if (!pvalid) {
+        ptt = task_tiles(p, q[pt]);
+        ps = 0;
+        pvalid = true;
       }
+      if (ps >= ptt.nst) {
+        ++pt;
+        pvalid = false;
+        continue;
+      }
+      if (ptt.attn) {
+        const int p0 = ptt.t0 + ps * ptt.pps;
+        const uint32_t bytes = (uint32_t)(min(ptt.pps, ptt.t1 - p0) * ptt.row);
+        prefetch_l2(ptt.k + (int64_t)p0 * ptt.row, bytes);
+        prefetch_l2(ptt.v + (int64_t)p0 * ptt.row, bytes);
+      } else {
+        prefetch_l2(ptt.k + (int64_t)ps * ptt.stride, ptt.bytes);
+      }
+      ++ps;
+      ++prefetched;
+      continue;
     }
-    if (p.trace) {
-      int64_t* tr = trace_row(p, i);
-      tr[TR_P_LAST] = (int64_t)global_timer();
-      tr[TR_P_BLOCKED] = blocked;
-    }
+    // nothing to issue: wait for the oldest slot to be released
+    const int64_t c0 = p.trace ? clock64() : 0;
+    ok = wait_phase(&sm.empty[slot], phase ^ 1u, m.status, abort_flag, p.timeout_ns, ct,
+                    SITE_EMPTY) && !*abort_flag;
+    if (p.trace) blocked += clock64() - c0;
   }
   // Every copy this CTA issued must land before its shared memory goes away.
   // Consumers normally wait for all of them already; when they stop early
@@ -301,7 +392,6 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       }
     }
   }
-  (void)ok;
 }
 
 // -------------------------------------------------------------- consumers
@@ -382,9 +472,14 @@ __device__ __forceinline__ bool mbar_try_wait32(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, const StepParams& p,
                                           volatile int32_t* abort_flag, uint32_t task,
                                           int64_t* starved = nullptr) {
-  if (mbar_try_wait32(bar, parity)) return true;
-  const uint64_t t0 = global_timer();
+  // try_wait itself blocks for a while before reporting an incomplete
+  // phase, so a starvation measurement must time the first call too
   const int64_t c0 = starved ? clock64() : 0;
+  if (mbar_try_wait32(bar, parity)) {
+    if (starved) *starved += clock64() - c0;
+    return true;
+  }
+  const uint64_t t0 = global_timer();
   for (uint32_t spin = 1;; ++spin) {
     if (mbar_try_wait32(bar, parity)) {
       if (starved) *starved += clock64() - c0;
@@ -401,12 +496,13 @@ __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, const S
 
 template <int FMT>
 struct Fmt;
+// passes per tile = tile bytes / (256 threads x chunk bytes)
 template <>
-struct Fmt<AMK_FORMAT_BF16> { static constexpr int kPasses = 4, kChunkBytes = 16; };
+struct Fmt<AMK_FORMAT_BF16> { static constexpr int kChunkBytes = 16, kPasses = kStageBytes / (256 * 16); };
 template <>
-struct Fmt<AMK_FORMAT_INT8> { static constexpr int kPasses = 8, kChunkBytes = 8; };
+struct Fmt<AMK_FORMAT_INT8> { static constexpr int kChunkBytes = 8, kPasses = kStageBytes / (256 * 8); };
 template <>
-struct Fmt<AMK_FORMAT_INT4> { static constexpr int kPasses = 16, kChunkBytes = 4; };
+struct Fmt<AMK_FORMAT_INT4> { static constexpr int kChunkBytes = 4, kPasses = kStageBytes / (256 * 4); };
 
 // Sum P per-lane values over the warp.  Lanes whose low (5 - log2 P) bits
 // are zero return the total of value index (lane >> (5 - log2 P)); the other
@@ -597,7 +693,8 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   const int ngt = M.Kt >> 7;
   const uint32_t side_s0 = kStageBytes + (uint32_t)((rsub * ngt + (chunk >> 4)) * 2);
   const uint32_t side_z0 = kStageBytes + (uint32_t)(M.Rt * ngt * 2 + rsub * ngt + (chunk >> 4));
-  uint32_t slot = (uint32_t)(stage % kStages), phase = (uint32_t)((stage / kStages) & 1);
+  const uint32_t nslots = (uint32_t)m.ring_slots;
+  uint32_t slot = (uint32_t)stage % nslots, phase = ((uint32_t)stage / nslots) & 1u;
   bool failed = false;
   int64_t starved = 0;
 
@@ -629,7 +726,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
       }
       __syncwarp();
       if (lane == 0) mbar_arrive32(empty0 + slot * 8);
-      if (++slot == kStages) { slot = 0; phase ^= 1u; }
+      if (++slot == nslots) { slot = 0; phase ^= 1u; }
     }
     float v[P];
 #pragma unroll
@@ -742,7 +839,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   constexpr int DPL = HD / 32;
   constexpr int PPS = (kStageBytes / 2) / (HD * 2);   // positions per stage
   constexpr int NPW = PPS / kConsumerWarps;           // positions per warp per stage
-  constexpr int R = (16 / G) < NPW ? (16 / G) : NPW;  // positions per block
+  constexpr int R = (32 / G) < NPW ? (32 / G) : NPW;  // positions per block
   constexpr int V = R * G;                            // scores per block
   constexpr int LS = 32 / V;                          // lanes per score after the reduction
   const DevModel& m = p.m;
@@ -828,7 +925,8 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
   const uint32_t full0 = smem_addr(&sm.full[0]);
   const uint32_t empty0 = smem_addr(&sm.empty[0]);
-  uint32_t slot = (uint32_t)(stage % kStages), phase = (uint32_t)((stage / kStages) & 1);
+  const uint32_t nslots = (uint32_t)m.ring_slots;
+  uint32_t slot = (uint32_t)stage % nslots, phase = ((uint32_t)stage / nslots) & 1u;
   bool failed = false;
   int64_t starved = 0;
   int t0, t1;
@@ -869,7 +967,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     }
     __syncwarp();
     if (lane == 0) mbar_arrive32(empty0 + slot * 8);
-    if (++slot == kStages) { slot = 0; phase ^= 1u; }
+    if (++slot == nslots) { slot = 0; phase ^= 1u; }
   }
   // the current position, written this step by the QKV tasks
   if (!failed && j == m.splits - 1 && warp == 0) {
@@ -943,72 +1041,74 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   consumer_sync();
   if (tr) tr[TR_A_TICKET] = (int64_t)global_timer();
   if (sm.flag) {
-    // LSE merge of the S splits of this KV head.  Shared memory use is
-    // O(G) for any S.  One pass gives each head's maximum M and normaliser
-    // L = sum_s l_s 2^(m_s - M) (running maximum, rescaled sums); then every
-    // output element sums its S partials with independent loads.
+    // LSE merge of the S splits of this KV head, in chunks of up to SC splits.
+    // Per chunk every load is issued at once (the (m, l) pairs by one thread
+    // each, every output element's SC partial sums by its thread), so a
+    // chunk costs one L2 round trip; a running (M, L, A) per element folds
+    // the chunks together.  Shared memory: 2 * SC * G floats.
+    constexpr int SC = 24;
+    constexpr int EPT = (G * HD + kConsumerThreads - 1) / kConsumerThreads;  // elements per thread
+    static_assert(SC * G <= kConsumerThreads, "one (m, l) pair per thread");
     const int S = m.splits;
     const float* pg = m.part + (int64_t)g * S * m.part_stride;
-    float* red = sm.scratch;  // [8][G] maxima, [8][G] sums, [G] M, [G] 1/L
-    const int hh = tid % G;   // every index tid + k*256 has head tid % G
-    float lm = -INFINITY, ll = 0.f;
-    for (int idx = tid; idx < S * G; idx += kConsumerThreads) {
-      const float* ps = pg + (int64_t)(idx / G) * m.part_stride + hh * (HD + 2) + HD;
-      const float ms = __ldcg(ps), ls = __ldcg(ps + 1);
-      if (ms == -INFINITY) continue;
-      const float mn = fmaxf(lm, ms);
-      ll = (lm == -INFINITY ? 0.f : ll * exp2f(lm - mn)) + ls * exp2f(ms - mn);
-      lm = mn;
-    }
+    float* ml = sm.scratch;  // [SC][G] maxima, then [SC][G] normalisers
+    float runM[EPT], runL[EPT], runA[EPT];
 #pragma unroll
-    for (int msk = G; msk < 32; msk <<= 1) {
-      const float om = __shfl_xor_sync(0xFFFFFFFFu, lm, msk);
-      const float ol = __shfl_xor_sync(0xFFFFFFFFu, ll, msk);
-      const float mn = fmaxf(lm, om);
-      if (mn != -INFINITY) {
-        ll = (lm == -INFINITY ? 0.f : ll * exp2f(lm - mn)) + (om == -INFINITY ? 0.f : ol * exp2f(om - mn));
-        lm = mn;
+    for (int e = 0; e < EPT; ++e) { runM[e] = -INFINITY; runL[e] = 0.f; runA[e] = 0.f; }
+    for (int c0 = 0; c0 < S; c0 += SC) {
+      const int sc = min(SC, S - c0);
+      float mv = 0.f, lv = 0.f;
+      if (tid < sc * G) {
+        const float* pp = pg + (int64_t)(c0 + tid / G) * m.part_stride + (tid % G) * (HD + 2) + HD;
+        mv = __ldcg(pp);
+        lv = __ldcg(pp + 1);
       }
-    }
-    if (lane < G) {
-      red[warp * G + lane] = lm;
-      red[8 * G + warp * G + lane] = ll;
-    }
-    consumer_sync();
-    if (tid < G) {
-      float M = -INFINITY;
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red[w * G + tid]);
-      float L = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float mw = red[w * G + tid];
-        if (mw != -INFINITY) L = fmaf(red[8 * G + w * G + tid], exp2f(mw - M), L);
-      }
-      red[16 * G + tid] = M;
-      red[17 * G + tid] = 1.0f / L;
-    }
-    consumer_sync();
-    for (int idx = tid; idx < G * HD; idx += kConsumerThreads) {
-      const int h = idx / HD, d = idx % HD;
-      const float M = red[16 * G + h];
-      const float* ph = pg + h * (HD + 2);
-      float A = 0.f;
-      int s = 0;
-      for (; s + 8 <= S; s += 8) {
-        float ms[8], av[8];
+      float av[EPT][SC];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          ms[u] = __ldcg(ph + (int64_t)(s + u) * m.part_stride + HD);
-          av[u] = __ldcg(ph + (int64_t)(s + u) * m.part_stride + d);
+      for (int e = 0; e < EPT; ++e) {
+        const int idx = tid + e * kConsumerThreads;
+        const int h = idx / HD, d = idx % HD;
+#pragma unroll
+        for (int s2 = 0; s2 < SC; ++s2)
+          av[e][s2] = (idx < G * HD && s2 < sc)
+                          ? __ldcg(pg + (int64_t)(c0 + s2) * m.part_stride + h * (HD + 2) + d) : 0.f;
+      }
+      if (tid < sc * G) {
+        ml[tid] = mv;
+        ml[SC * G + tid] = lv;
+      }
+      consumer_sync();
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const int idx = tid + e * kConsumerThreads;
+        if (idx >= G * HD) continue;
+        const int h = idx / HD;
+        float Mc = -INFINITY;
+        for (int s2 = 0; s2 < sc; ++s2) Mc = fmaxf(Mc, ml[s2 * G + h]);
+        if (Mc == -INFINITY) continue;
+        float Lc = 0.f, Ac = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < SC; ++s2) {
+          if (s2 < sc) {
+            const float ms = ml[s2 * G + h];
+            const float w = ms == -INFINITY ? 0.f : exp2f(ms - Mc);
+            Lc = fmaf(ml[SC * G + s2 * G + h], w, Lc);
+            Ac = fmaf(av[e][s2], w, Ac);
+          }
         }
+        const float Mn = fmaxf(runM[e], Mc);
+        const float wr = runM[e] == -INFINITY ? 0.f : exp2f(runM[e] - Mn);
+        const float wc = exp2f(Mc - Mn);
+        runL[e] = runL[e] * wr + Lc * wc;
+        runA[e] = runA[e] * wr + Ac * wc;
+        runM[e] = Mn;
+      }
+      consumer_sync();  // the next chunk reuses ml
+    }
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (ms[u] != -INFINITY) A = fmaf(av[u], exp2f(ms[u] - M), A);
-      }
-      for (; s < S; ++s) {
-        const float ms = __ldcg(ph + (int64_t)s * m.part_stride + HD);
-        if (ms != -INFINITY) A = fmaf(__ldcg(ph + (int64_t)s * m.part_stride + d), exp2f(ms - M), A);
-      }
-      m.o[(int64_t)(g * G + h) * HD + d] = A * red[17 * G + h];
+    for (int e = 0; e < EPT; ++e) {
+      const int idx = tid + e * kConsumerThreads;
+      if (idx < G * HD) m.o[(int64_t)(g * G + idx / HD) * HD + idx % HD] = runA[e] / runL[e];
     }
     consumer_sync();
     if (tid == 0) red_release_add(m.counters + t.a2, 1u);
@@ -1093,9 +1193,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const DevTask* q = p.m.tasks + q0;
   int64_t* hdr = p.trace ? p.trace + (int64_t)c * (1 + p.trace_stride) * kTraceWords : nullptr;
   if (hdr && tid == 0) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
     hdr[0] = (int64_t)global_timer();
     hdr[1] = clock64();
     hdr[4] = n;
+    hdr[5] = smid;
   }
   if (tid >= kConsumerThreads) {
     if (tid == kConsumerThreads) producer_loop(p, sm, q, n);

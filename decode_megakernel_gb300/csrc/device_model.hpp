@@ -36,6 +36,8 @@ struct DevModel {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, max_seq;
   int32_t group, splits, part_stride, num_ctas;
   float rms_eps;
+  int32_t prefetch_tiles;      // tiles the producer may prefetch into L2 ahead of its copies
+  int32_t ring_slots;          // slots of the ring in use (1 <= ring_slots <= kStages)
   int32_t pad0;
   const uint16_t* embed;       // bf16 [vocab][hidden], row major
   const uint16_t* final_norm;  // bf16 [hidden]
@@ -93,8 +95,9 @@ enum WaitSite : uint32_t {
 // kernel geometry
 constexpr int kConsumerWarps = kConsumerThreads / 32;  // 8
 constexpr int kThreads = kConsumerThreads + 32;        // + one producer warp
-constexpr int kStages = 12;
-constexpr int kSlotBytes = kStageBytes + kSideBytes;   // 17408
+constexpr int kRingBytes = 196608;                     // 192 KB of slots at most
+constexpr int kStages = kRingBytes / kStageBytes;      // slots that fit (ring_slots <= kStages)
+constexpr int kSlotBytes = kStageBytes + kSideBytes;   // 34816
 constexpr int kScratchFloats = 4352;                   // GEMV row partials / attention merge
 constexpr int kSmemBytes = kStages * kSlotBytes + kScratchFloats * 4 + 2 * kStages * 8 + 256;
 

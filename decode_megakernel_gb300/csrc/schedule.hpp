@@ -77,21 +77,24 @@ struct Schedule {
 
 // Tiled layout of one weight matrix in the workspace.  Rows are grouped in
 // row blocks of Rt rows; a row block is nkt tiles of [Rt x Kt] elements,
-// each tile one 16 KB TMA stage; in_features is zero-padded to Kp = nkt*Kt.
+// each tile one TMA stage of kStageBytes; in_features is zero-padded to Kp = nkt*Kt.
 struct MatGeom {
   int32_t fmt = 0;
   int32_t rows = 0, rows_padded = 0;  // real rows, rows padded to Rt
   int32_t K = 0, Kp = 0, Kt = 0, nkt = 0, Rt = 0;
   int32_t cpr_shift = 0;              // log2(Kt / 8): threads sharing one row
-  int64_t tile_bytes = 0;             // code bytes of one tile (16384)
+  int64_t tile_bytes = 0;             // code bytes of one tile (kStageBytes)
   int64_t side_bytes = 0;             // per-tile scale/zero bytes (int4)
   int64_t rb_bytes = 0;               // one row block: nkt * (tile + side)
   int64_t bytes = 0;                  // whole matrix
   int32_t n_rb() const { return rows_padded / Rt; }
 };
 
-constexpr int kStageBytes = 16384;
-constexpr int kSideBytes = 1024;
+#ifndef AMK_STAGE_BYTES
+#define AMK_STAGE_BYTES 16384
+#endif
+constexpr int kStageBytes = AMK_STAGE_BYTES;    // one weight tile = one ring stage
+constexpr int kSideBytes = kStageBytes / 16;     // int4 scales / zeros of a tile
 constexpr int kConsumerThreads = 256;
 constexpr int kRowsMax = 256;
 constexpr int kMaxHReg = 64;        // activation floats a consumer thread keeps in registers

@@ -106,6 +106,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama8b-bf16")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--num-ctas", type=int, default=0)
+    ap.add_argument("--ring-slots", type=int, default=0)
+    ap.add_argument("--l2-prefetch-tiles", type=int, default=0)
     ap.add_argument("--save", default="")
     args = ap.parse_args(argv)
     wl = wc.workload(args.workload)
@@ -114,7 +116,9 @@ def main(argv=None):
     w = synth.model_weights(cfg, seed=synth.WEIGHT_SEED, device=dev)
     kv = synth.synthetic_kv_cache(cfg, wl.prompt_len, wl.max_seq, device=dev)
     dec = amk.Decoder(w, wl.max_seq, kv_cache=kv,
-                      sched=amk.make_schedule_config(num_ctas=args.num_ctas))
+                      sched=amk.make_schedule_config(num_ctas=args.num_ctas,
+                                                     l2_prefetch_tiles=args.l2_prefetch_tiles,
+                                     ring_slots=args.ring_slots))
     del w
     torch.cuda.empty_cache()
     dec.set_kv_length(wl.prompt_len)

@@ -62,10 +62,11 @@ def test_lowering_structure_8b(amk):
     T_QKV, T_O, T_GU, T_DOWN, T_LM = 0, 2, 3, 4, 5
     # row block sizes (bf16, Kt = 2048 -> 4 rows of 2048 per 16 KB tile)
     rows = {T_QKV: 6144, T_O: 4096, T_GU: 28672, T_DOWN: 4096, T_LM: 128256}
+    rt = 4
     for typ, nrows in rows.items():
         layers = range(m.n_layers) if typ != T_LM else [m.n_layers - 1]
         for l in layers:
-            cov = [0] * (nrows // 4)
+            cov = [0] * (nrows // rt)
             for t in s.tasks:
                 if t.type == typ and t.layer == l:
                     for rb in range(t.a[0], t.a[1]):
