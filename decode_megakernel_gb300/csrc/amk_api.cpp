@@ -67,9 +67,40 @@ struct Layout {
   size_t w[M_NUM] = {};
   size_t scales[M_NUM] = {};
   size_t mats = 0, embed = 0, attn_norm = 0, ffn_norm = 0, final_norm = 0, rope = 0;
-  size_t x = 0, q = 0, o = 0, a = 0, part = 0, logits = 0, counters = 0, status = 0;
+  size_t xres = 0, xmid = 0, qkv = 0, o = 0, a = 0, part = 0, status = 0, logits = 0;
   size_t tasks = 0, queue_off = 0, queue_body = 0, total = 0;
 };
+
+}  // namespace
+
+namespace amk {
+
+// Per-step scratch regions (256-byte aligned) from one base: tagged x_res,
+// x_mid, qkv, o, a, attention partials, then 64 bytes of status words.
+StepScratchPlan step_scratch_plan(const ModelGeom& g) {
+  const amk_config& c = g.cfg;
+  StepScratchPlan plan;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  const size_t qd = (size_t)c.n_heads * c.head_dim;
+  plan.xres = take((size_t)c.hidden * 4);
+  plan.xmid = take((size_t)c.hidden * 4);
+  plan.qkv = take((size_t)c.n_kv_heads * (g.group + 2) * c.head_dim * 4);
+  plan.o = take(qd * 4);
+  plan.a = take((size_t)c.ffn * 4);
+  plan.part = take((size_t)c.n_kv_heads * g.splits * g.part_stride * 4);
+  plan.status = take(64);
+  plan.total = off;
+  return plan;
+}
+
+}  // namespace amk
+
+namespace {
 
 Layout make_layout(const ModelGeom& g, const Schedule& s) {
   const amk_config& c = g.cfg;
@@ -94,15 +125,18 @@ Layout make_layout(const ModelGeom& g, const Schedule& s) {
   L.ffn_norm = take((size_t)c.n_layers * c.hidden * 2);
   L.final_norm = take((size_t)c.hidden * 2);
   L.rope = take((size_t)c.max_seq * (c.head_dim / 2) * sizeof(float) * 2);
-  const size_t qd = (size_t)c.n_heads * c.head_dim;
-  L.x = take((size_t)c.hidden * 4);
-  L.q = take(qd * 4);
-  L.o = take(qd * 4);
-  L.a = take((size_t)c.ffn * 4);
-  L.part = take((size_t)c.n_kv_heads * g.splits * g.part_stride * 4);
+  // per-step scratch (tagged words), then the status words: the same
+  // regions in the same order as step_scratch_plan
+  StepScratchPlan sp = step_scratch_plan(g);
+  const size_t base = take(sp.total);
+  L.xres = base + sp.xres;
+  L.xmid = base + sp.xmid;
+  L.qkv = base + sp.qkv;
+  L.o = base + sp.o;
+  L.a = base + sp.a;
+  L.part = base + sp.part;
+  L.status = base + sp.status;
   L.logits = take((size_t)c.vocab * 4);
-  L.counters = take(s.counters.size() * 4);
-  L.status = take(64);
   size_t n_queued = 0;
   for (const auto& q : s.queues) n_queued += q.size();
   L.tasks = take(n_queued * sizeof(DevTask));
@@ -138,6 +172,11 @@ amk_status resolve_ctas(const amk_schedule_config* sched, BuildOptions* opt, std
 }
 
 int lm_format(const amk_config& c) { return c.tied_embeddings ? AMK_FORMAT_BF16 : c.lm_head_format; }
+
+// tag_base of a launch: version v of the step carries tag 1 + (tag_base + v - 1) mod kTagPeriod
+uint32_t tag_base_of(uint32_t epoch, int n_layers) {
+  return (uint32_t)(((uint64_t)epoch * (uint64_t)n_layers) % (uint64_t)kTagPeriod);
+}
 
 amk_status plan(const amk_config* cfg, const amk_schedule_config* sched, ModelGeom* g,
                 Schedule* s, std::string* why) {
@@ -175,7 +214,7 @@ amk_status launch_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits, 
   p.logits = logits;
   p.token = token;
   p.pos = pos;
-  p.epoch = ++ctx->epoch;
+  p.tag_base = tag_base_of(++ctx->epoch, ctx->cfg.n_layers);
   p.skip_lm = skip_lm;
   p.timeout_ns = ctx->timeout_ns;
   p.trace = nullptr;
@@ -233,23 +272,7 @@ amk_status internal_begin_step(amk_ctx* ctx, int32_t token, int32_t pos, const f
   if (cudaGetDevice(&cur) != cudaSuccess || cur != ctx->device)
     return fail(ctx, AMK_ERR_INVALID_ARG, "the context's device is not the current device");
   *dm = ctx->dm;
-  // the same regions, in the same order, as in the context's workspace
-  const amk_config& c = ctx->cfg;
-  const size_t qd = (size_t)c.n_heads * c.head_dim;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    size_t at = off;
-    off = align256(off + bytes);
-    return at;
-  };
-  plan->x = take((size_t)c.hidden * 4);
-  plan->q = take(qd * 4);
-  plan->o = take(qd * 4);
-  plan->a = take((size_t)c.ffn * 4);
-  plan->part = take((size_t)c.n_kv_heads * ctx->geom.splits * ctx->geom.part_stride * 4);
-  plan->counters = take((size_t)((uint8_t*)ctx->dm.status - (uint8_t*)ctx->dm.counters));
-  plan->status = take(64);
-  plan->total = off;
+  *plan = step_scratch_plan(ctx->geom);
   plan->stream = ctx->stream;
   plan->device = ctx->device;
   return AMK_OK;
@@ -262,7 +285,7 @@ amk_status internal_launch(amk_ctx* ctx, const DevModel& dm, int32_t token, int3
   p.logits = logits;
   p.token = token;
   p.pos = pos;
-  p.epoch = epoch;
+  p.tag_base = tag_base_of(epoch, ctx->cfg.n_layers);
   p.skip_lm = 0;
   p.timeout_ns = ctx->timeout_ns;
   p.trace = nullptr;
@@ -505,12 +528,12 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   dm.ffn_norm = (const uint16_t*)(ws + L.ffn_norm);
   dm.rope = (const float2*)(ws + L.rope);
   dm.kv = (uint16_t*)kv_cache_dev;
-  dm.x = (float*)(ws + L.x);
-  dm.q = (float*)(ws + L.q);
-  dm.o = (float*)(ws + L.o);
-  dm.a = (float*)(ws + L.a);
-  dm.part = (float*)(ws + L.part);
-  dm.counters = (uint32_t*)(ws + L.counters);
+  dm.xres = (uint32_t*)(ws + L.xres);
+  dm.xmid = (uint32_t*)(ws + L.xmid);
+  dm.qkv = (uint32_t*)(ws + L.qkv);
+  dm.o = (uint32_t*)(ws + L.o);
+  dm.a = (uint32_t*)(ws + L.a);
+  dm.part = (uint32_t*)(ws + L.part);
   dm.status = (uint32_t*)(ws + L.status);
   dm.tasks = (const DevTask*)(ws + L.tasks);
   dm.queue_off = (const int32_t*)(ws + L.queue_off);
@@ -528,14 +551,10 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
       DevTask d{};
       d.type = (int16_t)t.type;
       d.layer = (int16_t)t.layer;
-      d.wait_counter = t.waits.empty() ? -1 : t.waits[0].counter;
-      d.wait_count = t.waits.empty() ? 0u : (uint32_t)t.waits[0].threshold;
-      d.signal = t.signal;
       d.a0 = (int32_t)t.a[0];
       d.a1 = (int32_t)t.a[1];
       d.a2 = (int32_t)t.a[2];
       d.a3 = (int32_t)t.a[3];
-      if (t.waits.size() > 1) return bail(fail(ctx, AMK_ERR_SCHEDULE_INVALID, "kernel supports one wait per task"));
       tasks.push_back(d);
     }
   }
@@ -559,9 +578,8 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.queue_off, qoff.data(), qoff.size() * 4, cudaMemcpyHostToDevice, st_));
   AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.queue_body, qbody.data(), qbody.size() * 4, cudaMemcpyHostToDevice, st_));
   AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice, st_));
-  AMK_CUDA(ctx, cudaMemsetAsync(ws + L.counters, 0, s.counters.size() * 4, st_));
-  AMK_CUDA(ctx, cudaMemsetAsync(ws + L.status, 0, 64, st_));
-  AMK_CUDA(ctx, cudaMemsetAsync(ws + L.x, 0, L.counters - L.x, st_));
+  // tagged scratch and status start zeroed: tag 0 is never a version's tag
+  AMK_CUDA(ctx, cudaMemsetAsync(ws + L.xres, 0, L.status + 64 - L.xres, st_));
 
   // weights: embedding (row major copy), norms, tiled matrices
   const size_t H2 = (size_t)c.hidden * 2;
@@ -678,7 +696,7 @@ amk_status amk_debug_trace_step(amk_ctx* ctx, int32_t token, int32_t pos, float*
   p.logits = logits_dev;
   p.token = token;
   p.pos = pos;
-  p.epoch = ++ctx->epoch;
+  p.tag_base = tag_base_of(++ctx->epoch, ctx->cfg.n_layers);
   p.skip_lm = 0;
   p.timeout_ns = ctx->timeout_ns;
   p.trace = trace_dev;

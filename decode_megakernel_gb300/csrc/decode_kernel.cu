@@ -1,22 +1,25 @@
 // Persistent batch-1 decode kernel for sm_103a.
 //
-// One cooperative CTA per SM walks its static task queue (wait -> dispatch
-// -> signal on monotonic counters, the execution model of the
-// AutoMegaKernel "Layer 0" VM).  Unlike the pages' design, a CTA is split
-// into a producer warp and eight consumer warps:
-//   * the producer streams every weight tile (and the KV-cache history) of
-//     the CTA's whole queue through a shared-memory ring of kStageBytes
-//     stages (128 KB in flight by default) with 1-D TMA bulk copies
-//     completing on mbarriers.  Weights never depend on
-//     activations, so the producer runs ahead across the counter waits;
-//     this hides the per-tile cross-SM synchronisation cost the pages name
-//     as the bottleneck on high-bandwidth GPUs (AMK "Experimental results":
-//     training-class GPUs).
-//   * the consumers wait on counters, keep the activation vector in
-//     registers, reduce with warp shuffles, apply the fused epilogues
-//     (RoPE + KV append, residual adds, SwiGLU, logits) and signal.
-// Every wait is bounded by %globaltimer: on expiry the kernel records a
-// status word, lets its own copies land and returns.
+// One cooperative CTA per SM walks its static task queue, the execution
+// model of the AutoMegaKernel "Layer 0" VM (wait -> dispatch -> signal over
+// a local queue).  Two departures from the pages' design:
+//   * a CTA is split into a producer warp and eight consumer warps.  The
+//     producer streams every weight tile (and the KV-cache history) of the
+//     CTA's whole queue through a shared-memory ring of kStageBytes stages
+//     (128 KB in flight by default) with 1-D TMA bulk copies completing on
+//     mbarriers.  Weights never depend on activations, so the producer runs
+//     ahead across the consumers' waits; this hides the per-tile cross-SM
+//     synchronisation cost the pages name as the bottleneck on
+//     high-bandwidth GPUs (AMK "Experimental results": training-class GPUs).
+//   * the monotonic counters are fused into the data: every value handed
+//     between CTAs is a tagged word (fp32 rounded to 24 bits | 8-bit version
+//     tag).  A task polls its inputs until they carry the version it needs
+//     and its tagged stores are its signal, so a hand-off costs one L2 round
+//     trip instead of a release fence, a counter poll and a data load.
+// The consumers keep the activation vector in registers, reduce with warp
+// shuffles and apply the fused epilogues (RoPE + KV append, residual adds,
+// SwiGLU, logits).  Every wait is bounded by %globaltimer: on expiry the
+// kernel records a status word, lets its own copies land and returns.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -87,27 +90,57 @@ __device__ __forceinline__ uint64_t global_timer() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// Tagged words.  A value handed from one CTA to another inside a step is an
+// fp32 rounded to nearest-even at bit 4 (28 of its 32 bits kept, i.e. 19
+// explicit significand bits) whose low nibble carries the version tag.  A 32-bit store and load are single-copy
+// atomic, so a reader that sees the awaited tag also sees that version's
+// value: no fence, flag or counter round trip stands between producer and
+// consumer.
+constexpr uint32_t kTagMask = 0xFu;
+
+__device__ __forceinline__ uint32_t tag_of(const StepParams& p, int version) {
+  return 1u + (p.tag_base + (uint32_t)(version + kTagPeriod - 1)) % (uint32_t)kTagPeriod;
+}
+
+__device__ __forceinline__ uint32_t tag_word(float v, uint32_t tag) {
+  uint32_t b = __float_as_uint(v);
+  b += 0x7u + ((b >> 4) & 1u);
+  return (b & ~kTagMask) | tag;
+}
+
+__device__ __forceinline__ float tag_value(uint32_t w) { return __uint_as_float(w & ~kTagMask); }
+
+// the value a tagged word would carry (same rounding), as a float
+__device__ __forceinline__ float tag_round(float v) { return tag_value(tag_word(v, 0u)); }
+
+__device__ __forceinline__ bool tags_are(const uint4& v, uint32_t tag) {
+  return ((v.x & kTagMask) == tag) & ((v.y & kTagMask) == tag) & ((v.z & kTagMask) == tag) &
+         ((v.w & kTagMask) == tag);
+}
+
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint32_t* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
   return v;
 }
 
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
   uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+__device__ __forceinline__ void st_relaxed_v4(uint32_t* p, uint4 v) {
+  asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
                : "memory");
-  return old;
 }
 
 // named barrier 1: the 256 consumer threads only (the producer warp never joins)
@@ -138,7 +171,6 @@ struct Smem {
   uint64_t empty[kStages];
   float misc[32];
   int32_t abort_flag;
-  int32_t flag;
 };
 static_assert(sizeof(Smem) <= kSmemBytes, "shared memory layout");
 
@@ -153,18 +185,57 @@ __device__ void set_status(uint32_t* status, uint32_t code, uint32_t task, uint3
   }
 }
 
-// Bounded wait on a counter: true once counter >= target (wrap-safe).
-__device__ bool wait_counter(const uint32_t* ctr, uint32_t target, uint32_t* status,
-                             volatile int32_t* abort_flag, uint64_t timeout_ns, uint32_t task) {
-  const uint64_t t0 = global_timer();
-  for (uint32_t spin = 1;; ++spin) {
-    if ((int32_t)(ld_acquire(ctr) - target) >= 0) return true;
-    if ((spin & 31u) == 0u) {
-      if (*abort_flag || ld_relaxed(status) != 0u) return false;
-      if (global_timer() - t0 > timeout_ns) {
-        set_status(status, ST_TIMEOUT, task, SITE_COUNTER);
-        return false;
-      }
+// Bounded poll of N 16-byte vectors of tagged words (bit i of `active`
+// selects vector i; the others are left alone) until every tag equals
+// `tag`.  Only the vectors still stale are reloaded.  Returns false when
+// the CTA is aborting, or after timeout_ns, having recorded ST_TIMEOUT and
+// raised the abort flag.
+template <int N, typename Addr>
+__device__ __forceinline__ bool poll_tagged(Addr at, uint4 (&v)[N], uint32_t active, uint32_t tag,
+                                            uint32_t* status, volatile int32_t* abort_flag,
+                                            uint64_t timeout_ns, uint32_t task) {
+  static_assert(N <= 32, "one pending bit per vector");
+  uint32_t pending = active;
+  uint64_t t0 = 0;
+  for (;;) {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (pending & (1u << i)) v[i] = ld_relaxed_v4(at(i));
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((pending & (1u << i)) && tags_are(v[i], tag)) pending &= ~(1u << i);
+    if (!pending) return true;
+    if (*abort_flag) return false;
+    const uint64_t now = global_timer();
+    if (!t0) {
+      t0 = now;
+    } else if (now - t0 > timeout_ns) {
+      set_status(status, ST_TIMEOUT, task, SITE_DATA);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Bounded poll of one tagged word; its value goes to *out.
+__device__ __forceinline__ bool poll_word(const uint32_t* ptr, uint32_t tag, float* out,
+                                          uint32_t* status, volatile int32_t* abort_flag,
+                                          uint64_t timeout_ns, uint32_t task) {
+  uint64_t t0 = 0;
+  for (;;) {
+    const uint32_t w = ld_relaxed(ptr);
+    if ((w & kTagMask) == tag) {
+      *out = tag_value(w);
+      return true;
+    }
+    if (*abort_flag) return false;
+    const uint64_t now = global_timer();
+    if (!t0) {
+      t0 = now;
+    } else if (now - t0 > timeout_ns) {
+      set_status(status, ST_TIMEOUT, task, SITE_DATA);
+      *abort_flag = 1;
+      return false;
     }
   }
 }
@@ -266,6 +337,8 @@ __device__ __forceinline__ TaskTiles task_tiles(const StepParams& p, const DevTa
     tt.v = reinterpret_cast<const uint8_t*>(kv_row(m, t.layer, 1, t.a0, 0));
     tt.nst = (tt.t1 - tt.t0 + tt.pps - 1) / tt.pps;
     tt.attn = true;
+  } else if (t.type == T_COMBINE) {
+    tt.nst = 0;
   } else {
     const int kind = mat_kind(t.type);
     const DevMat M = m.mat[kind];
@@ -278,9 +351,9 @@ __device__ __forceinline__ TaskTiles task_tiles(const StepParams& p, const DevTa
 }
 
 // Producer: one thread streams every tile of the CTA's queue into the ring.
-// Whenever no slot is free it prefetches later tiles into L2 (up to
-// m.prefetch_tiles ahead of the last copy), so HBM keeps streaming while the
-// consumers wait on a counter; the ring copies then hit L2.
+// Whenever no slot is free it may prefetch later tiles into L2 (up to
+// m.prefetch_tiles ahead of the last copy, off by default), so HBM keeps
+// streaming while the consumers wait for their inputs.
 __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
   const uint64_t pol_w = policy_evict_first();
@@ -548,33 +621,94 @@ __device__ __forceinline__ void load8_bf16(const uint16_t* src, float2* d) {
 }
 
 // Activation chunk owned by a consumer thread: h[kt] holds act[kt*Kt + chunk*8 + 0..7]
-// as four pairs.  QKV, gate/up and LM head take rmsnorm(x) * w_norm; O takes
-// o; down takes a.
+// as four pairs.  QKV takes rmsnorm(x_res) * w_norm (layer 0: of the
+// embedding row), gate/up rmsnorm(x_mid) * w_norm, the LM head
+// rmsnorm(x_res) * w_final; O takes o, down takes a.  Tagged inputs are
+// polled until they carry the version the task reads: the raw words land
+// in h itself (one register set for the poll and the GEMV), stale chunks
+// are reloaded until their tags match, then the tag bytes are cleared.
+// Returns false when the CTA is aborting (h is then unspecified).
 template <int NKT>
-__device__ __forceinline__ void load_activation(const StepParams& p, Smem& sm, const DevTask& t,
-                                                const DevMat& M, int chunk, float2 (&h)[NKT][4]) {
+__device__ __forceinline__ bool load_activation(const StepParams& p, Smem& sm, const DevTask& t,
+                                                const DevMat& M, int chunk, float2 (&h)[NKT][4],
+                                                uint32_t task_idx, int64_t* tr) {
   const DevModel& m = p.m;
   const int tid = threadIdx.x;
   const bool norm = t.type == T_QKV || t.type == T_GATEUP || t.type == T_LMHEAD;
   const bool from_embed = t.type == T_QKV && t.layer == 0;
-  const float* src = t.type == T_OPROJ ? m.o : t.type == T_DOWN ? m.a : m.x;
   const uint16_t* emb = m.embed + (int64_t)p.token * m.hidden;
-  float ss = 0.f;
+  const uint32_t* src = t.type == T_OPROJ ? m.o : t.type == T_DOWN ? m.a
+                        : t.type == T_GATEUP ? m.xmid : m.xres;
+  const int version = t.type == T_QKV ? t.layer : t.type == T_LMHEAD ? m.n_layers : t.layer + 1;
+  const uint32_t tag = tag_of(p, version);
+  auto load_raw = [&](const uint32_t* b, int kt) {
+    const uint4 w0 = ld_relaxed_v4(b), w1 = ld_relaxed_v4(b + 4);
+    h[kt][0] = make_float2(__uint_as_float(w0.x), __uint_as_float(w0.y));
+    h[kt][1] = make_float2(__uint_as_float(w0.z), __uint_as_float(w0.w));
+    h[kt][2] = make_float2(__uint_as_float(w1.x), __uint_as_float(w1.y));
+    h[kt][3] = make_float2(__uint_as_float(w1.z), __uint_as_float(w1.w));
+  };
+  auto stale = [&](int kt) {
+    uint32_t bad = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      bad |= ((__float_as_uint(h[kt][i].x) & kTagMask) ^ tag) | ((__float_as_uint(h[kt][i].y) & kTagMask) ^ tag);
+    return bad != 0;
+  };
+  uint32_t pending = 0;
 #pragma unroll
   for (int kt = 0; kt < NKT; ++kt) {
     const int k = kt * M.Kt + chunk * 8;
     if (k < M.K) {  // K is a multiple of 8
       if (from_embed) load8_bf16(emb + k, h[kt]);
-      else load8_f32(src + k, h[kt]);
+      else load_raw(src + k, kt);
     } else {
 #pragma unroll
       for (int i = 0; i < 4; ++i) h[kt][i] = make_float2(0.f, 0.f);
     }
+  }
+  bool ok = true;
+  if (!from_embed) {
+#pragma unroll
+    for (int kt = 0; kt < NKT; ++kt)
+      if (kt * M.Kt + chunk * 8 < M.K && stale(kt)) pending |= 1u << kt;
+    uint64_t t0 = 0;
+    while (pending) {
+      if (sm.abort_flag) { ok = false; break; }
+      const uint64_t now = global_timer();
+      if (!t0) {
+        t0 = now;
+      } else if (now - t0 > p.timeout_ns) {
+        set_status(m.status, ST_TIMEOUT, task_idx, SITE_DATA);
+        sm.abort_flag = 1;
+        ok = false;
+        break;
+      }
+      // an opaque copy of the base keeps the compiler from holding NKT
+      // precomputed addresses in registers across the retries
+      const uint32_t* b = src + chunk * 8;
+      asm volatile("" : "+l"(b));
+#pragma unroll
+      for (int kt = 0; kt < NKT; ++kt)
+        if (pending & (1u << kt)) {
+          load_raw(b + kt * M.Kt, kt);
+          if (!stale(kt)) pending &= ~(1u << kt);
+        }
+    }
+#pragma unroll
+    for (int kt = 0; kt < NKT; ++kt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        h[kt][i] = make_float2(tag_value(__float_as_uint(h[kt][i].x)), tag_value(__float_as_uint(h[kt][i].y)));
+  }
+  if (tr) tr[TR_C_WAITED] = (int64_t)global_timer();
+  if (!norm) return ok;
+  // threads tid < Kt/8 hold every chunk once: their squares sum to sum(x^2)
+  float ss = 0.f;
+#pragma unroll
+  for (int kt = 0; kt < NKT; ++kt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) ss = fmaf(h[kt][i].x, h[kt][i].x, fmaf(h[kt][i].y, h[kt][i].y, ss));
-  }
-  if (!norm) return;
-  // threads tid < Kt/8 hold every chunk once: their squares sum to sum(x^2)
   const int cpr = 1 << M.cpr_shift;
   ss = warp_sum(tid < cpr ? ss : 0.f);
   if ((tid & 31) == 0) sm.misc[tid >> 5] = ss;
@@ -596,6 +730,7 @@ __device__ __forceinline__ void load_activation(const StepParams& p, Smem& sm, c
         h[kt][i] = make_float2(h[kt][i].x * r * w8[i].x, h[kt][i].y * r * w8[i].y);
     }
   }
+  return ok;
 }
 
 // One chunk of one row against the thread's activations, accumulated as a
@@ -662,7 +797,23 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   volatile int32_t* abort_flag = &sm.abort_flag;
 
   float2 h[NKT][4];
-  load_activation<NKT>(p, sm, t, M, chunk, h);
+  bool failed = !load_activation<NKT>(p, sm, t, M, chunk, h, task_idx, tr);
+  // residual row of O / down (one row per thread): loaded now so that the
+  // load overlaps the GEMV; its tag is checked (and the word re-polled if
+  // stale) in the epilogue
+  const int nrows = (t.a1 - t.a0) * M.Rt;
+  const int row0 = t.a0 * M.Rt;
+  const bool has_resid = (t.type == T_OPROJ || t.type == T_DOWN) && tid < nrows && row0 + tid < M.rows;
+  const uint32_t* resid_src = t.type == T_OPROJ ? m.xres + row0 + tid : m.xmid + row0 + tid;
+  const uint32_t resid_tag = tag_of(p, t.type == T_OPROJ ? t.layer : t.layer + 1);
+  uint32_t resid_w = 0;
+  if (has_resid) {
+    if (t.type == T_OPROJ && t.layer == 0)   // layer 0: the embedding row, a constant
+      resid_w = tag_word(__uint_as_float((uint32_t)__ldg(m.embed + (int64_t)p.token * m.hidden + row0 + tid) << 16),
+                         resid_tag);
+    else
+      resid_w = ld_relaxed(resid_src);
+  }
   float hs[NKT];  // int4: per-chunk activation sums, then activations pre-scaled by 2^-s
   if constexpr (FMT == AMK_FORMAT_INT4) {
 #pragma unroll
@@ -677,13 +828,6 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
     }
   }
 
-  // layer-0 QKV tasks also initialise their slice of the residual stream
-  if (t.type == T_QKV && t.layer == 0) {
-    const uint16_t* emb = m.embed + (int64_t)p.token * m.hidden;
-    for (int e = t.a2 + tid; e < t.a3; e += kConsumerThreads)
-      m.x[e] = __uint_as_float((uint32_t)emb[e] << 16);
-  }
-
   const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
   const uint32_t full0 = smem_addr(&sm.full[0]);
   const uint32_t empty0 = smem_addr(&sm.empty[0]);
@@ -695,7 +839,6 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   const uint32_t side_z0 = kStageBytes + (uint32_t)(M.Rt * ngt * 2 + rsub * ngt + (chunk >> 4));
   const uint32_t nslots = (uint32_t)m.ring_slots;
   uint32_t slot = (uint32_t)stage % nslots, phase = ((uint32_t)stage / nslots) & 1u;
-  bool failed = false;
   int64_t starved = 0;
 
   float* red = sm.scratch;
@@ -745,9 +888,8 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   if (tr) tr[TR_C_STARVED] = starved;
   if (consumer_sync_or(failed)) return -1;
 
-  // epilogue: one row (or one row pair) per thread
-  const int nrows = nrb * M.Rt;
-  const int row0 = t.a0 * M.Rt;
+  // epilogue: one row (or one row pair) per thread; tagged stores of version layer + 1
+  const uint32_t tag = tag_of(p, t.layer + 1);
   const int nwg = 1 << wpg_shift;
   auto row_sum = [&](int r) {
     float y = 0.f;
@@ -755,6 +897,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
     return y;
   };
   if (t.type == T_QKV || t.type == T_GATEUP) {
+    const int hd = m.head_dim, half = hd >> 1, G = m.group, gw = (G + 2) * hd;
     for (int pr = tid; pr < nrows / 2; pr += kConsumerThreads) {
       const int R = row0 + 2 * pr;
       if (R >= M.rows) continue;
@@ -765,32 +908,35 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
         y1 *= fp16_bits_to_float(sc[R + 1]);
       }
       if (t.type == T_GATEUP) {
-        m.a[R >> 1] = silu(y0) * y1;
+        st_relaxed(m.a + (R >> 1), tag_word(silu(y0) * y1, tag));
         continue;
       }
-      const int hd = m.head_dim, half = hd >> 1;
-      const int qd = m.n_heads * hd, kvd = m.n_kv_heads * hd;
-      if (R < qd + kvd) {
+      // packed QKV rows per KV head: G query heads, k, v (RoPE pairs adjacent)
+      const int grp = R / gw, r = R % gw, slot_h = r / hd, within = r % hd;
+      uint32_t* dst = m.qkv + (int64_t)grp * gw + slot_h * hd;
+      if (slot_h <= G) {
         // rotate-half RoPE pair (i, i + hd/2) at position pos
-        const bool is_q = R < qd;
-        const int rr = is_q ? R : R - qd;
-        const int head = rr / hd, i = (rr % hd) >> 1;
+        const int i = within >> 1;
         const float2 cs2 = m.rope[(int64_t)p.pos * half + i];
-        const float a = y0 * cs2.x - y1 * cs2.y;
-        const float b = y1 * cs2.x + y0 * cs2.y;
-        if (is_q) {
-          m.q[head * hd + i] = a;
-          m.q[head * hd + half + i] = b;
-        } else {
-          uint16_t* kr = const_cast<uint16_t*>(kv_row(m, t.layer, 0, head, p.pos));
-          kr[i] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-          kr[half + i] = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+        float a = y0 * cs2.x - y1 * cs2.y;
+        float b = y1 * cs2.x + y0 * cs2.y;
+        if (slot_h == G) {  // k: the cache holds bf16, attention uses the same values
+          const __nv_bfloat16 ka = __float2bfloat16_rn(a), kb = __float2bfloat16_rn(b);
+          uint16_t* kr = const_cast<uint16_t*>(kv_row(m, t.layer, 0, grp, p.pos));
+          kr[i] = __bfloat16_as_ushort(ka);
+          kr[half + i] = __bfloat16_as_ushort(kb);
+          a = __bfloat162float(ka);
+          b = __bfloat162float(kb);
         }
+        st_relaxed(dst + i, tag_word(a, tag));
+        st_relaxed(dst + half + i, tag_word(b, tag));
       } else {
-        const int vr = R - qd - kvd;
-        uint16_t* vrow = const_cast<uint16_t*>(kv_row(m, t.layer, 1, vr / hd, p.pos));
-        vrow[vr % hd] = __bfloat16_as_ushort(__float2bfloat16_rn(y0));
-        vrow[vr % hd + 1] = __bfloat16_as_ushort(__float2bfloat16_rn(y1));
+        const __nv_bfloat16 v0 = __float2bfloat16_rn(y0), v1 = __float2bfloat16_rn(y1);
+        uint16_t* vrow = const_cast<uint16_t*>(kv_row(m, t.layer, 1, grp, p.pos));
+        vrow[within] = __bfloat16_as_ushort(v0);
+        vrow[within + 1] = __bfloat16_as_ushort(v1);
+        st_relaxed(dst + within, tag_word(__bfloat162float(v0), tag));
+        st_relaxed(dst + within + 1, tag_word(__bfloat162float(v1), tag));
       }
     }
   } else {
@@ -804,8 +950,12 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
       }
       if (t.type == T_LMHEAD) {
         p.logits[R] = y;
-      } else {  // O projection / down projection: residual add on owned rows
-        m.x[R] = __ldcg(m.x + R) + y;
+      } else {  // O / down: residual add on the owned row (r == tid)
+        float resid = tag_value(resid_w);
+        if ((resid_w & kTagMask) != resid_tag &&
+            !poll_word(resid_src, resid_tag, &resid, m.status, abort_flag, p.timeout_ns, task_idx))
+          continue;   // aborting: the step's status word already says why
+        st_relaxed((t.type == T_OPROJ ? m.xmid : m.xres) + R, tag_word(resid + y, tag));
       }
     }
   }
@@ -847,14 +997,39 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   const int g = t.a0, j = t.a1;
   volatile int32_t* abort_flag = &sm.abort_flag;
 
-  // queries of the group, pre-scaled so that scores are in log2 units
+  const uint32_t tag = tag_of(p, t.layer + 1);
+  const uint32_t* gq = m.qkv + (int64_t)g * (G + 2) * HD;   // q heads, k, v of this KV head
+  // queries of the group and, for the last split, the step's k and v:
+  // polled by 16-byte vectors into shared memory (k, v into the scratch
+  // tail, which the warp merge below never reaches)
+  constexpr int QV = G * HD / 4, KVV = HD / 2;
+  static_assert(QV + KVV <= kConsumerThreads, "one vector per thread");
+  static_assert(kConsumerWarps * G * (HD + 2) <= kScratchFloats - 2 * 128, "warp merge reaches the k, v tail");
+  const bool last = j == m.splits - 1;
+  bool failed = false;
+  float* qs = sm.scratch;
+  float* kvs = sm.scratch + kScratchFloats - 2 * HD;   // [k | v] of the current position
+  if (tid < QV || (last && tid < QV + KVV)) {
+    const uint32_t* src = tid < QV ? gq + tid * 4 : gq + G * HD + (tid - QV) * 4;
+    float* dst = tid < QV ? qs + tid * 4 : kvs + (tid - QV) * 4;
+    uint4 v[1];
+    failed = !poll_tagged<1>([&](int) { return src; }, v, 1u, tag, m.status, abort_flag,
+                             p.timeout_ns, task_idx);
+    dst[0] = tag_value(v[0].x);
+    dst[1] = tag_value(v[0].y);
+    dst[2] = tag_value(v[0].z);
+    dst[3] = tag_value(v[0].w);
+  }
+  if (tr) tr[TR_C_WAITED] = (int64_t)global_timer();
+  failed = consumer_sync_or(failed);
+  // queries pre-scaled so that scores are in log2 units
   const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
   float qr[G][DPL];
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int d = 0; d < DPL; ++d)
-      qr[h][d] = __ldcg(m.q + (int64_t)(g * G + h) * HD + lane * DPL + d) * qscale;
+    for (int d = 0; d < DPL; ++d) qr[h][d] = qs[h * HD + lane * DPL + d] * qscale;
+  consumer_sync();   // qs is reused by the warp merge below
   float mx[G], l[G], acc[G][DPL];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -927,7 +1102,6 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   const uint32_t empty0 = smem_addr(&sm.empty[0]);
   const uint32_t nslots = (uint32_t)m.ring_slots;
   uint32_t slot = (uint32_t)stage % nslots, phase = ((uint32_t)stage / nslots) & 1u;
-  bool failed = false;
   int64_t starved = 0;
   int t0, t1;
   attn_range(p.pos, m.splits, j, &t0, &t1);
@@ -970,18 +1144,12 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     if (++slot == nslots) { slot = 0; phase ^= 1u; }
   }
   // the current position, written this step by the QKV tasks
-  if (!failed && j == m.splits - 1 && warp == 0) {
+  if (!failed && last && warp == 0) {
     float kf[R][DPL], vf[R][DPL];
-    const uint16_t* kr = kv_row(m, t.layer, 0, g, p.pos) + lane * DPL;
-    const uint16_t* vr = kv_row(m, t.layer, 1, g, p.pos) + lane * DPL;
-    if constexpr (DPL == 4) {
-      const uint2 kw = __ldcg(reinterpret_cast<const uint2*>(kr));
-      const uint2 vw = __ldcg(reinterpret_cast<const uint2*>(vr));
-      unpack(kw.x, kw.y, kf[0]);
-      unpack(vw.x, vw.y, vf[0]);
-    } else {
-      unpack(__ldcg(reinterpret_cast<const unsigned int*>(kr)), 0u, kf[0]);
-      unpack(__ldcg(reinterpret_cast<const unsigned int*>(vr)), 0u, vf[0]);
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+      kf[0][d] = kvs[lane * DPL + d];
+      vf[0][d] = kvs[HD + lane * DPL + d];
     }
 #pragma unroll
     for (int r = 1; r < R; ++r)
@@ -1008,7 +1176,12 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     }
   }
   if (consumer_sync_or(failed)) return -1;
-  float* part = m.part + (int64_t)(g * m.splits + j) * m.part_stride;
+  // partial of this split: acc [G][HD], then (m, l) per head, then padding,
+  // as tagged words.  m is rounded to the tagged grid before it scales acc
+  // and l, so the stored (m, acc, l) stay consistent; an empty split stores
+  // m = -1e30 (weight 0 in the merge) instead of -inf, which has no room for
+  // a tag.
+  uint32_t* part = m.part + (int64_t)(g * m.splits + j) * m.part_stride;
   for (int idx = tid; idx < G * HD; idx += kConsumerThreads) {
     const int h = idx / HD, d = idx % HD;
     float M = -INFINITY;
@@ -1016,6 +1189,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg[w * WS + h * (HD + 2) + HD]);
     float L = 0.f, A = 0.f;
     if (M != -INFINITY) {
+      M = tag_round(M);
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
         const float mw = mg[w * WS + h * (HD + 2) + HD];
@@ -1023,98 +1197,116 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
         L = fmaf(mg[w * WS + h * (HD + 2) + HD + 1], sc, L);
         A = fmaf(mg[w * WS + h * (HD + 2) + d], sc, A);
       }
+    } else {
+      M = -1e30f;
     }
-    part[h * (HD + 2) + d] = A;
+    st_relaxed(part + idx, tag_word(A, tag));
     if (d == 0) {
-      part[h * (HD + 2) + HD] = M;
-      part[h * (HD + 2) + HD + 1] = L;
+      st_relaxed(part + G * HD + 2 * h, tag_word(M, tag));
+      st_relaxed(part + G * HD + 2 * h + 1, tag_word(L, tag));
     }
   }
-  consumer_sync();
+  for (int idx = G * HD + 2 * G + tid; idx < m.part_stride; idx += kConsumerThreads)
+    st_relaxed(part + idx, tag_word(0.f, tag));
   if (tr) tr[TR_A_MERGED] = (int64_t)global_timer();
-
-  // ticket: the last split of this KV head to arrive merges all splits
-  if (tid == 0) {
-    const uint32_t old = atom_add_acq_rel(m.counters + t.signal, 1u);
-    sm.flag = (old + 1u == p.epoch * (uint32_t)m.splits) ? 1 : 0;
-  }
-  consumer_sync();
-  if (tr) tr[TR_A_TICKET] = (int64_t)global_timer();
-  if (sm.flag) {
-    // LSE merge of the S splits of this KV head, in chunks of up to SC splits.
-    // Per chunk every load is issued at once (the (m, l) pairs by one thread
-    // each, every output element's SC partial sums by its thread), so a
-    // chunk costs one L2 round trip; a running (M, L, A) per element folds
-    // the chunks together.  Shared memory: 2 * SC * G floats.
-    constexpr int SC = 24;
-    constexpr int EPT = (G * HD + kConsumerThreads - 1) / kConsumerThreads;  // elements per thread
-    static_assert(SC * G <= kConsumerThreads, "one (m, l) pair per thread");
-    const int S = m.splits;
-    const float* pg = m.part + (int64_t)g * S * m.part_stride;
-    float* ml = sm.scratch;  // [SC][G] maxima, then [SC][G] normalisers
-    float runM[EPT], runL[EPT], runA[EPT];
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) { runM[e] = -INFINITY; runL[e] = 0.f; runA[e] = 0.f; }
-    for (int c0 = 0; c0 < S; c0 += SC) {
-      const int sc = min(SC, S - c0);
-      float mv = 0.f, lv = 0.f;
-      if (tid < sc * G) {
-        const float* pp = pg + (int64_t)(c0 + tid / G) * m.part_stride + (tid % G) * (HD + 2) + HD;
-        mv = __ldcg(pp);
-        lv = __ldcg(pp + 1);
-      }
-      float av[EPT][SC];
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        const int idx = tid + e * kConsumerThreads;
-        const int h = idx / HD, d = idx % HD;
-#pragma unroll
-        for (int s2 = 0; s2 < SC; ++s2)
-          av[e][s2] = (idx < G * HD && s2 < sc)
-                          ? __ldcg(pg + (int64_t)(c0 + s2) * m.part_stride + h * (HD + 2) + d) : 0.f;
-      }
-      if (tid < sc * G) {
-        ml[tid] = mv;
-        ml[SC * G + tid] = lv;
-      }
-      consumer_sync();
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        const int idx = tid + e * kConsumerThreads;
-        if (idx >= G * HD) continue;
-        const int h = idx / HD;
-        float Mc = -INFINITY;
-        for (int s2 = 0; s2 < sc; ++s2) Mc = fmaxf(Mc, ml[s2 * G + h]);
-        if (Mc == -INFINITY) continue;
-        float Lc = 0.f, Ac = 0.f;
-#pragma unroll
-        for (int s2 = 0; s2 < SC; ++s2) {
-          if (s2 < sc) {
-            const float ms = ml[s2 * G + h];
-            const float w = ms == -INFINITY ? 0.f : exp2f(ms - Mc);
-            Lc = fmaf(ml[SC * G + s2 * G + h], w, Lc);
-            Ac = fmaf(av[e][s2], w, Ac);
-          }
-        }
-        const float Mn = fmaxf(runM[e], Mc);
-        const float wr = runM[e] == -INFINITY ? 0.f : exp2f(runM[e] - Mn);
-        const float wc = exp2f(Mc - Mn);
-        runL[e] = runL[e] * wr + Lc * wc;
-        runA[e] = runA[e] * wr + Ac * wc;
-        runM[e] = Mn;
-      }
-      consumer_sync();  // the next chunk reuses ml
-    }
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      const int idx = tid + e * kConsumerThreads;
-      if (idx < G * HD) m.o[(int64_t)(g * G + idx / HD) * HD + idx % HD] = runA[e] / runL[e];
-    }
-    consumer_sync();
-    if (tid == 0) red_release_add(m.counters + t.a2, 1u);
-    if (tr) tr[TR_A_COMBINED] = (int64_t)global_timer();
-  }
   return stage + nst;
+}
+
+// LSE merge of one query head's S attention splits into o (AMK's split-K
+// attention followed by its combine step): o = sum_s w_s acc_s / sum_s w_s l_s
+// with w_s = 2^(m_s - max_s m_s).  Per chunk of up to NH * SC splits, a
+// thread polls SC acc vectors (4 consecutive dims of the head, splits
+// hf, hf + NH, ...) while the first threads poll the chunk's (m, l) pairs
+// into shared memory; the chunk maximum then gives every weight directly,
+// a running (M, L, A) per thread folds the chunks, and the NH subsets are
+// merged through shared memory.
+// Head size and group are runtime values here (one instance serves every
+// model): HD in {64, 128}, so NE in {16, 32} quads and NH in {16, 8} subsets.
+__device__ __noinline__ int combine_task(const StepParams& p, Smem& sm, const DevTask t, int stage,
+                                         uint32_t task_idx, int64_t* tr) {
+  constexpr int SC = 4;                          // acc vectors polled at once per thread
+  static_assert((kConsumerThreads / 16) * SC <= kConsumerThreads, "one (m, l) vector per thread");
+  static_assert((kConsumerThreads / 16) * SC * 2 + kConsumerThreads * 6 <= kScratchFloats,
+                "combine exceeds the scratch");
+  const DevModel& m = p.m;
+  const int HD = m.head_dim, G = m.group;
+  const int NE = HD / 4;                         // dim quads of the head
+  const int NH = kConsumerThreads / NE;          // split subsets
+  const int CH = NH * SC;                        // splits per chunk
+  const int tid = threadIdx.x;
+  const int g = t.a0, hh = t.a1, S = m.splits, ps = m.part_stride;
+  const int e = tid % NE, hf = tid / NE;
+  const uint32_t tag = tag_of(p, t.layer + 1);
+  volatile int32_t* abort_flag = &sm.abort_flag;
+  const uint32_t* pg = m.part + (int64_t)g * S * ps;
+  float* mls = sm.scratch;                  // [CH][2] (m, l) of the head, per split of the chunk
+  float* sub = sm.scratch + CH * 2;         // [NH][NE][6] subset states
+  float M = -INFINITY, L = 0.f, A[4] = {0.f, 0.f, 0.f, 0.f};
+  bool failed = false;
+  for (int c0 = 0; c0 < S; c0 += CH) {
+    const int nc = min(CH, S - c0);
+    uint4 v[SC];
+    uint32_t act = 0;
+#pragma unroll
+    for (int i = 0; i < SC; ++i)
+      if (hf + i * NH < nc) act |= 1u << i;
+    const uint32_t* base = pg + (int64_t)(c0 + hf) * ps + hh * HD + e * 4;
+    const int64_t step = (int64_t)NH * ps;
+    if (!failed)
+      failed = !poll_tagged<SC>([&](int i) { return base + i * step; }, v, act, tag, m.status,
+                                abort_flag, p.timeout_ns, task_idx);
+    if (tid < nc && !failed) {
+      // (m, l) of heads 2k and 2k + 1 share a vector (G == 1: m, l, pad, pad)
+      const uint32_t* mlp = pg + (int64_t)(c0 + tid) * ps + G * HD + (hh >> 1) * 4;
+      uint4 mv[1];
+      failed = !poll_tagged<1>([&](int) { return mlp; }, mv, 1u, tag, m.status, abort_flag,
+                               p.timeout_ns, task_idx);
+      mls[tid * 2] = tag_value((hh & 1) ? mv[0].z : mv[0].x);
+      mls[tid * 2 + 1] = tag_value((hh & 1) ? mv[0].w : mv[0].y);
+    }
+    if (consumer_sync_or(failed)) return -1;
+    float Mc = -INFINITY;
+    for (int s = 0; s < nc; ++s) Mc = fmaxf(Mc, mls[s * 2]);
+    const float Mn = fmaxf(M, Mc);
+    const float a = exp2f(M - Mn);
+    L *= a;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) A[c] *= a;
+#pragma unroll
+    for (int i = 0; i < SC; ++i) {
+      if (!(act & (1u << i))) continue;
+      const int s = hf + i * NH;
+      const float w = exp2f(mls[s * 2] - Mn);
+      L = fmaf(mls[s * 2 + 1], w, L);
+      A[0] = fmaf(tag_value(v[i].x), w, A[0]);
+      A[1] = fmaf(tag_value(v[i].y), w, A[1]);
+      A[2] = fmaf(tag_value(v[i].z), w, A[2]);
+      A[3] = fmaf(tag_value(v[i].w), w, A[3]);
+    }
+    M = Mn;
+    consumer_sync();   // mls is refilled by the next chunk
+  }
+  if (tr) tr[TR_C_WAITED] = (int64_t)global_timer();
+  float* mine = sub + (hf * NE + e) * 6;
+  mine[0] = M; mine[1] = L; mine[2] = A[0]; mine[3] = A[1]; mine[4] = A[2]; mine[5] = A[3];
+  consumer_sync();
+  if (hf == 0) {
+    float Mt = -INFINITY;
+    for (int k = 0; k < NH; ++k) Mt = fmaxf(Mt, sub[(k * NE + e) * 6]);
+    float Lt = 0.f, At[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < NH; ++k) {
+      const float* o = sub + (k * NE + e) * 6;
+      const float w = exp2f(o[0] - Mt);   // a subset without splits has M = -inf: weight 0
+      Lt = fmaf(o[1], w, Lt);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) At[c] = fmaf(o[2 + c], w, At[c]);
+    }
+    const float inv = 1.0f / Lt;
+    st_relaxed_v4(m.o + (int64_t)(g * G + hh) * HD + e * 4,
+                  make_uint4(tag_word(At[0] * inv, tag), tag_word(At[1] * inv, tag),
+                             tag_word(At[2] * inv, tag), tag_word(At[3] * inv, tag)));
+  }
+  return stage;
 }
 
 template <int HD>
@@ -1130,6 +1322,8 @@ __device__ __forceinline__ int attn_dispatch(const StepParams& p, Smem& sm, cons
   }
 }
 
+// Runs the CTA's queue in order.  There is no wait or signal around a task:
+// each task polls its own tagged inputs and its stores are the signal.
 template <int QKV_FMT, int LM_FMT>
 __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
@@ -1138,24 +1332,17 @@ __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
   volatile int32_t* abort_flag = &sm.abort_flag;
   for (int i = 0; i < n; ++i) {
     const DevTask t = q[i];
-    bool failed = false;
     int64_t* tr = p.trace ? trace_row(p, i) : nullptr;
     if (tr && tid == 0) {
       tr[TR_C_BEGIN] = (int64_t)global_timer();
       tr[TR_TAG] = t.type | (t.layer << 8);
     }
-    if (t.wait_counter >= 0 && tid == 0)
-      failed = !wait_counter(m.counters + t.wait_counter, p.epoch * t.wait_count, m.status,
-                             abort_flag, p.timeout_ns, (uint32_t)i);
-    if (consumer_sync_or(failed)) {
-      *abort_flag = 1;
-      return;
-    }
-    if (tr && tid == 0) tr[TR_C_WAITED] = (int64_t)global_timer();
     int64_t* tr0 = tid == 0 ? tr : nullptr;
     if (t.type == T_ATTN)
       stage = m.head_dim == 128 ? attn_dispatch<128>(p, sm, t, stage, (uint32_t)i, tr0)
                                 : attn_dispatch<64>(p, sm, t, stage, (uint32_t)i, tr0);
+    else if (t.type == T_COMBINE)
+      stage = combine_task(p, sm, t, stage, (uint32_t)i, tr0);
     else if (t.type == T_LMHEAD) stage = gemv_dispatch<LM_FMT>(p, sm, t, stage, (uint32_t)i, tr0);
     else stage = gemv_dispatch<QKV_FMT>(p, sm, t, stage, (uint32_t)i, tr0);
     if (stage < 0) {
@@ -1163,10 +1350,7 @@ __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       return;
     }
     if (tr && tid == 0) tr[TR_C_DONE] = (int64_t)global_timer();
-    if (t.type != T_ATTN) {
-      consumer_sync();  // epilogue stores done; scratch free for the next task
-      if (tid == 0 && t.signal >= 0) red_release_add(m.counters + t.signal, 1u);
-    }
+    consumer_sync();  // every thread's stores issued; scratch free for the next task
     if (tr && tid == 0) tr[TR_C_SIGNALLED] = (int64_t)global_timer();
   }
 }
@@ -1182,7 +1366,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
     sm.abort_flag = 0;
-    sm.flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -1244,20 +1427,24 @@ struct PackArgs {
   int kind, fmt, n_heads, n_kv_heads, head_dim;
 };
 
-// packed row -> (source index, source row) or -1
+// packed row -> (source index, source row) or -1.  QKV rows are packed per
+// KV head g: its query heads g*G .. g*G+G-1, then k head g, then v head g
+// (G = n_heads / n_kv_heads); within a q or k head, row 2i holds dim i and
+// row 2i+1 dim i + hd/2, so that each rotate-half RoPE pair sits in one
+// thread's pair of rows.  Gate/up rows interleave (gate r, up r).
 __device__ int pack_source(const PackArgs& a, int pr, int* row) {
   const DevMat& M = a.dst;
   if (pr >= M.rows) return -1;
   if (a.kind == M_QKV) {
-    const int hd = a.head_dim, qd = a.n_heads * hd, kvd = a.n_kv_heads * hd;
-    if (pr < qd + kvd) {
-      const int rr = pr < qd ? pr : pr - qd;
-      const int i = rr % hd;
-      *row = rr / hd * hd + (i >> 1) + (i & 1) * (hd / 2);
-      return pr < qd ? 0 : 1;
+    const int hd = a.head_dim, G = a.n_heads / a.n_kv_heads, gw = (G + 2) * hd;
+    const int grp = pr / gw, r = pr % gw, slot = r / hd, i = r % hd;
+    const int paired = (i >> 1) + (i & 1) * (hd / 2);
+    if (slot < G) {
+      *row = (grp * G + slot) * hd + paired;
+      return 0;
     }
-    *row = pr - qd - kvd;
-    return 2;
+    *row = grp * hd + (slot == G ? paired : i);
+    return slot == G ? 1 : 2;
   }
   if (a.kind == M_GU) {
     *row = pr >> 1;
@@ -1341,13 +1528,15 @@ void launch_pack_matrix(int kind, int fmt, const DevMat& dst, int layer, const v
 
 // ---------------------------------------------------------- test aids
 
-// A wait on a counter nothing signals: must end with ST_TIMEOUT, not hang.
+// A poll on tagged words nothing writes: must end with ST_TIMEOUT, not hang.
 __global__ void watchdog_probe_kernel(uint32_t* scratch, uint64_t timeout_ns) {
   __shared__ int32_t abort_flag;
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    // scratch[0] counter (stays 0), scratch[16..20) status words
-    wait_counter(scratch, 1u, scratch + 16, &abort_flag, timeout_ns, blockIdx.x);
+    // scratch[0..4) stay 0 (tag 0 is never written), scratch[16..20) status words
+    uint4 v[1];
+    poll_tagged<1>([&](int) { return (const uint32_t*)scratch; }, v, 1u, 1u, scratch + 16,
+                   &abort_flag, timeout_ns, blockIdx.x);
   }
 }
 

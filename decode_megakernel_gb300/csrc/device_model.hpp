@@ -7,15 +7,15 @@
 
 namespace amk {
 
-// One task of a CTA's queue as the kernel reads it (32 bytes).
+// One task of a CTA's queue as the kernel reads it (32 bytes).  A task's
+// inputs are tagged words: it polls them until they carry the version it
+// needs, so the task table holds no wait or signal.
 struct alignas(16) DevTask {
   int16_t type;
   int16_t layer;
-  int32_t wait_counter;   // -1: no wait
-  uint32_t wait_count;    // producers of wait_counter per step
-  int32_t signal;         // -1: no signal
-  int32_t a0, a1, a2, a3; // GEMV: row blocks [a0, a1), layer-0 QKV x slice [a2, a3)
-                          // ATTN: kv head a0, split a1, completion counter a2
+  int32_t a0, a1, a2, a3;   // GEMV: row blocks [a0, a1); ATTN: kv head a0, split a1;
+                            // COMBINE: kv head a0, query head a1 within its group
+  int32_t pad[3];
 };
 static_assert(sizeof(DevTask) == 32, "DevTask layout");
 
@@ -45,12 +45,14 @@ struct DevModel {
   const uint16_t* ffn_norm;    // bf16 [n_layers][hidden]
   const float2* rope;          // (cos, sin) [max_seq][head_dim / 2]
   uint16_t* kv;                // bf16 [n_layers][2][n_kv_heads][max_seq][head_dim]
-  float* x;                    // residual stream [hidden]
-  float* q;                    // rotated queries [n_heads * head_dim]
-  float* o;                    // attention output [n_heads * head_dim]
-  float* a;                    // SwiGLU activations [ffn]
-  float* part;                 // attention partials [n_kv_heads][splits][group][head_dim + 2]
-  uint32_t* counters;
+  // per-step scratch of tagged words (fp32 rounded to 28 bits | 4-bit version tag)
+  uint32_t* xres;              // residual stream entering a layer [hidden]
+  uint32_t* xmid;              // residual stream after attention [hidden]
+  uint32_t* qkv;               // [n_kv_heads][(group + 2) * head_dim]: rotated q heads, k, v
+  uint32_t* o;                 // attention output [n_heads * head_dim]
+  uint32_t* a;                 // SwiGLU activations [ffn]
+  uint32_t* part;              // attention partials [n_kv_heads][splits][part_stride]:
+                               // acc [group][head_dim], then (m, l) per head, zero padding
   uint32_t* status;            // [0] code, [1] cta, [2] task, [3] site
   const DevTask* tasks;        // queue of CTA c: tasks[queue_off[c] .. queue_off[c + 1])
   const int32_t* queue_off;    // [num_ctas + 1]
@@ -62,7 +64,8 @@ struct StepParams {
   float* logits;               // [vocab] fp32 output (unused when skip_lm)
   int32_t token;
   int32_t pos;
-  uint32_t epoch;              // 1-based launch index: counter targets are epoch * producers
+  uint32_t tag_base;           // (launch index * n_layers) mod kTagPeriod: version v carries
+                               // tag 1 + (tag_base + v - 1) mod kTagPeriod (tag 0 is never written)
   int32_t skip_lm;
   uint64_t timeout_ns;
   // optional per-task timestamps (tuning aid): null, or
@@ -73,23 +76,23 @@ struct StepParams {
 };
 
 // Trace record words.  Row 0 of a CTA: start / end %globaltimer and clock64,
-// task count.  Row 1 + i for task i: consumer begin (before its wait), wait
-// satisfied, main loop done, signalled; producer first / last issue, cycles
-// blocked on a full ring; task type | layer << 8; consumer cycles spent
-// waiting for ring data; attention only: stage loop done, warp merge and
-// partial stored, ticket taken, split merge done (last split only).
+// task count, SM id.  Row 1 + i for task i: consumer begin, inputs arrived
+// (thread 0's tagged poll done), main loop done, outputs stored; producer
+// first / last issue, cycles blocked on a full ring; task type | layer << 8;
+// consumer cycles spent waiting for ring data; attention only: stage loop
+// done, warp merge done and partial stored.
 constexpr int kTraceWords = 16;
 enum TraceWord : int {
   TR_C_BEGIN = 0, TR_C_WAITED = 1, TR_C_DONE = 2, TR_C_SIGNALLED = 3,
   TR_P_FIRST = 4, TR_P_LAST = 5, TR_P_BLOCKED = 6, TR_TAG = 7,
-  TR_C_STARVED = 8, TR_A_STAGES = 9, TR_A_MERGED = 10, TR_A_TICKET = 11, TR_A_COMBINED = 12
+  TR_C_STARVED = 8, TR_A_STAGES = 9, TR_A_MERGED = 10
 };
 
 enum DevStatus : uint32_t {
   ST_OK = 0, ST_TIMEOUT = 1, ST_CHECK = 2
 };
 enum WaitSite : uint32_t {
-  SITE_COUNTER = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5
+  SITE_DATA = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5
 };
 
 // kernel geometry
@@ -98,16 +101,20 @@ constexpr int kThreads = kConsumerThreads + 32;        // + one producer warp
 constexpr int kRingBytes = 196608;                     // 192 KB of slots at most
 constexpr int kStages = kRingBytes / kStageBytes;      // slots that fit (ring_slots <= kStages)
 constexpr int kSlotBytes = kStageBytes + kSideBytes;   // 34816
-constexpr int kScratchFloats = 4352;                   // GEMV row partials / attention merge
+constexpr int kScratchFloats = 4608;                   // GEMV row partials / attention merge
 constexpr int kSmemBytes = kStages * kSlotBytes + kScratchFloats * 4 + 2 * kStages * 8 + 256;
 
-// Byte offsets of the per-step scratch regions (x, q, o, a, attention
-// partials, counters, status) laid out from one base address.
+// Byte offsets of the per-step scratch regions (tagged x_res, x_mid, qkv,
+// o, a, attention partials, then the status words) laid out from one base
+// address.
 struct StepScratchPlan {
-  size_t x = 0, q = 0, o = 0, a = 0, part = 0, counters = 0, status = 0, total = 0;
+  size_t xres = 0, xmid = 0, qkv = 0, o = 0, a = 0, part = 0, status = 0, total = 0;
   void* stream = nullptr;
   int device = 0;
 };
+
+// the per-step scratch of a model (amk_api.cpp)
+StepScratchPlan step_scratch_plan(const ModelGeom& g);
 
 // launch wrappers (decode_kernel.cu)
 int decode_smem_bytes();

@@ -99,6 +99,10 @@ amk_status plan_geometry(const amk_config& c, const BuildOptions& opt, ModelGeom
     *why = "hidden and ffn must be multiples of 8";
     return AMK_ERR_UNSUPPORTED;
   }
+  if (c.n_layers > kMaxVersions) {
+    *why = "n_layers must be <= 4096";
+    return AMK_ERR_UNSUPPORTED;
+  }
   if (opt.num_ctas <= 0 || opt.num_ctas > 4096) {
     *why = "num_ctas must be in [1, 4096]";
     return AMK_ERR_INVALID_ARG;
@@ -122,7 +126,11 @@ amk_status plan_geometry(const amk_config& c, const BuildOptions& opt, ModelGeom
   g->splits = splits;
   g->group = group;
   g->rows_max = opt.max_rows_per_task > 0 ? std::min(opt.max_rows_per_task, kRowsMax) : kRowsMax;
-  g->part_stride = group * (c.head_dim + 2);
+  g->part_stride = (group * (c.head_dim + 2) + 3) / 4 * 4;
+  if (g->mat[M_QKV].Rt % 2) {
+    *why = "qkv tiles must hold an even number of rows (RoPE pairs)";
+    return AMK_ERR_UNSUPPORTED;
+  }
   return AMK_OK;
 }
 
@@ -141,11 +149,6 @@ struct Builder {
     s.queues.assign(C, {});
   }
 
-  int counter() {
-    s.counters.push_back({});
-    return (int)s.counters.size() - 1;
-  }
-
   int task(int type, int layer, int queue) {
     Task t;
     t.type = type;
@@ -153,17 +156,12 @@ struct Builder {
     t.queue = queue;
     s.tasks.push_back(t);
     int id = (int)s.tasks.size() - 1;
-    if (queue >= 0) s.queues[queue].push_back(id);
+    s.queues[queue].push_back(id);
     return id;
   }
 
-  void signal(int t, int c) {
-    s.tasks[t].signal = c;
-    s.counters[c].producers++;
-  }
-
-  void acc(int t, int buf, int64_t lo, int64_t hi, bool write) {
-    if (hi > lo) s.tasks[t].acc.push_back({buf, lo, hi, write ? 1 : 0});
+  void acc(int t, int buf, int64_t lo, int64_t hi, bool write, int version) {
+    if (hi > lo) s.tasks[t].acc.push_back({buf, lo, hi, write ? 1 : 0, version});
   }
 
   // Row blocks of one matrix split over the CTAs; extra blocks go to the
@@ -202,127 +200,112 @@ struct Builder {
     return ids;
   }
 
-  // packed QKV rows [p0, p1) -> the ranges of Q / KVCUR they write
-  void qkv_writes(int t, int layer, int64_t p0, int64_t p1) {
+  // Packed QKV rows [p0, p1) -> the QKV words and KV-cache row elements
+  // they write.  Packed order is per KV head g: its `group` query heads,
+  // then its k head (both with RoPE pairs (i, i + hd/2) in adjacent rows),
+  // then its v head.
+  void qkv_writes(int t, int layer, int64_t p0, int64_t p1, int v) {
     const amk_config& c = g.cfg;
-    const int hd = c.head_dim, half = hd / 2;
-    const int64_t qd = (int64_t)c.n_heads * hd, kvd = (int64_t)c.n_kv_heads * hd;
-    auto rope_region = [&](int64_t r0, int64_t r1, int64_t base, int buf, int64_t off) {
-      // r0, r1 relative to the region start; pairs (2i, 2i+1) -> dims i, i + half
-      for (int64_t h0 = r0 / hd * hd; h0 < r1; h0 += hd) {
-        int64_t a = std::max(r0, h0) - h0, b = std::min(r1, h0 + hd) - h0;
-        if (b <= a) continue;
-        int64_t i0 = a / 2, i1 = (b + 1) / 2;
-        acc(t, buf, off + base + h0 + i0, off + base + h0 + i1, true);
-        acc(t, buf, off + base + h0 + half + i0, off + base + h0 + half + i1, true);
+    const int hd = c.head_dim, half = hd / 2, G = g.group;
+    const int64_t gw = (int64_t)(G + 2) * hd, kvd = (int64_t)c.n_kv_heads * hd;
+    for (int64_t h0 = p0 / hd * hd; h0 < p1; h0 += hd) {   // one head of rows at a time
+      const int64_t a = std::max(p0, h0) - h0, b = std::min(p1, h0 + hd) - h0;
+      if (b <= a) continue;
+      const int64_t grp = h0 / gw, slot = (h0 % gw) / hd;   // slot G: k, G + 1: v
+      const int64_t base = grp * gw + slot * hd;
+      if (slot <= G) {
+        const int64_t i0 = a / 2, i1 = (b + 1) / 2;
+        acc(t, B_QKV, base + i0, base + i1, true, v);
+        acc(t, B_QKV, base + half + i0, base + half + i1, true, v);
+        if (slot == G) {
+          const int64_t kb = (int64_t)(layer * 2 + 0) * kvd + grp * hd;
+          acc(t, B_KVROW, kb + i0, kb + i1, true, 0);
+          acc(t, B_KVROW, kb + half + i0, kb + half + i1, true, 0);
+        }
+      } else {
+        acc(t, B_QKV, base + a, base + b, true, v);
+        const int64_t vb = (int64_t)(layer * 2 + 1) * kvd + grp * hd;
+        acc(t, B_KVROW, vb + a, vb + b, true, 0);
       }
-    };
-    if (p0 < qd) rope_region(p0, std::min(p1, qd), 0, B_Q, 0);
-    if (p1 > qd && p0 < qd + kvd)
-      rope_region(std::max(p0, qd) - qd, std::min(p1, qd + kvd) - qd, 0, B_KVCUR,
-                  (int64_t)(layer * 2 + 0) * kvd);
-    if (p1 > qd + kvd)
-      acc(t, B_KVCUR, (int64_t)(layer * 2 + 1) * kvd + std::max(p0, qd + kvd) - qd - kvd,
-          (int64_t)(layer * 2 + 1) * kvd + std::min<int64_t>(p1, qd + 2 * kvd) - qd - kvd, true);
+    }
   }
 
   Schedule build() {
     const amk_config& c = g.cfg;
     const int L = c.n_layers, H = c.hidden, F = c.ffn, hd = c.head_dim;
     const int64_t qd = (int64_t)c.n_heads * hd, kvd = (int64_t)c.n_kv_heads * hd;
-    const int S = g.splits, G = g.group, ps = g.part_stride;
+    const int S = g.splits, G = g.group, ps = g.part_stride, NKV = c.n_kv_heads;
+    const int64_t gw = (int64_t)(G + 2) * hd;
 
+    s.versions = L;
     s.buffers.resize(B_NUM);
-    s.buffers[B_X] = {H, BUF_SCRATCH};
-    s.buffers[B_Q] = {qd, BUF_SCRATCH};
-    s.buffers[B_KVCUR] = {(int64_t)L * 2 * kvd, BUF_STATE};
-    s.buffers[B_PART] = {(int64_t)c.n_kv_heads * S * ps, BUF_SCRATCH};
-    s.buffers[B_O] = {qd, BUF_SCRATCH};
-    s.buffers[B_A] = {F, BUF_SCRATCH};
+    s.buffers[B_XRES] = {H, BUF_TAGGED};
+    s.buffers[B_XMID] = {H, BUF_TAGGED};
+    s.buffers[B_QKV] = {NKV * gw, BUF_TAGGED};
+    s.buffers[B_PART] = {(int64_t)NKV * S * ps, BUF_TAGGED};
+    s.buffers[B_O] = {qd, BUF_TAGGED};
+    s.buffers[B_A] = {F, BUF_TAGGED};
+    s.buffers[B_KVROW] = {(int64_t)L * 2 * kvd, BUF_STATE};
     s.buffers[B_LOGITS] = {c.vocab, BUF_OUTPUT};
 
-    int prev_down = -1;
     for (int l = 0; l < L; ++l) {
-      const int c_qkv = counter(), c_attn = counter(), c_o = counter(), c_gu = counter(),
-                c_down = counter();
-      std::vector<int> tickets(c.n_kv_heads);
-      for (auto& tk : tickets) tk = counter();
-
-      // QKV
-      auto qkv = distribute(M_QKV, T_QKV, l);
-      const int nq = (int)qkv.size();
-      for (int i = 0; i < nq; ++i) {
-        int t = qkv[i];
-        if (prev_down >= 0) s.tasks[t].waits.push_back({prev_down, s.counters[prev_down].producers});
-        signal(t, c_qkv);
+      const int v = l + 1;   // version written by every tagged write of layer l
+      // QKV: rmsnorm(x_res) (layer 0: the embedding row, a constant) -> q, k, v
+      for (int t : distribute(M_QKV, T_QKV, l)) {
         const MatGeom& m = g.mat[M_QKV];
-        int64_t p0 = s.tasks[t].a[0] * m.Rt, p1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
-        if (l > 0) {
-          acc(t, B_X, 0, H, false);
-        } else {
-          // layer 0 also writes its share of x = embedding row
-          int64_t xs0 = (int64_t)H * i / nq, xs1 = (int64_t)H * (i + 1) / nq;
-          s.tasks[t].a[2] = xs0;
-          s.tasks[t].a[3] = xs1;
-          acc(t, B_X, xs0, xs1, true);
-        }
-        qkv_writes(t, l, p0, p1);
+        const int64_t p0 = s.tasks[t].a[0] * m.Rt, p1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
+        if (l > 0) acc(t, B_XRES, 0, H, false, l);
+        qkv_writes(t, l, p0, p1, v);
       }
-
-      // attention: one task per (kv head, split), then the completion merge
-      for (int gh = 0; gh < c.n_kv_heads; ++gh) {
+      // attention: one task per (kv head, split) ...
+      for (int gh = 0; gh < NKV; ++gh)
         for (int j = 0; j < S; ++j) {
-          int t = task(T_ATTN, l, (gh * S + j) % C);
+          const int t = task(T_ATTN, l, (gh * S + j) % C);
           s.tasks[t].a[0] = gh;
           s.tasks[t].a[1] = j;
-          s.tasks[t].a[2] = c_attn;
-          s.tasks[t].waits.push_back({c_qkv, s.counters[c_qkv].producers});
-          signal(t, tickets[gh]);
-          acc(t, B_Q, (int64_t)gh * G * hd, (int64_t)(gh + 1) * G * hd, false);
-          if (j == S - 1) {
-            acc(t, B_KVCUR, (int64_t)(l * 2 + 0) * kvd + gh * hd, (int64_t)(l * 2 + 0) * kvd + (gh + 1) * hd, false);
-            acc(t, B_KVCUR, (int64_t)(l * 2 + 1) * kvd + gh * hd, (int64_t)(l * 2 + 1) * kvd + (gh + 1) * hd, false);
-          }
-          acc(t, B_PART, (int64_t)(gh * S + j) * ps, (int64_t)(gh * S + j + 1) * ps, true);
+          acc(t, B_QKV, gh * gw, gh * gw + (int64_t)G * hd, false, v);
+          if (j == S - 1) acc(t, B_QKV, gh * gw + (int64_t)G * hd, (gh + 1) * gw, false, v);
+          acc(t, B_PART, (int64_t)(gh * S + j) * ps, (int64_t)(gh * S + j + 1) * ps, true, v);
         }
-        int cb = task(T_COMBINE, l, -1);
-        s.tasks[cb].a[0] = gh;
-        s.counters[tickets[gh]].completion = cb;
-        signal(cb, c_attn);
-        acc(cb, B_PART, (int64_t)gh * S * ps, (int64_t)(gh + 1) * S * ps, false);
-        acc(cb, B_O, (int64_t)gh * G * hd, (int64_t)(gh + 1) * G * hd, true);
-      }
-
-      // O projection + residual
+      // ... then one LSE merge per query head, queued after every attention
+      // task of the layer, spread over the CTAs of its kv head's splits.  It
+      // reads the head's acc words of every split and the 4-word vector that
+      // holds the head's (m, l) pair.
+      for (int gh = 0; gh < NKV; ++gh)
+        for (int hh = 0; hh < G; ++hh) {
+          const int t = task(T_COMBINE, l, (gh * S + hh * std::max(1, S / G)) % C);
+          s.tasks[t].a[0] = gh;
+          s.tasks[t].a[1] = hh;
+          for (int j = 0; j < S; ++j) {
+            const int64_t sb = (int64_t)(gh * S + j) * ps;
+            acc(t, B_PART, sb + (int64_t)hh * hd, sb + (int64_t)(hh + 1) * hd, false, v);
+            acc(t, B_PART, sb + (int64_t)G * hd + (hh / 2) * 4, sb + (int64_t)G * hd + (hh / 2) * 4 + 4, false, v);
+          }
+          acc(t, B_O, (int64_t)(gh * G + hh) * hd, (int64_t)(gh * G + hh + 1) * hd, true, v);
+        }
+      // O projection: x_mid = x_res (layer 0: embedding) + o Wo^T
       for (int t : distribute(M_O, T_OPROJ, l)) {
-        s.tasks[t].waits.push_back({c_attn, s.counters[c_attn].producers});
-        signal(t, c_o);
         const MatGeom& m = g.mat[M_O];
-        int64_t r0 = s.tasks[t].a[0] * m.Rt, r1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
-        acc(t, B_O, 0, qd, false);
-        acc(t, B_X, r0, r1, false);
-        acc(t, B_X, r0, r1, true);
+        const int64_t r0 = s.tasks[t].a[0] * m.Rt, r1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
+        acc(t, B_O, 0, qd, false, v);
+        if (l > 0) acc(t, B_XRES, r0, r1, false, l);
+        acc(t, B_XMID, r0, r1, true, v);
       }
-      // gate/up + SwiGLU
+      // gate/up + SwiGLU: a = silu(g) * u of rmsnorm(x_mid)
       for (int t : distribute(M_GU, T_GATEUP, l)) {
-        s.tasks[t].waits.push_back({c_o, s.counters[c_o].producers});
-        signal(t, c_gu);
         const MatGeom& m = g.mat[M_GU];
-        int64_t p0 = s.tasks[t].a[0] * m.Rt, p1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
-        acc(t, B_X, 0, H, false);
-        acc(t, B_A, p0 / 2, (p1 + 1) / 2, true);
+        const int64_t p0 = s.tasks[t].a[0] * m.Rt, p1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
+        acc(t, B_XMID, 0, H, false, v);
+        acc(t, B_A, p0 / 2, (p1 + 1) / 2, true, v);
       }
-      // down + residual
+      // down: x_res = x_mid + a Wd^T
       for (int t : distribute(M_DOWN, T_DOWN, l)) {
-        s.tasks[t].waits.push_back({c_gu, s.counters[c_gu].producers});
-        signal(t, c_down);
         const MatGeom& m = g.mat[M_DOWN];
-        int64_t r0 = s.tasks[t].a[0] * m.Rt, r1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
-        acc(t, B_A, 0, F, false);
-        acc(t, B_X, r0, r1, false);
-        acc(t, B_X, r0, r1, true);
+        const int64_t r0 = s.tasks[t].a[0] * m.Rt, r1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
+        acc(t, B_A, 0, F, false, v);
+        acc(t, B_XMID, r0, r1, false, v);
+        acc(t, B_XRES, r0, r1, true, v);
       }
-      prev_down = c_down;
     }
 
     s.body_len.resize(C);
@@ -330,11 +313,10 @@ struct Builder {
 
     // LM head (skipped by prefill)
     for (int t : distribute(M_LM, T_LMHEAD, L - 1)) {
-      s.tasks[t].waits.push_back({prev_down, s.counters[prev_down].producers});
       const MatGeom& m = g.mat[M_LM];
-      int64_t r0 = s.tasks[t].a[0] * m.Rt, r1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
-      acc(t, B_X, 0, H, false);
-      acc(t, B_LOGITS, r0, r1, true);
+      const int64_t r0 = s.tasks[t].a[0] * m.Rt, r1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
+      acc(t, B_XRES, 0, H, false, L);
+      acc(t, B_LOGITS, r0, r1, true, 0);
     }
     return std::move(s);
   }
@@ -364,51 +346,33 @@ Report fail(std::string m) {
 }  // namespace
 
 Report validate(const Schedule& s) {
-  const int64_t T = (int64_t)s.tasks.size(), NC = (int64_t)s.counters.size(),
-                NQ = (int64_t)s.queues.size(), NB = (int64_t)s.buffers.size();
+  const int64_t T = (int64_t)s.tasks.size(), NQ = (int64_t)s.queues.size(),
+                NB = (int64_t)s.buffers.size();
+  const int32_t V = s.versions;
   if ((int64_t)s.body_len.size() != NQ) return fail("body_len size differs from queue count");
+  if (V < 1 || V > kMaxVersions) return fail(fmt_msg("versions per step %lld outside [1, %lld]", V, kMaxVersions));
+  for (int64_t b = 0; b < NB; ++b) {
+    const Buffer& B = s.buffers[b];
+    if (B.size <= 0 || B.kind < BUF_TAGGED || B.kind > BUF_STATE)
+      return fail(fmt_msg("buffer %lld: bad size or kind", b));
+  }
 
   // ---- referential integrity ------------------------------------------
-  std::vector<int32_t> producers(NC, 0);
-  std::vector<std::vector<int32_t>> prod_list(NC);
   for (int64_t t = 0; t < T; ++t) {
     const Task& k = s.tasks[t];
     if (k.type < 0 || k.type >= T_NUM_TYPES) return fail(fmt_msg("task %lld: bad type", t));
-    if (k.queue < -1 || k.queue >= NQ) return fail(fmt_msg("task %lld: bad queue %lld", t, k.queue));
-    for (const Wait& w : k.waits)
-      if (w.counter < 0 || w.counter >= NC) return fail(fmt_msg("task %lld: wait on bad counter", t));
-    if (k.signal < -1 || k.signal >= NC) return fail(fmt_msg("task %lld: bad signal counter", t));
-    if (k.signal >= 0) {
-      producers[k.signal]++;
-      prod_list[k.signal].push_back((int32_t)t);
-    }
-    if (k.acc.empty()) return fail(fmt_msg("task %lld writes and reads nothing", t));
+    if (k.queue < 0 || k.queue >= NQ) return fail(fmt_msg("task %lld: bad queue %lld", t, k.queue));
     bool writes = false;
     for (const Access& a : k.acc) {
       if (a.buffer < 0 || a.buffer >= NB) return fail(fmt_msg("task %lld: bad buffer", t));
       if (a.lo < 0 || a.hi <= a.lo || a.hi > s.buffers[a.buffer].size)
         return fail(fmt_msg("task %lld: access [%lld, %lld) out of its buffer", t, a.lo, a.hi));
+      const bool tagged = s.buffers[a.buffer].kind == BUF_TAGGED;
+      if (tagged ? (a.version < 1 || a.version > V) : a.version != 0)
+        return fail(fmt_msg("task %lld: version %lld invalid for buffer %lld", t, a.version, a.buffer));
       writes |= a.write != 0;
     }
     if (!writes) return fail(fmt_msg("task %lld writes nothing (unreachable work)", t));
-  }
-  std::vector<int32_t> completion_of(T, -1);
-  for (int64_t c = 0; c < NC; ++c) {
-    const Counter& k = s.counters[c];
-    if (k.producers != producers[c])
-      return fail(fmt_msg("counter %lld: declares %lld producers, %lld tasks signal it", c,
-                          k.producers, producers[c]));
-    if (k.completion != -1) {
-      if (k.completion < 0 || k.completion >= T) return fail(fmt_msg("counter %lld: bad completion", c));
-      if (s.tasks[k.completion].queue != -1)
-        return fail(fmt_msg("counter %lld: completion task is queued", c));
-      if (completion_of[k.completion] != -1)
-        return fail(fmt_msg("task %lld completes two counters", k.completion));
-      if (!s.tasks[k.completion].waits.empty())
-        return fail(fmt_msg("completion task %lld waits", k.completion));
-      if (k.producers == 0) return fail(fmt_msg("counter %lld: completion without producers", c));
-      completion_of[k.completion] = (int32_t)c;
-    }
   }
   std::vector<int32_t> lane_pos(T, 0), lane_of(T, -1);
   for (int64_t q = 0; q < NQ; ++q) {
@@ -424,46 +388,53 @@ Report validate(const Schedule& s) {
       lane_pos[t] = (int32_t)i + 1;
     }
   }
-  int64_t n_lanes = NQ;
-  for (int64_t t = 0; t < T; ++t) {
-    if (s.tasks[t].queue >= 0 && lane_of[t] == -1) return fail(fmt_msg("task %lld not in its queue", t));
-    if (s.tasks[t].queue == -1) {
-      if (completion_of[t] == -1) return fail(fmt_msg("task %lld has no queue and completes nothing", t));
-      lane_of[t] = (int32_t)n_lanes++;
-      lane_pos[t] = 1;
-    }
-  }
-
-  // ---- wait thresholds: 1 <= t <= #producers ---------------------------
   for (int64_t t = 0; t < T; ++t)
-    for (const Wait& w : s.tasks[t].waits)
-      if (w.threshold < 1 || w.threshold > producers[w.counter])
-        return fail(fmt_msg("task %lld: wait threshold %lld outside [1, %lld producers]", t,
-                            w.threshold, producers[w.counter]));
-
-  // ---- body (prefill) closure: body tasks never wait on skipped work ----
+    if (lane_of[t] == -1) return fail(fmt_msg("task %lld not in its queue", t));
   std::vector<char> in_body(T, 0);
   for (int64_t q = 0; q < NQ; ++q)
     for (int i = 0; i < s.body_len[q]; ++i) in_body[s.queues[q][i]] = 1;
-  for (int64_t t = 0; t < T; ++t)
-    if (s.tasks[t].queue == -1) {
-      // a completion belongs to the body iff its trigger's producers do
-      bool all = true, any = false;
-      for (int32_t p : prod_list[completion_of[t]]) {
-        all &= in_body[p] != 0;
-        any |= in_body[p] != 0;
-      }
-      if (any && !all) return fail(fmt_msg("completion %lld mixes body and skipped producers", t));
-      in_body[t] = all ? 1 : 0;
-    }
-  for (int64_t t = 0; t < T; ++t) {
-    if (!in_body[t]) continue;
-    for (const Wait& w : s.tasks[t].waits)
-      for (int32_t p : prod_list[w.counter])
-        if (!in_body[p]) return fail(fmt_msg("body task %lld waits on skipped task %lld", t, p));
-  }
 
-  // ---- acyclicity of queue-order + producer->consumer edges --------------
+  // ---- versions: one writer per element and version, every version whole --
+  // writers[b][v]: write accesses of version v to tagged buffer b, by lo
+  struct W { int64_t lo, hi; int32_t task; };
+  std::vector<std::vector<std::vector<W>>> writers(NB);
+  for (int64_t b = 0; b < NB; ++b)
+    if (s.buffers[b].kind == BUF_TAGGED) writers[b].resize(V + 1);
+  for (int64_t t = 0; t < T; ++t)
+    for (const Access& a : s.tasks[t].acc)
+      if (a.write && s.buffers[a.buffer].kind == BUF_TAGGED) {
+        if (!in_body[t])
+          return fail(fmt_msg("task %lld writes tagged buffer %lld outside the prefill body", t, a.buffer));
+        writers[a.buffer][a.version].push_back({a.lo, a.hi, (int32_t)t});
+      }
+  for (int64_t b = 0; b < NB; ++b) {
+    if (s.buffers[b].kind != BUF_TAGGED) continue;
+    for (int32_t v = 1; v <= V; ++v) {
+      auto& w = writers[b][v];
+      std::sort(w.begin(), w.end(), [](const W& x, const W& y) { return x.lo < y.lo; });
+      int64_t end = 0;
+      for (const W& x : w) {
+        if (x.lo < end)
+          return fail(fmt_msg("buffer %lld version %lld: element %lld has two writers", b, v, x.lo));
+        if (x.lo > end)
+          return fail(fmt_msg("buffer %lld version %lld: element %lld is never written", b, v, end));
+        end = x.hi;
+      }
+      if (end < s.buffers[b].size)
+        return fail(fmt_msg("buffer %lld version %lld: element %lld is never written", b, v, end));
+    }
+  }
+  // writers of version v overlapping [lo, hi), in element order
+  auto overlapping = [&](int32_t b, int32_t v, int64_t lo, int64_t hi, auto&& fn) {
+    const auto& w = writers[b][v];
+    auto it = std::upper_bound(w.begin(), w.end(), lo, [](int64_t x, const W& y) { return x < y.lo; });
+    if (it != w.begin()) --it;
+    for (; it != w.end() && it->lo < hi; ++it)
+      if (it->hi > lo) fn(*it);
+  };
+
+  // ---- acyclicity of queue order + writer -> reader edges ---------------
+  std::vector<std::vector<int32_t>> preds(T);   // writers a task waits for
   std::vector<std::vector<int32_t>> succ(T);
   std::vector<int32_t> indeg(T, 0);
   auto edge = [&](int32_t a, int32_t b) {
@@ -473,116 +444,145 @@ Report validate(const Schedule& s) {
   for (int64_t q = 0; q < NQ; ++q)
     for (size_t i = 1; i < s.queues[q].size(); ++i) edge(s.queues[q][i - 1], s.queues[q][i]);
   for (int64_t t = 0; t < T; ++t) {
-    for (const Wait& w : s.tasks[t].waits)
-      for (int32_t p : prod_list[w.counter]) edge(p, (int32_t)t);
-    if (completion_of[t] >= 0)
-      for (int32_t p : prod_list[completion_of[t]]) edge(p, (int32_t)t);
+    for (const Access& a : s.tasks[t].acc)
+      if (!a.write && s.buffers[a.buffer].kind == BUF_TAGGED)
+        overlapping(a.buffer, a.version, a.lo, a.hi, [&](const W& w) {
+          if (w.task != t) preds[t].push_back(w.task);
+        });
+    auto& p = preds[t];
+    std::sort(p.begin(), p.end());
+    p.erase(std::unique(p.begin(), p.end()), p.end());
+    for (int32_t w : p) edge(w, (int32_t)t);
   }
+  // a task that reads its own write of the version it waits for never starts
+  for (int64_t t = 0; t < T; ++t)
+    for (const Access& a : s.tasks[t].acc)
+      if (!a.write && s.buffers[a.buffer].kind == BUF_TAGGED) {
+        bool self = false;
+        overlapping(a.buffer, a.version, a.lo, a.hi, [&](const W& w) { self |= w.task == t; });
+        if (self) return fail(fmt_msg("task %lld waits for its own write", t));
+      }
   std::vector<int32_t> topo;
   topo.reserve(T);
-  for (int64_t t = 0; t < T; ++t)
-    if (!indeg[t]) topo.push_back((int32_t)t);
-  for (size_t i = 0; i < topo.size(); ++i)
-    for (int32_t b : succ[topo[i]])
-      if (--indeg[b] == 0) topo.push_back(b);
-  if ((int64_t)topo.size() != T) {
-    for (int64_t t = 0; t < T; ++t)
-      if (indeg[t]) return fail(fmt_msg("dependency cycle through task %lld", t));
-  }
-
-  // ---- deadlock: run the queues to a fixpoint (counters only grow) -------
   {
-    std::vector<int64_t> val(NC, 0);
+    std::vector<int32_t> deg = indeg;
+    for (int64_t t = 0; t < T; ++t)
+      if (!deg[t]) topo.push_back((int32_t)t);
+    for (size_t i = 0; i < topo.size(); ++i)
+      for (int32_t b : succ[topo[i]])
+        if (--deg[b] == 0) topo.push_back(b);
+    if ((int64_t)topo.size() != T) {
+      for (int64_t t = 0; t < T; ++t)
+        if (deg[t]) return fail(fmt_msg("dependency cycle through task %lld", t));
+    }
+  }
+  // prefill body: body tasks never wait for skipped work
+  for (int64_t t = 0; t < T; ++t)
+    if (in_body[t])
+      for (int32_t w : preds[t])
+        if (!in_body[w]) return fail(fmt_msg("body task %lld waits on skipped task %lld", t, w));
+
+  // ---- deadlock: run the queues to a fixpoint ----------------------------
+  {
+    std::vector<int32_t> missing(T);
+    for (int64_t t = 0; t < T; ++t) missing[t] = (int32_t)preds[t].size();
+    std::vector<std::vector<int32_t>> readers(T);
+    for (int64_t t = 0; t < T; ++t)
+      for (int32_t w : preds[t]) readers[w].push_back((int32_t)t);
     std::vector<size_t> head(NQ, 0);
-    int64_t done = 0;
-    std::vector<int32_t> pending;
-    auto fire = [&](int32_t t) {
-      pending.push_back(t);
-      while (!pending.empty()) {
-        int32_t k = pending.back();
-        pending.pop_back();
-        ++done;
-        int32_t c = s.tasks[k].signal;
-        if (c >= 0 && ++val[c] == producers[c] && s.counters[c].completion >= 0)
-          pending.push_back(s.counters[c].completion);
-      }
-    };
     bool progress = true;
     while (progress) {
       progress = false;
-      for (int64_t q = 0; q < NQ; ++q) {
-        while (head[q] < s.queues[q].size()) {
-          int32_t t = s.queues[q][head[q]];
-          bool ready = true;
-          for (const Wait& w : s.tasks[t].waits) ready &= val[w.counter] >= w.threshold;
-          if (!ready) break;
+      for (int64_t q = 0; q < NQ; ++q)
+        while (head[q] < s.queues[q].size() && missing[s.queues[q][head[q]]] == 0) {
+          for (int32_t r : readers[s.queues[q][head[q]]]) missing[r]--;
           ++head[q];
-          fire(t);
           progress = true;
         }
-      }
     }
     for (int64_t q = 0; q < NQ; ++q)
       if (head[q] < s.queues[q].size())
         return fail(fmt_msg("deadlock: queue %lld stalls at task %lld", q, s.queues[q][head[q]]));
-    if (done != T) return fail("deadlock: a completion task never fires");
   }
 
-  // ---- races: vector clocks over lanes (queues + completion tasks) --------
+  // ---- happens-before: vector clocks over the queues ---------------------
+  const int64_t Wd = NQ;
+  std::vector<int32_t> vc((size_t)T * Wd, 0);
   {
-    const int64_t W = n_lanes;
-    std::vector<int32_t> vc((size_t)T * W, 0);
-    std::vector<int32_t> tmp(W);
     std::vector<int32_t> prev_in_lane(T, -1);
     for (int64_t q = 0; q < NQ; ++q)
       for (size_t i = 1; i < s.queues[q].size(); ++i) prev_in_lane[s.queues[q][i]] = s.queues[q][i - 1];
     for (int32_t t : topo) {
-      int32_t* v = &vc[(size_t)t * W];
-      if (prev_in_lane[t] >= 0) std::memcpy(v, &vc[(size_t)prev_in_lane[t] * W], W * sizeof(int32_t));
-      auto join_all = [&](const std::vector<int32_t>& ps) {
-        for (int32_t p : ps) {
-          const int32_t* pv = &vc[(size_t)p * W];
-          for (int64_t i = 0; i < W; ++i) v[i] = std::max(v[i], pv[i]);
-        }
-      };
-      for (const Wait& w : s.tasks[t].waits) {
-        const auto& ps = prod_list[w.counter];
-        if (w.threshold == (int32_t)ps.size()) {
-          join_all(ps);
-        } else {
-          // any `threshold` of the producers may be the ones that finished:
-          // only what precedes every producer is guaranteed to precede us
-          std::fill(tmp.begin(), tmp.end(), INT32_MAX);
-          for (int32_t p : ps) {
-            const int32_t* pv = &vc[(size_t)p * W];
-            for (int64_t i = 0; i < W; ++i) tmp[i] = std::min(tmp[i], pv[i]);
-          }
-          for (int64_t i = 0; i < W; ++i) v[i] = std::max(v[i], tmp[i]);
-        }
+      int32_t* v = &vc[(size_t)t * Wd];
+      if (prev_in_lane[t] >= 0) std::memcpy(v, &vc[(size_t)prev_in_lane[t] * Wd], Wd * sizeof(int32_t));
+      for (int32_t p : preds[t]) {
+        const int32_t* pv = &vc[(size_t)p * Wd];
+        for (int64_t i = 0; i < Wd; ++i) v[i] = std::max(v[i], pv[i]);
       }
-      if (completion_of[t] >= 0) join_all(prod_list[completion_of[t]]);
       v[lane_of[t]] = lane_pos[t];
     }
-    auto hb = [&](int32_t a, int32_t b) { return vc[(size_t)b * W + lane_of[a]] >= lane_pos[a]; };
+  }
+  auto hb = [&](int32_t a, int32_t b) { return vc[(size_t)b * Wd + lane_of[a]] >= lane_pos[a]; };
 
+  // tagged buffers: writers of consecutive versions ordered (so the whole
+  // chain is), and every reader of v finished before the writer of v + 1
+  for (int64_t b = 0; b < NB; ++b) {
+    if (s.buffers[b].kind != BUF_TAGGED) continue;
+    for (int32_t v = 1; v < V; ++v)
+      for (const W& w : writers[b][v]) {
+        bool ok = true;
+        int32_t bad = -1;
+        overlapping((int32_t)b, v + 1, w.lo, w.hi, [&](const W& n) {
+          if (ok && n.task != w.task && !hb(w.task, n.task)) { ok = false; bad = n.task; }
+        });
+        if (!ok)
+          return fail(fmt_msg("buffer %lld: writer %lld of a version not ordered before writer %lld of the next", b, w.task, bad));
+      }
+  }
+  for (int64_t t = 0; t < T; ++t)
+    for (const Access& a : s.tasks[t].acc) {
+      if (a.write || s.buffers[a.buffer].kind != BUF_TAGGED || a.version == V) continue;
+      bool ok = true;
+      int32_t bad = -1;
+      overlapping(a.buffer, a.version + 1, a.lo, a.hi, [&](const W& n) {
+        if (ok && n.task != t && !hb((int32_t)t, n.task)) { ok = false; bad = n.task; }
+      });
+      if (!ok)
+        return fail(fmt_msg("buffer %lld: reader %lld may find the next version written by %lld", a.buffer, t, bad));
+    }
+  // tag aliasing: when a reader starts, the words it polls are at most
+  // kMaxTagGap versions behind.  A word holds at least the newest version
+  // whose writer happened before the reader's queue predecessor finished
+  // (writers are chained by version), else the previous step's last one.
+  for (int64_t t = 0; t < T; ++t) {
+    const int32_t prev = lane_pos[t] > 1 ? s.queues[lane_of[t]][lane_pos[t] - 2] : -1;
+    for (const Access& a : s.tasks[t].acc) {
+      if (a.write || s.buffers[a.buffer].kind != BUF_TAGGED || a.version <= kMaxTagGap) continue;
+      bool ok = false;
+      for (int32_t u = a.version - 1; u >= a.version - kMaxTagGap && !ok && prev >= 0; --u) {
+        bool all = true;
+        overlapping(a.buffer, u, a.lo, a.hi, [&](const W& w) { all = all && hb(w.task, prev); });
+        ok = all;
+      }
+      if (!ok)
+        return fail(fmt_msg("buffer %lld: reader %lld may find a version %lld or more behind (tags alias)",
+                            a.buffer, t, kTagPeriod));
+    }
+  }
+  // untagged buffers: every write ordered against every overlapping access
+  for (int64_t b = 0; b < NB; ++b) {
+    if (s.buffers[b].kind == BUF_TAGGED) continue;
     struct Acc { int64_t lo, hi; int32_t task; int32_t write; };
-    std::vector<std::vector<Acc>> per_buf(NB);
+    std::vector<Acc> v;
     for (int64_t t = 0; t < T; ++t)
-      for (const Access& a : s.tasks[t].acc) per_buf[a.buffer].push_back({a.lo, a.hi, (int32_t)t, a.write});
-    for (int64_t b = 0; b < NB; ++b) {
-      auto& v = per_buf[b];
-      std::vector<Acc> writes;
-      for (auto& a : v)
-        if (a.write) writes.push_back(a);
-      std::sort(v.begin(), v.end(), [](const Acc& x, const Acc& y) { return x.lo < y.lo; });
-      for (const Acc& w : writes) {
-        // every access overlapping w: the sorted prefix with lo < w.hi
-        for (const Acc& a : v) {
-          if (a.lo >= w.hi) break;
-          if (a.hi <= w.lo || a.task == w.task) continue;
-          if (!hb(w.task, a.task) && !hb(a.task, w.task))
-            return fail(fmt_msg("race on buffer %lld between tasks %lld and %lld", b, w.task, a.task));
-        }
+      for (const Access& a : s.tasks[t].acc)
+        if (a.buffer == b) v.push_back({a.lo, a.hi, (int32_t)t, a.write});
+    std::sort(v.begin(), v.end(), [](const Acc& x, const Acc& y) { return x.lo < y.lo; });
+    for (size_t i = 0; i < v.size(); ++i) {
+      for (size_t j = i + 1; j < v.size() && v[j].lo < v[i].hi; ++j) {
+        if (!(v[i].write || v[j].write) || v[i].task == v[j].task) continue;
+        if (!hb(v[i].task, v[j].task) && !hb(v[j].task, v[i].task))
+          return fail(fmt_msg("race on buffer %lld between tasks %lld and %lld", b, v[i].task, v[j].task));
       }
     }
   }
@@ -605,37 +605,28 @@ Report validate(const Schedule& s) {
   }
 
   Report ok;
-  ok.msg = fmt_msg("accepted: %lld tasks, %lld counters, %lld queues", T, NC, NQ);
+  ok.msg = fmt_msg("accepted: %lld tasks, %lld queues, %lld versions", T, NQ, V);
   return ok;
 }
 
 // ------------------------------------------------------------ serialisation
 
 std::vector<int64_t> serialize(const Schedule& s) {
-  int64_t nw = 0, na = 0, ni = 0;
-  for (const Task& t : s.tasks) {
-    nw += (int64_t)t.waits.size();
-    na += (int64_t)t.acc.size();
-  }
+  int64_t na = 0, ni = 0;
+  for (const Task& t : s.tasks) na += (int64_t)t.acc.size();
   for (const auto& q : s.queues) ni += (int64_t)q.size();
   std::vector<int64_t> o;
-  o.reserve(9 + s.buffers.size() * 2 + s.counters.size() * 2 + s.tasks.size() * 12 + nw * 2 +
-            na * 4 + s.queues.size() * 3 + ni);
-  o.insert(o.end(), {0x414D4B53, 1, (int64_t)s.tasks.size(), (int64_t)s.counters.size(),
-                     (int64_t)s.queues.size(), (int64_t)s.buffers.size(), nw, na, ni});
+  o.reserve(8 + s.buffers.size() * 2 + s.tasks.size() * 9 + na * 5 + s.queues.size() * 3 + ni);
+  o.insert(o.end(), {0x414D4B53, 2, (int64_t)s.tasks.size(), (int64_t)s.queues.size(),
+                     (int64_t)s.buffers.size(), na, ni, s.versions});
   for (const Buffer& b : s.buffers) o.insert(o.end(), {b.size, b.kind});
-  for (const Counter& c : s.counters) o.insert(o.end(), {c.producers, c.completion});
-  int64_t wb = 0, ab = 0;
+  int64_t ab = 0;
   for (const Task& t : s.tasks) {
-    o.insert(o.end(), {t.type, t.layer, t.queue, wb, (int64_t)t.waits.size(), t.signal, ab,
-                       (int64_t)t.acc.size(), t.a[0], t.a[1], t.a[2], t.a[3]});
-    wb += (int64_t)t.waits.size();
+    o.insert(o.end(), {t.type, t.layer, t.queue, ab, (int64_t)t.acc.size(), t.a[0], t.a[1], t.a[2], t.a[3]});
     ab += (int64_t)t.acc.size();
   }
   for (const Task& t : s.tasks)
-    for (const Wait& w : t.waits) o.insert(o.end(), {w.counter, w.threshold});
-  for (const Task& t : s.tasks)
-    for (const Access& a : t.acc) o.insert(o.end(), {a.buffer, a.lo, a.hi, a.write});
+    for (const Access& a : t.acc) o.insert(o.end(), {a.buffer, a.lo, a.hi, a.write, a.version});
   int64_t ib = 0;
   for (size_t q = 0; q < s.queues.size(); ++q) {
     o.insert(o.end(), {ib, (int64_t)s.queues[q].size(), (int64_t)s.body_len[q]});
@@ -651,16 +642,17 @@ bool deserialize(const int64_t* w, size_t n, Schedule* out, std::string* why) {
     *why = m;
     return false;
   };
-  if (n < 9 || w[0] != 0x414D4B53 || w[1] != 1) return bad("not a serialised schedule");
-  const int64_t nt = w[2], nc = w[3], nq = w[4], nb = w[5], nw = w[6], na = w[7], ni = w[8];
+  if (n < 8 || w[0] != 0x414D4B53 || w[1] != 2) return bad("not a serialised schedule");
+  const int64_t nt = w[2], nq = w[3], nb = w[4], na = w[5], ni = w[6], nv = w[7];
   const int64_t lim = (int64_t)1 << 31;
-  for (int64_t v : {nt, nc, nq, nb, nw, na, ni})
+  for (int64_t v : {nt, nq, nb, na, ni, nv})
     if (v < 0 || v >= lim) return bad("schedule header sizes out of range");
-  const int64_t need = 9 + nb * 2 + nc * 2 + nt * 12 + nw * 2 + na * 4 + nq * 3 + ni;
+  const int64_t need = 8 + nb * 2 + nt * 9 + na * 5 + nq * 3 + ni;
   if ((int64_t)n != need) return bad("schedule length does not match its header");
   auto fits32 = [](int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; };
-  const int64_t* p = w + 9;
+  const int64_t* p = w + 8;
   Schedule s;
+  s.versions = (int32_t)nv;
   s.buffers.resize(nb);
   for (auto& b : s.buffers) {
     b.size = p[0];
@@ -668,42 +660,26 @@ bool deserialize(const int64_t* w, size_t n, Schedule* out, std::string* why) {
     b.kind = (int32_t)p[1];
     p += 2;
   }
-  s.counters.resize(nc);
-  for (auto& c : s.counters) {
-    if (!fits32(p[0]) || !fits32(p[1])) return bad("bad counter");
-    c.producers = (int32_t)p[0];
-    c.completion = (int32_t)p[1];
-    p += 2;
-  }
   const int64_t* tasks = p;
-  p += nt * 12;
-  const int64_t* waits = p;
-  p += nw * 2;
+  p += nt * 9;
   const int64_t* accs = p;
-  p += na * 4;
+  p += na * 5;
   s.tasks.resize(nt);
   for (int64_t t = 0; t < nt; ++t) {
-    const int64_t* r = tasks + t * 12;
-    for (int i = 0; i < 8; ++i)
+    const int64_t* r = tasks + t * 9;
+    for (int i = 0; i < 3; ++i)
       if (!fits32(r[i])) return bad("task field out of range");
     Task& k = s.tasks[t];
     k.type = (int32_t)r[0];
     k.layer = (int32_t)r[1];
     k.queue = (int32_t)r[2];
-    if (r[3] < 0 || r[4] < 0 || r[3] + r[4] > nw) return bad("task wait range out of bounds");
+    if (r[3] < 0 || r[4] < 0 || r[3] + r[4] > na) return bad("task access range out of bounds");
     for (int64_t i = 0; i < r[4]; ++i) {
-      const int64_t* wr = waits + (r[3] + i) * 2;
-      if (!fits32(wr[0]) || !fits32(wr[1])) return bad("bad wait");
-      k.waits.push_back({(int32_t)wr[0], (int32_t)wr[1]});
+      const int64_t* ar = accs + (r[3] + i) * 5;
+      if (!fits32(ar[0]) || !fits32(ar[3]) || !fits32(ar[4])) return bad("bad access");
+      k.acc.push_back({(int32_t)ar[0], ar[1], ar[2], (int32_t)ar[3], (int32_t)ar[4]});
     }
-    k.signal = (int32_t)r[5];
-    if (r[6] < 0 || r[7] < 0 || r[6] + r[7] > na) return bad("task access range out of bounds");
-    for (int64_t i = 0; i < r[7]; ++i) {
-      const int64_t* ar = accs + (r[6] + i) * 4;
-      if (!fits32(ar[0]) || !fits32(ar[3])) return bad("bad access");
-      k.acc.push_back({(int32_t)ar[0], ar[1], ar[2], (int32_t)ar[3]});
-    }
-    for (int i = 0; i < 4; ++i) k.a[i] = r[8 + i];
+    for (int i = 0; i < 4; ++i) k.a[i] = r[5 + i];
   }
   const int64_t* queues = p;
   p += nq * 3;

@@ -11,22 +11,44 @@
 // referential integrity (AMK "The safety gate").  This file is the
 // host-side half of that design for this kernel.
 //
+// Tagged data instead of counters.  Every value one CTA hands to another
+// inside a step is a 32-bit tagged word: an fp32 rounded to 28 bits with
+// a 4-bit version tag in the low nibble.  A writer stores the word once per
+// version; a reader polls the words it needs until every tag equals the
+// version it waits for.  A read of [lo, hi) at version v is thus a wait on
+// one counter per element, with one producer and threshold 1, fused with
+// the data so that neither a fence nor a separate flag round trip is
+// needed.  The gate's conditions carry over element by element:
+//   * referential integrity: ids and ranges valid, every task queued once;
+//   * each element of a tagged buffer has exactly one writer per version
+//     and is written at every version 1..V of the step, all inside the
+//     prefill body;  this makes every read satisfiable (1 <= t <= #producers);
+//   * tags cycle through kTagPeriod values, so a stale word must never be
+//     kTagPeriod or more versions behind the one awaited: when a reader
+//     starts (its queue predecessor done), every element it reads must
+//     already hold a version within kMaxTagGap of the awaited one;
+//   * the graph of queue order plus writer -> reader edges is acyclic and
+//     the queues run to completion (no deadlock);
+//   * happens-before: the writers of an element are ordered by version and
+//     every reader of version v finishes before the writer of v + 1 starts
+//     (otherwise it could wait for a tag that is already gone); untagged
+//     buffers (KV-cache rows, logits) are race free;
+//   * outputs are reachable: every element of an output buffer is written.
+//
 // Serialised form (int64 little-endian words), used by amk_build_schedule /
 // amk_validate_serialized and by the tests that build adversarial schedules:
-//   header  [0x414D4B53, version=1, n_tasks, n_counters, n_queues, n_buffers,
-//            n_waits, n_access, n_queue_items]
-//   buffers n_buffers x [size, kind]             kind: 0 scratch, 1 output, 2 state
-//   counters n_counters x [producers_per_step, completion_task or -1]
-//   tasks   n_tasks x [type, layer, queue, wait_begin, wait_count, signal,
-//                      access_begin, access_count, a0, a1, a2, a3]
-//   waits   n_waits x [counter, threshold]
-//   access  n_access x [buffer, lo, hi, write]
+//   header  [0x414D4B53, version=2, n_tasks, n_queues, n_buffers, n_access,
+//            n_queue_items, versions_per_step]
+//   buffers n_buffers x [size, kind]        kind: 0 tagged, 1 output, 2 state
+//   tasks   n_tasks x [type, layer, queue, access_begin, access_count,
+//                      a0, a1, a2, a3]
+//   access  n_access x [buffer, lo, hi, write, version]
 //   queues  n_queues x [item_begin, item_count, body_count]
 //   items   n_queue_items x [task]
-// A task with queue -1 is a completion task: it runs once, on whichever CTA
-// delivers the last signal of the counter naming it as its completion.
-// body_count is the queue prefix that runs when the LM head is skipped
-// (prefill); the remaining items of a queue must be skippable.
+// A tagged access names a version in [1, versions_per_step]; an access to
+// an output or state buffer names version 0.  body_count is the queue
+// prefix that runs when the LM head is skipped (prefill); the remaining
+// items of a queue must be skippable.
 #pragma once
 
 #include <cstdint>
@@ -44,36 +66,45 @@ enum TaskType : int32_t {
   T_GATEUP = 3,   // rmsnorm + gate/up GEMV + SwiGLU
   T_DOWN = 4,     // down GEMV + residual
   T_LMHEAD = 5,   // final rmsnorm + LM-head GEMV
-  T_COMBINE = 6,  // LSE merge of one KV head's attention splits (completion task)
+  T_COMBINE = 6,  // LSE merge of one query head's attention splits
   T_NUM_TYPES = 7
 };
 
-enum BufKind : int32_t { BUF_SCRATCH = 0, BUF_OUTPUT = 1, BUF_STATE = 2 };
+enum BufKind : int32_t { BUF_TAGGED = 0, BUF_OUTPUT = 1, BUF_STATE = 2 };
 
 // matrix kinds of the GEMV tasks
 enum MatKind : int32_t { M_QKV = 0, M_O = 1, M_GU = 2, M_DOWN = 3, M_LM = 4, M_NUM = 5 };
 
-struct Wait { int32_t counter; int32_t threshold; };
-struct Access { int32_t buffer; int64_t lo, hi; int32_t write; };
+struct Access {
+  int32_t buffer;
+  int64_t lo, hi;
+  int32_t write;
+  int32_t version;   // tagged buffers: 1..versions_per_step; others 0
+};
 
 struct Task {
   int32_t type = 0, layer = 0, queue = -1;
-  std::vector<Wait> waits;
-  int32_t signal = -1;
   std::vector<Access> acc;
   int64_t a[4] = {0, 0, 0, 0};
 };
 
-struct Counter { int32_t producers = 0; int32_t completion = -1; };
-struct Buffer { int64_t size = 0; int32_t kind = BUF_SCRATCH; };
+struct Buffer { int64_t size = 0; int32_t kind = BUF_TAGGED; };
 
 struct Schedule {
   std::vector<Task> tasks;
-  std::vector<Counter> counters;
   std::vector<std::vector<int32_t>> queues;
   std::vector<int32_t> body_len;   // per queue
   std::vector<Buffer> buffers;
+  int32_t versions = 0;            // versions of every tagged buffer per step
 };
+
+// Versions per step, and the tag arithmetic: version v of launch e carries
+// tag 1 + ((e * V + v - 1) mod kTagPeriod); tag 0 is never written.  A word
+// at most kMaxTagGap versions behind the awaited one therefore never shows
+// the awaited tag.
+constexpr int kMaxVersions = 4096;
+constexpr int kTagPeriod = 15;
+constexpr int kMaxTagGap = kTagPeriod - 1;
 
 // Tiled layout of one weight matrix in the workspace.  Rows are grouped in
 // row blocks of Rt rows; a row block is nkt tiles of [Rt x Kt] elements,
@@ -104,7 +135,7 @@ struct ModelGeom {
   amk_config cfg{};
   MatGeom mat[M_NUM];
   int32_t num_ctas = 0, splits = 0, group = 0, rows_max = 0;
-  int32_t part_stride = 0;   // floats of one attention partial: group * (head_dim + 2)
+  int32_t part_stride = 0;   // words of one attention partial: group * (head_dim + 2), rounded up to 4
 };
 
 struct BuildOptions {
@@ -117,8 +148,16 @@ struct BuildOptions {
 amk_status plan_geometry(const amk_config& cfg, const BuildOptions& opt, ModelGeom* g,
                          std::string* why);
 
-// Buffers of the per-step scratch the validator reasons about.
-enum BufId : int32_t { B_X = 0, B_Q, B_KVCUR, B_PART, B_O, B_A, B_LOGITS, B_NUM };
+// Buffers the validator reasons about.  Tagged (per-step scratch):
+//   XRES  residual stream entering a layer (written by down, read by QKV / O / LM head)
+//   XMID  residual stream after attention (written by O, read by gate/up and down)
+//   QKV   rotated q heads, k and v of the step's position, grouped per KV head:
+//         [n_kv_heads][(group + 2) * head_dim]
+//   PART  attention partials [n_kv_heads][splits][part_stride]
+//   O     attention output [n_heads * head_dim];  A  SwiGLU output [ffn]
+// State: KVROW, the KV-cache rows at the step's position [n_layers][2][n_kv_heads * head_dim].
+// Output: LOGITS [vocab].
+enum BufId : int32_t { B_XRES = 0, B_XMID, B_QKV, B_PART, B_O, B_A, B_KVROW, B_LOGITS, B_NUM };
 
 // Lower a model to the task DAG (tasks, counters, per-CTA queues, accesses).
 Schedule build_schedule(const ModelGeom& g);

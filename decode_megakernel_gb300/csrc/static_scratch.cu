@@ -2,9 +2,9 @@
 // library instead of the context's workspace.
 //
 // A decode step needs, besides its inputs (the loaded weights, the KV cache,
-// token and position) and its output (the logits), some scratch: the fp32
-// activations x, q, o, a, the attention partials, the synchronisation
-// counters and a status word.  amk_decode_step keeps them in the workspace
+// token and position) and its output (the logits), some scratch: the tagged
+// activation words (x_res, x_mid, qkv, o, a, attention partials) and a
+// status word.  amk_decode_step keeps them in the workspace
 // the caller handed to amk_load_weights.  amk_decode_step_static_scratch
 // takes them from g_step_scratch below, a file-scope device array that
 // every GPU loading this library holds until the process exits.  It calls
@@ -27,7 +27,7 @@ amk_status internal_launch(amk_ctx* ctx, const DevModel& dm, int32_t token, int3
 amk_status internal_end_step(amk_ctx* ctx, int32_t pos, const uint32_t status[4]);
 amk_status internal_fail(amk_ctx* ctx, amk_status st, const char* msg);
 
-// 1 MiB: an 8B-shape model with 19 attention splits per KV head needs ~420 KB.
+// 1 MiB: an 8B-shape model with 19 attention splits per KV head needs ~450 KB.
 constexpr size_t kStaticScratchBytes = size_t(1) << 20;
 
 static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchBytes];
@@ -80,19 +80,20 @@ extern "C" amk_status amk_decode_step_static_scratch(amk_ctx* ctx, int32_t token
     return internal_fail(ctx, AMK_ERR_CUDA, msg);
   }
   uint8_t* b = static_cast<uint8_t*>(base);
-  dm.x = reinterpret_cast<float*>(b + plan.x);
-  dm.q = reinterpret_cast<float*>(b + plan.q);
-  dm.o = reinterpret_cast<float*>(b + plan.o);
-  dm.a = reinterpret_cast<float*>(b + plan.a);
-  dm.part = reinterpret_cast<float*>(b + plan.part);
-  dm.counters = reinterpret_cast<uint32_t*>(b + plan.counters);
+  dm.xres = reinterpret_cast<uint32_t*>(b + plan.xres);
+  dm.xmid = reinterpret_cast<uint32_t*>(b + plan.xmid);
+  dm.qkv = reinterpret_cast<uint32_t*>(b + plan.qkv);
+  dm.o = reinterpret_cast<uint32_t*>(b + plan.o);
+  dm.a = reinterpret_cast<uint32_t*>(b + plan.a);
+  dm.part = reinterpret_cast<uint32_t*>(b + plan.part);
   dm.status = reinterpret_cast<uint32_t*>(b + plan.status);
   cudaStream_t s = static_cast<cudaStream_t>(plan.stream);
 
-  // The array keeps whatever the previous call left.  The counters and the
-  // status word must start at zero (the step then runs as launch 1); every
-  // other region is fully written before it is read within a step.
-  e = cudaMemsetAsync(b + plan.counters, 0, plan.status + 64 - plan.counters, s);
+  // The array keeps whatever the previous call left.  Every call runs as
+  // launch 1, so a previous call's words carry exactly the version tags
+  // this one waits for: the whole plan (tagged words and status) is zeroed
+  // first, and tag 0 is never a version's tag.
+  e = cudaMemsetAsync(b, 0, plan.total, s);
   if (e != cudaSuccess) return internal_fail(ctx, AMK_ERR_CUDA, "clearing the static scratch failed");
   st = internal_launch(ctx, dm, token, pos, logits_dev, 1u);
   if (st != AMK_OK) return st;

@@ -4,10 +4,12 @@
 
 loads the workload's model (seeded weights, a KV cache whose first P
 positions are declared valid), runs a few untraced warm-up steps, records
-one step and prints, per task type averaged over layers: the time consumers
-spend waiting on their counter, the time their work takes after the wait,
-the span each phase adds to the step's critical path, and how long the
-producer warps sat on a full ring.
+one step and prints, per task type averaged over layers: the time
+consumers spend polling for their tagged inputs, the time their work takes
+after the inputs arrived, the hand-off lag (from the last task of the
+previous phase finishing to the median CTA of this phase having its
+inputs), the span each phase adds to the step's critical path, and how
+long the producer warps sat on a full ring.
 """
 from __future__ import annotations
 
@@ -17,7 +19,8 @@ import sys
 
 import numpy as np
 
-TYPE_NAMES = {0: "qkv", 1: "attn", 2: "o_proj", 3: "gate_up", 4: "down", 5: "lm_head"}
+TYPE_NAMES = {0: "qkv", 1: "attn", 6: "combine", 2: "o_proj", 3: "gate_up", 4: "down",
+              5: "lm_head"}
 WORDS = 16  # int64 words per trace row
 
 
@@ -44,14 +47,15 @@ def summarize(tr: np.ndarray, n_layers: int) -> str:
             r = tr[c, 1 + i]
             rows.append((c, int(r[7]) & 0xFF, int(r[7]) >> 8, r))
     out = [f"step {step_us:.1f} us on {tr.shape[0]} CTAs; SM clock ~{clk_ghz:.2f} GHz"]
-    out.append(f"{'task':8s} {'wait':>8s} {'work':>8s} {'work max':>9s} {'signal':>7s} "
-               f"{'span':>8s} {'blocked':>8s} {'starved':>8s}   (us, mean over layers; "
-               f"wait/work/signal/blocked/starved mean over CTAs)")
+    out.append(f"{'task':8s} {'wait':>8s} {'work':>8s} {'work max':>9s} {'store':>7s} "
+               f"{'lag':>7s} {'span':>8s} {'blocked':>8s} {'starved':>8s}   (us, mean over layers; "
+               f"wait/work/store/blocked/starved mean over CTAs)")
     # phase order along the critical path
-    order = [0, 1, 2, 3, 4]
-    prev_end = {}
+    order = [0, 1, 6, 2, 3, 4]
+    last_end = None
     att = []
     spans = {k: [] for k in order + [5]}
+    lags = {k: [] for k in order + [5]}
     stats = {k: [] for k in order + [5]}
     for layer in range(n_layers):
         for ty in order + ([5] if layer == n_layers - 1 else []):
@@ -61,18 +65,17 @@ def summarize(tr: np.ndarray, n_layers: int) -> str:
             a = np.array(sel, dtype=np.float64)
             wait = (a[:, 1] - a[:, 0]) / 1e3
             work = (a[:, 2] - a[:, 1]) / 1e3
-            sig = (a[:, 3] - a[:, 2]) / 1e3
+            store = (a[:, 3] - a[:, 2]) / 1e3
             blocked = a[:, 6] / clk_ghz / 1e3
             starved = a[:, 8] / clk_ghz / 1e3
             if ty == 1:
-                att.append(((a[:, 9] - a[:, 1]).mean() / 1e3, (a[:, 10] - a[:, 9]).mean() / 1e3,
-                            (a[:, 11] - a[:, 10]).mean() / 1e3,
-                            ((a[:, 12] - a[:, 11])[a[:, 12] > 0]).mean() / 1e3))
+                att.append(((a[:, 9] - a[:, 1]).mean() / 1e3, (a[:, 10] - a[:, 9]).mean() / 1e3))
             end = a[:, 3].max()
-            start_ref = prev_end.get("last", a[:, 0].min())
+            start_ref = last_end if last_end is not None else a[:, 0].min()
             spans[ty].append((end - start_ref) / 1e3)
-            prev_end["last"] = end
-            stats[ty].append((wait.mean(), work.mean(), work.max(), sig.mean(), blocked.mean(),
+            lags[ty].append((np.median(a[:, 1]) - start_ref) / 1e3)
+            last_end = end
+            stats[ty].append((wait.mean(), work.mean(), work.max(), store.mean(), blocked.mean(),
                               starved.mean()))
     total_span = 0.0
     for ty in order + [5]:
@@ -82,12 +85,11 @@ def summarize(tr: np.ndarray, n_layers: int) -> str:
         sp = float(np.mean(spans[ty]))
         total_span += sp * len(spans[ty])
         out.append(f"{TYPE_NAMES[ty]:8s} {s[0]:8.2f} {s[1]:8.2f} {s[2]:9.2f} {s[3]:7.2f} "
-                   f"{sp:8.2f} {s[4]:8.2f} {s[5]:8.2f}")
+                   f"{float(np.mean(lags[ty])):7.2f} {sp:8.2f} {s[4]:8.2f} {s[5]:8.2f}")
     out.append(f"sum of spans {total_span:.1f} us")
     if att:
         a = np.array(att).mean(0)
-        out.append(f"attention: stage loop {a[0]:.2f}, warp merge + partial store {a[1]:.2f}, "
-                   f"ticket {a[2]:.2f}, split merge (last split) {a[3]:.2f} us")
+        out.append(f"attention: stage loop {a[0]:.2f}, warp merge + partial store {a[1]:.2f} us")
     return "\n".join(out)
 
 

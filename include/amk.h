@@ -115,7 +115,7 @@ typedef struct amk_ctx amk_ctx;
 
 /*
  * Bytes of device workspace amk_load_weights needs for this model (repacked
- * weights, activations, task table, counters).  Host only when
+ * weights, tagged activation words, task table, status words).  Host only when
  * sched->num_ctas > 0; otherwise it reads the SM count of the current
  * device.  Returns 0 for an unsupported or invalid configuration.
  */
@@ -136,9 +136,12 @@ size_t amk_kv_cache_bytes(const amk_config* cfg);
  *                  amk_prefill, amk_decode_step or amk_set_kv_length;
  *   stream         cudaStream_t (NULL = legacy default stream) that every
  *                  launch of this context is ordered on.
- * The schedule is checked (acyclic, every wait threshold t with
- * 1 <= t <= #producers, races, output coverage; AMK "The safety gate")
- * before anything is launched: a failure returns AMK_ERR_SCHEDULE_INVALID.
+ * The schedule is checked (one writer per element and version, every read
+ * satisfiable, acyclic, readers ordered before the next version's writer,
+ * no stale word old enough for its 4-bit tag to alias, race-free untagged
+ * buffers, output coverage; the conditions of AMK "The safety gate" for
+ * counters fused with the data) before anything is
+ * launched: a failure returns AMK_ERR_SCHEDULE_INVALID.
  * Synchronous: on return the caller's weight buffers are no longer needed.
  */
 amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights,
@@ -171,14 +174,15 @@ amk_status amk_decode_step_host(amk_ctx* ctx, int32_t token, int32_t pos, float*
  * loop that is not allowed to allocate once it has started.  Such a caller
  * still passes its inputs (the loaded context, token, position) and its
  * output (logits_dev, fp32 [vocab], device memory); the scratch the step
- * needs besides them (fp32 activations, attention partials, synchronisation
- * counters, status word) comes from a fixed array inside libamk.so instead
+ * needs besides them (the tagged activation words and attention partials,
+ * status word) comes from a fixed array inside libamk.so instead
  * of the context's workspace.  The AMK pages have no counterpart to this
  * entry point.
  *   - Size limit: the array holds 1 MiB on every GPU that loads the library,
  *     kept until the process exits.  A model whose per-step scratch exceeds
  *     it (roughly: n_kv_heads * attn_splits * group * (head_dim + 2) * 4
- *     bytes of partials plus 4 * (hidden + 2 * n_heads * head_dim + ffn))
+ *     bytes of partials plus 4 * (2 * hidden + n_heads * head_dim +
+ *     n_kv_heads * (group + 2) * head_dim + ffn))
  *     is rejected with AMK_ERR_OOM and a message giving both sizes.
  *   - Allocation: none.  No cudaMalloc, cudaFree or allocating library call.
  *   - Set-up: the first call on each device looks up the array's device
@@ -186,7 +190,8 @@ amk_status amk_decode_step_host(amk_ctx* ctx, int32_t token, int32_t pos, float*
  *     first call before any stream capture.  The context's device must be
  *     the current device.
  *   - Sharing: every call uses the same array and finds the previous call's
- *     contents there; the call clears the counters and status word itself.
+ *     contents there; the call zeroes the whole scratch plan itself (each
+ *     call runs as launch 1, so old words would carry the awaited tags).
  *     Calls that overlap on the GPU (other streams, other threads, other
  *     contexts on the same device) race on the array and must not be made.
  *   - Synchronous: returns after the step has finished, with the device
@@ -213,8 +218,10 @@ const char* amk_last_error(const amk_ctx* ctx);
 
 /*
  * Schedule introspection (host only).  amk_build_schedule lowers a config
- * to the task DAG the kernel would run (AMK "Layer 2": a typed Schedule IR
- * synchronised by monotonic counters) and serialises it as int64 words
+ * to the task DAG the kernel would run (AMK "Layer 2": a typed Schedule IR;
+ * here its counters are fused with the data as version-tagged words, each
+ * access naming the version it writes or waits for) and serialises it as
+ * int64 words
  * into buf (cap bytes); *needed receives the size.  The format is
  * documented in decode_megakernel_gb300/csrc/schedule.hpp.
  * amk_validate_serialized runs the safety gate on such a buffer (which may
@@ -226,7 +233,7 @@ amk_status amk_validate_serialized(const void* buf, size_t bytes, char* report, 
 
 /*
  * Watchdog probe (test aid): launches a small grid of the decode kernel's
- * bounded wait on a counter that nothing ever signals, with the given
+ * bounded poll on a tagged word that nothing ever writes, with the given
  * limit, and returns the status the device reported (expected
  * AMK_ERR_TIMEOUT) in *device_status.  scratch_dev: >= 256 bytes of
  * caller device memory.  Nothing hangs: every wait is time bounded.
@@ -240,12 +247,12 @@ amk_status amk_debug_watchdog_probe(void* scratch_dev, void* stream, int32_t lim
  * the int64 buffer size and, in *stride, the longest task queue S.  The
  * buffer is [num_ctas][1 + S][16]: row 0 of a CTA holds its start and end
  * %globaltimer (ns) and clock64, and its task count; row 1 + i holds, for
- * its i-th task: consumer begin (before the counter wait), wait satisfied,
- * work done, signalled (%globaltimer ns); producer first and last copy
- * issued (ns) and clock64 cycles blocked on a full ring; task type | layer
- * << 8; consumer clock64 cycles spent waiting for ring data; for attention
- * tasks, the ends of the stage loop, of the warp merge, of the ticket and
- * (last split only) of the split merge (ns).  amk_debug_trace_step runs
+ * its i-th task: consumer begin, inputs arrived (thread 0's tagged poll
+ * done), work done, outputs stored (%globaltimer ns); producer first and
+ * last copy issued (ns) and clock64 cycles blocked on a full ring; task
+ * type | layer << 8; consumer clock64 cycles spent waiting for ring data;
+ * for attention tasks, the ends of the stage loop and of the warp merge
+ * with the partial stored (ns).  Row 0 word 5 holds the CTA's SM id.  amk_debug_trace_step runs
  * amk_decode_step with the recording on and waits for it.  trace_dev:
  * caller device memory, 8-byte aligned.
  */

@@ -6,13 +6,15 @@
 * Adversarial schedules made by mutating real ones: the validator never
   accepts one that the brute-force ground truth (tests/schedule_model.py)
   finds unsafe.  The mutations follow the failure classes the AMK safety
-  gate is meant to catch: cycles, thresholds outside [1, #producers],
-  dropped producers, consumers queued before producers, unjoined
-  multi-producer counters, unordered writers, unreachable outputs and
-  dangling ids.
+  gate is meant to catch, restated for version-tagged data: cycles
+  (waiting for a later version), unsatisfiable waits (a version nobody
+  writes), dropped or duplicated producers, consumers queued before their
+  producers, readers that may find the next version already written,
+  unordered writers, unreachable outputs and dangling ids.
 """
 import random
 
+import numpy as np
 import pytest
 
 from workload import configs as wc
@@ -56,10 +58,11 @@ def test_knob_lowerings_accepted(amk, knobs):
 
 
 def test_lowering_structure_8b(amk):
-    """Rows covered once per layer; per-CTA streamed bytes balanced."""
+    """Rows covered once per layer; per-CTA streamed bytes balanced; every
+    tagged word written once per version."""
     m = wc.LLAMA_8B_BF16
     s = sm.parse(lowered(amk, m, 2176, num_ctas=152))
-    T_QKV, T_O, T_GU, T_DOWN, T_LM = 0, 2, 3, 4, 5
+    T_QKV, T_ATTN, T_O, T_GU, T_DOWN, T_LM, T_COMB = 0, 1, 2, 3, 4, 5, 6
     # row block sizes (bf16, Kt = 2048 -> 4 rows of 2048 per 16 KB tile)
     rows = {T_QKV: 6144, T_O: 4096, T_GU: 28672, T_DOWN: 4096, T_LM: 128256}
     rt = 4
@@ -80,9 +83,21 @@ def test_lowering_structure_8b(amk):
         if t.type in rb_bytes:
             per[t.queue] += (t.a[1] - t.a[0]) * rb_bytes[t.type]
     assert max(per) / min(per) < 1.01
-    # one attention task per (kv head, split), one combine per kv head and layer
-    assert sum(t.type == 1 for t in s.tasks) == m.n_layers * 8 * 19
-    assert sum(t.type == 6 for t in s.tasks) == m.n_layers * 8
+    # one attention task per (kv head, split), one merge per query head and layer
+    assert sum(t.type == T_ATTN for t in s.tasks) == m.n_layers * 8 * 19
+    assert sum(t.type == T_COMB for t in s.tasks) == m.n_layers * 32
+    assert s.versions == m.n_layers
+    # tagged buffers: each version written exactly once per element
+    for b, (size, kind) in enumerate(s.buffers):
+        if kind != sm.TAGGED:
+            continue
+        for v in range(1, s.versions + 1):
+            cnt = np.zeros(size, dtype=np.int64)
+            for t in s.tasks:
+                for bb, lo, hi, wr, ver in t.acc:
+                    if bb == b and wr and ver == v:
+                        cnt[lo:hi] += 1
+            assert (cnt == 1).all(), (b, v)
 
 
 def test_ground_truth_agrees_on_real_lowerings(amk):
@@ -100,74 +115,85 @@ def _rand_task(s, rng, pred=lambda t: True):
     return rng.choice(ids) if ids else None
 
 
+def _tagged(s, a):
+    return 0 <= a[0] < len(s.buffers) and s.buffers[a[0]][1] == sm.TAGGED
+
+
+def _pick_access(s, rng, write):
+    cand = [(i, j) for i, t in enumerate(s.tasks) for j, a in enumerate(t.acc)
+            if bool(a[3]) == write and _tagged(s, a)]
+    return rng.choice(cand) if cand else (None, None)
+
+
 def mutate(s, rng):
     """One structural mutation; returns its name."""
-    kind = rng.randrange(14)
+    kind = rng.randrange(15)
     T = len(s.tasks)
-    if kind == 0:   # cycle: an early task waits on the last counter
-        t = _rand_task(s, rng, lambda t: t.queue >= 0)
-        c = max(range(len(s.counters)), key=lambda c: max(
-            (i for i, x in enumerate(s.tasks) if x.signal == c), default=-1))
-        s.tasks[t].waits = [(c, s.counters[c][0])]
-        return "cycle"
-    if kind == 1:   # threshold 0 or above #producers
-        t = _rand_task(s, rng, lambda t: bool(t.waits))
-        c, th = s.tasks[t].waits[0]
-        s.tasks[t].waits[0] = (c, rng.choice([0, s.counters[c][0] + 1, -3]))
-        return "threshold"
-    if kind == 2:   # drop a producer, keep the counter consistent
-        t = _rand_task(s, rng, lambda t: t.signal >= 0 and t.queue >= 0)
-        c = s.tasks[t].signal
-        s.tasks[t].signal = -1
-        s.counters[c][0] -= 1
-        for x in s.tasks:
-            x.waits = [(cc, min(th, s.counters[cc][0])) for cc, th in x.waits]
-        return "drop-producer"
-    if kind == 3:   # drop a producer, inconsistent count
-        t = _rand_task(s, rng, lambda t: t.signal >= 0)
-        s.tasks[t].signal = -1
-        return "dangling-producer"
+    if kind == 0:   # cycle: an early reader waits for a later version
+        i, j = _pick_access(s, rng, write=False)
+        if i is not None:
+            b, lo, hi, wr, v = s.tasks[i].acc[j]
+            s.tasks[i].acc[j] = (b, lo, hi, wr, min(s.versions, v + rng.randrange(1, 3)))
+        return "later-version"
+    if kind == 1:   # stale read: wait for an older version
+        i, j = _pick_access(s, rng, write=False)
+        if i is not None:
+            b, lo, hi, wr, v = s.tasks[i].acc[j]
+            s.tasks[i].acc[j] = (b, lo, hi, wr, max(1, v - 1))
+        return "older-version"
+    if kind == 2:   # drop a write: some version of some element is never written
+        i, j = _pick_access(s, rng, write=True)
+        if i is not None and len(s.tasks[i].acc) > 1:
+            del s.tasks[i].acc[j]
+        return "drop-write"
+    if kind == 3:   # a writer writes the wrong version
+        i, j = _pick_access(s, rng, write=True)
+        if i is not None:
+            b, lo, hi, wr, v = s.tasks[i].acc[j]
+            s.tasks[i].acc[j] = (b, lo, hi, wr, rng.choice([max(1, v - 1), min(s.versions, v + 1)]))
+        return "write-version"
     if kind == 4:   # consumer before its producer in one queue: swap neighbours
         q = rng.randrange(len(s.queues))
         if len(s.queues[q]) >= 2:
             i = rng.randrange(len(s.queues[q]) - 1)
             s.queues[q][i], s.queues[q][i + 1] = s.queues[q][i + 1], s.queues[q][i]
         return "swap"
-    if kind == 5:   # unjoined multi-producer counter: threshold below #producers
-        t = _rand_task(s, rng, lambda t: bool(t.waits) and s.counters[t.waits[0][0]][0] > 1)
-        if t is not None:
-            c, th = s.tasks[t].waits[0]
-            s.tasks[t].waits[0] = (c, rng.randrange(1, th))
-        return "partial-wait"
-    if kind == 6:   # remove a wait
-        t = _rand_task(s, rng, lambda t: bool(t.waits))
-        s.tasks[t].waits = []
-        return "no-wait"
+    if kind == 5:   # duplicate writer: copy a write into another task
+        i, j = _pick_access(s, rng, write=True)
+        t2 = rng.randrange(T)
+        if i is not None:
+            s.tasks[t2].acc.append(s.tasks[i].acc[j])
+        return "duplicate-write"
+    if kind == 6:   # remove a read (the task no longer waits, keeps running early)
+        i, j = _pick_access(s, rng, write=False)
+        if i is not None:
+            del s.tasks[i].acc[j]
+        return "drop-read"
     if kind == 7:   # widen a write so that two writers overlap
-        t = _rand_task(s, rng, lambda t: any(a[3] for a in t.acc))
-        acc = list(s.tasks[t].acc)
-        j = rng.choice([k for k, a in enumerate(acc) if a[3]])
-        b, lo, hi, w = acc[j]
-        acc[j] = (b, max(0, lo - rng.randrange(1, 64)), min(s.buffers[b][0], hi + rng.randrange(1, 64)), w)
-        s.tasks[t].acc = acc
+        i, j = _pick_access(s, rng, write=True)
+        if i is not None:
+            b, lo, hi, wr, v = s.tasks[i].acc[j]
+            s.tasks[i].acc[j] = (b, max(0, lo - rng.randrange(1, 64)),
+                                 min(s.buffers[b][0], hi + rng.randrange(1, 64)), wr, v)
         return "overlap"
     if kind == 8:   # unreachable output: drop the writes of one LM-head task
         t = _rand_task(s, rng, lambda t: t.type == 5)
-        s.tasks[t].acc = [a for a in s.tasks[t].acc if not a[3]] + [(0, 0, 1, 0)]
+        if t is not None:
+            s.tasks[t].acc = [a for a in s.tasks[t].acc if not a[3]] + [(0, 0, 1, 1, s.versions)]
         return "uncovered-output"
     if kind == 9:   # dangling ids
         t = rng.randrange(T)
         which = rng.randrange(3)
         if which == 0:
-            s.tasks[t].signal = len(s.counters) + 5
+            s.tasks[t].queue = len(s.queues) + 2
         elif which == 1 and s.tasks[t].acc:
-            b, lo, hi, w = s.tasks[t].acc[0]
-            s.tasks[t].acc[0] = (len(s.buffers) + 1, lo, hi, w)
+            b, lo, hi, wr, v = s.tasks[t].acc[0]
+            s.tasks[t].acc[0] = (len(s.buffers) + 1, lo, hi, wr, v)
         else:
             s.queues[rng.randrange(len(s.queues))].append(T + 3)
         return "dangling-id"
-    if kind == 10:  # move a task to the front of another queue
-        t = _rand_task(s, rng, lambda t: t.queue >= 0)
+    if kind == 10:  # move a task to another queue position
+        t = rng.randrange(T)
         q0 = s.tasks[t].queue
         q1 = rng.randrange(len(s.queues))
         s.queues[q0].remove(t)
@@ -176,33 +202,36 @@ def mutate(s, rng):
         s.tasks[t].queue = q1
         s.body[q1] = min(s.body[q1] + 1, len(s.queues[q1]))
         return "move"
-    if kind == 11:  # a completion task that waits, or loses its trigger
-        t = _rand_task(s, rng, lambda t: t.queue == -1)
-        if t is not None:
-            if rng.random() < 0.5:
-                s.tasks[t].waits = [(0, 1)]
-            else:
-                for c in s.counters:
-                    if c[1] == t:
-                        c[1] = -1
-        return "completion"
-    if kind == 12:  # prefill body that needs the LM head, or a body cut short
+    if kind == 11:  # retarget a read to another tagged buffer's range
+        i, j = _pick_access(s, rng, write=False)
+        if i is not None:
+            b, lo, hi, wr, v = s.tasks[i].acc[j]
+            b2 = rng.choice([k for k, x in enumerate(s.buffers) if x[1] == sm.TAGGED])
+            size = s.buffers[b2][0]
+            lo2 = rng.randrange(size)
+            s.tasks[i].acc[j] = (b2, lo2, min(size, lo2 + (hi - lo)), wr, v)
+        return "retarget"
+    if kind == 12:  # prefill body cut short or extended
         q = rng.randrange(len(s.queues))
         s.body[q] = rng.randrange(len(s.queues[q]) + 2)
         return "body"
-    # random field tweak
-    t = rng.randrange(T)
-    if s.tasks[t].waits:
-        c, th = s.tasks[t].waits[0]
-        s.tasks[t].waits[0] = (rng.randrange(len(s.counters)), th)
-    return "retarget"
+    if kind == 13:  # version bookkeeping
+        s.versions = rng.choice([0, s.versions - 1, s.versions + 1, 200])
+        return "versions"
+    # shrink a write (a hole in some version)
+    i, j = _pick_access(s, rng, write=True)
+    if i is not None:
+        b, lo, hi, wr, v = s.tasks[i].acc[j]
+        if hi - lo > 1:
+            s.tasks[i].acc[j] = (b, lo + 1, hi, wr, v)
+    return "shrink-write"
 
 
 def test_adversarial_no_false_accepts(amk):
     rng = random.Random(1234)
-    bases = [sm.parse(lowered(amk, m, 20, num_ctas=n))
+    bases = [sm.parse(lowered(amk, m, 20, num_ctas=n, attn_splits=sp))
              for m in (wc.TINY, wc.with_format(wc.TINY, "int8"))
-             for n in (2, 3, 4)]
+             for n, sp in ((2, 0), (3, 2), (4, 0))]
     stats = {"unsafe": 0, "safe": 0, "rejected_safe": 0}
     for i in range(1500):
         s = sm.clone(rng.choice(bases))
@@ -217,3 +246,33 @@ def test_adversarial_no_false_accepts(amk):
             assert st != amk.AMK_OK, f"false accept after {names}: truth says {why}"
     print(stats)
     assert stats["unsafe"] > 1000
+
+
+def _alias_case(reader_first: bool):
+    """A 1-element tagged buffer written at versions 1..20 by a chain of
+    tasks on queue 0, and a reader of version 20.  Alone on queue 1, the
+    reader may start while the word still holds version 0 (the previous
+    step's last), 20 versions behind: with 4-bit tags that aliases.  Queued
+    after the writer of version 20, it finds at worst version 19."""
+    V = 20
+    bufs = [(1, sm.TAGGED), (1, sm.OUTPUT), (1, sm.OUTPUT)]
+    tasks = [sm.Task(0, 0, 0, acc=[(0, 0, 1, 1, v)]) for v in range(1, V + 1)]
+    r = sm.Task(0, 0, 1 if reader_first else 0, acc=[(0, 0, 1, 0, V), (1, 0, 1, 1, 0)])
+    other = sm.Task(0, 0, 1, acc=[(2, 0, 1, 1, 0)])
+    tasks += [r, other]
+    if reader_first:
+        queues = [list(range(V)), [V, V + 1]]
+    else:
+        queues = [list(range(V + 1)), [V + 1]]
+    return sm.Schedule(bufs, tasks, queues, [len(q) for q in queues], V)
+
+
+@pytest.mark.parametrize("reader_first", [True, False])
+def test_tag_alias_gate(amk, reader_first):
+    s = _alias_case(reader_first)
+    ok, why = sm.truth(s)
+    st, rep = amk.amk_validate_serialized(sm.serialize(s))
+    assert ok == (not reader_first), why
+    assert (st == amk.AMK_OK) == ok, rep
+    if reader_first:
+        assert "alias" in rep and "alias" in why
