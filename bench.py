@@ -82,7 +82,8 @@ def profiled_traffic(workload: str):
         for line in f:
             if ":" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split(":", 1)
-                fields[k.strip()] = v.strip().strip("`")
+                v = v.split()
+                fields[k.strip()] = v[0].strip("`") if v else ""
     if fields.get("kernel_sources_sha256") != kernel_source_hash():
         return None
     try:
