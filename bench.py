@@ -57,7 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--ring-slots", type=int, default=0)
-    ap.add_argument("--l2-prefetch-tiles", type=int, default=0, help="0: off (library default)")
+    ap.add_argument("--l2-prefetch-tiles", type=int, default=0, help="0: library default, -1: off")
     return ap.parse_args(argv)
 
 
@@ -291,9 +291,8 @@ def run_ours(args, wl, rank, world, local_rank):
     P, D = wl.prompt_len, wl.decode_steps
     max_seq = wl.max_seq
     stream = torch.cuda.Stream(device=dev)
-    sched = amk.make_schedule_config(num_ctas=args.num_ctas,
-                                     l2_prefetch_tiles=args.l2_prefetch_tiles,
-                                     ring_slots=args.ring_slots)
+    sched = amk.make_schedule_config(num_ctas=args.num_ctas, ring_slots=args.ring_slots,
+                                     l2_prefetch_tiles=args.l2_prefetch_tiles)
 
     weights = synth.model_weights(cfg, seed=synth.WEIGHT_SEED, device=dev)
     dec = amk.Decoder(weights, max_seq, stream=stream, sched=sched)

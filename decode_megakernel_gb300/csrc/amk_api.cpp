@@ -15,10 +15,13 @@
 
 using namespace amk;
 
-// Default bytes of weight tiles in flight per SM.  Below the ring's capacity
-// on purpose: on GB300 the decode step measured fastest with 128 KB in
-// flight (16 KB stages x 8), and plain streaming peaks at 96-128 KB per SM.
-constexpr int kDefaultRingBytes = 131072;
+// Default weight tiles in flight per SM: the whole weight ring, 128 KB of
+// 16 KB tiles (plain streaming on GB300 peaks at 96-128 KB per SM; more
+// slots measured no faster).
+constexpr int kDefaultRingSlots = kWeightSlots;
+
+// Default L2 prefetch budget during the attention chain (tiles of 16 KB).
+constexpr int kDefaultPrefetchTiles = 0;
 
 struct amk_ctx {
   amk_config cfg{};
@@ -153,7 +156,7 @@ amk_status resolve_ctas(const amk_schedule_config* sched, BuildOptions* opt, std
     opt->attn_splits = sched->attn_splits;
     opt->max_rows_per_task = sched->max_rows_per_task;
     if (sched->num_ctas < 0 || sched->attn_splits < 0 || sched->max_rows_per_task < 0 ||
-        sched->watchdog_ms < 0 || sched->l2_prefetch_tiles < -1 || sched->ring_slots < 0) {
+        sched->watchdog_ms < 0 || sched->ring_slots < 0 || sched->l2_prefetch_tiles < -1) {
       *why = "negative schedule knob";
       return AMK_ERR_INVALID_ARG;
     }
@@ -518,9 +521,11 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   dm.part_stride = g.part_stride;
   dm.num_ctas = g.num_ctas;
   dm.rms_eps = c.rms_eps;
-  dm.prefetch_tiles = sched && sched->l2_prefetch_tiles > 0 ? std::min(sched->l2_prefetch_tiles, 1024) : 0;
-  dm.ring_slots = sched && sched->ring_slots > 0 ? std::min<int32_t>(sched->ring_slots, kStages)
-                                                 : std::min<int32_t>(kDefaultRingBytes / kStageBytes, kStages);
+  dm.ring_slots = sched && sched->ring_slots > 0 ? std::min<int32_t>(sched->ring_slots, kWeightSlots)
+                                                 : kDefaultRingSlots;
+  dm.prefetch_tiles = !sched || sched->l2_prefetch_tiles == 0 ? kDefaultPrefetchTiles
+                      : sched->l2_prefetch_tiles < 0          ? 0
+                                                              : std::min(sched->l2_prefetch_tiles, 1024);
   dm.pad0 = 0;
   dm.embed = (const uint16_t*)(ws + L.embed);
   dm.final_norm = (const uint16_t*)(ws + L.final_norm);

@@ -165,12 +165,16 @@ __device__ __forceinline__ bool consumer_sync_or(bool pred) {
 // ------------------------------------------------------------ shared memory
 
 struct Smem {
-  uint8_t ring[kStages][kSlotBytes];
+  uint8_t ring[kWeightSlots][kSlotBytes];   // weight tiles of GEMV tasks
+  uint8_t kv[kKvSlots][kStageBytes];        // K then V history tiles of attention tasks
   float scratch[kScratchFloats];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kWeightSlots];
+  uint64_t empty[kWeightSlots];
+  uint64_t kfull[kKvSlots];
+  uint64_t kempty[kKvSlots];
   float misc[32];
   int32_t abort_flag;
+  int32_t cur_task;   // queue index of the consumers' current task (read by the producer)
 };
 static_assert(sizeof(Smem) <= kSmemBytes, "shared memory layout");
 
@@ -350,121 +354,194 @@ __device__ __forceinline__ TaskTiles task_tiles(const StepParams& p, const DevTa
   return tt;
 }
 
-// Producer: one thread streams every tile of the CTA's queue into the ring.
-// Whenever no slot is free it may prefetch later tiles into L2 (up to
-// m.prefetch_tiles ahead of the last copy, off by default), so HBM keeps
-// streaming while the consumers wait for their inputs.
+// One cursor of the producer: walks the queue, issuing the tiles of the
+// tasks of its kind into its ring.
+struct RingCursor {
+  int task = 0, tile = 0;
+  TaskTiles tt;
+  bool valid = false;
+  uint32_t slot = 0, phase = 0;
+  uint32_t issued = 0;   // slots that have held a copy
+  uint32_t parity = 0;   // parity of each slot's last issued phase
+  int64_t blocked = 0;   // trace: ns spent with a full ring
+};
+
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Producer: one thread streams the tiles of the CTA's queue.  Weight tiles
+// of GEMV tasks go to the weight ring, K,V history tiles of attention
+// tasks to the KV ring, each through its own cursor over the queue: weights
+// never depend on activations and the history never depends on this step,
+// so both run ahead of the consumers, bounded only by their ring.  The KV
+// of the next attention task thus lands as soon as a KV slot frees up,
+// typically a layer ahead.
 __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_kv = policy_evict_normal();
   volatile int32_t* abort_flag = &sm.abort_flag;
-  const uint32_t nslots = (uint32_t)m.ring_slots;
-  uint32_t slot = 0, phase = 0;
-  uint32_t issued = 0;     // slots that have held a copy
-  uint32_t parity = 0;     // parity of each slot's last issued phase
+  const uint32_t wslots = (uint32_t)m.ring_slots;
+  RingCursor w, a;
   bool ok = true;
-  const int64_t ahead = m.prefetch_tiles;
+  uint64_t wait_t0 = 0;
+  // L2 prefetch of weight tiles beyond the full weight ring while the
+  // consumers are in the attention -> merge -> O chain, where they consume
+  // no weights for several microseconds: HBM keeps streaming, and the ring
+  // later refills from L2.  pf walks the weight tiles ahead of w.
+  RingCursor pf;
+  int64_t w_seq = 0, pf_seq = 0;   // weight tiles copied / prefetched so far
+  const int64_t pf_budget = m.prefetch_tiles;
+  volatile int32_t* cur_task = &sm.cur_task;
 
-  int ct = 0, cs = 0;                // copy cursor: task, tile
-  TaskTiles ctt;
-  bool cvalid = false;
-  int pt = 0, ps = 0;                // prefetch cursor
-  TaskTiles ptt;
-  bool pvalid = false;
-  int64_t copied = 0, prefetched = 0;
-  int64_t blocked = 0;
-
-  while (ct < n && ok) {
-    if (!cvalid) {
-      ctt = task_tiles(p, q[ct]);
-      cs = 0;
-      cvalid = true;
-      blocked = 0;
-      if (p.trace) trace_row(p, ct)[TR_P_FIRST] = (int64_t)global_timer();
+  // next step of cursor c over tasks of its kind: true if it issued a copy
+  // or moved on; *blocked when its ring is full
+  auto step = [&](RingCursor& c, bool kv, bool* blocked) -> bool {
+    *blocked = false;
+    if (c.task >= n) return false;
+    if (!c.valid) {
+      const DevTask& t = q[c.task];
+      const bool mine = kv ? t.type == T_ATTN : (t.type != T_ATTN && t.type != T_COMBINE);
+      if (!mine) {
+        ++c.task;
+        return true;
+      }
+      c.tt = task_tiles(p, t);
+      c.tile = 0;
+      c.valid = true;
+      c.blocked = 0;
+      if (p.trace) trace_row(p, c.task)[TR_P_FIRST] = (int64_t)global_timer();
     }
-    if (cs == ctt.nst) {
+    if (c.tile == c.tt.nst) {
       if (p.trace) {
-        int64_t* tr = trace_row(p, ct);
+        int64_t* tr = trace_row(p, c.task);
         tr[TR_P_LAST] = (int64_t)global_timer();
-        tr[TR_P_BLOCKED] = blocked;
+        tr[TR_P_BLOCKED] = c.blocked;
       }
-      ++ct;
-      cvalid = false;
+      ++c.task;
+      c.valid = false;
+      return true;
+    }
+    uint64_t* empty = kv ? &sm.kempty[c.slot] : &sm.empty[c.slot];
+    if (!mbar_test_wait(empty, c.phase ^ 1u)) {
+      *blocked = true;
+      return false;
+    }
+    uint64_t* full = kv ? &sm.kfull[c.slot] : &sm.full[c.slot];
+    if (kv) {
+      const int p0 = c.tt.t0 + c.tile * c.tt.pps;
+      const uint32_t bytes = (uint32_t)(min(c.tt.pps, c.tt.t1 - p0) * c.tt.row);
+      mbar_arrive_expect_tx(full, 2 * bytes);
+      bulk_copy_g2s(sm.kv[c.slot], c.tt.k + (int64_t)p0 * c.tt.row, bytes, full, pol_kv);
+      bulk_copy_g2s(sm.kv[c.slot] + kStageBytes / 2, c.tt.v + (int64_t)p0 * c.tt.row, bytes, full, pol_kv);
+    } else {
+      mbar_arrive_expect_tx(full, c.tt.bytes);
+      bulk_copy_g2s(sm.ring[c.slot], c.tt.k + (int64_t)c.tile * c.tt.stride, c.tt.bytes, full, pol_w);
+      ++w_seq;
+    }
+    c.issued |= 1u << c.slot;
+    c.parity = (c.parity & ~(1u << c.slot)) | (c.phase << c.slot);
+    if (++c.slot == (kv ? (uint32_t)kKvSlots : wslots)) {
+      c.slot = 0;
+      c.phase ^= 1u;
+    }
+    ++c.tile;
+    return true;
+  };
+
+  while (ok && (w.task < n || a.task < n)) {
+    if (*abort_flag) { ok = false; break; }
+    bool wb, ab;
+    const bool wp = step(w, false, &wb);
+    const bool ap = step(a, true, &ab);
+    if (wp || ap) {
+      wait_t0 = 0;
       continue;
     }
-    if (mbar_test_wait(&sm.empty[slot], phase ^ 1u)) {
-      if (*abort_flag) { ok = false; break; }
-      if (ctt.attn) {
-        const int p0 = ctt.t0 + cs * ctt.pps;
-        const uint32_t bytes = (uint32_t)(min(ctt.pps, ctt.t1 - p0) * ctt.row);
-        mbar_arrive_expect_tx(&sm.full[slot], 2 * bytes);
-        bulk_copy_g2s(sm.ring[slot], ctt.k + (int64_t)p0 * ctt.row, bytes, &sm.full[slot], pol_kv);
-        bulk_copy_g2s(sm.ring[slot] + kStageBytes / 2, ctt.v + (int64_t)p0 * ctt.row, bytes,
-                      &sm.full[slot], pol_kv);
-      } else {
-        mbar_arrive_expect_tx(&sm.full[slot], ctt.bytes);
-        bulk_copy_g2s(sm.ring[slot], ctt.k + (int64_t)cs * ctt.stride, ctt.bytes, &sm.full[slot], pol_w);
+    // both cursors wait for a consumer to release a slot (or are done).
+    // In the attention chain, prefetch the next weight tile into L2 instead.
+    if (wb && pf_budget > 0) {
+      const int ct = *cur_task;
+      const int cty = ct < n ? q[ct].type : T_LMHEAD;
+      if (cty == T_ATTN || cty == T_COMBINE || cty == T_OPROJ) {
+        if (pf_seq < w_seq) {   // the copies caught up: restart from the copy cursor
+          pf = w;
+          pf_seq = w_seq;
+        }
+        bool issued_pf = false;
+        while (pf_seq < w_seq + pf_budget && pf.task < n && !issued_pf) {
+          if (!pf.valid) {
+            const DevTask& t = q[pf.task];
+            if (t.type == T_ATTN || t.type == T_COMBINE) {
+              ++pf.task;
+              continue;
+            }
+            pf.tt = task_tiles(p, t);
+            pf.tile = 0;
+            pf.valid = true;
+          }
+          if (pf.tile == pf.tt.nst) {
+            ++pf.task;
+            pf.valid = false;
+            continue;
+          }
+          prefetch_l2(pf.tt.k + (int64_t)pf.tile * pf.tt.stride, pf.tt.bytes);
+          ++pf.tile;
+          ++pf_seq;
+          issued_pf = true;
+        }
+        if (issued_pf) {
+          wait_t0 = 0;
+          continue;
+        }
       }
-      issued |= 1u << slot;
-      parity = (parity & ~(1u << slot)) | (phase << slot);
-      if (++slot == nslots) { slot = 0; phase ^= 1u; }
-      ++cs;
-      ++copied;
-      continue;
     }
-    // no free slot: prefetch a later tile into L2 while there is one in reach
-    if (prefetched < copied) {  // the copies overtook the prefetches
-      pt = ct;
-      ps = cs;
-      ptt = ctt;
-      pvalid = true;
-      prefetched = copied;
+    // sleep briefly on the weight ring, then look at both again
+    const uint64_t now = global_timer();
+    if (!wait_t0) {
+      wait_t0 = now;
+    } else if (now - wait_t0 > p.timeout_ns) {
+      set_status(m.status, ST_TIMEOUT, (uint32_t)min(w.task, a.task), SITE_EMPTY);
+      *abort_flag = 1;
+      ok = false;
+      break;
     }
-    if (pt < n && prefetched < copied + ahead) {
-      if (!pvalid) {
-        ptt = task_tiles(p, q[pt]);
-        ps = 0;
-        pvalid = true;
-      }
-      if (ps >= ptt.nst) {
-        ++pt;
-        pvalid = false;
-        continue;
-      }
-      if (ptt.attn) {
-        const int p0 = ptt.t0 + ps * ptt.pps;
-        const uint32_t bytes = (uint32_t)(min(ptt.pps, ptt.t1 - p0) * ptt.row);
-        prefetch_l2(ptt.k + (int64_t)p0 * ptt.row, bytes);
-        prefetch_l2(ptt.v + (int64_t)p0 * ptt.row, bytes);
-      } else {
-        prefetch_l2(ptt.k + (int64_t)ps * ptt.stride, ptt.bytes);
-      }
-      ++ps;
-      ++prefetched;
-      continue;
+    if (wb) mbar_try_wait_hint(&sm.empty[w.slot], w.phase ^ 1u, 200);
+    else if (ab) mbar_try_wait_hint(&sm.kempty[a.slot], a.phase ^ 1u, 200);
+    if (p.trace) {
+      const int64_t dt = (int64_t)(global_timer() - now);
+      if (wb) w.blocked += dt;
+      if (ab) a.blocked += dt;
     }
-    // nothing to issue: wait for the oldest slot to be released
-    const int64_t c0 = p.trace ? clock64() : 0;
-    ok = wait_phase(&sm.empty[slot], phase ^ 1u, m.status, abort_flag, p.timeout_ns, ct,
-                    SITE_EMPTY) && !*abort_flag;
-    if (p.trace) blocked += clock64() - c0;
   }
   // Every copy this CTA issued must land before its shared memory goes away.
   // Consumers normally wait for all of them already; when they stop early
   // (a failed wait anywhere) this is what keeps the CTA from exiting with
   // a copy in flight.
-  for (int s = 0; s < kStages; ++s) {
-    if (!(issued & (1u << s))) continue;
-    const uint32_t par = (parity >> s) & 1u;
-    const uint64_t t0 = global_timer();
-    while (!mbar_try_wait(&sm.full[s], par)) {
-      if (global_timer() - t0 > p.timeout_ns) {
-        set_status(m.status, ST_TIMEOUT, 0xFFFFFFFFu, SITE_DRAIN);
-        break;
+  auto drain = [&](const RingCursor& c, uint64_t* full, int slots) {
+    for (int s2 = 0; s2 < slots; ++s2) {
+      if (!(c.issued & (1u << s2))) continue;
+      const uint32_t par = (c.parity >> s2) & 1u;
+      const uint64_t t0 = global_timer();
+      while (!mbar_try_wait(&full[s2], par)) {
+        if (global_timer() - t0 > p.timeout_ns) {
+          set_status(m.status, ST_TIMEOUT, 0xFFFFFFFFu, SITE_DRAIN);
+          break;
+        }
       }
     }
-  }
+  };
+  drain(w, sm.full, kWeightSlots);
+  drain(a, sm.kfull, kKvSlots);
 }
 
 // -------------------------------------------------------------- consumers
@@ -977,38 +1054,56 @@ __device__ __forceinline__ int gemv_dispatch(const StepParams& p, Smem& sm, cons
   }
 }
 
-// Split-K GQA attention of one KV head over one context split.  Per ring
-// stage a warp takes NPW cached positions; scores for R positions x G heads
-// are reduced in one transposed warp reduction, then the warp's running
-// softmax state is rescaled once per block of R positions.  The last split
-// of a KV head to finish merges all splits (LSE combine) into o.
-// HD: head_dim (a lane owns HD/32 dims of every head), G: query heads per KV head.
+// Split-K GQA attention of one KV head over one context split (positions
+// [t0, t1) of the cache, plus the step's own position for the last split).
+// The K,V history comes through the KV ring in chunks of up to kKvSlots
+// stages, all resident at once.  Each warp takes a contiguous run of a
+// chunk's positions and works alone until the final merge:
+//   scores: lanes own HD/32 dims; the partial dots of a group of R = 32/G
+//     positions x G heads go through one transposed warp reduction, which
+//     leaves one (position, head) score per lane;
+//   softmax: one maximum and one sum per head and chunk (log2(R)-level
+//     shuffles among the lanes holding that head), folded into the warp's
+//     running (m, l, acc);
+//   values: weight * V over the run, packed fp32 FMAs, weights broadcast
+//     from the warp's slice of shared memory.
+// The eight warp states are merged (LSE) through shared memory and stored
+// as the split's partial (acc, m, l).
 template <int HD, int G>
-__device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTask t, int stage,
+__device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTask t, int kstage,
                                       uint32_t task_idx, int64_t* tr) {
-  constexpr int DPL = HD / 32;
-  constexpr int PPS = (kStageBytes / 2) / (HD * 2);   // positions per stage
-  constexpr int NPW = PPS / kConsumerWarps;           // positions per warp per stage
-  constexpr int R = (32 / G) < NPW ? (32 / G) : NPW;  // positions per block
-  constexpr int V = R * G;                            // scores per block
-  constexpr int LS = 32 / V;                          // lanes per score after the reduction
+  constexpr int DPL = HD / 32;                         // dims per lane
+  constexpr int PPS = (kStageBytes / 2) / (HD * 2);   // cached positions per KV stage
+  constexpr int CP = kKvSlots * PPS;                  // positions per chunk at most
+  constexpr int R = 32 / G;                           // positions per score group
+  constexpr int CPW = CP / kConsumerWarps;            // positions of a warp's run at most
+  constexpr int NG = (CPW + R - 1) / R;               // score groups per warp
+  constexpr int PWW = NG * R * G;                     // weight floats per warp
+  // scratch (floats): per-warp weights and q staging at the front, reused
+  // at the end by the warp states [warp][G][HD + 2]; the step's own k, v at
+  // the back
+  constexpr int PW_OFF = 0, QS_OFF = kConsumerWarps * PWW, MG_OFF = 0;
+  constexpr int WS = G * (HD + 2);
+  constexpr int KV_OFF = kScratchFloats - 2 * HD;
+  static_assert(QS_OFF + G * HD <= KV_OFF && MG_OFF + kConsumerWarps * WS <= KV_OFF,
+                "attention scratch");
   const DevModel& m = p.m;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = t.a0, j = t.a1;
   volatile int32_t* abort_flag = &sm.abort_flag;
+  float* pw = sm.scratch + PW_OFF + warp * PWW;
+  float* qs = sm.scratch + QS_OFF;
+  float* mg = sm.scratch + MG_OFF;
+  float* kvs = sm.scratch + KV_OFF;
 
   const uint32_t tag = tag_of(p, t.layer + 1);
   const uint32_t* gq = m.qkv + (int64_t)g * (G + 2) * HD;   // q heads, k, v of this KV head
-  // queries of the group and, for the last split, the step's k and v:
-  // polled by 16-byte vectors into shared memory (k, v into the scratch
-  // tail, which the warp merge below never reaches)
   constexpr int QV = G * HD / 4, KVV = HD / 2;
   static_assert(QV + KVV <= kConsumerThreads, "one vector per thread");
-  static_assert(kConsumerWarps * G * (HD + 2) <= kScratchFloats - 2 * 128, "warp merge reaches the k, v tail");
   const bool last = j == m.splits - 1;
   bool failed = false;
-  float* qs = sm.scratch;
-  float* kvs = sm.scratch + kScratchFloats - 2 * HD;   // [k | v] of the current position
+  // inputs: q of the group (and, last split, the step's k and v) by
+  // 16-byte vectors into shared memory
   if (tid < QV || (last && tid < QV + KVV)) {
     const uint32_t* src = tid < QV ? gq + tid * 4 : gq + G * HD + (tid - QV) * 4;
     float* dst = tid < QV ? qs + tid * 4 : kvs + (tid - QV) * 4;
@@ -1022,6 +1117,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   }
   if (tr) tr[TR_C_WAITED] = (int64_t)global_timer();
   failed = consumer_sync_or(failed);
+  if (tr) tr[TR_A_INPUTS] = (int64_t)global_timer();
   // queries pre-scaled so that scores are in log2 units
   const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
   float qr[G][DPL];
@@ -1029,7 +1125,6 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int d = 0; d < DPL; ++d) qr[h][d] = qs[h * HD + lane * DPL + d] * qscale;
-  consumer_sync();   // qs is reused by the warp merge below
   float mx[G], l[G], acc[G][DPL];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -1039,133 +1134,159 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     for (int d = 0; d < DPL; ++d) acc[h][d] = 0.f;
   }
 
-  // one block of `np` (<= R) positions whose K and V rows this lane holds
-  auto block = [&](const float (&kf)[R][DPL], const float (&vf)[R][DPL], int np) {
-    float sc[V];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float s = 0.f;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) s = fmaf(qr[h][d], kf[r][d], s);
-        sc[r * G + h] = s;
-      }
-    float s = transpose_reduce<V>(sc, lane);   // score of (r, h) = lane / LS
-    const int idx = lane / LS;
-    const int my_r = idx / G, my_h = idx % G;
-    if (my_r >= np) s = -INFINITY;               // positions past the end of the split
-    // block maximum per head: reduce over the lanes holding other positions
-    float bm = s;
-#pragma unroll
-    for (int msk = LS * G; msk < 32; msk <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, msk));
-    float alpha[G], mnew[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float b = __shfl_sync(0xFFFFFFFFu, bm, h * LS);
-      mnew[h] = fmaxf(mx[h], b);
-      alpha[h] = exp2f(mx[h] - mnew[h]);
-    }
-    float mine = mnew[0];
-#pragma unroll
-    for (int h = 1; h < G; ++h) mine = my_h == h ? mnew[h] : mine;
-    const float pe = exp2f(s - mine);            // 0 for the padding positions
-    float bs = pe;
-#pragma unroll
-    for (int msk = LS * G; msk < 32; msk <<= 1) bs += __shfl_xor_sync(0xFFFFFFFFu, bs, msk);
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      l[h] = fmaf(l[h], alpha[h], __shfl_sync(0xFFFFFFFFu, bs, h * LS));
-      mx[h] = mnew[h];
-#pragma unroll
-      for (int d = 0; d < DPL; ++d) acc[h][d] *= alpha[h];
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float pr = __shfl_sync(0xFFFFFFFFu, pe, (r * G + h) * LS);
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(pr, vf[r][d], acc[h][d]);
-      }
-  };
-  auto unpack = [&](uint32_t lo, uint32_t hi, float* f) {
-    if constexpr (DPL == 4) {
-      f[0] = bf16_lo(lo); f[1] = bf16_hi(lo); f[2] = bf16_lo(hi); f[3] = bf16_hi(hi);
-    } else {
-      f[0] = bf16_lo(lo); f[1] = bf16_hi(lo);
-    }
-  };
-
-  const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
-  const uint32_t full0 = smem_addr(&sm.full[0]);
-  const uint32_t empty0 = smem_addr(&sm.empty[0]);
-  const uint32_t nslots = (uint32_t)m.ring_slots;
-  uint32_t slot = (uint32_t)stage % nslots, phase = ((uint32_t)stage / nslots) & 1u;
+  const uint32_t kv0 = smem_addr(&sm.kv[0][0]);
+  const uint32_t kfull0 = smem_addr(&sm.kfull[0]);
+  const uint32_t kempty0 = smem_addr(&sm.kempty[0]);
   int64_t starved = 0;
   int t0, t1;
   attn_range(p.pos, m.splits, j, &t0, &t1);
-  int nst = 0;
-  for (int s0 = t0; s0 < t1; s0 += PPS) {
-    const int np = min(PPS, t1 - s0);
-    ++nst;
-    if (!failed)
-      failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
-    if (!failed) {
-      const uint32_t kt = ring0 + slot * kSlotBytes;
-      const uint32_t vt = kt + kStageBytes / 2;
-      // warp w takes positions [w*NPW, (w+1)*NPW) of the stage
+  const int ncached = t1 - t0;
+  const int nst = (ncached + PPS - 1) / PPS;
+  uint32_t kslot = (uint32_t)kstage % kKvSlots, kphase = ((uint32_t)kstage / kKvSlots) & 1u;
+
+  // cached positions, in chunks of up to kKvSlots resident stages
+  for (int c0 = 0; c0 < ncached; c0 += CP) {
+    const int len = min(CP, ncached - c0);
+    const int s_begin = c0 / PPS, s_end = (c0 + len + PPS - 1) / PPS;
+    const uint32_t slot0 = kslot;
+    // every warp waits for all of the chunk's stages (runs may span them all)
+    for (int s2 = s_begin; s2 < s_end; ++s2) {
+      if (!failed)
+        failed = !wait_full(kfull0 + kslot * 8, kphase, p, abort_flag, task_idx, tr ? &starved : nullptr);
+      if (++kslot == (uint32_t)kKvSlots) { kslot = 0; kphase ^= 1u; }
+    }
+    // this warp's run of positions [c0 + w0, c0 + w0 + n); a position's row
+    // sits in the slot of its stage, counted from the chunk's first slot
+    const int per = (len + kConsumerWarps - 1) / kConsumerWarps;
+    const int w0 = min(len, warp * per);
+    const int n = min(len, w0 + per) - w0;
+    auto row_addr = [&](int pi) -> uint32_t {
+      uint32_t slot = slot0 + (uint32_t)(pi / PPS - s_begin);
+      if (slot >= (uint32_t)kKvSlots) slot -= kKvSlots;
+      return kv0 + slot * kStageBytes + (uint32_t)(((pi % PPS) * HD + lane * DPL) * 2);
+    };
+    if (!failed && n > 0) {
+      // scores: lane holds (r, h) = (lane / G, lane % G) of each group
+      float sc[NG];
 #pragma unroll
-      for (int b0 = 0; b0 < NPW; b0 += R) {
-        const int first = warp * NPW + b0;
-        const int nb = min(R, np - first);
-        if (nb > 0) {
-          float kf[R][DPL], vf[R][DPL];
+      for (int gi = 0; gi < NG; ++gi) {
+        sc[gi] = -INFINITY;
+        if (gi * R < n) {
+          float v[32];
 #pragma unroll
           for (int r = 0; r < R; ++r) {
-            const int pi = min(first + r, np - 1);
-            const uint32_t ko = kt + (uint32_t)((pi * HD + lane * DPL) * 2);
-            const uint32_t vo = vt + (uint32_t)((pi * HD + lane * DPL) * 2);
+            const uint32_t ad = row_addr(c0 + w0 + min(gi * R + r, n - 1));
+            float kf[DPL];
             if constexpr (DPL == 4) {
-              const uint2 kw = lds64(ko), vw = lds64(vo);
-              unpack(kw.x, kw.y, kf[r]);
-              unpack(vw.x, vw.y, vf[r]);
+              const uint2 w = lds64(ad);
+              kf[0] = bf16_lo(w.x); kf[1] = bf16_hi(w.x); kf[2] = bf16_lo(w.y); kf[3] = bf16_hi(w.y);
             } else {
-              unpack(lds32(ko), 0u, kf[r]);
-              unpack(lds32(vo), 0u, vf[r]);
+              const uint32_t w = lds32(ad);
+              kf[0] = bf16_lo(w); kf[1] = bf16_hi(w);
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              float d0 = 0.f;
+#pragma unroll
+              for (int d = 0; d < DPL; ++d) d0 = fmaf(qr[h][d], kf[d], d0);
+              v[r * G + h] = d0;
             }
           }
-          block(kf, vf, nb);
+          const float s1 = transpose_reduce<32>(v, lane);
+          if (gi * R + lane / G < n) sc[gi] = s1;
         }
       }
+      // softmax of the run, per head: lanes of one head differ in lane / G
+      float cm = sc[0];
+#pragma unroll
+      for (int gi = 1; gi < NG; ++gi) cm = fmaxf(cm, sc[gi]);
+#pragma unroll
+      for (int msk = G; msk < 32; msk <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, msk));
+      float mnew[G], alpha[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        mnew[h] = fmaxf(mx[h], __shfl_sync(0xFFFFFFFFu, cm, h));
+        alpha[h] = exp2f(mx[h] - mnew[h]);   // 0 on the first chunk
+      }
+      float mine = mnew[0];
+#pragma unroll
+      for (int h = 1; h < G; ++h) mine = (lane % G) == h ? mnew[h] : mine;
+      float ls = 0.f;
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) {
+        const float e = exp2f(sc[gi] - mine);   // 0 for padding (-inf)
+        pw[(gi * R + lane / G) * G + lane % G] = e;
+        ls += e;
+      }
+#pragma unroll
+      for (int msk = G; msk < 32; msk <<= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, msk);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        l[h] = fmaf(l[h], alpha[h], __shfl_sync(0xFFFFFFFFu, ls, h));
+        mx[h] = mnew[h];
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[h][d] *= alpha[h];
+      }
+      __syncwarp();
+      // values
+      for (int i = 0; i < n; ++i) {
+        const uint32_t ad = row_addr(c0 + w0 + i) + kStageBytes / 2;
+        float vf[DPL];
+        if constexpr (DPL == 4) {
+          const uint2 w = lds64(ad);
+          vf[0] = bf16_lo(w.x); vf[1] = bf16_hi(w.x); vf[2] = bf16_lo(w.y); vf[3] = bf16_hi(w.y);
+        } else {
+          const uint32_t w = lds32(ad);
+          vf[0] = bf16_lo(w); vf[1] = bf16_hi(w);
+        }
+        float wgt[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) wgt[h] = pw[i * G + h];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(wgt[h], vf[d], acc[h][d]);
+      }
+      __syncwarp();   // pw is rewritten by the next chunk
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive32(empty0 + slot * 8);
-    if (++slot == nslots) { slot = 0; phase ^= 1u; }
+    // release the chunk's stages
+    if (lane == 0) {
+      uint32_t sl = slot0;
+      for (int s2 = s_begin; s2 < s_end; ++s2) {
+        mbar_arrive32(kempty0 + sl * 8);
+        if (++sl == (uint32_t)kKvSlots) sl = 0;
+      }
+    }
   }
-  // the current position, written this step by the QKV tasks
+  // the step's own position (last split), written this step by the QKV
+  // tasks: one more online-softmax update on warp 0
   if (!failed && last && warp == 0) {
-    float kf[R][DPL], vf[R][DPL];
+    float kf[DPL], vf[DPL];
 #pragma unroll
     for (int d = 0; d < DPL; ++d) {
-      kf[0][d] = kvs[lane * DPL + d];
-      vf[0][d] = kvs[HD + lane * DPL + d];
+      kf[d] = kvs[lane * DPL + d];
+      vf[d] = kvs[HD + lane * DPL + d];
     }
 #pragma unroll
-    for (int r = 1; r < R; ++r)
+    for (int h = 0; h < G; ++h) {
+      float d0 = 0.f;
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) { kf[r][d] = kf[0][d]; vf[r][d] = vf[0][d]; }
-    block(kf, vf, 1);
+      for (int d = 0; d < DPL; ++d) d0 = fmaf(qr[h][d], kf[d], d0);
+      const float s1 = warp_sum(d0);
+      const float mnew = fmaxf(mx[h], s1);
+      const float alpha = exp2f(mx[h] - mnew), e = exp2f(s1 - mnew);
+      l[h] = fmaf(l[h], alpha, e);
+      mx[h] = mnew;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(e, vf[d], acc[h][d] * alpha);
+    }
   }
-
   if (tr) {
     tr[TR_C_STARVED] = starved;
     tr[TR_A_STAGES] = (int64_t)global_timer();
   }
-  // merge the eight warps' partial softmax states
-  float* mg = sm.scratch;  // [warp][G][HD + 2]
-  constexpr int WS = G * (HD + 2);
-  static_assert(kConsumerWarps * WS <= kScratchFloats, "warp merge exceeds the scratch");
+  // merge the eight warps' states (mg overlaps pw and qs: wait for all)
+  consumer_sync();
 #pragma unroll
   for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -1209,7 +1330,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   for (int idx = G * HD + 2 * G + tid; idx < m.part_stride; idx += kConsumerThreads)
     st_relaxed(part + idx, tag_word(0.f, tag));
   if (tr) tr[TR_A_MERGED] = (int64_t)global_timer();
-  return stage + nst;
+  return kstage + nst;
 }
 
 // LSE merge of one query head's S attention splits into o (AMK's split-K
@@ -1328,24 +1449,25 @@ template <int QKV_FMT, int LM_FMT>
 __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
   const int tid = threadIdx.x;
-  int stage = 0;
+  int stage = 0, kstage = 0;   // weight-ring and KV-ring stages consumed so far
   volatile int32_t* abort_flag = &sm.abort_flag;
   for (int i = 0; i < n; ++i) {
     const DevTask t = q[i];
     int64_t* tr = p.trace ? trace_row(p, i) : nullptr;
+    if (tid == 0) *(volatile int32_t*)&sm.cur_task = i;
     if (tr && tid == 0) {
       tr[TR_C_BEGIN] = (int64_t)global_timer();
       tr[TR_TAG] = t.type | (t.layer << 8);
     }
     int64_t* tr0 = tid == 0 ? tr : nullptr;
     if (t.type == T_ATTN)
-      stage = m.head_dim == 128 ? attn_dispatch<128>(p, sm, t, stage, (uint32_t)i, tr0)
-                                : attn_dispatch<64>(p, sm, t, stage, (uint32_t)i, tr0);
+      kstage = m.head_dim == 128 ? attn_dispatch<128>(p, sm, t, kstage, (uint32_t)i, tr0)
+                                 : attn_dispatch<64>(p, sm, t, kstage, (uint32_t)i, tr0);
     else if (t.type == T_COMBINE)
       stage = combine_task(p, sm, t, stage, (uint32_t)i, tr0);
     else if (t.type == T_LMHEAD) stage = gemv_dispatch<LM_FMT>(p, sm, t, stage, (uint32_t)i, tr0);
     else stage = gemv_dispatch<QKV_FMT>(p, sm, t, stage, (uint32_t)i, tr0);
-    if (stage < 0) {
+    if (stage < 0 || kstage < 0) {
       *abort_flag = 1;
       return;
     }
@@ -1361,11 +1483,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kWeightSlots; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
+    for (int s = 0; s < kKvSlots; ++s) {
+      mbar_init(&sm.kfull[s], 1);
+      mbar_init(&sm.kempty[s], kConsumerWarps);
+    }
     sm.abort_flag = 0;
+    sm.cur_task = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }

@@ -36,8 +36,9 @@ struct DevModel {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, max_seq;
   int32_t group, splits, part_stride, num_ctas;
   float rms_eps;
-  int32_t prefetch_tiles;      // tiles the producer may prefetch into L2 ahead of its copies
-  int32_t ring_slots;          // slots of the ring in use (1 <= ring_slots <= kStages)
+  int32_t ring_slots;          // slots of the weight ring in use (1 <= ring_slots <= kWeightSlots)
+  int32_t prefetch_tiles;      // weight tiles the producer may prefetch into L2 beyond its full
+                               // ring while the consumers are in attention / merge / O tasks
   int32_t pad0;
   const uint16_t* embed;       // bf16 [vocab][hidden], row major
   const uint16_t* final_norm;  // bf16 [hidden]
@@ -79,13 +80,14 @@ struct StepParams {
 // task count, SM id.  Row 1 + i for task i: consumer begin, inputs arrived
 // (thread 0's tagged poll done), main loop done, outputs stored; producer
 // first / last issue, cycles blocked on a full ring; task type | layer << 8;
-// consumer cycles spent waiting for ring data; attention only: stage loop
-// done, warp merge done and partial stored.
+// consumer cycles spent waiting for ring data; attention only: chunk loop
+// done, partial stored, every thread's inputs arrived.  Producer blocked
+// time is in ns.
 constexpr int kTraceWords = 16;
 enum TraceWord : int {
   TR_C_BEGIN = 0, TR_C_WAITED = 1, TR_C_DONE = 2, TR_C_SIGNALLED = 3,
   TR_P_FIRST = 4, TR_P_LAST = 5, TR_P_BLOCKED = 6, TR_TAG = 7,
-  TR_C_STARVED = 8, TR_A_STAGES = 9, TR_A_MERGED = 10
+  TR_C_STARVED = 8, TR_A_STAGES = 9, TR_A_MERGED = 10, TR_A_INPUTS = 11
 };
 
 enum DevStatus : uint32_t {
@@ -98,11 +100,15 @@ enum WaitSite : uint32_t {
 // kernel geometry
 constexpr int kConsumerWarps = kConsumerThreads / 32;  // 8
 constexpr int kThreads = kConsumerThreads + 32;        // + one producer warp
-constexpr int kRingBytes = 196608;                     // 192 KB of slots at most
-constexpr int kStages = kRingBytes / kStageBytes;      // slots that fit (ring_slots <= kStages)
-constexpr int kSlotBytes = kStageBytes + kSideBytes;   // 34816
+// The weight ring (tiles of GEMV tasks) and the KV ring (K,V history tiles
+// of attention tasks) are separate so that the KV of the next attention
+// task is loaded as soon as a KV slot frees up, never behind weight tiles.
+constexpr int kWeightSlots = 8;                        // 136 KB: 16 KB tiles + int4 side data
+constexpr int kKvSlots = 4;                            // 64 KB: K then V of up to 32 (hd 128) positions each
+constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one weight slot
 constexpr int kScratchFloats = 4608;                   // GEMV row partials / attention merge
-constexpr int kSmemBytes = kStages * kSlotBytes + kScratchFloats * 4 + 2 * kStages * 8 + 256;
+constexpr int kSmemBytes = kWeightSlots * kSlotBytes + kKvSlots * kStageBytes + kScratchFloats * 4 +
+                           2 * (kWeightSlots + kKvSlots) * 8 + 256;
 
 // Byte offsets of the per-step scratch regions (tagged x_res, x_mid, qkv,
 // o, a, attention partials, then the status words) laid out from one base

@@ -66,10 +66,11 @@ def summarize(tr: np.ndarray, n_layers: int) -> str:
             wait = (a[:, 1] - a[:, 0]) / 1e3
             work = (a[:, 2] - a[:, 1]) / 1e3
             store = (a[:, 3] - a[:, 2]) / 1e3
-            blocked = a[:, 6] / clk_ghz / 1e3
+            blocked = a[:, 6] / 1e3
             starved = a[:, 8] / clk_ghz / 1e3
             if ty == 1:
-                att.append(((a[:, 9] - a[:, 1]).mean() / 1e3, (a[:, 10] - a[:, 9]).mean() / 1e3))
+                att.append(((a[:, 11] - a[:, 0]).mean() / 1e3, (a[:, 9] - a[:, 11]).mean() / 1e3,
+                            (a[:, 10] - a[:, 9]).mean() / 1e3))
             end = a[:, 3].max()
             start_ref = last_end if last_end is not None else a[:, 0].min()
             spans[ty].append((end - start_ref) / 1e3)
@@ -89,7 +90,8 @@ def summarize(tr: np.ndarray, n_layers: int) -> str:
     out.append(f"sum of spans {total_span:.1f} us")
     if att:
         a = np.array(att).mean(0)
-        out.append(f"attention: stage loop {a[0]:.2f}, warp merge + partial store {a[1]:.2f} us")
+        out.append(f"attention: all inputs arrived {a[0]:.2f} after begin, chunk loop {a[1]:.2f}, "
+                   f"warp merge + partial store {a[2]:.2f} us")
     return "\n".join(out)
 
 
@@ -119,8 +121,8 @@ def main(argv=None):
     kv = synth.synthetic_kv_cache(cfg, wl.prompt_len, wl.max_seq, device=dev)
     dec = amk.Decoder(w, wl.max_seq, kv_cache=kv,
                       sched=amk.make_schedule_config(num_ctas=args.num_ctas,
-                                                     l2_prefetch_tiles=args.l2_prefetch_tiles,
-                                     ring_slots=args.ring_slots))
+                                                     ring_slots=args.ring_slots,
+                                                     l2_prefetch_tiles=args.l2_prefetch_tiles))
     del w
     torch.cuda.empty_cache()
     dec.set_kv_length(wl.prompt_len)

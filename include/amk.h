@@ -104,10 +104,11 @@ typedef struct {
     int32_t attn_splits;        /* context splits per KV head (default: num_ctas / n_kv_heads) */
     int32_t max_rows_per_task;  /* rows of one GEMV task (default and maximum 256) */
     int32_t watchdog_ms;        /* device wait limit before AMK_ERR_TIMEOUT (default 2000) */
-    int32_t l2_prefetch_tiles;  /* tiles each CTA may prefetch into L2 beyond its ring
-                                   when no slot is free (default 0: off) */
-    int32_t ring_slots;         /* shared-memory ring slots in use per CTA (default: 128 KB
-                                   worth; at most the 192 KB the ring holds) */
+    int32_t ring_slots;         /* slots of the per-CTA weight ring in use, 1..8 (default 8:
+                                   128 KB of 16 KB weight tiles in flight) */
+    int32_t l2_prefetch_tiles;  /* weight tiles a CTA may prefetch into L2 beyond its full
+                                   ring while its consumers run attention, the split merge
+                                   or the O projection (-1: off; 0: default) */
     int32_t reserved[2];
 } amk_schedule_config;
 
