@@ -80,6 +80,7 @@ def _load():
         "amk_prefill": (C.c_int, [P, C.POINTER(C.c_int32), C.c_int32, C.c_int32]),
         "amk_decode_step": (C.c_int, [P, C.c_int32, C.c_int32, P]),
         "amk_decode_step_host": (C.c_int, [P, C.c_int32, C.c_int32, P]),
+        "amk_generate": (C.c_int, [P, C.c_int32, C.c_int32, C.c_int32, P, P]),
         "amk_decode_step_static_scratch": (C.c_int, [P, C.c_int32, C.c_int32, P]),
         "amk_set_kv_length": (C.c_int, [P, C.c_int32]),
         "amk_kv_length": (C.c_int32, [P]),
@@ -152,6 +153,12 @@ def amk_decode_step(ctx, token: int, pos: int, logits_ptr: int) -> int:
 
 def amk_decode_step_host(ctx, token: int, pos: int, logits_host_ptr: int) -> int:
     return int(lib.amk_decode_step_host(ctx, int(token), int(pos), C.c_void_p(logits_host_ptr)))
+
+
+def amk_generate(ctx, first_token: int, pos: int, n_steps: int, tokens_dev_ptr: int,
+                 logits_dev_ptr: int = 0) -> int:
+    return int(lib.amk_generate(ctx, int(first_token), int(pos), int(n_steps),
+                                C.c_void_p(tokens_dev_ptr), C.c_void_p(logits_dev_ptr or None)))
 
 
 def amk_decode_step_static_scratch(ctx, token: int, pos: int, logits_ptr: int) -> int:
@@ -290,6 +297,17 @@ class Decoder:
     def decode_step_host(self, token: int, pos: int, logits_host: torch.Tensor):
         assert logits_host.dtype == torch.float32 and not logits_host.is_cuda
         check(amk_decode_step_host(self.ctx, token, pos, logits_host.data_ptr()), self.ctx)
+
+    def generate(self, first_token: int, pos: int, n_steps: int, tokens: torch.Tensor,
+                 logits: torch.Tensor | None = None):
+        """Greedy decoding on the device (amk_generate): tokens (int32 cuda
+        [n_steps]) receives the argmax of each step's logits."""
+        assert tokens.dtype == torch.int32 and tokens.is_cuda and tokens.numel() >= n_steps
+        lp = 0
+        if logits is not None:
+            assert logits.dtype == torch.float32 and logits.is_cuda
+            lp = logits.data_ptr()
+        check(amk_generate(self.ctx, first_token, pos, n_steps, tokens.data_ptr(), lp), self.ctx)
 
     def set_kv_length(self, n: int):
         check(amk_set_kv_length(self.ctx, n), self.ctx)

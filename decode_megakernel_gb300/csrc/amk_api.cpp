@@ -40,6 +40,8 @@ struct amk_ctx {
   uint64_t timeout_ns = 0;
   amk_status poisoned = AMK_OK;
   int32_t max_queue = 0;  // longest per-CTA task queue (trace sizing)
+  int32_t n_lm = 0;       // LM-head tasks: argmax pairs per step
+  uint32_t* amax[2] = {nullptr, nullptr};  // per-step argmax pairs, double buffered
   std::string err;
 };
 
@@ -70,7 +72,7 @@ struct Layout {
   size_t w[M_NUM] = {};
   size_t scales[M_NUM] = {};
   size_t mats = 0, embed = 0, attn_norm = 0, ffn_norm = 0, final_norm = 0, rope = 0;
-  size_t xres = 0, xmid = 0, qkv = 0, o = 0, a = 0, part = 0, status = 0, logits = 0;
+  size_t xres = 0, xmid = 0, qkv = 0, o = 0, a = 0, part = 0, status = 0, logits = 0, amax = 0;
   size_t tasks = 0, queue_off = 0, queue_body = 0, total = 0;
 };
 
@@ -140,6 +142,7 @@ Layout make_layout(const ModelGeom& g, const Schedule& s) {
   L.part = base + sp.part;
   L.status = base + sp.status;
   L.logits = take((size_t)c.vocab * 4);
+  L.amax = take((size_t)s.buffers[B_AMAX].size * 4 * 2);
   size_t n_queued = 0;
   for (const auto& q : s.queues) n_queued += q.size();
   L.tasks = take(n_queued * sizeof(DevTask));
@@ -211,18 +214,27 @@ bool linear_ok(const amk_linear& l, int fmt) {
   return aligned(l.w, 4) && l.scales && aligned(l.scales, 2) && l.zeros;
 }
 
-amk_status launch_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits, int skip_lm) {
+// Launch parameters of one step; greedy-decoding and trace fields off.
+StepParams make_params(const amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
+                       float* logits, int skip_lm, uint32_t epoch) {
   StepParams p;
-  p.m = ctx->dm;
+  p.m = dm;
   p.logits = logits;
   p.token = token;
   p.pos = pos;
-  p.tag_base = tag_base_of(++ctx->epoch, ctx->cfg.n_layers);
+  p.tag_base = tag_base_of(epoch, ctx->cfg.n_layers);
   p.skip_lm = skip_lm;
   p.timeout_ns = ctx->timeout_ns;
   p.trace = nullptr;
   p.trace_stride = 0;
-  p.pad1 = 0;
+  p.n_lm = ctx->n_lm;
+  p.amax = nullptr;
+  p.token_src = nullptr;
+  p.token_out = nullptr;
+  return p;
+}
+
+amk_status launch_params(amk_ctx* ctx, StepParams& p) {
   void* args[] = {&p};
   cudaError_t e = cudaLaunchCooperativeKernel(ctx->kernel, dim3(ctx->geom.num_ctas),
                                               dim3(kThreads), args, (size_t)ctx->smem, ctx->stream);
@@ -231,6 +243,11 @@ amk_status launch_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits, 
     return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel");
   }
   return AMK_OK;
+}
+
+amk_status launch_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits, int skip_lm) {
+  StepParams p = make_params(ctx, ctx->dm, token, pos, logits, skip_lm, ++ctx->epoch);
+  return launch_params(ctx, p);
 }
 
 amk_status step_checks(amk_ctx* ctx, int32_t token, int32_t pos) {
@@ -283,25 +300,8 @@ amk_status internal_begin_step(amk_ctx* ctx, int32_t token, int32_t pos, const f
 
 amk_status internal_launch(amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
                            float* logits, uint32_t epoch) {
-  StepParams p;
-  p.m = dm;
-  p.logits = logits;
-  p.token = token;
-  p.pos = pos;
-  p.tag_base = tag_base_of(epoch, ctx->cfg.n_layers);
-  p.skip_lm = 0;
-  p.timeout_ns = ctx->timeout_ns;
-  p.trace = nullptr;
-  p.trace_stride = 0;
-  p.pad1 = 0;
-  void* args[] = {&p};
-  cudaError_t e = cudaLaunchCooperativeKernel(ctx->kernel, dim3(ctx->geom.num_ctas),
-                                              dim3(kThreads), args, (size_t)ctx->smem, ctx->stream);
-  if (e != cudaSuccess) {
-    ctx->poisoned = AMK_ERR_CUDA;
-    return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel");
-  }
-  return AMK_OK;
+  StepParams p = make_params(ctx, dm, token, pos, logits, 0, epoch);
+  return launch_params(ctx, p);
 }
 
 amk_status internal_end_step(amk_ctx* ctx, int32_t pos, const uint32_t status[4]) {
@@ -565,6 +565,9 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   }
   qoff[s.queues.size()] = (int32_t)tasks.size();
   for (const auto& q : s.queues) ctx->max_queue = std::max<int32_t>(ctx->max_queue, (int32_t)q.size());
+  ctx->n_lm = (int32_t)(s.buffers[B_AMAX].size / 2);
+  ctx->amax[0] = (uint32_t*)(ws + L.amax);
+  ctx->amax[1] = ctx->amax[0] + 2 * ctx->n_lm;
 
   // rotate-half RoPE table, computed in double and rounded to float
   const int half = c.head_dim / 2;
@@ -660,6 +663,31 @@ amk_status amk_decode_step_host(amk_ctx* ctx, int32_t token, int32_t pos, float*
   return amk_sync(ctx);
 }
 
+amk_status amk_generate(amk_ctx* ctx, int32_t first_token, int32_t pos, int32_t n_steps,
+                        int32_t* tokens_dev, float* logits_dev) {
+  amk_status st = step_checks(ctx, first_token, pos);
+  if (st != AMK_OK) return st;
+  if (n_steps < 1 || (int64_t)pos + n_steps > ctx->cfg.max_seq)
+    return fail(ctx, AMK_ERR_INVALID_ARG, "n_steps must be >= 1 and pos + n_steps <= max_seq");
+  if (!tokens_dev || ((uintptr_t)tokens_dev & 3) || (logits_dev && ((uintptr_t)logits_dev & 3)))
+    return fail(ctx, AMK_ERR_INVALID_ARG, "tokens_dev NULL or misaligned, or logits_dev misaligned");
+  float* logits = logits_dev ? logits_dev : ctx->logits_stage;
+  for (int32_t i = 0; i < n_steps; ++i) {
+    StepParams p = make_params(ctx, ctx->dm, first_token, pos + i, logits, 0, ++ctx->epoch);
+    p.amax = ctx->amax[i & 1];
+    if (i > 0) {
+      p.token_src = ctx->amax[(i - 1) & 1];
+      p.token_out = tokens_dev + (i - 1);
+    }
+    st = launch_params(ctx, p);
+    if (st != AMK_OK) return st;
+    ctx->kv_len = pos + i + 1;
+  }
+  launch_argmax_pairs(ctx->amax[(n_steps - 1) & 1], ctx->n_lm, tokens_dev + (n_steps - 1), ctx->stream);
+  AMK_CUDA(ctx, cudaGetLastError());
+  return AMK_OK;
+}
+
 amk_status amk_set_kv_length(amk_ctx* ctx, int32_t n) {
   if (!ctx) return fail(nullptr, AMK_ERR_INVALID_ARG, "context is NULL");
   if (n < 0 || n > ctx->cfg.max_seq) return fail(ctx, AMK_ERR_INVALID_ARG, "KV length out of range");
@@ -696,24 +724,11 @@ amk_status amk_debug_trace_step(amk_ctx* ctx, int32_t token, int32_t pos, float*
       trace_bytes < amk_debug_trace_bytes(ctx, nullptr))
     return fail(ctx, AMK_ERR_INVALID_ARG, "bad logits or trace buffer (see amk_debug_trace_bytes)");
   AMK_CUDA(ctx, cudaMemsetAsync(trace_dev, 0, amk_debug_trace_bytes(ctx, nullptr), ctx->stream));
-  StepParams p;
-  p.m = ctx->dm;
-  p.logits = logits_dev;
-  p.token = token;
-  p.pos = pos;
-  p.tag_base = tag_base_of(++ctx->epoch, ctx->cfg.n_layers);
-  p.skip_lm = 0;
-  p.timeout_ns = ctx->timeout_ns;
+  StepParams p = make_params(ctx, ctx->dm, token, pos, logits_dev, 0, ++ctx->epoch);
   p.trace = trace_dev;
   p.trace_stride = ctx->max_queue;
-  p.pad1 = 0;
-  void* args[] = {&p};
-  cudaError_t e = cudaLaunchCooperativeKernel(ctx->kernel, dim3(ctx->geom.num_ctas),
-                                              dim3(kThreads), args, (size_t)ctx->smem, ctx->stream);
-  if (e != cudaSuccess) {
-    ctx->poisoned = AMK_ERR_CUDA;
-    return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel");
-  }
+  st = launch_params(ctx, p);
+  if (st != AMK_OK) return st;
   ctx->kv_len = pos + 1;
   return amk_sync(ctx);
 }

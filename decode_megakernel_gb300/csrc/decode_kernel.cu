@@ -175,6 +175,7 @@ struct Smem {
   float misc[32];
   int32_t abort_flag;
   int32_t cur_task;   // queue index of the consumers' current task (read by the producer)
+  int32_t token;      // the step's input token
 };
 static_assert(sizeof(Smem) <= kSmemBytes, "shared memory layout");
 
@@ -674,6 +675,30 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[P], int lane) {
   return v[0];
 }
 
+// (value, index) argmax: the larger value wins, the smaller index on a tie
+__device__ __forceinline__ void amax_merge(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+// argmax over the 256 consumer threads' (v, i); the result is valid in
+// thread 0.  Uses sm.misc[0..16).
+__device__ __forceinline__ void block_amax(float& v, int& i, float* misc) {
+  const int tid = threadIdx.x, lane = tid & 31;
+#pragma unroll
+  for (int msk = 16; msk >= 1; msk >>= 1)
+    amax_merge(v, i, __shfl_xor_sync(0xFFFFFFFFu, v, msk), __shfl_xor_sync(0xFFFFFFFFu, i, msk));
+  if (lane == 0) {
+    misc[2 * (tid >> 5)] = v;
+    misc[2 * (tid >> 5) + 1] = __int_as_float(i);
+  }
+  consumer_sync();
+  if (tid == 0)
+    for (int w = 1; w < kConsumerWarps; ++w) amax_merge(v, i, misc[2 * w], __float_as_int(misc[2 * w + 1]));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int msk = 16; msk >= 1; msk >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, msk);
@@ -713,7 +738,7 @@ __device__ __forceinline__ bool load_activation(const StepParams& p, Smem& sm, c
   const int tid = threadIdx.x;
   const bool norm = t.type == T_QKV || t.type == T_GATEUP || t.type == T_LMHEAD;
   const bool from_embed = t.type == T_QKV && t.layer == 0;
-  const uint16_t* emb = m.embed + (int64_t)p.token * m.hidden;
+  const uint16_t* emb = m.embed + (int64_t)sm.token * m.hidden;
   const uint32_t* src = t.type == T_OPROJ ? m.o : t.type == T_DOWN ? m.a
                         : t.type == T_GATEUP ? m.xmid : m.xres;
   const int version = t.type == T_QKV ? t.layer : t.type == T_LMHEAD ? m.n_layers : t.layer + 1;
@@ -886,7 +911,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   uint32_t resid_w = 0;
   if (has_resid) {
     if (t.type == T_OPROJ && t.layer == 0)   // layer 0: the embedding row, a constant
-      resid_w = tag_word(__uint_as_float((uint32_t)__ldg(m.embed + (int64_t)p.token * m.hidden + row0 + tid) << 16),
+      resid_w = tag_word(__uint_as_float((uint32_t)__ldg(m.embed + (int64_t)sm.token * m.hidden + row0 + tid) << 16),
                          resid_tag);
     else
       resid_w = ld_relaxed(resid_src);
@@ -1017,6 +1042,8 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
       }
     }
   } else {
+    float best_v = -INFINITY;   // LM head: this thread's (max logit, row)
+    int best_i = 0x7FFFFFFF;
     for (int r = tid; r < nrows; r += kConsumerThreads) {
       const int R = row0 + r;
       if (R >= M.rows) continue;
@@ -1027,12 +1054,21 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
       }
       if (t.type == T_LMHEAD) {
         p.logits[R] = y;
+        amax_merge(best_v, best_i, y, R);
       } else {  // O / down: residual add on the owned row (r == tid)
         float resid = tag_value(resid_w);
         if ((resid_w & kTagMask) != resid_tag &&
             !poll_word(resid_src, resid_tag, &resid, m.status, abort_flag, p.timeout_ns, task_idx))
           continue;   // aborting: the step's status word already says why
         st_relaxed((t.type == T_OPROJ ? m.xmid : m.xres) + R, tag_word(resid + y, tag));
+      }
+    }
+    // greedy decoding on the device: this task's (max logit, row) pair
+    if (t.type == T_LMHEAD && p.amax) {
+      block_amax(best_v, best_i, sm.misc);
+      if (tid == 0) {
+        p.amax[2 * t.a2] = __float_as_uint(best_v);
+        p.amax[2 * t.a2 + 1] = (uint32_t)best_i;
       }
     }
   }
@@ -1513,6 +1549,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   if (tid >= kConsumerThreads) {
     if (tid == kConsumerThreads) producer_loop(p, sm, q, n);
   } else {
+    // the step's token: given, or (greedy decoding on the device) the
+    // argmax of the previous step's LM-task pairs
+    if (p.token_src) {
+      float v = -INFINITY;
+      int i = 0x7FFFFFFF;
+      for (int k = tid; k < p.n_lm; k += kConsumerThreads)
+        amax_merge(v, i, __uint_as_float(__ldcg(p.token_src + 2 * k)), (int)__ldcg(p.token_src + 2 * k + 1));
+      block_amax(v, i, sm.misc);
+      if (tid == 0) {
+        if (i < 0 || i >= p.m.vocab) {   // no finite logit: report, read a valid row
+          set_status(p.m.status, ST_CHECK, 0xFFFFFFFFu, SITE_TOKEN);
+          i = 0;
+        }
+        sm.token = i;
+        if (p.token_out && c == 0) *p.token_out = i;
+      }
+    } else if (tid == 0) {
+      sm.token = p.token;
+    }
+    consumer_sync();
     consumer_loop<FMT, LM_FMT>(p, sm, q, n);
   }
   if (hdr && tid == 0) {
@@ -1665,6 +1721,21 @@ __global__ void watchdog_probe_kernel(uint32_t* scratch, uint64_t timeout_ns) {
     poll_tagged<1>([&](int) { return (const uint32_t*)scratch; }, v, 1u, 1u, scratch + 16,
                    &abort_flag, timeout_ns, blockIdx.x);
   }
+}
+
+// argmax over n (value bits, index) pairs, one block of 256 threads
+__global__ void argmax_pairs_kernel(const uint32_t* pairs, int n, int32_t* out) {
+  __shared__ float misc[32];
+  float v = -INFINITY;
+  int i = 0x7FFFFFFF;
+  for (int k = threadIdx.x; k < n; k += kConsumerThreads)
+    amax_merge(v, i, __uint_as_float(pairs[2 * k]), (int)pairs[2 * k + 1]);
+  block_amax(v, i, misc);
+  if (threadIdx.x == 0) *out = i == 0x7FFFFFFF ? -1 : i;
+}
+
+void launch_argmax_pairs(const uint32_t* pairs, int n, int32_t* out, void* stream) {
+  argmax_pairs_kernel<<<1, kConsumerThreads, 0, (cudaStream_t)stream>>>(pairs, n, out);
 }
 
 void launch_watchdog_probe(uint32_t* scratch, uint64_t timeout_ns, void* stream) {

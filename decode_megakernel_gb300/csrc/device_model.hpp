@@ -73,7 +73,11 @@ struct StepParams {
   // int64 [num_ctas][1 + trace_stride][kTraceWords], see TraceWord below
   int64_t* trace;
   int32_t trace_stride;
-  int32_t pad1;
+  int32_t n_lm;                // LM-head tasks: argmax pairs per step
+  // greedy decoding on the device (all null for a plain step):
+  uint32_t* amax;              // [n_lm][2] this step's (max logit bits, row) per LM task
+  const uint32_t* token_src;   // the previous step's pairs: this step's token is their argmax
+  int32_t* token_out;          // CTA 0 records the token it derived there
 };
 
 // Trace record words.  Row 0 of a CTA: start / end %globaltimer and clock64,
@@ -94,7 +98,7 @@ enum DevStatus : uint32_t {
   ST_OK = 0, ST_TIMEOUT = 1, ST_CHECK = 2
 };
 enum WaitSite : uint32_t {
-  SITE_DATA = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5
+  SITE_DATA = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5, SITE_TOKEN = 6
 };
 
 // kernel geometry
@@ -131,6 +135,8 @@ void launch_pack_matrix(int kind, int fmt, const DevMat& dst, int layer, const v
                         const void* z1, const void* w2, const void* s2, const void* z2,
                         int n_heads, int n_kv_heads, int head_dim, void* stream);
 void launch_watchdog_probe(uint32_t* scratch, uint64_t timeout_ns, void* stream);
+// token = argmax over n argmax pairs (the last step of a device greedy loop)
+void launch_argmax_pairs(const uint32_t* pairs, int n, int32_t* out, void* stream);
 void launch_debug_dequant(int fmt, const void* w, const void* scales, const void* zeros,
                           int rows, int K, float* out, void* stream);
 

@@ -311,12 +311,18 @@ struct Builder {
     s.body_len.resize(C);
     for (int q = 0; q < C; ++q) s.body_len[q] = (int)s.queues[q].size();
 
-    // LM head (skipped by prefill)
-    for (int t : distribute(M_LM, T_LMHEAD, L - 1)) {
+    // LM head (skipped by prefill).  LM task k also writes the (value,
+    // index) of its rows' largest logit to pair k of the argmax buffer.
+    const std::vector<int> lm = distribute(M_LM, T_LMHEAD, L - 1);
+    s.buffers[B_AMAX] = {(int64_t)lm.size() * 2, BUF_OUTPUT};
+    for (size_t k = 0; k < lm.size(); ++k) {
+      const int t = lm[k];
       const MatGeom& m = g.mat[M_LM];
       const int64_t r0 = s.tasks[t].a[0] * m.Rt, r1 = std::min<int64_t>(s.tasks[t].a[1] * m.Rt, m.rows);
+      s.tasks[t].a[2] = (int64_t)k;
       acc(t, B_XRES, 0, H, false, L);
       acc(t, B_LOGITS, r0, r1, true, 0);
+      acc(t, B_AMAX, (int64_t)k * 2, (int64_t)k * 2 + 2, true, 0);
     }
     return std::move(s);
   }

@@ -156,8 +156,8 @@ amk_status plan_geometry(const amk_config& cfg, const BuildOptions& opt, ModelGe
 //   PART  attention partials [n_kv_heads][splits][part_stride]
 //   O     attention output [n_heads * head_dim];  A  SwiGLU output [ffn]
 // State: KVROW, the KV-cache rows at the step's position [n_layers][2][n_kv_heads * head_dim].
-// Output: LOGITS [vocab].
-enum BufId : int32_t { B_XRES = 0, B_XMID, B_QKV, B_PART, B_O, B_A, B_KVROW, B_LOGITS, B_NUM };
+// Output: LOGITS [vocab]; AMAX [n_lm_tasks][2], each LM task's (max logit, its index).
+enum BufId : int32_t { B_XRES = 0, B_XMID, B_QKV, B_PART, B_O, B_A, B_KVROW, B_LOGITS, B_AMAX, B_NUM };
 
 // Lower a model to the task DAG (tasks, counters, per-CTA queues, accesses).
 Schedule build_schedule(const ModelGeom& g);

@@ -203,6 +203,25 @@ amk_status amk_decode_step_host(amk_ctx* ctx, int32_t token, int32_t pos, float*
 amk_status amk_decode_step_static_scratch(amk_ctx* ctx, int32_t token, int32_t pos,
                                           float* logits_dev);
 
+/*
+ * Greedy decoding on the device: n_steps decode steps from position pos
+ * with no host round trip between them: the argmax of each step's
+ * logits is the next step's token.  Step 0 consumes first_token;
+ * each LM-head task also records the (max logit, row) of its rows, and
+ * step i + 1 takes as its token the argmax of step i's records (the larger
+ * logit wins, the smaller token id on a tie, as torch.argmax).  tokens_dev
+ * (device, int32 [n_steps], 4-byte aligned) receives the generated tokens:
+ * tokens_dev[i] = argmax of step i's logits.  logits_dev: NULL, or device
+ * fp32 [vocab] that holds the last step's logits on completion.  Checks as
+ * amk_decode_step for (first_token, pos); pos + n_steps <= max_seq.
+ * Asynchronous: n_steps + 1 launches on the context's stream (the last
+ * reduces the final step's records); the valid KV length becomes
+ * pos + n_steps.  Device failures surface at amk_sync; a step whose
+ * logits have no finite maximum reports AMK_ERR_DEVICE_CHECK.
+ */
+amk_status amk_generate(amk_ctx* ctx, int32_t first_token, int32_t pos, int32_t n_steps,
+                        int32_t* tokens_dev, float* logits_dev);
+
 /* Declare KV positions [0, n) valid (a cache filled by the caller). */
 amk_status amk_set_kv_length(amk_ctx* ctx, int32_t n);
 int32_t amk_kv_length(const amk_ctx* ctx);

@@ -156,6 +156,40 @@ def test_tiny_greedy_loop(amk, orc, dev):
     assert gpu_seq == orc_seq or near_tie > 0, (gpu_seq, orc_seq)
 
 
+@pytest.mark.parametrize("knobs,steps", [(dict(), 24), (dict(num_ctas=8), 12), (dict(), 1)])
+def test_device_greedy_matches_host_loop(amk, dev, knobs, steps):
+    """amk_generate (argmax fused into the LM head, the token never leaves
+    the GPU) produces exactly the tokens and final logits of a host loop of
+    amk_decode_step + torch.argmax (first index on ties, as the device)."""
+    cfg = wc.TINY
+    max_seq = 16 + steps
+    w = synth.model_weights(cfg, seed=5, device=dev)
+    sched = amk.make_schedule_config(**knobs)
+    prompt = synth.prompt_tokens(cfg, 16).tolist()
+    a = amk.Decoder(w, max_seq, sched=sched)
+    b = amk.Decoder(w, max_seq, sched=sched)
+    for d in (a, b):
+        d.prefill(prompt[:-1], 0)
+    pos = len(prompt) - 1
+    toks = torch.full((steps,), -7, dtype=torch.int32, device=dev)
+    la = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+    a.generate(prompt[-1], pos, steps, toks, la)
+    a.sync()
+    assert amk.amk_kv_length(a.ctx) == pos + steps
+    lb = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+    t, host = prompt[-1], []
+    for i in range(steps):
+        b.decode_step(t, pos + i, lb)
+        t = int(torch.argmax(lb).item())
+        host.append(t)
+    b.sync()
+    assert toks.cpu().tolist() == host
+    assert torch.equal(la, lb)
+    assert torch.equal(a.kv, b.kv)
+    a.close()
+    b.close()
+
+
 def test_prefill_equals_decode_steps_and_rollback(amk, dev):
     cfg = wc.TINY
     w = synth.model_weights(cfg, seed=4, device=dev)
