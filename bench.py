@@ -355,6 +355,20 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e_max_ms, e2e_units = reduce_over_ranks(e2e_s * 1e3, float(n_e2e))
     e2e_value = e2e_units / (e2e_max_ms / 1e3)
     assert np.isfinite(host_logits.numpy()).all()
+
+    # greedy decoding on the device (amk_generate: the argmax feeds the next
+    # step with no host round trip), device-timed on the decode stream
+    n_gen = min(K, D)
+    gen_tokens = torch.empty(n_gen, dtype=torch.int32, device=dev)
+    dec.generate(toks[0], P, min(4, n_gen), gen_tokens)
+    dec.sync()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    dec.generate(toks[0], P, n_gen, gen_tokens)
+    g1.record(stream)
+    dec.sync()
+    gen_ms = g0.elapsed_time(g1)
+    gen_max_ms, gen_units = reduce_over_ranks(gen_ms, float(n_gen))
     dec.close()
     del dec
     torch.cuda.empty_cache()
@@ -373,6 +387,9 @@ def run_ours(args, wl, rank, world, local_rank):
                      "launch_ms_p10_p50_p90": [float(np.percentile(per, q)) for q in (10, 50, 90)]},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 8,
                 "d2h_bytes_per_step": cfg.vocab * 4},
+        "device_greedy": {"value": gen_units / (gen_max_ms / 1e3), "unit": "tok/s", "steps": n_gen,
+                          "what": "amk_generate: argmax fused into the LM head, n_gen launches back "
+                                  "to back with no host round trip (+1 final reduction)"},
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
