@@ -205,6 +205,37 @@ amk_status plan(const amk_config* cfg, const amk_schedule_config* sched, ModelGe
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
+// The KV cache as a 2-D tensor for TMA: rows of head_dim bf16 (one row per
+// layer, K/V, KV head and position), boxes of 64 dims x the positions of
+// one KV stage, 128-byte swizzle (conflict-free ldmatrix reads).  The
+// driver's encoder is reached through the runtime's entry-point query.
+amk_status encode_kv_map(amk_ctx* ctx, const amk_config& c, void* kv, CUtensorMap* out) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                CUtensorMapFloatOOBfill);
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || !fn || q != cudaDriverEntryPointSuccess)
+    return fail(ctx, AMK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int pps = (kStageBytes / 2) / (c.head_dim * 2);
+  const cuuint64_t dims[2] = {(cuuint64_t)c.head_dim,
+                              (cuuint64_t)c.n_layers * 2 * c.n_kv_heads * c.max_seq};
+  const cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)pps};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = reinterpret_cast<EncodeFn>(fn)(
+      out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (KV cache) failed: %d", (int)r);
+    return fail(ctx, AMK_ERR_CUDA, buf);
+  }
+  return AMK_OK;
+}
+
 // present and aligned for the kernel's vector loads (bf16 rows are read 16
 // bytes, int8 rows 8 bytes, int4 rows 4 bytes, fp16 scales 2 bytes at a time)
 bool linear_ok(const amk_linear& l, int fmt) {
@@ -543,6 +574,10 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   dm.tasks = (const DevTask*)(ws + L.tasks);
   dm.queue_off = (const int32_t*)(ws + L.queue_off);
   dm.queue_body = (const int32_t*)(ws + L.queue_body);
+  {
+    amk_status kst = encode_kv_map(ctx, c, kv_cache_dev, &dm.kv_map);
+    if (kst != AMK_OK) return bail(kst);
+  }
   ctx->logits_stage = (float*)(ws + L.logits);
 
   // task table, queue order per CTA

@@ -72,6 +72,18 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// 2-D tiled TMA load of one box (coordinates: x = element, y = row) into
+// shared memory, completing on an mbarrier; the tensor map lives in the
+// kernel's parameter space.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -324,6 +336,7 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 struct TaskTiles {
   const uint8_t* k = nullptr;
   const uint8_t* v = nullptr;
+  int rk = 0, rv = 0;   // attention: KV-cache tensor rows of position 0 (K, V)
   int64_t stride = 0;   // weights: bytes between tiles
   uint32_t bytes = 0;   // weights: bytes per tile
   int nst = 0;          // number of tiles
@@ -338,8 +351,8 @@ __device__ __forceinline__ TaskTiles task_tiles(const StepParams& p, const DevTa
     attn_range(p.pos, m.splits, t.a1, &tt.t0, &tt.t1);
     tt.pps = attn_positions_per_stage(m.head_dim);
     tt.row = m.head_dim * 2;
-    tt.k = reinterpret_cast<const uint8_t*>(kv_row(m, t.layer, 0, t.a0, 0));
-    tt.v = reinterpret_cast<const uint8_t*>(kv_row(m, t.layer, 1, t.a0, 0));
+    tt.rk = ((t.layer * 2 + 0) * m.n_kv_heads + t.a0) * m.max_seq;
+    tt.rv = ((t.layer * 2 + 1) * m.n_kv_heads + t.a0) * m.max_seq;
     tt.nst = (tt.t1 - tt.t0 + tt.pps - 1) / tt.pps;
     tt.attn = true;
   } else if (t.type == T_COMBINE) {
@@ -439,11 +452,16 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
     }
     uint64_t* full = kv ? &sm.kfull[c.slot] : &sm.full[c.slot];
     if (kv) {
+      // K then V of positions [p0, p0 + pps): boxes of 64 dims x pps rows,
+      // 128-byte swizzled (rows past the split are loaded too and masked)
       const int p0 = c.tt.t0 + c.tile * c.tt.pps;
-      const uint32_t bytes = (uint32_t)(min(c.tt.pps, c.tt.t1 - p0) * c.tt.row);
-      mbar_arrive_expect_tx(full, 2 * bytes);
-      bulk_copy_g2s(sm.kv[c.slot], c.tt.k + (int64_t)p0 * c.tt.row, bytes, full, pol_kv);
-      bulk_copy_g2s(sm.kv[c.slot] + kStageBytes / 2, c.tt.v + (int64_t)p0 * c.tt.row, bytes, full, pol_kv);
+      const int nbox = m.head_dim / 64;
+      mbar_arrive_expect_tx(full, kStageBytes);
+      for (int b = 0; b < nbox; ++b) {
+        tma_load_2d(sm.kv[c.slot] + b * c.tt.pps * 128, &m.kv_map, 64 * b, c.tt.rk + p0, full, pol_kv);
+        tma_load_2d(sm.kv[c.slot] + kStageBytes / 2 + b * c.tt.pps * 128, &m.kv_map, 64 * b,
+                    c.tt.rv + p0, full, pol_kv);
+      }
     } else {
       mbar_arrive_expect_tx(full, c.tt.bytes);
       bulk_copy_g2s(sm.ring[c.slot], c.tt.k + (int64_t)c.tile * c.tt.stride, c.tt.bytes, full, pol_w);
@@ -1090,100 +1108,147 @@ __device__ __forceinline__ int gemv_dispatch(const StepParams& p, Smem& sm, cons
   }
 }
 
+// ldmatrix / mma.sync helpers (bf16 in, fp32 accumulate)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// d += a (16x16, row) * b (16x8, col)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (x0, x1) as bf16 pairs hi + lo with x ~= hi + lo to about 2^-16 relative
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // Split-K GQA attention of one KV head over one context split (positions
-// [t0, t1) of the cache, plus the step's own position for the last split).
-// The K,V history comes through the KV ring in chunks of up to kKvSlots
-// stages, all resident at once.  Each warp takes a contiguous run of a
-// chunk's positions and works alone until the final merge:
-//   scores: lanes own HD/32 dims; the partial dots of a group of R = 32/G
-//     positions x G heads go through one transposed warp reduction, which
-//     leaves one (position, head) score per lane;
-//   softmax: one maximum and one sum per head and chunk (log2(R)-level
-//     shuffles among the lanes holding that head), folded into the warp's
-//     running (m, l, acc);
-//   values: weight * V over the run, packed fp32 FMAs, weights broadcast
-//     from the warp's slice of shared memory.
-// The eight warp states are merged (LSE) through shared memory and stored
-// as the split's partial (acc, m, l).
+// [t0, t1) of the cache, plus the step's own position for the last split),
+// on the tensor cores.  The K,V history arrives through the KV ring in
+// 128-byte-swizzled boxes; a chunk of up to kKvSlots resident stages is
+// split into runs of 16 (hd 128) or 32 (hd 64) positions, one per warp.
+// Per 16 positions a warp computes
+//   S^T [16 positions x 8 heads] = K [16 x hd] . Q^T [hd x 8]    (hd/16 mma pairs)
+//   O^T [hd x 8]              += V^T [hd x 16] . P^T [16 x 8]    (hd/16 mma pairs)
+// with ldmatrix fragments of K and (transposed) V, G <= 8 real heads in the
+// 8 columns, and q and P split into bf16 hi + lo so that the products keep
+// fp32-level accuracy (K, V are bf16 already).  The softmax is one maximum
+// and one sum per head and chunk over the run, folded into the warp's
+// running (m, l, O); the eight warp states are merged (LSE) through shared
+// memory and stored as the split's partial (acc, m, l).
 template <int HD, int G>
 __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTask t, int kstage,
                                       uint32_t task_idx, int64_t* tr) {
-  constexpr int DPL = HD / 32;                         // dims per lane
   constexpr int PPS = (kStageBytes / 2) / (HD * 2);   // cached positions per KV stage
   constexpr int CP = kKvSlots * PPS;                  // positions per chunk at most
-  constexpr int R = 32 / G;                           // positions per score group
-  constexpr int CPW = CP / kConsumerWarps;            // positions of a warp's run at most
-  constexpr int NG = (CPW + R - 1) / R;               // score groups per warp
-  constexpr int PWW = NG * R * G;                     // weight floats per warp
-  // scratch (floats): per-warp weights and q staging at the front, reused
-  // at the end by the warp states [warp][G][HD + 2]; the step's own k, v at
-  // the back
-  constexpr int PW_OFF = 0, QS_OFF = kConsumerWarps * PWW, MG_OFF = 0;
+  constexpr int RUN = CP / kConsumerWarps;            // positions of a warp's run at most
+  constexpr int MT = RUN / 16;                        // 16-position tiles per run
+  constexpr int KS = HD / 16;                         // k-steps (QK) and dim tiles (PV)
+  static_assert(G <= 8 && RUN % 16 == 0 && HD % 64 == 0, "attention tile shapes");
+  // scratch (floats): q staging, the step's own k / v as bf16 rows, then
+  // at the end the warp states [warp][G][HD + 2]
   constexpr int WS = G * (HD + 2);
-  constexpr int KV_OFF = kScratchFloats - 2 * HD;
-  static_assert(QS_OFF + G * HD <= KV_OFF && MG_OFF + kConsumerWarps * WS <= KV_OFF,
+  constexpr int QS_OFF = 0, CUR_OFF = kScratchFloats - HD, MG_OFF = 0;
+  static_assert(QS_OFF + G * HD <= CUR_OFF && MG_OFF + kConsumerWarps * WS <= CUR_OFF,
                 "attention scratch");
   const DevModel& m = p.m;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq4 = lane >> 2, tq4 = lane & 3;   // mma fragment coordinates
   const int g = t.a0, j = t.a1;
   volatile int32_t* abort_flag = &sm.abort_flag;
-  float* pw = sm.scratch + PW_OFF + warp * PWW;
   float* qs = sm.scratch + QS_OFF;
   float* mg = sm.scratch + MG_OFF;
-  float* kvs = sm.scratch + KV_OFF;
+  uint16_t* cur = reinterpret_cast<uint16_t*>(sm.scratch + CUR_OFF);   // [2][HD] bf16: k, v
 
   const uint32_t tag = tag_of(p, t.layer + 1);
-  const uint32_t* gq = m.qkv + (int64_t)g * (G + 2) * HD;   // q heads, k, v of this KV head
+  const uint32_t* gqp = m.qkv + (int64_t)g * (G + 2) * HD;   // q heads, k, v of this KV head
   constexpr int QV = G * HD / 4, KVV = HD / 2;
   static_assert(QV + KVV <= kConsumerThreads, "one vector per thread");
   const bool last = j == m.splits - 1;
   bool failed = false;
-  // inputs: q of the group (and, last split, the step's k and v) by
-  // 16-byte vectors into shared memory
+  // inputs: q of the group (fp32) and, last split, the step's k and v (as
+  // the bf16 they are) by 16-byte vectors into shared memory
   if (tid < QV || (last && tid < QV + KVV)) {
-    const uint32_t* src = tid < QV ? gq + tid * 4 : gq + G * HD + (tid - QV) * 4;
-    float* dst = tid < QV ? qs + tid * 4 : kvs + (tid - QV) * 4;
+    const uint32_t* src = tid < QV ? gqp + tid * 4 : gqp + G * HD + (tid - QV) * 4;
     uint4 v[1];
     failed = !poll_tagged<1>([&](int) { return src; }, v, 1u, tag, m.status, abort_flag,
                              p.timeout_ns, task_idx);
-    dst[0] = tag_value(v[0].x);
-    dst[1] = tag_value(v[0].y);
-    dst[2] = tag_value(v[0].z);
-    dst[3] = tag_value(v[0].w);
+    if (tid < QV) {
+      float* dst = qs + tid * 4;
+      dst[0] = tag_value(v[0].x);
+      dst[1] = tag_value(v[0].y);
+      dst[2] = tag_value(v[0].z);
+      dst[3] = tag_value(v[0].w);
+    } else {
+      // k dims then v dims; the words carry bf16 values, whose bits are the
+      // upper half of the fp32 (the tag sits in the low nibble)
+      uint16_t* dst = cur + (tid - QV) * 4;
+      dst[0] = (uint16_t)(v[0].x >> 16);
+      dst[1] = (uint16_t)(v[0].y >> 16);
+      dst[2] = (uint16_t)(v[0].z >> 16);
+      dst[3] = (uint16_t)(v[0].w >> 16);
+    }
   }
   if (tr) tr[TR_C_WAITED] = (int64_t)global_timer();
   failed = consumer_sync_or(failed);
   if (tr) tr[TR_A_INPUTS] = (int64_t)global_timer();
-  // queries pre-scaled so that scores are in log2 units
+  // Q^T fragments (hi, lo) of every k-step, pre-scaled into log2 units;
+  // columns (heads) >= G are zero
   const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
-  float qr[G][DPL];
+  uint32_t qb[KS][2][2];   // [k-step][b0 / b1][hi / lo]
 #pragma unroll
-  for (int h = 0; h < G; ++h)
+  for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) qr[h][d] = qs[h * HD + lane * DPL + d] * qscale;
-  float mx[G], l[G], acc[G][DPL];
+    for (int half = 0; half < 2; ++half) {
+      const int d = ks * 16 + half * 8 + 2 * tq4;
+      float x0 = 0.f, x1 = 0.f;
+      if (gq4 < G) {
+        x0 = qs[gq4 * HD + d] * qscale;
+        x1 = qs[gq4 * HD + d + 1] * qscale;
+      }
+      split_bf16x2(x0, x1, qb[ks][half][0], qb[ks][half][1]);
+    }
+  // warp state: running max / sum of heads 2*tq4 and 2*tq4 + 1, O^T fragments
+  float mx0 = -INFINITY, mx1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[KS][4];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    mx[h] = -INFINITY;
-    l[h] = 0.f;
+  for (int k2 = 0; k2 < KS; ++k2)
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) acc[h][d] = 0.f;
-  }
+    for (int e = 0; e < 4; ++e) o[k2][e] = 0.f;
 
   const uint32_t kv0 = smem_addr(&sm.kv[0][0]);
+  const uint32_t cur0 = smem_addr(cur);
   const uint32_t kfull0 = smem_addr(&sm.kfull[0]);
   const uint32_t kempty0 = smem_addr(&sm.kempty[0]);
   int64_t starved = 0;
   int t0, t1;
   attn_range(p.pos, m.splits, j, &t0, &t1);
   const int ncached = t1 - t0;
+  const int ntotal = ncached + (last ? 1 : 0);
   const int nst = (ncached + PPS - 1) / PPS;
   uint32_t kslot = (uint32_t)kstage % kKvSlots, kphase = ((uint32_t)kstage / kKvSlots) & 1u;
 
-  // cached positions, in chunks of up to kKvSlots resident stages
-  for (int c0 = 0; c0 < ncached; c0 += CP) {
-    const int len = min(CP, ncached - c0);
-    const int s_begin = c0 / PPS, s_end = (c0 + len + PPS - 1) / PPS;
+  for (int c0 = 0; c0 < ntotal; c0 += CP) {
+    const int len = min(CP, ntotal - c0);
+    const int s_begin = c0 / PPS;
+    const int s_end = min(c0 + len, ncached) > c0 ? (min(c0 + len, ncached) + PPS - 1) / PPS : s_begin;
     const uint32_t slot0 = kslot;
     // every warp waits for all of the chunk's stages (runs may span them all)
     for (int s2 = s_begin; s2 < s_end; ++s2) {
@@ -1191,101 +1256,113 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
         failed = !wait_full(kfull0 + kslot * 8, kphase, p, abort_flag, task_idx, tr ? &starved : nullptr);
       if (++kslot == (uint32_t)kKvSlots) { kslot = 0; kphase ^= 1u; }
     }
-    // this warp's run of positions [c0 + w0, c0 + w0 + n); a position's row
-    // sits in the slot of its stage, counted from the chunk's first slot
+    // shared address of 16-byte chunk c (8 dims) of K (kv = 0) or V (kv = 1)
+    // of task position pi: a swizzled ring row, or the step's own k / v
+    auto addr_of = [&](int pi, int c, int kv) -> uint32_t {
+      if (pi >= ncached) return cur0 + (uint32_t)(kv * HD * 2 + c * 16);
+      uint32_t slot = slot0 + (uint32_t)(pi / PPS - s_begin);
+      if (slot >= (uint32_t)kKvSlots) slot -= kKvSlots;
+      const int r = pi % PPS;
+      return kv0 + slot * kStageBytes + (uint32_t)(kv * (kStageBytes / 2) + (c >> 3) * (PPS * 128) + r * 128 +
+                                                   (((c & 7) ^ (r & 7)) << 4));
+    };
+    // this warp's run [c0 + w0, c0 + w0 + n)
     const int per = (len + kConsumerWarps - 1) / kConsumerWarps;
     const int w0 = min(len, warp * per);
     const int n = min(len, w0 + per) - w0;
-    auto row_addr = [&](int pi) -> uint32_t {
-      uint32_t slot = slot0 + (uint32_t)(pi / PPS - s_begin);
-      if (slot >= (uint32_t)kKvSlots) slot -= kKvSlots;
-      return kv0 + slot * kStageBytes + (uint32_t)(((pi % PPS) * HD + lane * DPL) * 2);
-    };
     if (!failed && n > 0) {
-      // scores: lane holds (r, h) = (lane / G, lane % G) of each group
-      float sc[NG];
+      const int base = c0 + w0;
+      const int plast = base + n - 1;   // padding rows read this position (masked)
+      // scores S^T: rows (positions) gq4 and gq4 + 8 of each tile, columns
+      // (heads) 2*tq4 and 2*tq4 + 1
+      float sc[MT][4];
 #pragma unroll
-      for (int gi = 0; gi < NG; ++gi) {
-        sc[gi] = -INFINITY;
-        if (gi * R < n) {
-          float v[32];
+      for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const uint32_t ad = row_addr(c0 + w0 + min(gi * R + r, n - 1));
-            float kf[DPL];
-            if constexpr (DPL == 4) {
-              const uint2 w = lds64(ad);
-              kf[0] = bf16_lo(w.x); kf[1] = bf16_hi(w.x); kf[2] = bf16_lo(w.y); kf[3] = bf16_hi(w.y);
-            } else {
-              const uint32_t w = lds32(ad);
-              kf[0] = bf16_lo(w); kf[1] = bf16_hi(w);
-            }
+        for (int e = 0; e < 4; ++e) sc[mt][e] = 0.f;
+        if (mt * 16 < n) {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int pi = min(base + mt * 16 + rr + 8 * (mi & 1), plast);
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float d0 = 0.f;
-#pragma unroll
-              for (int d = 0; d < DPL; ++d) d0 = fmaf(qr[h][d], kf[d], d0);
-              v[r * G + h] = d0;
-            }
+          for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(addr_of(pi, 2 * ks + (mi >> 1), 0), a);
+            mma_bf16_16816(sc[mt], a, qb[ks][0][0], qb[ks][1][0]);
+            mma_bf16_16816(sc[mt], a, qb[ks][0][1], qb[ks][1][1]);
           }
-          const float s1 = transpose_reduce<32>(v, lane);
-          if (gi * R + lane / G < n) sc[gi] = s1;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (mt * 16 + gq4 + 8 * (e >> 1) >= n) sc[mt][e] = -INFINITY;
+      }
+      // softmax of the run for heads 2*tq4, 2*tq4 + 1: lanes of a head
+      // differ in gq4 (lane bits 2..4)
+      float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        cm0 = fmaxf(cm0, fmaxf(sc[mt][0], sc[mt][2]));
+        cm1 = fmaxf(cm1, fmaxf(sc[mt][1], sc[mt][3]));
+      }
+#pragma unroll
+      for (int msk = 4; msk < 32; msk <<= 1) {
+        cm0 = fmaxf(cm0, __shfl_xor_sync(0xFFFFFFFFu, cm0, msk));
+        cm1 = fmaxf(cm1, __shfl_xor_sync(0xFFFFFFFFu, cm1, msk));
+      }
+      const float mn0 = fmaxf(mx0, cm0), mn1 = fmaxf(mx1, cm1);
+      const float al0 = exp2f(mx0 - mn0), al1 = exp2f(mx1 - mn1);   // 0 on the first chunk
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        sc[mt][0] = exp2f(sc[mt][0] - mn0);
+        sc[mt][1] = exp2f(sc[mt][1] - mn1);
+        sc[mt][2] = exp2f(sc[mt][2] - mn0);
+        sc[mt][3] = exp2f(sc[mt][3] - mn1);
+        ls0 += sc[mt][0] + sc[mt][2];
+        ls1 += sc[mt][1] + sc[mt][3];
+      }
+#pragma unroll
+      for (int msk = 4; msk < 32; msk <<= 1) {
+        ls0 += __shfl_xor_sync(0xFFFFFFFFu, ls0, msk);
+        ls1 += __shfl_xor_sync(0xFFFFFFFFu, ls1, msk);
+      }
+      l0 = fmaf(l0, al0, ls0);
+      l1 = fmaf(l1, al1, ls1);
+      mx0 = mn0;
+      mx1 = mn1;
+#pragma unroll
+      for (int k2 = 0; k2 < KS; ++k2) {
+        o[k2][0] *= al0;
+        o[k2][1] *= al1;
+        o[k2][2] *= al0;
+        o[k2][3] *= al1;
+      }
+      // values: P^T fragments (positions 2*tq4 (+1), (+8) of head gq4)
+      // gathered from the lanes holding them, then O^T += V^T . P^T
+      const int sa = (2 * tq4) * 4 + (gq4 >> 1), sb = (2 * tq4 + 1) * 4 + (gq4 >> 1);
+      const bool odd = (gq4 & 1) != 0;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        if (mt * 16 >= n) continue;
+        const float a0 = __shfl_sync(0xFFFFFFFFu, sc[mt][0], sa), a1 = __shfl_sync(0xFFFFFFFFu, sc[mt][1], sa);
+        const float a2 = __shfl_sync(0xFFFFFFFFu, sc[mt][2], sa), a3 = __shfl_sync(0xFFFFFFFFu, sc[mt][3], sa);
+        const float b0 = __shfl_sync(0xFFFFFFFFu, sc[mt][0], sb), b1 = __shfl_sync(0xFFFFFFFFu, sc[mt][1], sb);
+        const float b2 = __shfl_sync(0xFFFFFFFFu, sc[mt][2], sb), b3 = __shfl_sync(0xFFFFFFFFu, sc[mt][3], sb);
+        uint32_t pb0h, pb0l, pb1h, pb1l;
+        split_bf16x2(odd ? a1 : a0, odd ? b1 : b0, pb0h, pb0l);   // positions 2*tq4, 2*tq4 + 1
+        split_bf16x2(odd ? a3 : a2, odd ? b3 : b2, pb1h, pb1l);   // positions 2*tq4 + 8, + 9
+        const int mi = lane >> 3, rr = lane & 7;
+        const int pi = min(base + mt * 16 + rr + 8 * (mi >> 1), plast);
+#pragma unroll
+        for (int k2 = 0; k2 < KS; ++k2) {
+          uint32_t a[4];
+          ldsm_x4_trans(addr_of(pi, 2 * k2 + (mi & 1), 1), a);
+          mma_bf16_16816(o[k2], a, pb0h, pb1h);
+          mma_bf16_16816(o[k2], a, pb0l, pb1l);
         }
       }
-      // softmax of the run, per head: lanes of one head differ in lane / G
-      float cm = sc[0];
-#pragma unroll
-      for (int gi = 1; gi < NG; ++gi) cm = fmaxf(cm, sc[gi]);
-#pragma unroll
-      for (int msk = G; msk < 32; msk <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, msk));
-      float mnew[G], alpha[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        mnew[h] = fmaxf(mx[h], __shfl_sync(0xFFFFFFFFu, cm, h));
-        alpha[h] = exp2f(mx[h] - mnew[h]);   // 0 on the first chunk
-      }
-      float mine = mnew[0];
-#pragma unroll
-      for (int h = 1; h < G; ++h) mine = (lane % G) == h ? mnew[h] : mine;
-      float ls = 0.f;
-#pragma unroll
-      for (int gi = 0; gi < NG; ++gi) {
-        const float e = exp2f(sc[gi] - mine);   // 0 for padding (-inf)
-        pw[(gi * R + lane / G) * G + lane % G] = e;
-        ls += e;
-      }
-#pragma unroll
-      for (int msk = G; msk < 32; msk <<= 1) ls += __shfl_xor_sync(0xFFFFFFFFu, ls, msk);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        l[h] = fmaf(l[h], alpha[h], __shfl_sync(0xFFFFFFFFu, ls, h));
-        mx[h] = mnew[h];
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) acc[h][d] *= alpha[h];
-      }
-      __syncwarp();
-      // values
-      for (int i = 0; i < n; ++i) {
-        const uint32_t ad = row_addr(c0 + w0 + i) + kStageBytes / 2;
-        float vf[DPL];
-        if constexpr (DPL == 4) {
-          const uint2 w = lds64(ad);
-          vf[0] = bf16_lo(w.x); vf[1] = bf16_hi(w.x); vf[2] = bf16_lo(w.y); vf[3] = bf16_hi(w.y);
-        } else {
-          const uint32_t w = lds32(ad);
-          vf[0] = bf16_lo(w); vf[1] = bf16_hi(w);
-        }
-        float wgt[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) wgt[h] = pw[i * G + h];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(wgt[h], vf[d], acc[h][d]);
-      }
-      __syncwarp();   // pw is rewritten by the next chunk
     }
     // release the chunk's stages
+    __syncwarp();
     if (lane == 0) {
       uint32_t sl = slot0;
       for (int s2 = s_begin; s2 < s_end; ++s2) {
@@ -1294,42 +1371,35 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
       }
     }
   }
-  // the step's own position (last split), written this step by the QKV
-  // tasks: one more online-softmax update on warp 0
-  if (!failed && last && warp == 0) {
-    float kf[DPL], vf[DPL];
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) {
-      kf[d] = kvs[lane * DPL + d];
-      vf[d] = kvs[HD + lane * DPL + d];
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float d0 = 0.f;
-#pragma unroll
-      for (int d = 0; d < DPL; ++d) d0 = fmaf(qr[h][d], kf[d], d0);
-      const float s1 = warp_sum(d0);
-      const float mnew = fmaxf(mx[h], s1);
-      const float alpha = exp2f(mx[h] - mnew), e = exp2f(s1 - mnew);
-      l[h] = fmaf(l[h], alpha, e);
-      mx[h] = mnew;
-#pragma unroll
-      for (int d = 0; d < DPL; ++d) acc[h][d] = fmaf(e, vf[d], acc[h][d] * alpha);
-    }
-  }
   if (tr) {
     tr[TR_C_STARVED] = starved;
     tr[TR_A_STAGES] = (int64_t)global_timer();
   }
-  // merge the eight warps' states (mg overlaps pw and qs: wait for all)
+  // merge the eight warps' states (mg overlaps the q staging: wait for all)
   consumer_sync();
+  {
+    const int h0 = 2 * tq4, h1 = 2 * tq4 + 1;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) mg[warp * WS + h * (HD + 2) + lane * DPL + d] = acc[h][d];
-    if (lane == 0) {
-      mg[warp * WS + h * (HD + 2) + HD] = mx[h];
-      mg[warp * WS + h * (HD + 2) + HD + 1] = l[h];
+    for (int k2 = 0; k2 < KS; ++k2) {
+      const int d = k2 * 16 + gq4;
+      if (h0 < G) {
+        mg[warp * WS + h0 * (HD + 2) + d] = o[k2][0];
+        mg[warp * WS + h0 * (HD + 2) + d + 8] = o[k2][2];
+      }
+      if (h1 < G) {
+        mg[warp * WS + h1 * (HD + 2) + d] = o[k2][1];
+        mg[warp * WS + h1 * (HD + 2) + d + 8] = o[k2][3];
+      }
+    }
+    if (gq4 == 0) {
+      if (h0 < G) {
+        mg[warp * WS + h0 * (HD + 2) + HD] = mx0;
+        mg[warp * WS + h0 * (HD + 2) + HD + 1] = l0;
+      }
+      if (h1 < G) {
+        mg[warp * WS + h1 * (HD + 2) + HD] = mx1;
+        mg[warp * WS + h1 * (HD + 2) + HD + 1] = l1;
+      }
     }
   }
   if (consumer_sync_or(failed)) return -1;
@@ -1488,6 +1558,7 @@ __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
   int stage = 0, kstage = 0;   // weight-ring and KV-ring stages consumed so far
   volatile int32_t* abort_flag = &sm.abort_flag;
   for (int i = 0; i < n; ++i) {
+    if (*abort_flag) return;
     const DevTask t = q[i];
     int64_t* tr = p.trace ? trace_row(p, i) : nullptr;
     if (tid == 0) *(volatile int32_t*)&sm.cur_task = i;
@@ -1515,7 +1586,7 @@ __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
 
 template <int FMT, int LM_FMT>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ StepParams p) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -1527,7 +1598,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       mbar_init(&sm.kfull[s], 1);
       mbar_init(&sm.kempty[s], kConsumerWarps);
     }
-    sm.abort_flag = 0;
+    // the swizzled KV boxes need 1 KB alignment: refuse to run without it
+    sm.abort_flag = (smem_addr(&sm.kv[0][0]) & 1023u) ? 1 : 0;
+    if (sm.abort_flag) set_status(p.m.status, ST_CHECK, 0xFFFFFFFFu, SITE_SMEM);
     sm.cur_task = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -1,6 +1,8 @@
 // Structures shared by the host library and the persistent decode kernel.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (a plain 128-byte descriptor)
+
 #include <cstdint>
 
 #include "schedule.hpp"
@@ -58,6 +60,10 @@ struct DevModel {
   const DevTask* tasks;        // queue of CTA c: tasks[queue_off[c] .. queue_off[c + 1])
   const int32_t* queue_off;    // [num_ctas + 1]
   const int32_t* queue_body;   // [num_ctas]: tasks run when the LM head is skipped
+  // TMA descriptor of the KV cache seen as rows of head_dim bf16
+  // ([n_layers * 2 * n_kv_heads * max_seq][head_dim]), boxes of 64 dims x
+  // (positions per KV stage) with the 128-byte swizzle
+  CUtensorMap kv_map;
 };
 
 struct StepParams {
@@ -98,7 +104,7 @@ enum DevStatus : uint32_t {
   ST_OK = 0, ST_TIMEOUT = 1, ST_CHECK = 2
 };
 enum WaitSite : uint32_t {
-  SITE_DATA = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5, SITE_TOKEN = 6
+  SITE_DATA = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5, SITE_TOKEN = 6, SITE_SMEM = 7
 };
 
 // kernel geometry
