@@ -916,6 +916,34 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   const int wg = warp & ((1 << wpg_shift) - 1);
   volatile int32_t* abort_flag = &sm.abort_flag;
 
+  // constants the task reads after its input arrives go to L1 first (no
+  // registers held): norm weights, and for the epilogue of this thread's
+  // row (pair) its RoPE table entry or its int8 row scale(s)
+  {
+    const bool norm = t.type == T_QKV || t.type == T_GATEUP || t.type == T_LMHEAD;
+    if (norm) {
+      const uint16_t* nw = t.type == T_QKV ? m.attn_norm + (int64_t)t.layer * m.hidden
+                           : t.type == T_GATEUP ? m.ffn_norm + (int64_t)t.layer * m.hidden
+                                                : m.final_norm;
+#pragma unroll
+      for (int kt = 0; kt < NKT; ++kt) {
+        const int k = kt * M.Kt + chunk * 8;
+        if (k < M.K) asm volatile("prefetch.global.L1 [%0];" ::"l"(nw + k));
+      }
+    }
+    const int rows = (t.a1 - t.a0) * M.Rt, r0 = t.a0 * M.Rt;
+    const int my = (t.type == T_QKV || t.type == T_GATEUP) ? r0 + 2 * tid : r0 + tid;
+    if (my < min(r0 + rows, M.rows)) {
+      if (t.type == T_QKV) {
+        const int hd = m.head_dim, gw = (m.group + 2) * hd;
+        const int within = (my % gw) % hd, slot_h = (my % gw) / hd;
+        if (slot_h <= m.group)
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(m.rope + (int64_t)p.pos * (hd >> 1) + (within >> 1)));
+      }
+      if (FMT == AMK_FORMAT_INT8)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(M.scales + (kind == M_LM ? 0 : (int64_t)t.layer * M.rows_padded) + my));
+    }
+  }
   float2 h[NKT][4];
   bool failed = !load_activation<NKT>(p, sm, t, M, chunk, h, task_idx, tr);
   // residual row of O / down (one row per thread): loaded now so that the
