@@ -53,7 +53,7 @@ class amk_schedule_config(C.Structure):
     _fields_ = [("num_ctas", C.c_int32), ("attn_splits", C.c_int32),
                 ("max_rows_per_task", C.c_int32), ("watchdog_ms", C.c_int32),
                 ("ring_slots", C.c_int32), ("l2_prefetch_tiles", C.c_int32),
-                ("reserved", C.c_int32 * 2)]
+                ("prefill_chunk", C.c_int32), ("reserved", C.c_int32 * 1)]
 
 
 class AmkError(RuntimeError):
@@ -73,6 +73,7 @@ def _load():
     schp = C.POINTER(amk_schedule_config)
     sig = {
         "amk_workspace_bytes": (C.c_size_t, [cfgp, schp]),
+        "amk_prefill_chunk": (C.c_int32, [P]),
         "amk_check_config": (C.c_int, [cfgp]),
         "amk_kv_cache_bytes": (C.c_size_t, [cfgp]),
         "amk_load_weights": (C.c_int, [cfgp, C.POINTER(amk_weights), P, C.c_size_t, P, P, schp,
@@ -176,6 +177,10 @@ def amk_kv_length(ctx) -> int:
     return int(lib.amk_kv_length(ctx))
 
 
+def amk_prefill_chunk(ctx) -> int:
+    return int(lib.amk_prefill_chunk(ctx))
+
+
 def amk_sync(ctx) -> int:
     return int(lib.amk_sync(ctx))
 
@@ -237,9 +242,9 @@ def make_config(model, max_seq: int) -> amk_config:
 
 
 def make_schedule_config(num_ctas=0, attn_splits=0, max_rows_per_task=0, watchdog_ms=0,
-                         ring_slots=0, l2_prefetch_tiles=0):
+                         ring_slots=0, l2_prefetch_tiles=0, prefill_chunk=0):
     return amk_schedule_config(num_ctas, attn_splits, max_rows_per_task, watchdog_ms,
-                               ring_slots, l2_prefetch_tiles, (C.c_int32 * 2)())
+                               ring_slots, l2_prefetch_tiles, prefill_chunk, (C.c_int32 * 1)())
 
 
 def _ptr(t):
@@ -308,6 +313,11 @@ class Decoder:
             assert logits.dtype == torch.float32 and logits.is_cuda
             lp = logits.data_ptr()
         check(amk_generate(self.ctx, first_token, pos, n_steps, tokens.data_ptr(), lp), self.ctx)
+
+    @property
+    def prefill_chunk(self) -> int:
+        """Tokens per tensor-core prefill chunk (0: prefill by decode steps)."""
+        return amk_prefill_chunk(self.ctx)
 
     def set_kv_length(self, n: int):
         check(amk_set_kv_length(self.ctx, n), self.ctx)

@@ -1,6 +1,6 @@
 """Build libamk.so in-tree with nvcc for sm_103a.
 
-Three translation units compiled in parallel, then linked with the static
+The translation units compiled in parallel, then linked with the static
 CUDA runtime.  No cmake, no torch extension machinery: the library is a
 plain C-ABI shared object loaded through ctypes.
 """
@@ -18,8 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libamk.so")
 
-SOURCES = ["decode_kernel.cu", "amk_api.cpp", "schedule.cpp", "static_scratch.cu"]
-HEADERS = ["device_model.hpp", "schedule.hpp"]
+SOURCES = ["decode_kernel.cu", "amk_api.cpp", "schedule.cpp", "static_scratch.cu", "prefill.cu"]
+HEADERS = ["device_model.hpp", "schedule.hpp", "prefill.hpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE]

@@ -11,6 +11,7 @@
 
 #include "../../include/amk.h"
 #include "device_model.hpp"
+#include "prefill.hpp"
 #include "schedule.hpp"
 
 using namespace amk;
@@ -42,6 +43,17 @@ struct amk_ctx {
   int32_t max_queue = 0;  // longest per-CTA task queue (trace sizing)
   int32_t n_lm = 0;       // LM-head tasks: argmax pairs per step
   uint32_t* amax[2] = {nullptr, nullptr};  // per-step argmax pairs, double buffered
+  // tensor-core prefill (bf16 weights): chunk buffers and tensor maps
+  struct Prefill {
+    int32_t chunk = 0;        // tokens per chunk; 0: prefill by decode steps
+    float* x = nullptr;       // residual rows [chunk][hidden]
+    uint16_t* h1[kPfParts] = {};  // normed rows, bf16 parts [chunk][hidden]
+    uint16_t* h2[kPfParts] = {};  // attention output [chunk][qd] or SwiGLU [chunk][ffn], bf16 parts
+    float* q = nullptr;       // rotated queries [chunk][qd]
+    int32_t* tokens = nullptr;  // [max_seq]
+    CUtensorMap a_h1[kPfParts], a_o[kPfParts], a_a[kPfParts];   // activation operands (parts)
+    std::vector<CUtensorMap> w[M_NUM];     // weight operands per layer (QKV, O, gate/up, down)
+  } pf;
   std::string err;
 };
 
@@ -73,7 +85,9 @@ struct Layout {
   size_t scales[M_NUM] = {};
   size_t mats = 0, embed = 0, attn_norm = 0, ffn_norm = 0, final_norm = 0, rope = 0;
   size_t xres = 0, xmid = 0, qkv = 0, o = 0, a = 0, part = 0, status = 0, logits = 0, amax = 0;
-  size_t tasks = 0, queue_off = 0, queue_body = 0, total = 0;
+  size_t tasks = 0, queue_off = 0, queue_body = 0;
+  size_t pf_x = 0, pf_h1[kPfParts] = {}, pf_h2[kPfParts] = {}, pf_q = 0, pf_tok = 0;
+  size_t total = 0;
 };
 
 }  // namespace
@@ -148,6 +162,14 @@ Layout make_layout(const ModelGeom& g, const Schedule& s) {
   L.tasks = take(n_queued * sizeof(DevTask));
   L.queue_off = take((s.queues.size() + 1) * 4);
   L.queue_body = take(s.queues.size() * 4);
+  if (g.prefill_chunk > 0) {
+    const size_t P = (size_t)g.prefill_chunk, qd = (size_t)c.n_heads * c.head_dim;
+    L.pf_x = take(P * c.hidden * 4);
+    for (int i = 0; i < kPfParts; ++i) L.pf_h1[i] = take(P * c.hidden * 2);
+    for (int i = 0; i < kPfParts; ++i) L.pf_h2[i] = take(P * std::max<size_t>(qd, c.ffn) * 2);
+    L.pf_q = take(P * qd * 4);
+    L.pf_tok = take((size_t)c.max_seq * 4);
+  }
   L.total = off;
   return L;
 }
@@ -159,7 +181,8 @@ amk_status resolve_ctas(const amk_schedule_config* sched, BuildOptions* opt, std
     opt->attn_splits = sched->attn_splits;
     opt->max_rows_per_task = sched->max_rows_per_task;
     if (sched->num_ctas < 0 || sched->attn_splits < 0 || sched->max_rows_per_task < 0 ||
-        sched->watchdog_ms < 0 || sched->ring_slots < 0 || sched->l2_prefetch_tiles < -1) {
+        sched->watchdog_ms < 0 || sched->ring_slots < 0 || sched->l2_prefetch_tiles < -1 ||
+        sched->prefill_chunk < -1) {
       *why = "negative schedule knob";
       return AMK_ERR_INVALID_ARG;
     }
@@ -195,6 +218,17 @@ amk_status plan(const amk_config* cfg, const amk_schedule_config* sched, ModelGe
   if (st != AMK_OK) return st;
   st = plan_geometry(*cfg, opt, g, why);
   if (st != AMK_OK) return st;
+  // tensor-core prefill: bf16 weights only; chunk rounded up to whole
+  // 128-token GEMM tiles and to no more than the cache holds
+  {
+    const int32_t want = sched ? sched->prefill_chunk : 0;
+    g->prefill_chunk = 0;
+    if (cfg->weight_format == AMK_FORMAT_BF16 && want >= 0) {
+      const int64_t chunk = want > 0 ? want : kPfDefaultChunk;
+      const int64_t cap = ((int64_t)cfg->max_seq + kPfBM - 1) / kPfBM * kPfBM;
+      g->prefill_chunk = (int32_t)std::min<int64_t>((chunk + kPfBM - 1) / kPfBM * kPfBM, cap);
+    }
+  }
   if (!decode_kernel_for(cfg->weight_format, lm_format(*cfg))) {
     *why = "no kernel for this weight / LM-head format pair";
     return AMK_ERR_UNSUPPORTED;
@@ -209,29 +243,83 @@ bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0;
 // layer, K/V, KV head and position), boxes of 64 dims x the positions of
 // one KV stage, 128-byte swizzle (conflict-free ldmatrix reads).  The
 // driver's encoder is reached through the runtime's entry-point query.
-amk_status encode_kv_map(amk_ctx* ctx, const amk_config& c, void* kv, CUtensorMap* out) {
+// A bf16 tensor map with 128-byte swizzle (rank <= 4; strides of dims
+// 1.. in bytes).  The driver's encoder is reached through the runtime's
+// entry-point query.
+amk_status encode_bf16_map(amk_ctx* ctx, const char* what, CUtensorMap* out, void* base, int rank,
+                           const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                                 CUtensorMapFloatOOBfill);
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q{};
-  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-  if (e != cudaSuccess || !fn || q != cudaDriverEntryPointSuccess)
-    return fail(ctx, AMK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  static void* fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q{};
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || !fn || q != cudaDriverEntryPointSuccess) {
+      fn = nullptr;
+      return fail(ctx, AMK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    }
+  }
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = reinterpret_cast<EncodeFn>(fn)(
+      out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, base, dims, strides, box, estr,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[128];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (%s) failed: %d", what, (int)r);
+    return fail(ctx, AMK_ERR_CUDA, buf);
+  }
+  return AMK_OK;
+}
+
+// The KV cache as a 2-D tensor for TMA: rows of head_dim bf16 (one row per
+// layer, K/V, KV head and position), boxes of 64 dims x the positions of
+// one KV stage, 128-byte swizzle (conflict-free ldmatrix reads).
+amk_status encode_kv_map(amk_ctx* ctx, const amk_config& c, void* kv, CUtensorMap* out) {
   const int pps = (kStageBytes / 2) / (c.head_dim * 2);
   const cuuint64_t dims[2] = {(cuuint64_t)c.head_dim,
                               (cuuint64_t)c.n_layers * 2 * c.n_kv_heads * c.max_seq};
   const cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)pps};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = reinterpret_cast<EncodeFn>(fn)(
-      out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    char buf[96];
-    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled (KV cache) failed: %d", (int)r);
-    return fail(ctx, AMK_ERR_CUDA, buf);
+  return encode_bf16_map(ctx, "KV cache", out, kv, 2, dims, strides, box);
+}
+
+// Tensor maps of the tensor-core prefill.  Activation operands (each of
+// the kPfParts bf16 parts): [chunk][K] row major, boxes of 64 k x 128 tokens.  Weight operands: the
+// decode kernel's packed tiles of one layer's matrix as a 4-D tensor
+// {Kt, Rt, nkt, row blocks}, boxes {64, Rt, 1, 128 / Rt}, so that one box
+// is a 128-row x 64-k slice in plain row order.
+amk_status encode_prefill_maps(amk_ctx* ctx, const DevMat* mats) {
+  const amk_config& c = ctx->cfg;
+  auto& pf = ctx->pf;
+  const cuuint64_t P = (cuuint64_t)pf.chunk, qd = (cuuint64_t)c.n_heads * c.head_dim;
+  auto act = [&](CUtensorMap* m, void* base, cuuint64_t K) {
+    const cuuint64_t dims[2] = {K, P};
+    const cuuint64_t strides[1] = {K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kPfBK, (cuuint32_t)kPfBM};
+    return encode_bf16_map(ctx, "prefill activations", m, base, 2, dims, strides, box);
+  };
+  for (int i = 0; i < kPfParts; ++i) {
+    amk_status st = act(&pf.a_h1[i], pf.h1[i], (cuuint64_t)c.hidden);
+    if (st == AMK_OK) st = act(&pf.a_o[i], pf.h2[i], qd);
+    if (st == AMK_OK) st = act(&pf.a_a[i], pf.h2[i], (cuuint64_t)c.ffn);
+    if (st != AMK_OK) return st;
+  }
+  for (int k : {M_QKV, M_O, M_GU, M_DOWN}) {
+    const DevMat& m = mats[k];
+    pf.w[k].resize(c.n_layers);
+    const cuuint64_t dims[4] = {(cuuint64_t)m.Kt, (cuuint64_t)m.Rt, (cuuint64_t)m.nkt,
+                                (cuuint64_t)(m.rows_padded / m.Rt)};
+    const cuuint64_t strides[3] = {(cuuint64_t)m.Kt * 2, (cuuint64_t)m.stage_bytes,
+                                   (cuuint64_t)m.nkt * m.stage_bytes};
+    const cuuint32_t box[4] = {(cuuint32_t)kPfBK, (cuuint32_t)m.Rt, 1, (cuuint32_t)(kPfBN / m.Rt)};
+    for (int l = 0; l < c.n_layers; ++l) {
+      void* base = const_cast<uint8_t*>(m.base) + (int64_t)l * m.layer_bytes;
+      amk_status st = encode_bf16_map(ctx, "prefill weights", &pf.w[k][l], base, 4, dims, strides, box);
+      if (st != AMK_OK) return st;
+    }
   }
   return AMK_OK;
 }
@@ -655,17 +743,111 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
                        weights->lm_head.zeros, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                        c.n_heads, c.n_kv_heads, c.head_dim, st_);
   AMK_CUDA(ctx, cudaGetLastError());
+  if (g.prefill_chunk > 0) {
+    auto& pf = ctx->pf;
+    pf.chunk = g.prefill_chunk;
+    pf.x = (float*)(ws + L.pf_x);
+    for (int i = 0; i < kPfParts; ++i) {
+      pf.h1[i] = (uint16_t*)(ws + L.pf_h1[i]);
+      pf.h2[i] = (uint16_t*)(ws + L.pf_h2[i]);
+    }
+    pf.q = (float*)(ws + L.pf_q);
+    pf.tokens = (int32_t*)(ws + L.pf_tok);
+    amk_status pst = encode_prefill_maps(ctx, mats);
+    if (pst != AMK_OK) return bail(pst);
+  }
   AMK_CUDA(ctx, cudaStreamSynchronize(st_));
   ctx->kv_len = 0;
   *out = ctx;
   return AMK_OK;
 }
 
+namespace {
+
+// The tensor-core prefill of tokens (already on the device) at positions
+// start_pos .. start_pos + n - 1, chunk by chunk, layer by layer.
+amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
+  const amk_config& c = ctx->cfg;
+  const ModelGeom& geo = ctx->geom;
+  auto& pf = ctx->pf;
+  const DevModel& dm = ctx->dm;
+  cudaStream_t s = ctx->stream;
+  const int qd = c.n_heads * c.head_dim;
+  const size_t H = (size_t)c.hidden;
+  PrefillGemm g{};
+  g.hd = c.head_dim;
+  g.group = geo.group;
+  g.n_kv = c.n_kv_heads;
+  g.max_seq = c.max_seq;
+  g.x = pf.x;
+  g.ldx = c.hidden;
+  g.q = pf.q;
+  g.ldq = qd;
+  g.kv = dm.kv;
+  g.rope = dm.rope;
+  for (int i = 0; i < kPfParts; ++i) g.out[i] = pf.h2[i];
+  g.ldo = c.ffn;
+  g.status = dm.status;
+  g.timeout_ns = ctx->timeout_ns;
+  PrefillAttn at{};
+  at.q = pf.q;
+  at.ldq = qd;
+  at.kv = dm.kv;
+  at.n_kv = c.n_kv_heads;
+  at.max_seq = c.max_seq;
+  at.group = geo.group;
+  at.hd = c.head_dim;
+  for (int i = 0; i < kPfParts; ++i) at.o[i] = pf.h2[i];
+  at.ldo = qd;
+  auto gemm = [&](int epi, int kind, int layer, const CUtensorMap* a) {
+    const MatGeom& m = geo.mat[kind];
+    g.N = m.rows;
+    g.nk = m.Kp / kPfBK;
+    g.Kt = m.Kt;
+    g.Rt = m.Rt;
+    g.layer = layer;
+    return launch_prefill_gemm(epi, a, &pf.w[kind][layer], g, s);
+  };
+  for (int32_t c0 = 0; c0 < n; c0 += pf.chunk) {
+    const int T = std::min<int32_t>(pf.chunk, n - c0);
+    g.T = at.T = T;
+    g.s0 = at.s0 = start_pos + c0;
+    AMK_CUDA(ctx, launch_prefill_embed(pf.tokens + c0, T, dm.embed, c.hidden, pf.x, s));
+    for (int l = 0; l < c.n_layers; ++l) {
+      AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.attn_norm + l * H, c.rms_eps, pf.h1, s));
+      AMK_CUDA(ctx, gemm(PE_QKV, M_QKV, l, pf.a_h1));
+      at.layer = l;
+      AMK_CUDA(ctx, launch_prefill_attn(at, s));
+      if (l == c.n_layers - 1) break;   // the rest of the last layer feeds no K,V
+      AMK_CUDA(ctx, gemm(PE_RESID, M_O, l, pf.a_o));
+      AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.ffn_norm + l * H, c.rms_eps, pf.h1, s));
+      AMK_CUDA(ctx, gemm(PE_SWIGLU, M_GU, l, pf.a_h1));
+      AMK_CUDA(ctx, gemm(PE_RESID, M_DOWN, l, pf.a_a));
+    }
+  }
+  return AMK_OK;
+}
+
+}  // namespace
+
 amk_status amk_prefill(amk_ctx* ctx, const int32_t* host_tokens, int32_t n, int32_t start_pos) {
   if (!ctx) return fail(nullptr, AMK_ERR_INVALID_ARG, "context is NULL");
   if (n < 0 || (n > 0 && !host_tokens)) return fail(ctx, AMK_ERR_INVALID_ARG, "bad token array");
   if (start_pos < 0 || (int64_t)start_pos + n > ctx->cfg.max_seq)
     return fail(ctx, AMK_ERR_INVALID_ARG, "prefill runs past max_seq");
+  if (ctx->pf.chunk > 0 && n > 0) {
+    amk_status st = step_checks(ctx, host_tokens[0], start_pos);
+    if (st != AMK_OK) return st;
+    for (int32_t i = 0; i < n; ++i)
+      if (host_tokens[i] < 0 || host_tokens[i] >= ctx->cfg.vocab)
+        return fail(ctx, AMK_ERR_INVALID_ARG, "token out of range");
+    AMK_CUDA(ctx, cudaMemcpyAsync(ctx->pf.tokens, host_tokens, (size_t)n * 4, cudaMemcpyHostToDevice,
+                                  ctx->stream));
+    st = prefill_tensor_cores(ctx, n, start_pos);
+    if (st != AMK_OK) return st;
+    ctx->kv_len = start_pos + n;
+    return AMK_OK;
+  }
   for (int32_t i = 0; i < n; ++i) {
     amk_status st = step_checks(ctx, host_tokens[i], start_pos + i);
     if (st != AMK_OK) return st;
@@ -729,6 +911,8 @@ amk_status amk_set_kv_length(amk_ctx* ctx, int32_t n) {
   ctx->kv_len = n;
   return AMK_OK;
 }
+
+int32_t amk_prefill_chunk(const amk_ctx* ctx) { return ctx ? ctx->pf.chunk : -1; }
 
 int32_t amk_kv_length(const amk_ctx* ctx) { return ctx ? ctx->kv_len : -1; }
 

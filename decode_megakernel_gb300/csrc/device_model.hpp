@@ -104,7 +104,10 @@ enum DevStatus : uint32_t {
   ST_OK = 0, ST_TIMEOUT = 1, ST_CHECK = 2
 };
 enum WaitSite : uint32_t {
-  SITE_DATA = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5, SITE_TOKEN = 6, SITE_SMEM = 7
+  SITE_DATA = 1, SITE_FULL = 2, SITE_EMPTY = 3, SITE_DRAIN = 4, SITE_PROBE = 5, SITE_TOKEN = 6, SITE_SMEM = 7,
+  // tensor-core prefill GEMM: TMA producer (stage free), MMA issuer (stage
+  // loaded), epilogue (accumulator complete)
+  SITE_PF_TMA = 8, SITE_PF_MMA = 9, SITE_PF_EPI = 10
 };
 
 // kernel geometry

@@ -1,0 +1,667 @@
+// Tensor-core prefill kernels (see prefill.hpp for the algorithm).
+//
+// GEMM: one 128-token x 128-row output tile per CTA.  Warp 0 (one thread)
+// streams k blocks of the activation parts and the weight tile through a
+// kPfStages-deep ring with TMA; warp 1 (one thread) issues tcgen05.mma
+// (kind::f16, bf16 x bf16 -> fp32, M 128, N 128, K 16) into one of two
+// 128-column TMEM accumulators, a fresh one every kPfSegKB k blocks, and
+// releases each stage with tcgen05.commit; warps 2..5 read each finished
+// segment back (tcgen05.ld, one token row per thread), add it into fp32
+// registers, hand the buffer back, and at the end run the fused epilogue.  Every wait is bounded by the context's watchdog
+// limit; a timeout records ST_TIMEOUT in the status words.
+//
+// Attention: flash-attention over the KV cache with mma.sync (bf16 in,
+// fp32 accumulate), one CTA per (16 query tokens, KV head), one warp per
+// query head of the group; q and P split into bf16 hi + lo as in the decode
+// kernel's attention (softmax weights and pre-scaled scores need no more:
+// the attention's K,V are bf16 already).
+#include "device_model.hpp"
+#include "prefill.hpp"
+
+#include <cuda_bf16.h>
+
+namespace amk {
+
+namespace {
+
+constexpr uint32_t kPfATile = kPfBM * kPfBK * 2;   // 16 KB: 128 tokens x 64 k, bf16
+constexpr uint32_t kPfBTile = kPfBN * kPfBK * 2;   // 16 KB: 128 rows x 64 k, bf16
+
+struct __align__(1024) GemmSmem {
+  uint8_t a[kPfStages][kPfParts][kPfATile];
+  uint8_t w[kPfStages][kPfBTile];
+  uint64_t full[kPfStages], empty[kPfStages];
+  uint64_t acc_full[2], acc_empty[2];   // TMEM accumulator buffers: segment done / drained
+  uint32_t tmem;
+  uint32_t failed;
+};
+
+__device__ __forceinline__ uint32_t s_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// bounded wait for a phase of an mbarrier: false after limit_ns
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (bar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  while (!bar_try_wait(bar, parity))
+    if (now_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+__device__ void pf_timeout(uint32_t* status, uint32_t site) {
+  if (atomicCAS(&status[0], 0u, (uint32_t)ST_TIMEOUT) == 0u) {
+    status[1] = blockIdx.x;
+    status[2] = blockIdx.y;
+    status[3] = site;
+    __threadfence();
+  }
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* m, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(m), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* m, int x, int y, int z, int w,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];"
+      ::"r"(dst), "l"(m), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 bytes (64 bf16 of k), 8-row swizzle
+// atoms 1024 bytes apart.  The k-th 16-element slice starts k * 32 bytes in.
+__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address / 16
+  d |= (uint64_t)1 << 16;                              // leading offset (unused when swizzled)
+  d |= (uint64_t)(1024 >> 4) << 32;                    // stride offset: next 8-row atom
+  d |= (uint64_t)1 << 46;                              // descriptor version
+  d |= (uint64_t)2 << 61;                              // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M x N.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPfBN >> 3) << 17) |
+                            ((uint32_t)(kPfBM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+
+// x = p[0] + p[1] + p[2] to 2^-27 relative: each part is the bf16 rounding
+// of what the previous parts left (the remainders are exact in fp32)
+__device__ __forceinline__ void split3_bf16(float x, uint16_t (&p)[kPfParts]) {
+#pragma unroll
+  for (int i = 0; i < kPfParts; ++i) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    p[i] = __bfloat16_as_ushort(h);
+    x -= __bfloat162float(h);
+  }
+}
+
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Epilogue of 16 consecutive packed rows [n, n + 16) of token t (t < T).
+template <int EPI>
+__device__ __forceinline__ void gemm_epilogue(const PrefillGemm& g, int t, int n, const uint32_t (&v)[16]) {
+  if constexpr (EPI == PE_RESID) {
+    float* xr = g.x + (int64_t)t * g.ldx + n;
+    if (n + 16 <= g.N) {
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) {
+        float4 a = *reinterpret_cast<float4*>(xr + j);
+        a.x += __uint_as_float(v[j]);
+        a.y += __uint_as_float(v[j + 1]);
+        a.z += __uint_as_float(v[j + 2]);
+        a.w += __uint_as_float(v[j + 3]);
+        *reinterpret_cast<float4*>(xr + j) = a;
+      }
+    } else {
+      for (int j = 0; j < 16 && n + j < g.N; ++j) xr[j] += __uint_as_float(v[j]);
+    }
+  } else if constexpr (EPI == PE_SWIGLU) {
+    // packed rows interleave gate (even) and up (odd) of unit n / 2 + i
+    const int j0 = n >> 1;
+    uint16_t part[kPfParts][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint16_t p[kPfParts];
+      split3_bf16(silu(__uint_as_float(v[2 * i])) * __uint_as_float(v[2 * i + 1]), p);
+#pragma unroll
+      for (int k = 0; k < kPfParts; ++k) part[k][i] = p[k];
+    }
+#pragma unroll
+    for (int k = 0; k < kPfParts; ++k) {
+      uint16_t* d = g.out[k] + (int64_t)t * g.ldo + j0;
+      if (n + 16 <= g.N)
+        *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(part[k]);
+      else
+        for (int i = 0; i < 8 && n + 2 * i + 1 < g.N; ++i) d[i] = part[k][i];
+    }
+  } else {
+    // packed QKV rows per KV head grp: G query heads, k, v (hd rows each);
+    // in a q or k head, rows 2i, 2i + 1 hold dims i, i + hd/2 (a rotate-half
+    // RoPE pair).  A 16-row chunk never straddles a head (hd % 16 == 0).
+    const int hd = g.hd, half = hd >> 1, G = g.group, gw = (G + 2) * hd;
+    const int grp = n / gw, slot = (n % gw) / hd, within = (n % gw) % hd;
+    const int pos = g.s0 + t;
+    if (n >= g.N) return;
+    if (slot <= G) {
+      const float2* cs = g.rope + (int64_t)pos * half;
+      float* qrow = g.q + (int64_t)t * g.ldq + (int64_t)(grp * G + slot) * hd;
+      uint16_t* krow = g.kv + ((((int64_t)g.layer * 2 + 0) * g.n_kv + grp) * g.max_seq + pos) * hd;
+#pragma unroll
+      for (int pr = 0; pr < 8; ++pr) {
+        const int i = (within >> 1) + pr;
+        const float y0 = __uint_as_float(v[2 * pr]), y1 = __uint_as_float(v[2 * pr + 1]);
+        const float2 c = cs[i];
+        const float a = y0 * c.x - y1 * c.y;
+        const float b = y1 * c.x + y0 * c.y;
+        if (slot < G) {
+          qrow[i] = a;
+          qrow[half + i] = b;
+        } else {
+          krow[i] = bf16_bits(a);
+          krow[half + i] = bf16_bits(b);
+        }
+      }
+    } else {
+      uint16_t* vrow = g.kv + ((((int64_t)g.layer * 2 + 1) * g.n_kv + grp) * g.max_seq + pos) * hd + within;
+      uint16_t o[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j] = bf16_bits(__uint_as_float(v[j]));
+      *reinterpret_cast<uint4*>(vrow) = *reinterpret_cast<const uint4*>(o);
+      *reinterpret_cast<uint4*>(vrow + 8) = *reinterpret_cast<const uint4*>(o + 8);
+    }
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kPfGemmThreads, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
+                        const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_w,
+                        const __grid_constant__ PrefillGemm g) {
+  extern __shared__ uint8_t pf_smem_raw[];
+  GemmSmem& sm = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.x * kPfBM, n0 = blockIdx.y * kPfBN;
+  if (tid == 0) {
+    for (int s = 0; s < kPfStages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&sm.full[s])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&sm.empty[s])));
+    }
+    for (int b = 0; b < 2; ++b) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&sm.acc_full[b])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(s_addr(&sm.acc_empty[b])));
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    sm.failed = 0;
+  }
+  if (warp == 1) {   // the MMA warp owns the accumulators' TMEM columns
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s_addr(&sm.tmem)),
+                 "r"(2 * kPfBN));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = sm.tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {   // TMA producer
+      for (int kb = 0; kb < g.nk; ++kb) {
+        const int s = kb % kPfStages;
+        const uint32_t ph = (uint32_t)(kb / kPfStages) & 1u;
+        if (!bar_wait(s_addr(&sm.empty[s]), ph ^ 1u, g.timeout_ns)) {
+          pf_timeout(g.status, SITE_PF_TMA);
+          sm.failed = 1;
+          break;
+        }
+        const uint32_t fb = s_addr(&sm.full[s]);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                     "r"(kPfParts * kPfATile + kPfBTile)
+                     : "memory");
+        const int k = kb * kPfBK;
+        tma_2d(s_addr(sm.a[s][0]), &map_a0, k, m0, fb);
+        tma_2d(s_addr(sm.a[s][1]), &map_a1, k, m0, fb);
+        tma_2d(s_addr(sm.a[s][2]), &map_a2, k, m0, fb);
+        tma_4d(s_addr(sm.w[s]), &map_w, k % g.Kt, 0, k / g.Kt, n0 / g.Rt, fb);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {   // MMA issuer: the parts of A against the same W slice
+      for (int kb = 0; kb < g.nk; ++kb) {
+        const int seg = kb / kPfSegKB, b = seg & 1;
+        const uint32_t dt = tmem + (uint32_t)(b * kPfBN);
+        const bool first = kb % kPfSegKB == 0;
+        if (first) {   // this buffer's previous segment must have been drained
+          if (!bar_wait(s_addr(&sm.acc_empty[b]), ((uint32_t)(seg >> 1) & 1u) ^ 1u, g.timeout_ns)) {
+            pf_timeout(g.status, SITE_PF_MMA);
+            sm.failed = 1;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;");
+        }
+        const int s = kb % kPfStages;
+        const uint32_t ph = (uint32_t)(kb / kPfStages) & 1u;
+        if (!bar_wait(s_addr(&sm.full[s]), ph, g.timeout_ns)) {
+          pf_timeout(g.status, SITE_PF_MMA);
+          sm.failed = 1;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint32_t bw = s_addr(sm.w[s]);
+#pragma unroll
+        for (int k = 0; k < kPfBK / 16; ++k) {
+          const uint64_t bd = kmajor_sw128_desc(bw + k * 32);
+#pragma unroll
+          for (int part = 0; part < kPfParts; ++part)
+            umma_bf16(dt, kmajor_sw128_desc(s_addr(sm.a[s][part]) + k * 32), bd,
+                      (!first || k != 0 || part != 0) ? 1u : 0u);
+        }
+        umma_commit(s_addr(&sm.empty[s]));
+        // the segment is complete once every MMA issued into it has finished
+        if (kb % kPfSegKB == kPfSegKB - 1 || kb == g.nk - 1) umma_commit(s_addr(&sm.acc_full[b]));
+      }
+    }
+  } else {
+    const int quarter = warp & 3;   // TMEM lanes this warp may read: 32 * quarter ..
+    const int t = m0 + quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    float acc[kPfBN];
+#pragma unroll
+    for (int i = 0; i < kPfBN; ++i) acc[i] = 0.f;
+    const int nseg = (g.nk + kPfSegKB - 1) / kPfSegKB;
+    bool ok = true;
+    for (int seg = 0; seg < nseg && ok; ++seg) {
+      const int b = seg & 1;
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(s_addr(&sm.acc_full[b]), (uint32_t)(seg >> 1) & 1u, g.timeout_ns));
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;");
+#pragma unroll
+      for (int c = 0; c < kPfBN; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + (uint32_t)(b * kPfBN + c), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[c + j] += __uint_as_float(v[j]);
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s_addr(&sm.acc_empty[b])) : "memory");
+    }
+    if (!ok) {
+      if (lane == 0) pf_timeout(g.status, SITE_PF_EPI);
+    } else if (!sm.failed && t < g.T) {
+#pragma unroll
+      for (int c = 0; c < kPfBN; c += 16) {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(acc[c + j]);
+        if (n0 + c < g.N) gemm_epilogue<EPI>(g, t, n0 + c, v);
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kPfBN));
+  }
+}
+
+// ------------------------------------------------------------ elementwise
+
+__global__ void prefill_embed_kernel(const int32_t* tokens, int T, const uint16_t* embed, int hidden, float* x) {
+  const int t = blockIdx.x;
+  if (t >= T) return;
+  const uint16_t* e = embed + (int64_t)tokens[t] * hidden;
+  float* xr = x + (int64_t)t * hidden;
+  for (int k = threadIdx.x; k < hidden; k += blockDim.x) xr[k] = __uint_as_float((uint32_t)e[k] << 16);
+}
+
+// one CTA (256 threads) per token row
+struct Parts {
+  uint16_t* p[kPfParts];
+};
+
+__global__ void __launch_bounds__(256) prefill_norm_kernel(const float* x, int T, int hidden, const uint16_t* w,
+                                                           float eps, const Parts out) {
+  __shared__ float part[8];
+  const int t = blockIdx.x;
+  if (t >= T) return;
+  const float* xr = x + (int64_t)t * hidden;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < hidden; k += blockDim.x) ss = fmaf(xr[k], xr[k], ss);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += part[i];
+  const float r = rsqrtf(tot / (float)hidden + eps);
+  for (int k = threadIdx.x; k < hidden; k += blockDim.x) {
+    uint16_t p[kPfParts];
+    split3_bf16(xr[k] * r * __uint_as_float((uint32_t)w[k] << 16), p);
+#pragma unroll
+    for (int i = 0; i < kPfParts; ++i) out.p[i][(int64_t)t * hidden + k] = p[i];
+  }
+}
+
+// -------------------------------------------------------------- attention
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// d += a (16x16, row) * b (16x8, col)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+template <int HD>
+struct AttnShape {
+  static constexpr int RP = HD + 8;   // bf16 row pitch: rows 16 bytes apart in the banks
+  static constexpr int KV_ELEMS = 2 * kPfKB * RP;   // one K or V buffer pair (double buffered)
+  static int bytes(int group) { return (2 * KV_ELEMS + group * 2 * kPfQT * RP) * 2; }
+};
+
+// Shared memory (bf16 elements): K [2][64][RP], V [2][64][RP], then per
+// warp (query head) q hi [16][RP] and q lo [16][RP].
+template <int HD>
+__global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) {
+  using S = AttnShape<HD>;
+  constexpr int RP = S::RP, KS = HD / 16, DN = HD / 8;
+  extern __shared__ __align__(16) uint16_t at_smem[];
+  uint16_t* ks = at_smem;
+  uint16_t* vs = at_smem + S::KV_ELEMS;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int g = blockIdx.y, G = a.group;
+  const int tb = blockIdx.x * kPfQT;
+  const int head = g * G + warp;
+  uint16_t* qh = at_smem + 2 * S::KV_ELEMS + warp * 2 * kPfQT * RP;
+  uint16_t* ql = qh + kPfQT * RP;
+
+  // this block's queries, pre-scaled into log2 units, as bf16 hi + lo
+  const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
+  for (int i = lane; i < kPfQT * HD / 4; i += 32) {
+    const int r = i / (HD / 4), d = (i % (HD / 4)) * 4;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tb + r < a.T) x = *reinterpret_cast<const float4*>(a.q + (int64_t)(tb + r) * a.ldq + (int64_t)head * HD + d);
+    uint32_t h0, l0, h1, l1;
+    split_bf16x2(x.x * qscale, x.y * qscale, h0, l0);
+    split_bf16x2(x.z * qscale, x.w * qscale, h1, l1);
+    *reinterpret_cast<uint2*>(qh + r * RP + d) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(ql + r * RP + d) = make_uint2(l0, l1);
+  }
+
+  // positions [0, kv_end) are needed by the block's last valid token
+  const int t_last = min(a.T, tb + kPfQT) - 1;
+  const int kv_end = a.s0 + t_last + 1;
+  const int nblk = (kv_end + kPfKB - 1) / kPfKB;
+  const uint16_t* kbase = a.kv + (((int64_t)a.layer * 2 + 0) * a.n_kv + g) * a.max_seq * HD;
+  const uint16_t* vbase = a.kv + (((int64_t)a.layer * 2 + 1) * a.n_kv + g) * a.max_seq * HD;
+  auto load_block = [&](int blk, int buf) {
+    constexpr int CH = HD / 8;   // 16-byte chunks per row
+    for (int i = tid; i < 2 * kPfKB * CH; i += nthr) {
+      const int which = i / (kPfKB * CH), r = (i / CH) % kPfKB, c = i % CH;
+      const int p = blk * kPfKB + r;
+      uint16_t* dst = (which ? vs : ks) + buf * kPfKB * RP + r * RP + c * 8;
+      if (p < kv_end)
+        cp_async16(s_addr(dst), (which ? vbase : kbase) + (int64_t)p * HD + c * 8);
+      else   // past the filled cache: zeros (masked scores must meet finite values)
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+  float o[DN][4];
+#pragma unroll
+  for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  const int lim0 = a.s0 + tb + gq, lim1 = lim0 + 8;   // last visible position of rows gq, gq + 8
+
+  load_block(0, 0);
+  for (int blk = 0; blk < nblk; ++blk) {
+    const int buf = blk & 1;
+    if (blk + 1 < nblk) {
+      load_block(blk + 1, buf ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    const uint32_t kb_s = s_addr(ks + buf * kPfKB * RP), vb_s = s_addr(vs + buf * kPfKB * RP);
+
+    // S = Q K^T: 16 tokens x 64 positions, 8 tiles of 8 positions
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      uint32_t qa_h[4], qa_l[4];
+      const uint32_t qoff = (uint32_t)(((lane & 15) * RP + k * 16 + (lane >> 4) * 8) * 2);
+      ldsm_x4(s_addr(qh) + qoff, qa_h);
+      ldsm_x4(s_addr(ql) + qoff, qa_l);
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        const int mi = lane >> 3;
+        const int key = (2 * np + (mi >> 1)) * 8 + (lane & 7);
+        uint32_t kf[4];
+        ldsm_x4(kb_s + (uint32_t)((key * RP + k * 16 + (mi & 1) * 8) * 2), kf);
+        mma16816(s[2 * np], qa_h, kf[0], kf[1]);
+        mma16816(s[2 * np], qa_l, kf[0], kf[1]);
+        mma16816(s[2 * np + 1], qa_h, kf[2], kf[3]);
+        mma16816(s[2 * np + 1], qa_l, kf[2], kf[3]);
+      }
+    }
+    // causal mask, online softmax (rows gq and gq + 8 of the warp's tile)
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int p = blk * kPfKB + nt * 8 + 2 * tq + e;
+        if (p > lim0) s[nt][e] = -INFINITY;
+        if (p > lim1) s[nt][2 + e] = -INFINITY;
+        mx[0] = fmaxf(mx[0], s[nt][e]);
+        mx[1] = fmaxf(mx[1], s[nt][2 + e]);
+      }
+    float alpha[2], mu[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 2));
+      const float mn = fmaxf(mrow[r], mx[r]);
+      mu[r] = mn == -INFINITY ? 0.f : mn;
+      alpha[r] = exp2f(mrow[r] - mu[r]);
+      mrow[r] = mn;
+      lrow[r] *= alpha[r];
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s[nt][e] = exp2f(s[nt][e] - mu[e >> 1]);
+        lrow[e >> 1] += s[nt][e];
+      }
+#pragma unroll
+    for (int dn = 0; dn < DN; ++dn) {
+      o[dn][0] *= alpha[0];
+      o[dn][1] *= alpha[0];
+      o[dn][2] *= alpha[1];
+      o[dn][3] *= alpha[1];
+    }
+    // O += P V: 4 k-steps of 16 positions, P as bf16 hi + lo A fragments
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t pa_h[4], pa_l[4];
+      split_bf16x2(s[2 * kk][0], s[2 * kk][1], pa_h[0], pa_l[0]);
+      split_bf16x2(s[2 * kk][2], s[2 * kk][3], pa_h[1], pa_l[1]);
+      split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], pa_h[2], pa_l[2]);
+      split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], pa_h[3], pa_l[3]);
+#pragma unroll
+      for (int dp = 0; dp < DN / 2; ++dp) {
+        const int mi = lane >> 3;
+        const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
+        uint32_t vf[4];
+        ldsm_x4_trans(vb_s + (uint32_t)((key * RP + (2 * dp + (mi >> 1)) * 8) * 2), vf);
+        mma16816(o[2 * dp], pa_h, vf[0], vf[1]);
+        mma16816(o[2 * dp], pa_l, vf[0], vf[1]);
+        mma16816(o[2 * dp + 1], pa_h, vf[2], vf[3]);
+        mma16816(o[2 * dp + 1], pa_l, vf[2], vf[3]);
+      }
+    }
+    __syncthreads();   // the buffer is reloaded two blocks on
+  }
+  // normalise and store rows gq, gq + 8 of the tile
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    lrow[r] += __shfl_xor_sync(0xFFFFFFFFu, lrow[r], 1);
+    lrow[r] += __shfl_xor_sync(0xFFFFFFFFu, lrow[r], 2);
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int t = tb + gq + 8 * r;
+    if (t >= a.T) continue;
+    const float inv = 1.0f / lrow[r];
+    const int64_t row = (int64_t)t * a.ldo + (int64_t)head * HD;
+#pragma unroll
+    for (int dn = 0; dn < DN; ++dn) {
+      uint16_t p0[kPfParts], p1[kPfParts];
+      split3_bf16(o[dn][2 * r] * inv, p0);
+      split3_bf16(o[dn][2 * r + 1] * inv, p1);
+      const int d = dn * 8 + 2 * tq;
+#pragma unroll
+      for (int i = 0; i < kPfParts; ++i)
+        *reinterpret_cast<uint32_t*>(a.o[i] + row + d) = (uint32_t)p0[i] | ((uint32_t)p1[i] << 16);
+    }
+  }
+}
+
+}  // namespace
+
+int prefill_gemm_smem_bytes() { return (int)sizeof(GemmSmem) + 1024; }
+
+int prefill_attn_smem_bytes(int head_dim, int group) {
+  return head_dim == 64 ? AttnShape<64>::bytes(group) : AttnShape<128>::bytes(group);
+}
+
+cudaError_t launch_prefill_embed(const int32_t* tokens, int T, const uint16_t* embed, int hidden, float* x,
+                                 cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  prefill_embed_kernel<<<T, 256, 0, s>>>(tokens, T, embed, hidden, x);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_norm(const float* x, int T, int hidden, const uint16_t* w, float eps,
+                                uint16_t* const* out, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  Parts p;
+  for (int i = 0; i < kPfParts; ++i) p.p[i] = out[i];
+  prefill_norm_kernel<<<T, 256, 0, s>>>(x, T, hidden, w, eps, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap* w, const PrefillGemm& g,
+                                cudaStream_t s) {
+  if (g.T <= 0) return cudaSuccess;
+  const int smem = prefill_gemm_smem_bytes();
+  const dim3 grid((g.T + kPfBM - 1) / kPfBM, (g.N + kPfBN - 1) / kPfBN);
+  const void* fn = epi == PE_QKV      ? (const void*)prefill_gemm_kernel<PE_QKV>
+                   : epi == PE_RESID  ? (const void*)prefill_gemm_kernel<PE_RESID>
+                                      : (const void*)prefill_gemm_kernel<PE_SWIGLU>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (epi == PE_QKV)
+    prefill_gemm_kernel<PE_QKV><<<grid, kPfGemmThreads, smem, s>>>(a[0], a[1], a[2], *w, g);
+  else if (epi == PE_RESID)
+    prefill_gemm_kernel<PE_RESID><<<grid, kPfGemmThreads, smem, s>>>(a[0], a[1], a[2], *w, g);
+  else
+    prefill_gemm_kernel<PE_SWIGLU><<<grid, kPfGemmThreads, smem, s>>>(a[0], a[1], a[2], *w, g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s) {
+  if (a.T <= 0) return cudaSuccess;
+  const int smem = prefill_attn_smem_bytes(a.hd, a.group);
+  const dim3 grid((a.T + kPfQT - 1) / kPfQT, a.n_kv);
+  const void* fn = a.hd == 64 ? (const void*)prefill_attn_kernel<64> : (const void*)prefill_attn_kernel<128>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (a.hd == 64)
+    prefill_attn_kernel<64><<<grid, 32 * a.group, smem, s>>>(a);
+  else
+    prefill_attn_kernel<128><<<grid, 32 * a.group, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace amk

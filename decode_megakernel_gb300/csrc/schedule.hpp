@@ -136,6 +136,7 @@ struct ModelGeom {
   MatGeom mat[M_NUM];
   int32_t num_ctas = 0, splits = 0, group = 0, rows_max = 0;
   int32_t part_stride = 0;   // words of one attention partial: group * (head_dim + 2), rounded up to 4
+  int32_t prefill_chunk = 0; // tokens per tensor-core prefill chunk (0: prefill by decode steps)
 };
 
 struct BuildOptions {

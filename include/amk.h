@@ -109,7 +109,11 @@ typedef struct {
     int32_t l2_prefetch_tiles;  /* weight tiles a CTA may prefetch into L2 beyond its full
                                    ring while its consumers run attention, the split merge
                                    or the O projection (-1: off; 0: default) */
-    int32_t reserved[2];
+    int32_t prefill_chunk;      /* tokens per chunk of the tensor-core prefill (bf16 weights):
+                                   0: default 1024 (at most max_seq rounded up to 128);
+                                   -1: prefill through the decode kernel, one launch per
+                                   token (always so for int8 / int4 weights) */
+    int32_t reserved[1];
 } amk_schedule_config;
 
 typedef struct amk_ctx amk_ctx;
@@ -150,9 +154,17 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights,
                             void* stream, const amk_schedule_config* sched, amk_ctx** out);
 
 /*
- * n decode steps of host_tokens at positions start_pos.. with the LM head
- * skipped: fills the KV cache.  start_pos must be <= the valid KV length and
- * start_pos + n <= max_seq.  Asynchronous (one launch per token).
+ * Fill the KV cache with the K,V rows of host_tokens at positions
+ * start_pos .. start_pos + n - 1 (start_pos <= the valid KV length,
+ * start_pos + n <= max_seq, every token in [0, vocab)); no logits.
+ * With bf16 weights (and prefill_chunk >= 0) the tokens go through the
+ * tensor-core prefill in chunks of prefill_chunk tokens: per layer an
+ * RMSNorm, a QKV GEMM with RoPE and the KV append fused, causal GQA
+ * attention over the cache, and the O / gate-up / down GEMMs with the
+ * residual adds and SwiGLU fused (tcgen05 MMAs with fp32 accumulation, the
+ * activations split into bf16 hi + lo halves).  Otherwise each token is one
+ * decode step with the LM head skipped.  Asynchronous; host_tokens may be
+ * reused once the call returns.
  */
 amk_status amk_prefill(amk_ctx* ctx, const int32_t* host_tokens, int32_t n, int32_t start_pos);
 
@@ -221,6 +233,11 @@ amk_status amk_decode_step_static_scratch(amk_ctx* ctx, int32_t token, int32_t p
  */
 amk_status amk_generate(amk_ctx* ctx, int32_t first_token, int32_t pos, int32_t n_steps,
                         int32_t* tokens_dev, float* logits_dev);
+
+/* Tokens per chunk of the context's tensor-core prefill; 0 when
+ * amk_prefill runs decode steps (int8 / int4 weights, or prefill_chunk
+ * -1); -1 for a NULL context. */
+int32_t amk_prefill_chunk(const amk_ctx* ctx);
 
 /* Declare KV positions [0, n) valid (a cache filled by the caller). */
 amk_status amk_set_kv_length(amk_ctx* ctx, int32_t n);

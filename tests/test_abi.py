@@ -81,6 +81,29 @@ def test_sizes(amk):
     assert amk.amk_workspace_bytes(bad, sc) == 0
 
 
+def test_prefill_chunk_sizes_the_workspace(amk):
+    """bf16 weights get the tensor-core prefill's chunk buffers (x fp32,
+    normed rows and attention / SwiGLU rows as three bf16 parts, rotated q
+    fp32, the token ids); prefill_chunk = -1 and int8 / int4 weights do not."""
+    c = amk.make_config(wc.LLAMA_8B_BF16, 2176)
+    base = amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152, prefill_chunk=-1))
+    dflt = amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152))
+    m = wc.LLAMA_8B_BF16
+    qd = m.n_heads * m.head_dim
+    per_tok = m.hidden * 4 + 3 * m.hidden * 2 + 3 * max(qd, m.ffn) * 2 + qd * 4
+    expect = 1024 * per_tok + 2176 * 4
+    assert expect <= dflt - base <= expect + 10 * 256
+    # a chunk is whole 128-token tiles, and no more than the cache holds
+    c1 = amk.make_config(wc.LLAMA_8B_BF16, 200)
+    small = amk.amk_workspace_bytes(c1, amk.make_schedule_config(num_ctas=152, prefill_chunk=-1))
+    big = amk.amk_workspace_bytes(c1, amk.make_schedule_config(num_ctas=152, prefill_chunk=5000))
+    assert 256 * per_tok <= big - small <= 256 * per_tok + 200 * 4 + 10 * 256
+    c8 = amk.make_config(wc.LLAMA_8B_INT8, 2176)
+    assert (amk.amk_workspace_bytes(c8, amk.make_schedule_config(num_ctas=152)) ==
+            amk.amk_workspace_bytes(c8, amk.make_schedule_config(num_ctas=152, prefill_chunk=-1)))
+    assert amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152, prefill_chunk=-2)) == 0
+
+
 def test_host_argument_checks_need_no_gpu(amk):
     c = cfg_of(amk)
     st, ctx = amk.amk_load_weights(c, amk.amk_weights(), 0, 0, 0, 0)

@@ -191,10 +191,13 @@ def test_device_greedy_matches_host_loop(amk, dev, knobs, steps):
 
 
 def test_prefill_equals_decode_steps_and_rollback(amk, dev):
+    """The decode-kernel prefill (prefill_chunk = -1) is the decode step
+    with the LM head skipped: bit-identical K,V."""
     cfg = wc.TINY
     w = synth.model_weights(cfg, seed=4, device=dev)
     toks = synth.prompt_tokens(cfg, 12).tolist()
-    a = amk.Decoder(w, 16)
+    a = amk.Decoder(w, 16, sched=amk.make_schedule_config(prefill_chunk=-1))
+    assert a.prefill_chunk == 0
     a.prefill(toks, 0)
     a.sync()
     b = amk.Decoder(w, 16)
@@ -215,6 +218,79 @@ def test_prefill_equals_decode_steps_and_rollback(amk, dev):
         b.decode_step(cfg.vocab, 6, logits)
     a.close()
     b.close()
+
+
+def kv_layers(a, b):
+    """Per-layer view of two K,V caches [L, 2, n_kv, P, hd]: layer 0 strict
+    (kv_close), every layer's bit-identical share, and the mean |difference|
+    relative to the mean |value| over all layers."""
+    first = kv_close(a[:1], b[:1])
+    same = [float((bits(a[l]) == bits(b[l])).mean()) for l in range(a.shape[0])]
+    x = a.float().cpu().numpy().astype(np.float64)
+    y = b.float().cpu().numpy().astype(np.float64)
+    rel_mean = float(np.abs(x - y).sum() / np.abs(y).sum())
+    return first, same, rel_mean
+
+
+@pytest.mark.parametrize("variant,chunk,prompt,split", [
+    ("tiny", 0, 12, None),       # one chunk, one partial 128-token tile
+    ("tiny", 128, 300, 100),     # two calls (history from the first), three chunks, ragged tail
+    ("hd128", 128, 200, None),   # head_dim 128, group 4
+    ("mha", 0, 40, 17),          # group 1
+    ("tied", 256, 260, None),
+])
+def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, prompt, split):
+    """The tensor-core prefill (tcgen05 GEMMs, mma.sync attention) against
+    the oracle's batched causal prefill, then decode steps on top of it.
+
+    Layer 0's K,V come straight from the embedding, RMSNorm, the QKV GEMM
+    and RoPE: within two bf16 steps of the oracle and >= 99.9% bit-identical.
+    Deeper layers inherit every bf16 rounding of the layers below: a V entry
+    that rounds the other way moves the next layer's input by a bf16 step
+    of that value (divided by the tokens attending to it), so the shares of
+    identical entries drop by a few percent per layer for any fp32
+    implementation (the decode kernel run with two CTA counts differs the
+    same way); those layers are held to >= 90% identical and a mean
+    |difference| <= 1e-3 of the mean |value|.  The contract itself: the
+    logits of the decode steps that follow within 5e-2, same top-1."""
+    base = dict(wc.TINY.__dict__)
+    if variant == "hd128":
+        base.update(n_heads=4, n_kv_heads=1, head_dim=128, hidden=512)
+    elif variant == "mha":
+        base.update(n_kv_heads=4)
+    elif variant == "tied":
+        base.update(tied_embeddings=True)
+    cfg = wc.ModelConfig(**base)
+    steps = 4
+    max_seq = prompt + steps
+    w = synth.model_weights(cfg, seed=6, device=dev)
+    dec = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=chunk))
+    om = orc.OracleModel(w.to("cpu"), max_seq)
+    kv_o = synth.empty_kv_cache(cfg, max_seq)
+    toks = synth.prompt_tokens(cfg, prompt).tolist()
+    want = min(((chunk or 1024) + 127) // 128 * 128, (max_seq + 127) // 128 * 128)
+    assert dec.prefill_chunk == want   # the tensor-core path is the one that runs
+    if split:
+        dec.prefill(toks[:split], 0)
+        dec.prefill(toks[split:], split)
+    else:
+        dec.prefill(toks, 0)
+    assert amk.amk_kv_length(dec.ctx) == prompt
+    om.prefill(kv_o, toks, 0)
+    dec.sync()
+    (ok0, same0, worst0), same, rel_mean = kv_layers(dec.kv[:, :, :, :prompt], kv_o[:, :, :, :prompt])
+    print(f"{variant} chunk {chunk} P {prompt}: layer 0 identical {same0:.4f} worst/allow {worst0:.3f}; "
+          f"per layer {' '.join(f'{x:.4f}' for x in same)}; mean |diff| / mean |kv| {rel_mean:.2e}")
+    assert ok0 and same0 >= 0.999
+    assert min(same) >= 0.90 and rel_mean <= 1e-3
+    logits = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+    for i, tok in enumerate(synth.decode_tokens(cfg, steps).tolist()):
+        dec.decode_step(tok, prompt + i, logits)
+        ref = om.decode_step(kv_o, tok, prompt + i)
+        got = logits.double().cpu().numpy()
+        assert float(np.abs(got - ref).max()) <= TOL
+        assert int(np.argmax(got)) == int(np.argmax(ref))
+    dec.close()
 
 
 @pytest.mark.parametrize("fmt", ["int8", "int4"])
@@ -296,5 +372,52 @@ def test_full_size_synthetic_kv(amk, orc, dev, name, prompt_len):
     assert ok and same > 0.98
     dec.close()
     del dec, kv, kv_o, om
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_full_size_tensor_core_prefill_matches_decode_steps(amk, dev):
+    """8B bf16 shape: the tensor-core prefill of 256 prompt tokens (chunks
+    of 128: the second chunk attends to the first through the cache)
+    against the decode-kernel prefill (one decode step per token, itself
+    held to the oracle by the tests above).  Layer 0 within two bf16 steps
+    and >= 99.9% identical; through 32 layers the bf16 K,V round trips
+    amplify every rounding difference (the decode kernel against itself
+    with 76 instead of 152 CTAs: 74% identical at the last layer), so the
+    deep layers are held to a mean |difference| <= 3% of the mean |value|;
+    the next decode step's logits within 5e-2, same top-1."""
+    wl = wc.workload("llama8b-bf16")
+    cfg = wl.model
+    P, max_seq = 256, 264
+    w = synth.model_weights(cfg, seed=0, device=dev)
+    a = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=128))
+    b = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=-1))
+    del w
+    gc.collect()
+    toks = synth.prompt_tokens(cfg, P).tolist()
+    a.prefill(toks, 0)
+    b.prefill(toks, 0)
+    a.sync()
+    b.sync()
+    (ok0, same0, worst0), same, rel_mean = kv_layers(a.kv[:, :, :, :P], b.kv[:, :, :, :P])
+    print(f"8B prefill: layer 0 identical {same0:.4f} worst/allow {worst0:.3f}; last layer identical "
+          f"{same[-1]:.4f}; mean |diff| / mean |kv| {rel_mean:.2e}")
+    assert ok0 and same0 >= 0.999
+    assert rel_mean <= 0.03
+    la = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+    lb = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+    tok = int(synth.decode_tokens(cfg, 1)[0])
+    a.decode_step(tok, P, la)
+    b.decode_step(tok, P, lb)
+    a.sync()
+    b.sync()
+    err = float((la - lb).abs().max())
+    print(f"8B prefill: next-step max|dlogit| {err:.3e}")
+    assert err <= TOL
+    assert int(la.argmax()) == int(lb.argmax())
+    a.close()
+    b.close()
+    del a, b
     gc.collect()
     torch.cuda.empty_cache()
