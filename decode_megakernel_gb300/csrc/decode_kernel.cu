@@ -1278,9 +1278,19 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     const int s_begin = c0 / PPS;
     const int s_end = min(c0 + len, ncached) > c0 ? (min(c0 + len, ncached) + PPS - 1) / PPS : s_begin;
     const uint32_t slot0 = kslot;
-    // every warp waits for all of the chunk's stages (runs may span them all)
+    // this warp's run [c0 + w0, c0 + w0 + n)
+    const int per = (len + kConsumerWarps - 1) / kConsumerWarps;
+    const int w0 = min(len, warp * per);
+    const int n = min(len, w0 + per) - w0;
+    // a warp waits only for the stages that hold its run's cached positions
+    // (an mbarrier wait costs ~300 cycles even on a completed phase); every
+    // stage is some warp's, and a stage's slot is refilled only after all
+    // eight warps released it, so no slot is released before its data
+    // landed and was read
+    const int cfirst = c0 + w0, clast = min(c0 + w0 + n, ncached) - 1;
     for (int s2 = s_begin; s2 < s_end; ++s2) {
-      if (!failed)
+      const bool mine = s2 * PPS <= clast && (s2 + 1) * PPS > cfirst;
+      if (!failed && mine)
         failed = !wait_full(kfull0 + kslot * 8, kphase, p, abort_flag, task_idx, tr ? &starved : nullptr);
       if (++kslot == (uint32_t)kKvSlots) { kslot = 0; kphase ^= 1u; }
     }
@@ -1294,10 +1304,6 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
       return kv0 + slot * kStageBytes + (uint32_t)(kv * (kStageBytes / 2) + (c >> 3) * (PPS * 128) + r * 128 +
                                                    (((c & 7) ^ (r & 7)) << 4));
     };
-    // this warp's run [c0 + w0, c0 + w0 + n)
-    const int per = (len + kConsumerWarps - 1) / kConsumerWarps;
-    const int w0 = min(len, warp * per);
-    const int n = min(len, w0 + per) - w0;
     if (!failed && n > 0) {
       const int base = c0 + w0;
       const int plast = base + n - 1;   // padding rows read this position (masked)
