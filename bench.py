@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--ring-slots", type=int, default=0)
     ap.add_argument("--l2-prefetch-tiles", type=int, default=0, help="0: library default, -1: off")
+    ap.add_argument("--prefill-parts", type=int, default=0,
+                    help="bf16 parts of the prefill GEMM activations (0: library default, 3; or 2)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prompt's prefill (its last run bracketed by "
                          "cudaProfilerStart/Stop) and print its JSON block")
@@ -290,15 +292,15 @@ def measured_peak_tflops():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def prefill_block(wl, best_ms, runs_ms, dec_chunk):
+def prefill_block(wl, best_ms, runs_ms, dec_chunk, parts=3):
     """The prompt's prefill: tok/s and, for the tensor-core path, useful
     flops (workload.configs.prefill_flops) per second against the measured
     bf16 tensor peak (a burst figure: the prefill is timed alone)."""
     from workload import configs as wc
     cfg, P = wl.model, wl.prompt_len
     out = {"value": P / (best_ms / 1e3), "unit": "tok/s", "tokens": P, "ms": best_ms, "runs_ms": runs_ms,
-           "path": "tensor-core GEMMs (tcgen05), chunk %d" % dec_chunk if dec_chunk
-           else "decode kernel, one launch per token"}
+           "path": "tensor-core GEMMs (tcgen05), chunk %d, %d activation parts" % (dec_chunk, parts)
+           if dec_chunk else "decode kernel, one launch per token"}
     if dec_chunk:
         fl = wc.prefill_flops(cfg, P)
         peak, src = measured_peak_tflops()
@@ -306,8 +308,8 @@ def prefill_block(wl, best_ms, runs_ms, dec_chunk):
         out["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                            "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (cuBLAS, burst)",
                            "algorithmic_flops": fl,
-                           "note": "GEMM activations enter as three bf16 parts: the tensor cores "
-                                   "execute 3x the GEMM flops counted here"}
+                           "note": "GEMM activations enter as %d bf16 parts: the tensor cores "
+                                   "execute %dx the GEMM flops counted here" % (parts, parts)}
     return out
 
 
@@ -329,7 +331,8 @@ def run_ours(args, wl, rank, world, local_rank):
     max_seq = wl.max_seq
     stream = torch.cuda.Stream(device=dev)
     sched = amk.make_schedule_config(num_ctas=args.num_ctas, ring_slots=args.ring_slots,
-                                     l2_prefetch_tiles=args.l2_prefetch_tiles)
+                                     l2_prefetch_tiles=args.l2_prefetch_tiles,
+                                     prefill_parts=args.prefill_parts)
 
     weights = synth.model_weights(cfg, seed=synth.WEIGHT_SEED, device=dev)
     dec = amk.Decoder(weights, max_seq, stream=stream, sched=sched)
@@ -360,7 +363,7 @@ def run_ours(args, wl, rank, world, local_rank):
     pf_chunk = dec.prefill_chunk
     if args.prefill_only:
         dec.close()
-        return {"impl": "ours", "workload": wl.name, "prefill": prefill_block(wl, pf_best, pf_ms, pf_chunk)}
+        return {"impl": "ours", "workload": wl.name, "prefill": prefill_block(wl, pf_best, pf_ms, pf_chunk, args.prefill_parts or 3)}
 
     logits = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
     pos_of = lambda i: P + (i % D)  # noqa: E731
@@ -449,7 +452,7 @@ def run_ours(args, wl, rank, world, local_rank):
                           "what": "amk_generate: argmax fused into the LM head, n_gen launches back "
                                   "to back with no host round trip (+1 final reduction)"},
         "clocks": clocks,
-        "prefill": prefill_block(wl, pf_best, pf_ms, pf_chunk),
+        "prefill": prefill_block(wl, pf_best, pf_ms, pf_chunk, args.prefill_parts or 3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w_cpu, kv = host_weights_and_kv(wl, dev)

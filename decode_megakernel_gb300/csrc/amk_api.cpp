@@ -46,6 +46,7 @@ struct amk_ctx {
   // tensor-core prefill (bf16 weights): chunk buffers and tensor maps
   struct Prefill {
     int32_t chunk = 0;        // tokens per chunk; 0: prefill by decode steps
+    int32_t parts = kPfDefaultParts;   // bf16 parts of the GEMM activations
     float* x = nullptr;       // residual rows [chunk][hidden]
     uint16_t* h1[kPfParts] = {};  // normed rows, bf16 parts [chunk][hidden]
     uint16_t* h2[kPfParts] = {};  // attention output [chunk][qd] or SwiGLU [chunk][ffn], bf16 parts
@@ -182,7 +183,8 @@ amk_status resolve_ctas(const amk_schedule_config* sched, BuildOptions* opt, std
     opt->max_rows_per_task = sched->max_rows_per_task;
     if (sched->num_ctas < 0 || sched->attn_splits < 0 || sched->max_rows_per_task < 0 ||
         sched->watchdog_ms < 0 || sched->ring_slots < 0 || sched->l2_prefetch_tiles < -1 ||
-        sched->prefill_chunk < -1) {
+        sched->prefill_chunk < -1 || (sched->prefill_parts != 0 && sched->prefill_parts != 2 &&
+                                      sched->prefill_parts != 3)) {
       *why = "negative schedule knob";
       return AMK_ERR_INVALID_ARG;
     }
@@ -289,8 +291,8 @@ amk_status encode_kv_map(amk_ctx* ctx, const amk_config& c, void* kv, CUtensorMa
 // Tensor maps of the tensor-core prefill.  Activation operands (each of
 // the kPfParts bf16 parts): [chunk][K] row major, boxes of 64 k x 128 tokens.  Weight operands: the
 // decode kernel's packed tiles of one layer's matrix as a 4-D tensor
-// {Kt, Rt, nkt, row blocks}, boxes {64, Rt, 1, 128 / Rt}, so that one box
-// is a 128-row x 64-k slice in plain row order.
+// {Kt, Rt, nkt, row blocks}, boxes {64, Rt, 1, 256 / Rt}, so that one box
+// is a 256-row x 64-k slice in plain row order.
 amk_status encode_prefill_maps(amk_ctx* ctx, const DevMat* mats) {
   const amk_config& c = ctx->cfg;
   auto& pf = ctx->pf;
@@ -746,6 +748,7 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   if (g.prefill_chunk > 0) {
     auto& pf = ctx->pf;
     pf.chunk = g.prefill_chunk;
+    pf.parts = sched && sched->prefill_parts ? sched->prefill_parts : kPfDefaultParts;
     pf.x = (float*)(ws + L.pf_x);
     for (int i = 0; i < kPfParts; ++i) {
       pf.h1[i] = (uint16_t*)(ws + L.pf_h1[i]);
@@ -787,6 +790,7 @@ amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
   g.rope = dm.rope;
   for (int i = 0; i < kPfParts; ++i) g.out[i] = pf.h2[i];
   g.ldo = c.ffn;
+  g.parts = pf.parts;
   g.status = dm.status;
   g.timeout_ns = ctx->timeout_ns;
   PrefillAttn at{};
@@ -799,6 +803,7 @@ amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
   at.hd = c.head_dim;
   for (int i = 0; i < kPfParts; ++i) at.o[i] = pf.h2[i];
   at.ldo = qd;
+  at.parts = pf.parts;
   auto gemm = [&](int epi, int kind, int layer, const CUtensorMap* a) {
     const MatGeom& m = geo.mat[kind];
     g.N = m.rows;
@@ -814,13 +819,13 @@ amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
     g.s0 = at.s0 = start_pos + c0;
     AMK_CUDA(ctx, launch_prefill_embed(pf.tokens + c0, T, dm.embed, c.hidden, pf.x, s));
     for (int l = 0; l < c.n_layers; ++l) {
-      AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.attn_norm + l * H, c.rms_eps, pf.h1, s));
+      AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.attn_norm + l * H, c.rms_eps, pf.h1, pf.parts, s));
       AMK_CUDA(ctx, gemm(PE_QKV, M_QKV, l, pf.a_h1));
       at.layer = l;
       AMK_CUDA(ctx, launch_prefill_attn(at, s));
       if (l == c.n_layers - 1) break;   // the rest of the last layer feeds no K,V
       AMK_CUDA(ctx, gemm(PE_RESID, M_O, l, pf.a_o));
-      AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.ffn_norm + l * H, c.rms_eps, pf.h1, s));
+      AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.ffn_norm + l * H, c.rms_eps, pf.h1, pf.parts, s));
       AMK_CUDA(ctx, gemm(PE_SWIGLU, M_GU, l, pf.a_h1));
       AMK_CUDA(ctx, gemm(PE_RESID, M_DOWN, l, pf.a_a));
     }

@@ -1,13 +1,14 @@
 // Tensor-core prefill kernels (see prefill.hpp for the algorithm).
 //
-// GEMM: one 128-token x 128-row output tile per CTA.  Warp 0 (one thread)
-// streams k blocks of the activation parts and the weight tile through a
+// GEMM: one 128-token x 256-row output tile per CTA.  Warp 0 (one thread)
+// streams k blocks of the activation parts and the weight slice through a
 // kPfStages-deep ring with TMA; warp 1 (one thread) issues tcgen05.mma
-// (kind::f16, bf16 x bf16 -> fp32, M 128, N 128, K 16) into one of two
-// 128-column TMEM accumulators, a fresh one every kPfSegKB k blocks, and
-// releases each stage with tcgen05.commit; warps 2..5 read each finished
-// segment back (tcgen05.ld, one token row per thread), add it into fp32
-// registers, hand the buffer back, and at the end run the fused epilogue.  Every wait is bounded by the context's watchdog
+// (kind::f16, bf16 x bf16 -> fp32, M 128, N 256, K 16) into one of two
+// 256-column TMEM accumulators, a fresh one every kPfSegKB k blocks, and
+// releases each stage with tcgen05.commit; eight epilogue warps (two per
+// TMEM lane quarter, 128 columns each) read each finished segment back
+// (tcgen05.ld, one token row per thread), add it into fp32 registers, hand
+// the buffer back, and at the end run the fused epilogue.  Every wait is bounded by the context's watchdog
 // limit; a timeout records ST_TIMEOUT in the status words.
 //
 // Attention: flash-attention over the KV cache with mma.sync (bf16 in,
@@ -25,12 +26,22 @@ namespace amk {
 namespace {
 
 constexpr uint32_t kPfATile = kPfBM * kPfBK * 2;   // 16 KB: 128 tokens x 64 k, bf16
-constexpr uint32_t kPfBTile = kPfBN * kPfBK * 2;   // 16 KB: 128 rows x 64 k, bf16
+constexpr uint32_t kPfBTile = kPfBN * kPfBK * 2;   // 32 KB: 256 rows x 64 k, bf16
+constexpr int kPfEpiCols = kPfBN / (kPfEpiWarps / 4);   // accumulator columns per epilogue warp
 
+// one stage: the activation parts (128 x 64 bf16 each) and the weight
+// slice (256 x 64 bf16); as many stages as fit in 200 KB of shared memory
+template <int PARTS>
+struct GemmShape {
+  static constexpr int kStages = (200 * 1024) / (PARTS * (int)kPfATile + (int)kPfBTile);
+};
+
+template <int PARTS>
 struct __align__(1024) GemmSmem {
-  uint8_t a[kPfStages][kPfParts][kPfATile];
-  uint8_t w[kPfStages][kPfBTile];
-  uint64_t full[kPfStages], empty[kPfStages];
+  static constexpr int S = GemmShape<PARTS>::kStages;
+  uint8_t a[S][PARTS][kPfATile];
+  uint8_t w[S][kPfBTile];
+  uint64_t full[S], empty[S];
   uint64_t acc_full[2], acc_empty[2];   // TMEM accumulator buffers: segment done / drained
   uint32_t tmem;
   uint32_t failed;
@@ -130,9 +141,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 
 __device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
-// x = p[0] + p[1] + p[2] to 2^-27 relative: each part is the bf16 rounding
-// of what the previous parts left (the remainders are exact in fp32)
-__device__ __forceinline__ void split3_bf16(float x, uint16_t (&p)[kPfParts]) {
+// x = p[0] + p[1] + p[2] to 2^-27 relative (the first two: 2^-18): each
+// part is the bf16 rounding of what the previous parts left (the remainders
+// are exact in fp32)
+__device__ __forceinline__ void split_parts(float x, uint16_t (&p)[kPfParts]) {
 #pragma unroll
   for (int i = 0; i < kPfParts; ++i) {
     const __nv_bfloat16 h = __float2bfloat16_rn(x);
@@ -176,12 +188,13 @@ __device__ __forceinline__ void gemm_epilogue(const PrefillGemm& g, int t, int n
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       uint16_t p[kPfParts];
-      split3_bf16(silu(__uint_as_float(v[2 * i])) * __uint_as_float(v[2 * i + 1]), p);
+      split_parts(silu(__uint_as_float(v[2 * i])) * __uint_as_float(v[2 * i + 1]), p);
 #pragma unroll
       for (int k = 0; k < kPfParts; ++k) part[k][i] = p[k];
     }
 #pragma unroll
     for (int k = 0; k < kPfParts; ++k) {
+      if (k >= g.parts) break;
       uint16_t* d = g.out[k] + (int64_t)t * g.ldo + j0;
       if (n + 16 <= g.N)
         *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(part[k]);
@@ -226,13 +239,19 @@ __device__ __forceinline__ void gemm_epilogue(const PrefillGemm& g, int t, int n
   }
 }
 
-template <int EPI>
+// the activation parts' maps and the weight slice's map of one GEMM
+struct GemmMaps {
+  CUtensorMap a[kPfParts];
+  CUtensorMap w;
+};
+
+template <int EPI, int PARTS>
 __global__ void __launch_bounds__(kPfGemmThreads, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-                        const __grid_constant__ CUtensorMap map_a2, const __grid_constant__ CUtensorMap map_w,
-                        const __grid_constant__ PrefillGemm g) {
+    prefill_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ PrefillGemm g) {
+  constexpr int kPfStages = GemmShape<PARTS>::kStages;
   extern __shared__ uint8_t pf_smem_raw[];
-  GemmSmem& sm = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
+  GemmSmem<PARTS>& sm =
+      *reinterpret_cast<GemmSmem<PARTS>*>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.x * kPfBM, n0 = blockIdx.y * kPfBN;
   if (tid == 0) {
@@ -242,7 +261,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&sm.acc_full[b])));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(s_addr(&sm.acc_empty[b])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s_addr(&sm.acc_empty[b])), "r"(kPfEpiWarps));
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     sm.failed = 0;
@@ -270,13 +289,12 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
         }
         const uint32_t fb = s_addr(&sm.full[s]);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                     "r"(kPfParts * kPfATile + kPfBTile)
+                     "r"(PARTS * kPfATile + kPfBTile)
                      : "memory");
         const int k = kb * kPfBK;
-        tma_2d(s_addr(sm.a[s][0]), &map_a0, k, m0, fb);
-        tma_2d(s_addr(sm.a[s][1]), &map_a1, k, m0, fb);
-        tma_2d(s_addr(sm.a[s][2]), &map_a2, k, m0, fb);
-        tma_4d(s_addr(sm.w[s]), &map_w, k % g.Kt, 0, k / g.Kt, n0 / g.Rt, fb);
+#pragma unroll
+        for (int part = 0; part < PARTS; ++part) tma_2d(s_addr(sm.a[s][part]), &maps.a[part], k, m0, fb);
+        tma_4d(s_addr(sm.w[s]), &maps.w, k % g.Kt, 0, k / g.Kt, n0 / g.Rt, fb);
       }
     }
   } else if (warp == 1) {
@@ -306,7 +324,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
         for (int k = 0; k < kPfBK / 16; ++k) {
           const uint64_t bd = kmajor_sw128_desc(bw + k * 32);
 #pragma unroll
-          for (int part = 0; part < kPfParts; ++part)
+          for (int part = 0; part < PARTS; ++part)
             umma_bf16(dt, kmajor_sw128_desc(s_addr(sm.a[s][part]) + k * 32), bd,
                       (!first || k != 0 || part != 0) ? 1u : 0u);
         }
@@ -317,11 +335,12 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
     }
   } else {
     const int quarter = warp & 3;   // TMEM lanes this warp may read: 32 * quarter ..
+    const int col0 = ((warp - 2) >> 2) * kPfEpiCols;   // this warp's accumulator columns
     const int t = m0 + quarter * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    float acc[kPfBN];
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col0;
+    float acc[kPfEpiCols];
 #pragma unroll
-    for (int i = 0; i < kPfBN; ++i) acc[i] = 0.f;
+    for (int i = 0; i < kPfEpiCols; ++i) acc[i] = 0.f;
     const int nseg = (g.nk + kPfSegKB - 1) / kPfSegKB;
     bool ok = true;
     for (int seg = 0; seg < nseg && ok; ++seg) {
@@ -330,7 +349,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
       if (!ok) break;
       asm volatile("tcgen05.fence::after_thread_sync;");
 #pragma unroll
-      for (int c = 0; c < kPfBN; c += 16) {
+      for (int c = 0; c < kPfEpiCols; c += 16) {
         uint32_t v[16];
         tmem_ld16(lane_base + (uint32_t)(b * kPfBN + c), v);
 #pragma unroll
@@ -344,11 +363,11 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
       if (lane == 0) pf_timeout(g.status, SITE_PF_EPI);
     } else if (!sm.failed && t < g.T) {
 #pragma unroll
-      for (int c = 0; c < kPfBN; c += 16) {
+      for (int c = 0; c < kPfEpiCols; c += 16) {
         uint32_t v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(acc[c + j]);
-        if (n0 + c < g.N) gemm_epilogue<EPI>(g, t, n0 + c, v);
+        if (n0 + col0 + c < g.N) gemm_epilogue<EPI>(g, t, n0 + col0 + c, v);
       }
     }
   }
@@ -377,7 +396,7 @@ struct Parts {
 };
 
 __global__ void __launch_bounds__(256) prefill_norm_kernel(const float* x, int T, int hidden, const uint16_t* w,
-                                                           float eps, const Parts out) {
+                                                           float eps, const Parts out, int parts) {
   __shared__ float part[8];
   const int t = blockIdx.x;
   if (t >= T) return;
@@ -393,9 +412,10 @@ __global__ void __launch_bounds__(256) prefill_norm_kernel(const float* x, int T
   const float r = rsqrtf(tot / (float)hidden + eps);
   for (int k = threadIdx.x; k < hidden; k += blockDim.x) {
     uint16_t p[kPfParts];
-    split3_bf16(xr[k] * r * __uint_as_float((uint32_t)w[k] << 16), p);
+    split_parts(xr[k] * r * __uint_as_float((uint32_t)w[k] << 16), p);
 #pragma unroll
-    for (int i = 0; i < kPfParts; ++i) out.p[i][(int64_t)t * hidden + k] = p[i];
+    for (int i = 0; i < kPfParts; ++i)
+      if (i < parts) out.p[i][(int64_t)t * hidden + k] = p[i];
   }
 }
 
@@ -597,19 +617,21 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
 #pragma unroll
     for (int dn = 0; dn < DN; ++dn) {
       uint16_t p0[kPfParts], p1[kPfParts];
-      split3_bf16(o[dn][2 * r] * inv, p0);
-      split3_bf16(o[dn][2 * r + 1] * inv, p1);
+      split_parts(o[dn][2 * r] * inv, p0);
+      split_parts(o[dn][2 * r + 1] * inv, p1);
       const int d = dn * 8 + 2 * tq;
 #pragma unroll
       for (int i = 0; i < kPfParts; ++i)
-        *reinterpret_cast<uint32_t*>(a.o[i] + row + d) = (uint32_t)p0[i] | ((uint32_t)p1[i] << 16);
+        if (i < a.parts) *reinterpret_cast<uint32_t*>(a.o[i] + row + d) = (uint32_t)p0[i] | ((uint32_t)p1[i] << 16);
     }
   }
 }
 
 }  // namespace
 
-int prefill_gemm_smem_bytes() { return (int)sizeof(GemmSmem) + 1024; }
+int prefill_gemm_smem_bytes(int parts) {
+  return (parts == 2 ? (int)sizeof(GemmSmem<2>) : (int)sizeof(GemmSmem<3>)) + 1024;
+}
 
 int prefill_attn_smem_bytes(int head_dim, int group) {
   return head_dim == 64 ? AttnShape<64>::bytes(group) : AttnShape<128>::bytes(group);
@@ -623,31 +645,40 @@ cudaError_t launch_prefill_embed(const int32_t* tokens, int T, const uint16_t* e
 }
 
 cudaError_t launch_prefill_norm(const float* x, int T, int hidden, const uint16_t* w, float eps,
-                                uint16_t* const* out, cudaStream_t s) {
+                                uint16_t* const* out, int parts, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   Parts p;
   for (int i = 0; i < kPfParts; ++i) p.p[i] = out[i];
-  prefill_norm_kernel<<<T, 256, 0, s>>>(x, T, hidden, w, eps, p);
+  prefill_norm_kernel<<<T, 256, 0, s>>>(x, T, hidden, w, eps, p, parts);
+  return cudaGetLastError();
+}
+
+template <int EPI, int PARTS>
+cudaError_t launch_gemm_instance(const GemmMaps& maps, const PrefillGemm& g, cudaStream_t s) {
+  const int smem = prefill_gemm_smem_bytes(PARTS);
+  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<EPI, PARTS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((g.T + kPfBM - 1) / kPfBM, (g.N + kPfBN - 1) / kPfBN);
+  prefill_gemm_kernel<EPI, PARTS><<<grid, kPfGemmThreads, smem, s>>>(maps, g);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap* w, const PrefillGemm& g,
                                 cudaStream_t s) {
   if (g.T <= 0) return cudaSuccess;
-  const int smem = prefill_gemm_smem_bytes();
-  const dim3 grid((g.T + kPfBM - 1) / kPfBM, (g.N + kPfBN - 1) / kPfBN);
-  const void* fn = epi == PE_QKV      ? (const void*)prefill_gemm_kernel<PE_QKV>
-                   : epi == PE_RESID  ? (const void*)prefill_gemm_kernel<PE_RESID>
-                                      : (const void*)prefill_gemm_kernel<PE_SWIGLU>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  if (epi == PE_QKV)
-    prefill_gemm_kernel<PE_QKV><<<grid, kPfGemmThreads, smem, s>>>(a[0], a[1], a[2], *w, g);
-  else if (epi == PE_RESID)
-    prefill_gemm_kernel<PE_RESID><<<grid, kPfGemmThreads, smem, s>>>(a[0], a[1], a[2], *w, g);
-  else
-    prefill_gemm_kernel<PE_SWIGLU><<<grid, kPfGemmThreads, smem, s>>>(a[0], a[1], a[2], *w, g);
-  return cudaGetLastError();
+  if (g.parts != 2 && g.parts != 3) return cudaErrorInvalidValue;
+  GemmMaps maps;
+  for (int i = 0; i < kPfParts; ++i) maps.a[i] = a[i];
+  maps.w = *w;
+  if (g.parts == 2) {
+    if (epi == PE_QKV) return launch_gemm_instance<PE_QKV, 2>(maps, g, s);
+    if (epi == PE_RESID) return launch_gemm_instance<PE_RESID, 2>(maps, g, s);
+    return launch_gemm_instance<PE_SWIGLU, 2>(maps, g, s);
+  }
+  if (epi == PE_QKV) return launch_gemm_instance<PE_QKV, 3>(maps, g, s);
+  if (epi == PE_RESID) return launch_gemm_instance<PE_RESID, 3>(maps, g, s);
+  return launch_gemm_instance<PE_SWIGLU, 3>(maps, g, s);
 }
 
 cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s) {

@@ -8,21 +8,23 @@
 // Per chunk of T <= chunk tokens at positions s0 .. s0 + T - 1:
 //   X = E[tokens]                                            (fp32 [T][H])
 //   per layer l:
-//     H1 = rmsnorm(X) * w_attn[l]            as three bf16 parts [T][H]
+//     H1 = rmsnorm(X) * w_attn[l]            as bf16 parts [T][H]
 //     QKV GEMM, epilogue: RoPE; q -> Q (fp32 [T][n_heads * hd]); k, v ->
 //       the KV cache (bf16) at positions s0 + t
-//     attention (causal over positions 0 .. s0 + t, GQA) -> O, three bf16 parts
+//     attention (causal over positions 0 .. s0 + t, GQA) -> O, bf16 parts
 //     (last layer: stop, the rest of it feeds no K,V)
 //     X += O Wo^T;  H1 = rmsnorm(X) * w_ffn[l]
-//     gate/up GEMM, epilogue silu(g) * u -> A, three bf16 parts [T][F]
+//     gate/up GEMM, epilogue silu(g) * u -> A, bf16 parts [T][F]
 //     X += A Wd^T
-// Every GEMM activation operand is split into three bf16 parts, x = p0 + p1
-// + p2 to 2^-27 relative (p0 = bf16(x), p1 = bf16(x - p0), p2 = bf16(x - p0
-// - p1); each subtraction is exact in fp32), and the three parts are
-// multiplied against the bf16 weights into one fp32 accumulator: the
-// products carry the activation's full fp32 precision, as the decode
-// kernel's fp32 GEMVs do.  (Two parts, 2^-18, measurably moved the K,V
-// away from the fp32 path: 1.4% of the bf16 entries rounded differently.)
+// Every GEMM activation operand is split into bf16 parts, x = p0 + p1 (+
+// p2) to 2^-18 (2^-27) relative (p0 = bf16(x), p1 = bf16(x - p0), p2 =
+// bf16(x - p0 - p1); each subtraction is exact in fp32), and the parts are
+// multiplied against the bf16 weights into one fp32 accumulator.  Three
+// parts (the default) carry the activation's full fp32 precision, as the
+// decode kernel's fp32 GEMVs do; two parts take two thirds of the tensor
+// work (measured on the 8B shape: 53 instead of 75 ms for 2048 tokens) and
+// leave ~0.3% of the first layer's bf16 K,V one step off the fp32 path
+// (three parts: ~0.04%).
 #pragma once
 
 #include <cuda.h>
@@ -33,10 +35,10 @@
 namespace amk {
 
 constexpr int kPfBM = 128;      // tokens per GEMM tile (MMA M, TMEM lanes)
-constexpr int kPfBN = 128;      // packed weight rows per GEMM tile (MMA N, TMEM columns)
+constexpr int kPfBN = 256;      // packed weight rows per GEMM tile (MMA N, TMEM columns)
 constexpr int kPfBK = 64;       // k per pipeline stage: one 128-byte swizzled row
-constexpr int kPfParts = 3;     // bf16 parts of a GEMM activation operand
-constexpr int kPfStages = 3;    // GEMM pipeline depth (3 x (3 + 1) x 16 KB of shared memory)
+constexpr int kPfParts = 3;     // bf16 parts of a GEMM activation operand at most (buffers, maps)
+constexpr int kPfDefaultParts = 3;
 // The tensor cores' fp32 accumulation truncates (measured: a bias toward
 // zero that grows with K, ~1e-7 of the sum of |terms| at K = 4096 against
 // ~1e-10 for an fp32 FMA chain), so the GEMM accumulates in TMEM only over
@@ -44,7 +46,9 @@ constexpr int kPfStages = 3;    // GEMM pipeline depth (3 x (3 + 1) x 16 KB of s
 // sums into fp32 registers of the epilogue warps, two TMEM buffers
 // alternating so that the MMAs never wait for the promotion.
 constexpr int kPfSegKB = 2;
-constexpr int kPfGemmThreads = 192;   // TMA warp, MMA warp, four epilogue warps
+// epilogue warps: two per TMEM lane quarter, each owning 128 accumulator columns
+constexpr int kPfEpiWarps = 8;
+constexpr int kPfGemmThreads = 64 + 32 * kPfEpiWarps;   // TMA warp, MMA warp, epilogue warps
 constexpr int kPfQT = 16;       // query tokens per attention CTA (one m16 tile per head)
 constexpr int kPfKB = 64;       // cached positions per attention key block
 constexpr int kPfDefaultChunk = 1024;
@@ -52,9 +56,10 @@ constexpr int kPfDefaultChunk = 1024;
 enum PrefillEpi : int32_t { PE_QKV = 0, PE_RESID = 1, PE_SWIGLU = 2 };
 
 // One GEMM D[T][N] = A[T][K] . W[N][K]^T over a packed weight matrix and its
-// epilogue.  A arrives through three 2-D tensor maps (its bf16 parts, each
-// [rows][K], boxes of 64 x 128, 128-byte swizzle); W through a 4-D map over the decode
-// kernel's tile layout ({Kt, Rt, nkt, n_rb}, boxes {64, Rt, 1, 128 / Rt}).
+// epilogue.  A arrives through kPfParts 2-D tensor maps (its bf16 parts,
+// each [rows][K], boxes of 64 x 128, 128-byte swizzle); W through a 4-D map
+// over the decode kernel's tile layout ({Kt, Rt, nkt, n_rb}, boxes
+// {64, Rt, 1, 256 / Rt}).
 struct PrefillGemm {
   int32_t T;              // tokens (rows of D that are stored)
   int32_t N;              // packed weight rows (columns of D that are used)
@@ -68,15 +73,16 @@ struct PrefillGemm {
   int32_t ldq;
   uint16_t* kv;           // PE_QKV: KV cache bf16 [L][2][n_kv][max_seq][hd]
   const float2* rope;     // PE_QKV: (cos, sin) [max_seq][hd / 2]
-  uint16_t* out[kPfParts];   // PE_SWIGLU: silu(g) * u as three bf16 parts [T][ldo]
+  uint16_t* out[kPfParts];   // PE_SWIGLU: silu(g) * u as bf16 parts [T][ldo]
   int32_t ldo;
+  int32_t parts;          // bf16 parts of the activations (2 or 3)
   uint32_t* status;       // device status words (a timed-out wait records ST_TIMEOUT)
   uint64_t timeout_ns;
 };
 
 // Causal GQA attention of a chunk: queries Q (fp32, RoPE applied) of
 // tokens [0, T) at positions s0 + t against the cache's K,V of positions
-// [0, s0 + t]; output O as three bf16 parts [T][ldo] in head order.
+// [0, s0 + t]; output O as bf16 parts [T][ldo] in head order.
 struct PrefillAttn {
   const float* q;
   int32_t ldq;
@@ -85,18 +91,19 @@ struct PrefillAttn {
   int32_t T, s0;
   uint16_t* o[kPfParts];
   int32_t ldo;
+  int32_t parts;          // bf16 parts written (2 or 3)
 };
 
-int prefill_gemm_smem_bytes();
+int prefill_gemm_smem_bytes(int parts);
 int prefill_attn_smem_bytes(int head_dim, int group);
 
 // X[t][:] = float(embed[tokens[t]][:]) for t < T
 cudaError_t launch_prefill_embed(const int32_t* tokens, int T, const uint16_t* embed, int hidden,
                                  float* x, cudaStream_t s);
-// out[0..2][t][:] = the bf16 parts of rmsnorm(X[t]) * w for t < T (row stride hidden)
+// out[i][t][:] = the bf16 parts of rmsnorm(X[t]) * w for t < T (row stride hidden)
 cudaError_t launch_prefill_norm(const float* x, int T, int hidden, const uint16_t* w, float eps,
-                                uint16_t* const* out, cudaStream_t s);
-// a: kPfParts tensor maps of the activation parts
+                                uint16_t* const* out, int parts, cudaStream_t s);
+// a: the g.parts tensor maps of the activation parts
 cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap* w, const PrefillGemm& g,
                                 cudaStream_t s);
 cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s);

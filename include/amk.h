@@ -113,7 +113,9 @@ typedef struct {
                                    0: default 1024 (at most max_seq rounded up to 128);
                                    -1: prefill through the decode kernel, one launch per
                                    token (always so for int8 / int4 weights) */
-    int32_t reserved[1];
+    int32_t prefill_parts;      /* bf16 parts per activation operand of the prefill GEMMs:
+                                   0 or 3: three (fp32-level products, the default); 2: two
+                                   (2^-18 relative, two thirds of the tensor work) */
 } amk_schedule_config;
 
 typedef struct amk_ctx amk_ctx;

@@ -232,19 +232,22 @@ def kv_layers(a, b):
     return first, same, rel_mean
 
 
-@pytest.mark.parametrize("variant,chunk,prompt,split", [
-    ("tiny", 0, 12, None),       # one chunk, one partial 128-token tile
-    ("tiny", 128, 300, 100),     # two calls (history from the first), three chunks, ragged tail
-    ("hd128", 128, 200, None),   # head_dim 128, group 4
-    ("mha", 0, 40, 17),          # group 1
-    ("tied", 256, 260, None),
+@pytest.mark.parametrize("variant,chunk,prompt,split,parts", [
+    ("tiny", 0, 12, None, 0),       # one chunk, one partial 128-token tile
+    ("tiny", 128, 300, 100, 0),     # two calls (history from the first), three chunks, ragged tail
+    ("hd128", 128, 200, None, 0),   # head_dim 128, group 4
+    ("mha", 0, 40, 17, 0),          # group 1
+    ("tied", 256, 260, None, 0),
+    ("tiny", 128, 300, 100, 2),     # two activation parts
+    ("hd128", 0, 200, None, 2),
 ])
-def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, prompt, split):
+def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, prompt, split, parts):
     """The tensor-core prefill (tcgen05 GEMMs, mma.sync attention) against
     the oracle's batched causal prefill, then decode steps on top of it.
 
     Layer 0's K,V come straight from the embedding, RMSNorm, the QKV GEMM
-    and RoPE: within two bf16 steps of the oracle and >= 99.9% bit-identical.
+    and RoPE: within two bf16 steps of the oracle and >= 99.9% bit-identical
+    (>= 99.5% with two activation parts, 2^-18 instead of 2^-27).
     Deeper layers inherit every bf16 rounding of the layers below: a V entry
     that rounds the other way moves the next layer's input by a bf16 step
     of that value (divided by the tokens attending to it), so the shares of
@@ -264,7 +267,7 @@ def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, promp
     steps = 4
     max_seq = prompt + steps
     w = synth.model_weights(cfg, seed=6, device=dev)
-    dec = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=chunk))
+    dec = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=chunk, prefill_parts=parts))
     om = orc.OracleModel(w.to("cpu"), max_seq)
     kv_o = synth.empty_kv_cache(cfg, max_seq)
     toks = synth.prompt_tokens(cfg, prompt).tolist()
@@ -279,9 +282,10 @@ def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, promp
     om.prefill(kv_o, toks, 0)
     dec.sync()
     (ok0, same0, worst0), same, rel_mean = kv_layers(dec.kv[:, :, :, :prompt], kv_o[:, :, :, :prompt])
-    print(f"{variant} chunk {chunk} P {prompt}: layer 0 identical {same0:.4f} worst/allow {worst0:.3f}; "
-          f"per layer {' '.join(f'{x:.4f}' for x in same)}; mean |diff| / mean |kv| {rel_mean:.2e}")
-    assert ok0 and same0 >= 0.999
+    print(f"{variant} chunk {chunk} P {prompt} parts {parts or 3}: layer 0 identical {same0:.4f} "
+          f"worst/allow {worst0:.3f}; per layer {' '.join(f'{x:.4f}' for x in same)}; "
+          f"mean |diff| / mean |kv| {rel_mean:.2e}")
+    assert ok0 and same0 >= (0.995 if parts == 2 else 0.999)
     assert min(same) >= 0.90 and rel_mean <= 1e-3
     logits = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
     for i, tok in enumerate(synth.decode_tokens(cfg, steps).tolist()):
@@ -377,7 +381,8 @@ def test_full_size_synthetic_kv(amk, orc, dev, name, prompt_len):
 
 
 @pytest.mark.slow
-def test_full_size_tensor_core_prefill_matches_decode_steps(amk, dev):
+@pytest.mark.parametrize("parts", [3, 2])
+def test_full_size_tensor_core_prefill_matches_decode_steps(amk, dev, parts):
     """8B bf16 shape: the tensor-core prefill of 256 prompt tokens (chunks
     of 128: the second chunk attends to the first through the cache)
     against the decode-kernel prefill (one decode step per token, itself
@@ -391,7 +396,7 @@ def test_full_size_tensor_core_prefill_matches_decode_steps(amk, dev):
     cfg = wl.model
     P, max_seq = 256, 264
     w = synth.model_weights(cfg, seed=0, device=dev)
-    a = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=128))
+    a = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=128, prefill_parts=parts))
     b = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=-1))
     del w
     gc.collect()
@@ -401,9 +406,9 @@ def test_full_size_tensor_core_prefill_matches_decode_steps(amk, dev):
     a.sync()
     b.sync()
     (ok0, same0, worst0), same, rel_mean = kv_layers(a.kv[:, :, :, :P], b.kv[:, :, :, :P])
-    print(f"8B prefill: layer 0 identical {same0:.4f} worst/allow {worst0:.3f}; last layer identical "
-          f"{same[-1]:.4f}; mean |diff| / mean |kv| {rel_mean:.2e}")
-    assert ok0 and same0 >= 0.999
+    print(f"8B prefill, {parts} parts: layer 0 identical {same0:.4f} worst/allow {worst0:.3f}; last layer "
+          f"identical {same[-1]:.4f}; mean |diff| / mean |kv| {rel_mean:.2e}")
+    assert ok0 and same0 >= (0.995 if parts == 2 else 0.999)
     assert rel_mean <= 0.03
     la = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
     lb = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
