@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--ring-slots", type=int, default=0)
     ap.add_argument("--l2-prefetch-tiles", type=int, default=0, help="0: library default, -1: off")
+    ap.add_argument("--prefill-chunk", type=int, default=0,
+                    help="tokens per tensor-core prefill chunk (0: library default; -1: decode steps)")
     ap.add_argument("--prefill-parts", type=int, default=0,
                     help="bf16 parts of the prefill GEMM activations (0: library default, 3; or 2)")
     ap.add_argument("--prefill-only", action="store_true",
@@ -332,7 +334,7 @@ def run_ours(args, wl, rank, world, local_rank):
     stream = torch.cuda.Stream(device=dev)
     sched = amk.make_schedule_config(num_ctas=args.num_ctas, ring_slots=args.ring_slots,
                                      l2_prefetch_tiles=args.l2_prefetch_tiles,
-                                     prefill_parts=args.prefill_parts)
+                                     prefill_chunk=args.prefill_chunk, prefill_parts=args.prefill_parts)
 
     weights = synth.model_weights(cfg, seed=synth.WEIGHT_SEED, device=dev)
     dec = amk.Decoder(weights, max_seq, stream=stream, sched=sched)

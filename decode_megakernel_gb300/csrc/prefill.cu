@@ -12,8 +12,9 @@
 // limit; a timeout records ST_TIMEOUT in the status words.
 //
 // Attention: flash-attention over the KV cache with mma.sync (bf16 in,
-// fp32 accumulate), one CTA per (16 query tokens, KV head), one warp per
-// query head of the group; q and P split into bf16 hi + lo as in the decode
+// fp32 accumulate), one CTA per (16 x attn_groups(G) query tokens, KV head),
+// one warp per (query head of the group, 16 tokens), all warps sharing the
+// CTA's K,V tiles; q and P split into bf16 hi + lo as in the decode
 // kernel's attention (softmax weights and pre-scaled scores need no more:
 // the attention's K,V are bf16 already).
 #include "device_model.hpp"
@@ -446,15 +447,20 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-token groups per attention CTA: up to eight warps (G of them per group)
+__host__ __device__ constexpr int attn_groups(int group) {
+  return group >= 8 ? 1 : group >= 4 ? 2 : 4;
+}
+
 template <int HD>
 struct AttnShape {
   static constexpr int RP = HD + 8;   // bf16 row pitch: rows 16 bytes apart in the banks
   static constexpr int KV_ELEMS = 2 * kPfKB * RP;   // one K or V buffer pair (double buffered)
-  static int bytes(int group) { return (2 * KV_ELEMS + group * 2 * kPfQT * RP) * 2; }
+  static int bytes(int group) { return (2 * KV_ELEMS + group * attn_groups(group) * 2 * kPfQT * RP) * 2; }
 };
 
 // Shared memory (bf16 elements): K [2][64][RP], V [2][64][RP], then per
-// warp (query head) q hi [16][RP] and q lo [16][RP].
+// warp (query head x token group) q hi [16][RP] and q lo [16][RP].
 template <int HD>
 __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) {
   using S = AttnShape<HD>;
@@ -465,8 +471,10 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
   const int gq = lane >> 2, tq = lane & 3;
   const int g = blockIdx.y, G = a.group;
-  const int tb = blockIdx.x * kPfQT;
-  const int head = g * G + warp;
+  const int cta_tokens = kPfQT * attn_groups(G);
+  const int tb0 = blockIdx.x * cta_tokens;          // the CTA's first token
+  const int tb = tb0 + (warp / G) * kPfQT;           // this warp's first token
+  const int head = g * G + warp % G;
   uint16_t* qh = at_smem + 2 * S::KV_ELEMS + warp * 2 * kPfQT * RP;
   uint16_t* ql = qh + kPfQT * RP;
 
@@ -483,8 +491,8 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
     *reinterpret_cast<uint2*>(ql + r * RP + d) = make_uint2(l0, l1);
   }
 
-  // positions [0, kv_end) are needed by the block's last valid token
-  const int t_last = min(a.T, tb + kPfQT) - 1;
+  // positions [0, kv_end) are needed by the CTA's last valid token
+  const int t_last = min(a.T, tb0 + cta_tokens) - 1;
   const int kv_end = a.s0 + t_last + 1;
   const int nblk = (kv_end + kPfKB - 1) / kPfKB;
   const uint16_t* kbase = a.kv + (((int64_t)a.layer * 2 + 0) * a.n_kv + g) * a.max_seq * HD;
@@ -684,14 +692,16 @@ cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap
 cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   const int smem = prefill_attn_smem_bytes(a.hd, a.group);
-  const dim3 grid((a.T + kPfQT - 1) / kPfQT, a.n_kv);
+  const int groups = attn_groups(a.group), cta_tokens = kPfQT * groups;
+  const dim3 grid((a.T + cta_tokens - 1) / cta_tokens, a.n_kv);
+  const int threads = 32 * a.group * groups;
   const void* fn = a.hd == 64 ? (const void*)prefill_attn_kernel<64> : (const void*)prefill_attn_kernel<128>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (a.hd == 64)
-    prefill_attn_kernel<64><<<grid, 32 * a.group, smem, s>>>(a);
+    prefill_attn_kernel<64><<<grid, threads, smem, s>>>(a);
   else
-    prefill_attn_kernel<128><<<grid, 32 * a.group, smem, s>>>(a);
+    prefill_attn_kernel<128><<<grid, threads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

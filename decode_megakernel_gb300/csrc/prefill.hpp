@@ -49,9 +49,9 @@ constexpr int kPfSegKB = 2;
 // epilogue warps: two per TMEM lane quarter, each owning 128 accumulator columns
 constexpr int kPfEpiWarps = 8;
 constexpr int kPfGemmThreads = 64 + 32 * kPfEpiWarps;   // TMA warp, MMA warp, epilogue warps
-constexpr int kPfQT = 16;       // query tokens per attention CTA (one m16 tile per head)
+constexpr int kPfQT = 16;       // query tokens of one attention warp (one m16 tile of one head)
 constexpr int kPfKB = 64;       // cached positions per attention key block
-constexpr int kPfDefaultChunk = 1024;
+constexpr int kPfDefaultChunk = 2048;
 
 enum PrefillEpi : int32_t { PE_QKV = 0, PE_RESID = 1, PE_SWIGLU = 2 };
 

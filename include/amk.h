@@ -110,7 +110,7 @@ typedef struct {
                                    ring while its consumers run attention, the split merge
                                    or the O projection (-1: off; 0: default) */
     int32_t prefill_chunk;      /* tokens per chunk of the tensor-core prefill (bf16 weights):
-                                   0: default 1024 (at most max_seq rounded up to 128);
+                                   0: default 2048 (at most max_seq rounded up to 128);
                                    -1: prefill through the decode kernel, one launch per
                                    token (always so for int8 / int4 weights) */
     int32_t prefill_parts;      /* bf16 parts per activation operand of the prefill GEMMs:

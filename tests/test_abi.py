@@ -91,7 +91,7 @@ def test_prefill_chunk_sizes_the_workspace(amk):
     m = wc.LLAMA_8B_BF16
     qd = m.n_heads * m.head_dim
     per_tok = m.hidden * 4 + 3 * m.hidden * 2 + 3 * max(qd, m.ffn) * 2 + qd * 4
-    expect = 1024 * per_tok + 2176 * 4
+    expect = 2048 * per_tok + 2176 * 4
     assert expect <= dflt - base <= expect + 10 * 256
     # a chunk is whole 128-token tiles, and no more than the cache holds
     c1 = amk.make_config(wc.LLAMA_8B_BF16, 200)

@@ -271,7 +271,7 @@ def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, promp
     om = orc.OracleModel(w.to("cpu"), max_seq)
     kv_o = synth.empty_kv_cache(cfg, max_seq)
     toks = synth.prompt_tokens(cfg, prompt).tolist()
-    want = min(((chunk or 1024) + 127) // 128 * 128, (max_seq + 127) // 128 * 128)
+    want = min(((chunk or 2048) + 127) // 128 * 128, (max_seq + 127) // 128 * 128)
     assert dec.prefill_chunk == want   # the tensor-core path is the one that runs
     if split:
         dec.prefill(toks[:split], 0)
