@@ -46,7 +46,7 @@ METRIC = "batch-1 decode tok/s (Llama-8B-shape bf16); % of weight+KV bytes/HBM r
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["decode_kernel.cu", "device_model.hpp", "schedule.cpp", "schedule.hpp"]
+KERNEL_SOURCES = ["decode_kernel.cu", "device_model.hpp", "schedule.cpp", "schedule.hpp", "ptx.cuh"]
 
 
 def parse_args(argv=None):

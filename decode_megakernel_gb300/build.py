@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libamk.so")
 
 SOURCES = ["decode_kernel.cu", "amk_api.cpp", "schedule.cpp", "static_scratch.cu", "prefill.cu"]
-HEADERS = ["device_model.hpp", "schedule.hpp", "prefill.hpp"]
+HEADERS = ["device_model.hpp", "schedule.hpp", "prefill.hpp", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE]

@@ -4,22 +4,25 @@
 // model of the AutoMegaKernel "Layer 0" VM (wait -> dispatch -> signal over
 // a local queue).  Two departures from the pages' design:
 //   * a CTA is split into a producer warp and eight consumer warps.  The
-//     producer streams every weight tile (and the KV-cache history) of the
-//     CTA's whole queue through a shared-memory ring of kStageBytes stages
-//     (128 KB in flight by default) with 1-D TMA bulk copies completing on
-//     mbarriers.  Weights never depend on activations, so the producer runs
-//     ahead across the consumers' waits; this hides the per-tile cross-SM
-//     synchronisation cost the pages name as the bottleneck on
-//     high-bandwidth GPUs (AMK "Experimental results": training-class GPUs).
+//     producer streams the weight tiles of the CTA's whole queue through a
+//     shared-memory weight ring (8 x 16 KB tiles in flight, 1-D TMA bulk
+//     copies completing on mbarriers) and the K,V history of its attention
+//     tasks through a separate 4-slot KV ring (2-D swizzled TMA boxes).
+//     Weights never depend on activations and the history never depends on
+//     the current step, so the producer runs ahead across the consumers'
+//     waits; this hides the per-tile cross-SM synchronisation cost the
+//     pages name as the bottleneck on high-bandwidth GPUs (AMK
+//     "Experimental results": training-class GPUs).
 //   * the monotonic counters are fused into the data: every value handed
-//     between CTAs is a tagged word (fp32 rounded to 24 bits | 8-bit version
+//     between CTAs is a tagged word (fp32 rounded to 28 bits | 4-bit version
 //     tag).  A task polls its inputs until they carry the version it needs
 //     and its tagged stores are its signal, so a hand-off costs one L2 round
 //     trip instead of a release fence, a counter poll and a data load.
 // The consumers keep the activation vector in registers, reduce with warp
 // shuffles and apply the fused epilogues (RoPE + KV append, residual adds,
-// SwiGLU, logits).  Every wait is bounded by %globaltimer: on expiry the
-// kernel records a status word, lets its own copies land and returns.
+// SwiGLU, logits); attention runs on the tensor cores (mma.sync).  Every
+// wait is bounded by %globaltimer: on expiry the kernel records a status
+// word, lets its own copies land and returns.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -27,14 +30,12 @@
 #include <cuda_runtime.h>
 
 #include "device_model.hpp"
+#include "ptx.cuh"
 
 namespace amk {
 
 // ------------------------------------------------------------------ PTX
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
@@ -96,11 +97,6 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t global_timer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // Tagged words.  A value handed from one CTA to another inside a step is an
 // fp32 rounded to nearest-even at bit 4 (28 of its 32 bits kept, i.e. 19
@@ -625,17 +621,6 @@ __device__ __forceinline__ uint32_t lds8(uint32_t a) {
 __device__ __forceinline__ void mbar_arrive32(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait32(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 // Bounded wait for a ring slot's data (consumer side).
 __device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, const StepParams& p,
@@ -894,7 +879,6 @@ __device__ __forceinline__ float chunk_dot_u4(uint32_t a, uint32_t side_s, uint3
   return fmaf(s, fmaf(-z, hs, d.x + d.y), acc);
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // GEMV task: rows [a0*Rt, a1*Rt) of one tiled matrix against the activation.
 // `stage` counts the ring stages this CTA has consumed so far; returns the
@@ -1136,36 +1120,6 @@ __device__ __forceinline__ int gemv_dispatch(const StepParams& p, Smem& sm, cons
   }
 }
 
-// ldmatrix / mma.sync helpers (bf16 in, fp32 accumulate)
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// d += a (16x16, row) * b (16x8, col)
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// (x0, x1) as bf16 pairs hi + lo with x ~= hi + lo to about 2^-16 relative
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
 
 // Split-K GQA attention of one KV head over one context split (positions
 // [t0, t1) of the cache, plus the step's own position for the last split),

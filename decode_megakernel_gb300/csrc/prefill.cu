@@ -19,6 +19,7 @@
 // the attention's K,V are bf16 already).
 #include "device_model.hpp"
 #include "prefill.hpp"
+#include "ptx.cuh"
 
 #include <cuda_bf16.h>
 
@@ -48,32 +49,15 @@ struct __align__(1024) GemmSmem {
   uint32_t failed;
 };
 
-__device__ __forceinline__ uint32_t s_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
-__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
 // bounded wait for a phase of an mbarrier: false after limit_ns
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (bar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = now_ns();
-  while (!bar_try_wait(bar, parity))
-    if (now_ns() - t0 > limit_ns) return false;
+  if (mbar_try_wait32(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  while (!mbar_try_wait32(bar, parity))
+    if (global_timer() - t0 > limit_ns) return false;
   return true;
 }
 
@@ -154,15 +138,7 @@ __device__ __forceinline__ void split_parts(float x, uint16_t (&p)[kPfParts]) {
   }
 }
 
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // Epilogue of 16 consecutive packed rows [n, n + 16) of token t (t < T).
 template <int EPI>
@@ -257,19 +233,19 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
   const int m0 = blockIdx.x * kPfBM, n0 = blockIdx.y * kPfBN;
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&sm.full[s])));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&sm.empty[s])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[s])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.empty[s])));
     }
     for (int b = 0; b < 2; ++b) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(s_addr(&sm.acc_full[b])));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s_addr(&sm.acc_empty[b])), "r"(kPfEpiWarps));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.acc_full[b])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.acc_empty[b])), "r"(kPfEpiWarps));
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     sm.failed = 0;
   }
   if (warp == 1) {   // the MMA warp owns the accumulators' TMEM columns
     __syncwarp();
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s_addr(&sm.tmem)),
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem)),
                  "r"(2 * kPfBN));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
@@ -283,19 +259,19 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
       for (int kb = 0; kb < g.nk; ++kb) {
         const int s = kb % kPfStages;
         const uint32_t ph = (uint32_t)(kb / kPfStages) & 1u;
-        if (!bar_wait(s_addr(&sm.empty[s]), ph ^ 1u, g.timeout_ns)) {
+        if (!bar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, g.timeout_ns)) {
           pf_timeout(g.status, SITE_PF_TMA);
           sm.failed = 1;
           break;
         }
-        const uint32_t fb = s_addr(&sm.full[s]);
+        const uint32_t fb = smem_addr(&sm.full[s]);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
                      "r"(PARTS * kPfATile + kPfBTile)
                      : "memory");
         const int k = kb * kPfBK;
 #pragma unroll
-        for (int part = 0; part < PARTS; ++part) tma_2d(s_addr(sm.a[s][part]), &maps.a[part], k, m0, fb);
-        tma_4d(s_addr(sm.w[s]), &maps.w, k % g.Kt, 0, k / g.Kt, n0 / g.Rt, fb);
+        for (int part = 0; part < PARTS; ++part) tma_2d(smem_addr(sm.a[s][part]), &maps.a[part], k, m0, fb);
+        tma_4d(smem_addr(sm.w[s]), &maps.w, k % g.Kt, 0, k / g.Kt, n0 / g.Rt, fb);
       }
     }
   } else if (warp == 1) {
@@ -305,7 +281,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
         const uint32_t dt = tmem + (uint32_t)(b * kPfBN);
         const bool first = kb % kPfSegKB == 0;
         if (first) {   // this buffer's previous segment must have been drained
-          if (!bar_wait(s_addr(&sm.acc_empty[b]), ((uint32_t)(seg >> 1) & 1u) ^ 1u, g.timeout_ns)) {
+          if (!bar_wait(smem_addr(&sm.acc_empty[b]), ((uint32_t)(seg >> 1) & 1u) ^ 1u, g.timeout_ns)) {
             pf_timeout(g.status, SITE_PF_MMA);
             sm.failed = 1;
             break;
@@ -314,24 +290,24 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
         }
         const int s = kb % kPfStages;
         const uint32_t ph = (uint32_t)(kb / kPfStages) & 1u;
-        if (!bar_wait(s_addr(&sm.full[s]), ph, g.timeout_ns)) {
+        if (!bar_wait(smem_addr(&sm.full[s]), ph, g.timeout_ns)) {
           pf_timeout(g.status, SITE_PF_MMA);
           sm.failed = 1;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;");
-        const uint32_t bw = s_addr(sm.w[s]);
+        const uint32_t bw = smem_addr(sm.w[s]);
 #pragma unroll
         for (int k = 0; k < kPfBK / 16; ++k) {
           const uint64_t bd = kmajor_sw128_desc(bw + k * 32);
 #pragma unroll
           for (int part = 0; part < PARTS; ++part)
-            umma_bf16(dt, kmajor_sw128_desc(s_addr(sm.a[s][part]) + k * 32), bd,
+            umma_bf16(dt, kmajor_sw128_desc(smem_addr(sm.a[s][part]) + k * 32), bd,
                       (!first || k != 0 || part != 0) ? 1u : 0u);
         }
-        umma_commit(s_addr(&sm.empty[s]));
+        umma_commit(smem_addr(&sm.empty[s]));
         // the segment is complete once every MMA issued into it has finished
-        if (kb % kPfSegKB == kPfSegKB - 1 || kb == g.nk - 1) umma_commit(s_addr(&sm.acc_full[b]));
+        if (kb % kPfSegKB == kPfSegKB - 1 || kb == g.nk - 1) umma_commit(smem_addr(&sm.acc_full[b]));
       }
     }
   } else {
@@ -346,7 +322,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
     bool ok = true;
     for (int seg = 0; seg < nseg && ok; ++seg) {
       const int b = seg & 1;
-      ok = __all_sync(0xFFFFFFFFu, bar_wait(s_addr(&sm.acc_full[b]), (uint32_t)(seg >> 1) & 1u, g.timeout_ns));
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.acc_full[b]), (uint32_t)(seg >> 1) & 1u, g.timeout_ns));
       if (!ok) break;
       asm volatile("tcgen05.fence::after_thread_sync;");
 #pragma unroll
@@ -358,7 +334,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
       }
       asm volatile("tcgen05.fence::before_thread_sync;");
       __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s_addr(&sm.acc_empty[b])) : "memory");
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm.acc_empty[b])) : "memory");
     }
     if (!ok) {
       if (lane == 0) pf_timeout(g.status, SITE_PF_EPI);
@@ -422,26 +398,6 @@ __global__ void __launch_bounds__(256) prefill_norm_kernel(const float* x, int T
 
 // -------------------------------------------------------------- attention
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// d += a (16x16, row) * b (16x8, col)
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -504,7 +460,7 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
       const int p = blk * kPfKB + r;
       uint16_t* dst = (which ? vs : ks) + buf * kPfKB * RP + r * RP + c * 8;
       if (p < kv_end)
-        cp_async16(s_addr(dst), (which ? vbase : kbase) + (int64_t)p * HD + c * 8);
+        cp_async16(smem_addr(dst), (which ? vbase : kbase) + (int64_t)p * HD + c * 8);
       else   // past the filled cache: zeros (masked scores must meet finite values)
         *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
@@ -527,7 +483,7 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
       asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    const uint32_t kb_s = s_addr(ks + buf * kPfKB * RP), vb_s = s_addr(vs + buf * kPfKB * RP);
+    const uint32_t kb_s = smem_addr(ks + buf * kPfKB * RP), vb_s = smem_addr(vs + buf * kPfKB * RP);
 
     // S = Q K^T: 16 tokens x 64 positions, 8 tiles of 8 positions
     float s[8][4];
@@ -537,18 +493,18 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
     for (int k = 0; k < KS; ++k) {
       uint32_t qa_h[4], qa_l[4];
       const uint32_t qoff = (uint32_t)(((lane & 15) * RP + k * 16 + (lane >> 4) * 8) * 2);
-      ldsm_x4(s_addr(qh) + qoff, qa_h);
-      ldsm_x4(s_addr(ql) + qoff, qa_l);
+      ldsm_x4(smem_addr(qh) + qoff, qa_h);
+      ldsm_x4(smem_addr(ql) + qoff, qa_l);
 #pragma unroll
       for (int np = 0; np < 4; ++np) {
         const int mi = lane >> 3;
         const int key = (2 * np + (mi >> 1)) * 8 + (lane & 7);
         uint32_t kf[4];
         ldsm_x4(kb_s + (uint32_t)((key * RP + k * 16 + (mi & 1) * 8) * 2), kf);
-        mma16816(s[2 * np], qa_h, kf[0], kf[1]);
-        mma16816(s[2 * np], qa_l, kf[0], kf[1]);
-        mma16816(s[2 * np + 1], qa_h, kf[2], kf[3]);
-        mma16816(s[2 * np + 1], qa_l, kf[2], kf[3]);
+        mma_bf16_16816(s[2 * np], qa_h, kf[0], kf[1]);
+        mma_bf16_16816(s[2 * np], qa_l, kf[0], kf[1]);
+        mma_bf16_16816(s[2 * np + 1], qa_h, kf[2], kf[3]);
+        mma_bf16_16816(s[2 * np + 1], qa_l, kf[2], kf[3]);
       }
     }
     // causal mask, online softmax (rows gq and gq + 8 of the warp's tile)
@@ -602,10 +558,10 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
         const int key = kk * 16 + (mi & 1) * 8 + (lane & 7);
         uint32_t vf[4];
         ldsm_x4_trans(vb_s + (uint32_t)((key * RP + (2 * dp + (mi >> 1)) * 8) * 2), vf);
-        mma16816(o[2 * dp], pa_h, vf[0], vf[1]);
-        mma16816(o[2 * dp], pa_l, vf[0], vf[1]);
-        mma16816(o[2 * dp + 1], pa_h, vf[2], vf[3]);
-        mma16816(o[2 * dp + 1], pa_l, vf[2], vf[3]);
+        mma_bf16_16816(o[2 * dp], pa_h, vf[0], vf[1]);
+        mma_bf16_16816(o[2 * dp], pa_l, vf[0], vf[1]);
+        mma_bf16_16816(o[2 * dp + 1], pa_h, vf[2], vf[3]);
+        mma_bf16_16816(o[2 * dp + 1], pa_l, vf[2], vf[3]);
       }
     }
     __syncthreads();   // the buffer is reloaded two blocks on
