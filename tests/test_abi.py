@@ -102,6 +102,10 @@ def test_prefill_chunk_sizes_the_workspace(amk):
     assert (amk.amk_workspace_bytes(c8, amk.make_schedule_config(num_ctas=152)) ==
             amk.amk_workspace_bytes(c8, amk.make_schedule_config(num_ctas=152, prefill_chunk=-1)))
     assert amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152, prefill_chunk=-2)) == 0
+    # two or three bf16 parts per prefill activation (0: default); nothing else
+    for parts, ok in [(0, True), (2, True), (3, True), (1, False), (4, False), (-1, False)]:
+        ws = amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152, prefill_parts=parts))
+        assert (ws == dflt) if ok else (ws == 0)
 
 
 def test_host_argument_checks_need_no_gpu(amk):
