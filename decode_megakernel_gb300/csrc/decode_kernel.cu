@@ -566,25 +566,59 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float2 bf16x2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 
-// int8 byte i of (w ^ 0x80808080) placed under the exponent of 2^23: 2^23 + q + 128
-__device__ __forceinline__ float i8_biased(uint32_t w_xor80, int i) {
-  return __uint_as_float(__byte_perm(w_xor80, 0x4B000000u, 0x7440u | (uint32_t)i));
+// Two int8 codes held offset-binary (u = q + 128) in bytes 0, 1 (sel
+// 0x5140) or 2, 3 (sel 0x5342) of w, as an f16 pair of q: each byte goes
+// under the f16 exponent of 1024 (the value 1024 + u, exact), then 1152 is
+// subtracted (exact: |q| <= 128 needs 8 of f16's 11 significand bits).
+__device__ __forceinline__ uint32_t i8x2_f16(uint32_t w_ob, uint32_t sel) {
+  const uint32_t biased = __byte_perm(w_ob, 0x64646464u, sel);
+  const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&biased), __half2half2(__ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&q);
 }
-__device__ __forceinline__ float i8_at(uint32_t w_xor80, int i) {
-  return i8_biased(w_xor80, i) - 8388736.0f;
+__device__ __forceinline__ uint32_t i8x2_lo(uint32_t w_ob) { return i8x2_f16(w_ob, 0x5140u); }
+__device__ __forceinline__ uint32_t i8x2_hi(uint32_t w_ob) { return i8x2_f16(w_ob, 0x5342u); }
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
 }
 
-// int4 nibble i of w as float (exact)
-__device__ __forceinline__ float u4_at(uint32_t w, int i) {
-  return __uint_as_float(0x4B000000u | ((w >> (4 * i)) & 0xFu)) - 8388608.0f;
+// d += a (16x16, row) * b (16x8, col), f16 in, fp32 accumulate
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// int4 nibble i of w, left where it sits, under the exponent of 2^23:
-// 2^23 + q * 2^s with s = u4_shift(i); (value - 2^23) is exact.
-__device__ __forceinline__ constexpr int u4_shift(int i) { return i < 5 ? 4 * i : 4 * i - 12; }
-__device__ __forceinline__ float u4_biased(uint32_t w, uint32_t w_hi, int i) {
-  return i < 5 ? __uint_as_float(0x4B000000u | (w & (0xFu << (4 * i))))
-               : __uint_as_float(0x4B000000u | (w_hi & (0xFu << (4 * i - 12))));
+// One mma A fragment of int4 codes as f16 q - z (see pack_kernel): the
+// 32-bit word holds nibbles (row R, k, k+1) at bits 0-3 / 16-19, (R, k+2,
+// k+3) at 4-7 / 20-23, (R+2, k, k+1) at 8-11 / 24-27 and (R+2, k+2, k+3) at
+// 12-15 / 28-31.  A nibble pair masked in place under the f16 exponent of
+// 1024 reads 1024 + q (bits 0-3) or 1024 + 16 q (bits 4-7); then
+//   (1024 + q) - (1024 + z) = q - z,   (1024 + 16 q) / 16 - (64 + z) = q - z,
+// both exact in f16 (|q - z| <= 15).  zc0 / zc1: f16 pair of 1024 + z for row
+// R / R + 2, zf0 / zf1: f16 pair of -(64 + z).
+__device__ __forceinline__ void u4_fragment(uint32_t w, uint32_t zc0, uint32_t zf0, uint32_t zc1, uint32_t zf1,
+                                            uint32_t (&a)[4]) {
+  const __half2 sixteenth = __half2half2(__ushort_as_half(0x2C00));   // 1/16
+  const uint32_t w8 = w >> 8;
+  const uint32_t p0 = (w & 0x000F000Fu) | 0x64006400u, p2 = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t p1 = (w8 & 0x000F000Fu) | 0x64006400u, p3 = (w8 & 0x00F000F0u) | 0x64006400u;
+  const __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&p0), *reinterpret_cast<const __half2*>(&zc0));
+  const __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&p1), *reinterpret_cast<const __half2*>(&zc1));
+  const __half2 r2 = __hfma2(*reinterpret_cast<const __half2*>(&p2), sixteenth, *reinterpret_cast<const __half2*>(&zf0));
+  const __half2 r3 = __hfma2(*reinterpret_cast<const __half2*>(&p3), sixteenth, *reinterpret_cast<const __half2*>(&zf1));
+  a[0] = *reinterpret_cast<const uint32_t*>(&r0);
+  a[1] = *reinterpret_cast<const uint32_t*>(&r1);
+  a[2] = *reinterpret_cast<const uint32_t*>(&r2);
+  a[3] = *reinterpret_cast<const uint32_t*>(&r3);
+}
+// zero point z (0..15) as the pair constants of u4_fragment
+__device__ __forceinline__ uint32_t u4_zc(uint32_t z) { return __byte_perm(z, 0x64u, 0x4040u); }
+__device__ __forceinline__ uint32_t u4_zf(uint32_t zc) {
+  const __half2 r = __hsub2(__half2half2(__ushort_as_half(0x6380)), *reinterpret_cast<const __half2*>(&zc));   // 960 - (1024 + z)
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __device__ __forceinline__ float fp16_bits_to_float(uint16_t b) {
@@ -850,33 +884,72 @@ __device__ __forceinline__ float2 chunk_dot(uint32_t a, const float2 (&h)[4], fl
     acc = __ffma2_rn(bf16x2(w.w), h[3], acc);
     return acc;
   } else {
-    const uint2 w = lds64(a);
-    const uint32_t x = w.x ^ 0x80808080u, y = w.y ^ 0x80808080u;
-    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
-    acc = __ffma2_rn(__fadd2_rn(make_float2(i8_biased(x, 0), i8_biased(x, 1)), bias), h[0], acc);
-    acc = __ffma2_rn(__fadd2_rn(make_float2(i8_biased(x, 2), i8_biased(x, 3)), bias), h[1], acc);
-    acc = __ffma2_rn(__fadd2_rn(make_float2(i8_biased(y, 0), i8_biased(y, 1)), bias), h[2], acc);
-    acc = __ffma2_rn(__fadd2_rn(make_float2(i8_biased(y, 2), i8_biased(y, 3)), bias), h[3], acc);
+    static_assert(FMT == AMK_FORMAT_BF16, "int8 / int4 run on the tensor cores (act_fragments)");
     return acc;
   }
 }
 
-// int4 chunk: h holds act * 2^-s per element position (see u4_shift), hs the
-// chunk's plain sum; returns acc + s_g * (sum(q * act) - z_g * sum(act)).
-__device__ __forceinline__ float chunk_dot_u4(uint32_t a, uint32_t side_s, uint32_t side_z,
-                                              const float2 (&h)[4], float hs, float acc) {
-  const uint32_t w = lds32(a);
-  const float s = fp16_bits_to_float((uint16_t)lds16(side_s));
-  const float z = (float)lds8(side_z);
-  const uint32_t w_hi = w >> 12;
-  const float2 bias = make_float2(-8388608.0f, -8388608.0f);
-  float2 d = make_float2(0.f, 0.f);
+// int8 GEMV on the tensor cores (mma.sync m16n8k16, f16 in, fp32 accumulate).
+// An int8 tile is 8 rows x 2048 codes; warp w owns k [256w, 256w + 256) of
+// every tile, the same k its lanes hold as activation chunks (lane l:
+// 256w + 8l .. + 8).  Per k block j (0..3) of the warp and row half hf
+// (rows 4hf .. 4hf + 3) one mma computes D = A B with
+//   A row m = 4r + s  (r: row of the half, s = 0..3: which 16-k segment),
+//   A col kr          (position inside the segment),
+//   B col n = s' + 4p (s': segment, p: 0 = hi, 1 = lo f16 part of the act),
+// where segment s, position kr of lane-quad block j means
+//   k = 256w + 16 (4s + ((kr & 7) >> 1)) + 4j + (kr & 1) + 2 (kr >> 3).
+// Only D entries with s = s' are wanted; their sum over s and p is row r's
+// dot over the warp's 64 k of block j.  So lane (g, t) = (lane >> 2,
+// lane & 3) needs the 16 activations k = 256w + 16 (lane & 15) + 0..15 (as
+// hi parts in lanes 0..15, lo parts in lanes 16..31) and the 8 codes
+//   rows R = 4hf + (lane >> 4), R + 2;  k = 256w + 16 (lane & 15) + 4j + 0..3
+// stored in the tile as 16 bytes per (w, j, lane): row half 0 then 1, each
+// {W[R][k], W[R][k+1], W[R+2][k], W[R+2][k+1], W[R][k+2], W[R][k+3],
+//  W[R+2][k+2], W[R+2][k+3]} offset-binary (q + 128).
+// The activations are scaled by 2^-e (e from the warp's largest |act|, so
+// that the hi part stays in f16 range and the lo part clear of f16
+// underflow); hi + lo keep 22 significant bits.  Returns 2^e.
+template <int NKT>
+__device__ __forceinline__ float act_fragments(const float2 (&h)[NKT][4], uint32_t (&b)[NKT][4][2], float* stage,
+                                              int lane) {
+  float mx = 0.f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 q = __fadd2_rn(make_float2(u4_biased(w, w_hi, 2 * i), u4_biased(w, w_hi, 2 * i + 1)), bias);
-    d = __ffma2_rn(q, h[i], d);
+  for (int kt = 0; kt < NKT; ++kt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fmaxf(fabsf(h[kt][i].x), fabsf(h[kt][i].y)));
+#pragma unroll
+  for (int msk = 16; msk >= 1; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, msk));
+  // max * 2^-e in [2^14, 2^15); finite inputs only (a NaN or inf propagates)
+  int e = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127 - 14 : 0;
+  e = max(-126, min(126, e));
+  const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+  const bool lo_part = lane >= 16;
+  float4* st = reinterpret_cast<float4*>(stage);
+  const float4* src = st + (lane & 15) * 4;
+#pragma unroll
+  for (int kt = 0; kt < NKT; ++kt) {
+    st[2 * lane] = make_float4(h[kt][0].x, h[kt][0].y, h[kt][1].x, h[kt][1].y);
+    st[2 * lane + 1] = make_float4(h[kt][2].x, h[kt][2].y, h[kt][3].x, h[kt][3].y);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 v = src[j];
+      const float x[4] = {v.x * down, v.y * down, v.z * down, v.w * down};
+      uint32_t r[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const __half2 hi = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);   // exact difference
+        r[i] = lo_part ? *reinterpret_cast<const uint32_t*>(&lo) : *reinterpret_cast<const uint32_t*>(&hi);
+      }
+      b[kt][j][0] = r[0];
+      b[kt][j][1] = r[1];
+    }
+    __syncwarp();
   }
-  return fmaf(s, fmaf(-z, hs, d.x + d.y), acc);
+  return __uint_as_float((uint32_t)(127 + e) << 23);
 }
 
 
@@ -946,42 +1019,150 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
     else
       resid_w = ld_relaxed(resid_src);
   }
-  float hs[NKT];  // int4: per-chunk activation sums, then activations pre-scaled by 2^-s
-  if constexpr (FMT == AMK_FORMAT_INT4) {
-#pragma unroll
-    for (int kt = 0; kt < NKT; ++kt) {
-      hs[kt] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        hs[kt] += h[kt][i].x + h[kt][i].y;
-        h[kt][i].x *= 1.0f / (float)(1 << u4_shift(2 * i));        // exact: power of two
-        h[kt][i].y *= 1.0f / (float)(1 << u4_shift(2 * i + 1));
-      }
-    }
-  }
+  // int8 / int4: the activations as mma B fragments (staged through this
+  // warp's slice of the scratch above the row partials), scaled by 1 / act_up
+  constexpr bool kMma = FMT != AMK_FORMAT_BF16;
+  uint32_t bq[kMma ? NKT : 1][4][2];
+  float act_up = 1.f;
+  if constexpr (kMma) act_up = act_fragments<NKT>(h, bq, sm.scratch + kActStageOffset + warp * 256, lane);
 
   const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
   const uint32_t full0 = smem_addr(&sm.full[0]);
   const uint32_t empty0 = smem_addr(&sm.empty[0]);
   const uint32_t off0 = (uint32_t)(((rsub << cs) + chunk) * EB);   // pass 0 chunk
   const uint32_t pass_stride = (uint32_t)((rpp << cs) * EB);       // rows between passes
-  // int4 side data: fp16 scales [Rt][Kt/128] then u8 zeros [Rt][Kt/128]
-  const int ngt = M.Kt >> 7;
-  const uint32_t side_s0 = kStageBytes + (uint32_t)((rsub * ngt + (chunk >> 4)) * 2);
-  const uint32_t side_z0 = kStageBytes + (uint32_t)(M.Rt * ngt * 2 + rsub * ngt + (chunk >> 4));
   const uint32_t nslots = (uint32_t)m.ring_slots;
   uint32_t slot = (uint32_t)stage % nslots, phase = ((uint32_t)stage / nslots) & 1u;
   int64_t starved = 0;
 
   float* red = sm.scratch;
   const int nrb = t.a1 - t.a0;
-  for (int rb = 0; rb < nrb; ++rb) {
-    float2 acc2[FMT == AMK_FORMAT_INT4 ? 1 : P];
-    float acc1[FMT == AMK_FORMAT_INT4 ? P : 1];
+  if constexpr (FMT == AMK_FORMAT_INT8) {
+    // D entries this lane keeps (see act_fragments): segment of row m = g is
+    // g & 3; column 2t (+1 when that segment is odd) has the same segment
+    // when t & 1 == (g & 3) >> 1
+    const int sg = (lane >> 2) & 3;
+    const bool keep = (lane & 1) == (sg >> 1);
+    const bool odd = (sg & 1) != 0;
+    const uint32_t unit0 = (uint32_t)(warp * 4 * 32 + lane) * 16;
+    for (int rb = 0; rb < nrb; ++rb) {
+      float d[2][2][4];   // [row half][k block parity][fragment]
 #pragma unroll
-    for (int i = 0; i < (FMT == AMK_FORMAT_INT4 ? 1 : P); ++i) acc2[i] = make_float2(0.f, 0.f);
+      for (int a = 0; a < 2; ++a)
 #pragma unroll
-    for (int i = 0; i < (FMT == AMK_FORMAT_INT4 ? P : 1); ++i) acc1[i] = 0.f;
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) d[a][c][e] = 0.f;
+#pragma unroll
+      for (int kt = 0; kt < NKT; ++kt) {
+        if (!failed)
+          failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
+        if (!failed) {
+          const uint32_t tile = ring0 + slot * kSlotBytes + unit0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = lds128(tile + (uint32_t)j * 512u);
+            mma_f16_16816(d[0][j & 1], i8x2_lo(v.x), i8x2_hi(v.x), i8x2_lo(v.y), i8x2_hi(v.y), bq[kt][j][0],
+                          bq[kt][j][1]);
+            mma_f16_16816(d[1][j & 1], i8x2_lo(v.z), i8x2_hi(v.z), i8x2_lo(v.w), i8x2_hi(v.w), bq[kt][j][0],
+                          bq[kt][j][1]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive32(empty0 + slot * 8);
+        if (++slot == nslots) { slot = 0; phase ^= 1u; }
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float e0 = odd ? d[hf][0][1] + d[hf][1][1] : d[hf][0][0] + d[hf][1][0];
+        const float e2 = odd ? d[hf][0][3] + d[hf][1][3] : d[hf][0][2] + d[hf][1][2];
+        float v0 = keep ? e0 : 0.f;   // row 4 hf + (lane >> 4)
+        float v1 = keep ? e2 : 0.f;   // row 4 hf + (lane >> 4) + 2
+#pragma unroll
+        for (int msk = 1; msk < 16; msk <<= 1) {
+          v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, msk);
+          v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, msk);
+        }
+        if ((lane & 15) == 0) {
+          const int r = rb * 8 + 4 * hf + (lane >> 4);
+          red[r * 8 + warp] = v0 * act_up;
+          red[(r + 2) * 8 + warp] = v1 * act_up;
+        }
+      }
+    }
+  } else if constexpr (FMT == AMK_FORMAT_INT4) {
+    // 16 rows x 2048 codes per tile: per k block j the lane's 16 bytes hold
+    // one A word per row quarter q (rows 4q .. 4q + 3).  A lane's codes (and
+    // the D entries it keeps) all lie in its segment sg, i.e. at k in
+    // [256w + 64 sg, + 64) of every tile: quantisation group 2w + (sg >> 1)
+    // of the tile, so one zero point and one scale per row serve all four
+    // k blocks.  Side data: fp16 scales [16][16], then u8 zeros [16][16].
+    const int sg = (lane >> 2) & 3;
+    const bool keep = (lane & 1) == (sg >> 1);
+    const bool odd = (sg & 1) != 0;
+    const uint32_t unit0 = (uint32_t)(warp * 4 * 32 + lane) * 16;
+    const int rl = lane >> 4;                 // row R = 4q + rl, and R + 2
+    const int gq = 2 * warp + (sg >> 1);      // the lane's group in every tile
+    for (int rb = 0; rb < nrb; ++rb) {
+      float acc[4][2];   // [q][R, R + 2], scaled by the group scales
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0.f;
+#pragma unroll
+      for (int kt = 0; kt < NKT; ++kt) {
+        if (!failed)
+          failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
+        if (!failed) {
+          const uint32_t tile = ring0 + slot * kSlotBytes;
+          const uint32_t side = tile + kStageBytes;
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = lds128(tile + unit0 + (uint32_t)j * 512u);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int R = 4 * q + rl;
+            const uint32_t zc0 = u4_zc(lds8(side + 512u + (uint32_t)(R * 16 + gq)));
+            const uint32_t zc1 = u4_zc(lds8(side + 512u + (uint32_t)((R + 2) * 16 + gq)));
+            const float s0 = fp16_bits_to_float((uint16_t)lds16(side + (uint32_t)(R * 16 + gq) * 2));
+            const float s1 = fp16_bits_to_float((uint16_t)lds16(side + (uint32_t)((R + 2) * 16 + gq) * 2));
+            const uint32_t zf0 = u4_zf(zc0), zf1 = u4_zf(zc1);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t w = q == 0 ? v[j].x : q == 1 ? v[j].y : q == 2 ? v[j].z : v[j].w;
+              uint32_t a[4];
+              u4_fragment(w, zc0, zf0, zc1, zf1, a);
+              mma_f16_16816(d, a[0], a[1], a[2], a[3], bq[kt][j][0], bq[kt][j][1]);
+            }
+            const float e0 = keep ? (odd ? d[1] : d[0]) : 0.f;
+            const float e2 = keep ? (odd ? d[3] : d[2]) : 0.f;
+            acc[q][0] = fmaf(s0, e0, acc[q][0]);
+            acc[q][1] = fmaf(s1, e2, acc[q][1]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive32(empty0 + slot * 8);
+        if (++slot == nslots) { slot = 0; phase ^= 1u; }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float v0 = acc[q][0], v1 = acc[q][1];
+#pragma unroll
+        for (int msk = 1; msk < 16; msk <<= 1) {
+          v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, msk);
+          v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, msk);
+        }
+        if ((lane & 15) == 0) {
+          const int r = rb * 16 + 4 * q + rl;
+          red[r * 8 + warp] = v0 * act_up;
+          red[(r + 2) * 8 + warp] = v1 * act_up;
+        }
+      }
+    }
+  } else
+  for (int rb = 0; rb < nrb; ++rb) {   // bf16: packed FMA
+    float2 acc2[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) acc2[i] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int kt = 0; kt < NKT; ++kt) {
       if (!failed)
@@ -989,15 +1170,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
       if (!failed) {
         const uint32_t tile = ring0 + slot * kSlotBytes;
 #pragma unroll
-        for (int ps = 0; ps < P; ++ps) {
-          if constexpr (FMT == AMK_FORMAT_INT4)
-            acc1[ps] = chunk_dot_u4(tile + off0 + ps * pass_stride,
-                                    tile + side_s0 + (uint32_t)(ps * rpp * ngt * 2),
-                                    tile + side_z0 + (uint32_t)(ps * rpp * ngt), h[kt], hs[kt],
-                                    acc1[ps]);
-          else
-            acc2[ps] = chunk_dot<FMT>(tile + off0 + ps * pass_stride, h[kt], acc2[ps]);
-        }
+        for (int ps = 0; ps < P; ++ps) acc2[ps] = chunk_dot<FMT>(tile + off0 + ps * pass_stride, h[kt], acc2[ps]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive32(empty0 + slot * 8);
@@ -1005,10 +1178,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
     }
     float v[P];
 #pragma unroll
-    for (int i = 0; i < P; ++i) {
-      if constexpr (FMT == AMK_FORMAT_INT4) v[i] = acc1[i];
-      else v[i] = acc2[i].x + acc2[i].y;
-    }
+    for (int i = 0; i < P; ++i) v[i] = acc2[i].x + acc2[i].y;
     const float tot = transpose_reduce<P>(v, lane);
     constexpr int kLaneStride = 32 / P;
     if ((lane & (kLaneStride - 1)) == 0) {
@@ -1698,10 +1868,89 @@ __device__ int pack_source(const PackArgs& a, int pr, int* row) {
   return 0;
 }
 
+// int8 code of physical row pr at k, offset-binary (q + 128); padding is q = 0
+__device__ __forceinline__ uint32_t pack_i8_code(const PackArgs& a, int pr, int k) {
+  int row = 0;
+  const int src = pack_source(a, pr, &row);
+  const int8_t q = (src >= 0 && k < a.dst.K) ? static_cast<const int8_t*>(a.w[src])[(int64_t)row * a.dst.K + k] : 0;
+  return (uint32_t)(uint8_t)q ^ 0x80u;
+}
+
 __global__ void pack_kernel(const PackArgs a) {
   const DevMat& M = a.dst;
   const int chunks = M.Kp / 8;
   const int64_t total = (int64_t)M.rows_padded * chunks;
+  if (a.fmt == AMK_FORMAT_INT8) {
+    // tensor-core fragment order (act_fragments): 8-byte units
+    // ((w * 4 + j) * 32 + lane) * 2 + hf of each 8 x 2048 tile
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+      if (idx < M.rows_padded) {
+        int row = 0;
+        const int src = pack_source(a, (int)idx, &row);
+        a.scales_dst[idx] = src >= 0 ? static_cast<const uint16_t*>(a.s[src])[row] : (uint16_t)0;
+      }
+      const int64_t per_rb = (int64_t)M.nkt * 2048;
+      const int rb = (int)(idx / per_rb);
+      const int rem = (int)(idx % per_rb);
+      const int kt = rem / 2048, u = rem % 2048;
+      const int hf = u & 1, lane = (u >> 1) & 31, j = (u >> 6) & 3, w = u >> 8;
+      const int pr0 = rb * 8 + 4 * hf + (lane >> 4), pr1 = pr0 + 2;
+      const int k0 = kt * 2048 + 256 * w + 16 * (lane & 15) + 4 * j;
+      const uint32_t lo = pack_i8_code(a, pr0, k0) | pack_i8_code(a, pr0, k0 + 1) << 8 |
+                          pack_i8_code(a, pr1, k0) << 16 | pack_i8_code(a, pr1, k0 + 1) << 24;
+      const uint32_t hi = pack_i8_code(a, pr0, k0 + 2) | pack_i8_code(a, pr0, k0 + 3) << 8 |
+                          pack_i8_code(a, pr1, k0 + 2) << 16 | pack_i8_code(a, pr1, k0 + 3) << 24;
+      uint8_t* tile = const_cast<uint8_t*>(M.base) + ((int64_t)rb * M.nkt + kt) * M.stage_bytes;
+      *reinterpret_cast<uint2*>(tile + (int64_t)u * 8) = make_uint2(lo, hi);
+    }
+    return;
+  }
+  if (a.fmt == AMK_FORMAT_INT4) {
+    // tensor-core fragment order (gemv_task, u4_fragment): 32-bit words
+    // ((w * 4 + j) * 32 + lane) * 4 + rq of each 16 x 2048 tile, then the
+    // side data: fp16 scales [16][16], u8 zeros [16][16] per tile
+    const int ng_pad = M.Kp / 128;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+      if (idx < (int64_t)M.rows_padded * ng_pad) {
+        const int pr = (int)(idx / ng_pad), gg = (int)(idx % ng_pad);
+        int row = 0;
+        const int src = pack_source(a, pr, &row);
+        uint16_t sc = 0;
+        uint8_t zz = 0;
+        if (src >= 0 && gg * 128 < M.K) {
+          const int ng = M.K / 128, zb = (ng + 1) / 2;
+          sc = static_cast<const uint16_t*>(a.s[src])[(int64_t)row * ng + gg];
+          const uint8_t zbyte = static_cast<const uint8_t*>(a.z[src])[(int64_t)row * zb + gg / 2];
+          zz = (gg & 1) ? (zbyte >> 4) : (zbyte & 15);
+        }
+        uint8_t* side = const_cast<uint8_t*>(M.base) + ((int64_t)(pr / 16) * M.nkt + gg / 16) * M.stage_bytes + kStageBytes;
+        reinterpret_cast<uint16_t*>(side)[(pr % 16) * 16 + gg % 16] = sc;
+        side[512 + (pr % 16) * 16 + gg % 16] = zz;
+      }
+      const int64_t per_rb = (int64_t)M.nkt * 4096;
+      const int rb = (int)(idx / per_rb);
+      const int rem = (int)(idx % per_rb);
+      const int kt = rem / 4096, u = rem % 4096;
+      const int rq = u & 3, lane = (u >> 2) & 31, j = (u >> 7) & 3, w = u >> 9;
+      const int pr0 = rb * 16 + 4 * rq + (lane >> 4), pr1 = pr0 + 2;
+      const int k0 = kt * 2048 + 256 * w + 16 * (lane & 15) + 4 * j;
+      auto nib = [&](int pr, int k) -> uint32_t {
+        int row = 0;
+        const int src = pack_source(a, pr, &row);
+        if (src < 0 || k >= M.K) return 0u;
+        const uint8_t b = static_cast<const uint8_t*>(a.w[src])[(int64_t)row * (M.K / 2) + k / 2];
+        return (k & 1) ? (uint32_t)(b >> 4) : (uint32_t)(b & 15);
+      };
+      const uint32_t word = nib(pr0, k0) | nib(pr0, k0 + 2) << 4 | nib(pr1, k0) << 8 | nib(pr1, k0 + 2) << 12 |
+                            nib(pr0, k0 + 1) << 16 | nib(pr0, k0 + 3) << 20 | nib(pr1, k0 + 1) << 24 |
+                            nib(pr1, k0 + 3) << 28;
+      uint8_t* tile = const_cast<uint8_t*>(M.base) + ((int64_t)rb * M.nkt + kt) * M.stage_bytes;
+      *reinterpret_cast<uint32_t*>(tile + (int64_t)u * 4) = word;
+    }
+    return;
+  }
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int pr = (int)(idx / chunks);
@@ -1717,32 +1966,6 @@ __global__ void pack_kernel(const PackArgs a) {
       if (live) v = *reinterpret_cast<const uint4*>(
                     static_cast<const uint16_t*>(a.w[src]) + (int64_t)row * M.K + k);
       *reinterpret_cast<uint4*>(tile + ((int64_t)r * M.Kt + kk) * 2) = v;
-    } else if (a.fmt == AMK_FORMAT_INT8) {
-      uint2 v = make_uint2(0, 0);
-      if (live) v = *reinterpret_cast<const uint2*>(
-                    static_cast<const int8_t*>(a.w[src]) + (int64_t)row * M.K + k);
-      *reinterpret_cast<uint2*>(tile + (int64_t)r * M.Kt + kk) = v;
-      if (c == 0)
-        a.scales_dst[pr] = src >= 0 ? static_cast<const uint16_t*>(a.s[src])[row] : (uint16_t)0;
-    } else {
-      uint32_t v = 0;
-      if (live) v = *reinterpret_cast<const uint32_t*>(
-                    static_cast<const uint8_t*>(a.w[src]) + (int64_t)row * (M.K / 2) + k / 2);
-      *reinterpret_cast<uint32_t*>(tile + ((int64_t)r * M.Kt + kk) / 2) = v;
-      if ((kk & 127) == 0) {
-        const int ngt = M.Kt >> 7, gl = kk >> 7, gg = k >> 7;
-        uint16_t sc = 0;
-        uint8_t zz = 0;
-        if (live) {
-          const int ng = M.K / 128, zb = (ng + 1) / 2;
-          sc = static_cast<const uint16_t*>(a.s[src])[(int64_t)row * ng + gg];
-          const uint8_t zbyte = static_cast<const uint8_t*>(a.z[src])[(int64_t)row * zb + gg / 2];
-          zz = (gg & 1) ? (zbyte >> 4) : (zbyte & 15);
-        }
-        uint8_t* side = tile + kStageBytes;
-        reinterpret_cast<uint16_t*>(side)[r * ngt + gl] = sc;
-        side[M.Rt * ngt * 2 + r * ngt + gl] = zz;
-      }
     }
   }
 }
@@ -1818,16 +2041,30 @@ __global__ void dequant_kernel(int fmt, const void* w, const void* scales, const
     } else if (fmt == AMK_FORMAT_INT8) {
       const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const int8_t*>(w) + (int64_t)r * K + k);
       const float s = fp16_bits_to_float(static_cast<const uint16_t*>(scales)[r]);
-      const uint32_t a = v.x ^ 0x80808080u, b = v.y ^ 0x80808080u;
-      for (int i = 0; i < 4; ++i) o[i] = i8_at(a, i) * s;
-      for (int i = 0; i < 4; ++i) o[4 + i] = i8_at(b, i) * s;
+      const uint32_t a = v.x ^ 0x80808080u, b = v.y ^ 0x80808080u;   // offset-binary, as packed
+      const float2 q[4] = {f16x2_to_float2(i8x2_lo(a)), f16x2_to_float2(i8x2_hi(a)),
+                           f16x2_to_float2(i8x2_lo(b)), f16x2_to_float2(i8x2_hi(b))};
+      for (int i = 0; i < 4; ++i) {
+        o[2 * i] = q[i].x * s;
+        o[2 * i + 1] = q[i].y * s;
+      }
     } else {
       const uint32_t v = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(w) + (int64_t)r * (K / 2) + k / 2);
       const int ng = K / 128, zb = (ng + 1) / 2, g = k / 128;
       const float s = fp16_bits_to_float(static_cast<const uint16_t*>(scales)[(int64_t)r * ng + g]);
       const uint8_t zbyte = static_cast<const uint8_t*>(zeros)[(int64_t)r * zb + g / 2];
-      const float z = (float)((g & 1) ? (zbyte >> 4) : (zbyte & 15));
-      for (int i = 0; i < 8; ++i) o[i] = (u4_at(v, i) - z) * s;
+      const uint32_t zc = u4_zc((g & 1) ? (zbyte >> 4) : (zbyte & 15u)), zf = u4_zf(zc);
+      // codes k .. k+7 (low nibble = even k) rearranged into one fragment
+      // word: its "row R" takes k .. k+3, its "row R + 2" k+4 .. k+7
+      auto nb = [&](int i) { return (v >> (4 * i)) & 15u; };
+      const uint32_t word = nb(0) | nb(2) << 4 | nb(4) << 8 | nb(6) << 12 | nb(1) << 16 | nb(3) << 20 |
+                            nb(5) << 24 | nb(7) << 28;
+      uint32_t q[4];
+      u4_fragment(word, zc, zf, zc, zf, q);
+      const float2 f0 = f16x2_to_float2(q[0]), f2 = f16x2_to_float2(q[2]);   // k, k+1 / k+2, k+3
+      const float2 f1 = f16x2_to_float2(q[1]), f3 = f16x2_to_float2(q[3]);   // k+4, k+5 / k+6, k+7
+      o[0] = f0.x * s; o[1] = f0.y * s; o[2] = f2.x * s; o[3] = f2.y * s;
+      o[4] = f1.x * s; o[5] = f1.y * s; o[6] = f3.x * s; o[7] = f3.y * s;
     }
   }
 }

@@ -120,6 +120,10 @@ constexpr int kWeightSlots = 8;                        // 136 KB: 16 KB tiles + 
 constexpr int kKvSlots = 4;                            // 64 KB: K then V of up to 32 (hd 128) positions each
 constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one weight slot
 constexpr int kScratchFloats = 4608;                   // GEMV row partials / attention merge
+// int8 / int4 GEMV tasks stage each warp's activations (256 floats) above the row
+// partials, which take at most kRowsMax rows x 8 warps
+constexpr int kActStageOffset = kRowsMax * kConsumerWarps;
+static_assert(kActStageOffset + kConsumerWarps * 256 <= kScratchFloats, "activation staging");
 constexpr int kSmemBytes = kWeightSlots * kSlotBytes + kKvSlots * kStageBytes + kScratchFloats * 4 +
                            2 * (kWeightSlots + kKvSlots) * 8 + 256;
 

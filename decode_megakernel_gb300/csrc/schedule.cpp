@@ -30,10 +30,14 @@ bool plan_matrix(int fmt, int rows, int K, MatGeom* m, std::string* why, const c
     return false;
   }
   // Kt: tile width.  A consumer thread owns one 8-element chunk of every
-  // K tile, so it keeps 8 * nkt activation floats in registers.
+  // K tile, so it keeps 8 * nkt activation floats in registers.  int8 and
+  // int4 tiles (8 or 16 rows x 2048 codes) are in tensor-core fragment order
+  // with each warp owning 256 k of every tile, so they take Kt = 2048
+  // whatever K is.
   int best_kt = 0;
   int64_t best_kp = 0;
   for (int kt : {2048, 1024, 512, 256}) {
+    if (fmt != AMK_FORMAT_BF16 && kt != 2048) continue;
     int64_t kp = round_up(K, kt);
     if (kp / kt * 8 > kMaxHReg) continue;
     if (best_kt == 0 || kp < best_kp) {
