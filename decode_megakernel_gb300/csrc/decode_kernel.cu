@@ -173,13 +173,10 @@ __device__ __forceinline__ bool consumer_sync_or(bool pred) {
 // ------------------------------------------------------------ shared memory
 
 struct Smem {
-  uint8_t ring[kWeightSlots][kSlotBytes];   // weight tiles of GEMV tasks
-  uint8_t kv[kKvSlots][kStageBytes];        // K then V history tiles of attention tasks
+  uint8_t pool[kPoolSlots][kSlotBytes];     // weight ring [0, ring_slots), then the KV ring
   float scratch[kScratchFloats];
-  uint64_t full[kWeightSlots];
-  uint64_t empty[kWeightSlots];
-  uint64_t kfull[kKvSlots];
-  uint64_t kempty[kKvSlots];
+  uint64_t full[kPoolSlots];
+  uint64_t empty[kPoolSlots];
   float misc[32];
   int32_t abort_flag;
   int32_t cur_task;   // queue index of the consumers' current task (read by the producer)
@@ -401,6 +398,7 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
   const uint64_t pol_kv = policy_evict_normal();
   volatile int32_t* abort_flag = &sm.abort_flag;
   const uint32_t wslots = (uint32_t)m.ring_slots;
+  const uint32_t kvslots = (uint32_t)kPoolSlots - wslots;
   RingCursor w, a;
   bool ok = true;
   uint64_t wait_t0 = 0;
@@ -441,12 +439,13 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       c.valid = false;
       return true;
     }
-    uint64_t* empty = kv ? &sm.kempty[c.slot] : &sm.empty[c.slot];
+    const uint32_t ps = kv ? wslots + c.slot : c.slot;   // pool slot
+    uint64_t* empty = &sm.empty[ps];
     if (!mbar_test_wait(empty, c.phase ^ 1u)) {
       *blocked = true;
       return false;
     }
-    uint64_t* full = kv ? &sm.kfull[c.slot] : &sm.full[c.slot];
+    uint64_t* full = &sm.full[ps];
     if (kv) {
       // K then V of positions [p0, p0 + pps): boxes of 64 dims x pps rows,
       // 128-byte swizzled (rows past the split are loaded too and masked)
@@ -454,18 +453,18 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       const int nbox = m.head_dim / 64;
       mbar_arrive_expect_tx(full, kStageBytes);
       for (int b = 0; b < nbox; ++b) {
-        tma_load_2d(sm.kv[c.slot] + b * c.tt.pps * 128, &m.kv_map, 64 * b, c.tt.rk + p0, full, pol_kv);
-        tma_load_2d(sm.kv[c.slot] + kStageBytes / 2 + b * c.tt.pps * 128, &m.kv_map, 64 * b,
+        tma_load_2d(sm.pool[ps] + b * c.tt.pps * 128, &m.kv_map, 64 * b, c.tt.rk + p0, full, pol_kv);
+        tma_load_2d(sm.pool[ps] + kStageBytes / 2 + b * c.tt.pps * 128, &m.kv_map, 64 * b,
                     c.tt.rv + p0, full, pol_kv);
       }
     } else {
       mbar_arrive_expect_tx(full, c.tt.bytes);
-      bulk_copy_g2s(sm.ring[c.slot], c.tt.k + (int64_t)c.tile * c.tt.stride, c.tt.bytes, full, pol_w);
+      bulk_copy_g2s(sm.pool[ps], c.tt.k + (int64_t)c.tile * c.tt.stride, c.tt.bytes, full, pol_w);
       ++w_seq;
     }
     c.issued |= 1u << c.slot;
     c.parity = (c.parity & ~(1u << c.slot)) | (c.phase << c.slot);
-    if (++c.slot == (kv ? (uint32_t)kKvSlots : wslots)) {
+    if (++c.slot == (kv ? kvslots : wslots)) {
       c.slot = 0;
       c.phase ^= 1u;
     }
@@ -531,7 +530,7 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       break;
     }
     if (wb) mbar_try_wait_hint(&sm.empty[w.slot], w.phase ^ 1u, 200);
-    else if (ab) mbar_try_wait_hint(&sm.kempty[a.slot], a.phase ^ 1u, 200);
+    else if (ab) mbar_try_wait_hint(&sm.empty[wslots + a.slot], a.phase ^ 1u, 200);
     if (p.trace) {
       const int64_t dt = (int64_t)(global_timer() - now);
       if (wb) w.blocked += dt;
@@ -555,8 +554,8 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       }
     }
   };
-  drain(w, sm.full, kWeightSlots);
-  drain(a, sm.kfull, kKvSlots);
+  drain(w, sm.full, (int)wslots);
+  drain(a, sm.full + wslots, (int)kvslots);
 }
 
 // -------------------------------------------------------------- consumers
@@ -1026,7 +1025,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   float act_up = 1.f;
   if constexpr (kMma) act_up = act_fragments<NKT>(h, bq, sm.scratch + kActStageOffset + warp * 256, lane);
 
-  const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
+  const uint32_t ring0 = smem_addr(&sm.pool[0][0]);
   const uint32_t full0 = smem_addr(&sm.full[0]);
   const uint32_t empty0 = smem_addr(&sm.empty[0]);
   const uint32_t off0 = (uint32_t)(((rsub << cs) + chunk) * EB);   // pass 0 chunk
@@ -1294,7 +1293,7 @@ __device__ __forceinline__ int gemv_dispatch(const StepParams& p, Smem& sm, cons
 // Split-K GQA attention of one KV head over one context split (positions
 // [t0, t1) of the cache, plus the step's own position for the last split),
 // on the tensor cores.  The K,V history arrives through the KV ring in
-// 128-byte-swizzled boxes; a chunk of up to kKvSlots resident stages is
+// 128-byte-swizzled boxes; a chunk of up to kKvChunkStages resident stages is
 // split into runs of 16 (hd 128) or 32 (hd 64) positions, one per warp.
 // Per 16 positions a warp computes
 //   S^T [16 positions x 8 heads] = K [16 x hd] . Q^T [hd x 8]    (hd/16 mma pairs)
@@ -1309,7 +1308,7 @@ template <int HD, int G>
 __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTask t, int kstage,
                                       uint32_t task_idx, int64_t* tr) {
   constexpr int PPS = (kStageBytes / 2) / (HD * 2);   // cached positions per KV stage
-  constexpr int CP = kKvSlots * PPS;                  // positions per chunk at most
+  constexpr int CP = kKvChunkStages * PPS;            // positions per chunk at most
   constexpr int RUN = CP / kConsumerWarps;            // positions of a warp's run at most
   constexpr int MT = RUN / 16;                        // 16-position tiles per run
   constexpr int KS = HD / 16;                         // k-steps (QK) and dim tiles (PV)
@@ -1385,17 +1384,18 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[k2][e] = 0.f;
 
-  const uint32_t kv0 = smem_addr(&sm.kv[0][0]);
+  const uint32_t kvs = (uint32_t)(kPoolSlots - m.ring_slots);   // KV ring slots (>= kKvChunkStages)
+  const uint32_t kv0 = smem_addr(&sm.pool[m.ring_slots][0]);
   const uint32_t cur0 = smem_addr(cur);
-  const uint32_t kfull0 = smem_addr(&sm.kfull[0]);
-  const uint32_t kempty0 = smem_addr(&sm.kempty[0]);
+  const uint32_t kfull0 = smem_addr(&sm.full[m.ring_slots]);
+  const uint32_t kempty0 = smem_addr(&sm.empty[m.ring_slots]);
   int64_t starved = 0;
   int t0, t1;
   attn_range(p.pos, m.splits, j, &t0, &t1);
   const int ncached = t1 - t0;
   const int ntotal = ncached + (last ? 1 : 0);
   const int nst = (ncached + PPS - 1) / PPS;
-  uint32_t kslot = (uint32_t)kstage % kKvSlots, kphase = ((uint32_t)kstage / kKvSlots) & 1u;
+  uint32_t kslot = (uint32_t)kstage % kvs, kphase = ((uint32_t)kstage / kvs) & 1u;
 
   for (int c0 = 0; c0 < ntotal; c0 += CP) {
     const int len = min(CP, ntotal - c0);
@@ -1416,16 +1416,16 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
       const bool mine = s2 * PPS <= clast && (s2 + 1) * PPS > cfirst;
       if (!failed && mine)
         failed = !wait_full(kfull0 + kslot * 8, kphase, p, abort_flag, task_idx, tr ? &starved : nullptr);
-      if (++kslot == (uint32_t)kKvSlots) { kslot = 0; kphase ^= 1u; }
+      if (++kslot == kvs) { kslot = 0; kphase ^= 1u; }
     }
     // shared address of 16-byte chunk c (8 dims) of K (kv = 0) or V (kv = 1)
     // of task position pi: a swizzled ring row, or the step's own k / v
     auto addr_of = [&](int pi, int c, int kv) -> uint32_t {
       if (pi >= ncached) return cur0 + (uint32_t)(kv * HD * 2 + c * 16);
       uint32_t slot = slot0 + (uint32_t)(pi / PPS - s_begin);
-      if (slot >= (uint32_t)kKvSlots) slot -= kKvSlots;
+      if (slot >= kvs) slot -= kvs;
       const int r = pi % PPS;
-      return kv0 + slot * kStageBytes + (uint32_t)(kv * (kStageBytes / 2) + (c >> 3) * (PPS * 128) + r * 128 +
+      return kv0 + slot * kSlotBytes + (uint32_t)(kv * (kStageBytes / 2) + (c >> 3) * (PPS * 128) + r * 128 +
                                                    (((c & 7) ^ (r & 7)) << 4));
     };
     if (!failed && n > 0) {
@@ -1525,7 +1525,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
       uint32_t sl = slot0;
       for (int s2 = s_begin; s2 < s_end; ++s2) {
         mbar_arrive32(kempty0 + sl * 8);
-        if (++sl == (uint32_t)kKvSlots) sl = 0;
+        if (++sl == kvs) sl = 0;
       }
     }
   }
@@ -1748,16 +1748,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
   if (tid == 0) {
-    for (int s = 0; s < kWeightSlots; ++s) {
+    for (int s = 0; s < kPoolSlots; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
-    for (int s = 0; s < kKvSlots; ++s) {
-      mbar_init(&sm.kfull[s], 1);
-      mbar_init(&sm.kempty[s], kConsumerWarps);
-    }
-    // the swizzled KV boxes need 1 KB alignment: refuse to run without it
-    sm.abort_flag = (smem_addr(&sm.kv[0][0]) & 1023u) ? 1 : 0;
+    // the swizzled KV boxes need 1 KB alignment (slots are 17 KB apart):
+    // refuse to run without it
+    static_assert(kSlotBytes % 1024 == 0, "KV slot alignment");
+    sm.abort_flag = (smem_addr(&sm.pool[0][0]) & 1023u) ? 1 : 0;
     if (sm.abort_flag) set_status(p.m.status, ST_CHECK, 0xFFFFFFFFu, SITE_SMEM);
     sm.cur_task = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

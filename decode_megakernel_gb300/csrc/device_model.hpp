@@ -38,7 +38,7 @@ struct DevModel {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, max_seq;
   int32_t group, splits, part_stride, num_ctas;
   float rms_eps;
-  int32_t ring_slots;          // slots of the weight ring in use (1 <= ring_slots <= kWeightSlots)
+  int32_t ring_slots;          // weight-ring slots (1 <= ring_slots <= kWeightSlots); KV ring: the rest of the pool
   int32_t prefetch_tiles;      // weight tiles the producer may prefetch into L2 beyond its full
                                // ring while the consumers are in attention / merge / O tasks
   int32_t pad0;
@@ -113,19 +113,22 @@ enum WaitSite : uint32_t {
 // kernel geometry
 constexpr int kConsumerWarps = kConsumerThreads / 32;  // 8
 constexpr int kThreads = kConsumerThreads + 32;        // + one producer warp
-// The weight ring (tiles of GEMV tasks) and the KV ring (K,V history tiles
-// of attention tasks) are separate so that the KV of the next attention
+// One pool of shared-memory slots holds the weight ring (tiles of GEMV
+// tasks, slots [0, ring_slots)) and the KV ring (K,V history stages of
+// attention tasks, the other slots), so that the KV of the next attention
 // task is loaded as soon as a KV slot frees up, never behind weight tiles.
-constexpr int kWeightSlots = 8;                        // 136 KB: 16 KB tiles + int4 side data
-constexpr int kKvSlots = 4;                            // 64 KB: K then V of up to 32 (hd 128) positions each
-constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one weight slot
+// The split is a load-time knob: long contexts give the KV ring more slots.
+constexpr int kWeightSlots = 8;                        // most weight slots (the default: 136 KB in flight)
+constexpr int kPoolSlots = 12;                         // weight + KV slots
+constexpr int kKvChunkStages = 4;                      // KV stages an attention chunk holds at once
+static_assert(kPoolSlots - kWeightSlots >= kKvChunkStages, "the KV ring must hold a chunk");
+constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one slot (a KV stage uses kStageBytes of it)
 constexpr int kScratchFloats = 4608;                   // GEMV row partials / attention merge
 // int8 / int4 GEMV tasks stage each warp's activations (256 floats) above the row
 // partials, which take at most kRowsMax rows x 8 warps
 constexpr int kActStageOffset = kRowsMax * kConsumerWarps;
 static_assert(kActStageOffset + kConsumerWarps * 256 <= kScratchFloats, "activation staging");
-constexpr int kSmemBytes = kWeightSlots * kSlotBytes + kKvSlots * kStageBytes + kScratchFloats * 4 +
-                           2 * (kWeightSlots + kKvSlots) * 8 + 256;
+constexpr int kSmemBytes = kPoolSlots * kSlotBytes + kScratchFloats * 4 + 2 * kPoolSlots * 8 + 256;
 
 // Byte offsets of the per-step scratch regions (tagged x_res, x_mid, qkv,
 // o, a, attention partials, then the status words) laid out from one base
