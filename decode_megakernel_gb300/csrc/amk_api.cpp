@@ -20,6 +20,7 @@ using namespace amk;
 // 16 KB tiles (plain streaming on GB300 peaks at 96-128 KB per SM; more
 // slots measured no faster).
 constexpr int kDefaultRingSlots = kWeightSlots;
+constexpr int kLongContextRingSlots = kPoolSlots - 2 * kKvChunkStages;   // 4 weight, 8 KV slots
 
 // Default L2 prefetch budget during the attention chain (tiles of 16 KB).
 constexpr int kDefaultPrefetchTiles = 0;
@@ -42,6 +43,7 @@ struct amk_ctx {
   amk_status poisoned = AMK_OK;
   int32_t max_queue = 0;  // longest per-CTA task queue (trace sizing)
   int32_t n_lm = 0;       // LM-head tasks: argmax pairs per step
+  bool ring_auto = true;  // ring_slots chosen per step (schedule knob 0)
   uint32_t* amax[2] = {nullptr, nullptr};  // per-step argmax pairs, double buffered
   // tensor-core prefill (bf16 weights): chunk buffers and tensor maps
   struct Prefill {
@@ -340,6 +342,17 @@ StepParams make_params(const amk_ctx* ctx, const DevModel& dm, int32_t token, in
                        float* logits, int skip_lm, uint32_t epoch) {
   StepParams p;
   p.m = dm;
+  if (ctx->ring_auto) {
+    // quantised consumers are bound by their own arithmetic, not by the
+    // weight bytes in flight, so when a context split holds more than one
+    // attention chunk of K,V stages the KV ring takes 8 of the 12 slots
+    // (8B int4 at 16K context: 339 -> 366 tok/s) and the next chunk loads
+    // while the current one is computed
+    const int pps = (kStageBytes / 2) / (2 * dm.head_dim);
+    const int per_split = (pos + dm.splits) / dm.splits;   // ceil((pos + 1) / splits)
+    const bool quantised = ctx->cfg.weight_format != AMK_FORMAT_BF16;
+    p.m.ring_slots = quantised && per_split > kKvChunkStages * pps ? kLongContextRingSlots : kDefaultRingSlots;
+  }
   p.logits = logits;
   p.token = token;
   p.pos = pos;
@@ -644,6 +657,7 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   dm.rms_eps = c.rms_eps;
   dm.ring_slots = sched && sched->ring_slots > 0 ? std::min<int32_t>(sched->ring_slots, kWeightSlots)
                                                  : kDefaultRingSlots;
+  ctx->ring_auto = !(sched && sched->ring_slots > 0);
   dm.prefetch_tiles = !sched || sched->l2_prefetch_tiles == 0 ? kDefaultPrefetchTiles
                       : sched->l2_prefetch_tiles < 0          ? 0
                                                               : std::min(sched->l2_prefetch_tiles, 1024);
