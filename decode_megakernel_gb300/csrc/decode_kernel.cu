@@ -173,16 +173,26 @@ __device__ __forceinline__ bool consumer_sync_or(bool pred) {
 // ------------------------------------------------------------ shared memory
 
 struct Smem {
-  uint8_t pool[kPoolSlots][kSlotBytes];     // weight ring [0, ring_slots), then the KV ring
+  uint8_t ring[kWeightSlots][kSlotBytes];   // weight ring [0, ring_slots); the rest lent to the KV ring
+  uint8_t kv[kKvChunkStages][kStageBytes];  // KV ring slots 0..3 (slot k >= 4: ring[ring_slots + k - 4])
   float scratch[kScratchFloats];
-  uint64_t full[kPoolSlots];
-  uint64_t empty[kPoolSlots];
+  uint64_t full[kWeightSlots];
+  uint64_t empty[kWeightSlots];
+  uint64_t kfull[kPoolSlots - kKvChunkStages];    // KV ring slots (at most 8)
+  uint64_t kempty[kPoolSlots - kKvChunkStages];
   float misc[32];
   int32_t abort_flag;
   int32_t cur_task;   // queue index of the consumers' current task (read by the producer)
   int32_t token;      // the step's input token
 };
 static_assert(sizeof(Smem) <= kSmemBytes, "shared memory layout");
+
+// KV ring slot k: the dedicated stage buffers first, then the weight slots
+// the weight ring leaves unused (ring_slots = kWeightSlots + kKvChunkStages
+// - KV slots)
+__device__ __forceinline__ uint8_t* kv_slot(Smem& sm, int ring_slots, uint32_t k) {
+  return k < (uint32_t)kKvChunkStages ? sm.kv[k] : sm.ring[ring_slots + (int)k - kKvChunkStages];
+}
 
 // ------------------------------------------------------------- status
 
@@ -439,13 +449,12 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       c.valid = false;
       return true;
     }
-    const uint32_t ps = kv ? wslots + c.slot : c.slot;   // pool slot
-    uint64_t* empty = &sm.empty[ps];
+    uint64_t* empty = kv ? &sm.kempty[c.slot] : &sm.empty[c.slot];
     if (!mbar_test_wait(empty, c.phase ^ 1u)) {
       *blocked = true;
       return false;
     }
-    uint64_t* full = &sm.full[ps];
+    uint64_t* full = kv ? &sm.kfull[c.slot] : &sm.full[c.slot];
     if (kv) {
       // K then V of positions [p0, p0 + pps): boxes of 64 dims x pps rows,
       // 128-byte swizzled (rows past the split are loaded too and masked)
@@ -453,13 +462,14 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       const int nbox = m.head_dim / 64;
       mbar_arrive_expect_tx(full, kStageBytes);
       for (int b = 0; b < nbox; ++b) {
-        tma_load_2d(sm.pool[ps] + b * c.tt.pps * 128, &m.kv_map, 64 * b, c.tt.rk + p0, full, pol_kv);
-        tma_load_2d(sm.pool[ps] + kStageBytes / 2 + b * c.tt.pps * 128, &m.kv_map, 64 * b,
+        uint8_t* dst = kv_slot(sm, (int)wslots, c.slot);
+        tma_load_2d(dst + b * c.tt.pps * 128, &m.kv_map, 64 * b, c.tt.rk + p0, full, pol_kv);
+        tma_load_2d(dst + kStageBytes / 2 + b * c.tt.pps * 128, &m.kv_map, 64 * b,
                     c.tt.rv + p0, full, pol_kv);
       }
     } else {
       mbar_arrive_expect_tx(full, c.tt.bytes);
-      bulk_copy_g2s(sm.pool[ps], c.tt.k + (int64_t)c.tile * c.tt.stride, c.tt.bytes, full, pol_w);
+      bulk_copy_g2s(sm.ring[c.slot], c.tt.k + (int64_t)c.tile * c.tt.stride, c.tt.bytes, full, pol_w);
       ++w_seq;
     }
     c.issued |= 1u << c.slot;
@@ -530,7 +540,7 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       break;
     }
     if (wb) mbar_try_wait_hint(&sm.empty[w.slot], w.phase ^ 1u, 200);
-    else if (ab) mbar_try_wait_hint(&sm.empty[wslots + a.slot], a.phase ^ 1u, 200);
+    else if (ab) mbar_try_wait_hint(&sm.kempty[a.slot], a.phase ^ 1u, 200);
     if (p.trace) {
       const int64_t dt = (int64_t)(global_timer() - now);
       if (wb) w.blocked += dt;
@@ -555,7 +565,7 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
     }
   };
   drain(w, sm.full, (int)wslots);
-  drain(a, sm.full + wslots, (int)kvslots);
+  drain(a, sm.kfull, (int)kvslots);
 }
 
 // -------------------------------------------------------------- consumers
@@ -1043,7 +1053,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   float act_up = 1.f;
   if constexpr (kMma) act_up = act_fragments<NKT>(h, bq, sm.scratch + kActStageOffset + warp * 256, lane);
 
-  const uint32_t ring0 = smem_addr(&sm.pool[0][0]);
+  const uint32_t ring0 = smem_addr(&sm.ring[0][0]);
   const uint32_t full0 = smem_addr(&sm.full[0]);
   const uint32_t empty0 = smem_addr(&sm.empty[0]);
   const uint32_t off0 = (uint32_t)(((rsub << cs) + chunk) * EB);   // pass 0 chunk
@@ -1336,7 +1346,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   constexpr int RUN = CP / kConsumerWarps;            // positions of a warp's run at most
   constexpr int MT = RUN / 16;                        // 16-position tiles per run
   constexpr int KS = HD / 16;                         // k-steps (QK) and dim tiles (PV)
-  static_assert(G <= 8 && RUN % 16 == 0 && HD % 64 == 0, "attention tile shapes");
+  static_assert(G <= 8 && RUN % 16 == 0 && HD % 64 == 0 && RUN <= PPS, "attention tile shapes");
   // scratch (floats): q staging, the step's own k / v as bf16 rows, then
   // at the end the warp states [warp][G][HD + 2]
   constexpr int WS = G * (HD + 2);
@@ -1409,10 +1419,9 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     for (int e = 0; e < 4; ++e) o[k2][e] = 0.f;
 
   const uint32_t kvs = (uint32_t)(kPoolSlots - m.ring_slots);   // KV ring slots (>= kKvChunkStages)
-  const uint32_t kv0 = smem_addr(&sm.pool[m.ring_slots][0]);
   const uint32_t cur0 = smem_addr(cur);
-  const uint32_t kfull0 = smem_addr(&sm.full[m.ring_slots]);
-  const uint32_t kempty0 = smem_addr(&sm.empty[m.ring_slots]);
+  const uint32_t kfull0 = smem_addr(&sm.kfull[0]);
+  const uint32_t kempty0 = smem_addr(&sm.kempty[0]);
   int64_t starved = 0;
   int t0, t1;
   attn_range(p.pos, m.splits, j, &t0, &t1);
@@ -1444,13 +1453,20 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     }
     // shared address of 16-byte chunk c (8 dims) of K (kv = 0) or V (kv = 1)
     // of task position pi: a swizzled ring row, or the step's own k / v
+    // The warp's run (at most RUN <= PPS positions) lies in stages stA and
+    // stA + 1 at most: their slot addresses are computed once per chunk.
+    const int stA = (c0 + w0) / PPS;
+    auto slot_base = [&](int st) -> uint32_t {
+      uint32_t slot = slot0 + (uint32_t)(st - s_begin);
+      if (slot >= kvs) slot -= kvs;
+      return smem_addr(kv_slot(sm, m.ring_slots, slot));
+    };
+    const uint32_t baseA = slot_base(stA), baseB = slot_base(stA + 1);
     auto addr_of = [&](int pi, int c, int kv) -> uint32_t {
       if (pi >= ncached) return cur0 + (uint32_t)(kv * HD * 2 + c * 16);
-      uint32_t slot = slot0 + (uint32_t)(pi / PPS - s_begin);
-      if (slot >= kvs) slot -= kvs;
       const int r = pi % PPS;
-      return kv0 + slot * kSlotBytes + (uint32_t)(kv * (kStageBytes / 2) + (c >> 3) * (PPS * 128) + r * 128 +
-                                                   (((c & 7) ^ (r & 7)) << 4));
+      return (pi / PPS == stA ? baseA : baseB) +
+             (uint32_t)(kv * (kStageBytes / 2) + (c >> 3) * (PPS * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
     };
     if (!failed && n > 0) {
       const int base = c0 + w0;
@@ -1772,14 +1788,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
   if (tid == 0) {
-    for (int s = 0; s < kPoolSlots; ++s) {
+    for (int s = 0; s < kWeightSlots; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
-    // the swizzled KV boxes need 1 KB alignment (slots are 17 KB apart):
+    for (int s = 0; s < kPoolSlots - kKvChunkStages; ++s) {
+      mbar_init(&sm.kfull[s], 1);
+      mbar_init(&sm.kempty[s], kConsumerWarps);
+    }
+    // the swizzled KV boxes need 1 KB alignment (slots are 16 or 17 KB apart):
     // refuse to run without it
-    static_assert(kSlotBytes % 1024 == 0, "KV slot alignment");
-    sm.abort_flag = (smem_addr(&sm.pool[0][0]) & 1023u) ? 1 : 0;
+    static_assert(kSlotBytes % 1024 == 0 && kStageBytes % 1024 == 0, "KV slot alignment");
+    sm.abort_flag = ((smem_addr(&sm.ring[0][0]) | smem_addr(&sm.kv[0][0])) & 1023u) ? 1 : 0;
     if (sm.abort_flag) set_status(p.m.status, ST_CHECK, 0xFFFFFFFFu, SITE_SMEM);
     sm.cur_task = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

@@ -113,22 +113,23 @@ enum WaitSite : uint32_t {
 // kernel geometry
 constexpr int kConsumerWarps = kConsumerThreads / 32;  // 8
 constexpr int kThreads = kConsumerThreads + 32;        // + one producer warp
-// One pool of shared-memory slots holds the weight ring (tiles of GEMV
-// tasks, slots [0, ring_slots)) and the KV ring (K,V history stages of
-// attention tasks, the other slots), so that the KV of the next attention
-// task is loaded as soon as a KV slot frees up, never behind weight tiles.
-// The split is a load-time knob: long contexts give the KV ring more slots.
-constexpr int kWeightSlots = 8;                        // most weight slots (the default: 136 KB in flight)
-constexpr int kPoolSlots = 12;                         // weight + KV slots
+// The weight ring (tiles of GEMV tasks, slots [0, ring_slots) of the eight
+// 17 KB weight slots) and the KV ring (K,V history stages of attention
+// tasks: four dedicated 16 KB slots plus the weight slots the weight ring
+// leaves unused) are separate, so that the KV of the next attention task is
+// loaded as soon as a KV slot frees up, never behind weight tiles.  The
+// split is a per-launch choice: long contexts give the KV ring more slots.
+constexpr int kWeightSlots = 8;                        // weight slots (the default ring: 136 KB in flight)
 constexpr int kKvChunkStages = 4;                      // KV stages an attention chunk holds at once
-static_assert(kPoolSlots - kWeightSlots >= kKvChunkStages, "the KV ring must hold a chunk");
-constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one slot (a KV stage uses kStageBytes of it)
+constexpr int kPoolSlots = kWeightSlots + kKvChunkStages;   // weight + KV slots of a CTA
+constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one weight slot
 constexpr int kScratchFloats = 4608;                   // GEMV row partials / attention merge
 // int8 / int4 GEMV tasks stage each warp's activations (256 floats) above the row
 // partials, which take at most kRowsMax rows x 8 warps
 constexpr int kActStageOffset = kRowsMax * kConsumerWarps;
 static_assert(kActStageOffset + kConsumerWarps * 256 <= kScratchFloats, "activation staging");
-constexpr int kSmemBytes = kPoolSlots * kSlotBytes + kScratchFloats * 4 + 2 * kPoolSlots * 8 + 256;
+constexpr int kSmemBytes = kWeightSlots * kSlotBytes + kKvChunkStages * kStageBytes + kScratchFloats * 4 +
+                           2 * kPoolSlots * 8 + 256;
 
 // Byte offsets of the per-step scratch regions (tagged x_res, x_mid, qkv,
 // o, a, attention partials, then the status words) laid out from one base
