@@ -178,8 +178,8 @@ struct Smem {
   float scratch[kScratchFloats];
   uint64_t full[kWeightSlots];
   uint64_t empty[kWeightSlots];
-  uint64_t kfull[kPoolSlots - kKvChunkStages];    // KV ring slots (at most 8)
-  uint64_t kempty[kPoolSlots - kKvChunkStages];
+  uint64_t kfull[kMaxKvSlots];    // KV ring slots: kPoolSlots - ring_slots <= kMaxKvSlots
+  uint64_t kempty[kMaxKvSlots];
   float misc[32];
   int32_t abort_flag;
   int32_t cur_task;   // queue index of the consumers' current task (read by the producer)
@@ -1792,7 +1792,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
-    for (int s = 0; s < kPoolSlots - kKvChunkStages; ++s) {
+    for (int s = 0; s < kMaxKvSlots; ++s) {
       mbar_init(&sm.kfull[s], 1);
       mbar_init(&sm.kempty[s], kConsumerWarps);
     }
@@ -1800,6 +1800,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     // refuse to run without it
     static_assert(kSlotBytes % 1024 == 0 && kStageBytes % 1024 == 0, "KV slot alignment");
     sm.abort_flag = ((smem_addr(&sm.ring[0][0]) | smem_addr(&sm.kv[0][0])) & 1023u) ? 1 : 0;
+    // the weight / KV split must leave the KV ring within its slots and barriers
+    if (p.m.ring_slots < 1 || p.m.ring_slots > kWeightSlots) sm.abort_flag = 1;
     if (sm.abort_flag) set_status(p.m.status, ST_CHECK, 0xFFFFFFFFu, SITE_SMEM);
     sm.cur_task = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

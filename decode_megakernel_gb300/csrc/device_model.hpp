@@ -122,6 +122,7 @@ constexpr int kThreads = kConsumerThreads + 32;        // + one producer warp
 constexpr int kWeightSlots = 8;                        // weight slots (the default ring: 136 KB in flight)
 constexpr int kKvChunkStages = 4;                      // KV stages an attention chunk holds at once
 constexpr int kPoolSlots = kWeightSlots + kKvChunkStages;   // weight + KV slots of a CTA
+constexpr int kMaxKvSlots = kPoolSlots - 1;            // KV slots when the weight ring keeps one
 constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one weight slot
 constexpr int kScratchFloats = 4608;                   // GEMV row partials / attention merge
 // int8 / int4 GEMV tasks stage each warp's activations (256 floats) above the row
@@ -129,7 +130,7 @@ constexpr int kScratchFloats = 4608;                   // GEMV row partials / at
 constexpr int kActStageOffset = kRowsMax * kConsumerWarps;
 static_assert(kActStageOffset + kConsumerWarps * 256 <= kScratchFloats, "activation staging");
 constexpr int kSmemBytes = kWeightSlots * kSlotBytes + kKvChunkStages * kStageBytes + kScratchFloats * 4 +
-                           2 * kPoolSlots * 8 + 256;
+                           2 * (kWeightSlots + kMaxKvSlots) * 8 + 256;
 
 // Byte offsets of the per-step scratch regions (tagged x_res, x_mid, qkv,
 // o, a, attention partials, then the status words) laid out from one base

@@ -126,6 +126,25 @@ def test_schedule_knobs(amk, orc, dev, knobs):
     assert err <= TOL and agree >= 0.99
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "int4"])
+@pytest.mark.parametrize("ring_slots", [0, 1, 4, 8])
+def test_ring_split_long_context(amk, orc, dev, fmt, ring_slots):
+    # one context split per KV head holding 600 positions: three attention
+    # chunks of 256 (head_dim 64), streamed through 4 KV slots (ring_slots
+    # 8), 8 (4) or 11 (1); 0 lets the library choose per step (int4 with
+    # more than one chunk per split: 8 KV slots, some lent from the weight
+    # ring)
+    base = dict(wc.TINY.__dict__)
+    if fmt == "int4":
+        base.update(weight_format="int4", ffn=768)
+    cfg = wc.ModelConfig(**base)
+    sched = amk.make_schedule_config(num_ctas=8, attn_splits=1, ring_slots=ring_slots, prefill_chunk=-1)
+    err, agree, ul = run_teacher_forced(amk, orc, dev, cfg, 600, 4, sched=sched)
+    print(f"{fmt} ring_slots {ring_slots}: max|dlogit| {err:.3e}, top-1 {agree:.3f}, kv same {ul[1]:.4f}")
+    assert err <= TOL and agree >= 0.99
+    assert ul[0] and ul[1] > 0.99
+
+
 def test_tiny_greedy_loop(amk, orc, dev):
     cfg = wc.TINY
     steps, max_seq = 32, 48
