@@ -96,7 +96,8 @@ def test_tiny_teacher_forced(amk, orc, dev):
     assert ul[0] and ul[1] > 0.99
 
 
-@pytest.mark.parametrize("variant", ["tied", "mha", "hd128", "int8", "int8-lmbf16", "int4", "int4-lmbf16"])
+@pytest.mark.parametrize("variant", ["tied", "mha", "hd128", "int8", "int8-lmbf16", "int4", "int4-lmbf16",
+                                     "int8-longrow", "int4-longrow"])
 def test_tiny_variants(amk, orc, dev, variant):
     base = dict(wc.TINY.__dict__)
     if variant == "tied":
@@ -109,6 +110,10 @@ def test_tiny_variants(amk, orc, dev, variant):
         base.update(weight_format="int8", lm_head_bf16=variant.endswith("lmbf16"))
     else:
         base.update(weight_format="int4", ffn=768, lm_head_bf16=variant.endswith("lmbf16"))
+    if variant.endswith("longrow"):
+        # a down projection of 4 K tiles (in_features 8192): the int4 consumer
+        # runs its rolled tile loop over rotated fragments there
+        base.update(ffn=8192)
     cfg = wc.ModelConfig(**base)
     err, agree, ul = run_teacher_forced(amk, orc, dev, cfg, 9, 6)
     print(f"{variant}: max|dlogit| {err:.3e}, top-1 {agree:.3f}, kv same {ul[1]:.4f}, "
