@@ -7,7 +7,9 @@
 //     producer streams the weight tiles of the CTA's whole queue through a
 //     shared-memory weight ring (8 x 16 KB tiles in flight, 1-D TMA bulk
 //     copies completing on mbarriers) and the K,V history of its attention
-//     tasks through a separate 4-slot KV ring (2-D swizzled TMA boxes).
+//     tasks through a separate KV ring (2-D swizzled TMA boxes; four
+//     slots of its own plus the weight slots a smaller weight ring leaves
+//     unused).
 //     Weights never depend on activations and the history never depends on
 //     the current step, so the producer runs ahead across the consumers'
 //     waits; this hides the per-tile cross-SM synchronisation cost the
@@ -20,7 +22,8 @@
 //     trip instead of a release fence, a counter poll and a data load.
 // The consumers keep the activation vector in registers, reduce with warp
 // shuffles and apply the fused epilogues (RoPE + KV append, residual adds,
-// SwiGLU, logits); attention runs on the tensor cores (mma.sync).  Every
+// SwiGLU, logits); bf16 GEMVs run on packed FMA, int8 / int4 GEMVs and
+// attention on the tensor cores (mma.sync).  Every
 // wait is bounded by %globaltimer: on expiry the kernel records a status
 // word, lets its own copies land and returns.
 #include <algorithm>
