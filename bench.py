@@ -45,6 +45,8 @@ if ROOT not in sys.path:
 METRIC = "batch-1 decode tok/s (Llama-8B-shape bf16); % of weight+KV bytes/HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e spec-sheet figure (context only)
+DEFAULT_LEGS = "llama1b,llama8b-int8,llama8b-int4"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["decode_kernel.cu", "device_model.hpp", "schedule.cpp", "schedule.hpp", "ptx.cuh"]
 
@@ -66,10 +68,20 @@ def parse_args(argv=None):
                     help="tokens per tensor-core prefill chunk (0: library default; -1: decode steps)")
     ap.add_argument("--prefill-parts", type=int, default=0,
                     help="bf16 parts of the prefill GEMM activations (0: library default, 3; or 2)")
+    ap.add_argument("--kv", choices=["auto", "prefill", "synthetic"], default="auto",
+                    help="KV history of the first P positions: the prompt's prefill, or a seeded "
+                         "synthetic history (auto: prefill for bf16 weights up to 4096 tokens)")
+    ap.add_argument("--legs", default=None,
+                    help="comma-separated other workloads timed after the headline (one GPU); "
+                         "default: the other three bench workloads when the headline is the default")
+    ap.add_argument("--no-probe", action="store_true", help="skip the read-only HBM probe")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prompt's prefill (its last run bracketed by "
                          "cudaProfilerStart/Stop) and print its JSON block")
-    return ap.parse_args(argv)
+    args = ap.parse_args(argv)
+    if args.legs is None:
+        args.legs = DEFAULT_LEGS if args.workload == "llama8b-bf16" else ""
+    return args
 
 
 # ------------------------------------------------------------------ helpers
@@ -191,13 +203,15 @@ def barrier():
 # ------------------------------------------------------------ cpu oracle leg
 
 def oracle_sample(weights_cpu, kv_cpu, pos: int, token: int, n_samples: int | None,
-                  seconds: float | None, warmup: int = 0):
+                  seconds: float | None, warmup: int = 0, threads: int | None = None):
     """Time the oracle on samples of one decode step: sample i runs layer
     i mod L and LM-head rows of slice i mod L (1/L of the vocabulary).
     Returns (samples timed, seconds, cores)."""
     from oracle import binding as orc
     cfg = weights_cpu.cfg
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    if threads:
+        cores = threads
     orc.set_threads(cores)
     om = orc.OracleModel(weights_cpu, kv_cpu.shape[3])
     L, V = cfg.n_layers, cfg.vocab
@@ -315,8 +329,199 @@ def prefill_block(wl, best_ms, runs_ms, dec_chunk, parts=3):
     return out
 
 
-def run_ours(args, wl, rank, world, local_rank):
+def load_decoder(amk, wl, dev, stream, sched, kv_mode):
+    """The workload's model loaded through the C ABI, with the first P
+    positions of its KV cache valid: prefilled by amk_prefill from the
+    seeded prompt (kv_mode "prefill"), or a seeded synthetic history
+    declared valid with amk_set_kv_length ("synthetic": the int8 / int4
+    prefill is one decode launch per token, 16K launches for the int4
+    workload)."""
+    import torch
+    from workload import synth
+    cfg, P = wl.model, wl.prompt_len
+    weights = synth.model_weights(cfg, seed=synth.WEIGHT_SEED, device=dev)
+    kv = None
+    if kv_mode == "synthetic":
+        kv = synth.synthetic_kv_cache(cfg, P, wl.max_seq, device=dev)
+    dec = amk.Decoder(weights, wl.max_seq, stream=stream, sched=sched, kv_cache=kv)
+    del weights
+    torch.cuda.empty_cache()
+    if kv_mode == "synthetic":
+        dec.set_kv_length(P)
+    else:
+        dec.prefill(synth.prompt_tokens(cfg, P).tolist(), 0)
+    dec.sync()
+    return dec
+
+
+def kv_mode_for(wl, args):
+    if args.kv != "auto":
+        return args.kv
+    return "prefill" if wl.model.weight_format == "bf16" and wl.prompt_len <= 4096 else "synthetic"
+
+
+def time_decode(dec, wl, args, dev, stream, K, W, profile=False):
+    """W untimed then K timed decode steps (teacher-forced seeded tokens,
+    positions P .. P + D - 1 cyclic) with CUDA events on the decode stream;
+    returns (total ms, per-step ms, positions, clocks)."""
+    import torch
+    from workload import synth
+    cfg, P, D = wl.model, wl.prompt_len, wl.decode_steps
+    toks = synth.decode_tokens(cfg, D).tolist()
+    logits = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
+    pos_of = lambda i: P + (i % D)  # noqa: E731
+    sampler = ClockSampler(gpu_id_for(dev))
+    for i in range(W):
+        dec.decode_step(toks[i % D], pos_of(i), logits)
+    dec.sync()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    # cudaProfilerStart/Stop bracket the timed region so that a profiler run
+    # with collection off at start (ncu --profile-from-start off) lists
+    # exactly the launches timed here; without a profiler they do nothing.
+    if profile:
+        torch.cuda.profiler.start()
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(K):
+            j = W + i
+            dec.decode_step(toks[j % D], pos_of(j), logits)
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if profile:
+        torch.cuda.profiler.stop()
+    barrier()
+    clocks = sampler.stop()
+    dec.sync()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
+    total_ms = evs[0].elapsed_time(evs[K])
+    positions = [pos_of(W + i) for i in range(K)]
+    return total_ms, per, positions, clocks
+
+
+def roofline_block(wl, per, positions):
     import numpy as np
+    from workload import configs as wc
+    K = len(per)
+    mean_bytes = sum(wc.step_bytes(wl.model, p) for p in positions) / K
+    mean_launch_s = (sum(per) / K) / 1e3
+    achieved = mean_bytes / mean_launch_s / 1e9
+    peak, peak_src = measured_peak_gbs()
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
+            "peak_source": f"{peak_src} hbm_gbs (copy)",
+            "algorithmic_bytes_per_launch": mean_bytes,
+            "mean_launch_ms": mean_launch_s * 1e3,
+            "launch_ms_p10_p50_p90": [float(np.percentile(per, q)) for q in (10, 50, 90)]}
+
+
+def time_e2e(dec, wl, n):
+    """n steps through amk_decode_step_host (launch parameters in, logits
+    back into pinned host memory), timed on the host."""
+    import numpy as np
+    import torch
+    from workload import synth
+    cfg, P, D = wl.model, wl.prompt_len, wl.decode_steps
+    toks = synth.decode_tokens(cfg, D).tolist()
+    host_logits = torch.empty(cfg.vocab, dtype=torch.float32, pin_memory=True)
+    for i in range(min(3, n)):
+        dec.decode_step_host(toks[i % D], P + (i % D), host_logits)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(n):
+        dec.decode_step_host(toks[i % D], P + (i % D), host_logits)
+    secs = time.perf_counter() - t0
+    assert np.isfinite(host_logits.numpy()).all()
+    return secs
+
+
+def hbm_read_probe(amk, dev, gib=4.0, reps=10):
+    """Read-only stream rate of this GPU (amk_debug_hbm_read_probe): best of
+    `reps` passes over a buffer of `gib` GiB (> 30x L2), per mode."""
+    import torch
+    nbytes = int(gib * (1 << 30)) // 16384 * 16384
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.zeros(8 * sms, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {"bytes": nbytes}
+    for mode, name in ((0, "bulk_ring_gbs"), (1, "ld128_gbs")):
+        best = None
+        for r in range(reps + 2):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            amk.check(amk.amk_debug_hbm_read_probe(mode, buf.data_ptr(), nbytes, out.data_ptr(), out.numel(),
+                                                   stream.cuda_stream))
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if mode == 0 and int(out[1::2][:sms].abs().sum()) != 0:
+                raise RuntimeError("hbm read probe: a bulk copy did not land")
+            ms = e0.elapsed_time(e1)
+            if r >= 2:
+                best = ms if best is None else min(best, ms)
+        res[name] = nbytes / (best / 1e3) / 1e9
+    del buf
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_leg(amk, wl, args, dev, stream, sched, K, W, n_e2e, profile=False, greedy=True, dec=None):
+    """One workload: load (unless given a loaded decoder), time K decode
+    steps, e2e and device greedy."""
+    import torch
+    from workload import synth
+    kv_mode = kv_mode_for(wl, args)
+    if dec is None:
+        dec = load_decoder(amk, wl, dev, stream, sched, kv_mode)
+    total_ms, per, positions, clocks = time_decode(dec, wl, args, dev, stream, K, W, profile)
+    leg = {"workload": wl.name, "model": wl.description, "kv_history": kv_mode,
+           "steps": K, "warmup": W, "total_ms": total_ms, "per_ms": per,
+           "roofline": roofline_block(wl, per, positions), "clocks": clocks}
+    if n_e2e > 0:
+        leg["e2e_s"] = time_e2e(dec, wl, n_e2e)
+        leg["e2e_steps"] = n_e2e
+    if greedy:
+        # greedy decoding on the device (amk_generate: the argmax feeds the
+        # next step with no host round trip), device-timed on the decode stream
+        D = wl.decode_steps
+        n_gen = min(K, D)
+        tok0 = int(synth.decode_tokens(wl.model, 1)[0])
+        gen_tokens = torch.empty(n_gen, dtype=torch.int32, device=dev)
+        dec.generate(tok0, wl.prompt_len, min(4, n_gen), gen_tokens)
+        dec.sync()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        dec.generate(tok0, wl.prompt_len, n_gen, gen_tokens)
+        g1.record(stream)
+        dec.sync()
+        leg["greedy_ms"] = g0.elapsed_time(g1)
+        leg["greedy_steps"] = n_gen
+    leg["_dec"] = dec
+    return leg
+
+
+def leg_summary(leg, cfg):
+    """The per-workload object of the bench line (one GPU)."""
+    K = leg["steps"]
+    value = K / (leg["total_ms"] / 1e3)
+    out = {"workload": leg["workload"], "model": leg["model"], "kv_history": leg["kv_history"],
+           "metric": "batch-1 decode tok/s", "value": value, "unit": "tok/s",
+           "ms_per_step": leg["total_ms"] / K, "steps": K, "warmup": leg["warmup"],
+           "roofline": {k: v for k, v in leg["roofline"].items()
+                        if k in ("bound", "achieved", "peak", "unit", "frac", "traffic",
+                                 "algorithmic_bytes_per_launch", "mean_launch_ms")},
+           "clocks": leg["clocks"]}
+    if "e2e_s" in leg:
+        out["e2e"] = {"value": leg["e2e_steps"] / leg["e2e_s"], "unit": "tok/s", "h2d_bytes_per_step": 8,
+                      "d2h_bytes_per_step": cfg.vocab * 4}
+    if "greedy_ms" in leg:
+        out["device_greedy_tok_s"] = leg["greedy_steps"] / (leg["greedy_ms"] / 1e3)
+    return out
+
+
+def run_ours(args, wl, rank, world, local_rank):
     import torch
 
     import __graft_entry__
@@ -329,138 +534,104 @@ def run_ours(args, wl, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     cfg = wl.model
-    P, D = wl.prompt_len, wl.decode_steps
-    max_seq = wl.max_seq
+    P = wl.prompt_len
     stream = torch.cuda.Stream(device=dev)
     sched = amk.make_schedule_config(num_ctas=args.num_ctas, ring_slots=args.ring_slots,
                                      l2_prefetch_tiles=args.l2_prefetch_tiles,
                                      prefill_chunk=args.prefill_chunk, prefill_parts=args.prefill_parts)
-
-    weights = synth.model_weights(cfg, seed=synth.WEIGHT_SEED, device=dev)
-    dec = amk.Decoder(weights, max_seq, stream=stream, sched=sched)
     num_ctas = args.num_ctas or torch.cuda.get_device_properties(dev).multi_processor_count
-    del weights
-    torch.cuda.empty_cache()
-    prompt = synth.prompt_tokens(cfg, P).tolist()
-    toks = synth.decode_tokens(cfg, D).tolist()
-    dec.prefill(prompt, 0)
-    dec.sync()
+    kv_mode = kv_mode_for(wl, args)
+
     # the prompt's prefill (tensor-core GEMMs with bf16 weights), timed on
     # the decode stream; rerunning it rewrites the same K,V
-    pf_ms = []
-    for r in range(3):
-        last = args.prefill_only and r == 2
-        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if last:
-            torch.cuda.synchronize(dev)
-            torch.cuda.profiler.start()
-        p0.record(stream)
-        dec.prefill(prompt, 0)
-        p1.record(stream)
-        dec.sync()
-        if last:
-            torch.cuda.profiler.stop()
-        pf_ms.append(p0.elapsed_time(p1))
-    pf_best = min(pf_ms)
-    pf_chunk = dec.prefill_chunk
-    if args.prefill_only:
-        dec.close()
-        return {"impl": "ours", "workload": wl.name, "prefill": prefill_block(wl, pf_best, pf_ms, pf_chunk, args.prefill_parts or 3)}
-
-    logits = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
-    pos_of = lambda i: P + (i % D)  # noqa: E731
-    sampler = ClockSampler(gpu_id_for(dev))
-    for i in range(args.warmup):
-        dec.decode_step(toks[i % D], pos_of(i), logits)
-    dec.sync()
+    pf = None
+    if kv_mode == "prefill" or args.prefill_only:
+        dec = load_decoder(amk, wl, dev, stream, sched, "prefill")
+        prompt = synth.prompt_tokens(cfg, P).tolist()
+        pf_ms = []
+        for r in range(3):
+            last = args.prefill_only and r == 2
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if last:
+                torch.cuda.synchronize(dev)
+                torch.cuda.profiler.start()
+            p0.record(stream)
+            dec.prefill(prompt, 0)
+            p1.record(stream)
+            dec.sync()
+            if last:
+                torch.cuda.profiler.stop()
+            pf_ms.append(p0.elapsed_time(p1))
+        pf = prefill_block(wl, min(pf_ms), pf_ms, dec.prefill_chunk, args.prefill_parts or 3)
+        if args.prefill_only:
+            dec.close()
+            return {"impl": "ours", "workload": wl.name, "prefill": pf}
+    else:
+        dec = None
 
     K = args.steps
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
-    barrier()
-    torch.cuda.synchronize(dev)
-    # cudaProfilerStart/Stop bracket the timed region so that a profiler run
-    # with collection off at start (ncu --profile-from-start off) lists
-    # exactly the launches timed here; without a profiler they do nothing.
-    torch.cuda.profiler.start()
-    with torch.cuda.stream(stream):
-        evs[0].record(stream)
-        for i in range(K):
-            j = args.warmup + i
-            dec.decode_step(toks[j % D], pos_of(j), logits)
-            evs[i + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    torch.cuda.profiler.stop()
-    barrier()
-    clocks = sampler.stop()
-    dec.sync()
-    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
-    total_ms = evs[0].elapsed_time(evs[K])
-    max_ms, units = reduce_over_ranks(total_ms, float(K))
-    value = units / (max_ms / 1e3)
-
-    # roofline of the decode kernel (the whole step is this one kernel)
-    positions = [pos_of(args.warmup + i) for i in range(K)]
-    mean_bytes = sum(wc.step_bytes(cfg, p) for p in positions) / K
-    mean_launch_s = (sum(per) / K) / 1e3
-    achieved = mean_bytes / mean_launch_s / 1e9
-    peak, peak_src = measured_peak_gbs()
-
-    # end to end through the host-buffer entry point
-    n_e2e = args.e2e_steps or K
-    host_logits = torch.empty(cfg.vocab, dtype=torch.float32, pin_memory=True)
-    for i in range(min(3, n_e2e)):
-        dec.decode_step_host(toks[i % D], pos_of(i), host_logits)
-    barrier()
-    t0 = time.perf_counter()
-    for i in range(n_e2e):
-        dec.decode_step_host(toks[i % D], pos_of(i), host_logits)
-    e2e_s = time.perf_counter() - t0
-    e2e_max_ms, e2e_units = reduce_over_ranks(e2e_s * 1e3, float(n_e2e))
-    e2e_value = e2e_units / (e2e_max_ms / 1e3)
-    assert np.isfinite(host_logits.numpy()).all()
-
-    # greedy decoding on the device (amk_generate: the argmax feeds the next
-    # step with no host round trip), device-timed on the decode stream
-    n_gen = min(K, D)
-    gen_tokens = torch.empty(n_gen, dtype=torch.int32, device=dev)
-    dec.generate(toks[0], P, min(4, n_gen), gen_tokens)
-    dec.sync()
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    dec.generate(toks[0], P, n_gen, gen_tokens)
-    g1.record(stream)
-    dec.sync()
-    gen_ms = g0.elapsed_time(g1)
-    gen_max_ms, gen_units = reduce_over_ranks(gen_ms, float(n_gen))
+    leg = run_leg(amk, wl, args, dev, stream, sched, K, args.warmup, args.e2e_steps or K, profile=True,
+                  dec=dec)
+    dec = leg.pop("_dec")
     dec.close()
     del dec
     torch.cuda.empty_cache()
+    max_ms, units = reduce_over_ranks(leg["total_ms"], float(K))
+    value = units / (max_ms / 1e3)
+    e2e_max_ms, e2e_units = reduce_over_ranks(leg["e2e_s"] * 1e3, float(leg["e2e_steps"]))
+    gen_max_ms, gen_units = reduce_over_ranks(leg["greedy_ms"], float(leg["greedy_steps"]))
 
+    roof = leg["roofline"]
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_block(wl, args, num_ctas),
         "gpu_launches": K,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
-                     "peak_source": f"{peak_src} hbm_gbs (copy)",
-                     "algorithmic_bytes_per_launch": mean_bytes,
-                     "mean_launch_ms": mean_launch_s * 1e3,
-                     "launch_ms_p10_p50_p90": [float(np.percentile(per, q)) for q in (10, 50, 90)]},
-        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 8,
+        "roofline": roof,
+        "e2e": {"value": e2e_units / (e2e_max_ms / 1e3), "unit": "tok/s", "h2d_bytes_per_step": 8,
                 "d2h_bytes_per_step": cfg.vocab * 4},
-        "device_greedy": {"value": gen_units / (gen_max_ms / 1e3), "unit": "tok/s", "steps": n_gen,
-                          "what": "amk_generate: argmax fused into the LM head, n_gen launches back "
+        "device_greedy": {"value": gen_units / (gen_max_ms / 1e3), "unit": "tok/s",
+                          "steps": leg["greedy_steps"],
+                          "what": "amk_generate: argmax fused into the LM head, launches back "
                                   "to back with no host round trip (+1 final reduction)"},
-        "clocks": clocks,
-        "prefill": prefill_block(wl, pf_best, pf_ms, pf_chunk, args.prefill_parts or 3),
+        "clocks": leg["clocks"],
+        "prefill": pf,
     }
+    if world == 1 and not args.no_probe:
+        probe = hbm_read_probe(amk, dev)
+        best = max(probe["bulk_ring_gbs"], probe["ld128_gbs"])
+        probe["nominal_gbs"] = NOMINAL_HBM_GBS
+        probe["read_probe_frac_of_nominal"] = best / NOMINAL_HBM_GBS
+        line["hbm_read_probe"] = probe
+        roof["frac_of_read_probe"] = roof["achieved"] / best
+        roof["frac_of_nominal"] = roof["achieved"] / NOMINAL_HBM_GBS
+    # the other workloads, one GPU only (replicas report the headline alone)
+    if world == 1 and args.legs:
+        legs = {}
+        for name in [n.strip() for n in args.legs.split(",") if n.strip()]:
+            if name == wl.name or name == args.workload:
+                continue
+            lw = wc.workload(name)
+            lsched = amk.make_schedule_config(num_ctas=args.num_ctas)
+            lk = min(K, lw.decode_steps)
+            lg = run_leg(amk, lw, args, dev, stream, lsched, lk, args.warmup, lk, greedy=True)
+            d = lg.pop("_dec")
+            d.close()
+            del d
+            torch.cuda.empty_cache()
+            legs[name] = leg_summary(lg, lw.model)
+        line["workloads"] = legs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w_cpu, kv = host_weights_and_kv(wl, dev)
-        n, secs, cores = oracle_sample(w_cpu, kv, P, toks[0], n_samples=None, seconds=args.cpu_seconds)
+        tok = int(synth.decode_tokens(cfg, 1)[0])
+        n, secs, cores = oracle_sample(w_cpu, kv, P, tok, n_samples=None, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": (n / cfg.n_layers) / secs, "unit": "tok/s", "cores": cores,
                                 "kind": "oracle", "sample": cpu_sample_desc(wl, n)}
+        n1, secs1, _ = oracle_sample(w_cpu, kv, P, tok, n_samples=None, seconds=args.cpu_seconds / 2,
+                                     threads=1)
+        line["cpu_baseline_1core"] = {"value": (n1 / cfg.n_layers) / secs1, "unit": "tok/s", "cores": 1,
+                                      "kind": "oracle", "sample": cpu_sample_desc(wl, n1)}
     return line if rank == 0 else None
 
 

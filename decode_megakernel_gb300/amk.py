@@ -96,6 +96,7 @@ def _load():
         "amk_debug_trace_step": (C.c_int, [P, C.c_int32, C.c_int32, P, P, C.c_size_t]),
         "amk_debug_dequant": (C.c_int, [C.c_int32, C.POINTER(amk_linear), C.c_int32, C.c_int32,
                                         P, P]),
+        "amk_debug_hbm_read_probe": (C.c_int, [C.c_int32, P, C.c_size_t, P, C.c_size_t, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -228,6 +229,12 @@ def amk_debug_dequant(fmt: int, w_ptr, s_ptr, z_ptr, out_features, in_features, 
     lin = amk_linear(w_ptr, s_ptr, z_ptr)
     return int(lib.amk_debug_dequant(int(fmt), C.byref(lin), int(out_features), int(in_features),
                                      C.c_void_p(out_ptr), C.c_void_p(stream_ptr)))
+
+
+def amk_debug_hbm_read_probe(mode: int, buf_ptr: int, nbytes: int, out_ptr: int, out_words: int,
+                             stream_ptr: int) -> int:
+    return int(lib.amk_debug_hbm_read_probe(int(mode), C.c_void_p(buf_ptr), int(nbytes),
+                                            C.c_void_p(out_ptr), int(out_words), C.c_void_p(stream_ptr)))
 
 
 # ------------------------------------------------------------ marshalling helpers

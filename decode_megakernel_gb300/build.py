@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libamk.so")
 
-SOURCES = ["decode_kernel.cu", "amk_api.cpp", "schedule.cpp", "static_scratch.cu", "prefill.cu"]
+SOURCES = ["decode_kernel.cu", "amk_api.cpp", "schedule.cpp", "static_scratch.cu", "prefill.cu", "hbm_probe.cu"]
 HEADERS = ["device_model.hpp", "schedule.hpp", "prefill.hpp", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -36,7 +36,7 @@ struct amk_ctx {
   DevModel dm{};
   const void* kernel = nullptr;
   int smem = 0;
-  uint32_t epoch = 0;
+  uint32_t tag_base = 0;  // tag base of the latest launch (see next_tag_base)
   int32_t kv_len = 0;
   float* logits_stage = nullptr;
   uint64_t timeout_ns = 0;
@@ -206,9 +206,16 @@ amk_status resolve_ctas(const amk_schedule_config* sched, BuildOptions* opt, std
 
 int lm_format(const amk_config& c) { return c.tied_embeddings ? AMK_FORMAT_BF16 : c.lm_head_format; }
 
-// tag_base of a launch: version v of the step carries tag 1 + (tag_base + v - 1) mod kTagPeriod
-uint32_t tag_base_of(uint32_t epoch, int n_layers) {
-  return (uint32_t)(((uint64_t)epoch * (uint64_t)n_layers) % (uint64_t)kTagPeriod);
+// tag_base of a launch: version v of the step carries tag 1 + (tag_base + v - 1) mod kTagPeriod.
+// Launch e of a context has tag_base (e * n_layers) mod kTagPeriod, so that
+// the tags of consecutive launches continue one another.  The context keeps
+// the base itself, advanced modulo kTagPeriod at every launch, rather than
+// a launch counter: a counter would wrap after 2^32 launches to a value
+// whose base breaks that continuity (2^32 is 1 mod 15), letting a reader
+// accept the previous launch's words.
+uint32_t next_tag_base(amk_ctx* ctx) {
+  ctx->tag_base = (ctx->tag_base + (uint32_t)(ctx->cfg.n_layers % kTagPeriod)) % (uint32_t)kTagPeriod;
+  return ctx->tag_base;
 }
 
 amk_status plan(const amk_config* cfg, const amk_schedule_config* sched, ModelGeom* g,
@@ -339,7 +346,7 @@ bool linear_ok(const amk_linear& l, int fmt) {
 
 // Launch parameters of one step; greedy-decoding and trace fields off.
 StepParams make_params(const amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
-                       float* logits, int skip_lm, uint32_t epoch) {
+                       float* logits, int skip_lm, uint32_t tag_base) {
   StepParams p;
   p.m = dm;
   if (ctx->ring_auto) {
@@ -356,7 +363,7 @@ StepParams make_params(const amk_ctx* ctx, const DevModel& dm, int32_t token, in
   p.logits = logits;
   p.token = token;
   p.pos = pos;
-  p.tag_base = tag_base_of(epoch, ctx->cfg.n_layers);
+  p.tag_base = tag_base;
   p.skip_lm = skip_lm;
   p.timeout_ns = ctx->timeout_ns;
   p.trace = nullptr;
@@ -380,7 +387,7 @@ amk_status launch_params(amk_ctx* ctx, StepParams& p) {
 }
 
 amk_status launch_step(amk_ctx* ctx, int32_t token, int32_t pos, float* logits, int skip_lm) {
-  StepParams p = make_params(ctx, ctx->dm, token, pos, logits, skip_lm, ++ctx->epoch);
+  StepParams p = make_params(ctx, ctx->dm, token, pos, logits, skip_lm, next_tag_base(ctx));
   return launch_params(ctx, p);
 }
 
@@ -432,9 +439,13 @@ amk_status internal_begin_step(amk_ctx* ctx, int32_t token, int32_t pos, const f
   return AMK_OK;
 }
 
-amk_status internal_launch(amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
-                           float* logits, uint32_t epoch) {
-  StepParams p = make_params(ctx, dm, token, pos, logits, 0, epoch);
+// A launch on scratch that the caller zeroed: it runs with the tag base of
+// a context's first launch (tag 0, which zeroed words carry, is never a
+// version's tag).
+amk_status internal_launch_fresh(amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
+                                 float* logits) {
+  const uint32_t base = (uint32_t)(ctx->cfg.n_layers % kTagPeriod);
+  StepParams p = make_params(ctx, dm, token, pos, logits, 0, base);
   return launch_params(ctx, p);
 }
 
@@ -450,6 +461,13 @@ amk_status internal_end_step(amk_ctx* ctx, int32_t pos, const uint32_t status[4]
 }
 
 amk_status internal_fail(amk_ctx* ctx, amk_status st, const char* msg) { return fail(ctx, st, msg); }
+
+// A CUDA call of a step failed after its launch: the context is poisoned as
+// amk_sync does in that case.
+amk_status internal_poison(amk_ctx* ctx, cudaError_t e, const char* what) {
+  ctx->poisoned = AMK_ERR_CUDA;
+  return cuda_fail(ctx, e, what);
+}
 
 }  // namespace amk
 
@@ -909,7 +927,7 @@ amk_status amk_generate(amk_ctx* ctx, int32_t first_token, int32_t pos, int32_t 
     return fail(ctx, AMK_ERR_INVALID_ARG, "tokens_dev NULL or misaligned, or logits_dev misaligned");
   float* logits = logits_dev ? logits_dev : ctx->logits_stage;
   for (int32_t i = 0; i < n_steps; ++i) {
-    StepParams p = make_params(ctx, ctx->dm, first_token, pos + i, logits, 0, ++ctx->epoch);
+    StepParams p = make_params(ctx, ctx->dm, first_token, pos + i, logits, 0, next_tag_base(ctx));
     p.amax = ctx->amax[i & 1];
     if (i > 0) {
       p.token_src = ctx->amax[(i - 1) & 1];
@@ -962,7 +980,7 @@ amk_status amk_debug_trace_step(amk_ctx* ctx, int32_t token, int32_t pos, float*
       trace_bytes < amk_debug_trace_bytes(ctx, nullptr))
     return fail(ctx, AMK_ERR_INVALID_ARG, "bad logits or trace buffer (see amk_debug_trace_bytes)");
   AMK_CUDA(ctx, cudaMemsetAsync(trace_dev, 0, amk_debug_trace_bytes(ctx, nullptr), ctx->stream));
-  StepParams p = make_params(ctx, ctx->dm, token, pos, logits_dev, 0, ++ctx->epoch);
+  StepParams p = make_params(ctx, ctx->dm, token, pos, logits_dev, 0, next_tag_base(ctx));
   p.trace = trace_dev;
   p.trace_stride = ctx->max_queue;
   st = launch_params(ctx, p);
@@ -998,6 +1016,26 @@ amk_status amk_debug_dequant(int32_t format, const amk_linear* lin, int32_t out_
   launch_debug_dequant(format, lin->w, lin->scales, lin->zeros, out_features, in_features, out_dev, stream);
   AMK_CUDA(nullptr, cudaGetLastError());
   AMK_CUDA(nullptr, cudaStreamSynchronize((cudaStream_t)stream));
+  return AMK_OK;
+}
+
+amk_status amk_debug_hbm_read_probe(int32_t mode, const void* buf_dev, size_t bytes, uint32_t* out_dev,
+                                    size_t out_words, void* stream) {
+  if (mode != 0 && mode != 1)
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "hbm read probe: mode must be 0 (bulk ring) or 1 (128-bit loads)");
+  if (!buf_dev || !out_dev || !aligned(buf_dev, 16) || !aligned(out_dev, 4) || bytes == 0 ||
+      bytes % kHbmProbeTileBytes)
+    return fail(nullptr, AMK_ERR_INVALID_ARG,
+                "hbm read probe: buffer must be 16-byte aligned and a non-zero multiple of 16384 bytes");
+  int dev = 0, sms = 0;
+  AMK_CUDA(nullptr, cudaGetDevice(&dev));
+  AMK_CUDA(nullptr, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const size_t need = (size_t)2 * (mode == 0 ? sms : 4 * sms);
+  if (out_words < need)
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "hbm read probe: out buffer needs 8 * SM count words");
+  cudaStream_t s = (cudaStream_t)stream;
+  AMK_CUDA(nullptr, cudaMemsetAsync(out_dev, 0, need * sizeof(uint32_t), s));
+  AMK_CUDA(nullptr, launch_hbm_probe(mode, buf_dev, bytes, out_dev, sms, 2000000000ull, stream));
   return AMK_OK;
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>   // CUtensorMap (a plain 128-byte descriptor)
+#include <cuda_runtime.h>
 
 #include <cstdint>
 
@@ -157,5 +158,10 @@ void launch_watchdog_probe(uint32_t* scratch, uint64_t timeout_ns, void* stream)
 void launch_argmax_pairs(const uint32_t* pairs, int n, int32_t* out, void* stream);
 void launch_debug_dequant(int fmt, const void* w, const void* scales, const void* zeros,
                           int rows, int K, float* out, void* stream);
+// read-only HBM stream probe (hbm_probe.cu): mode 0 bulk-copy ring, mode 1
+// 128-bit loads; out holds 2 words per CTA (sms CTAs, or 4 * sms in mode 1)
+constexpr uint64_t kHbmProbeTileBytes = 16384;
+cudaError_t launch_hbm_probe(int mode, const void* buf, uint64_t bytes, uint32_t* out, int sms,
+                             uint64_t timeout_ns, void* stream);
 
 }  // namespace amk

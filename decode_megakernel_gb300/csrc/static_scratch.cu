@@ -13,7 +13,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 
 #include "../../include/amk.h"
 #include "device_model.hpp"
@@ -22,10 +21,11 @@ namespace amk {
 
 amk_status internal_begin_step(amk_ctx* ctx, int32_t token, int32_t pos, const float* logits,
                                DevModel* dm, StepScratchPlan* plan);
-amk_status internal_launch(amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
-                           float* logits, uint32_t epoch);
+amk_status internal_launch_fresh(amk_ctx* ctx, const DevModel& dm, int32_t token, int32_t pos,
+                                 float* logits);
 amk_status internal_end_step(amk_ctx* ctx, int32_t pos, const uint32_t status[4]);
 amk_status internal_fail(amk_ctx* ctx, amk_status st, const char* msg);
+amk_status internal_poison(amk_ctx* ctx, cudaError_t e, const char* what);
 
 // 1 MiB: an 8B-shape model with 19 attention splits per KV head needs ~450 KB.
 constexpr size_t kStaticScratchBytes = size_t(1) << 20;
@@ -34,23 +34,17 @@ static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchByte
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_lookup_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_step_scratch on `device` (which must be current).
-// Host code may only name the array through this address: the symbol
-// itself is a host-side stand-in.  Looked up once per device.
-cudaError_t scratch_address(int device, void** out) {
-  if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_lookup_mutex);
-  if (!g_scratch_addr[device]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_step_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[device] = p;
-  }
-  *out = g_scratch_addr[device];
+// Device address of g_step_scratch in the current device's context.  Host
+// code may only name the array through this address: the symbol itself is a
+// host-side stand-in.  Looked up on every call (the lookup allocates
+// nothing), so that an address never outlives the context it belongs to
+// (after a cudaDeviceReset the library's device code is loaded anew, at a
+// new address).
+cudaError_t scratch_address(void** out) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_step_scratch);
+  if (e != cudaSuccess) return e;
+  *out = p;
   return cudaSuccess;
 }
 
@@ -73,7 +67,7 @@ extern "C" amk_status amk_decode_step_static_scratch(amk_ctx* ctx, int32_t token
     return internal_fail(ctx, AMK_ERR_OOM, msg);
   }
   void* base = nullptr;
-  cudaError_t e = scratch_address(plan.device, &base);
+  cudaError_t e = scratch_address(&base);
   if (e != cudaSuccess) {
     char msg[160];
     snprintf(msg, sizeof msg, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
@@ -95,11 +89,11 @@ extern "C" amk_status amk_decode_step_static_scratch(amk_ctx* ctx, int32_t token
   // first, and tag 0 is never a version's tag.
   e = cudaMemsetAsync(b, 0, plan.total, s);
   if (e != cudaSuccess) return internal_fail(ctx, AMK_ERR_CUDA, "clearing the static scratch failed");
-  st = internal_launch(ctx, dm, token, pos, logits_dev, 1u);
+  st = internal_launch_fresh(ctx, dm, token, pos, logits_dev);
   if (st != AMK_OK) return st;
   uint32_t status[4] = {0, 0, 0, 0};
   e = cudaMemcpyAsync(status, dm.status, sizeof status, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return internal_fail(ctx, AMK_ERR_CUDA, "reading the step status failed");
+  if (e != cudaSuccess) return internal_poison(ctx, e, "reading the step status");
   return internal_end_step(ctx, pos, status);
 }

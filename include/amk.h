@@ -204,18 +204,22 @@ amk_status amk_decode_step_host(amk_ctx* ctx, int32_t token, int32_t pos, float*
  *     n_kv_heads * (group + 2) * head_dim + ffn))
  *     is rejected with AMK_ERR_OOM and a message giving both sizes.
  *   - Allocation: none.  No cudaMalloc, cudaFree or allocating library call.
- *   - Set-up: the first call on each device looks up the array's device
- *     address (cudaGetSymbolAddress) with that device current; make that
- *     first call before any stream capture.  The context's device must be
- *     the current device.
+ *   - Set-up: every call looks up the array's device address
+ *     (cudaGetSymbolAddress) in the current device's context, so that an
+ *     address never outlives its context (for example across a
+ *     cudaDeviceReset); the first call on a device may load the library's
+ *     device code, so make it before any stream capture.  The context's
+ *     device must be the current device.
  *   - Sharing: every call uses the same array and finds the previous call's
  *     contents there; the call zeroes the whole scratch plan itself (each
- *     call runs as launch 1, so old words would carry the awaited tags).
+ *     call runs with the tags of a context's first launch, so old words
+ *     would carry the awaited tags).
  *     Calls that overlap on the GPU (other streams, other threads, other
  *     contexts on the same device) race on the array and must not be made.
  *   - Synchronous: returns after the step has finished, with the device
  *     status of that step (AMK_ERR_TIMEOUT / AMK_ERR_DEVICE_CHECK poison the
- *     context as for amk_sync).  Checks and KV bookkeeping are those of
+ *     context as for amk_sync, and so does a CUDA error while waiting for
+ *     the step: AMK_ERR_CUDA).  Checks and KV bookkeeping are those of
  *     amk_decode_step.
  */
 amk_status amk_decode_step_static_scratch(amk_ctx* ctx, int32_t token, int32_t pos,
@@ -311,6 +315,25 @@ amk_status amk_debug_trace_step(amk_ctx* ctx, int32_t token, int32_t pos, float*
  */
 amk_status amk_debug_dequant(int32_t format, const amk_linear* lin, int32_t out_features,
                              int32_t in_features, float* out_dev, void* stream);
+
+/*
+ * Read-only HBM stream probe (measurement aid).  The decode step's floor is
+ * set by how fast the GPU can stream bytes it only reads (AMK "Problem
+ * statement": t_min = weight_bytes / HBM bandwidth); a copy benchmark moves
+ * every byte twice and may settle at a different rate.  This launches one
+ * pass over buf_dev (bytes: a non-zero multiple of 16384, 16-byte aligned),
+ * asynchronously on `stream`, so that the caller can time it with events:
+ *   mode 0: one CTA per SM keeps eight 16 KB cp.async.bulk copies in flight
+ *           into shared memory (the decode kernel's producer without its
+ *           consumers);
+ *   mode 1: 128-bit non-caching global loads from four CTAs per SM.
+ * out_dev (device, >= 8 * SM-count uint32 words) receives per-CTA checksum
+ * and failure words (a nonzero failure word: a copy did not land within
+ * 2 s).  Errors: AMK_ERR_INVALID_ARG for a bad mode, size or alignment,
+ * AMK_ERR_CUDA for a failed launch.
+ */
+amk_status amk_debug_hbm_read_probe(int32_t mode, const void* buf_dev, size_t bytes, uint32_t* out_dev,
+                                    size_t out_words, void* stream);
 
 #ifdef __cplusplus
 }

@@ -8,9 +8,11 @@ fixed 1 MiB array inside libamk.so instead of the context's workspace.
 
 Checked here through the C ABI: two calls in a row give the logits of the
 regular decode step (same tolerance as the other parity tests) and write
-the same K,V; a model whose per-step scratch exceeds the array is refused
-with AMK_ERR_OOM without harming the context.  Kept in a file of its own,
-collected last.
+the same K,V; the second call leaves the device's free memory and torch's
+allocator untouched (the first may load the library's device code, which
+holds the array); a model whose per-step scratch exceeds the array is
+refused with AMK_ERR_OOM without harming the context.  Kept in a file of
+its own, collected last.
 """
 import numpy as np
 import pytest
@@ -56,8 +58,16 @@ def test_two_calls_match_the_regular_step(amk, model):
         regular.sync()
         got.fill_(float("nan"))
         torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info(dev)[0]
+        stats0 = torch.cuda.memory_stats(dev)
         st = amk.amk_decode_step_static_scratch(no_alloc.ctx, tok, pos, got.data_ptr())
         assert st == amk.AMK_OK, amk.last_error(no_alloc.ctx)
+        free1 = torch.cuda.mem_get_info(dev)[0]
+        stats1 = torch.cuda.memory_stats(dev)
+        for key in ("allocation.all.allocated", "segment.all.allocated", "reserved_bytes.all.current"):
+            assert stats1.get(key, 0) == stats0.get(key, 0), key
+        if i > 0:   # the first call may load the library's device code (and the array with it)
+            assert free1 == free0, (free0, free1)
         diff = float((got - ref).abs().max())
         print(f"{model.name} call {i}: max |dlogit| vs regular step {diff:.3e}")
         assert np.isfinite(diff) and diff <= TOL

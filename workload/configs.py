@@ -188,7 +188,26 @@ WORKLOADS = {
 }
 
 
+# Profiling cases: the per-layer shapes of the 8B workloads with only four
+# layers (about 1 GB on the device with the 16K-position history), so that
+# a many-pass counter capture of one decode launch stays small.  Not bench
+# lines; the decode kernel runs them with the same tiles and schedule rules.
+PROFILE_WORKLOADS = {
+    "llama8b-int4-4l": Workload(replace(LLAMA_8B_INT4, name="llama8b-int4-4l", n_layers=4),
+                                prompt_len=16384, decode_steps=64,
+                                description="4 layers of the 8B int4 shape; KV 16384 + 64 decode"),
+    "llama8b-int8-4l": Workload(replace(LLAMA_8B_INT8, name="llama8b-int8-4l", n_layers=4),
+                                prompt_len=2048, decode_steps=128,
+                                description="4 layers of the 8B int8 shape; KV 2048 + 128 decode"),
+    "llama8b-bf16-4l": Workload(replace(LLAMA_8B_BF16, name="llama8b-bf16-4l", n_layers=4),
+                                prompt_len=2048, decode_steps=128,
+                                description="4 layers of the 8B bf16 shape; KV 2048 + 128 decode"),
+}
+
+
 def workload(name: str) -> Workload:
+    if name in PROFILE_WORKLOADS:
+        return PROFILE_WORKLOADS[name]
     return WORKLOADS[name]
 
 
