@@ -75,6 +75,9 @@ def lib():
         L.orc_prefill.restype = C.c_int
         L.orc_prefill.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights), C.c_void_p,
                                   C.POINTER(C.c_int32), C.c_int64, C.c_int64]
+        L.orc_prefill_batched.restype = C.c_int
+        L.orc_prefill_batched.argtypes = [C.POINTER(OrcConfig), C.POINTER(OrcWeights), C.c_void_p,
+                                          C.POINTER(C.c_int32), C.c_int64, C.c_int64]
         L.orc_set_threads.argtypes = [C.c_int]
         L.orc_get_threads.restype = C.c_int
         _lib = L
@@ -235,6 +238,7 @@ class OracleModel:
         return out
 
     def prefill(self, kv: torch.Tensor, tokens, start_pos: int = 0):
+        """Sequential decode steps without logits (orc_prefill)."""
         self._check_kv(kv)
         t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
         rc = lib().orc_prefill(C.byref(self._cfg), C.byref(self._weights),
@@ -242,6 +246,17 @@ class OracleModel:
                                t.ctypes.data_as(C.POINTER(C.c_int32)), t.size, int(start_pos))
         if rc != 0:
             raise ValueError("oracle prefill rejected its arguments")
+
+    def prefill_batched(self, kv: torch.Tensor, tokens, start_pos: int = 0):
+        """The batched causal prefill (orc_prefill_batched): layer-major over
+        all the prompt's tokens."""
+        self._check_kv(kv)
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        rc = lib().orc_prefill_batched(C.byref(self._cfg), C.byref(self._weights),
+                                       C.c_void_p(kv.data_ptr()),
+                                       t.ctypes.data_as(C.POINTER(C.c_int32)), t.size, int(start_pos))
+        if rc != 0:
+            raise ValueError("oracle batched prefill rejected its arguments")
 
 
 def library_path() -> str:

@@ -311,3 +311,80 @@ int orc_prefill(const orc_config* c, const orc_weights* w, uint16_t* kv,
     }
     return 0;
 }
+
+/* The prefill as the pages' batched form of the same decoder: every layer
+ * processes all n prompt tokens before the next layer starts (a separate
+ * loop nest from orc_prefill's token-by-token steps).  Per layer: RMSNorm
+ * and the Q, K, V maps of every token; RoPE of each token at its position;
+ * the K, V rows of all n positions written to the cache; causal attention
+ * of token t over positions [0, start_pos + t]; the O map and residual; the
+ * SwiGLU block and residual.  Each element is computed by the same
+ * operations in the same order as in a decode step, so the cache it leaves
+ * equals orc_prefill's bit for bit. */
+int orc_prefill_batched(const orc_config* c, const orc_weights* w, uint16_t* kv,
+                        const int32_t* tokens, int64_t n, int64_t start_pos) {
+    if (check_config(c) || !w || !kv || (n > 0 && !tokens) || n < 0) return -1;
+    if (start_pos < 0 || start_pos + n > c->max_seq) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        if (tokens[t] < 0 || tokens[t] >= c->vocab) return -1;
+    if (n == 0) return 0;
+    const int64_t H = c->hidden, F = c->ffn, hd = c->head_dim;
+    const int64_t qd = (int64_t)c->n_heads * hd, kvd = (int64_t)c->n_kv_heads * hd;
+    const int64_t layer_stride = 2 * kvd * c->max_seq;
+    const int64_t kv_half = kvd * c->max_seq;
+
+    double* X = (double*)malloc(sizeof(double) * (size_t)(n * H));    /* residual rows */
+    double* Hn = (double*)malloc(sizeof(double) * (size_t)(n * H));   /* normed rows */
+    double* Q = (double*)malloc(sizeof(double) * (size_t)(n * qd));
+    double* K = (double*)malloc(sizeof(double) * (size_t)(n * kvd));
+    double* V = (double*)malloc(sizeof(double) * (size_t)(n * kvd));
+    double* O = (double*)malloc(sizeof(double) * (size_t)(n * qd));
+    double* Y = (double*)malloc(sizeof(double) * (size_t)H);
+    double* G = (double*)malloc(sizeof(double) * (size_t)F);
+    double* U = (double*)malloc(sizeof(double) * (size_t)F);
+
+    for (int64_t t = 0; t < n; ++t)
+        for (int64_t i = 0; i < H; ++i)
+            X[t * H + i] = orc_bf16_to_double(w->embed[(int64_t)tokens[t] * H + i]);
+
+    for (int32_t l = 0; l < c->n_layers; ++l) {
+        const orc_layer* L = &w->layers[l];
+        uint16_t* kc = kv + l * layer_stride;
+        uint16_t* vc = kc + kv_half;
+        /* projections of every token, then RoPE at each token's position */
+        for (int64_t t = 0; t < n; ++t) {
+            orc_rmsnorm(X + t * H, L->attn_norm, H, c->rms_eps, Hn + t * H);
+            orc_linear_apply(&L->wq, qd, H, Hn + t * H, Q + t * qd);
+            orc_linear_apply(&L->wk, kvd, H, Hn + t * H, K + t * kvd);
+            orc_linear_apply(&L->wv, kvd, H, Hn + t * H, V + t * kvd);
+            orc_rope(Q + t * qd, c->n_heads, (int32_t)hd, start_pos + t, c->rope_theta);
+            orc_rope(K + t * kvd, c->n_kv_heads, (int32_t)hd, start_pos + t, c->rope_theta);
+        }
+        /* the K, V rows of all prompt positions */
+        for (int64_t t = 0; t < n; ++t)
+            for (int32_t gh = 0; gh < c->n_kv_heads; ++gh)
+                for (int64_t d = 0; d < hd; ++d) {
+                    const int64_t at = ((int64_t)gh * c->max_seq + start_pos + t) * hd + d;
+                    kc[at] = orc_bf16_from_double(K[t * kvd + gh * hd + d]);
+                    vc[at] = orc_bf16_from_double(V[t * kvd + gh * hd + d]);
+                }
+        /* causal attention: token t sees positions 0 .. start_pos + t */
+        for (int64_t t = 0; t < n; ++t)
+            orc_attention(Q + t * qd, kc, vc, c->n_heads, c->n_kv_heads, (int32_t)hd, c->max_seq,
+                          start_pos + t + 1, O + t * qd);
+        /* O map + residual, then the SwiGLU block + residual, per token */
+        for (int64_t t = 0; t < n; ++t) {
+            double* x = X + t * H;
+            orc_linear_apply(&L->wo, H, qd, O + t * qd, Y);
+            for (int64_t i = 0; i < H; ++i) x[i] += Y[i];
+            orc_rmsnorm(x, L->ffn_norm, H, c->rms_eps, Hn + t * H);
+            orc_linear_apply(&L->wg, F, H, Hn + t * H, G);
+            orc_linear_apply(&L->wu, F, H, Hn + t * H, U);
+            for (int64_t j = 0; j < F; ++j) G[j] = orc_silu(G[j]) * U[j];
+            orc_linear_apply(&L->wd, H, F, G, Y);
+            for (int64_t i = 0; i < H; ++i) x[i] += Y[i];
+        }
+    }
+    free(X); free(Hn); free(Q); free(K); free(V); free(O); free(Y); free(G); free(U);
+    return 0;
+}

@@ -117,6 +117,12 @@ int orc_logits_rows(const orc_config* cfg, const orc_weights* w, const double* x
 int orc_prefill(const orc_config* cfg, const orc_weights* w, uint16_t* kv,
                 const int32_t* tokens, int64_t n, int64_t start_pos);
 
+/* The same prefill as one batched, causal loop nest: layer by layer over
+ * all n tokens (projections, RoPE, the K,V rows of every position, causal
+ * attention, O map, SwiGLU block).  Leaves the cache orc_prefill leaves. */
+int orc_prefill_batched(const orc_config* cfg, const orc_weights* w, uint16_t* kv,
+                        const int32_t* tokens, int64_t n, int64_t start_pos);
+
 #ifdef __cplusplus
 }
 #endif

@@ -267,7 +267,8 @@ def kv_layers(a, b):
 ])
 def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, prompt, split, parts):
     """The tensor-core prefill (tcgen05 GEMMs, mma.sync attention) against
-    the oracle's batched causal prefill, then decode steps on top of it.
+    the oracle's batched causal prefill (orc_prefill_batched, itself pinned
+    equal to sequential decode steps), then decode steps on top of it.
 
     Layer 0's K,V come straight from the embedding, RMSNorm, the QKV GEMM
     and RoPE: within two bf16 steps of the oracle and >= 99.9% bit-identical
@@ -303,7 +304,7 @@ def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, promp
     else:
         dec.prefill(toks, 0)
     assert amk.amk_kv_length(dec.ctx) == prompt
-    om.prefill(kv_o, toks, 0)
+    om.prefill_batched(kv_o, toks, 0)
     dec.sync()
     (ok0, same0, worst0), same, rel_mean = kv_layers(dec.kv[:, :, :, :prompt], kv_o[:, :, :, :prompt])
     print(f"{variant} chunk {chunk} P {prompt} parts {parts or 3}: layer 0 identical {same0:.4f} "
@@ -356,19 +357,22 @@ def test_watchdog_reports_timeout_without_hanging(amk, dev):
 
 # ---------------------------------------------------------------- full size
 
-FULL = [("llama1b", 512), ("llama8b-bf16", 2048), ("llama8b-int8", 2048), ("llama8b-int4", 16384)]
+# (workload, KV history length, teacher-forced decode steps)
+FULL = [("llama1b", 512, 128), ("llama8b-bf16", 2048, 32), ("llama8b-int8", 2048, 16),
+        ("llama8b-int4", 16384, 8)]
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,prompt_len", FULL)
-def test_full_size_synthetic_kv(amk, orc, dev, name, prompt_len):
+@pytest.mark.parametrize("name,prompt_len,steps", FULL)
+def test_full_size_teacher_forced(amk, orc, dev, name, prompt_len, steps):
     """Full-size model in the launch configuration the benchmark times (one
-    CTA per SM): the KV history [0, P) is a seeded synthetic input given to
-    both sides, then two decode steps at P and P+1 are compared on every
-    logit."""
+    CTA per SM), teacher-forced: the KV history [0, P) is a seeded synthetic
+    input given to both sides, then `steps` decode steps at P, P+1, ... on
+    the seeded token stream are compared on every logit (max |dlogit| <=
+    5e-2 at every step, top-1 agreement >= 99%), and the K,V rows the steps
+    append are compared layer by layer with the oracle's."""
     wl = wc.workload(name)
     cfg = wl.model
-    steps = 2
     max_seq = prompt_len + steps
     w = synth.model_weights(cfg, seed=0, device=dev)
     kv = synth.synthetic_kv_cache(cfg, prompt_len, max_seq, device=dev)
@@ -380,22 +384,29 @@ def test_full_size_synthetic_kv(amk, orc, dev, name, prompt_len):
     dec.set_kv_length(prompt_len)
     logits = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
     toks = synth.decode_tokens(cfg, steps).tolist()
+    errs, agree = [], 0
     for i, tok in enumerate(toks):
         pos = prompt_len + i
         dec.decode_step(tok, pos, logits)
         ref = om.decode_step(kv_o, tok, pos)
         got = logits.double().cpu().numpy()
-        err = float(np.abs(got - ref).max())
-        print(f"{name} pos {pos}: max|dlogit| {err:.3e} (logit std {ref.std():.3f})")
-        assert err <= TOL
-        assert int(np.argmax(got)) == int(np.argmax(ref))
+        errs.append(float(np.abs(got - ref).max()))
+        agree += int(np.argmax(got) == np.argmax(ref))
     dec.sync()
-    # K,V written by the two steps agree with the oracle's within two bf16
-    # steps everywhere; at full depth the residual stream has drifted by
-    # ~1e-5 relative (fp32 and 28-bit hand-offs, attention sums on the
-    # tensor cores), which flips the bf16 rounding of a few percent of the
-    # entries of the deepest layers.
-    ok, same, worst = kv_close(kv[:, :, :, prompt_len:max_seq], kv_o[:, :, :, prompt_len:max_seq])
+    new = kv[:, :, :, prompt_len:max_seq]
+    new_o = kv_o[:, :, :, prompt_len:max_seq]
+    per_layer = [float((bits(new[l]) == bits(new_o[l])).mean()) for l in range(cfg.n_layers)]
+    print(f"{name}: {steps} steps, max|dlogit| {max(errs):.3e} (mean {np.mean(errs):.3e}), "
+          f"top-1 {agree / steps:.3f}; K,V bit-identical per layer "
+          + " ".join(f"{x:.3f}" for x in per_layer))
+    assert max(errs) <= TOL
+    assert agree / steps >= 0.99
+    # K,V the steps append agree with the oracle's within two bf16 steps
+    # everywhere; at full depth the residual stream has drifted by ~1e-5
+    # relative (fp32 and 28-bit hand-offs, attention sums on the tensor
+    # cores), which flips the bf16 rounding of a few percent of the entries
+    # of the deepest layers.
+    ok, same, worst = kv_close(new, new_o)
     print(f"{name}: kv bit-identical {same:.4f}, worst diff / allowance {worst:.3f}")
     assert ok and same > 0.98
     dec.close()

@@ -448,6 +448,39 @@ def test_prefill_equals_sequential_steps_and_leaves_tail(oracle):
     assert not kv1[:, :, :, len(toks):].float().abs().sum().item()
 
 
+@pytest.mark.parametrize("variant", ["tiny", "int4", "mha"])
+def test_batched_prefill_equals_sequential_decode(oracle, variant):
+    """The batched causal prefill (a separate, layer-major loop nest) leaves
+    the cache that token-by-token decode steps leave, bit for bit, also
+    when it continues a history (start_pos > 0), and the decode step that
+    follows sees the same logits."""
+    base = dict(wc.TINY.__dict__)
+    if variant == "int4":
+        base.update(weight_format="int4", ffn=768)
+    elif variant == "mha":
+        base.update(n_kv_heads=4)
+    cfg = wc.ModelConfig(**base)
+    w = synth.model_weights(cfg, seed=9)
+    m = oracle.OracleModel(w, 24)
+    toks = synth.prompt_tokens(cfg, 20).tolist()
+    seq = synth.empty_kv_cache(cfg, 24)
+    for p, t in enumerate(toks):
+        m.decode_step(seq, t, p, logits=False)
+    bat = synth.empty_kv_cache(cfg, 24)
+    m.prefill_batched(bat, toks[:7], 0)
+    m.prefill_batched(bat, toks[7:], 7)
+    assert np.array_equal(bf16_bits(seq), bf16_bits(bat))
+    assert bat[:, :, :, :20].float().abs().sum().item() > 0
+    assert not bat[:, :, :, 20:].float().abs().sum().item()
+    a = m.decode_step(seq, 5, 20)
+    b = m.decode_step(bat, 5, 20)
+    assert np.array_equal(a, b)
+    with pytest.raises(ValueError):
+        m.prefill_batched(bat, [cfg.vocab], 0)
+    with pytest.raises(ValueError):
+        m.prefill_batched(bat, [1, 2, 3, 4, 5], 20)   # beyond max_seq
+
+
 def test_decode_step_is_layers_then_logits(oracle):
     """The sampled halves compose to the full step exactly (same arithmetic)."""
     for cfg in (wc.TINY, wc.ModelConfig(**{**wc.TINY.__dict__, "weight_format": "int4", "ffn": 768}),
