@@ -1129,7 +1129,8 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
     // the D entries it keeps) all lie in its segment sg, i.e. at k in
     // [256w + 64 sg, + 64) of every tile: quantisation group 2w + (sg >> 1)
     // of the tile, so one zero point and one scale per row serve all four
-    // k blocks.  Side data: fp16 scales [16][16], then u8 zeros [16][16].
+    // k blocks.  Side data: fp16 scales [16 groups][2 row parities][8],
+    // then u8 zeros in the same order.
     const int sg = (lane >> 2) & 3;
     const bool keep = (lane & 1) == (sg >> 1);
     const bool odd = (sg & 1) != 0;
@@ -1152,13 +1153,19 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
           uint4 v[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) v[j] = lds128(tile + unit0 + (uint32_t)j * 512u);
+          // the scales and zero points of the lane's 8 rows (R = 4q + rl and
+          // R + 2 for q = 0..3: the rows of parity rl) in its group: 16 + 8
+          // contiguous bytes of the side data (pack_kernel)
+          const uint4 sc = lds128(side + (uint32_t)(gq * 2 + rl) * 16u);
+          const uint2 zz = lds64(side + 512u + (uint32_t)(gq * 2 + rl) * 8u);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const int R = 4 * q + rl;
-            const uint32_t zc0 = u4_zc(lds8(side + 512u + (uint32_t)(R * 16 + gq)));
-            const uint32_t zc1 = u4_zc(lds8(side + 512u + (uint32_t)((R + 2) * 16 + gq)));
-            const float s0 = fp16_bits_to_float((uint16_t)lds16(side + (uint32_t)(R * 16 + gq) * 2));
-            const float s1 = fp16_bits_to_float((uint16_t)lds16(side + (uint32_t)((R + 2) * 16 + gq) * 2));
+            // row R: entry 2q, row R + 2: entry 2q + 1
+            const uint32_t zw = q < 2 ? zz.x : zz.y;
+            const uint32_t zc0 = __byte_perm(zw, 0x64u, (q & 1) ? 0x4242u : 0x4040u);
+            const uint32_t zc1 = __byte_perm(zw, 0x64u, (q & 1) ? 0x4343u : 0x4141u);
+            const uint32_t sw = q == 0 ? sc.x : q == 1 ? sc.y : q == 2 ? sc.z : sc.w;
+            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sw));
             const uint32_t zf0 = u4_zf(zc0), zf1 = u4_zf(zc1);
             float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1170,8 +1177,8 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
             }
             const float e0 = keep ? (odd ? d[1] : d[0]) : 0.f;
             const float e2 = keep ? (odd ? d[3] : d[2]) : 0.f;
-            acc[q][0] = fmaf(s0, e0, acc[q][0]);
-            acc[q][1] = fmaf(s1, e2, acc[q][1]);
+            acc[q][0] = fmaf(s01.x, e0, acc[q][0]);
+            acc[q][1] = fmaf(s01.y, e2, acc[q][1]);
           }
         }
         __syncwarp();
@@ -1956,7 +1963,7 @@ __global__ void pack_kernel(const PackArgs a) {
   if (a.fmt == AMK_FORMAT_INT4) {
     // tensor-core fragment order (gemv_task, u4_fragment): 32-bit words
     // ((w * 4 + j) * 32 + lane) * 4 + rq of each 16 x 2048 tile, then the
-    // side data: fp16 scales [16][16], u8 zeros [16][16] per tile
+    // side data: fp16 scales [16 groups][2][8], u8 zeros [16][2][8] per tile
     const int ng_pad = M.Kp / 128;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -1972,9 +1979,13 @@ __global__ void pack_kernel(const PackArgs a) {
           const uint8_t zbyte = static_cast<const uint8_t*>(a.z[src])[(int64_t)row * zb + gg / 2];
           zz = (gg & 1) ? (zbyte >> 4) : (zbyte & 15);
         }
+        // side data of the tile: scales, then zero points, each ordered
+        // [group][row parity][row / 2], so that the 8 rows of one parity in
+        // one group (a lane's rows in gemv_task) are contiguous
         uint8_t* side = const_cast<uint8_t*>(M.base) + ((int64_t)(pr / 16) * M.nkt + gg / 16) * M.stage_bytes + kStageBytes;
-        reinterpret_cast<uint16_t*>(side)[(pr % 16) * 16 + gg % 16] = sc;
-        side[512 + (pr % 16) * 16 + gg % 16] = zz;
+        const int r16 = pr % 16, si = ((gg % 16) * 2 + (r16 & 1)) * 8 + (r16 >> 1);
+        reinterpret_cast<uint16_t*>(side)[si] = sc;
+        side[512 + si] = zz;
       }
       const int64_t per_rb = (int64_t)M.nkt * 4096;
       const int rb = (int)(idx / per_rb);
