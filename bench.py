@@ -67,7 +67,7 @@ def parse_args(argv=None):
     ap.add_argument("--prefill-chunk", type=int, default=0,
                     help="tokens per tensor-core prefill chunk (0: library default; -1: decode steps)")
     ap.add_argument("--prefill-parts", type=int, default=0,
-                    help="bf16 parts of the prefill GEMM activations (0: library default, 3; or 2)")
+                    help="bf16 parts of the prefill GEMM activations (0: library default, 2; or 3)")
     ap.add_argument("--kv", choices=["auto", "prefill", "synthetic"], default="auto",
                     help="KV history of the first P positions: the prompt's prefill, or a seeded "
                          "synthetic history (auto: prefill for bf16 weights up to 4096 tokens)")
@@ -562,7 +562,7 @@ def run_ours(args, wl, rank, world, local_rank):
             if last:
                 torch.cuda.profiler.stop()
             pf_ms.append(p0.elapsed_time(p1))
-        pf = prefill_block(wl, min(pf_ms), pf_ms, dec.prefill_chunk, args.prefill_parts or 3)
+        pf = prefill_block(wl, min(pf_ms), pf_ms, dec.prefill_chunk, args.prefill_parts or 2)
         if args.prefill_only:
             dec.close()
             return {"impl": "ours", "workload": wl.name, "prefill": pf}

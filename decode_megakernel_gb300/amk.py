@@ -78,6 +78,8 @@ def _load():
         "amk_kv_cache_bytes": (C.c_size_t, [cfgp]),
         "amk_load_weights": (C.c_int, [cfgp, C.POINTER(amk_weights), P, C.c_size_t, P, P, schp,
                                        C.POINTER(P)]),
+        "amk_load_weights_requeued": (C.c_int, [cfgp, C.POINTER(amk_weights), P, C.c_size_t, P, P, schp, P,
+                                                C.c_size_t, C.POINTER(P)]),
         "amk_prefill": (C.c_int, [P, C.POINTER(C.c_int32), C.c_int32, C.c_int32]),
         "amk_decode_step": (C.c_int, [P, C.c_int32, C.c_int32, P]),
         "amk_decode_step_host": (C.c_int, [P, C.c_int32, C.c_int32, P]),
@@ -91,6 +93,7 @@ def _load():
         "amk_last_error": (C.c_char_p, [P]),
         "amk_build_schedule": (C.c_int, [cfgp, schp, P, C.c_size_t, C.POINTER(C.c_size_t)]),
         "amk_validate_serialized": (C.c_int, [P, C.c_size_t, C.c_char_p, C.c_size_t]),
+        "amk_validate_requeued": (C.c_int, [cfgp, schp, P, C.c_size_t, C.c_char_p, C.c_size_t]),
         "amk_debug_watchdog_probe": (C.c_int, [P, P, C.c_int32, C.POINTER(C.c_int32)]),
         "amk_debug_trace_bytes": (C.c_size_t, [P, C.POINTER(C.c_int32)]),
         "amk_debug_trace_step": (C.c_int, [P, C.c_int32, C.c_int32, P, P, C.c_size_t]),
@@ -141,6 +144,16 @@ def amk_load_weights(cfg, weights, workspace_ptr, workspace_bytes, kv_ptr, strea
     st = lib.amk_load_weights(C.byref(cfg), C.byref(weights), C.c_void_p(workspace_ptr),
                               workspace_bytes, C.c_void_p(kv_ptr), C.c_void_p(stream_ptr),
                               C.byref(sched) if sched else None, C.byref(ctx))
+    return st, ctx
+
+
+def amk_load_weights_requeued(cfg, weights, workspace_ptr, workspace_bytes, kv_ptr, stream_ptr, sched,
+                              schedule: bytes):
+    ctx = C.c_void_p()
+    st = lib.amk_load_weights_requeued(C.byref(cfg), C.byref(weights), C.c_void_p(workspace_ptr),
+                                       workspace_bytes, C.c_void_p(kv_ptr), C.c_void_p(stream_ptr),
+                                       C.byref(sched) if sched else None, schedule, len(schedule),
+                                       C.byref(ctx))
     return st, ctx
 
 
@@ -202,6 +215,12 @@ def amk_build_schedule(cfg: amk_config, sched: amk_schedule_config | None = None
 def amk_validate_serialized(blob: bytes):
     rep = C.create_string_buffer(512)
     st = lib.amk_validate_serialized(blob, len(blob), rep, 512)
+    return int(st), rep.value.decode()
+
+
+def amk_validate_requeued(cfg: amk_config, sched: amk_schedule_config | None, blob: bytes):
+    rep = C.create_string_buffer(512)
+    st = lib.amk_validate_requeued(C.byref(cfg), C.byref(sched) if sched else None, blob, len(blob), rep, 512)
     return int(st), rep.value.decode()
 
 
@@ -270,7 +289,10 @@ class Decoder:
     wq..wd objects carrying .w / .scales / .zeros)."""
 
     def __init__(self, weights, max_seq: int, stream: torch.cuda.Stream | None = None,
-                 sched: amk_schedule_config | None = None, kv_cache: torch.Tensor | None = None):
+                 sched: amk_schedule_config | None = None, kv_cache: torch.Tensor | None = None,
+                 schedule: bytes | None = None):
+        """schedule: optional serialised re-queueing of the lowering's tasks
+        (amk_load_weights_requeued); None loads the library's own lowering."""
         cfg = weights.cfg
         self.model = cfg
         self.cfg = make_config(cfg, max_seq)
@@ -294,8 +316,13 @@ class Decoder:
         w = amk_weights(_ptr(weights.embed), _ptr(weights.final_norm),
                         _linear(weights.lm_head) if weights.lm_head is not None else amk_linear(),
                         C.cast(layers, C.POINTER(amk_layer_weights)))
-        st, ctx = amk_load_weights(self.cfg, w, self.workspace.data_ptr(), nbytes,
-                                   self.kv.data_ptr(), self.stream.cuda_stream, sched)
+        if schedule is None:
+            st, ctx = amk_load_weights(self.cfg, w, self.workspace.data_ptr(), nbytes,
+                                       self.kv.data_ptr(), self.stream.cuda_stream, sched)
+        else:
+            st, ctx = amk_load_weights_requeued(self.cfg, w, self.workspace.data_ptr(), nbytes,
+                                                self.kv.data_ptr(), self.stream.cuda_stream, sched,
+                                                bytes(schedule))
         check(st)
         self.ctx = ctx
 

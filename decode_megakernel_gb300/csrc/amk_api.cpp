@@ -521,6 +521,40 @@ size_t amk_workspace_bytes(const amk_config* cfg, const amk_schedule_config* sch
   return make_layout(g, s).total;
 }
 
+amk_status amk_validate_requeued(const amk_config* cfg, const amk_schedule_config* sched, const void* buf,
+                                size_t bytes, char* report, size_t cap) {
+  auto put = [&](const std::string& m) {
+    if (report && cap) {
+      size_t n = m.size() < cap - 1 ? m.size() : cap - 1;
+      std::memcpy(report, m.data(), n);
+      report[n] = 0;
+    }
+  };
+  ModelGeom g;
+  Schedule own, given, mine;
+  std::string why;
+  amk_status st = plan(cfg, sched, &g, &own, &why);
+  if (st != AMK_OK) {
+    put(why);
+    return fail(nullptr, st, why);
+  }
+  if (!buf || bytes % sizeof(int64_t) ||
+      !deserialize(static_cast<const int64_t*>(buf), bytes / sizeof(int64_t), &given, &why)) {
+    why = "malformed schedule: " + (why.empty() ? std::string("buffer is NULL or not whole int64 words") : why);
+    put(why);
+    return fail(nullptr, AMK_ERR_SCHEDULE_INVALID, why);
+  }
+  if (!requeue(own, given, &mine, &why)) {
+    why = "schedule does not re-queue this model's tasks: " + why;
+    put(why);
+    return fail(nullptr, AMK_ERR_SCHEDULE_INVALID, why);
+  }
+  Report r = validate(mine);
+  put(r.msg);
+  if (!r.ok) return fail(nullptr, AMK_ERR_SCHEDULE_INVALID, r.msg);
+  return AMK_OK;
+}
+
 amk_status amk_build_schedule(const amk_config* cfg, const amk_schedule_config* sched, void* buf,
                               size_t cap, size_t* needed) {
   ModelGeom g;
@@ -561,9 +595,16 @@ amk_status amk_validate_serialized(const void* buf, size_t bytes, char* report, 
   return AMK_OK;
 }
 
-amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, void* workspace_dev,
-                            size_t workspace_bytes, void* kv_cache_dev, void* stream,
-                            const amk_schedule_config* sched, amk_ctx** out) {
+}  // extern "C"
+
+namespace {
+
+// amk_load_weights, optionally with the lowering's tasks re-queued as a
+// given serialised schedule assigns them (amk_load_weights_requeued)
+amk_status load_impl(const amk_config* cfg, const amk_weights* weights, void* workspace_dev,
+                     size_t workspace_bytes, void* kv_cache_dev, void* stream,
+                     const amk_schedule_config* sched, const void* requeue_buf, size_t requeue_bytes,
+                     amk_ctx** out) {
   if (!out) return fail(nullptr, AMK_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!cfg || !weights || !workspace_dev || !kv_cache_dev)
@@ -585,6 +626,15 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   if (st != AMK_OK) return bail(fail(ctx, st, why));
   const amk_config& c = *cfg;
   const ModelGeom& g = ctx->geom;
+  if (requeue_buf) {
+    Schedule given, mine;
+    if (requeue_bytes % sizeof(int64_t) ||
+        !deserialize(static_cast<const int64_t*>(requeue_buf), requeue_bytes / sizeof(int64_t), &given, &why))
+      return bail(fail(ctx, AMK_ERR_SCHEDULE_INVALID, "malformed schedule: " + why));
+    if (!requeue(s, given, &mine, &why))
+      return bail(fail(ctx, AMK_ERR_SCHEDULE_INVALID, "schedule does not re-queue this model's tasks: " + why));
+    s = std::move(mine);
+  }
 
   // the safety gate: nothing is launched for a schedule that fails it
   Report rep = validate(s);
@@ -795,6 +845,28 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
   ctx->kv_len = 0;
   *out = ctx;
   return AMK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, void* workspace_dev,
+                            size_t workspace_bytes, void* kv_cache_dev, void* stream,
+                            const amk_schedule_config* sched, amk_ctx** out) {
+  return load_impl(cfg, weights, workspace_dev, workspace_bytes, kv_cache_dev, stream, sched, nullptr, 0, out);
+}
+
+amk_status amk_load_weights_requeued(const amk_config* cfg, const amk_weights* weights, void* workspace_dev,
+                                     size_t workspace_bytes, void* kv_cache_dev, void* stream,
+                                     const amk_schedule_config* sched, const void* schedule,
+                                     size_t schedule_bytes, amk_ctx** out) {
+  if (!schedule) {
+    if (out) *out = nullptr;
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "schedule is NULL");
+  }
+  return load_impl(cfg, weights, workspace_dev, workspace_bytes, kv_cache_dev, stream, sched, schedule,
+                   schedule_bytes, out);
 }
 
 namespace {

@@ -38,7 +38,7 @@ constexpr int kPfBM = 128;      // tokens per GEMM tile (MMA M, TMEM lanes)
 constexpr int kPfBN = 256;      // packed weight rows per GEMM tile (MMA N, TMEM columns)
 constexpr int kPfBK = 64;       // k per pipeline stage: one 128-byte swizzled row
 constexpr int kPfParts = 3;     // bf16 parts of a GEMM activation operand at most (buffers, maps)
-constexpr int kPfDefaultParts = 3;
+constexpr int kPfDefaultParts = 2;
 // The tensor cores' fp32 accumulation truncates (measured: a bias toward
 // zero that grows with K, ~1e-7 of the sum of |terms| at K = 4096 against
 // ~1e-10 for an fp32 FMA chain), so the GEMM accumulates in TMEM only over

@@ -3,6 +3,8 @@
 #include "schedule.hpp"
 
 #include <algorithm>
+#include <array>
+#include <map>
 #include <cstdio>
 #include <cstring>
 #include <numeric>
@@ -706,6 +708,64 @@ bool deserialize(const int64_t* w, size_t n, Schedule* out, std::string* why) {
     s.body_len[q] = (int32_t)r[2];
   }
   *out = std::move(s);
+  return true;
+}
+
+// ------------------------------------------------------------- requeue
+
+bool requeue(const Schedule& own, const Schedule& given, Schedule* out, std::string* why) {
+  auto bad = [&](const std::string& m) {
+    *why = m;
+    return false;
+  };
+  if (given.tasks.size() != own.tasks.size())
+    return bad(fmt_msg("the schedule has %lld tasks, the model's lowering %lld", (long long)given.tasks.size(),
+                       (long long)own.tasks.size()));
+  if (given.queues.size() != own.queues.size() || given.body_len.size() != own.queues.size())
+    return bad(fmt_msg("the schedule has %lld queues, the launch %lld CTAs", (long long)given.queues.size(),
+                       (long long)own.queues.size()));
+  // the lowering's task with the same type, layer and parameters
+  using Key = std::array<int64_t, 6>;
+  auto key = [](const Task& t) { return Key{t.type, t.layer, t.a[0], t.a[1], t.a[2], t.a[3]}; };
+  std::map<Key, int32_t> by_key;
+  for (size_t i = 0; i < own.tasks.size(); ++i)
+    if (!by_key.emplace(key(own.tasks[i]), (int32_t)i).second) return bad("the lowering has duplicate tasks");
+  std::vector<int32_t> map_to(given.tasks.size(), -1);
+  std::vector<char> used(own.tasks.size(), 0);
+  for (size_t i = 0; i < given.tasks.size(); ++i) {
+    auto it = by_key.find(key(given.tasks[i]));
+    if (it == by_key.end()) return bad(fmt_msg("task %lld is not a task of this model's lowering", (long long)i));
+    if (used[it->second]) return bad(fmt_msg("task %lld appears twice", (long long)i));
+    used[it->second] = 1;
+    map_to[i] = it->second;
+  }
+  Schedule r;
+  r.buffers = own.buffers;
+  r.versions = own.versions;
+  r.tasks = own.tasks;
+  r.queues.assign(given.queues.size(), {});
+  r.body_len = given.body_len;
+  std::vector<char> queued(own.tasks.size(), 0);
+  for (size_t q = 0; q < given.queues.size(); ++q) {
+    const auto& items = given.queues[q];
+    const int body = given.body_len[q];
+    if (body < 0 || body > (int)items.size()) return bad(fmt_msg("queue %lld: bad body length", (long long)q));
+    for (size_t i = 0; i < items.size(); ++i) {
+      const int32_t gt = items[i];
+      if (gt < 0 || gt >= (int32_t)given.tasks.size()) return bad(fmt_msg("queue %lld: bad task id", (long long)q));
+      const int32_t t = map_to[gt];
+      if (queued[t]) return bad(fmt_msg("queue %lld: a task is queued twice", (long long)q));
+      queued[t] = 1;
+      const bool lm = r.tasks[t].type == T_LMHEAD;
+      if (lm != ((int)i >= body))
+        return bad(fmt_msg("queue %lld: LM-head tasks must follow the body, and only they", (long long)q));
+      r.tasks[t].queue = (int32_t)q;
+      r.queues[q].push_back(t);
+    }
+  }
+  for (size_t t = 0; t < queued.size(); ++t)
+    if (!queued[t]) return bad(fmt_msg("task %lld of the lowering is in no queue", (long long)t));
+  *out = std::move(r);
   return true;
 }
 

@@ -169,4 +169,15 @@ Report validate(const Schedule& s);
 std::vector<int64_t> serialize(const Schedule& s);
 bool deserialize(const int64_t* w, size_t n_words, Schedule* out, std::string* why);
 
+// A re-queued lowering: the tasks of `own` (the library's lowering of a
+// model, whose accesses describe what the kernel does for each task's
+// parameters) placed in the queues, order and body lengths that `given`
+// (a serialised schedule from anywhere) assigns them.  `given` must hold
+// exactly the tasks of `own`, matched by (type, layer, a0..a3); its own
+// access lists are ignored.  Every queue must list its LM-head tasks after
+// its body and nothing else there (a step that skips the LM head runs the
+// body alone).  Returns false with the reason for anything else; the
+// result still has to pass validate() before it may run.
+bool requeue(const Schedule& own, const Schedule& given, Schedule* out, std::string* why);
+
 }  // namespace amk

@@ -118,8 +118,8 @@ typedef struct {
                                    -1: prefill through the decode kernel, one launch per
                                    token (always so for int8 / int4 weights) */
     int32_t prefill_parts;      /* bf16 parts per activation operand of the prefill GEMMs:
-                                   0 or 3: three (fp32-level products, the default); 2: two
-                                   (2^-18 relative, two thirds of the tensor work) */
+                                   0 or 2: two (activations to 2^-18 relative, the default);
+                                   3: three (fp32-level products, 1.5x the tensor work) */
 } amk_schedule_config;
 
 typedef struct amk_ctx amk_ctx;
@@ -158,6 +158,27 @@ size_t amk_kv_cache_bytes(const amk_config* cfg);
 amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights,
                             void* workspace_dev, size_t workspace_bytes, void* kv_cache_dev,
                             void* stream, const amk_schedule_config* sched, amk_ctx** out);
+
+/*
+ * amk_load_weights with the task queues of a given schedule: the schedule
+ * search's way to run a structural edit of the lowering (which CTA runs a
+ * task, and in which order), the pages' "SM assignment" choices of the
+ * ScheduleConfig (AMK "Layer 2").  schedule (host, schedule_bytes bytes)
+ * is a serialised schedule in the format of amk_build_schedule that holds
+ * exactly the tasks of this model's own lowering for (cfg, sched), matched
+ * by type, layer and parameters, in any queues and order, with each
+ * queue's LM-head tasks after its body and only there.  The library takes
+ * the task set and every task's memory accesses from its own lowering and
+ * only the placement from the given schedule, then runs the safety gate on
+ * the result: a schedule that is malformed, holds other tasks, or fails the
+ * gate (for example a queue order that deadlocks) returns
+ * AMK_ERR_SCHEDULE_INVALID with the reason, and nothing is launched.
+ * Everything else is as amk_load_weights (same workspace size).
+ */
+amk_status amk_load_weights_requeued(const amk_config* cfg, const amk_weights* weights,
+                                     void* workspace_dev, size_t workspace_bytes, void* kv_cache_dev,
+                                     void* stream, const amk_schedule_config* sched,
+                                     const void* schedule, size_t schedule_bytes, amk_ctx** out);
 
 /*
  * Fill the KV cache with the K,V rows of host_tokens at positions
@@ -277,6 +298,16 @@ const char* amk_last_error(const amk_ctx* ctx);
 amk_status amk_build_schedule(const amk_config* cfg, const amk_schedule_config* sched,
                               void* buf, size_t cap, size_t* needed);
 amk_status amk_validate_serialized(const void* buf, size_t bytes, char* report, size_t cap);
+
+/*
+ * The host-side half of amk_load_weights_requeued (host only when
+ * sched->num_ctas > 0): checks that the serialised schedule in buf re-queues
+ * exactly the tasks of this model's lowering, rebuilds it with the
+ * lowering's own accesses and runs the safety gate on it; writes a
+ * one-line report.  AMK_OK means amk_load_weights_requeued would accept it.
+ */
+amk_status amk_validate_requeued(const amk_config* cfg, const amk_schedule_config* sched, const void* buf,
+                                 size_t bytes, char* report, size_t cap);
 
 /*
  * Watchdog probe (test aid): launches a small grid of the decode kernel's

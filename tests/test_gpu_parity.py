@@ -119,7 +119,11 @@ def test_tiny_variants(amk, orc, dev, variant):
     print(f"{variant}: max|dlogit| {err:.3e}, top-1 {agree:.3f}, kv same {ul[1]:.4f}, "
           f"kv worst/allow {ul[2]:.3f}")
     assert err <= TOL and agree >= 0.99
-    assert ul[0] and ul[1] > 0.99
+    # the prompt's K,V: bf16 variants run the tensor-core prefill, whose
+    # activations enter its GEMMs as two bf16 parts (2^-18 relative): every
+    # entry within two bf16 steps, and rounding flips inherited through the
+    # layers leave >= 98% bit-identical; the others prefill by decode steps
+    assert ul[0] and ul[1] > (0.98 if cfg.weight_format == "bf16" else 0.99)
 
 
 @pytest.mark.parametrize("knobs", [dict(num_ctas=37, attn_splits=5, max_rows_per_task=32),
@@ -257,13 +261,13 @@ def kv_layers(a, b):
 
 
 @pytest.mark.parametrize("variant,chunk,prompt,split,parts", [
-    ("tiny", 0, 12, None, 0),       # one chunk, one partial 128-token tile
+    ("tiny", 0, 12, None, 0),       # one chunk, one partial 128-token tile (default: two parts)
     ("tiny", 128, 300, 100, 0),     # two calls (history from the first), three chunks, ragged tail
     ("hd128", 128, 200, None, 0),   # head_dim 128, group 4
     ("mha", 0, 40, 17, 0),          # group 1
     ("tied", 256, 260, None, 0),
-    ("tiny", 128, 300, 100, 2),     # two activation parts
-    ("hd128", 0, 200, None, 2),
+    ("tiny", 128, 300, 100, 3),     # three activation parts
+    ("hd128", 0, 200, None, 3),
 ])
 def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, prompt, split, parts):
     """The tensor-core prefill (tcgen05 GEMMs, mma.sync attention) against
@@ -271,8 +275,9 @@ def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, promp
     equal to sequential decode steps), then decode steps on top of it.
 
     Layer 0's K,V come straight from the embedding, RMSNorm, the QKV GEMM
-    and RoPE: within two bf16 steps of the oracle and >= 99.9% bit-identical
-    (>= 99.5% with two activation parts, 2^-18 instead of 2^-27).
+    and RoPE: within two bf16 steps of the oracle and >= 99.5% bit-identical
+    with the default two activation parts (2^-18), >= 99.9% with three
+    (2^-27).
     Deeper layers inherit every bf16 rounding of the layers below: a V entry
     that rounds the other way moves the next layer's input by a bf16 step
     of that value (divided by the tokens attending to it), so the shares of
@@ -307,10 +312,10 @@ def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, promp
     om.prefill_batched(kv_o, toks, 0)
     dec.sync()
     (ok0, same0, worst0), same, rel_mean = kv_layers(dec.kv[:, :, :, :prompt], kv_o[:, :, :, :prompt])
-    print(f"{variant} chunk {chunk} P {prompt} parts {parts or 3}: layer 0 identical {same0:.4f} "
+    print(f"{variant} chunk {chunk} P {prompt} parts {parts or 2}: layer 0 identical {same0:.4f} "
           f"worst/allow {worst0:.3f}; per layer {' '.join(f'{x:.4f}' for x in same)}; "
           f"mean |diff| / mean |kv| {rel_mean:.2e}")
-    assert ok0 and same0 >= (0.995 if parts == 2 else 0.999)
+    assert ok0 and same0 >= (0.999 if parts == 3 else 0.995)
     assert min(same) >= 0.90 and rel_mean <= 1e-3
     logits = torch.empty(cfg.vocab, dtype=torch.float32, device=dev)
     for i, tok in enumerate(synth.decode_tokens(cfg, steps).tolist()):

@@ -276,3 +276,46 @@ def test_tag_alias_gate(amk, reader_first):
     assert (st == amk.AMK_OK) == ok, rep
     if reader_first:
         assert "alias" in rep and "alias" in why
+
+
+# --------------------------------------------------- re-queued lowerings
+
+@pytest.mark.parametrize("knobs", [dict(num_ctas=8), dict(num_ctas=37, attn_splits=5, max_rows_per_task=32)])
+def test_requeued_lowerings(amk, knobs):
+    """amk_validate_requeued (the gate of amk_load_weights_requeued): the
+    library's own lowering and placement-only edits of it pass; an edit
+    whose queue order deadlocks, a task that is not the lowering's, a lost
+    or duplicated task and an LM-head task inside a body are refused."""
+    from decode_megakernel_gb300 import schedule_ir as ir
+    from decode_megakernel_gb300 import tune
+    c = amk.make_config(wc.TINY, 48)
+    sched = amk.make_schedule_config(**knobs)
+    blob = amk.amk_build_schedule(c, sched)
+    s = ir.parse(blob)
+    assert ir.serialize(s) == blob
+    assert amk.amk_validate_requeued(c, sched, blob)[0] == amk.AMK_OK
+    for edit in ("rotate_queues:1", "rotate_queues:3", "spread_combines:1", "spread_combines:2"):
+        st, rep = amk.amk_validate_requeued(c, sched, tune.apply_edit(blob, edit))
+        assert st == amk.AMK_OK, (edit, rep)
+    st, rep = amk.amk_validate_requeued(c, sched, tune.apply_edit(blob, "hoist_next_layer"))
+    assert st == amk.AMK_ERR_SCHEDULE_INVALID and "cycle" in rep
+    foreign = ir.parse(blob)
+    foreign.tasks[0].params[0] += 1
+    assert amk.amk_validate_requeued(c, sched, ir.serialize(foreign))[0] == amk.AMK_ERR_SCHEDULE_INVALID
+    lost = ir.parse(blob)
+    q = next(i for i, items in enumerate(lost.queues) if len(items) > 1)
+    lost.queues[q].pop(0)
+    lost.body[q] -= 1
+    st, rep = amk.amk_validate_requeued(c, sched, ir.serialize(lost))
+    assert st == amk.AMK_ERR_SCHEDULE_INVALID and "no queue" in rep
+    dup = ir.parse(blob)
+    dup.queues[q].insert(0, dup.queues[q][0])
+    dup.body[q] += 1
+    assert amk.amk_validate_requeued(c, sched, ir.serialize(dup))[0] == amk.AMK_ERR_SCHEDULE_INVALID
+    lm_in_body = ir.parse(blob)
+    q = next(i for i, items in enumerate(lm_in_body.queues)
+             if any(lm_in_body.tasks[t].type == ir.T_LMHEAD for t in items))
+    lm_in_body.body[q] = len(lm_in_body.queues[q])
+    st, rep = amk.amk_validate_requeued(c, sched, ir.serialize(lm_in_body))
+    assert st == amk.AMK_ERR_SCHEDULE_INVALID and "LM-head" in rep
+    assert amk.amk_validate_requeued(c, sched, b"\x00" * 16)[0] == amk.AMK_ERR_SCHEDULE_INVALID
