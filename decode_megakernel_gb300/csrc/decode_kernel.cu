@@ -1491,13 +1491,20 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
         if (mt * 16 < n) {
           const int mi = lane >> 3, rr = lane & 7;
           const int pi = min(base + mt * 16 + rr + 8 * (mi & 1), plast);
+          // four independent accumulation chains (k-step parity x hi / lo
+          // part of q), summed once: a single chain serialises 2 KS mma
+          float acc4[4][4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc4[c][0] = acc4[c][1] = acc4[c][2] = acc4[c][3] = 0.f;
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
             uint32_t a[4];
             ldsm_x4(addr_of(pi, 2 * ks + (mi >> 1), 0), a);
-            mma_bf16_16816(sc[mt], a, qb[ks][0][0], qb[ks][1][0]);
-            mma_bf16_16816(sc[mt], a, qb[ks][0][1], qb[ks][1][1]);
+            mma_bf16_16816(acc4[2 * (ks & 1)], a, qb[ks][0][0], qb[ks][1][0]);
+            mma_bf16_16816(acc4[2 * (ks & 1) + 1], a, qb[ks][0][1], qb[ks][1][1]);
           }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[mt][e] = (acc4[0][e] + acc4[2][e]) + (acc4[1][e] + acc4[3][e]);
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e)
