@@ -53,7 +53,8 @@ class amk_schedule_config(C.Structure):
     _fields_ = [("num_ctas", C.c_int32), ("attn_splits", C.c_int32),
                 ("max_rows_per_task", C.c_int32), ("watchdog_ms", C.c_int32),
                 ("ring_slots", C.c_int32), ("l2_prefetch_tiles", C.c_int32),
-                ("prefill_chunk", C.c_int32), ("prefill_parts", C.c_int32)]
+                ("prefill_chunk", C.c_int32), ("prefill_parts", C.c_int32),
+                ("prefill_tile_rows", C.c_int32)]
 
 
 class AmkError(RuntimeError):
@@ -268,9 +269,11 @@ def make_config(model, max_seq: int) -> amk_config:
 
 
 def make_schedule_config(num_ctas=0, attn_splits=0, max_rows_per_task=0, watchdog_ms=0,
-                         ring_slots=0, l2_prefetch_tiles=0, prefill_chunk=0, prefill_parts=0):
+                         ring_slots=0, l2_prefetch_tiles=0, prefill_chunk=0, prefill_parts=0,
+                         prefill_tile_rows=0):
     return amk_schedule_config(num_ctas, attn_splits, max_rows_per_task, watchdog_ms,
-                               ring_slots, l2_prefetch_tiles, prefill_chunk, prefill_parts)
+                               ring_slots, l2_prefetch_tiles, prefill_chunk, prefill_parts,
+                               prefill_tile_rows)
 
 
 def _ptr(t):

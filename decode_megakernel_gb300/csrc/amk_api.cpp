@@ -56,6 +56,8 @@ struct amk_ctx {
     int32_t* tokens = nullptr;  // [max_seq]
     CUtensorMap a_h1[kPfParts], a_o[kPfParts], a_a[kPfParts];   // activation operands (parts)
     std::vector<CUtensorMap> w[M_NUM];     // weight operands per layer (QKV, O, gate/up, down)
+    int32_t tile_rows = 0;                 // schedule knob: 0 = chosen per matrix
+    int32_t bn[M_NUM] = {};                // GEMM tile width per matrix (the weight maps' box rows)
   } pf;
   std::string err;
 };
@@ -186,8 +188,10 @@ amk_status resolve_ctas(const amk_schedule_config* sched, BuildOptions* opt, std
     if (sched->num_ctas < 0 || sched->attn_splits < 0 || sched->max_rows_per_task < 0 ||
         sched->watchdog_ms < 0 || sched->ring_slots < 0 || sched->l2_prefetch_tiles < -1 ||
         sched->prefill_chunk < -1 || (sched->prefill_parts != 0 && sched->prefill_parts != 2 &&
-                                      sched->prefill_parts != 3)) {
-      *why = "negative schedule knob";
+                                      sched->prefill_parts != 3) ||
+        (sched->prefill_tile_rows != 0 && sched->prefill_tile_rows != kPfBN &&
+         sched->prefill_tile_rows != kPfBNNarrow)) {
+      *why = "schedule knob out of range";
       return AMK_ERR_INVALID_ARG;
     }
   }
@@ -300,8 +304,10 @@ amk_status encode_kv_map(amk_ctx* ctx, const amk_config& c, void* kv, CUtensorMa
 // Tensor maps of the tensor-core prefill.  Activation operands (each of
 // the kPfParts bf16 parts): [chunk][K] row major, boxes of 64 k x 128 tokens.  Weight operands: the
 // decode kernel's packed tiles of one layer's matrix as a 4-D tensor
-// {Kt, Rt, nkt, row blocks}, boxes {64, Rt, 1, 256 / Rt}, so that one box
-// is a 256-row x 64-k slice in plain row order.
+// {Kt, Rt, nkt, row blocks}, boxes {64, Rt, 1, bn / Rt}, so that one box
+// is a bn-row x 64-k slice in plain row order; bn (256 or 224 rows, both
+// multiples of every Rt) per matrix from prefill_gemm_bn for a full chunk
+// on this device's SMs.
 amk_status encode_prefill_maps(amk_ctx* ctx, const DevMat* mats) {
   const amk_config& c = ctx->cfg;
   auto& pf = ctx->pf;
@@ -318,14 +324,18 @@ amk_status encode_prefill_maps(amk_ctx* ctx, const DevMat* mats) {
     if (st == AMK_OK) st = act(&pf.a_a[i], pf.h2[i], (cuuint64_t)c.ffn);
     if (st != AMK_OK) return st;
   }
+  int sms = 0;
+  AMK_CUDA(ctx, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
   for (int k : {M_QKV, M_O, M_GU, M_DOWN}) {
     const DevMat& m = mats[k];
+    pf.bn[k] = pf.tile_rows ? pf.tile_rows : prefill_gemm_bn(m.rows, pf.chunk, sms);
+    if (pf.bn[k] % m.Rt != 0) pf.bn[k] = kPfBN;
     pf.w[k].resize(c.n_layers);
     const cuuint64_t dims[4] = {(cuuint64_t)m.Kt, (cuuint64_t)m.Rt, (cuuint64_t)m.nkt,
                                 (cuuint64_t)(m.rows_padded / m.Rt)};
     const cuuint64_t strides[3] = {(cuuint64_t)m.Kt * 2, (cuuint64_t)m.stage_bytes,
                                    (cuuint64_t)m.nkt * m.stage_bytes};
-    const cuuint32_t box[4] = {(cuuint32_t)kPfBK, (cuuint32_t)m.Rt, 1, (cuuint32_t)(kPfBN / m.Rt)};
+    const cuuint32_t box[4] = {(cuuint32_t)kPfBK, (cuuint32_t)m.Rt, 1, (cuuint32_t)(pf.bn[k] / m.Rt)};
     for (int l = 0; l < c.n_layers; ++l) {
       void* base = const_cast<uint8_t*>(m.base) + (int64_t)l * m.layer_bytes;
       amk_status st = encode_bf16_map(ctx, "prefill weights", &pf.w[k][l], base, 4, dims, strides, box);
@@ -831,6 +841,7 @@ amk_status load_impl(const amk_config* cfg, const amk_weights* weights, void* wo
     auto& pf = ctx->pf;
     pf.chunk = g.prefill_chunk;
     pf.parts = sched && sched->prefill_parts ? sched->prefill_parts : kPfDefaultParts;
+    pf.tile_rows = sched ? sched->prefill_tile_rows : 0;
     pf.x = (float*)(ws + L.pf_x);
     for (int i = 0; i < kPfParts; ++i) {
       pf.h1[i] = (uint16_t*)(ws + L.pf_h1[i]);
@@ -915,7 +926,7 @@ amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
     g.Kt = m.Kt;
     g.Rt = m.Rt;
     g.layer = layer;
-    return launch_prefill_gemm(epi, a, &pf.w[kind][layer], g, s);
+    return launch_prefill_gemm(epi, a, &pf.w[kind][layer], pf.bn[kind], g, s);
   };
   for (int32_t c0 = 0; c0 < n; c0 += pf.chunk) {
     const int T = std::min<int32_t>(pf.chunk, n - c0);
@@ -925,9 +936,9 @@ amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
     for (int l = 0; l < c.n_layers; ++l) {
       AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.attn_norm + l * H, c.rms_eps, pf.h1, pf.parts, s));
       AMK_CUDA(ctx, gemm(PE_QKV, M_QKV, l, pf.a_h1));
+      if (l == c.n_layers - 1) break;   // the rest of the last layer feeds no K,V
       at.layer = l;
       AMK_CUDA(ctx, launch_prefill_attn(at, s));
-      if (l == c.n_layers - 1) break;   // the rest of the last layer feeds no K,V
       AMK_CUDA(ctx, gemm(PE_RESID, M_O, l, pf.a_o));
       AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.ffn_norm + l * H, c.rms_eps, pf.h1, pf.parts, s));
       AMK_CUDA(ctx, gemm(PE_SWIGLU, M_GU, l, pf.a_h1));

@@ -1,6 +1,7 @@
 // Tensor-core prefill kernels (see prefill.hpp for the algorithm).
 //
-// GEMM: one 128-token x 256-row output tile per CTA.  Warp 0 (one thread)
+// GEMM: one 128-token x BN-row output tile per CTA (BN = 256, or 224 where
+// that fills the SMs better: prefill_gemm_bn).  Warp 0 (one thread)
 // streams k blocks of the activation parts and the weight slice through a
 // kPfStages-deep ring with TMA; warp 1 (one thread) issues tcgen05.mma
 // (kind::f16, bf16 x bf16 -> fp32, M 128, N 256, K 16) into one of two
@@ -13,8 +14,8 @@
 //
 // Attention: flash-attention over the KV cache with mma.sync (bf16 in,
 // fp32 accumulate), one CTA per (16 x attn_groups(G) query tokens, KV head),
-// one warp per (query head of the group, 16 tokens), all warps sharing the
-// CTA's K,V tiles; q and P split into bf16 hi + lo as in the decode
+// launched longest first, two CTAs per SM; one warp per (query head of the
+// group, 16 tokens), all warps sharing the CTA's K,V tiles; q and P split into bf16 hi + lo as in the decode
 // kernel's attention (softmax weights and pre-scaled scores need no more:
 // the attention's K,V are bf16 already).
 #include "device_model.hpp"
@@ -28,21 +29,22 @@ namespace amk {
 namespace {
 
 constexpr uint32_t kPfATile = kPfBM * kPfBK * 2;   // 16 KB: 128 tokens x 64 k, bf16
-constexpr uint32_t kPfBTile = kPfBN * kPfBK * 2;   // 32 KB: 256 rows x 64 k, bf16
-constexpr int kPfEpiCols = kPfBN / (kPfEpiWarps / 4);   // accumulator columns per epilogue warp
+constexpr int kPfTmemCols = 2 * kPfBN;             // two accumulator buffers kPfBN columns apart
 
 // one stage: the activation parts (128 x 64 bf16 each) and the weight
-// slice (256 x 64 bf16); as many stages as fit in 200 KB of shared memory
-template <int PARTS>
+// slice (BN x 64 bf16); as many stages as fit in 200 KB of shared memory
+template <int PARTS, int BN>
 struct GemmShape {
-  static constexpr int kStages = (200 * 1024) / (PARTS * (int)kPfATile + (int)kPfBTile);
+  static constexpr uint32_t kBTile = (uint32_t)BN * kPfBK * 2;   // BN rows x 64 k, bf16
+  static constexpr int kStages = (200 * 1024) / (PARTS * (int)kPfATile + (int)kBTile);
+  static constexpr int kEpiCols = BN / (kPfEpiWarps / 4);       // accumulator columns per epilogue warp
 };
 
-template <int PARTS>
+template <int PARTS, int BN>
 struct __align__(1024) GemmSmem {
-  static constexpr int S = GemmShape<PARTS>::kStages;
+  static constexpr int S = GemmShape<PARTS, BN>::kStages;
   uint8_t a[S][PARTS][kPfATile];
-  uint8_t w[S][kPfBTile];
+  uint8_t w[S][GemmShape<PARTS, BN>::kBTile];
   uint64_t full[S], empty[S];
   uint64_t acc_full[2], acc_empty[2];   // TMEM accumulator buffers: segment done / drained
   uint32_t tmem;
@@ -99,15 +101,19 @@ __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, M x N.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPfBN >> 3) << 17) |
-                            ((uint32_t)(kPfBM >> 4) << 24);
+// K-major, M = kPfBM x N = BN (a multiple of 16 up to 256).
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc_bf16() {
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kPfBM >> 4) << 24);
+}
 
+template <int BN>
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate));
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc_bf16<BN>()), "r"(accumulate));
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -187,23 +193,41 @@ __device__ __forceinline__ void gemm_epilogue(const PrefillGemm& g, int t, int n
     const int pos = g.s0 + t;
     if (n >= g.N) return;
     if (slot <= G) {
-      const float2* cs = g.rope + (int64_t)pos * half;
-      float* qrow = g.q + (int64_t)t * g.ldq + (int64_t)(grp * G + slot) * hd;
-      uint16_t* krow = g.kv + ((((int64_t)g.layer * 2 + 0) * g.n_kv + grp) * g.max_seq + pos) * hd;
+      // dims i0 .. i0 + 7 and half + i0 .. + 7: two 8-wide runs of the row,
+      // stored with 16-byte vectors (i0 is a multiple of 8)
+      const int i0 = within >> 1;
+      const float4* cs = reinterpret_cast<const float4*>(g.rope + (int64_t)pos * half + i0);
+      float a[8], b[8];
 #pragma unroll
-      for (int pr = 0; pr < 8; ++pr) {
-        const int i = (within >> 1) + pr;
-        const float y0 = __uint_as_float(v[2 * pr]), y1 = __uint_as_float(v[2 * pr + 1]);
-        const float2 c = cs[i];
-        const float a = y0 * c.x - y1 * c.y;
-        const float b = y1 * c.x + y0 * c.y;
-        if (slot < G) {
-          qrow[i] = a;
-          qrow[half + i] = b;
-        } else {
-          krow[i] = bf16_bits(a);
-          krow[half + i] = bf16_bits(b);
+      for (int pp = 0; pp < 4; ++pp) {
+        const float4 c = cs[pp];   // (cos, sin) of dims i0 + 2 pp and i0 + 2 pp + 1
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pr = 2 * pp + e;
+          const float y0 = __uint_as_float(v[2 * pr]), y1 = __uint_as_float(v[2 * pr + 1]);
+          const float cx = e ? c.z : c.x, sy = e ? c.w : c.y;
+          a[pr] = y0 * cx - y1 * sy;
+          b[pr] = y1 * cx + y0 * sy;
         }
+      }
+      if (slot < G) {
+        float* qrow = g.q + (int64_t)t * g.ldq + (int64_t)(grp * G + slot) * hd;
+        float4* qa = reinterpret_cast<float4*>(qrow + i0);
+        float4* qb = reinterpret_cast<float4*>(qrow + half + i0);
+        qa[0] = make_float4(a[0], a[1], a[2], a[3]);
+        qa[1] = make_float4(a[4], a[5], a[6], a[7]);
+        qb[0] = make_float4(b[0], b[1], b[2], b[3]);
+        qb[1] = make_float4(b[4], b[5], b[6], b[7]);
+      } else {
+        uint16_t* krow = g.kv + ((((int64_t)g.layer * 2 + 0) * g.n_kv + grp) * g.max_seq + pos) * hd;
+        uint16_t ka[8], kb[8];
+#pragma unroll
+        for (int pr = 0; pr < 8; ++pr) {
+          ka[pr] = bf16_bits(a[pr]);
+          kb[pr] = bf16_bits(b[pr]);
+        }
+        *reinterpret_cast<uint4*>(krow + i0) = *reinterpret_cast<const uint4*>(ka);
+        *reinterpret_cast<uint4*>(krow + half + i0) = *reinterpret_cast<const uint4*>(kb);
       }
     } else {
       uint16_t* vrow = g.kv + ((((int64_t)g.layer * 2 + 1) * g.n_kv + grp) * g.max_seq + pos) * hd + within;
@@ -222,15 +246,16 @@ struct GemmMaps {
   CUtensorMap w;
 };
 
-template <int EPI, int PARTS>
+template <int EPI, int PARTS, int BN>
 __global__ void __launch_bounds__(kPfGemmThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ PrefillGemm g) {
-  constexpr int kPfStages = GemmShape<PARTS>::kStages;
+  using Shape = GemmShape<PARTS, BN>;
+  constexpr int kPfStages = Shape::kStages, kPfEpiCols = Shape::kEpiCols;
   extern __shared__ uint8_t pf_smem_raw[];
-  GemmSmem<PARTS>& sm =
-      *reinterpret_cast<GemmSmem<PARTS>*>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
+  GemmSmem<PARTS, BN>& sm = *reinterpret_cast<GemmSmem<PARTS, BN>*>(
+      (reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.x * kPfBM, n0 = blockIdx.y * kPfBN;
+  const int m0 = blockIdx.x * kPfBM, n0 = blockIdx.y * BN;
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[s])));
@@ -246,7 +271,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
   if (warp == 1) {   // the MMA warp owns the accumulators' TMEM columns
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem)),
-                 "r"(2 * kPfBN));
+                 "r"(kPfTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
@@ -266,7 +291,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
         }
         const uint32_t fb = smem_addr(&sm.full[s]);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                     "r"(PARTS * kPfATile + kPfBTile)
+                     "r"(PARTS * kPfATile + Shape::kBTile)
                      : "memory");
         const int k = kb * kPfBK;
 #pragma unroll
@@ -302,7 +327,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
           const uint64_t bd = kmajor_sw128_desc(bw + k * 32);
 #pragma unroll
           for (int part = 0; part < PARTS; ++part)
-            umma_bf16(dt, kmajor_sw128_desc(smem_addr(sm.a[s][part]) + k * 32), bd,
+            umma_bf16<BN>(dt, kmajor_sw128_desc(smem_addr(sm.a[s][part]) + k * 32), bd,
                       (!first || k != 0 || part != 0) ? 1u : 0u);
         }
         umma_commit(smem_addr(&sm.empty[s]));
@@ -353,7 +378,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
   if (warp == 1) {
     __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kPfBN));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kPfTmemCols));
   }
 }
 
@@ -418,17 +443,21 @@ struct AttnShape {
 // Shared memory (bf16 elements): K [2][64][RP], V [2][64][RP], then per
 // warp (query head x token group) q hi [16][RP] and q lo [16][RP].
 template <int HD>
-__global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) {
+__global__ void __launch_bounds__(256, 2) prefill_attn_kernel(const PrefillAttn a) {
   using S = AttnShape<HD>;
-  constexpr int RP = S::RP, KS = HD / 16, DN = HD / 8;
+  constexpr int RP = S::RP, KS = HD / 16, DN = HD / 8, NT = kPfKB / 8;
   extern __shared__ __align__(16) uint16_t at_smem[];
   uint16_t* ks = at_smem;
   uint16_t* vs = at_smem + S::KV_ELEMS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
   const int gq = lane >> 2, tq = lane & 3;
-  const int g = blockIdx.y, G = a.group;
+  // CTA i: KV head i mod n_kv, token block nb - 1 - i / n_kv.  The causal
+  // work of a token block grows with its position, so the CTAs launch
+  // longest first and the short ones fill the SMs at the end.
+  const int nb = (int)gridDim.x / a.n_kv;
+  const int g = (int)blockIdx.x % a.n_kv, G = a.group;
   const int cta_tokens = kPfQT * attn_groups(G);
-  const int tb0 = blockIdx.x * cta_tokens;          // the CTA's first token
+  const int tb0 = (nb - 1 - (int)blockIdx.x / a.n_kv) * cta_tokens;   // the CTA's first token
   const int tb = tb0 + (warp / G) * kPfQT;           // this warp's first token
   const int head = g * G + warp % G;
   uint16_t* qh = at_smem + 2 * S::KV_ELEMS + warp * 2 * kPfQT * RP;
@@ -485,32 +514,40 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
     __syncthreads();
     const uint32_t kb_s = smem_addr(ks + buf * kPfKB * RP), vb_s = smem_addr(vs + buf * kPfKB * RP);
 
-    // S = Q K^T: 16 tokens x 64 positions, 8 tiles of 8 positions
-    float s[8][4];
+    // S = Q K^T: 16 tokens x kPfKB positions, NT tiles of 8 positions; per
+    // k step the hi parts of q go into every tile before the lo parts, so
+    // that no mma waits on the one just issued
+    float s[NT][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+    for (int i = 0; i < NT; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
       uint32_t qa_h[4], qa_l[4];
       const uint32_t qoff = (uint32_t)(((lane & 15) * RP + k * 16 + (lane >> 4) * 8) * 2);
       ldsm_x4(smem_addr(qh) + qoff, qa_h);
       ldsm_x4(smem_addr(ql) + qoff, qa_l);
+      uint32_t kf[NT / 2][4];
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
+      for (int np = 0; np < NT / 2; ++np) {
         const int mi = lane >> 3;
         const int key = (2 * np + (mi >> 1)) * 8 + (lane & 7);
-        uint32_t kf[4];
-        ldsm_x4(kb_s + (uint32_t)((key * RP + k * 16 + (mi & 1) * 8) * 2), kf);
-        mma_bf16_16816(s[2 * np], qa_h, kf[0], kf[1]);
-        mma_bf16_16816(s[2 * np], qa_l, kf[0], kf[1]);
-        mma_bf16_16816(s[2 * np + 1], qa_h, kf[2], kf[3]);
-        mma_bf16_16816(s[2 * np + 1], qa_l, kf[2], kf[3]);
+        ldsm_x4(kb_s + (uint32_t)((key * RP + k * 16 + (mi & 1) * 8) * 2), kf[np]);
+      }
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {
+        mma_bf16_16816(s[2 * np], qa_h, kf[np][0], kf[np][1]);
+        mma_bf16_16816(s[2 * np + 1], qa_h, kf[np][2], kf[np][3]);
+      }
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {
+        mma_bf16_16816(s[2 * np], qa_l, kf[np][0], kf[np][1]);
+        mma_bf16_16816(s[2 * np + 1], qa_l, kf[np][2], kf[np][3]);
       }
     }
     // causal mask, online softmax (rows gq and gq + 8 of the warp's tile)
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int p = blk * kPfKB + nt * 8 + 2 * tq + e;
@@ -531,7 +568,7 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
       lrow[r] *= alpha[r];
     }
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         s[nt][e] = exp2f(s[nt][e] - mu[e >> 1]);
@@ -544,9 +581,10 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
       o[dn][2] *= alpha[1];
       o[dn][3] *= alpha[1];
     }
-    // O += P V: 4 k-steps of 16 positions, P as bf16 hi + lo A fragments
+    // O += P V: kPfKB / 16 k-steps of 16 positions, P as bf16 hi + lo A
+    // fragments
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
+    for (int kk = 0; kk < NT / 2; ++kk) {
       uint32_t pa_h[4], pa_l[4];
       split_bf16x2(s[2 * kk][0], s[2 * kk][1], pa_h[0], pa_l[0]);
       split_bf16x2(s[2 * kk][2], s[2 * kk][3], pa_h[1], pa_l[1]);
@@ -559,8 +597,8 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
         uint32_t vf[4];
         ldsm_x4_trans(vb_s + (uint32_t)((key * RP + (2 * dp + (mi >> 1)) * 8) * 2), vf);
         mma_bf16_16816(o[2 * dp], pa_h, vf[0], vf[1]);
-        mma_bf16_16816(o[2 * dp], pa_l, vf[0], vf[1]);
         mma_bf16_16816(o[2 * dp + 1], pa_h, vf[2], vf[3]);
+        mma_bf16_16816(o[2 * dp], pa_l, vf[0], vf[1]);
         mma_bf16_16816(o[2 * dp + 1], pa_l, vf[2], vf[3]);
       }
     }
@@ -593,8 +631,21 @@ __global__ void __launch_bounds__(256) prefill_attn_kernel(const PrefillAttn a) 
 
 }  // namespace
 
-int prefill_gemm_smem_bytes(int parts) {
-  return (parts == 2 ? (int)sizeof(GemmSmem<2>) : (int)sizeof(GemmSmem<3>)) + 1024;
+int prefill_gemm_smem_bytes(int parts, int bn) {
+  const int b = bn == kPfBNNarrow ? (parts == 2 ? (int)sizeof(GemmSmem<2, kPfBNNarrow>)
+                                                : (int)sizeof(GemmSmem<3, kPfBNNarrow>))
+                                  : (parts == 2 ? (int)sizeof(GemmSmem<2, kPfBN>) : (int)sizeof(GemmSmem<3, kPfBN>));
+  return b + 1024;
+}
+
+int prefill_gemm_bn(int n_rows, int T, int sms) {
+  if (sms <= 0 || T <= 0 || n_rows <= 0) return kPfBN;
+  const int64_t mt = (T + kPfBM - 1) / kPfBM;
+  auto cost = [&](int bn) {
+    const int64_t tiles = mt * ((n_rows + bn - 1) / bn);
+    return (tiles + sms - 1) / sms * bn;
+  };
+  return cost(kPfBNNarrow) < cost(kPfBN) ? kPfBNNarrow : kPfBN;
 }
 
 int prefill_attn_smem_bytes(int head_dim, int group) {
@@ -617,39 +668,42 @@ cudaError_t launch_prefill_norm(const float* x, int T, int hidden, const uint16_
   return cudaGetLastError();
 }
 
-template <int EPI, int PARTS>
+template <int EPI, int PARTS, int BN>
 cudaError_t launch_gemm_instance(const GemmMaps& maps, const PrefillGemm& g, cudaStream_t s) {
-  const int smem = prefill_gemm_smem_bytes(PARTS);
-  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<EPI, PARTS>,
+  const int smem = prefill_gemm_smem_bytes(PARTS, BN);
+  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<EPI, PARTS, BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((g.T + kPfBM - 1) / kPfBM, (g.N + kPfBN - 1) / kPfBN);
-  prefill_gemm_kernel<EPI, PARTS><<<grid, kPfGemmThreads, smem, s>>>(maps, g);
+  const dim3 grid((g.T + kPfBM - 1) / kPfBM, (g.N + BN - 1) / BN);
+  prefill_gemm_kernel<EPI, PARTS, BN><<<grid, kPfGemmThreads, smem, s>>>(maps, g);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap* w, const PrefillGemm& g,
+template <int PARTS, int BN>
+cudaError_t launch_gemm_epi(int epi, const GemmMaps& maps, const PrefillGemm& g, cudaStream_t s) {
+  if (epi == PE_QKV) return launch_gemm_instance<PE_QKV, PARTS, BN>(maps, g, s);
+  if (epi == PE_RESID) return launch_gemm_instance<PE_RESID, PARTS, BN>(maps, g, s);
+  return launch_gemm_instance<PE_SWIGLU, PARTS, BN>(maps, g, s);
+}
+
+cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap* w, int bn, const PrefillGemm& g,
                                 cudaStream_t s) {
   if (g.T <= 0) return cudaSuccess;
   if (g.parts != 2 && g.parts != 3) return cudaErrorInvalidValue;
+  if (bn != kPfBN && bn != kPfBNNarrow) return cudaErrorInvalidValue;
   GemmMaps maps;
   for (int i = 0; i < kPfParts; ++i) maps.a[i] = a[i];
   maps.w = *w;
-  if (g.parts == 2) {
-    if (epi == PE_QKV) return launch_gemm_instance<PE_QKV, 2>(maps, g, s);
-    if (epi == PE_RESID) return launch_gemm_instance<PE_RESID, 2>(maps, g, s);
-    return launch_gemm_instance<PE_SWIGLU, 2>(maps, g, s);
-  }
-  if (epi == PE_QKV) return launch_gemm_instance<PE_QKV, 3>(maps, g, s);
-  if (epi == PE_RESID) return launch_gemm_instance<PE_RESID, 3>(maps, g, s);
-  return launch_gemm_instance<PE_SWIGLU, 3>(maps, g, s);
+  if (g.parts == 2)
+    return bn == kPfBN ? launch_gemm_epi<2, kPfBN>(epi, maps, g, s) : launch_gemm_epi<2, kPfBNNarrow>(epi, maps, g, s);
+  return bn == kPfBN ? launch_gemm_epi<3, kPfBN>(epi, maps, g, s) : launch_gemm_epi<3, kPfBNNarrow>(epi, maps, g, s);
 }
 
 cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
   const int smem = prefill_attn_smem_bytes(a.hd, a.group);
   const int groups = attn_groups(a.group), cta_tokens = kPfQT * groups;
-  const dim3 grid((a.T + cta_tokens - 1) / cta_tokens, a.n_kv);
+  const dim3 grid((unsigned)(((a.T + cta_tokens - 1) / cta_tokens) * a.n_kv));
   const int threads = 32 * a.group * groups;
   const void* fn = a.hd == 64 ? (const void*)prefill_attn_kernel<64> : (const void*)prefill_attn_kernel<128>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

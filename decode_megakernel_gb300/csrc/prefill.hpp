@@ -11,8 +11,8 @@
 //     H1 = rmsnorm(X) * w_attn[l]            as bf16 parts [T][H]
 //     QKV GEMM, epilogue: RoPE; q -> Q (fp32 [T][n_heads * hd]); k, v ->
 //       the KV cache (bf16) at positions s0 + t
-//     attention (causal over positions 0 .. s0 + t, GQA) -> O, bf16 parts
 //     (last layer: stop, the rest of it feeds no K,V)
+//     attention (causal over positions 0 .. s0 + t, GQA) -> O, bf16 parts
 //     X += O Wo^T;  H1 = rmsnorm(X) * w_ffn[l]
 //     gate/up GEMM, epilogue silu(g) * u -> A, bf16 parts [T][F]
 //     X += A Wd^T
@@ -20,11 +20,11 @@
 // p2) to 2^-18 (2^-27) relative (p0 = bf16(x), p1 = bf16(x - p0), p2 =
 // bf16(x - p0 - p1); each subtraction is exact in fp32), and the parts are
 // multiplied against the bf16 weights into one fp32 accumulator.  Three
-// parts (the default) carry the activation's full fp32 precision, as the
-// decode kernel's fp32 GEMVs do; two parts take two thirds of the tensor
-// work (measured on the 8B shape: 53 instead of 75 ms for 2048 tokens) and
-// leave ~0.3% of the first layer's bf16 K,V one step off the fp32 path
-// (three parts: ~0.04%).
+// parts carry the activation's full fp32 precision, as the decode kernel's
+// fp32 GEMVs do; two parts (the default) take two thirds of the tensor work
+// (measured on the 8B shape: 50 instead of 71 ms for 2048 tokens) and leave
+// ~0.3% of the first layer's bf16 K,V one step off the fp32 path (three
+// parts: ~0.04%).
 #pragma once
 
 #include <cuda.h>
@@ -35,7 +35,8 @@
 namespace amk {
 
 constexpr int kPfBM = 128;      // tokens per GEMM tile (MMA M, TMEM lanes)
-constexpr int kPfBN = 256;      // packed weight rows per GEMM tile (MMA N, TMEM columns)
+constexpr int kPfBN = 256;      // packed weight rows per GEMM tile at most (MMA N, TMEM columns)
+constexpr int kPfBNNarrow = 224;   // the narrower tile width (a multiple of every Rt)
 constexpr int kPfBK = 64;       // k per pipeline stage: one 128-byte swizzled row
 constexpr int kPfParts = 3;     // bf16 parts of a GEMM activation operand at most (buffers, maps)
 constexpr int kPfDefaultParts = 2;
@@ -50,7 +51,7 @@ constexpr int kPfSegKB = 2;
 constexpr int kPfEpiWarps = 8;
 constexpr int kPfGemmThreads = 64 + 32 * kPfEpiWarps;   // TMA warp, MMA warp, epilogue warps
 constexpr int kPfQT = 16;       // query tokens of one attention warp (one m16 tile of one head)
-constexpr int kPfKB = 64;       // cached positions per attention key block
+constexpr int kPfKB = 32;       // cached positions per attention key block (two CTAs of 8 warps per SM)
 constexpr int kPfDefaultChunk = 2048;
 
 enum PrefillEpi : int32_t { PE_QKV = 0, PE_RESID = 1, PE_SWIGLU = 2 };
@@ -59,7 +60,7 @@ enum PrefillEpi : int32_t { PE_QKV = 0, PE_RESID = 1, PE_SWIGLU = 2 };
 // epilogue.  A arrives through kPfParts 2-D tensor maps (its bf16 parts,
 // each [rows][K], boxes of 64 x 128, 128-byte swizzle); W through a 4-D map
 // over the decode kernel's tile layout ({Kt, Rt, nkt, n_rb}, boxes
-// {64, Rt, 1, 256 / Rt}).
+// {64, Rt, 1, bn / Rt}, bn = kPfBN or kPfBNNarrow rows).
 struct PrefillGemm {
   int32_t T;              // tokens (rows of D that are stored)
   int32_t N;              // packed weight rows (columns of D that are used)
@@ -94,7 +95,13 @@ struct PrefillAttn {
   int32_t parts;          // bf16 parts written (2 or 3)
 };
 
-int prefill_gemm_smem_bytes(int parts);
+int prefill_gemm_smem_bytes(int parts, int bn);
+
+// Tile width of a GEMM with n_rows packed weight rows over T tokens on
+// `sms` SMs: kPfBN or kPfBNNarrow, whichever finishes first when every SM
+// runs one tile at a time and a tile takes time in proportion to its
+// width (ceil(tiles / sms) rounds of width bn); ties go to kPfBN.
+int prefill_gemm_bn(int n_rows, int T, int sms);
 int prefill_attn_smem_bytes(int head_dim, int group);
 
 // X[t][:] = float(embed[tokens[t]][:]) for t < T
@@ -103,8 +110,9 @@ cudaError_t launch_prefill_embed(const int32_t* tokens, int T, const uint16_t* e
 // out[i][t][:] = the bf16 parts of rmsnorm(X[t]) * w for t < T (row stride hidden)
 cudaError_t launch_prefill_norm(const float* x, int T, int hidden, const uint16_t* w, float eps,
                                 uint16_t* const* out, int parts, cudaStream_t s);
-// a: the g.parts tensor maps of the activation parts
-cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap* w, const PrefillGemm& g,
+// a: the g.parts tensor maps of the activation parts; w: the weight map,
+// encoded with boxes of bn rows (kPfBN or kPfBNNarrow)
+cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap* w, int bn, const PrefillGemm& g,
                                 cudaStream_t s);
 cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s);
 

@@ -120,6 +120,10 @@ typedef struct {
     int32_t prefill_parts;      /* bf16 parts per activation operand of the prefill GEMMs:
                                    0 or 2: two (activations to 2^-18 relative, the default);
                                    3: three (fp32-level products, 1.5x the tensor work) */
+    int32_t prefill_tile_rows;  /* weight rows per prefill GEMM tile (the MMA's N): 0 (default):
+                                   per matrix 256 or 224, whichever covers a full chunk in
+                                   fewer tile-rows when every SM runs one tile at a time;
+                                   256 or 224: that width for every matrix */
 } amk_schedule_config;
 
 typedef struct amk_ctx amk_ctx;

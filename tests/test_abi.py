@@ -106,6 +106,10 @@ def test_prefill_chunk_sizes_the_workspace(amk):
     for parts, ok in [(0, True), (2, True), (3, True), (1, False), (4, False), (-1, False)]:
         ws = amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152, prefill_parts=parts))
         assert (ws == dflt) if ok else (ws == 0)
+    # prefill GEMM tiles of 256 or 224 weight rows (0: chosen per matrix); nothing else
+    for rows, ok in [(0, True), (256, True), (224, True), (128, False), (192, False), (-1, False)]:
+        ws = amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152, prefill_tile_rows=rows))
+        assert (ws == dflt) if ok else (ws == 0)
 
 
 def test_host_argument_checks_need_no_gpu(amk):

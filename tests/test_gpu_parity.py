@@ -260,16 +260,19 @@ def kv_layers(a, b):
     return first, same, rel_mean
 
 
-@pytest.mark.parametrize("variant,chunk,prompt,split,parts", [
-    ("tiny", 0, 12, None, 0),       # one chunk, one partial 128-token tile (default: two parts)
-    ("tiny", 128, 300, 100, 0),     # two calls (history from the first), three chunks, ragged tail
-    ("hd128", 128, 200, None, 0),   # head_dim 128, group 4
-    ("mha", 0, 40, 17, 0),          # group 1
-    ("tied", 256, 260, None, 0),
-    ("tiny", 128, 300, 100, 3),     # three activation parts
-    ("hd128", 0, 200, None, 3),
+@pytest.mark.parametrize("variant,chunk,prompt,split,parts,rows", [
+    ("tiny", 0, 12, None, 0, 0),       # one chunk, one partial 128-token tile (default: two parts)
+    ("tiny", 128, 300, 100, 0, 0),     # two calls (history from the first), three chunks, ragged tail
+    ("hd128", 128, 200, None, 0, 0),   # head_dim 128, group 4
+    ("mha", 0, 40, 17, 0, 0),          # group 1
+    ("tied", 256, 260, None, 0, 0),
+    ("tiny", 128, 300, 100, 3, 0),     # three activation parts
+    ("hd128", 0, 200, None, 3, 0),
+    ("tiny", 128, 300, 100, 0, 256),   # 256-row GEMM tiles for every matrix
+    ("hd128", 0, 200, None, 3, 256),
+    ("tiny", 0, 140, None, 0, 224),    # 224-row tiles: partial last tile of 256-row matrices
 ])
-def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, prompt, split, parts):
+def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, prompt, split, parts, rows):
     """The tensor-core prefill (tcgen05 GEMMs, mma.sync attention) against
     the oracle's batched causal prefill (orc_prefill_batched, itself pinned
     equal to sequential decode steps), then decode steps on top of it.
@@ -297,7 +300,8 @@ def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, promp
     steps = 4
     max_seq = prompt + steps
     w = synth.model_weights(cfg, seed=6, device=dev)
-    dec = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=chunk, prefill_parts=parts))
+    dec = amk.Decoder(w, max_seq, sched=amk.make_schedule_config(prefill_chunk=chunk, prefill_parts=parts,
+                                                                  prefill_tile_rows=rows))
     om = orc.OracleModel(w.to("cpu"), max_seq)
     kv_o = synth.empty_kv_cache(cfg, max_seq)
     toks = synth.prompt_tokens(cfg, prompt).tolist()
@@ -312,7 +316,8 @@ def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, promp
     om.prefill_batched(kv_o, toks, 0)
     dec.sync()
     (ok0, same0, worst0), same, rel_mean = kv_layers(dec.kv[:, :, :, :prompt], kv_o[:, :, :, :prompt])
-    print(f"{variant} chunk {chunk} P {prompt} parts {parts or 2}: layer 0 identical {same0:.4f} "
+    print(f"{variant} chunk {chunk} P {prompt} parts {parts or 2} tile rows {rows or 'auto'}: "
+          f"layer 0 identical {same0:.4f} "
           f"worst/allow {worst0:.3f}; per layer {' '.join(f'{x:.4f}' for x in same)}; "
           f"mean |diff| / mean |kv| {rel_mean:.2e}")
     assert ok0 and same0 >= (0.999 if parts == 3 else 0.995)

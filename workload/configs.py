@@ -143,15 +143,15 @@ def step_flops(m: ModelConfig, pos: int) -> int:
 
 def prefill_flops(m: ModelConfig, n: int, start: int = 0) -> int:
     """Algorithmic flops of a prefill of n tokens at positions start..: the
-    QKV products of every layer, the O / gate-up / down products of every
-    layer but the last (its output feeds no K,V), and causal attention
-    (scores and values, 2 flops per multiply-add) of every layer."""
+    QKV products of every layer; causal attention (scores and values, 2
+    flops per multiply-add) and the O / gate-up / down products of every
+    layer but the last (their output feeds no K,V)."""
     shapes = {name: o * i for name, o, i in m.linear_shapes()}
     qkv = shapes["wq"] + shapes["wk"] + shapes["wv"]
     rest = shapes["wo"] + shapes["wg"] + shapes["wu"] + shapes["wd"]
     lin = qkv * m.n_layers + rest * (m.n_layers - 1)
     ctx = sum(start + t + 1 for t in range(n))   # positions each token attends to
-    attn = 4 * ctx * m.n_heads * m.head_dim * m.n_layers
+    attn = 4 * ctx * m.n_heads * m.head_dim * (m.n_layers - 1)
     return 2 * lin * n + attn
 
 
