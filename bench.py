@@ -94,9 +94,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, alg_bytes: float):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current kernel sources, else None: the summary's traffic_ratio
+    (DRAM bytes / algorithmic bytes, measured on a case of the same layer
+    shapes) times this launch's algorithmic bytes, or its
+    traffic_bytes_per_launch where it gives no ratio."""
     path = os.path.join(PROFILE_DIR, f"decode_kernel_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -110,6 +113,8 @@ def profiled_traffic(workload: str):
     if fields.get("kernel_sources_sha256") != kernel_source_hash():
         return None
     try:
+        if "traffic_ratio" in fields:
+            return int(float(fields["traffic_ratio"]) * alg_bytes)
         return int(float(fields["traffic_bytes_per_launch"]))
     except (KeyError, ValueError):
         return None
@@ -409,7 +414,7 @@ def roofline_block(wl, per, positions):
     achieved = mean_bytes / mean_launch_s / 1e9
     peak, peak_src = measured_peak_gbs()
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
+            "frac": achieved / peak, "traffic": profiled_traffic(wl.name, mean_bytes),
             "peak_source": f"{peak_src} hbm_gbs (copy)",
             "algorithmic_bytes_per_launch": mean_bytes,
             "mean_launch_ms": mean_launch_s * 1e3,
