@@ -24,6 +24,8 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 namespace amk {
 
 namespace {
@@ -62,6 +64,17 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, uint64_t
     if (global_timer() - t0 > limit_ns) return false;
   return true;
 }
+
+// Programmatic dependent launch: every prefill kernel is launched with
+// programmatic stream serialisation, so it may start (and run its prologue:
+// barrier setup, tensor-memory allocation) while the kernel before it on the
+// stream drains.  pdl_wait blocks until that kernel has completed and its
+// writes are visible; each kernel calls it before its first access to
+// global memory that another kernel writes or reads.  pdl_launch_dependents
+// lets the next kernel start launching once every CTA of this one has
+// called it (or exited).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ void pf_timeout(uint32_t* status, uint32_t site) {
   if (atomicCAS(&status[0], 0u, (uint32_t)ST_TIMEOUT) == 0u) {
@@ -256,6 +269,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
       (reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.x * kPfBM, n0 = blockIdx.y * BN;
+  pdl_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[s])));
@@ -278,6 +292,7 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t tmem = sm.tmem;
+  pdl_wait();   // the activation parts, the residual rows and the KV cache are the previous kernels'
 
   if (warp == 0) {
     if (lane == 0) {   // TMA producer
@@ -385,8 +400,10 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
 // ------------------------------------------------------------ elementwise
 
 __global__ void prefill_embed_kernel(const int32_t* tokens, int T, const uint16_t* embed, int hidden, float* x) {
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   if (t >= T) return;
+  pdl_wait();
   const uint16_t* e = embed + (int64_t)tokens[t] * hidden;
   float* xr = x + (int64_t)t * hidden;
   for (int k = threadIdx.x; k < hidden; k += blockDim.x) xr[k] = __uint_as_float((uint32_t)e[k] << 16);
@@ -397,27 +414,55 @@ struct Parts {
   uint16_t* p[kPfParts];
 };
 
-__global__ void __launch_bounds__(256) prefill_norm_kernel(const float* x, int T, int hidden, const uint16_t* w,
-                                                           float eps, const Parts out, int parts) {
-  __shared__ float part[8];
+// float4 groups of a row each thread holds in registers (hidden <= 4 *
+// kNormVec * 1024)
+constexpr int kNormVec = 8;
+
+// One CTA per token row: the row is loaded once into registers (all loads
+// in flight together), reduced, scaled by the norm weight and stored as
+// bf16 parts, four elements (8 bytes per part) at a time.
+__global__ void __launch_bounds__(1024) prefill_norm_kernel(const float* x, int T, int hidden, const uint16_t* w,
+                                                            float eps, const Parts out, int parts) {
+  __shared__ float part[32];
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   if (t >= T) return;
-  const float* xr = x + (int64_t)t * hidden;
+  pdl_wait();
+  const int n4 = hidden >> 2, tid = threadIdx.x, nt = blockDim.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + (int64_t)t * hidden);
+  float4 v[kNormVec];
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int k4 = tid + i * nt;
+    v[i] = k4 < n4 ? xr[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float ss = 0.f;
-  for (int k = threadIdx.x; k < hidden; k += blockDim.x) ss = fmaf(xr[k], xr[k], ss);
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i)
+    ss += fmaf(v[i].x, v[i].x, v[i].y * v[i].y) + fmaf(v[i].z, v[i].z, v[i].w * v[i].w);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  if ((tid & 31) == 0) part[tid >> 5] = ss;
   __syncthreads();
   float tot = 0.f;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += part[i];
+  for (int i = 0; i < (nt >> 5); ++i) tot += part[i];
   const float r = rsqrtf(tot / (float)hidden + eps);
-  for (int k = threadIdx.x; k < hidden; k += blockDim.x) {
-    uint16_t p[kPfParts];
-    split_parts(xr[k] * r * __uint_as_float((uint32_t)w[k] << 16), p);
+  const uint2* w4 = reinterpret_cast<const uint2*>(w);
 #pragma unroll
-    for (int i = 0; i < kPfParts; ++i)
-      if (i < parts) out.p[i][(int64_t)t * hidden + k] = p[i];
+  for (int i = 0; i < kNormVec; ++i) {
+    const int k4 = tid + i * nt;
+    if (k4 >= n4) break;
+    const uint2 wb = w4[k4];
+    const float y[4] = {v[i].x * r * __uint_as_float(wb.x << 16), v[i].y * r * __uint_as_float(wb.x & 0xFFFF0000u),
+                        v[i].z * r * __uint_as_float(wb.y << 16), v[i].w * r * __uint_as_float(wb.y & 0xFFFF0000u)};
+    uint16_t pp[4][kPfParts];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) split_parts(y[e], pp[e]);
+#pragma unroll
+    for (int j = 0; j < kPfParts; ++j)
+      if (j < parts)
+        *reinterpret_cast<uint2*>(out.p[j] + (int64_t)t * hidden + 4 * k4) =
+            make_uint2((uint32_t)pp[0][j] | ((uint32_t)pp[1][j] << 16), (uint32_t)pp[2][j] | ((uint32_t)pp[3][j] << 16));
   }
 }
 
@@ -450,6 +495,8 @@ __global__ void __launch_bounds__(256, 2) prefill_attn_kernel(const PrefillAttn 
   uint16_t* ks = at_smem;
   uint16_t* vs = at_smem + S::KV_ELEMS;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  pdl_launch_dependents();
+  pdl_wait();   // q and the K,V rows of this chunk come from the QKV GEMM
   const int gq = lane >> 2, tq = lane & 3;
   // CTA i: KV head i mod n_kv, token block nb - 1 - i / n_kv.  The causal
   // work of a token block grows with its position, so the CTAs launch
@@ -631,6 +678,23 @@ __global__ void __launch_bounds__(256, 2) prefill_attn_kernel(const PrefillAttn 
 
 }  // namespace
 
+// Launch with programmatic stream serialisation (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 int prefill_gemm_smem_bytes(int parts, int bn) {
   const int b = bn == kPfBNNarrow ? (parts == 2 ? (int)sizeof(GemmSmem<2, kPfBNNarrow>)
                                                 : (int)sizeof(GemmSmem<3, kPfBNNarrow>))
@@ -655,8 +719,7 @@ int prefill_attn_smem_bytes(int head_dim, int group) {
 cudaError_t launch_prefill_embed(const int32_t* tokens, int T, const uint16_t* embed, int hidden, float* x,
                                  cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  prefill_embed_kernel<<<T, 256, 0, s>>>(tokens, T, embed, hidden, x);
-  return cudaGetLastError();
+  return launch_pdl(prefill_embed_kernel, dim3(T), dim3(256), 0, s, tokens, T, embed, hidden, x);
 }
 
 cudaError_t launch_prefill_norm(const float* x, int T, int hidden, const uint16_t* w, float eps,
@@ -664,8 +727,12 @@ cudaError_t launch_prefill_norm(const float* x, int T, int hidden, const uint16_
   if (T <= 0) return cudaSuccess;
   Parts p;
   for (int i = 0; i < kPfParts; ++i) p.p[i] = out[i];
-  prefill_norm_kernel<<<T, 256, 0, s>>>(x, T, hidden, w, eps, p, parts);
-  return cudaGetLastError();
+  // threads: enough for kNormVec float4 each, whole warps, at least 128
+  const int n4 = hidden / 4;
+  int threads = ((n4 + kNormVec - 1) / kNormVec + 31) / 32 * 32;
+  threads = std::max(threads, 128);
+  if (hidden % 4 || threads > 1024) return cudaErrorInvalidValue;
+  return launch_pdl(prefill_norm_kernel, dim3(T), dim3(threads), 0, s, x, T, hidden, w, eps, p, parts);
 }
 
 template <int EPI, int PARTS, int BN>
@@ -675,8 +742,7 @@ cudaError_t launch_gemm_instance(const GemmMaps& maps, const PrefillGemm& g, cud
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((g.T + kPfBM - 1) / kPfBM, (g.N + BN - 1) / BN);
-  prefill_gemm_kernel<EPI, PARTS, BN><<<grid, kPfGemmThreads, smem, s>>>(maps, g);
-  return cudaGetLastError();
+  return launch_pdl(prefill_gemm_kernel<EPI, PARTS, BN>, grid, dim3(kPfGemmThreads), smem, s, maps, g);
 }
 
 template <int PARTS, int BN>
@@ -708,11 +774,8 @@ cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s) {
   const void* fn = a.hd == 64 ? (const void*)prefill_attn_kernel<64> : (const void*)prefill_attn_kernel<128>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (a.hd == 64)
-    prefill_attn_kernel<64><<<grid, threads, smem, s>>>(a);
-  else
-    prefill_attn_kernel<128><<<grid, threads, smem, s>>>(a);
-  return cudaGetLastError();
+  if (a.hd == 64) return launch_pdl(prefill_attn_kernel<64>, grid, dim3(threads), smem, s, a);
+  return launch_pdl(prefill_attn_kernel<128>, grid, dim3(threads), smem, s, a);
 }
 
 }  // namespace amk
