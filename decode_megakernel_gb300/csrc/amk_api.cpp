@@ -58,6 +58,7 @@ struct amk_ctx {
     std::vector<CUtensorMap> w[M_NUM];     // weight operands per layer (QKV, O, gate/up, down)
     int32_t tile_rows = 0;                 // schedule knob: 0 = chosen per matrix
     int32_t bn[M_NUM] = {};                // GEMM tile width per matrix (the weight maps' box rows)
+    CUtensorMap kv_attn;                   // the KV cache in boxes of 64 dims x kTcKeys positions
   } pf;
   std::string err;
 };
@@ -292,8 +293,8 @@ amk_status encode_bf16_map(amk_ctx* ctx, const char* what, CUtensorMap* out, voi
 // The KV cache as a 2-D tensor for TMA: rows of head_dim bf16 (one row per
 // layer, K/V, KV head and position), boxes of 64 dims x the positions of
 // one KV stage, 128-byte swizzle (conflict-free ldmatrix reads).
-amk_status encode_kv_map(amk_ctx* ctx, const amk_config& c, void* kv, CUtensorMap* out) {
-  const int pps = (kStageBytes / 2) / (c.head_dim * 2);
+amk_status encode_kv_map(amk_ctx* ctx, const amk_config& c, void* kv, CUtensorMap* out, int box_rows = 0) {
+  const int pps = box_rows > 0 ? box_rows : (kStageBytes / 2) / (c.head_dim * 2);
   const cuuint64_t dims[2] = {(cuuint64_t)c.head_dim,
                               (cuuint64_t)c.n_layers * 2 * c.n_kv_heads * c.max_seq};
   const cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
@@ -322,6 +323,10 @@ amk_status encode_prefill_maps(amk_ctx* ctx, const DevMat* mats) {
     amk_status st = act(&pf.a_h1[i], pf.h1[i], (cuuint64_t)c.hidden);
     if (st == AMK_OK) st = act(&pf.a_o[i], pf.h2[i], qd);
     if (st == AMK_OK) st = act(&pf.a_a[i], pf.h2[i], (cuuint64_t)c.ffn);
+    if (st != AMK_OK) return st;
+  }
+  if (c.head_dim % 64 == 0) {   // the tensor-core attention's K,V blocks
+    amk_status st = encode_kv_map(ctx, c, ctx->kv, &pf.kv_attn, kTcKeys);
     if (st != AMK_OK) return st;
   }
   int sms = 0;
@@ -919,6 +924,9 @@ amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
   for (int i = 0; i < kPfParts; ++i) at.o[i] = pf.h2[i];
   at.ldo = qd;
   at.parts = pf.parts;
+  at.status = dm.status;
+  at.timeout_ns = ctx->timeout_ns;
+  const CUtensorMap* kv_attn = c.head_dim % 64 == 0 ? &pf.kv_attn : nullptr;
   auto gemm = [&](int epi, int kind, int layer, const CUtensorMap* a) {
     const MatGeom& m = geo.mat[kind];
     g.N = m.rows;
@@ -938,7 +946,7 @@ amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
       AMK_CUDA(ctx, gemm(PE_QKV, M_QKV, l, pf.a_h1));
       if (l == c.n_layers - 1) break;   // the rest of the last layer feeds no K,V
       at.layer = l;
-      AMK_CUDA(ctx, launch_prefill_attn(at, s));
+      AMK_CUDA(ctx, launch_prefill_attn(at, kv_attn, s));
       AMK_CUDA(ctx, gemm(PE_RESID, M_O, l, pf.a_o));
       AMK_CUDA(ctx, launch_prefill_norm(pf.x, T, c.hidden, dm.ffn_norm + l * H, c.rms_eps, pf.h1, pf.parts, s));
       AMK_CUDA(ctx, gemm(PE_SWIGLU, M_GU, l, pf.a_h1));

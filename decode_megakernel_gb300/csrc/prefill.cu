@@ -676,6 +676,328 @@ __global__ void __launch_bounds__(256, 2) prefill_attn_kernel(const PrefillAttn 
   }
 }
 
+
+// ------------------------------------------------ attention on tcgen05
+//
+// One CTA: kTcRows query rows (TPC = 128 / G tokens x the G query heads
+// of KV head g, head-major: row = h * TPC + t) against the cache's keys
+// [0, kv_end) in blocks of kTcKeys.  Per block:
+//   S  = Q K^T           tcgen05.mma M 128, N 64: q as bf16 hi + lo (two
+//                        MMAs per 16-dim step) into one of two TMEM buffers
+//   softmax              eight math warps, a row's 64 scores split over two
+//                        warps (tcgen05.ld of 32 columns each); running max
+//                        and sum in registers, block maxima exchanged through
+//                        shared memory; P as bf16 hi + lo into shared memory
+//   O += P V             tcgen05.mma M 128, N head_dim, K 16 keys (P hi and
+//                        lo), V read in place from its TMA layout as an
+//                        MN-major operand; the block's product lands in TMEM
+//                        and is added into fp32 registers (O scaled by the
+//                        max correction), as the GEMM promotes its segments
+// Warp 0 streams K and V blocks with TMA (two stages), warp 1 issues the
+// MMAs, warps 2..9 compute.  S(i + 1) runs on the tensor cores while the
+// math warps work on block i.  Every wait is bounded.
+constexpr int kTcStages = 2;
+constexpr int kTcMathWarps = 8;
+constexpr int kTcThreads = 64 + 32 * kTcMathWarps;
+
+template <int HD>
+struct __align__(1024) TcAttnSmem {
+  static constexpr int A = HD / 64;                 // 128-byte atoms along the head dim
+  uint8_t q[2][A][kTcRows * 128];                   // q hi / lo: [part][atom][row][128 B], swizzled
+  uint8_t k[kTcStages][A][kTcKeys * 128];           // K block: [atom][key][128 B] (TMA, swizzled)
+  uint8_t v[kTcStages][A][kTcKeys * 128];           // V block, the same layout
+  uint8_t p[2][kTcRows * 128];                      // P hi / lo: [row][64 keys], swizzled
+  float mx[2][2][kTcRows];                          // block maxima [block parity][row half][row]
+  float ls[2][kTcRows];                             // row sums [row half][row]
+  uint64_t kv_full[kTcStages], kv_empty[kTcStages];
+  uint64_t q_full, s_full[2], p_full, pv_full, x_bar[2], l_bar;
+  uint32_t tmem;
+};
+
+struct TcAttnArgs {
+  CUtensorMap kv;   // KV cache rows, boxes of 64 dims x kTcKeys rows
+  PrefillAttn a;
+};
+
+// MN-major operand with 128-byte swizzle: rows of 128 bytes (64 elements
+// along M / N) for consecutive k, 8-row groups 1024 bytes apart, the next
+// 64 elements along M / N lbo bytes on.
+__device__ __forceinline__ uint64_t mnmajor_sw128_desc(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ TcAttnArgs args) {
+  using Sm = TcAttnSmem<HD>;
+  constexpr int A = Sm::A, DH = HD / 2;   // atoms; head dims per math warp (row half)
+  constexpr uint32_t kColPV = 128;        // TMEM columns: S buffers at 0 and 64, P.V at 128
+  constexpr uint32_t kIdS = idesc_bf16<kTcKeys>();
+  constexpr uint32_t kIdPV = idesc_bf16<HD>() | (1u << 16);   // B (V) MN-major
+  const PrefillAttn& a = args.a;
+  extern __shared__ uint8_t tc_smem_raw[];
+  Sm& sm = *reinterpret_cast<Sm*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.group, TPC = kTcRows / G;
+  const int nb = (a.T + TPC - 1) / TPC;
+  const int g = (int)blockIdx.x % a.n_kv;
+  const int tb0 = (nb - 1 - (int)blockIdx.x / a.n_kv) * TPC;   // longest first
+  const int kv_end = a.s0 + min(a.T, tb0 + TPC);               // keys [0, kv_end) are needed
+  const int nblk = (kv_end + kTcKeys - 1) / kTcKeys;
+  const int limit = a.s0 + a.T;                                 // keys [0, limit) are written
+  // first key of block i's window: the block itself, or for a block that
+  // would run past the written keys, the last kTcKeys written keys (the
+  // keys it repeats are masked)
+  auto win = [&](int i) { return min(i * kTcKeys, limit - kTcKeys); };
+  const int row_k = ((a.layer * 2 + 0) * a.n_kv + g) * a.max_seq;
+  const int row_v = ((a.layer * 2 + 1) * a.n_kv + g) * a.max_seq;
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int st = 0; st < kTcStages; ++st) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.kv_full[st])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.kv_empty[st])));
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.q_full)), "r"(kTcMathWarps));
+    for (int b = 0; b < 2; ++b) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.s_full[b])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.x_bar[b])), "r"(kTcMathWarps));
+    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.p_full)), "r"(kTcMathWarps));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pv_full)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.l_bar)), "r"(kTcMathWarps));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem)),
+                 "r"(256));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = sm.tmem;
+  pdl_wait();   // q and this chunk's K,V come from the QKV GEMM
+
+  if (warp == 0) {
+    if (lane == 0) {   // TMA producer: K and V of each block
+      int issued = 0;
+      for (int blk = 0; blk < nblk; ++blk) {
+        const int st = blk % kTcStages;
+        const uint32_t ph = (uint32_t)(blk / kTcStages) & 1u;
+        if (!bar_wait(smem_addr(&sm.kv_empty[st]), ph ^ 1u, a.timeout_ns)) {
+          pf_timeout(a.status, SITE_PF_TMA);
+          break;
+        }
+        const uint32_t fb = smem_addr(&sm.kv_full[st]);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                     "r"(2 * A * kTcKeys * 128)
+                     : "memory");
+        const int w0 = win(blk);
+#pragma unroll
+        for (int at = 0; at < A; ++at) {
+          tma_2d(smem_addr(sm.k[st][at]), &args.kv, 64 * at, row_k + w0, fb);
+          tma_2d(smem_addr(sm.v[st][at]), &args.kv, 64 * at, row_v + w0, fb);
+        }
+        ++issued;
+      }
+      // copies the consumers never waited for (they stopped early) land
+      // before the CTA's shared memory goes away
+      for (int blk = max(0, issued - kTcStages); blk < issued; ++blk)
+        bar_wait(smem_addr(&sm.kv_full[blk % kTcStages]), (uint32_t)(blk / kTcStages) & 1u, a.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {   // MMA issuer
+      bool ok = bar_wait(smem_addr(&sm.q_full), 0u, a.timeout_ns);
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      auto issue_s = [&](int blk) -> bool {
+        const int st = blk % kTcStages;
+        if (!bar_wait(smem_addr(&sm.kv_full[st]), (uint32_t)(blk / kTcStages) & 1u, a.timeout_ns)) return false;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint32_t d = tmem + (uint32_t)((blk & 1) * kTcKeys);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t off = (uint32_t)((ks & 3) * 32);
+          const uint64_t bd = kmajor_sw128_desc(smem_addr(sm.k[st][ks >> 2]) + off);
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+            umma_f16(d, kmajor_sw128_desc(smem_addr(sm.q[part][ks >> 2]) + off), bd, kIdS,
+                     (ks != 0 || part != 0) ? 1u : 0u);
+        }
+        umma_commit(smem_addr(&sm.s_full[blk & 1]));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int blk = 0; ok && blk < nblk; ++blk) {
+        if (blk + 1 < nblk && !(ok = issue_s(blk + 1))) break;
+        // P of this block written (and the previous block's P.V drained)
+        if (!(ok = bar_wait(smem_addr(&sm.p_full), (uint32_t)blk & 1u, a.timeout_ns))) break;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const int st = blk % kTcStages;
+#pragma unroll
+        for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+          const uint64_t bd = mnmajor_sw128_desc(smem_addr(sm.v[st][0]) + (uint32_t)(kk * 16 * 128),
+                                                 (uint32_t)(kTcKeys * 128));
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+            umma_f16(tmem + kColPV, kmajor_sw128_desc(smem_addr(sm.p[part]) + (uint32_t)(kk * 32)), bd, kIdPV,
+                     (kk != 0 || part != 0) ? 1u : 0u);
+        }
+        umma_commit(smem_addr(&sm.kv_empty[st]));
+        umma_commit(smem_addr(&sm.pv_full));
+      }
+      if (!ok) pf_timeout(a.status, SITE_PF_MMA);
+    }
+  } else {
+    // math warps: row r = TMEM lane, columns / dims of half hf
+    const int quarter = warp & 3, hf = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const int h_local = r / TPC, t = tb0 + r % TPC;
+    const bool row_ok = t < a.T;
+    const int pos = a.s0 + t;
+    const int head = g * G + h_local;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    // q row, this half's dims, pre-scaled into log2 units, as bf16 hi + lo
+    const float qscale = 1.4426950408889634f * rsqrtf((float)HD);
+#pragma unroll
+    for (int c = 0; c < DH / 8; ++c) {
+      const int d0 = hf * DH + c * 8;
+      float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+      if (row_ok) {
+        const float4* src = reinterpret_cast<const float4*>(a.q + (int64_t)t * a.ldq + (int64_t)head * HD + d0);
+        x0 = src[0];
+        x1 = src[1];
+      }
+      uint32_t hi[4], lo[4];
+      split_bf16x2(x0.x * qscale, x0.y * qscale, hi[0], lo[0]);
+      split_bf16x2(x0.z * qscale, x0.w * qscale, hi[1], lo[1]);
+      split_bf16x2(x1.x * qscale, x1.y * qscale, hi[2], lo[2]);
+      split_bf16x2(x1.z * qscale, x1.w * qscale, hi[3], lo[3]);
+      const int cc = (d0 & 63) >> 3;
+      const uint32_t off = (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
+      *reinterpret_cast<uint4*>(sm.q[0][d0 >> 6] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(sm.q[1][d0 >> 6] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cta(smem_addr(&sm.q_full));
+
+    float o[DH];
+#pragma unroll
+    for (int i = 0; i < DH; ++i) o[i] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int blk = 0; blk < nblk; ++blk) {
+      const int b = blk & 1;
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.s_full[b]), (uint32_t)(blk >> 1) & 1u, a.timeout_ns));
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      uint32_t sv[2][16];
+      tmem_ld16(lane_base + (uint32_t)(b * kTcKeys + hf * 32), sv[0]);
+      tmem_ld16(lane_base + (uint32_t)(b * kTcKeys + hf * 32 + 16), sv[1]);
+      // keys of the window; valid: not taken by an earlier block, causal
+      const int k0 = win(blk) + hf * 32, k_lo = blk * kTcKeys;
+      float sc[32];
+      float mh = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int key = k0 + c;
+        sc[c] = (row_ok && key >= k_lo && key <= pos) ? __uint_as_float(sv[c >> 4][c & 15]) : -INFINITY;
+        mh = fmaxf(mh, sc[c]);
+      }
+      sm.mx[b][hf][r] = mh;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(smem_addr(&sm.x_bar[b]));
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.x_bar[b]), (uint32_t)(blk >> 1) & 1u, a.timeout_ns));
+      if (!ok) break;
+      const float m_new = fmaxf(m_run, fmaxf(sm.mx[b][0][r], sm.mx[b][1][r]));
+      const float mu = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m_run - mu);   // 0 while nothing was seen
+      m_run = m_new;
+      float lsum = 0.f;
+      uint32_t ph[16], pl[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float p0 = exp2f(sc[2 * i] - mu), p1 = exp2f(sc[2 * i + 1] - mu);
+        lsum += p0 + p1;
+        split_bf16x2(p0, p1, ph[i], pl[i]);
+      }
+      l_run = fmaf(l_run, alpha, lsum);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int cc = 4 * hf + j;
+        const uint32_t off = (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(sm.p[0] + off) = make_uint4(ph[4 * j], ph[4 * j + 1], ph[4 * j + 2], ph[4 * j + 3]);
+        *reinterpret_cast<uint4*>(sm.p[1] + off) = make_uint4(pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(smem_addr(&sm.p_full));
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.pv_full), (uint32_t)blk & 1u, a.timeout_ns));
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;");
+#pragma unroll
+      for (int c = 0; c < DH; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + kColPV + (uint32_t)(hf * DH + c), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[c + j] = fmaf(o[c + j], alpha, __uint_as_float(v[j]));
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;");
+    }
+    if (ok) {
+      sm.ls[hf][r] = l_run;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(smem_addr(&sm.l_bar));
+      ok = __all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.l_bar), 0u, a.timeout_ns));
+    }
+    if (!ok) {
+      if (lane == 0) pf_timeout(a.status, SITE_PF_EPI);
+    } else if (row_ok) {
+      const float inv = 1.0f / (sm.ls[0][r] + sm.ls[1][r]);
+      const int64_t base = (int64_t)t * a.ldo + (int64_t)head * HD + hf * DH;
+#pragma unroll
+      for (int c = 0; c < DH; c += 8) {
+        uint16_t pp[8][kPfParts];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) split_parts(o[c + j] * inv, pp[j]);
+#pragma unroll
+        for (int i = 0; i < kPfParts; ++i) {
+          if (i >= a.parts) break;
+          *reinterpret_cast<uint4*>(a.o[i] + base + c) =
+              make_uint4((uint32_t)pp[0][i] | ((uint32_t)pp[1][i] << 16), (uint32_t)pp[2][i] | ((uint32_t)pp[3][i] << 16),
+                         (uint32_t)pp[4][i] | ((uint32_t)pp[5][i] << 16), (uint32_t)pp[6][i] | ((uint32_t)pp[7][i] << 16));
+        }
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+  }
+}
+
 }  // namespace
 
 // Launch with programmatic stream serialisation (see pdl_wait).
@@ -765,8 +1087,28 @@ cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap
   return bn == kPfBN ? launch_gemm_epi<3, kPfBN>(epi, maps, g, s) : launch_gemm_epi<3, kPfBNNarrow>(epi, maps, g, s);
 }
 
-cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s) {
+bool prefill_attn_uses_tc(int head_dim, int group, int s0, int T) {
+  return (head_dim == 64 || head_dim == 128) && group >= 1 && group <= kTcRows && kTcRows % group == 0 &&
+         s0 + T >= kTcKeys;
+}
+
+template <int HD>
+cudaError_t launch_attn_tc(const PrefillAttn& a, const CUtensorMap* kv_map, cudaStream_t s) {
+  const int smem = (int)sizeof(TcAttnSmem<HD>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  TcAttnArgs args;
+  args.kv = *kv_map;
+  args.a = a;
+  const int tpc = kTcRows / a.group;
+  const dim3 grid((unsigned)(((a.T + tpc - 1) / tpc) * a.n_kv));
+  return launch_pdl(prefill_attn_tc_kernel<HD>, grid, dim3(kTcThreads), (size_t)smem, s, args);
+}
+
+cudaError_t launch_prefill_attn(const PrefillAttn& a, const CUtensorMap* kv_map, cudaStream_t s) {
   if (a.T <= 0) return cudaSuccess;
+  if (kv_map && prefill_attn_uses_tc(a.hd, a.group, a.s0, a.T))
+    return a.hd == 64 ? launch_attn_tc<64>(a, kv_map, s) : launch_attn_tc<128>(a, kv_map, s);
   const int smem = prefill_attn_smem_bytes(a.hd, a.group);
   const int groups = attn_groups(a.group), cta_tokens = kPfQT * groups;
   const dim3 grid((unsigned)(((a.T + cta_tokens - 1) / cta_tokens) * a.n_kv));

@@ -93,7 +93,19 @@ struct PrefillAttn {
   uint16_t* o[kPfParts];
   int32_t ldo;
   int32_t parts;          // bf16 parts written (2 or 3)
+  uint32_t* status;       // device status words (a timed-out wait records ST_TIMEOUT)
+  uint64_t timeout_ns;
 };
+
+// Attention on the 5th-generation tensor cores (prefill_attn_tc_kernel):
+// one CTA per 128 query rows (128 / group tokens x the group's query
+// heads) and KV head, K,V blocks of kTcKeys positions by TMA.  Taken when
+// head_dim is 64 or 128, the group divides 128 and the cache holds at least
+// kTcKeys positions after the chunk (s0 + T >= kTcKeys: every key window
+// lies inside written positions); otherwise the mma.sync kernel runs.
+constexpr int kTcRows = 128;
+constexpr int kTcKeys = 64;
+bool prefill_attn_uses_tc(int head_dim, int group, int s0, int T);
 
 int prefill_gemm_smem_bytes(int parts, int bn);
 
@@ -114,6 +126,9 @@ cudaError_t launch_prefill_norm(const float* x, int T, int hidden, const uint16_
 // encoded with boxes of bn rows (kPfBN or kPfBNNarrow)
 cudaError_t launch_prefill_gemm(int epi, const CUtensorMap* a, const CUtensorMap* w, int bn, const PrefillGemm& g,
                                 cudaStream_t s);
-cudaError_t launch_prefill_attn(const PrefillAttn& a, cudaStream_t s);
+// kv_map: the KV cache as rows of head_dim bf16 ([L][2][n_kv][max_seq]
+// rows), boxes of 64 dims x kTcKeys rows, 128-byte swizzle (for the
+// tensor-core kernel)
+cudaError_t launch_prefill_attn(const PrefillAttn& a, const CUtensorMap* kv_map, cudaStream_t s);
 
 }  // namespace amk

@@ -271,9 +271,11 @@ def kv_layers(a, b):
     ("tiny", 128, 300, 100, 0, 256),   # 256-row GEMM tiles for every matrix
     ("hd128", 0, 200, None, 3, 256),
     ("tiny", 0, 140, None, 0, 224),    # 224-row tiles: partial last tile of 256-row matrices
+    ("mha", 0, 200, 70, 0, 0),         # group 1 on the tensor-core attention (128 tokens per CTA)
 ])
 def test_tensor_core_prefill_matches_oracle(amk, orc, dev, variant, chunk, prompt, split, parts, rows):
-    """The tensor-core prefill (tcgen05 GEMMs, mma.sync attention) against
+    """The tensor-core prefill (tcgen05 GEMMs; tcgen05 attention once the
+    cache holds 64 positions, mma.sync attention before) against
     the oracle's batched causal prefill (orc_prefill_batched, itself pinned
     equal to sequential decode steps), then decode steps on top of it.
 
