@@ -143,6 +143,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32 or 64 consecutive TMEM columns of the warp's lane quarter, one
+// register each, waited for in the same statement
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_x64(uint32_t taddr, uint32_t (&v)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 
 // x = p[0] + p[1] + p[2] to 2^-27 relative (the first two: 2^-18): each
@@ -690,13 +710,18 @@ __global__ void __launch_bounds__(256, 2) prefill_attn_kernel(const PrefillAttn 
 //                        shared memory; P as bf16 hi + lo into shared memory
 //   O += P V             tcgen05.mma M 128, N head_dim, K 16 keys (P hi and
 //                        lo), V read in place from its TMA layout as an
-//                        MN-major operand; the block's product lands in TMEM
-//                        and is added into fp32 registers (O scaled by the
-//                        max correction), as the GEMM promotes its segments
-// Warp 0 streams K and V blocks with TMA (two stages), warp 1 issues the
-// MMAs, warps 2..9 compute.  S(i + 1) runs on the tensor cores while the
-// math warps work on block i.  Every wait is bounded.
-constexpr int kTcStages = 2;
+//                        MN-major operand; the block's product lands in one
+//                        of two TMEM buffers and is added into fp32
+//                        registers (O scaled by the max correction), as the
+//                        GEMM promotes its segments, one block late: the
+//                        math warps compute block i's softmax while the
+//                        tensor cores run block i - 1's P.V
+// Warp 0 streams K blocks (each stage freed once its S is computed) and V
+// blocks (freed after P.V) with TMA, warp 1 issues the MMAs, warps 2..9
+// compute.  Every wait is bounded.
+constexpr int kTcKStages = 2;
+constexpr int kTcVStages = 2;
+constexpr uint32_t kTcTmemCols = 512;   // S buffers [0, 128), P.V buffers [128, 384)
 constexpr int kTcMathWarps = 8;
 constexpr int kTcThreads = 64 + 32 * kTcMathWarps;
 
@@ -704,13 +729,13 @@ template <int HD>
 struct __align__(1024) TcAttnSmem {
   static constexpr int A = HD / 64;                 // 128-byte atoms along the head dim
   uint8_t q[2][A][kTcRows * 128];                   // q hi / lo: [part][atom][row][128 B], swizzled
-  uint8_t k[kTcStages][A][kTcKeys * 128];           // K block: [atom][key][128 B] (TMA, swizzled)
-  uint8_t v[kTcStages][A][kTcKeys * 128];           // V block, the same layout
-  uint8_t p[2][kTcRows * 128];                      // P hi / lo: [row][64 keys], swizzled
+  uint8_t k[kTcKStages][A][kTcKeys * 128];          // K block: [atom][key][128 B] (TMA, swizzled)
+  uint8_t v[kTcVStages][A][kTcKeys * 128];          // V block, the same layout
+  uint8_t p[2][2][kTcRows * 128];                   // P [block parity][hi / lo]: [row][64 keys], swizzled
   float mx[2][2][kTcRows];                          // block maxima [block parity][row half][row]
   float ls[2][kTcRows];                             // row sums [row half][row]
-  uint64_t kv_full[kTcStages], kv_empty[kTcStages];
-  uint64_t q_full, s_full[2], p_full, pv_full, x_bar[2], l_bar;
+  uint64_t k_full[kTcKStages], k_empty[kTcKStages], v_full[kTcVStages], v_empty[kTcVStages];
+  uint64_t q_full, s_full[2], p_full, pv_full[2], x_bar[2], l_bar;
   uint32_t tmem;
 };
 
@@ -739,6 +764,27 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
       ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// 2^x by the SFU's approximate exp2 (ex2.approx), subnormal results
+// flushed to zero: softmax weights that small do not count
+__device__ __forceinline__ float exp2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// a non-blocking test of an mbarrier phase (acquire on success)
+__device__ __forceinline__ bool mbar_test32(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -747,7 +793,7 @@ template <int HD>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ TcAttnArgs args) {
   using Sm = TcAttnSmem<HD>;
   constexpr int A = Sm::A, DH = HD / 2;   // atoms; head dims per math warp (row half)
-  constexpr uint32_t kColPV = 128;        // TMEM columns: S buffers at 0 and 64, P.V at 128
+  constexpr uint32_t kColPV = 128;        // TMEM columns: S buffers at 0 and 64, P.V buffers at 128 and 256
   constexpr uint32_t kIdS = idesc_bf16<kTcKeys>();
   constexpr uint32_t kIdPV = idesc_bf16<HD>() | (1u << 16);   // B (V) MN-major
   const PrefillAttn& a = args.a;
@@ -770,9 +816,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
 
   pdl_launch_dependents();
   if (tid == 0) {
-    for (int st = 0; st < kTcStages; ++st) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.kv_full[st])));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.kv_empty[st])));
+    for (int st = 0; st < kTcKStages; ++st) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.k_full[st])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.k_empty[st])));
+    }
+    for (int st = 0; st < kTcVStages; ++st) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.v_full[st])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.v_empty[st])));
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.q_full)), "r"(kTcMathWarps));
     for (int b = 0; b < 2; ++b) {
@@ -780,14 +830,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.x_bar[b])), "r"(kTcMathWarps));
     }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.p_full)), "r"(kTcMathWarps));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pv_full)));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pv_full[0])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pv_full[1])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.l_bar)), "r"(kTcMathWarps));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&sm.tmem)),
-                 "r"(256));
+                 "r"(kTcTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
@@ -797,39 +848,60 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
   pdl_wait();   // q and this chunk's K,V come from the QKV GEMM
 
   if (warp == 0) {
-    if (lane == 0) {   // TMA producer: K and V of each block
-      int issued = 0;
-      for (int blk = 0; blk < nblk; ++blk) {
-        const int st = blk % kTcStages;
-        const uint32_t ph = (uint32_t)(blk / kTcStages) & 1u;
-        if (!bar_wait(smem_addr(&sm.kv_empty[st]), ph ^ 1u, a.timeout_ns)) {
-          pf_timeout(a.status, SITE_PF_TMA);
-          break;
-        }
-        const uint32_t fb = smem_addr(&sm.kv_full[st]);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                     "r"(2 * A * kTcKeys * 128)
-                     : "memory");
-        const int w0 = win(blk);
+    if (lane == 0) {   // TMA producer: K blocks run ahead of V blocks, each in its own ring
+      int kc = 0, vc = 0;   // next block to load, per ring
+      uint64_t t0 = global_timer();
+      bool ok = true;
+      while (kc < nblk || vc < nblk) {
+        bool moved = false;
+        if (kc < nblk &&
+            mbar_test32(smem_addr(&sm.k_empty[kc % kTcKStages]), ((uint32_t)(kc / kTcKStages) & 1u) ^ 1u)) {
+          const uint32_t fb = smem_addr(&sm.k_full[kc % kTcKStages]);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(A * kTcKeys * 128)
+                       : "memory");
 #pragma unroll
-        for (int at = 0; at < A; ++at) {
-          tma_2d(smem_addr(sm.k[st][at]), &args.kv, 64 * at, row_k + w0, fb);
-          tma_2d(smem_addr(sm.v[st][at]), &args.kv, 64 * at, row_v + w0, fb);
+          for (int at = 0; at < A; ++at)
+            tma_2d(smem_addr(sm.k[kc % kTcKStages][at]), &args.kv, 64 * at, row_k + win(kc), fb);
+          ++kc;
+          moved = true;
         }
-        ++issued;
+        if (vc < kc &&
+            mbar_test32(smem_addr(&sm.v_empty[vc % kTcVStages]), ((uint32_t)(vc / kTcVStages) & 1u) ^ 1u)) {
+          const uint32_t fb = smem_addr(&sm.v_full[vc % kTcVStages]);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(A * kTcKeys * 128)
+                       : "memory");
+#pragma unroll
+          for (int at = 0; at < A; ++at)
+            tma_2d(smem_addr(sm.v[vc % kTcVStages][at]), &args.kv, 64 * at, row_v + win(vc), fb);
+          ++vc;
+          moved = true;
+        }
+        if (moved) {
+          t0 = global_timer();
+        } else if (global_timer() - t0 > a.timeout_ns) {
+          pf_timeout(a.status, SITE_PF_TMA);
+          ok = false;
+          break;
+        } else {
+          __nanosleep(128);   // leave the issue slots to the math warps
+        }
       }
       // copies the consumers never waited for (they stopped early) land
       // before the CTA's shared memory goes away
-      for (int blk = max(0, issued - kTcStages); blk < issued; ++blk)
-        bar_wait(smem_addr(&sm.kv_full[blk % kTcStages]), (uint32_t)(blk / kTcStages) & 1u, a.timeout_ns);
+      if (!ok) {
+        for (int blk = max(0, kc - kTcKStages); blk < kc; ++blk)
+          bar_wait(smem_addr(&sm.k_full[blk % kTcKStages]), (uint32_t)(blk / kTcKStages) & 1u, a.timeout_ns);
+        for (int blk = max(0, vc - kTcVStages); blk < vc; ++blk)
+          bar_wait(smem_addr(&sm.v_full[blk % kTcVStages]), (uint32_t)(blk / kTcVStages) & 1u, a.timeout_ns);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {   // MMA issuer
       bool ok = bar_wait(smem_addr(&sm.q_full), 0u, a.timeout_ns);
       asm volatile("tcgen05.fence::after_thread_sync;");
       auto issue_s = [&](int blk) -> bool {
-        const int st = blk % kTcStages;
-        if (!bar_wait(smem_addr(&sm.kv_full[st]), (uint32_t)(blk / kTcStages) & 1u, a.timeout_ns)) return false;
+        const int st = blk % kTcKStages;
+        if (!bar_wait(smem_addr(&sm.k_full[st]), (uint32_t)(blk / kTcKStages) & 1u, a.timeout_ns)) return false;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t d = tmem + (uint32_t)((blk & 1) * kTcKeys);
 #pragma unroll
@@ -842,26 +914,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
                      (ks != 0 || part != 0) ? 1u : 0u);
         }
         umma_commit(smem_addr(&sm.s_full[blk & 1]));
+        umma_commit(smem_addr(&sm.k_empty[st]));
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int blk = 0; ok && blk < nblk; ++blk) {
         if (blk + 1 < nblk && !(ok = issue_s(blk + 1))) break;
-        // P of this block written (and the previous block's P.V drained)
+        // P of this block written (and block blk - 2's P.V drained from the
+        // TMEM buffer and P buffer this block reuses)
         if (!(ok = bar_wait(smem_addr(&sm.p_full), (uint32_t)blk & 1u, a.timeout_ns))) break;
+        const int st = blk % kTcVStages;
+        if (!(ok = bar_wait(smem_addr(&sm.v_full[st]), (uint32_t)(blk / kTcVStages) & 1u, a.timeout_ns))) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
-        const int st = blk % kTcStages;
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk) {
           const uint64_t bd = mnmajor_sw128_desc(smem_addr(sm.v[st][0]) + (uint32_t)(kk * 16 * 128),
                                                  (uint32_t)(kTcKeys * 128));
 #pragma unroll
           for (int part = 0; part < 2; ++part)
-            umma_f16(tmem + kColPV, kmajor_sw128_desc(smem_addr(sm.p[part]) + (uint32_t)(kk * 32)), bd, kIdPV,
+            umma_f16(tmem + kColPV + (uint32_t)((blk & 1) * 128),
+                     kmajor_sw128_desc(smem_addr(sm.p[blk & 1][part]) + (uint32_t)(kk * 32)), bd, kIdPV,
                      (kk != 0 || part != 0) ? 1u : 0u);
         }
-        umma_commit(smem_addr(&sm.kv_empty[st]));
-        umma_commit(smem_addr(&sm.pv_full));
+        umma_commit(smem_addr(&sm.v_empty[st]));
+        umma_commit(smem_addr(&sm.pv_full[blk & 1]));
       }
       if (!ok) pf_timeout(a.status, SITE_PF_MMA);
     }
@@ -902,25 +978,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
     float o[DH];
 #pragma unroll
     for (int i = 0; i < DH; ++i) o[i] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f, alpha_prev = 0.f;
+    // o = o * alpha + the P.V of block i (waits for it)
+    auto accumulate = [&](int i, float alpha) -> bool {
+      if (!__all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.pv_full[i & 1]), (uint32_t)(i >> 1) & 1u, a.timeout_ns)))
+        return false;
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      uint32_t v[DH];
+      if constexpr (DH == 64)
+        tmem_ld_x64(lane_base + kColPV + (uint32_t)((i & 1) * 128 + hf * DH), v);
+      else
+        tmem_ld_x32(lane_base + kColPV + (uint32_t)((i & 1) * 128 + hf * DH), v);
+#pragma unroll
+      for (int j = 0; j < DH; ++j) o[j] = fmaf(o[j], alpha, __uint_as_float(v[j]));
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      return true;
+    };
     bool ok = true;
     for (int blk = 0; blk < nblk; ++blk) {
       const int b = blk & 1;
       ok = __all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.s_full[b]), (uint32_t)(blk >> 1) & 1u, a.timeout_ns));
       if (!ok) break;
       asm volatile("tcgen05.fence::after_thread_sync;");
-      uint32_t sv[2][16];
-      tmem_ld16(lane_base + (uint32_t)(b * kTcKeys + hf * 32), sv[0]);
-      tmem_ld16(lane_base + (uint32_t)(b * kTcKeys + hf * 32 + 16), sv[1]);
-      // keys of the window; valid: not taken by an earlier block, causal
-      const int k0 = win(blk) + hf * 32, k_lo = blk * kTcKeys;
+      uint32_t sv[32];
+      tmem_ld_x32(lane_base + (uint32_t)(b * kTcKeys + hf * 32), sv);
+      // keys of the window; valid: not taken by an earlier block, causal.
+      // A block whose keys are all valid for every row of the CTA (all but
+      // the last one or two) needs no mask.
+      const int w0 = win(blk), k0 = w0 + hf * 32, k_lo = blk * kTcKeys;
       float sc[32];
       float mh = -INFINITY;
+      if (w0 == k_lo && k_lo + kTcKeys - 1 <= a.s0 + tb0) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int key = k0 + c;
-        sc[c] = (row_ok && key >= k_lo && key <= pos) ? __uint_as_float(sv[c >> 4][c & 15]) : -INFINITY;
-        mh = fmaxf(mh, sc[c]);
+        for (int c = 0; c < 32; ++c) {
+          sc[c] = __uint_as_float(sv[c]);
+          mh = fmaxf(mh, sc[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int key = k0 + c;
+          sc[c] = (row_ok && key >= k_lo && key <= pos) ? __uint_as_float(sv[c]) : -INFINITY;
+          mh = fmaxf(mh, sc[c]);
+        }
       }
       sm.mx[b][hf][r] = mh;
       __syncwarp();
@@ -929,13 +1029,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
       if (!ok) break;
       const float m_new = fmaxf(m_run, fmaxf(sm.mx[b][0][r], sm.mx[b][1][r]));
       const float mu = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(m_run - mu);   // 0 while nothing was seen
+      const float alpha = exp2_sfu(m_run - mu);   // 0 while nothing was seen
       m_run = m_new;
       float lsum = 0.f;
       uint32_t ph[16], pl[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float p0 = exp2f(sc[2 * i] - mu), p1 = exp2f(sc[2 * i + 1] - mu);
+        const float p0 = exp2_sfu(sc[2 * i] - mu), p1 = exp2_sfu(sc[2 * i + 1] - mu);
         lsum += p0 + p1;
         split_bf16x2(p0, p1, ph[i], pl[i]);
       }
@@ -944,25 +1044,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
       for (int j = 0; j < 4; ++j) {
         const int cc = 4 * hf + j;
         const uint32_t off = (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
-        *reinterpret_cast<uint4*>(sm.p[0] + off) = make_uint4(ph[4 * j], ph[4 * j + 1], ph[4 * j + 2], ph[4 * j + 3]);
-        *reinterpret_cast<uint4*>(sm.p[1] + off) = make_uint4(pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
+        *reinterpret_cast<uint4*>(sm.p[b][0] + off) = make_uint4(ph[4 * j], ph[4 * j + 1], ph[4 * j + 2], ph[4 * j + 3]);
+        *reinterpret_cast<uint4*>(sm.p[b][1] + off) = make_uint4(pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;");
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(smem_addr(&sm.p_full));
-      ok = __all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.pv_full), (uint32_t)blk & 1u, a.timeout_ns));
-      if (!ok) break;
-      asm volatile("tcgen05.fence::after_thread_sync;");
-#pragma unroll
-      for (int c = 0; c < DH; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + kColPV + (uint32_t)(hf * DH + c), v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) o[c + j] = fmaf(o[c + j], alpha, __uint_as_float(v[j]));
-      }
-      asm volatile("tcgen05.fence::before_thread_sync;");
+      // the previous block's P.V ran on the tensor cores meanwhile
+      if (blk > 0 && !(ok = accumulate(blk - 1, alpha_prev))) break;
+      alpha_prev = alpha;
     }
+    if (ok) ok = accumulate(nblk - 1, alpha_prev);
     if (ok) {
       sm.ls[hf][r] = l_run;
       __syncwarp();
@@ -994,7 +1087,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
   if (warp == 1) {
     __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols));
   }
 }
 
