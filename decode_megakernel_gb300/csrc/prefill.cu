@@ -717,13 +717,15 @@ __global__ void __launch_bounds__(256, 2) prefill_attn_kernel(const PrefillAttn 
 //                        math warps compute block i's softmax while the
 //                        tensor cores run block i - 1's P.V
 // Warp 0 streams K blocks (each stage freed once its S is computed) and V
-// blocks (freed after P.V) with TMA, warp 1 issues the MMAs, warps 2..9
-// compute.  Every wait is bounded.
+// blocks (freed after P.V) with TMA, warp 1 issues the S MMAs and warp 10
+// the P.V MMAs, warps 2..9 compute.  Every wait is bounded.
 constexpr int kTcKStages = 2;
 constexpr int kTcVStages = 2;
 constexpr uint32_t kTcTmemCols = 512;   // S buffers [0, 128), P.V buffers [128, 384)
 constexpr int kTcMathWarps = 8;
-constexpr int kTcThreads = 64 + 32 * kTcMathWarps;
+// warps: 0 TMA, 1 S issue, 2..9 math, 10 P.V issue
+constexpr int kTcThreads = 96 + 32 * kTcMathWarps;
+constexpr int kTcPvWarp = 2 + kTcMathWarps;
 
 template <int HD>
 struct __align__(1024) TcAttnSmem {
@@ -735,7 +737,7 @@ struct __align__(1024) TcAttnSmem {
   float mx[2][2][kTcRows];                          // block maxima [block parity][row half][row]
   float ls[2][kTcRows];                             // row sums [row half][row]
   uint64_t k_full[kTcKStages], k_empty[kTcKStages], v_full[kTcVStages], v_empty[kTcVStages];
-  uint64_t q_full, s_full[2], p_full, pv_full[2], x_bar[2], l_bar;
+  uint64_t q_full, s_full[2], s_free[2], p_full[2], pv_full[2], x_bar[2], l_bar;
   uint32_t tmem;
 };
 
@@ -829,7 +831,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.s_full[b])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.x_bar[b])), "r"(kTcMathWarps));
     }
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.p_full)), "r"(kTcMathWarps));
+    for (int b = 0; b < 2; ++b) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.s_free[b])), "r"(kTcMathWarps));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.p_full[b])), "r"(kTcMathWarps));
+    }
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pv_full[0])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.pv_full[1])));
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm.l_bar)), "r"(kTcMathWarps));
@@ -895,46 +900,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
           bar_wait(smem_addr(&sm.v_full[blk % kTcVStages]), (uint32_t)(blk / kTcVStages) & 1u, a.timeout_ns);
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {   // MMA issuer
+  } else if (warp == 1 || warp == kTcPvWarp) {
+    // MMA issue, split over two threads (issuing one of these small MMAs
+    // takes about as long as running it): warp 1 issues S = Q K^T, warp 10
+    // P.V.  Operand descriptors are computed once; a 16-element k step is
+    // 32 bytes further in the 128-byte rows, +2 in the descriptor's address
+    // field (which no step carries out of).
+    constexpr uint64_t kAtomQ = (kTcRows * 128) >> 4, kAtomK = (kTcKeys * 128) >> 4;   // atom strides
+    constexpr uint64_t kStageK = (uint64_t)(A * kTcKeys * 128) >> 4, kPart = (kTcRows * 128) >> 4;
+    if (lane == 0 && warp == 1) {
       bool ok = bar_wait(smem_addr(&sm.q_full), 0u, a.timeout_ns);
       asm volatile("tcgen05.fence::after_thread_sync;");
-      auto issue_s = [&](int blk) -> bool {
+      const uint64_t dq0 = kmajor_sw128_desc(smem_addr(sm.q[0][0])), dq1 = kmajor_sw128_desc(smem_addr(sm.q[1][0]));
+      const uint64_t dk0 = kmajor_sw128_desc(smem_addr(sm.k[0][0]));
+      for (int blk = 0; ok && blk < nblk; ++blk) {
+        // the S buffer this block reuses was read by the math warps
+        if (blk >= 2 && !(ok = bar_wait(smem_addr(&sm.s_free[blk & 1]), (uint32_t)((blk - 2) >> 1) & 1u, a.timeout_ns)))
+          break;
         const int st = blk % kTcKStages;
-        if (!bar_wait(smem_addr(&sm.k_full[st]), (uint32_t)(blk / kTcKStages) & 1u, a.timeout_ns)) return false;
+        if (!(ok = bar_wait(smem_addr(&sm.k_full[st]), (uint32_t)(blk / kTcKStages) & 1u, a.timeout_ns))) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t d = tmem + (uint32_t)((blk & 1) * kTcKeys);
+        const uint64_t dk = dk0 + (uint64_t)st * kStageK;
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint32_t off = (uint32_t)((ks & 3) * 32);
-          const uint64_t bd = kmajor_sw128_desc(smem_addr(sm.k[st][ks >> 2]) + off);
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-            umma_f16(d, kmajor_sw128_desc(smem_addr(sm.q[part][ks >> 2]) + off), bd, kIdS,
-                     (ks != 0 || part != 0) ? 1u : 0u);
+          const uint64_t step = (uint64_t)((ks & 3) * 2);
+          const uint64_t bd = dk + (uint64_t)(ks >> 2) * kAtomK + step;
+          umma_f16(d, dq0 + (uint64_t)(ks >> 2) * kAtomQ + step, bd, kIdS, ks != 0 ? 1u : 0u);
+          umma_f16(d, dq1 + (uint64_t)(ks >> 2) * kAtomQ + step, bd, kIdS, 1u);
         }
         umma_commit(smem_addr(&sm.s_full[blk & 1]));
         umma_commit(smem_addr(&sm.k_empty[st]));
-        return true;
-      };
-      if (ok) ok = issue_s(0);
+      }
+      if (!ok) pf_timeout(a.status, SITE_PF_MMA);
+    } else if (lane == 0) {
+      bool ok = true;
+      const uint64_t dp0 = kmajor_sw128_desc(smem_addr(sm.p[0][0]));
+      const uint64_t dv0 = mnmajor_sw128_desc(smem_addr(sm.v[0][0]), (uint32_t)(kTcKeys * 128));
       for (int blk = 0; ok && blk < nblk; ++blk) {
-        if (blk + 1 < nblk && !(ok = issue_s(blk + 1))) break;
         // P of this block written (and block blk - 2's P.V drained from the
         // TMEM buffer and P buffer this block reuses)
-        if (!(ok = bar_wait(smem_addr(&sm.p_full), (uint32_t)blk & 1u, a.timeout_ns))) break;
+        if (!(ok = bar_wait(smem_addr(&sm.p_full[blk & 1]), (uint32_t)(blk >> 1) & 1u, a.timeout_ns))) break;
         const int st = blk % kTcVStages;
         if (!(ok = bar_wait(smem_addr(&sm.v_full[st]), (uint32_t)(blk / kTcVStages) & 1u, a.timeout_ns))) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint32_t dpv = tmem + kColPV + (uint32_t)((blk & 1) * 128);
+        const uint64_t dv = dv0 + (uint64_t)st * kStageK;
+        const uint64_t dp = dp0 + (uint64_t)(blk & 1) * 2 * kPart;
 #pragma unroll
         for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-          const uint64_t bd = mnmajor_sw128_desc(smem_addr(sm.v[st][0]) + (uint32_t)(kk * 16 * 128),
-                                                 (uint32_t)(kTcKeys * 128));
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-            umma_f16(tmem + kColPV + (uint32_t)((blk & 1) * 128),
-                     kmajor_sw128_desc(smem_addr(sm.p[blk & 1][part]) + (uint32_t)(kk * 32)), bd, kIdPV,
-                     (kk != 0 || part != 0) ? 1u : 0u);
+          const uint64_t bd = dv + (uint64_t)(kk * 16 * 128 / 16);   // 16 keys = 16 rows of 128 bytes
+          umma_f16(dpv, dp + (uint64_t)(kk * 2), bd, kIdPV, kk != 0 ? 1u : 0u);
+          umma_f16(dpv, dp + kPart + (uint64_t)(kk * 2), bd, kIdPV, 1u);
         }
         umma_commit(smem_addr(&sm.v_empty[st]));
         umma_commit(smem_addr(&sm.pv_full[blk & 1]));
@@ -1002,6 +1019,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
       asm volatile("tcgen05.fence::after_thread_sync;");
       uint32_t sv[32];
       tmem_ld_x32(lane_base + (uint32_t)(b * kTcKeys + hf * 32), sv);
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(smem_addr(&sm.s_free[b]));   // S may be overwritten two blocks on
       // keys of the window; valid: not taken by an earlier block, causal.
       // A block whose keys are all valid for every row of the CTA (all but
       // the last one or two) needs no mask.
@@ -1050,7 +1070,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_attn_tc_kernel(const __
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;");
       __syncwarp();
-      if (lane == 0) mbar_arrive_cta(smem_addr(&sm.p_full));
+      if (lane == 0) mbar_arrive_cta(smem_addr(&sm.p_full[b]));
       // the previous block's P.V ran on the tensor cores meanwhile
       if (blk > 0 && !(ok = accumulate(blk - 1, alpha_prev))) break;
       alpha_prev = alpha;
