@@ -913,6 +913,11 @@ amk_status prefill_tensor_cores(amk_ctx* ctx, int32_t n, int32_t start_pos) {
   g.parts = pf.parts;
   g.status = dm.status;
   g.timeout_ns = ctx->timeout_ns;
+  {
+    int sms = 0;
+    AMK_CUDA(ctx, cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device));
+    g.ctas = sms;
+  }
   PrefillAttn at{};
   at.q = pf.q;
   at.ldq = qd;

@@ -1,7 +1,8 @@
 // Tensor-core prefill kernels (see prefill.hpp for the algorithm).
 //
-// GEMM: one 128-token x BN-row output tile per CTA (BN = 256, or 224 where
-// that fills the SMs better: prefill_gemm_bn).  Warp 0 (one thread)
+// GEMM: 128-token x BN-row output tiles (BN = 256, or 224 where that fills
+// the SMs better: prefill_gemm_bn), a persistent CTA per SM taking every
+// gridDim-th tile.  Warp 0 (one thread)
 // streams k blocks of the activation parts and the weight slice through a
 // kPfStages-deep ring with TMA; warp 1 (one thread) issues tcgen05.mma
 // (kind::f16, bf16 x bf16 -> fp32, M 128, N 256, K 16) into one of two
@@ -288,7 +289,13 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
   GemmSmem<PARTS, BN>& sm = *reinterpret_cast<GemmSmem<PARTS, BN>*>(
       (reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = blockIdx.x * kPfBM, n0 = blockIdx.y * BN;
+  // persistent: CTA c takes tiles c, c + gridDim.x, ... (token tile fastest,
+  // so the CTAs working at one time share weight slices through L2); each
+  // role keeps its ring stage and accumulator segment counters across tiles,
+  // so the next tile's loads and first MMAs overlap this tile's epilogue
+  const int mt = (g.T + kPfBM - 1) / kPfBM;
+  const int n_tiles = mt * ((g.N + BN - 1) / BN);
+  const int nseg = (g.nk + kPfSegKB - 1) / kPfSegKB;
   pdl_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
@@ -316,95 +323,117 @@ __global__ void __launch_bounds__(kPfGemmThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {   // TMA producer
-      for (int kb = 0; kb < g.nk; ++kb) {
-        const int s = kb % kPfStages;
-        const uint32_t ph = (uint32_t)(kb / kPfStages) & 1u;
-        if (!bar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, g.timeout_ns)) {
-          pf_timeout(g.status, SITE_PF_TMA);
-          sm.failed = 1;
-          break;
-        }
-        const uint32_t fb = smem_addr(&sm.full[s]);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
-                     "r"(PARTS * kPfATile + Shape::kBTile)
-                     : "memory");
-        const int k = kb * kPfBK;
+      int it = 0;      // ring stages used so far
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+        const int m0 = (tile % mt) * kPfBM, n0 = (tile / mt) * BN;
+        for (int kb = 0; kb < g.nk; ++kb, ++it) {
+          const int s = it % kPfStages;
+          const uint32_t ph = (uint32_t)(it / kPfStages) & 1u;
+          if (!bar_wait(smem_addr(&sm.empty[s]), ph ^ 1u, g.timeout_ns)) {
+            pf_timeout(g.status, SITE_PF_TMA);
+            sm.failed = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_addr(&sm.full[s]);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb),
+                       "r"(PARTS * kPfATile + Shape::kBTile)
+                       : "memory");
+          const int k = kb * kPfBK;
 #pragma unroll
-        for (int part = 0; part < PARTS; ++part) tma_2d(smem_addr(sm.a[s][part]), &maps.a[part], k, m0, fb);
-        tma_4d(smem_addr(sm.w[s]), &maps.w, k % g.Kt, 0, k / g.Kt, n0 / g.Rt, fb);
+          for (int part = 0; part < PARTS; ++part) tma_2d(smem_addr(sm.a[s][part]), &maps.a[part], k, m0, fb);
+          tma_4d(smem_addr(sm.w[s]), &maps.w, k % g.Kt, 0, k / g.Kt, n0 / g.Rt, fb);
+        }
       }
+      // copies the MMA warp never waited for (it stopped early) land before
+      // the CTA's shared memory goes away
+      if (!ok)
+        for (int j = max(0, it - kPfStages); j < it; ++j)
+          bar_wait(smem_addr(&sm.full[j % kPfStages]), (uint32_t)(j / kPfStages) & 1u, g.timeout_ns);
     }
   } else if (warp == 1) {
     if (lane == 0) {   // MMA issuer: the parts of A against the same W slice
-      for (int kb = 0; kb < g.nk; ++kb) {
-        const int seg = kb / kPfSegKB, b = seg & 1;
-        const uint32_t dt = tmem + (uint32_t)(b * kPfBN);
-        const bool first = kb % kPfSegKB == 0;
-        if (first) {   // this buffer's previous segment must have been drained
-          if (!bar_wait(smem_addr(&sm.acc_empty[b]), ((uint32_t)(seg >> 1) & 1u) ^ 1u, g.timeout_ns)) {
+      int it = 0, gseg = 0;   // ring stages and accumulator segments used so far
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+        for (int kb = 0; kb < g.nk; ++kb, ++it) {
+          const int seg = gseg + kb / kPfSegKB, b = seg & 1;
+          const uint32_t dt = tmem + (uint32_t)(b * kPfBN);
+          const bool first = kb % kPfSegKB == 0;
+          if (first) {   // this buffer's previous segment must have been drained
+            if (!bar_wait(smem_addr(&sm.acc_empty[b]), ((uint32_t)(seg >> 1) & 1u) ^ 1u, g.timeout_ns)) {
+              pf_timeout(g.status, SITE_PF_MMA);
+              sm.failed = 1;
+              ok = false;
+              break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;");
+          }
+          const int s = it % kPfStages;
+          const uint32_t ph = (uint32_t)(it / kPfStages) & 1u;
+          if (!bar_wait(smem_addr(&sm.full[s]), ph, g.timeout_ns)) {
             pf_timeout(g.status, SITE_PF_MMA);
             sm.failed = 1;
+            ok = false;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;");
-        }
-        const int s = kb % kPfStages;
-        const uint32_t ph = (uint32_t)(kb / kPfStages) & 1u;
-        if (!bar_wait(smem_addr(&sm.full[s]), ph, g.timeout_ns)) {
-          pf_timeout(g.status, SITE_PF_MMA);
-          sm.failed = 1;
-          break;
-        }
-        asm volatile("tcgen05.fence::after_thread_sync;");
-        const uint32_t bw = smem_addr(sm.w[s]);
+          const uint32_t bw = smem_addr(sm.w[s]);
 #pragma unroll
-        for (int k = 0; k < kPfBK / 16; ++k) {
-          const uint64_t bd = kmajor_sw128_desc(bw + k * 32);
+          for (int k = 0; k < kPfBK / 16; ++k) {
+            const uint64_t bd = kmajor_sw128_desc(bw + k * 32);
 #pragma unroll
-          for (int part = 0; part < PARTS; ++part)
-            umma_bf16<BN>(dt, kmajor_sw128_desc(smem_addr(sm.a[s][part]) + k * 32), bd,
-                      (!first || k != 0 || part != 0) ? 1u : 0u);
+            for (int part = 0; part < PARTS; ++part)
+              umma_bf16<BN>(dt, kmajor_sw128_desc(smem_addr(sm.a[s][part]) + k * 32), bd,
+                            (!first || k != 0 || part != 0) ? 1u : 0u);
+          }
+          umma_commit(smem_addr(&sm.empty[s]));
+          // the segment is complete once every MMA issued into it has finished
+          if (kb % kPfSegKB == kPfSegKB - 1 || kb == g.nk - 1) umma_commit(smem_addr(&sm.acc_full[b]));
         }
-        umma_commit(smem_addr(&sm.empty[s]));
-        // the segment is complete once every MMA issued into it has finished
-        if (kb % kPfSegKB == kPfSegKB - 1 || kb == g.nk - 1) umma_commit(smem_addr(&sm.acc_full[b]));
+        gseg += nseg;
       }
     }
   } else {
     const int quarter = warp & 3;   // TMEM lanes this warp may read: 32 * quarter ..
     const int col0 = ((warp - 2) >> 2) * kPfEpiCols;   // this warp's accumulator columns
-    const int t = m0 + quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col0;
-    float acc[kPfEpiCols];
-#pragma unroll
-    for (int i = 0; i < kPfEpiCols; ++i) acc[i] = 0.f;
-    const int nseg = (g.nk + kPfSegKB - 1) / kPfSegKB;
+    int gseg = 0;   // accumulator segments drained so far
     bool ok = true;
-    for (int seg = 0; seg < nseg && ok; ++seg) {
-      const int b = seg & 1;
-      ok = __all_sync(0xFFFFFFFFu, bar_wait(smem_addr(&sm.acc_full[b]), (uint32_t)(seg >> 1) & 1u, g.timeout_ns));
-      if (!ok) break;
-      asm volatile("tcgen05.fence::after_thread_sync;");
+    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+      const int m0 = (tile % mt) * kPfBM, n0 = (tile / mt) * BN;
+      const int t = m0 + quarter * 32 + lane;
+      float acc[kPfEpiCols];
 #pragma unroll
-      for (int c = 0; c < kPfEpiCols; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + (uint32_t)(b * kPfBN + c), v);
+      for (int i = 0; i < kPfEpiCols; ++i) acc[i] = 0.f;
+      for (int sg = 0; sg < nseg; ++sg, ++gseg) {
+        const int b = gseg & 1;
+        ok = __all_sync(0xFFFFFFFFu,
+                        bar_wait(smem_addr(&sm.acc_full[b]), (uint32_t)(gseg >> 1) & 1u, g.timeout_ns));
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;");
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[c + j] += __uint_as_float(v[j]);
+        for (int c = 0; c < kPfEpiCols; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(lane_base + (uint32_t)(b * kPfBN + c), v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[c + j] += __uint_as_float(v[j]);
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;");
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm.acc_empty[b])) : "memory");
       }
-      asm volatile("tcgen05.fence::before_thread_sync;");
-      __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm.acc_empty[b])) : "memory");
-    }
-    if (!ok) {
-      if (lane == 0) pf_timeout(g.status, SITE_PF_EPI);
-    } else if (!sm.failed && t < g.T) {
+      if (!ok) {
+        if (lane == 0) pf_timeout(g.status, SITE_PF_EPI);
+      } else if (!sm.failed && t < g.T) {
 #pragma unroll
-      for (int c = 0; c < kPfEpiCols; c += 16) {
-        uint32_t v[16];
+        for (int c = 0; c < kPfEpiCols; c += 16) {
+          uint32_t v[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(acc[c + j]);
-        if (n0 + col0 + c < g.N) gemm_epilogue<EPI>(g, t, n0 + col0 + c, v);
+          for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(acc[c + j]);
+          if (n0 + col0 + c < g.N) gemm_epilogue<EPI>(g, t, n0 + col0 + c, v);
+        }
       }
     }
   }
@@ -1176,7 +1205,8 @@ cudaError_t launch_gemm_instance(const GemmMaps& maps, const PrefillGemm& g, cud
   cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<EPI, PARTS, BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((g.T + kPfBM - 1) / kPfBM, (g.N + BN - 1) / BN);
+  const int tiles = ((g.T + kPfBM - 1) / kPfBM) * ((g.N + BN - 1) / BN);
+  const dim3 grid((unsigned)std::max(1, std::min(tiles, g.ctas)));
   return launch_pdl(prefill_gemm_kernel<EPI, PARTS, BN>, grid, dim3(kPfGemmThreads), smem, s, maps, g);
 }
 

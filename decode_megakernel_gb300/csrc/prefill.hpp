@@ -79,6 +79,7 @@ struct PrefillGemm {
   int32_t parts;          // bf16 parts of the activations (2 or 3)
   uint32_t* status;       // device status words (a timed-out wait records ST_TIMEOUT)
   uint64_t timeout_ns;
+  int32_t ctas;           // persistent CTAs (at most one per SM; fewer when there are fewer tiles)
 };
 
 // Causal GQA attention of a chunk: queries Q (fp32, RoPE applied) of
