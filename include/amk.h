@@ -107,9 +107,10 @@ typedef struct {
     int32_t ring_slots;         /* slots of the per-CTA weight ring, 1..8; the K,V history of
                                    attention streams through the other 12 - ring_slots slots
                                    of the CTA's shared-memory pool.  0 (default): chosen per
-                                   step, 8 (128 KB of 16 KB weight tiles in flight), or 4 when
-                                   the weights are int8 / int4 and a context split holds more
-                                   than one attention chunk (4 KV stages) */
+                                   step, 8 (128 KB of 16 KB weight tiles in flight), or 4
+                                   (int8) / 3 (int4) when the weights are quantised and a
+                                   context split holds more than one attention chunk (4 KV
+                                   stages) */
     int32_t l2_prefetch_tiles;  /* weight tiles a CTA may prefetch into L2 beyond its full
                                    ring while its consumers run attention, the split merge
                                    or the O projection (-1: off; 0: default) */
