@@ -81,6 +81,9 @@ def _load():
                                        C.POINTER(P)]),
         "amk_load_weights_requeued": (C.c_int, [cfgp, C.POINTER(amk_weights), P, C.c_size_t, P, P, schp, P,
                                                 C.c_size_t, C.POINTER(P)]),
+        "amk_weights_staging_bytes": (C.c_size_t, [cfgp]),
+        "amk_load_weights_staged": (C.c_int, [cfgp, C.POINTER(amk_weights), P, C.c_size_t, P, P, schp, P,
+                                              C.c_size_t, C.POINTER(P)]),
         "amk_prefill": (C.c_int, [P, C.POINTER(C.c_int32), C.c_int32, C.c_int32]),
         "amk_decode_step": (C.c_int, [P, C.c_int32, C.c_int32, P]),
         "amk_decode_step_host": (C.c_int, [P, C.c_int32, C.c_int32, P]),
@@ -145,6 +148,20 @@ def amk_load_weights(cfg, weights, workspace_ptr, workspace_bytes, kv_ptr, strea
     st = lib.amk_load_weights(C.byref(cfg), C.byref(weights), C.c_void_p(workspace_ptr),
                               workspace_bytes, C.c_void_p(kv_ptr), C.c_void_p(stream_ptr),
                               C.byref(sched) if sched else None, C.byref(ctx))
+    return st, ctx
+
+
+def amk_weights_staging_bytes(cfg) -> int:
+    return int(lib.amk_weights_staging_bytes(C.byref(cfg)))
+
+
+def amk_load_weights_staged(cfg, host_weights, workspace_ptr, workspace_bytes, kv_ptr, stream_ptr, sched,
+                            staging_ptr, staging_bytes):
+    ctx = C.c_void_p()
+    st = lib.amk_load_weights_staged(C.byref(cfg), C.byref(host_weights), C.c_void_p(workspace_ptr),
+                                     workspace_bytes, C.c_void_p(kv_ptr), C.c_void_p(stream_ptr),
+                                     C.byref(sched) if sched else None, C.c_void_p(staging_ptr), staging_bytes,
+                                     C.byref(ctx))
     return st, ctx
 
 
@@ -287,13 +304,15 @@ def _linear(lin):
 class Decoder:
     """One loaded model: owns (through torch) its workspace and KV cache.
 
-    ``weights`` holds device tensors with attributes embed, final_norm,
-    lm_head (or None when tied) and layers (dicts of attn_norm, ffn_norm and
-    wq..wd objects carrying .w / .scales / .zeros)."""
+    ``weights`` holds tensors with attributes embed, final_norm, lm_head
+    (or None when tied) and layers (dicts of attn_norm, ffn_norm and wq..wd
+    objects carrying .w / .scales / .zeros): device tensors, or host tensors
+    (then loaded through a device staging buffer, amk_load_weights_staged,
+    onto `device`)."""
 
     def __init__(self, weights, max_seq: int, stream: torch.cuda.Stream | None = None,
                  sched: amk_schedule_config | None = None, kv_cache: torch.Tensor | None = None,
-                 schedule: bytes | None = None):
+                 schedule: bytes | None = None, device: torch.device | None = None):
         """schedule: optional serialised re-queueing of the lowering's tasks
         (amk_load_weights_requeued); None loads the library's own lowering."""
         cfg = weights.cfg
@@ -304,7 +323,8 @@ class Decoder:
         nbytes = amk_workspace_bytes(self.cfg, sched)
         if nbytes == 0:
             raise AmkError(AMK_ERR_UNSUPPORTED, last_error())
-        dev = weights.embed.device
+        host = weights.embed.device.type == "cpu"
+        dev = (device or torch.device("cuda", torch.cuda.current_device())) if host else weights.embed.device
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         if kv_cache is None:
             kv_cache = torch.zeros((cfg.n_layers, 2, cfg.n_kv_heads, max_seq, cfg.head_dim),
@@ -319,7 +339,16 @@ class Decoder:
         w = amk_weights(_ptr(weights.embed), _ptr(weights.final_norm),
                         _linear(weights.lm_head) if weights.lm_head is not None else amk_linear(),
                         C.cast(layers, C.POINTER(amk_layer_weights)))
-        if schedule is None:
+        if host:
+            if schedule is not None:
+                raise ValueError("a re-queued schedule needs device weights")
+            sb = amk_weights_staging_bytes(self.cfg)
+            staging = torch.empty(max(sb, 256), dtype=torch.uint8, device=dev)
+            st, ctx = amk_load_weights_staged(self.cfg, w, self.workspace.data_ptr(), nbytes,
+                                              self.kv.data_ptr(), self.stream.cuda_stream, sched,
+                                              staging.data_ptr(), sb)
+            del staging
+        elif schedule is None:
             st, ctx = amk_load_weights(self.cfg, w, self.workspace.data_ptr(), nbytes,
                                        self.kv.data_ptr(), self.stream.cuda_stream, sched)
         else:

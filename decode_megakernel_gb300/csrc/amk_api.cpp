@@ -351,6 +351,52 @@ amk_status encode_prefill_maps(amk_ctx* ctx, const DevMat* mats) {
   return AMK_OK;
 }
 
+// Bytes of a linear map's tensors in its stored format (amk_linear): codes,
+// fp16 scales, packed 4-bit zero points.
+struct LinearBytes {
+  size_t w = 0, s = 0, z = 0;
+};
+LinearBytes linear_bytes(int fmt, int64_t rows, int64_t cols) {
+  LinearBytes b;
+  if (fmt == AMK_FORMAT_BF16) {
+    b.w = (size_t)(rows * cols * 2);
+  } else if (fmt == AMK_FORMAT_INT8) {
+    b.w = (size_t)(rows * cols);
+    b.s = (size_t)(rows * 2);
+  } else {
+    const int64_t ng = cols / 128;
+    b.w = (size_t)(rows * cols / 2);
+    b.s = (size_t)(rows * ng * 2);
+    b.z = (size_t)(rows * ((ng + 1) / 2));
+  }
+  return b;
+}
+
+size_t align256z(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// The linear maps packed together (the groups of launch_pack_matrix), as
+// (rows, cols, format) per member; the staging a host-memory load needs is
+// the largest group's bytes, each tensor 256-byte aligned.
+struct LinearShape {
+  int64_t rows, cols;
+};
+size_t group_staging_bytes(int fmt, std::initializer_list<LinearShape> members) {
+  size_t t = 0;
+  for (const LinearShape& m : members) {
+    const LinearBytes b = linear_bytes(fmt, m.rows, m.cols);
+    t += align256z(b.w) + align256z(b.s) + align256z(b.z);
+  }
+  return t;
+}
+size_t staging_bytes_of(const amk_config& c) {
+  const int64_t H = c.hidden, F = c.ffn, qd = (int64_t)c.n_heads * c.head_dim, kvd = (int64_t)c.n_kv_heads * c.head_dim;
+  const int f = c.weight_format;
+  size_t m = std::max({group_staging_bytes(f, {{qd, H}, {kvd, H}, {kvd, H}}), group_staging_bytes(f, {{H, qd}}),
+                       group_staging_bytes(f, {{F, H}, {F, H}}), group_staging_bytes(f, {{H, F}})});
+  if (!c.tied_embeddings) m = std::max(m, group_staging_bytes(lm_format(c), {{c.vocab, H}}));
+  return m;
+}
+
 // present and aligned for the kernel's vector loads (bf16 rows are read 16
 // bytes, int8 rows 8 bytes, int4 rows 4 bytes, fp16 scales 2 bytes at a time)
 bool linear_ok(const amk_linear& l, int fmt) {
@@ -620,10 +666,13 @@ namespace {
 
 // amk_load_weights, optionally with the lowering's tasks re-queued as a
 // given serialised schedule assigns them (amk_load_weights_requeued)
+// staging != NULL: the weights are in host memory; each group of matrices
+// is copied into the staging buffer and repacked from there (the device
+// never holds the caller's copy of the model).
 amk_status load_impl(const amk_config* cfg, const amk_weights* weights, void* workspace_dev,
                      size_t workspace_bytes, void* kv_cache_dev, void* stream,
                      const amk_schedule_config* sched, const void* requeue_buf, size_t requeue_bytes,
-                     amk_ctx** out) {
+                     amk_ctx** out, void* staging = nullptr, size_t staging_bytes = 0) {
   if (!out) return fail(nullptr, AMK_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!cfg || !weights || !workspace_dev || !kv_cache_dev)
@@ -659,19 +708,27 @@ amk_status load_impl(const amk_config* cfg, const amk_weights* weights, void* wo
   Report rep = validate(s);
   if (!rep.ok) return bail(fail(ctx, AMK_ERR_SCHEDULE_INVALID, "schedule rejected: " + rep.msg));
 
-  // weights present for every matrix
+  // weights present for every matrix (device pointers also aligned for the
+  // pack kernels' vector loads; host pointers are copied to aligned staging)
   const int lmf = lm_format(c);
-  if (!weights->embed || !weights->final_norm || !weights->layers || !aligned(weights->embed, 16) ||
-      !aligned(weights->final_norm, 2))
+  const bool host = staging != nullptr;
+  auto lin_ok = [&](const amk_linear& l, int fmt) {
+    if (!host) return linear_ok(l, fmt);
+    return l.w && (fmt == AMK_FORMAT_BF16 || l.scales) && (fmt != AMK_FORMAT_INT4 || l.zeros);
+  };
+  if (host && (((uintptr_t)staging & 255) || staging_bytes < staging_bytes_of(c)))
+    return bail(fail(ctx, AMK_ERR_INVALID_ARG, "staging buffer misaligned or smaller than amk_weights_staging_bytes"));
+  if (!weights->embed || !weights->final_norm || !weights->layers ||
+      (!host && (!aligned(weights->embed, 16) || !aligned(weights->final_norm, 2))))
     return bail(fail(ctx, AMK_ERR_INVALID_ARG, "missing or misaligned embedding, final norm or layer table"));
-  if (!c.tied_embeddings && !linear_ok(weights->lm_head, lmf))
+  if (!c.tied_embeddings && !lin_ok(weights->lm_head, lmf))
     return bail(fail(ctx, AMK_ERR_INVALID_ARG, "missing LM-head weights"));
   for (int l = 0; l < c.n_layers; ++l) {
     const amk_layer_weights& lw = weights->layers[l];
-    if (!lw.attn_norm || !lw.ffn_norm || !aligned(lw.attn_norm, 2) || !aligned(lw.ffn_norm, 2))
+    if (!lw.attn_norm || !lw.ffn_norm || (!host && (!aligned(lw.attn_norm, 2) || !aligned(lw.ffn_norm, 2))))
       return bail(fail(ctx, AMK_ERR_INVALID_ARG, "missing or misaligned norm weights"));
     for (const amk_linear* lin : {&lw.wq, &lw.wk, &lw.wv, &lw.wo, &lw.wg, &lw.wu, &lw.wd})
-      if (!linear_ok(*lin, c.weight_format))
+      if (!lin_ok(*lin, c.weight_format))
         return bail(fail(ctx, AMK_ERR_INVALID_ARG, "missing or misaligned linear weights / scales / zeros"));
   }
 
@@ -815,36 +872,73 @@ amk_status load_impl(const amk_config* cfg, const amk_weights* weights, void* wo
   // tagged scratch and status start zeroed: tag 0 is never a version's tag
   AMK_CUDA(ctx, cudaMemsetAsync(ws + L.xres, 0, L.status + 64 - L.xres, st_));
 
-  // weights: embedding (row major copy), norms, tiled matrices
+  // weights: embedding (row major copy), norms, tiled matrices.  Copies
+  // take the direction from the pointers (host or device memory); with
+  // host weights each group of matrices goes through the staging buffer,
+  // whose next fill is ordered on the stream after the pack that read it.
   const size_t H2 = (size_t)c.hidden * 2;
-  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.embed, weights->embed, (size_t)c.vocab * H2, cudaMemcpyDeviceToDevice, st_));
-  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.final_norm, weights->final_norm, H2, cudaMemcpyDeviceToDevice, st_));
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.embed, weights->embed, (size_t)c.vocab * H2, cudaMemcpyDefault, st_));
+  AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.final_norm, weights->final_norm, H2, cudaMemcpyDefault, st_));
+  const int64_t qd = (int64_t)c.n_heads * c.head_dim, kvd = (int64_t)c.n_kv_heads * c.head_dim;
+  // the group's linears with device pointers: the caller's, or copies in staging
+  auto staged = [&](int fmt, std::initializer_list<std::pair<const amk_linear*, LinearShape>> members,
+                    amk_linear* dst) -> amk_status {
+    size_t off = 0;
+    int i = 0;
+    for (const auto& mb : members) {
+      dst[i] = *mb.first;
+      if (host) {
+        const LinearBytes b = linear_bytes(fmt, mb.second.rows, mb.second.cols);
+        uint8_t* base = (uint8_t*)staging;
+        AMK_CUDA(ctx, cudaMemcpyAsync(base + off, mb.first->w, b.w, cudaMemcpyDefault, st_));
+        dst[i].w = base + off;
+        off += align256z(b.w);
+        if (b.s) {
+          AMK_CUDA(ctx, cudaMemcpyAsync(base + off, mb.first->scales, b.s, cudaMemcpyDefault, st_));
+          dst[i].scales = base + off;
+          off += align256z(b.s);
+        }
+        if (b.z) {
+          AMK_CUDA(ctx, cudaMemcpyAsync(base + off, mb.first->zeros, b.z, cudaMemcpyDefault, st_));
+          dst[i].zeros = base + off;
+          off += align256z(b.z);
+        }
+      }
+      ++i;
+    }
+    return AMK_OK;
+  };
+  const int64_t Hh = c.hidden, Ff = c.ffn;
   for (int l = 0; l < c.n_layers; ++l) {
     const amk_layer_weights& lw = weights->layers[l];
-    AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.attn_norm + l * H2, lw.attn_norm, H2, cudaMemcpyDeviceToDevice, st_));
-    AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.ffn_norm + l * H2, lw.ffn_norm, H2, cudaMemcpyDeviceToDevice, st_));
-    launch_pack_matrix(M_QKV, c.weight_format, mats[M_QKV], l, lw.wq.w, lw.wq.scales, lw.wq.zeros,
-                       lw.wk.w, lw.wk.scales, lw.wk.zeros, lw.wv.w, lw.wv.scales, lw.wv.zeros,
-                       c.n_heads, c.n_kv_heads, c.head_dim, st_);
-    launch_pack_matrix(M_O, c.weight_format, mats[M_O], l, lw.wo.w, lw.wo.scales, lw.wo.zeros,
-                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c.n_heads,
-                       c.n_kv_heads, c.head_dim, st_);
-    launch_pack_matrix(M_GU, c.weight_format, mats[M_GU], l, lw.wg.w, lw.wg.scales, lw.wg.zeros,
-                       lw.wu.w, lw.wu.scales, lw.wu.zeros, nullptr, nullptr, nullptr, c.n_heads,
-                       c.n_kv_heads, c.head_dim, st_);
-    launch_pack_matrix(M_DOWN, c.weight_format, mats[M_DOWN], l, lw.wd.w, lw.wd.scales, lw.wd.zeros,
-                       nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c.n_heads,
-                       c.n_kv_heads, c.head_dim, st_);
+    const int f = c.weight_format;
+    amk_linear d[3];
+    AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.attn_norm + l * H2, lw.attn_norm, H2, cudaMemcpyDefault, st_));
+    AMK_CUDA(ctx, cudaMemcpyAsync(ws + L.ffn_norm + l * H2, lw.ffn_norm, H2, cudaMemcpyDefault, st_));
+    if ((st = staged(f, {{&lw.wq, {qd, Hh}}, {&lw.wk, {kvd, Hh}}, {&lw.wv, {kvd, Hh}}}, d)) != AMK_OK) return bail(st);
+    launch_pack_matrix(M_QKV, f, mats[M_QKV], l, d[0].w, d[0].scales, d[0].zeros, d[1].w, d[1].scales, d[1].zeros,
+                       d[2].w, d[2].scales, d[2].zeros, c.n_heads, c.n_kv_heads, c.head_dim, st_);
+    if ((st = staged(f, {{&lw.wo, {Hh, qd}}}, d)) != AMK_OK) return bail(st);
+    launch_pack_matrix(M_O, f, mats[M_O], l, d[0].w, d[0].scales, d[0].zeros, nullptr, nullptr, nullptr, nullptr,
+                       nullptr, nullptr, c.n_heads, c.n_kv_heads, c.head_dim, st_);
+    if ((st = staged(f, {{&lw.wg, {Ff, Hh}}, {&lw.wu, {Ff, Hh}}}, d)) != AMK_OK) return bail(st);
+    launch_pack_matrix(M_GU, f, mats[M_GU], l, d[0].w, d[0].scales, d[0].zeros, d[1].w, d[1].scales, d[1].zeros,
+                       nullptr, nullptr, nullptr, c.n_heads, c.n_kv_heads, c.head_dim, st_);
+    if ((st = staged(f, {{&lw.wd, {Hh, Ff}}}, d)) != AMK_OK) return bail(st);
+    launch_pack_matrix(M_DOWN, f, mats[M_DOWN], l, d[0].w, d[0].scales, d[0].zeros, nullptr, nullptr, nullptr,
+                       nullptr, nullptr, nullptr, c.n_heads, c.n_kv_heads, c.head_dim, st_);
     AMK_CUDA(ctx, cudaGetLastError());
   }
-  if (c.tied_embeddings)
-    launch_pack_matrix(M_LM, AMK_FORMAT_BF16, mats[M_LM], 0, weights->embed, nullptr, nullptr,
+  if (c.tied_embeddings) {   // from the workspace's row-major copy of the embedding
+    launch_pack_matrix(M_LM, AMK_FORMAT_BF16, mats[M_LM], 0, ws + L.embed, nullptr, nullptr,
                        nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, c.n_heads,
                        c.n_kv_heads, c.head_dim, st_);
-  else
-    launch_pack_matrix(M_LM, lmf, mats[M_LM], 0, weights->lm_head.w, weights->lm_head.scales,
-                       weights->lm_head.zeros, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
-                       c.n_heads, c.n_kv_heads, c.head_dim, st_);
+  } else {
+    amk_linear d[1];
+    if ((st = staged(lmf, {{&weights->lm_head, {(int64_t)c.vocab, Hh}}}, d)) != AMK_OK) return bail(st);
+    launch_pack_matrix(M_LM, lmf, mats[M_LM], 0, d[0].w, d[0].scales, d[0].zeros, nullptr, nullptr, nullptr,
+                       nullptr, nullptr, nullptr, c.n_heads, c.n_kv_heads, c.head_dim, st_);
+  }
   AMK_CUDA(ctx, cudaGetLastError());
   if (g.prefill_chunk > 0) {
     auto& pf = ctx->pf;
@@ -875,6 +969,23 @@ amk_status amk_load_weights(const amk_config* cfg, const amk_weights* weights, v
                             size_t workspace_bytes, void* kv_cache_dev, void* stream,
                             const amk_schedule_config* sched, amk_ctx** out) {
   return load_impl(cfg, weights, workspace_dev, workspace_bytes, kv_cache_dev, stream, sched, nullptr, 0, out);
+}
+
+size_t amk_weights_staging_bytes(const amk_config* cfg) {
+  if (!cfg || amk_check_config(cfg) != AMK_OK) return 0;
+  return staging_bytes_of(*cfg);
+}
+
+amk_status amk_load_weights_staged(const amk_config* cfg, const amk_weights* host_weights, void* workspace_dev,
+                                   size_t workspace_bytes, void* kv_cache_dev, void* stream,
+                                   const amk_schedule_config* sched, void* staging_dev, size_t staging_bytes,
+                                   amk_ctx** out) {
+  if (!staging_dev) {
+    if (out) *out = nullptr;
+    return fail(nullptr, AMK_ERR_INVALID_ARG, "staging buffer is NULL");
+  }
+  return load_impl(cfg, host_weights, workspace_dev, workspace_bytes, kv_cache_dev, stream, sched, nullptr, 0, out,
+                   staging_dev, staging_bytes);
 }
 
 amk_status amk_load_weights_requeued(const amk_config* cfg, const amk_weights* weights, void* workspace_dev,

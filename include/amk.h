@@ -186,6 +186,32 @@ amk_status amk_load_weights_requeued(const amk_config* cfg, const amk_weights* w
                                      const void* schedule, size_t schedule_bytes, amk_ctx** out);
 
 /*
+ * Bytes of the device staging buffer amk_load_weights_staged needs for this
+ * model: the largest group of matrices repacked together (QKV, O, gate + up,
+ * down, or the untied LM head) in their stored formats, each tensor rounded
+ * up to 256 bytes; 0 for an unsupported config.  Host only.
+ */
+size_t amk_weights_staging_bytes(const amk_config* cfg);
+
+/*
+ * amk_load_weights with the weights in HOST memory (every pointer of
+ * host_weights, the layer table included, is host memory; page-locked
+ * memory copies fastest): the embedding and the norms are copied straight
+ * into the workspace, and each group of matrices is copied into staging_dev
+ * (caller-owned device memory, 256-byte aligned, at least
+ * amk_weights_staging_bytes) and repacked from there, so the device holds
+ * the packed model plus one staging buffer instead of the caller's copy of
+ * the model as well.  The call returns after the stream has finished the
+ * copies: staging_dev and the host weights may be freed when it returns.
+ * Errors as amk_load_weights; a NULL, misaligned or too small staging
+ * buffer is AMK_ERR_INVALID_ARG.
+ */
+amk_status amk_load_weights_staged(const amk_config* cfg, const amk_weights* host_weights, void* workspace_dev,
+                                   size_t workspace_bytes, void* kv_cache_dev, void* stream,
+                                   const amk_schedule_config* sched, void* staging_dev, size_t staging_bytes,
+                                   amk_ctx** out);
+
+/*
  * Fill the KV cache with the K,V rows of host_tokens at positions
  * start_pos .. start_pos + n - 1 (start_pos <= the valid KV length,
  * start_pos + n <= max_seq, every token in [0, vocab)); no logits.

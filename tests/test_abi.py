@@ -133,3 +133,39 @@ def test_validate_rejects_garbage(amk):
     assert st == amk.AMK_ERR_SCHEDULE_INVALID and "malformed" in rep
     st, rep = amk.amk_validate_serialized(b"\x01" * 7)
     assert st == amk.AMK_ERR_INVALID_ARG
+
+
+def test_staging_bytes_is_the_largest_group(amk):
+    """amk_weights_staging_bytes: the largest group of matrices packed
+    together (QKV, O, gate + up, down, the untied LM head), every tensor of
+    it (codes, fp16 scales, packed 4-bit zero points) rounded up to 256
+    bytes; the tied LM head packs from the workspace's embedding copy."""
+    def tensors(fmt, rows, cols):
+        if fmt == "bf16":
+            return [rows * cols * 2]
+        if fmt == "int8":
+            return [rows * cols, rows * 2]
+        ng = cols // 128
+        return [rows * cols // 2, rows * ng * 2, rows * ((ng + 1) // 2)]
+
+    def group(fmt, shapes):
+        return sum(-(-b // 256) * 256 for r, k in shapes for b in tensors(fmt, r, k))
+
+    for m in (wc.LLAMA_8B_BF16, wc.LLAMA_1B, wc.LLAMA_8B_INT8, wc.LLAMA_8B_INT4):
+        H, F, qd, kvd = m.hidden, m.ffn, m.q_dim, m.kv_dim
+        f = m.weight_format
+        want = max(group(f, [(qd, H), (kvd, H), (kvd, H)]), group(f, [(H, qd)]), group(f, [(F, H), (F, H)]),
+                   group(f, [(H, F)]))
+        if not m.tied_embeddings:
+            want = max(want, group(m.lm_head_format, [(m.vocab, H)]))
+        assert amk.amk_weights_staging_bytes(amk.make_config(m, 256)) == want, m.name
+    bad = cfg_of(amk, head_dim=96, hidden=384)
+    assert amk.amk_weights_staging_bytes(bad) == 0
+
+
+def test_staged_load_checks_its_buffer(amk):
+    """A NULL staging buffer is refused before anything touches a GPU."""
+    c = cfg_of(amk)
+    st, ctx = amk.amk_load_weights_staged(c, amk.amk_weights(), 256, 1 << 20, 256, 0,
+                                          amk.make_schedule_config(num_ctas=4), 0, 0)
+    assert st == amk.AMK_ERR_INVALID_ARG and not ctx.value
