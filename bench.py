@@ -63,6 +63,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--ring-slots", type=int, default=0)
+    ap.add_argument("--attn-splits", type=int, default=0, help="context splits per KV head (0: library default)")
     ap.add_argument("--l2-prefetch-tiles", type=int, default=0, help="0: library default, -1: off")
     ap.add_argument("--prefill-chunk", type=int, default=0,
                     help="tokens per tensor-core prefill chunk (0: library default; -1: decode steps)")
@@ -542,6 +543,7 @@ def run_ours(args, wl, rank, world, local_rank):
     P = wl.prompt_len
     stream = torch.cuda.Stream(device=dev)
     sched = amk.make_schedule_config(num_ctas=args.num_ctas, ring_slots=args.ring_slots,
+                                     attn_splits=args.attn_splits,
                                      l2_prefetch_tiles=args.l2_prefetch_tiles,
                                      prefill_chunk=args.prefill_chunk, prefill_parts=args.prefill_parts)
     num_ctas = args.num_ctas or torch.cuda.get_device_properties(dev).multi_processor_count
