@@ -16,12 +16,9 @@
 
 using namespace amk;
 
-// Default weight tiles in flight per SM: the whole weight ring, 128 KB of
-// 16 KB tiles (plain streaming on GB300 peaks at 96-128 KB per SM; more
-// slots measured no faster).
-constexpr int kDefaultRingSlots = kWeightSlots;
-constexpr int kLongContextRingSlots = kPoolSlots - 2 * kKvChunkStages;   // 4 weight, 8 KV slots
-constexpr int kLongContextRingSlotsInt4 = kLongContextRingSlots - 1;      // 3 weight, 9 KV slots
+// Default ring copies in flight per SM: eight 17 KB slots (plain streaming
+// on GB300 peaks at 96-128 KB in flight per SM).
+constexpr int kDefaultRingSlots = 8;
 
 // Default L2 prefetch budget during the attention chain (tiles of 16 KB).
 constexpr int kDefaultPrefetchTiles = 0;
@@ -44,7 +41,6 @@ struct amk_ctx {
   amk_status poisoned = AMK_OK;
   int32_t max_queue = 0;  // longest per-CTA task queue (trace sizing)
   int32_t n_lm = 0;       // LM-head tasks: argmax pairs per step
-  bool ring_auto = true;  // ring_slots chosen per step (schedule knob 0)
   uint32_t* amax[2] = {nullptr, nullptr};  // per-step argmax pairs, double buffered
   // tensor-core prefill (bf16 weights): chunk buffers and tensor maps
   struct Prefill {
@@ -411,20 +407,6 @@ StepParams make_params(const amk_ctx* ctx, const DevModel& dm, int32_t token, in
                        float* logits, int skip_lm, uint32_t tag_base) {
   StepParams p;
   p.m = dm;
-  if (ctx->ring_auto) {
-    // quantised consumers are bound by their own arithmetic, not by the
-    // weight bytes in flight, so when a context split holds more than one
-    // attention chunk of K,V stages the KV ring takes 8 of the 12 slots
-    // (8B int4 at 16K context: 339 -> 366 tok/s) and the next chunk loads
-    // while the current one is computed; int4, the slowest consumer, gives
-    // the KV ring a ninth (8B int4 at 16K: 401.4 -> 403.9 tok/s, three A/B
-    // pairs on one box)
-    const int pps = (kStageBytes / 2) / (2 * dm.head_dim);
-    const int per_split = (pos + dm.splits) / dm.splits;   // ceil((pos + 1) / splits)
-    const bool quantised = ctx->cfg.weight_format != AMK_FORMAT_BF16;
-    const int long_ctx = ctx->cfg.weight_format == AMK_FORMAT_INT4 ? kLongContextRingSlotsInt4 : kLongContextRingSlots;
-    p.m.ring_slots = quantised && per_split > kKvChunkStages * pps ? long_ctx : kDefaultRingSlots;
-  }
   p.logits = logits;
   p.token = token;
   p.pos = pos;
@@ -799,9 +781,8 @@ amk_status load_impl(const amk_config* cfg, const amk_weights* weights, void* wo
   dm.part_stride = g.part_stride;
   dm.num_ctas = g.num_ctas;
   dm.rms_eps = c.rms_eps;
-  dm.ring_slots = sched && sched->ring_slots > 0 ? std::min<int32_t>(sched->ring_slots, kWeightSlots)
+  dm.ring_slots = sched && sched->ring_slots > 0 ? std::min<int32_t>(sched->ring_slots, kRingSlots)
                                                  : kDefaultRingSlots;
-  ctx->ring_auto = !(sched && sched->ring_slots > 0);
   dm.prefetch_tiles = !sched || sched->l2_prefetch_tiles == 0 ? kDefaultPrefetchTiles
                       : sched->l2_prefetch_tiles < 0          ? 0
                                                               : std::min(sched->l2_prefetch_tiles, 1024);

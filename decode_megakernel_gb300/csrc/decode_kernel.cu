@@ -4,12 +4,11 @@
 // model of the AutoMegaKernel "Layer 0" VM (wait -> dispatch -> signal over
 // a local queue).  Two departures from the pages' design:
 //   * a CTA is split into a producer warp and eight consumer warps.  The
-//     producer streams the weight tiles of the CTA's whole queue through a
-//     shared-memory weight ring (8 x 16 KB tiles in flight, 1-D TMA bulk
-//     copies completing on mbarriers) and the K,V history of its attention
-//     tasks through a separate KV ring (2-D swizzled TMA boxes; four
-//     slots of its own plus the weight slots a smaller weight ring leaves
-//     unused).
+//     producer streams the weight tiles of the CTA's whole queue (1-D TMA
+//     bulk copies) and the K,V history of its attention tasks (2-D
+//     swizzled TMA boxes) through one shared-memory ring of twelve 17 KB
+//     slots, in queue order, with at most eight copies in flight; copies
+//     complete on mbarriers.
 //     Weights never depend on activations and the history never depends on
 //     the current step, so the producer runs ahead across the consumers'
 //     waits; this hides the per-tile cross-SM synchronisation cost the
@@ -176,26 +175,16 @@ __device__ __forceinline__ bool consumer_sync_or(bool pred) {
 // ------------------------------------------------------------ shared memory
 
 struct Smem {
-  uint8_t ring[kWeightSlots][kSlotBytes];   // weight ring [0, ring_slots); the rest lent to the KV ring
-  uint8_t kv[kKvChunkStages][kStageBytes];  // KV ring slots 0..3 (slot k >= 4: ring[ring_slots + k - 4])
+  uint8_t ring[kRingSlots][kSlotBytes];   // weight tiles and K,V stages, in queue order
   float scratch[kScratchFloats];
-  uint64_t full[kWeightSlots];
-  uint64_t empty[kWeightSlots];
-  uint64_t kfull[kMaxKvSlots];    // KV ring slots: kPoolSlots - ring_slots <= kMaxKvSlots
-  uint64_t kempty[kMaxKvSlots];
+  uint64_t full[kRingSlots];
+  uint64_t empty[kRingSlots];
   float misc[32];
   int32_t abort_flag;
   int32_t cur_task;   // queue index of the consumers' current task (read by the producer)
   int32_t token;      // the step's input token
 };
 static_assert(sizeof(Smem) <= kSmemBytes, "shared memory layout");
-
-// KV ring slot k: the dedicated stage buffers first, then the weight slots
-// the weight ring leaves unused (ring_slots = kWeightSlots + kKvChunkStages
-// - KV slots)
-__device__ __forceinline__ uint8_t* kv_slot(Smem& sm, int ring_slots, uint32_t k) {
-  return k < (uint32_t)kKvChunkStages ? sm.kv[k] : sm.ring[ring_slots + (int)k - kKvChunkStages];
-}
 
 // ------------------------------------------------------------- status
 
@@ -374,16 +363,14 @@ __device__ __forceinline__ TaskTiles task_tiles(const StepParams& p, const DevTa
   return tt;
 }
 
-// One cursor of the producer: walks the queue, issuing the tiles of the
-// tasks of its kind into its ring.
+// A cursor over the queue's ring tiles (the producer's copies, or the
+// L2 prefetches that run ahead of them).
 struct RingCursor {
   int task = 0, tile = 0;
   TaskTiles tt;
   bool valid = false;
   uint32_t slot = 0, phase = 0;
-  uint32_t issued = 0;   // slots that have held a copy
-  uint32_t parity = 0;   // parity of each slot's last issued phase
-  int64_t blocked = 0;   // trace: ns spent with a full ring
+  int64_t blocked = 0;   // trace: ns spent blocked
 };
 
 __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t ns) {
@@ -398,43 +385,41 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
   return ok != 0;
 }
 
-// Producer: one thread streams the tiles of the CTA's queue.  Weight tiles
-// of GEMV tasks go to the weight ring, K,V history tiles of attention
-// tasks to the KV ring, each through its own cursor over the queue: weights
-// never depend on activations and the history never depends on this step,
-// so both run ahead of the consumers, bounded only by their ring.  The KV
-// of the next attention task thus lands as soon as a KV slot frees up,
-// typically a layer ahead.
+// Producer: one thread streams the CTA's queue through the ring in the
+// order the consumers take it: the weight tiles of GEMV tasks and the K,V
+// history stages of attention tasks share the slots.  Neither depends on
+// this step's activations, so the producer runs up to a full ring ahead of
+// the consumers.  Copy k is issued once its slot is free and copy
+// k - ring_slots has landed: a TMA stream runs best with 96-128 KB in flight
+// per SM, and the rest of the ring keeps landed tiles for the consumers to
+// find when they come out of a hand-off (the attention -> merge -> O chain
+// consumes no weights for several microseconds).
 __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
   const uint64_t pol_w = policy_evict_first();
   const uint64_t pol_kv = policy_evict_normal();
   volatile int32_t* abort_flag = &sm.abort_flag;
-  const uint32_t wslots = (uint32_t)m.ring_slots;
-  const uint32_t kvslots = (uint32_t)kPoolSlots - wslots;
-  RingCursor w, a;
+  const uint32_t cap = (uint32_t)m.ring_slots;
+  RingCursor c;
+  uint32_t seq = 0;                          // copies issued
+  uint32_t issued = 0, parity = 0;           // slots that held a copy, parity of each one's last
   bool ok = true;
   uint64_t wait_t0 = 0;
-  // L2 prefetch of weight tiles beyond the full weight ring while the
-  // consumers are in the attention -> merge -> O chain, where they consume
-  // no weights for several microseconds: HBM keeps streaming, and the ring
-  // later refills from L2.  pf walks the weight tiles ahead of w.
+  // L2 prefetch of weight tiles beyond the ring while the consumers are in
+  // the attention -> merge -> O chain: pf walks the weight tiles ahead of
+  // the copy cursor (off by default).
   RingCursor pf;
   int64_t w_seq = 0, pf_seq = 0;   // weight tiles copied / prefetched so far
   const int64_t pf_budget = m.prefetch_tiles;
   volatile int32_t* cur_task = &sm.cur_task;
 
-  // next step of cursor c over tasks of its kind: true if it issued a copy
-  // or moved on; *blocked when its ring is full
-  auto step = [&](RingCursor& c, bool kv, bool* blocked) -> bool {
-    *blocked = false;
-    if (c.task >= n) return false;
+  while (ok && c.task < n) {
+    if (*abort_flag) { ok = false; break; }
     if (!c.valid) {
       const DevTask& t = q[c.task];
-      const bool mine = kv ? t.type == T_ATTN : (t.type != T_ATTN && t.type != T_COMBINE);
-      if (!mine) {
+      if (t.type == T_COMBINE) {   // no ring tiles
         ++c.task;
-        return true;
+        continue;
       }
       c.tt = task_tiles(p, t);
       c.tile = 0;
@@ -450,58 +435,60 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
       }
       ++c.task;
       c.valid = false;
-      return true;
+      continue;
     }
-    uint64_t* empty = kv ? &sm.kempty[c.slot] : &sm.empty[c.slot];
-    if (!mbar_test_wait(empty, c.phase ^ 1u)) {
-      *blocked = true;
-      return false;
-    }
-    uint64_t* full = kv ? &sm.kfull[c.slot] : &sm.full[c.slot];
-    if (kv) {
-      // K then V of positions [p0, p0 + pps): boxes of 64 dims x pps rows,
-      // 128-byte swizzled (rows past the split are loaded too and masked)
-      const int p0 = c.tt.t0 + c.tile * c.tt.pps;
-      const int nbox = m.head_dim / 64;
-      mbar_arrive_expect_tx(full, kStageBytes);
-      for (int b = 0; b < nbox; ++b) {
-        uint8_t* dst = kv_slot(sm, (int)wslots, c.slot);
-        tma_load_2d(dst + b * c.tt.pps * 128, &m.kv_map, 64 * b, c.tt.rk + p0, full, pol_kv);
-        tma_load_2d(dst + kStageBytes / 2 + b * c.tt.pps * 128, &m.kv_map, 64 * b,
-                    c.tt.rv + p0, full, pol_kv);
+    // what blocks copy seq: its slot still held, or copy seq - cap in flight
+    uint64_t* bar = nullptr;
+    uint32_t bpar = 0;
+    if (!mbar_test_wait(&sm.empty[c.slot], c.phase ^ 1u)) {
+      bar = &sm.empty[c.slot];
+      bpar = c.phase ^ 1u;
+    } else if (seq >= cap) {
+      const uint32_t back = seq - cap;
+      const uint32_t s2 = back % (uint32_t)kRingSlots, ph2 = (back / (uint32_t)kRingSlots) & 1u;
+      if (!mbar_test_wait(&sm.full[s2], ph2)) {
+        bar = &sm.full[s2];
+        bpar = ph2;
       }
-    } else {
-      mbar_arrive_expect_tx(full, c.tt.bytes);
-      bulk_copy_g2s(sm.ring[c.slot], c.tt.k + (int64_t)c.tile * c.tt.stride, c.tt.bytes, full, pol_w);
-      ++w_seq;
     }
-    c.issued |= 1u << c.slot;
-    c.parity = (c.parity & ~(1u << c.slot)) | (c.phase << c.slot);
-    if (++c.slot == (kv ? kvslots : wslots)) {
-      c.slot = 0;
-      c.phase ^= 1u;
-    }
-    ++c.tile;
-    return true;
-  };
-
-  while (ok && (w.task < n || a.task < n)) {
-    if (*abort_flag) { ok = false; break; }
-    bool wb, ab;
-    const bool wp = step(w, false, &wb);
-    const bool ap = step(a, true, &ab);
-    if (wp || ap) {
+    if (!bar) {
+      uint64_t* full = &sm.full[c.slot];
+      uint8_t* dst = sm.ring[c.slot];
+      if (c.tt.attn) {
+        // K then V of positions [p0, p0 + pps): boxes of 64 dims x pps rows,
+        // 128-byte swizzled (rows past the split are loaded too and masked)
+        const int p0 = c.tt.t0 + c.tile * c.tt.pps;
+        const int nbox = m.head_dim / 64;
+        mbar_arrive_expect_tx(full, kStageBytes);
+        for (int b = 0; b < nbox; ++b) {
+          tma_load_2d(dst + b * c.tt.pps * 128, &m.kv_map, 64 * b, c.tt.rk + p0, full, pol_kv);
+          tma_load_2d(dst + kStageBytes / 2 + b * c.tt.pps * 128, &m.kv_map, 64 * b, c.tt.rv + p0, full,
+                      pol_kv);
+        }
+      } else {
+        mbar_arrive_expect_tx(full, c.tt.bytes);
+        bulk_copy_g2s(dst, c.tt.k + (int64_t)c.tile * c.tt.stride, c.tt.bytes, full, pol_w);
+        ++w_seq;
+      }
+      issued |= 1u << c.slot;
+      parity = (parity & ~(1u << c.slot)) | (c.phase << c.slot);
+      if (++c.slot == (uint32_t)kRingSlots) {
+        c.slot = 0;
+        c.phase ^= 1u;
+      }
+      ++c.tile;
+      ++seq;
       wait_t0 = 0;
       continue;
     }
-    // both cursors wait for a consumer to release a slot (or are done).
-    // In the attention chain, prefetch the next weight tile into L2 instead.
-    if (wb && pf_budget > 0) {
+    // blocked.  In the attention chain, prefetch the next weight tiles into
+    // L2 instead (when enabled).
+    if (pf_budget > 0) {
       const int ct = *cur_task;
       const int cty = ct < n ? q[ct].type : T_LMHEAD;
       if (cty == T_ATTN || cty == T_COMBINE || cty == T_OPROJ) {
         if (pf_seq < w_seq) {   // the copies caught up: restart from the copy cursor
-          pf = w;
+          pf = c;
           pf_seq = w_seq;
         }
         bool issued_pf = false;
@@ -516,7 +503,7 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
             pf.tile = 0;
             pf.valid = true;
           }
-          if (pf.tile == pf.tt.nst) {
+          if (pf.tile == pf.tt.nst || pf.tt.attn) {
             ++pf.task;
             pf.valid = false;
             continue;
@@ -532,43 +519,34 @@ __device__ void producer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
         }
       }
     }
-    // sleep briefly on the weight ring, then look at both again
+    // sleep briefly on what blocks, then look again
     const uint64_t now = global_timer();
     if (!wait_t0) {
       wait_t0 = now;
     } else if (now - wait_t0 > p.timeout_ns) {
-      set_status(m.status, ST_TIMEOUT, (uint32_t)min(w.task, a.task), SITE_EMPTY);
+      set_status(m.status, ST_TIMEOUT, (uint32_t)c.task, SITE_EMPTY);
       *abort_flag = 1;
       ok = false;
       break;
     }
-    if (wb) mbar_try_wait_hint(&sm.empty[w.slot], w.phase ^ 1u, 200);
-    else if (ab) mbar_try_wait_hint(&sm.kempty[a.slot], a.phase ^ 1u, 200);
-    if (p.trace) {
-      const int64_t dt = (int64_t)(global_timer() - now);
-      if (wb) w.blocked += dt;
-      if (ab) a.blocked += dt;
-    }
+    mbar_try_wait_hint(bar, bpar, 200);
+    if (p.trace) c.blocked += (int64_t)(global_timer() - now);
   }
   // Every copy this CTA issued must land before its shared memory goes away.
   // Consumers normally wait for all of them already; when they stop early
   // (a failed wait anywhere) this is what keeps the CTA from exiting with
   // a copy in flight.
-  auto drain = [&](const RingCursor& c, uint64_t* full, int slots) {
-    for (int s2 = 0; s2 < slots; ++s2) {
-      if (!(c.issued & (1u << s2))) continue;
-      const uint32_t par = (c.parity >> s2) & 1u;
-      const uint64_t t0 = global_timer();
-      while (!mbar_try_wait(&full[s2], par)) {
-        if (global_timer() - t0 > p.timeout_ns) {
-          set_status(m.status, ST_TIMEOUT, 0xFFFFFFFFu, SITE_DRAIN);
-          break;
-        }
+  for (int s2 = 0; s2 < kRingSlots; ++s2) {
+    if (!(issued & (1u << s2))) continue;
+    const uint32_t par = (parity >> s2) & 1u;
+    const uint64_t t0 = global_timer();
+    while (!mbar_try_wait(&sm.full[s2], par)) {
+      if (global_timer() - t0 > p.timeout_ns) {
+        set_status(m.status, ST_TIMEOUT, 0xFFFFFFFFu, SITE_DRAIN);
+        break;
       }
     }
-  };
-  drain(w, sm.full, (int)wslots);
-  drain(a, sm.kfull, (int)kvslots);
+  }
 }
 
 // -------------------------------------------------------------- consumers
@@ -1061,7 +1039,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   const uint32_t empty0 = smem_addr(&sm.empty[0]);
   const uint32_t off0 = (uint32_t)(((rsub << cs) + chunk) * EB);   // pass 0 chunk
   const uint32_t pass_stride = (uint32_t)((rpp << cs) * EB);       // rows between passes
-  const uint32_t nslots = (uint32_t)m.ring_slots;
+  constexpr uint32_t nslots = (uint32_t)kRingSlots;
   uint32_t slot = (uint32_t)stage % nslots, phase = ((uint32_t)stage / nslots) & 1u;
   int64_t starved = 0;
 
@@ -1336,7 +1314,7 @@ __device__ __forceinline__ int gemv_dispatch(const StepParams& p, Smem& sm, cons
 
 // Split-K GQA attention of one KV head over one context split (positions
 // [t0, t1) of the cache, plus the step's own position for the last split),
-// on the tensor cores.  The K,V history arrives through the KV ring in
+// on the tensor cores.  The K,V history arrives through the ring in
 // 128-byte-swizzled boxes; a chunk of up to kKvChunkStages resident stages is
 // split into runs of 16 (hd 128) or 32 (hd 64) positions, one per warp.
 // Per 16 positions a warp computes
@@ -1349,7 +1327,7 @@ __device__ __forceinline__ int gemv_dispatch(const StepParams& p, Smem& sm, cons
 // running (m, l, O); the eight warp states are merged (LSE) through shared
 // memory and stored as the split's partial (acc, m, l).
 template <int HD, int G>
-__device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTask t, int kstage,
+__device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTask t, int stage,
                                       uint32_t task_idx, int64_t* tr) {
   constexpr int PPS = (kStageBytes / 2) / (HD * 2);   // cached positions per KV stage
   constexpr int CP = kKvChunkStages * PPS;            // positions per chunk at most
@@ -1428,17 +1406,17 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[k2][e] = 0.f;
 
-  const uint32_t kvs = (uint32_t)(kPoolSlots - m.ring_slots);   // KV ring slots (>= kKvChunkStages)
+  constexpr uint32_t kvs = (uint32_t)kRingSlots;   // the ring's slots (>= kKvChunkStages)
   const uint32_t cur0 = smem_addr(cur);
-  const uint32_t kfull0 = smem_addr(&sm.kfull[0]);
-  const uint32_t kempty0 = smem_addr(&sm.kempty[0]);
+  const uint32_t kfull0 = smem_addr(&sm.full[0]);
+  const uint32_t kempty0 = smem_addr(&sm.empty[0]);
   int64_t starved = 0;
   int t0, t1;
   attn_range(p.pos, m.splits, j, &t0, &t1);
   const int ncached = t1 - t0;
   const int ntotal = ncached + (last ? 1 : 0);
   const int nst = (ncached + PPS - 1) / PPS;
-  uint32_t kslot = (uint32_t)kstage % kvs, kphase = ((uint32_t)kstage / kvs) & 1u;
+  uint32_t kslot = (uint32_t)stage % kvs, kphase = ((uint32_t)stage / kvs) & 1u;
 
   for (int c0 = 0; c0 < ntotal; c0 += CP) {
     const int len = min(CP, ntotal - c0);
@@ -1469,7 +1447,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
     auto slot_base = [&](int st) -> uint32_t {
       uint32_t slot = slot0 + (uint32_t)(st - s_begin);
       if (slot >= kvs) slot -= kvs;
-      return smem_addr(kv_slot(sm, m.ring_slots, slot));
+      return smem_addr(&sm.ring[slot][0]);
     };
     const uint32_t baseA = slot_base(stA), baseB = slot_base(stA + 1);
     auto addr_of = [&](int pi, int c, int kv) -> uint32_t {
@@ -1651,7 +1629,7 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
   for (int idx = G * HD + 2 * G + tid; idx < m.part_stride; idx += kConsumerThreads)
     st_relaxed(part + idx, tag_word(0.f, tag));
   if (tr) tr[TR_A_MERGED] = (int64_t)global_timer();
-  return kstage + nst;
+  return stage + nst;
 }
 
 // LSE merge of one query head's S attention splits into o (AMK's split-K
@@ -1770,7 +1748,7 @@ template <int QKV_FMT, int LM_FMT>
 __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, int n) {
   const DevModel& m = p.m;
   const int tid = threadIdx.x;
-  int stage = 0, kstage = 0;   // weight-ring and KV-ring stages consumed so far
+  int stage = 0;   // ring tiles consumed so far
   volatile int32_t* abort_flag = &sm.abort_flag;
   for (int i = 0; i < n; ++i) {
     if (*abort_flag) return;
@@ -1783,13 +1761,13 @@ __device__ void consumer_loop(const StepParams& p, Smem& sm, const DevTask* q, i
     }
     int64_t* tr0 = tid == 0 ? tr : nullptr;
     if (t.type == T_ATTN)
-      kstage = m.head_dim == 128 ? attn_dispatch<128>(p, sm, t, kstage, (uint32_t)i, tr0)
-                                 : attn_dispatch<64>(p, sm, t, kstage, (uint32_t)i, tr0);
+      stage = m.head_dim == 128 ? attn_dispatch<128>(p, sm, t, stage, (uint32_t)i, tr0)
+                                : attn_dispatch<64>(p, sm, t, stage, (uint32_t)i, tr0);
     else if (t.type == T_COMBINE)
       stage = combine_task(p, sm, t, stage, (uint32_t)i, tr0);
     else if (t.type == T_LMHEAD) stage = gemv_dispatch<LM_FMT>(p, sm, t, stage, (uint32_t)i, tr0);
     else stage = gemv_dispatch<QKV_FMT>(p, sm, t, stage, (uint32_t)i, tr0);
-    if (stage < 0 || kstage < 0) {
+    if (stage < 0) {
       *abort_flag = 1;
       return;
     }
@@ -1805,20 +1783,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x;
   if (tid == 0) {
-    for (int s = 0; s < kWeightSlots; ++s) {
+    for (int s = 0; s < kRingSlots; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kConsumerWarps);
     }
-    for (int s = 0; s < kMaxKvSlots; ++s) {
-      mbar_init(&sm.kfull[s], 1);
-      mbar_init(&sm.kempty[s], kConsumerWarps);
-    }
-    // the swizzled KV boxes need 1 KB alignment (slots are 16 or 17 KB apart):
+    // the swizzled KV boxes need 1 KB alignment (slots are 17 KB apart):
     // refuse to run without it
     static_assert(kSlotBytes % 1024 == 0 && kStageBytes % 1024 == 0, "KV slot alignment");
-    sm.abort_flag = ((smem_addr(&sm.ring[0][0]) | smem_addr(&sm.kv[0][0])) & 1023u) ? 1 : 0;
-    // the weight / KV split must leave the KV ring within its slots and barriers
-    if (p.m.ring_slots < 1 || p.m.ring_slots > kWeightSlots) sm.abort_flag = 1;
+    sm.abort_flag = (smem_addr(&sm.ring[0][0]) & 1023u) ? 1 : 0;
+    // the in-flight cap must lie within the ring
+    if (p.m.ring_slots < 1 || p.m.ring_slots > kRingSlots) sm.abort_flag = 1;
     if (sm.abort_flag) set_status(p.m.status, ST_CHECK, 0xFFFFFFFFu, SITE_SMEM);
     sm.cur_task = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

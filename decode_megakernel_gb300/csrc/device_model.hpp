@@ -39,7 +39,7 @@ struct DevModel {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab, max_seq;
   int32_t group, splits, part_stride, num_ctas;
   float rms_eps;
-  int32_t ring_slots;          // weight-ring slots (1 <= ring_slots <= kWeightSlots); KV ring: the rest of the pool
+  int32_t ring_slots;          // ring copies in flight at most (1 <= ring_slots <= kRingSlots)
   int32_t prefetch_tiles;      // weight tiles the producer may prefetch into L2 beyond its full
                                // ring while the consumers are in attention / merge / O tasks
   int32_t pad0;
@@ -114,24 +114,19 @@ enum WaitSite : uint32_t {
 // kernel geometry
 constexpr int kConsumerWarps = kConsumerThreads / 32;  // 8
 constexpr int kThreads = kConsumerThreads + 32;        // + one producer warp
-// The weight ring (tiles of GEMV tasks, slots [0, ring_slots) of the eight
-// 17 KB weight slots) and the KV ring (K,V history stages of attention
-// tasks: four dedicated 16 KB slots plus the weight slots the weight ring
-// leaves unused) are separate, so that the KV of the next attention task is
-// loaded as soon as a KV slot frees up, never behind weight tiles.  The
-// split is a per-launch choice: long contexts give the KV ring more slots.
-constexpr int kWeightSlots = 8;                        // weight slots (the default ring: 136 KB in flight)
+// One ring per CTA carries the weight tiles of its GEMV tasks and the K,V
+// history stages of its attention tasks, in the order its consumers take
+// them.  Copies in flight are capped per launch (ring_slots); the other
+// slots hold landed tiles while the consumers wait at a hand-off.
+constexpr int kRingSlots = 12;                         // 17 KB slots
 constexpr int kKvChunkStages = 4;                      // KV stages an attention chunk holds at once
-constexpr int kPoolSlots = kWeightSlots + kKvChunkStages;   // weight + KV slots of a CTA
-constexpr int kMaxKvSlots = kPoolSlots - 1;            // KV slots when the weight ring keeps one
-constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one weight slot
+constexpr int kSlotBytes = kStageBytes + kSideBytes;   // one slot: a weight tile and its side data
 constexpr int kScratchFloats = 4608;                   // GEMV row partials / attention merge
 // int8 / int4 GEMV tasks stage each warp's activations (256 floats) above the row
 // partials, which take at most kRowsMax rows x 8 warps
 constexpr int kActStageOffset = kRowsMax * kConsumerWarps;
 static_assert(kActStageOffset + kConsumerWarps * 256 <= kScratchFloats, "activation staging");
-constexpr int kSmemBytes = kWeightSlots * kSlotBytes + kKvChunkStages * kStageBytes + kScratchFloats * 4 +
-                           2 * (kWeightSlots + kMaxKvSlots) * 8 + 256;
+constexpr int kSmemBytes = kRingSlots * kSlotBytes + kScratchFloats * 4 + 2 * kRingSlots * 8 + 256;
 
 // Byte offsets of the per-step scratch regions (tagged x_res, x_mid, qkv,
 // o, a, attention partials, then the status words) laid out from one base

@@ -104,13 +104,12 @@ typedef struct {
     int32_t attn_splits;        /* context splits per KV head (default: num_ctas / n_kv_heads) */
     int32_t max_rows_per_task;  /* rows of one GEMV task (default and maximum 256) */
     int32_t watchdog_ms;        /* device wait limit before AMK_ERR_TIMEOUT (default 2000) */
-    int32_t ring_slots;         /* slots of the per-CTA weight ring, 1..8; the K,V history of
-                                   attention streams through the other 12 - ring_slots slots
-                                   of the CTA's shared-memory pool.  0 (default): chosen per
-                                   step, 8 (128 KB of 16 KB weight tiles in flight), or 4
-                                   (int8) / 3 (int4) when the weights are quantised and a
-                                   context split holds more than one attention chunk (4 KV
-                                   stages) */
+    int32_t ring_slots;         /* copies in flight per CTA, 1..12.  Each CTA streams the
+                                   weight tiles of its GEMV tasks and the K,V history stages
+                                   of its attention tasks, in queue order, through one ring
+                                   of 12 shared-memory slots of 17 KB; a copy is issued once
+                                   its slot is free and the copy ring_slots before it has
+                                   landed.  0 (default): 8 */
     int32_t l2_prefetch_tiles;  /* weight tiles a CTA may prefetch into L2 beyond its full
                                    ring while its consumers run attention, the split merge
                                    or the O projection (-1: off; 0: default) */

@@ -139,10 +139,9 @@ def test_schedule_knobs(amk, orc, dev, knobs):
 @pytest.mark.parametrize("ring_slots", [0, 1, 4, 8])
 def test_ring_split_long_context(amk, orc, dev, fmt, ring_slots):
     # one context split per KV head holding 600 positions: three attention
-    # chunks of 256 (head_dim 64), streamed through 4 KV slots (ring_slots
-    # 8), 8 (4) or 11 (1); 0 lets the library choose per step (int4 with
-    # more than one chunk per split: 8 KV slots, some lent from the weight
-    # ring)
+    # chunks of 256 (head_dim 64) between the weight tiles in the CTA's
+    # ring, with 1, 4 or 8 copies in flight (0: the default, 8); the chunk
+    # loop wraps around the ring's 12 slots
     base = dict(wc.TINY.__dict__)
     if fmt == "int4":
         base.update(weight_format="int4", ffn=768)
