@@ -16,9 +16,12 @@
 
 using namespace amk;
 
-// Default ring copies in flight per SM: eight 17 KB slots (plain streaming
-// on GB300 peaks at 96-128 KB in flight per SM).
-constexpr int kDefaultRingSlots = 8;
+// Default ring copies in flight per SM: six 17 KB tiles, 102 KB (plain
+// streaming on GB300 peaks at 96-128 KB in flight per SM; 8B bf16 decode
+// at 3 / 4 / 5 / 6 / 7 / 8 / 10 / 12 copies: 358.8 / 379.2 / 385.5 / 386.1 /
+// 385.7 / 383.8 / 382.1 / 380.6 tok/s, the quantised and 1B workloads
+// within 0.3 % from 4 to 12)
+constexpr int kDefaultRingSlots = 6;
 
 // Default L2 prefetch budget during the attention chain (tiles of 16 KB).
 constexpr int kDefaultPrefetchTiles = 0;

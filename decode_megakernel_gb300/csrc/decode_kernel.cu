@@ -7,8 +7,8 @@
 //     producer streams the weight tiles of the CTA's whole queue (1-D TMA
 //     bulk copies) and the K,V history of its attention tasks (2-D
 //     swizzled TMA boxes) through one shared-memory ring of twelve 17 KB
-//     slots, in queue order, with at most eight copies in flight; copies
-//     complete on mbarriers.
+//     slots, in queue order, with at most six copies in flight (a launch
+//     parameter); copies complete on mbarriers.
 //     Weights never depend on activations and the history never depends on
 //     the current step, so the producer runs ahead across the consumers'
 //     waits; this hides the per-tile cross-SM synchronisation cost the

@@ -140,7 +140,7 @@ def test_schedule_knobs(amk, orc, dev, knobs):
 def test_ring_split_long_context(amk, orc, dev, fmt, ring_slots):
     # one context split per KV head holding 600 positions: three attention
     # chunks of 256 (head_dim 64) between the weight tiles in the CTA's
-    # ring, with 1, 4 or 8 copies in flight (0: the default, 8); the chunk
+    # ring, with 1, 4 or 8 copies in flight (0: the default, 6); the chunk
     # loop wraps around the ring's 12 slots
     base = dict(wc.TINY.__dict__)
     if fmt == "int4":
