@@ -1061,27 +1061,41 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
         for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int e = 0; e < 4; ++e) d[a][c][e] = 0.f;
-      constexpr bool kRoll = false;      // int8 tile code is short: unrolled (rotation measured slower)
-#pragma unroll(kRoll ? 1 : NKT)
-      for (int kt = 0; kt < NKT; ++kt) {
-        const int fk = kRoll ? 0 : kt;   // fragment index of this tile
+      // tiles in pairs: both waits first, then both tiles' loads and mma
+      // (each accumulator still sums its k blocks in tile order)
+#pragma unroll
+      for (int kt = 0; kt < NKT; kt += 2) {
+        const bool two = kt + 1 < NKT;
+        const uint32_t slot2 = slot + 1 == nslots ? 0u : slot + 1;
+        const uint32_t phase2 = slot + 1 == nslots ? phase ^ 1u : phase;
         if (!failed)
           failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
+        if (two && !failed)
+          failed = !wait_full(full0 + slot2 * 8, phase2, p, abort_flag, task_idx, tr ? &starved : nullptr);
         if (!failed) {
-          const uint32_t tile = ring0 + slot * kSlotBytes + unit0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 v = lds128(tile + (uint32_t)j * 512u);
-            mma_f16_16816(d[0][j & 1], i8x2_lo(v.x), i8x2_hi(v.x), i8x2_lo(v.y), i8x2_hi(v.y), bq[fk][j][0],
-                          bq[fk][j][1]);
-            mma_f16_16816(d[1][j & 1], i8x2_lo(v.z), i8x2_hi(v.z), i8x2_lo(v.w), i8x2_hi(v.w), bq[fk][j][0],
-                          bq[fk][j][1]);
+          for (int u = 0; u < 2; ++u) {
+            if (u == 1 && !two) break;
+            const int fk = u == 0 ? kt : (two ? kt + 1 : kt);
+            const uint32_t tile = ring0 + (u == 0 ? slot : slot2) * kSlotBytes + unit0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 v = lds128(tile + (uint32_t)j * 512u);
+              mma_f16_16816(d[0][j & 1], i8x2_lo(v.x), i8x2_hi(v.x), i8x2_lo(v.y), i8x2_hi(v.y), bq[fk][j][0],
+                            bq[fk][j][1]);
+              mma_f16_16816(d[1][j & 1], i8x2_lo(v.z), i8x2_hi(v.z), i8x2_lo(v.w), i8x2_hi(v.w), bq[fk][j][0],
+                            bq[fk][j][1]);
+            }
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive32(empty0 + slot * 8);
-        if (++slot == nslots) { slot = 0; phase ^= 1u; }
-        if constexpr (kRoll) rotate_fragments<NKT>(bq);
+        if (lane == 0) {
+          mbar_arrive32(empty0 + slot * 8);
+          if (two) mbar_arrive32(empty0 + slot2 * 8);
+        }
+        slot = slot2;
+        phase = phase2;
+        if (two && ++slot == nslots) { slot = 0; phase ^= 1u; }
       }
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
@@ -1119,50 +1133,79 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
       float acc[4][2];   // [q][R, R + 2], scaled by the group scales
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0.f;
-      constexpr bool kRoll = NKT >= 4;   // rolled loop over rotated fragments (measured faster for int4)
-#pragma unroll(kRoll ? 1 : NKT)
-      for (int kt = 0; kt < NKT; ++kt) {
-        const int fk = kRoll ? 0 : kt;   // fragment index of this tile
-        if (!failed)
-          failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
-        if (!failed) {
-          const uint32_t tile = ring0 + slot * kSlotBytes;
-          const uint32_t side = tile + kStageBytes;
-          uint4 v[4];
+      // one 16-row tile against fragment set fk: the lane's 4 code words
+      // per k block, its rows' scales and zero points from the side data
+      auto tile_mma = [&](uint32_t tile, int fk) {
+        const uint32_t side = tile + kStageBytes;
+        uint4 v[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = lds128(tile + unit0 + (uint32_t)j * 512u);
-          // the scales and zero points of the lane's 8 rows (R = 4q + rl and
-          // R + 2 for q = 0..3: the rows of parity rl) in its group: 16 + 8
-          // contiguous bytes of the side data (pack_kernel)
-          const uint4 sc = lds128(side + (uint32_t)(gq * 2 + rl) * 16u);
-          const uint2 zz = lds64(side + 512u + (uint32_t)(gq * 2 + rl) * 8u);
+        for (int j = 0; j < 4; ++j) v[j] = lds128(tile + unit0 + (uint32_t)j * 512u);
+        // the scales and zero points of the lane's 8 rows (R = 4q + rl and
+        // R + 2 for q = 0..3: the rows of parity rl) in its group: 16 + 8
+        // contiguous bytes of the side data (pack_kernel)
+        const uint4 sc = lds128(side + (uint32_t)(gq * 2 + rl) * 16u);
+        const uint2 zz = lds64(side + 512u + (uint32_t)(gq * 2 + rl) * 8u);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            // row R: entry 2q, row R + 2: entry 2q + 1
-            const uint32_t zw = q < 2 ? zz.x : zz.y;
-            const uint32_t zc0 = __byte_perm(zw, 0x64u, (q & 1) ? 0x4242u : 0x4040u);
-            const uint32_t zc1 = __byte_perm(zw, 0x64u, (q & 1) ? 0x4343u : 0x4141u);
-            const uint32_t sw = q == 0 ? sc.x : q == 1 ? sc.y : q == 2 ? sc.z : sc.w;
-            const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sw));
-            const uint32_t zf0 = u4_zf(zc0), zf1 = u4_zf(zc1);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int q = 0; q < 4; ++q) {
+          // row R: entry 2q, row R + 2: entry 2q + 1
+          const uint32_t zw = q < 2 ? zz.x : zz.y;
+          const uint32_t zc0 = __byte_perm(zw, 0x64u, (q & 1) ? 0x4242u : 0x4040u);
+          const uint32_t zc1 = __byte_perm(zw, 0x64u, (q & 1) ? 0x4343u : 0x4141u);
+          const uint32_t sw = q == 0 ? sc.x : q == 1 ? sc.y : q == 2 ? sc.z : sc.w;
+          const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sw));
+          const uint32_t zf0 = u4_zf(zc0), zf1 = u4_zf(zc1);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t w = q == 0 ? v[j].x : q == 1 ? v[j].y : q == 2 ? v[j].z : v[j].w;
-              uint32_t a[4];
-              u4_fragment(w, zc0, zf0, zc1, zf1, a);
-              mma_f16_16816(d, a[0], a[1], a[2], a[3], bq[fk][j][0], bq[fk][j][1]);
-            }
-            const float e0 = keep ? (odd ? d[1] : d[0]) : 0.f;
-            const float e2 = keep ? (odd ? d[3] : d[2]) : 0.f;
-            acc[q][0] = fmaf(s01.x, e0, acc[q][0]);
-            acc[q][1] = fmaf(s01.y, e2, acc[q][1]);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t w = q == 0 ? v[j].x : q == 1 ? v[j].y : q == 2 ? v[j].z : v[j].w;
+            uint32_t a[4];
+            u4_fragment(w, zc0, zf0, zc1, zf1, a);
+            mma_f16_16816(d, a[0], a[1], a[2], a[3], bq[fk][j][0], bq[fk][j][1]);
           }
+          const float e0 = keep ? (odd ? d[1] : d[0]) : 0.f;
+          const float e2 = keep ? (odd ? d[3] : d[2]) : 0.f;
+          acc[q][0] = fmaf(s01.x, e0, acc[q][0]);
+          acc[q][1] = fmaf(s01.y, e2, acc[q][1]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive32(empty0 + slot * 8);
-        if (++slot == nslots) { slot = 0; phase ^= 1u; }
-        if constexpr (kRoll) rotate_fragments<NKT>(bq);
+      };
+      if constexpr (NKT >= 4) {
+        // long rows: one rolled tile loop over rotated fragments (measured
+        // faster for int4 than NKT unrolled copies)
+#pragma unroll 1
+        for (int kt = 0; kt < NKT; ++kt) {
+          if (!failed)
+            failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
+          if (!failed) tile_mma(ring0 + slot * kSlotBytes, 0);
+          __syncwarp();
+          if (lane == 0) mbar_arrive32(empty0 + slot * 8);
+          if (++slot == nslots) { slot = 0; phase ^= 1u; }
+          rotate_fragments<NKT>(bq);
+        }
+      } else {
+        // short rows: tiles in pairs, both waits first (each accumulator
+        // still sums the tiles in order)
+#pragma unroll
+        for (int kt = 0; kt < NKT; kt += 2) {
+          const bool two = kt + 1 < NKT;
+          const uint32_t slot2 = slot + 1 == nslots ? 0u : slot + 1;
+          const uint32_t phase2 = slot + 1 == nslots ? phase ^ 1u : phase;
+          if (!failed)
+            failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
+          if (two && !failed)
+            failed = !wait_full(full0 + slot2 * 8, phase2, p, abort_flag, task_idx, tr ? &starved : nullptr);
+          if (!failed) {
+            tile_mma(ring0 + slot * kSlotBytes, kt);
+            if (two) tile_mma(ring0 + slot2 * kSlotBytes, two ? kt + 1 : kt);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive32(empty0 + slot * 8);
+            if (two) mbar_arrive32(empty0 + slot2 * 8);
+          }
+          slot = slot2;
+          phase = phase2;
+          if (two && ++slot == nslots) { slot = 0; phase ^= 1u; }
+        }
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -1184,18 +1227,37 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
     float2 acc2[P];
 #pragma unroll
     for (int i = 0; i < P; ++i) acc2[i] = make_float2(0.f, 0.f);
+    // tiles in pairs: both waits first, so that the second tile's shared
+    // loads issue with the first tile's FMAs in flight (the sums keep their
+    // order: tile kt, then kt + 1)
 #pragma unroll
-    for (int kt = 0; kt < NKT; ++kt) {
+    for (int kt = 0; kt < NKT; kt += 2) {
+      const bool two = kt + 1 < NKT;
+      const uint32_t slot2 = slot + 1 == nslots ? 0u : slot + 1;
+      const uint32_t phase2 = slot + 1 == nslots ? phase ^ 1u : phase;
       if (!failed)
         failed = !wait_full(full0 + slot * 8, phase, p, abort_flag, task_idx, tr ? &starved : nullptr);
+      if (two && !failed)
+        failed = !wait_full(full0 + slot2 * 8, phase2, p, abort_flag, task_idx, tr ? &starved : nullptr);
       if (!failed) {
         const uint32_t tile = ring0 + slot * kSlotBytes;
 #pragma unroll
         for (int ps = 0; ps < P; ++ps) acc2[ps] = chunk_dot<FMT>(tile + off0 + ps * pass_stride, h[kt], acc2[ps]);
+        if (two) {
+          const uint32_t tile2 = ring0 + slot2 * kSlotBytes;
+#pragma unroll
+          for (int ps = 0; ps < P; ++ps)
+            acc2[ps] = chunk_dot<FMT>(tile2 + off0 + ps * pass_stride, h[two ? kt + 1 : kt], acc2[ps]);
+        }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive32(empty0 + slot * 8);
-      if (++slot == nslots) { slot = 0; phase ^= 1u; }
+      if (lane == 0) {
+        mbar_arrive32(empty0 + slot * 8);
+        if (two) mbar_arrive32(empty0 + slot2 * 8);
+      }
+      slot = slot2;
+      phase = phase2;
+      if (two && ++slot == nslots) { slot = 0; phase ^= 1u; }
     }
     float v[P];
 #pragma unroll
@@ -1214,13 +1276,23 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
   // epilogue: one row (or one row pair) per thread; tagged stores of version layer + 1
   const uint32_t tag = tag_of(p, t.layer + 1);
   const int nwg = 1 << wpg_shift;
-  auto row_sum = [&](int r) {
+  auto row_sum = [&](int r) {   // the first nwg of the row's 8 partials, in warp order
+    const float4 a = *reinterpret_cast<const float4*>(red + r * 8);
+    const float4 b = *reinterpret_cast<const float4*>(red + r * 8 + 4);
     float y = 0.f;
-    for (int w = 0; w < nwg; ++w) y += red[r * 8 + w];
+    y += a.x;
+    y += nwg > 1 ? a.y : 0.f;
+    y += nwg > 2 ? a.z : 0.f;
+    y += nwg > 2 ? a.w : 0.f;
+    y += nwg > 4 ? b.x : 0.f;
+    y += nwg > 4 ? b.y : 0.f;
+    y += nwg > 4 ? b.z : 0.f;
+    y += nwg > 4 ? b.w : 0.f;
     return y;
   };
   if (t.type == T_QKV || t.type == T_GATEUP) {
     const int hd = m.head_dim, half = hd >> 1, G = m.group, gw = (G + 2) * hd;
+    const int hd_shift = hd == 128 ? 7 : 6;   // head_dim is 64 or 128
     for (int pr = tid; pr < nrows / 2; pr += kConsumerThreads) {
       const int R = row0 + 2 * pr;
       if (R >= M.rows) continue;
@@ -1235,7 +1307,7 @@ __device__ __noinline__ int gemv_task(const StepParams& p, Smem& sm, const DevTa
         continue;
       }
       // packed QKV rows per KV head: G query heads, k, v (RoPE pairs adjacent)
-      const int grp = R / gw, r = R % gw, slot_h = r / hd, within = r % hd;
+      const int grp = R / gw, r = R - grp * gw, slot_h = r >> hd_shift, within = r & (hd - 1);
       uint32_t* dst = m.qkv + (int64_t)grp * gw + slot_h * hd;
       if (slot_h <= G) {
         // rotate-half RoPE pair (i, i + hd/2) at position pos
