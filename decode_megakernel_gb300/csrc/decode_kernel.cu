@@ -179,7 +179,7 @@ struct Smem {
   float scratch[kScratchFloats];
   uint64_t full[kRingSlots];
   uint64_t empty[kRingSlots];
-  float misc[32];
+  alignas(16) float misc[32];
   int32_t abort_flag;
   int32_t cur_task;   // queue index of the consumers' current task (read by the producer)
   int32_t token;      // the step's input token
@@ -842,8 +842,13 @@ __device__ __forceinline__ bool load_activation(const StepParams& p, Smem& sm, c
   ss = warp_sum(tid < cpr ? ss : 0.f);
   if ((tid & 31) == 0) sm.misc[tid >> 5] = ss;
   consumer_sync();
+  // the eight warp sums in warp order (warps past cpr / 32 hold exact zeros)
+  static_assert(kConsumerWarps == 8, "eight warp sums");
+  const float4 m0 = *reinterpret_cast<const float4*>(sm.misc);
+  const float4 m1 = *reinterpret_cast<const float4*>(sm.misc + 4);
   float tot = 0.f;
-  for (int w = 0; w < (cpr >> 5); ++w) tot += sm.misc[w];
+  tot += m0.x; tot += m0.y; tot += m0.z; tot += m0.w;
+  tot += m1.x; tot += m1.y; tot += m1.z; tot += m1.w;
   const float r = rsqrtf(tot / (float)m.hidden + m.rms_eps);
   const uint16_t* nw = t.type == T_QKV ? m.attn_norm + (int64_t)t.layer * m.hidden
                        : t.type == T_GATEUP ? m.ffn_norm + (int64_t)t.layer * m.hidden
@@ -1717,6 +1722,8 @@ __device__ __noinline__ int attn_task(const StepParams& p, Smem& sm, const DevTa
 __device__ __noinline__ int combine_task(const StepParams& p, Smem& sm, const DevTask t, int stage,
                                          uint32_t task_idx, int64_t* tr) {
   constexpr int SC = 4;                          // acc vectors polled at once per thread
+  constexpr int kMaxNH = kConsumerThreads / 16;  // subsets at head size 64
+  constexpr int kMaxCH = kMaxNH * SC;            // and splits per chunk
   static_assert((kConsumerThreads / 16) * SC <= kConsumerThreads, "one (m, l) vector per thread");
   static_assert((kConsumerThreads / 16) * SC * 2 + kConsumerThreads * 6 <= kScratchFloats,
                 "combine exceeds the scratch");
@@ -1757,8 +1764,16 @@ __device__ __noinline__ int combine_task(const StepParams& p, Smem& sm, const De
       mls[tid * 2 + 1] = tag_value((hh & 1) ? mv[0].w : mv[0].y);
     }
     if (consumer_sync_or(failed)) return -1;
+    // the chunk maximum (exact in any order): (m, l) pairs two at a time,
+    // the loop bound the largest chunk (head size 64)
     float Mc = -INFINITY;
-    for (int s = 0; s < nc; ++s) Mc = fmaxf(Mc, mls[s * 2]);
+#pragma unroll
+    for (int s = 0; s < kMaxCH; s += 2) {
+      if (s >= nc) break;
+      const float4 q = *reinterpret_cast<const float4*>(mls + s * 2);
+      Mc = fmaxf(Mc, q.x);
+      if (s + 1 < nc) Mc = fmaxf(Mc, q.z);
+    }
     const float Mn = fmaxf(M, Mc);
     const float a = exp2f(M - Mn);
     L *= a;
@@ -1784,9 +1799,15 @@ __device__ __noinline__ int combine_task(const StepParams& p, Smem& sm, const De
   consumer_sync();
   if (hf == 0) {
     float Mt = -INFINITY;
-    for (int k = 0; k < NH; ++k) Mt = fmaxf(Mt, sub[(k * NE + e) * 6]);
+#pragma unroll
+    for (int k = 0; k < kMaxNH; ++k) {
+      if (k >= NH) break;
+      Mt = fmaxf(Mt, sub[(k * NE + e) * 6]);
+    }
     float Lt = 0.f, At[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < NH; ++k) {
+#pragma unroll
+    for (int k = 0; k < kMaxNH; ++k) {
+      if (k >= NH) break;
       const float* o = sub + (k * NE + e) * 6;
       const float w = exp2f(o[0] - Mt);   // a subset without splits has M = -inf: weight 0
       Lt = fmaf(o[1], w, Lt);
