@@ -109,7 +109,7 @@ typedef struct {
                                    of its attention tasks, in queue order, through one ring
                                    of 12 shared-memory slots of 17 KB; a copy is issued once
                                    its slot is free and the copy ring_slots before it has
-                                   landed.  0 (default): 6 */
+                                   landed.  0 (default): 6; values above 12 act as 12 */
     int32_t l2_prefetch_tiles;  /* weight tiles a CTA may prefetch into L2 beyond its full
                                    ring while its consumers run attention, the split merge
                                    or the O projection (-1: off; 0: default) */
