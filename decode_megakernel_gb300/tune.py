@@ -52,7 +52,7 @@ def knob_candidates(sms: int, n_kv: int, rng: random.Random, trials: int):
         "num_ctas": sorted({sms, sms - 2, sms - 8, (sms // 2) * 2}),
         "attn_splits": sorted({0, max(1, sms // n_kv // 2), max(1, sms // n_kv)}),
         "max_rows_per_task": [0, 128, 64],
-        "ring_slots": [0, 6, 4],
+        "ring_slots": [0, 4, 8],   # copies in flight (0: the default, 6)
         "l2_prefetch_tiles": [0, 16],
     }
     keys = list(grid)
