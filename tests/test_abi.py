@@ -169,3 +169,15 @@ def test_staged_load_checks_its_buffer(amk):
     st, ctx = amk.amk_load_weights_staged(c, amk.amk_weights(), 256, 1 << 20, 256, 0,
                                           amk.make_schedule_config(num_ctas=4), 0, 0)
     assert st == amk.AMK_ERR_INVALID_ARG and not ctx.value
+
+
+def test_ring_slots_knob(amk):
+    """ring_slots caps the decode ring's copies in flight: 0 (the default),
+    1..12 and larger values (acting as 12) are accepted and leave the
+    workspace unchanged; a negative value is refused."""
+    c = amk.make_config(wc.LLAMA_8B_BF16, 2176)
+    dflt = amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152))
+    assert dflt > 0
+    for rs, ok in [(0, True), (1, True), (6, True), (12, True), (20, True), (-1, False)]:
+        ws = amk.amk_workspace_bytes(c, amk.make_schedule_config(num_ctas=152, ring_slots=rs))
+        assert (ws == dflt) if ok else (ws == 0), rs
